@@ -1,0 +1,219 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module holds none of the verification arithmetic.  It builds logit rows
+with the shapes and value distributions of the five workloads (i.i.d.
+N(0, 2^2) logits, drafter = target + N(0, sigma^2), random draft trees,
+Packed-SS state) and draws the drafter's own proposals with torch's generator.
+The verify side's random numbers (acceptance uniforms, Gumbel noise) are not
+made here: both implementations derive them from the counter hash.
+
+All tensors are created on ``device`` with a ``torch.Generator`` seeded by
+``seed``; bf16 rows are rounded from fp32 to nearest-even by torch.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+# The five workloads: sizes, dtypes and seeds of the verify problems.
+CONFIGS = {
+    "greedy_tiny": dict(kind="greedy", B=1, K=8, V=32000, dtype="f32", seed=0),
+    "lossless_t1": dict(kind="sample", B=64, K=16, V=128256, dtype="bf16", seed=1,
+                        sigma=0.5, T=1.0),
+    "lenient_sweep": dict(kind="sample", B=128, K=16, V=151936, dtype="bf16", seed=2,
+                          sigma=(0.25, 1.0), T=(0.7, 1.0), lam=(1.0, 2.0, 4.0, 8.0)),
+    "tree": dict(kind="tree", B=32, N=64, V=151936, dtype="bf16", seed=3, L=32,
+                 max_depth=8, max_children=4, T=(0.0, 1.0)),
+    "packed": dict(kind="packed", B=256, K=32, W=32, V=151936, dtype="bf16", seed=4,
+                   T=(0.0, 1.0)),
+}
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _normal(shape, std, g, device):
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+
+
+def _pick_tokens(rows: torch.Tensor, p_match: float, g, device) -> torch.Tensor:
+    """Per row: the row's largest entry with probability p_match, else a uniform
+    other id (the draft-quality recipe of the greedy workloads)."""
+    V = rows.shape[-1]
+    best = rows.float().argmax(dim=-1)
+    other = torch.randint(0, V - 1, best.shape, generator=g, device=device)
+    other = other + (other >= best).to(other.dtype)
+    keep = torch.rand(best.shape, generator=g, device=device) < p_match
+    return torch.where(keep, best, other).to(torch.int32)
+
+
+def _draw_from_logits(rows: torch.Tensor, T: float, g, device) -> torch.Tensor:
+    """The drafter's own proposal: one categorical draw per row from
+    softmax(rows / T), by torch.multinomial (rows are flattened to 2-D)."""
+    flat = rows.reshape(-1, rows.shape[-1]).float()
+    probs = torch.softmax(flat / T, dim=-1)
+    out = torch.multinomial(probs, 1, generator=g).reshape(rows.shape[:-1])
+    return out.to(torch.int32)
+
+
+@dataclasses.dataclass
+class GreedyInputs:
+    target: torch.Tensor      # [B, K+1, V]
+    draft_ids: torch.Tensor   # [B, K] int32
+    draft_len: torch.Tensor   # [B] int32
+
+
+def greedy_inputs(B, K, V, dtype="f32", seed=0, p_match=0.8, device="cpu",
+                  ragged=False) -> GreedyInputs:
+    g = _gen(seed, device)
+    target = _normal((B, K + 1, V), 2.0, g, device).to(_TORCH_DTYPE[dtype])
+    ids = _pick_tokens(target[:, :K], p_match, g, device) if K > 0 else \
+        torch.zeros((B, 0), dtype=torch.int32, device=device)
+    if ragged:
+        dl = torch.randint(0, K + 1, (B,), generator=g, device=device).to(torch.int32)
+    else:
+        dl = torch.full((B,), K, dtype=torch.int32, device=device)
+    return GreedyInputs(target, ids, dl)
+
+
+@dataclasses.dataclass
+class SampleInputs:
+    target: torch.Tensor      # [B, K+1, V]
+    draft: torch.Tensor       # [B, K, V]
+    draft_ids: torch.Tensor   # [B, K] int32, drawn from softmax(draft / T_q)
+    draft_len: torch.Tensor   # [B] int32
+
+
+def sample_inputs(B, K, V, dtype="bf16", seed=1, sigma=0.5, T=1.0, device="cpu",
+                  ragged=False, target_std=2.0) -> SampleInputs:
+    g = _gen(seed, device)
+    tgt32 = _normal((B, K + 1, V), target_std, g, device)
+    drf32 = tgt32[:, :K] + _normal((B, K, V), sigma, g, device)
+    target = tgt32.to(_TORCH_DTYPE[dtype])
+    draft = drf32.to(_TORCH_DTYPE[dtype])
+    del tgt32, drf32
+    if K > 0:
+        ids = _draw_from_logits(draft, T, g, device)
+    else:
+        ids = torch.zeros((B, 0), dtype=torch.int32, device=device)
+    if ragged:
+        dl = torch.randint(0, K + 1, (B,), generator=g, device=device).to(torch.int32)
+    else:
+        dl = torch.full((B,), K, dtype=torch.int32, device=device)
+    return SampleInputs(target, draft, ids, dl)
+
+
+@dataclasses.dataclass
+class TreeInputs:
+    node_logits: torch.Tensor  # [B, N, V]
+    parent: torch.Tensor       # [B, N] int32, -1 = child of the root
+    node_pos: torch.Tensor     # [B, N] int32 in [0, L)
+    node_tok: torch.Tensor     # [B, N] int32
+    depth: np.ndarray          # [B, N] host-side depths (1 = child of root)
+
+
+def random_trees(B, N, L=32, max_depth=8, max_children=4, seed=3):
+    """Parents, positions and depths of B random draft trees (host numpy).
+    Node n picks a uniform parent among the root and the earlier nodes that
+    are shallower than max_depth and have fewer than max_children children;
+    its block position is uniform among those not used on its root path."""
+    rng = np.random.default_rng(seed)
+    parent = np.full((B, N), -1, np.int32)
+    pos = np.zeros((B, N), np.int32)
+    depth = np.zeros((B, N), np.int32)
+    for b in range(B):
+        children = np.zeros(N + 1, np.int64)  # index N is the root
+        for n in range(N):
+            cand = [N] if children[N] < max_children else []
+            cand += [m for m in range(n) if depth[b, m] < max_depth
+                     and children[m] < max_children and depth[b, m] < L]
+            if not cand:
+                raise ValueError("tree capacity exhausted")
+            par = cand[rng.integers(len(cand))]
+            children[par] += 1
+            used = set()
+            m = par
+            while m != N:
+                used.add(int(pos[b, m]))
+                m = parent[b, m] if parent[b, m] >= 0 else N
+            free = [s for s in range(L) if s not in used]
+            pos[b, n] = free[rng.integers(len(free))]
+            parent[b, n] = -1 if par == N else par
+            depth[b, n] = 1 if par == N else depth[b, par] + 1
+    return parent, pos, depth
+
+
+def tree_inputs(B, N, V, dtype="bf16", seed=3, L=32, max_depth=8, max_children=4,
+                p_match=0.8, device="cpu") -> TreeInputs:
+    parent, pos, depth = random_trees(B, N, L, max_depth, max_children, seed)
+    g = _gen(seed, device)
+    logits = _normal((B, N, V), 2.0, g, device).to(_TORCH_DTYPE[dtype])
+    tok = _pick_tokens(logits, p_match, g, device)
+    t = lambda a: torch.as_tensor(a, dtype=torch.int32, device=device)
+    return TreeInputs(logits, t(parent), t(pos), tok, depth)
+
+
+@dataclasses.dataclass
+class PackedInputs:
+    logits: torch.Tensor             # [B, K+W, V]
+    prev_draft: torch.Tensor         # [B, K-1] int32
+    prev_len: torch.Tensor           # [B] int32
+    prev_q_at_draft: torch.Tensor    # [B, K-1] fp32 (T > 0)
+    prev_draft_logits: torch.Tensor  # [B, W, V] (T > 0)
+    prev_q_offset: torch.Tensor      # [B] int32
+
+
+def packed_inputs(B, K, W, V, dtype="bf16", seed=4, T=0.0, p_match=0.8, device="cpu",
+                  sigma=0.5) -> PackedInputs:
+    """A Packed-SS state after a previous call that advanced by a_prev ~ U{1..W}:
+    the previous draft has W - a_prev tokens (capped at K - 1)."""
+    g = _gen(seed, device)
+    dt = _TORCH_DTYPE[dtype]
+    lg32 = _normal((B, K + W, V), 2.0, g, device)
+    a_prev = torch.randint(1, W + 1, (B,), generator=g, device=device)
+    prev_len = torch.clamp(W - a_prev, max=K - 1).to(torch.int32)
+    logits = lg32.to(dt)
+    if T == 0.0:
+        pd = _pick_tokens(logits[:, :K - 1], p_match, g, device) if K > 1 else \
+            torch.zeros((B, 0), dtype=torch.int32, device=device)
+        pq = torch.ones((B, K - 1), dtype=torch.float32, device=device)
+        pdl = torch.empty((B, W, V), dtype=dt, device=device)[:0]
+        del lg32
+        return PackedInputs(logits, pd, prev_len, pq, pdl, a_prev.to(torch.int32))
+    # previous drafter rows: row a_prev + i is the verify row i plus noise
+    prev32 = _normal((B, W, V), 2.0, g, device)
+    idx = torch.arange(W, device=device)[None, :] - a_prev[:, None]          # [B, W]
+    src = idx.clamp(0, K - 1)
+    use = (idx >= 0) & (idx < K)
+    gathered = torch.gather(lg32[:, :K], 1, src[:, :, None].expand(B, W, V))
+    prev32 = torch.where(use[:, :, None], gathered + _normal((B, W, V), sigma, g, device),
+                         prev32)
+    del gathered, lg32
+    pdl = prev32.to(dt)
+    del prev32
+    # the retained draft d_i ~ Q_i = softmax(row a_prev + i / T), and Q_i(d_i)
+    rows = torch.gather(pdl, 1, (a_prev[:, None] + torch.arange(K - 1, device=device)[None])
+                        .clamp(max=W - 1)[:, :, None].expand(B, K - 1, V))
+    pd = _draw_from_logits(rows, T, g, device) if K > 1 else \
+        torch.zeros((B, 0), dtype=torch.int32, device=device)
+    probs = torch.softmax(rows.float() / T, dim=-1)
+    pq = torch.gather(probs, 2, pd.long()[:, :, None])[:, :, 0].contiguous()
+    del rows, probs
+    return PackedInputs(logits, pd, prev_len, pq, pdl, a_prev.to(torch.int32))
+
+
+def to_numpy_logits(t: torch.Tensor) -> np.ndarray:
+    """fp32 -> float32 array; bf16 -> uint16 array of the raw bit patterns."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float32:
+        return t.numpy()
+    raise TypeError(t.dtype)

@@ -1,0 +1,611 @@
+/*
+ * sv_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously correct fp64 CPU restatement of draft-block
+ * verification.  The tests, the smoke check and the benchmark's CPU-baseline
+ * leg use it to check the CUDA library; no product code path calls it, and it
+ * shares no source (no header, helper, table or constant generator) with the
+ * CUDA library.
+ *
+ * Sources, cited below by short name with the section / equation / algorithm:
+ *   [PackedSS] "One Call Ahead: Packed Self-Speculative Decoding with Diffusion
+ *              Drafting"
+ *   [SPOT]     "On the SPOT: Enhancing Speculative Decoding for Diffusion
+ *              Language Models via Commit-Order Prediction"
+ *   [TwoTrade] "Speculative Diffusion is a Tale of Two Tradeoffs"
+ *
+ * Precision: every logit is upcast exactly to double; all arithmetic is fp64.
+ * Where the pages leave a step open, the choice is marked READING.
+ * Parity unpinned (no page fixes the result): the residual law of the ratio
+ * lenience mode for lambda > 1, and the tie-break between equally deep tree
+ * paths.  Everything else is pinned by the tests in tests/test_oracle_*.py.
+ */
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_BF16 = 1 };
+enum { OR_LOSSLESS = 0, OR_RATIO = 1, OR_LINEAR = 2 };
+/* Random-number streams (READING: the pages only ask for independent uniforms
+ * and Gumbels; [PackedSS] App. B.2 "Conditioning information" requires draft
+ * sampling, acceptance tests and corrections to use independent numbers). */
+enum { ST_ACCEPT = 1, ST_SAMPLE = 2, ST_DRAFT = 3, ST_TREE = 4 };
+/* A decision within this distance of its threshold is flagged, not compared. */
+#define OR_FLAG_EPS 1e-9
+
+/* ------------------------------------------------------------------------ */
+/* Counter-based random numbers.                                             */
+/* ------------------------------------------------------------------------ */
+
+/* SplitMix64 output function (Steele, Lea & Flood 2014; Vigna's reference
+ * splitmix64.c): advance by the golden gamma, then two xor-shift-multiply
+ * rounds and a final xor-shift. */
+uint64_t or_mix64(uint64_t x)
+{
+    uint64_t z = x + 0x9E3779B97F4A7C15ULL;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+/* MurmurHash3 32-bit finalizer (Appleby, public domain). */
+uint32_t or_fmix32(uint32_t h)
+{
+    h ^= h >> 16;
+    h *= 0x85EBCA6BU;
+    h ^= h >> 13;
+    h *= 0xC2B2AE35U;
+    h ^= h >> 16;
+    return h;
+}
+
+/* Row key: a chain of the 64-bit mixer over the counter fields. */
+uint64_t or_key(uint64_t seed, uint32_t stream, uint64_t seq, int64_t pos, uint64_t iter)
+{
+    uint64_t k = or_mix64(seed);
+    k = or_mix64(k ^ (uint64_t)stream);
+    k = or_mix64(k ^ seq);
+    k = or_mix64(k ^ (uint64_t)pos);
+    k = or_mix64(k ^ iter);
+    return k;
+}
+
+/* 52 random bits for vocabulary id v under row key k.  The top 16 bits are
+ * one half of a 32-bit word shared by the pair (2j, 2j+1); the low 36 bits
+ * come from a 64-bit mix of (k, v). */
+uint64_t or_bits52(uint64_t key, uint32_t v)
+{
+    uint32_t word = or_fmix32((uint32_t)key ^ ((v >> 1) * 0x9E3779B9U));
+    uint64_t prefix = (v & 1u) ? (uint64_t)(word >> 16) : (uint64_t)(word & 0xFFFFu);
+    uint64_t suffix = or_mix64(key ^ ((uint64_t)v * 0xD1B54A32D192ED03ULL)) >> 28;
+    return (prefix << 36) | suffix;
+}
+
+/* Uniform in the open interval (0,1): u = (2m + 1) / 2^53, exact in fp64. */
+double or_uniform(uint64_t key, uint32_t v)
+{
+    return (double)(2 * or_bits52(key, v) + 1) * 0x1p-53;
+}
+
+/* Standard Gumbel by inversion: G = -log(-log u). */
+double or_gumbel(uint64_t key, uint32_t v)
+{
+    return -log(-log(or_uniform(key, v)));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rows.                                                                     */
+/* ------------------------------------------------------------------------ */
+
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Copy row r (row_stride elements apart) of a logit tensor into fp64. */
+static void load_row(const void *base, int dtype, int64_t r, int64_t row_stride, int V, double *out)
+{
+    if (dtype == OR_BF16) {
+        const uint16_t *p = (const uint16_t *)base + r * row_stride;
+        for (int v = 0; v < V; ++v)
+            out[v] = bf16_to_double(p[v]);
+    } else {
+        const float *p = (const float *)base + r * row_stride;
+        for (int v = 0; v < V; ++v)
+            out[v] = (double)p[v];
+    }
+}
+
+/* log-sum-exp of x/T in index order: m + log(sum exp(z - m)), z = x/T.
+ * The temperature law pi_T ∝ p^(1/T) = softmax(x/T) is [SPOT] eq. (2). */
+double or_lse(const double *x, int V, double T)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double z = x[v] / T;
+        if (z > m)
+            m = z;
+    }
+    double s = 0.0;
+    for (int v = 0; v < V; ++v)
+        s += exp(x[v] / T - m);
+    return m + log(s);
+}
+
+/* argmax with the lowest index winning ties.  The pages ask only for a fixed
+ * deterministic rule ([SPOT] App. A.1 "Position selection"; [PackedSS]
+ * App. B.2 "Greedy decoding"); lowest index is the READING. */
+int or_argmax(const double *x, int V)
+{
+    int best = 0;
+    for (int v = 1; v < V; ++v)
+        if (x[v] > x[best])
+            best = v;
+    return best;
+}
+
+/* Gumbel-max sample: argmax over v of score[v] + G(key, v), skipping entries
+ * whose score is -inf (zero weight).  Pr[argmax = u] = softmax(score)_u is the
+ * Gumbel-argmax identity, [SPOT] App. A.3 eqs. (5)-(7).  *gap receives the
+ * difference between the best and second-best perturbed scores (+inf when
+ * only one entry is eligible).  Lowest index wins exact ties (READING). */
+int or_gumbel_argmax(const double *score, int V, uint64_t key, double *gap)
+{
+    int best = -1;
+    double b1 = -INFINITY, b2 = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        if (score[v] == -INFINITY)
+            continue;
+        double s = score[v] + or_gumbel(key, (uint32_t)v);
+        if (best < 0 || s > b1) {
+            b2 = b1;
+            b1 = s;
+            best = v;
+        } else if (s > b2) {
+            b2 = s;
+        }
+    }
+    if (gap)
+        *gap = (b2 == -INFINITY) ? INFINITY : b1 - b2;
+    return best;
+}
+
+/* Acceptance probability of a draft token from log p(d) and log q(d).
+ *   LOSSLESS: min{1, p/q}                      [PackedSS] §2.2; [TwoTrade] §2
+ *   RATIO:    min{1, lam p/q}, lam >= 1         READING of the "predefined
+ *             ratio" lenience named in [TwoTrade] §1
+ *   LINEAR:   min{1, ptilde/q}, ptilde = (1-mu)p + mu q, mu = lam in [0,1]
+ *                                              [TwoTrade] eq. (5), Alg. 1 */
+double or_accept_prob(double log_p, double log_q, int mode, double lam)
+{
+    double r = exp(log_p - log_q);
+    double a;
+    if (mode == OR_RATIO)
+        a = lam * r;
+    else if (mode == OR_LINEAR)
+        a = (1.0 - lam) * r + lam;
+    else
+        a = r;
+    return a < 1.0 ? a : 1.0;
+}
+
+/* Residual weights (unnormalised) used after the first rejection.
+ *   LOSSLESS: [p - q]_+                         [PackedSS] §2.2, Alg. 2
+ *   LINEAR:   [ptilde - q]_+                    [TwoTrade] Alg. 1
+ *   RATIO:    [p - q]_+  (READING: the lenience changes only the test;
+ *             parity unpinned for lam > 1)
+ * p and q are the normalised rows exp(x/Tp - Lp) and exp(y/Tq - Lq). */
+void or_residual_weights(const double *x, const double *y, int V, double Tp, double Tq,
+                         double Lp, double Lq, int mode, double lam, double *w)
+{
+    for (int v = 0; v < V; ++v) {
+        double p = exp(x[v] / Tp - Lp);
+        double q = exp(y[v] / Tq - Lq);
+        double pt = (mode == OR_LINEAR) ? (1.0 - lam) * p + lam * q : p;
+        double d = pt - q;
+        w[v] = d > 0.0 ? d : 0.0;
+    }
+}
+
+/* Total variation 1 - sum_v min{p_v, q_v}  ([TwoTrade] eq. (1); [SPOT]
+ * App. B.2 Step 4). */
+double or_tv(const double *x, const double *y, int V, double Tp, double Tq, double Lp, double Lq)
+{
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double p = exp(x[v] / Tp - Lp);
+        double q = exp(y[v] / Tq - Lq);
+        s += p < q ? p : q;
+    }
+    return 1.0 - s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Greedy verification, [PackedSS] §3.1 eqs. (1)-(2), Alg. 1 lines 3, 5-6.   */
+/* target: [B, K+1, V] rows; draft_ids: [B, K]; draft_len: [B] or NULL (=K). */
+/* ------------------------------------------------------------------------ */
+int or_verify_greedy(const void *target, int dtype, int64_t row_stride, int B, int K, int V,
+                     const int32_t *draft_ids, const int32_t *draft_len,
+                     int32_t *accept_len, int32_t *next_token)
+{
+    int err = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        int n = draft_len ? draft_len[b] : K;
+        if (n < 0 || n > K) {
+            err |= 1;
+            continue;
+        }
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        int h = 0, v_next = -1;
+        for (int i = 0; i <= n; ++i) {
+            load_row(target, dtype, (int64_t)b * (K + 1) + i, row_stride, V, x);
+            int v_i = or_argmax(x, V);
+            if (i < n && draft_ids[(int64_t)b * K + i] == v_i) {
+                ++h;
+                continue;
+            }
+            v_next = v_i; /* correction at the first mismatch, or bonus */
+            break;
+        }
+        accept_len[b] = h;
+        next_token[b] = v_next;
+        free(x);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Speculative sampling with lossless or lenient acceptance.                 */
+/* [PackedSS] §2.2 and Alg. 2 lines 5-8; [TwoTrade] §2 and Alg. 1 lines 7-12; */
+/* [SPOT] App. B.1 eqs. (13)-(14).                                           */
+/*   target [B, K+1, V], draft [B, K, V]; row i of a sequence predicts the   */
+/*   token at absolute position pos_base[b] + i.                             */
+/*   u_i   = U(seed, ACCEPT, b, pos_base + i, 0, v=0)                        */
+/*   next  = Gumbel-max of the residual (SAMPLE stream at the position of    */
+/*           the first rejection) or of the bonus row (SAMPLE at pos + n).   */
+/* Optional outputs (NULL to skip): p_at/q_at [B,K], lse_p [B,K+1],          */
+/* lse_q [B,K], tv [B,K], flags [B].  Rows beyond draft_len get NaN.         */
+/* ------------------------------------------------------------------------ */
+int or_verify_sample(const void *target, const void *draft, int dtype, int64_t row_stride,
+                     int B, int K, int V, const int32_t *draft_ids, const int32_t *draft_len,
+                     double Tp, double Tq, int mode, double lam, uint64_t seed,
+                     const int64_t *pos_base, int32_t *accept_len, int32_t *next_token,
+                     double *p_at, double *q_at, double *lse_p, double *lse_q, double *tv,
+                     int32_t *flags)
+{
+    int err = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        int n = draft_len ? draft_len[b] : K;
+        if (n < 0 || n > K) {
+            err |= 1;
+            continue;
+        }
+        int64_t pos0 = pos_base ? pos_base[b] : 0;
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        double *y = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        int h = 0, rejected = 0, nflag = 0;
+        /* per-row quantities for every verify row 0..n (outputs) */
+        for (int i = 0; i <= n; ++i) {
+            load_row(target, dtype, (int64_t)b * (K + 1) + i, row_stride, V, x);
+            double Lp = or_lse(x, V, Tp);
+            if (lse_p)
+                lse_p[(int64_t)b * (K + 1) + i] = Lp;
+            if (i == n)
+                break;
+            load_row(draft, dtype, (int64_t)b * K + i, row_stride, V, y);
+            double Lq = or_lse(y, V, Tq);
+            int d = draft_ids[(int64_t)b * K + i];
+            if (d < 0 || d >= V) {
+                err |= 2;
+                break;
+            }
+            double log_p = x[d] / Tp - Lp, log_q = y[d] / Tq - Lq;
+            if (lse_q)
+                lse_q[(int64_t)b * K + i] = Lq;
+            if (p_at)
+                p_at[(int64_t)b * K + i] = exp(log_p);
+            if (q_at)
+                q_at[(int64_t)b * K + i] = exp(log_q);
+            if (tv)
+                tv[(int64_t)b * K + i] = or_tv(x, y, V, Tp, Tq, Lp, Lq);
+            if (!rejected) {
+                /* left-to-right test; only positions up to the first
+                 * rejection are reached ([PackedSS] Alg. 2 line 6) */
+                double alpha = or_accept_prob(log_p, log_q, mode, lam);
+                double u = or_uniform(or_key(seed, ST_ACCEPT, (uint64_t)b, pos0 + i, 0), 0);
+                if (fabs(u - alpha) < OR_FLAG_EPS)
+                    ++nflag;
+                if (u < alpha)
+                    ++h;
+                else
+                    rejected = 1;
+            }
+        }
+        /* rows beyond the sequence's draft are not part of it */
+        for (int i = n; i < K; ++i) {
+            if (p_at) p_at[(int64_t)b * K + i] = NAN;
+            if (q_at) q_at[(int64_t)b * K + i] = NAN;
+            if (lse_q) lse_q[(int64_t)b * K + i] = NAN;
+            if (tv) tv[(int64_t)b * K + i] = NAN;
+            if (lse_p && i + 1 <= K) lse_p[(int64_t)b * (K + 1) + i + 1] = NAN;
+        }
+        /* correction or bonus ([PackedSS] Alg. 2 line 7) */
+        double gap = INFINITY;
+        int c;
+        load_row(target, dtype, (int64_t)b * (K + 1) + h, row_stride, V, x);
+        double Lp = or_lse(x, V, Tp);
+        uint64_t key = or_key(seed, ST_SAMPLE, (uint64_t)b, pos0 + h, 0);
+        if (h < n) {
+            load_row(draft, dtype, (int64_t)b * K + h, row_stride, V, y);
+            double Lq = or_lse(y, V, Tq);
+            or_residual_weights(x, y, V, Tp, Tq, Lp, Lq, mode, lam, w);
+            for (int v = 0; v < V; ++v)
+                w[v] = w[v] > 0.0 ? log(w[v]) : -INFINITY;
+            c = or_gumbel_argmax(w, V, key, &gap);
+        } else {
+            for (int v = 0; v < V; ++v)
+                w[v] = x[v] / Tp;
+            c = or_gumbel_argmax(w, V, key, &gap);
+        }
+        if (gap < OR_FLAG_EPS)
+            ++nflag;
+        accept_len[b] = h;
+        next_token[b] = c;
+        if (flags)
+            flags[b] = nflag;
+        free(x);
+        free(y);
+        free(w);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tree verification by state equality, [SPOT] §4.3 and App. A.1 "Draft      */
+/* trees", "State-equality verifier"; coupled noise [SPOT] eq. (4).          */
+/*   node_logits [B, N, V]: row n is the target conditional, at the state of */
+/*   node n's parent, for block position node_pos[n]; the node commits       */
+/*   token node_tok[n] there.  parent[b,n] in [-1, n-1] (-1: child of root). */
+/*   A node matches when the target's own commitment equals its token:       */
+/*     T == 0: argmax_v x_v;                                                 */
+/*     T > 0:  argmax_v x_v/T + G(seed, TREE, b, pos_base + node_pos, 0, v)  */
+/*   (the Gumbel row is shared by every node at the same absolute position). */
+/*   The accepted set is the deepest node whose whole root path matches      */
+/*   (READING for ties in depth: smallest node index; parity unpinned).      */
+/*   commit_count = path_len + 1: the verifier always commits the target's   */
+/*   own transition after the last accepted state.                           */
+/* ------------------------------------------------------------------------ */
+int or_verify_tree(const void *node_logits, int dtype, int64_t row_stride, int B, int N, int V,
+                   const int32_t *parent, const int32_t *node_pos, const int32_t *node_tok,
+                   double T, uint64_t seed, const int64_t *pos_base, int32_t *path_len,
+                   int32_t *path_nodes, int max_depth, int32_t *commit_count, uint8_t *match,
+                   int32_t *flags)
+{
+    int err = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        int64_t pos0 = pos_base ? pos_base[b] : 0;
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        int *ok = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+        int *depth = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+        int nflag = 0, best = -1;
+        for (int n = 0; n < N; ++n) {
+            int par = parent[(int64_t)b * N + n];
+            int pos = node_pos[(int64_t)b * N + n];
+            if (par < -1 || par >= n || pos < 0) {
+                err |= 1;
+                ok[n] = 0;
+                depth[n] = 0;
+                continue;
+            }
+            load_row(node_logits, dtype, (int64_t)b * N + n, row_stride, V, x);
+            int win;
+            if (T == 0.0) {
+                win = or_argmax(x, V);
+            } else {
+                double gap;
+                for (int v = 0; v < V; ++v)
+                    x[v] = x[v] / T;
+                win = or_gumbel_argmax(x, V, or_key(seed, ST_TREE, (uint64_t)b, pos0 + pos, 0), &gap);
+                if (gap < OR_FLAG_EPS)
+                    ++nflag;
+            }
+            int m = (win == node_tok[(int64_t)b * N + n]);
+            if (match)
+                match[(int64_t)b * N + n] = (uint8_t)m;
+            ok[n] = m && (par < 0 || ok[par]);
+            depth[n] = (par < 0) ? 1 : depth[par] + 1;
+            if (ok[n] && (best < 0 || depth[n] > depth[best]))
+                best = n;
+        }
+        int len = best < 0 ? 0 : depth[best];
+        path_len[b] = len;
+        commit_count[b] = len + 1;
+        for (int k = 0; k < max_depth; ++k)
+            path_nodes[(int64_t)b * max_depth + k] = -1;
+        for (int n = best, d = len; n >= 0; n = parent[(int64_t)b * N + n], --d)
+            if (d - 1 < max_depth)
+                path_nodes[(int64_t)b * max_depth + d - 1] = n;
+        if (flags)
+            flags[b] = nflag;
+        free(x);
+        free(ok);
+        free(depth);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One Packed-SS iteration, [PackedSS] §3.1 Alg. 1 (T == 0) and §3.2 Alg. 2  */
+/* (T > 0).                                                                  */
+/*   logits [B, K+W, V]: rows 0..K-1 verify rows (row i predicts absolute    */
+/*   position pos_base + i), rows K..K+W-1 drafter rows for positions        */
+/*   pos_base + j (draft, verifier and proposal share columns, Fig. 2).      */
+/*   prev_draft [B, K-1], prev_len [B] <= K-1: the draft D_{t-1}.            */
+/*   T > 0: prev_q_at_draft [B, K-1] holds Q_{t-1}(d) for each draft token;  */
+/*   prev_draft_logits [B, W, V] are the previous call's drafter rows and    */
+/*   prev_q_offset [B] = a_{t-1}, so Q_{t-1}^(i) is row a_{t-1} + i - 1      */
+/*   (Alg. 2 line 12: Q_t^(j) = q_t^(a+j)).                                  */
+/*   Stopping index a = min({A, remaining} ∪ {i : C_i = EOS}) (Alg. 1 l. 7). */
+/*   Next draft (z_{a+1}, ..., z_W) (eq. (4)); drafts at T > 0 are Gumbel-max */
+/*   samples keyed by the call index iter (DRAFT stream).                    */
+/*   confidence_j = max_v softmax(y_j)_v at temperature 1 (READING).          */
+/* ------------------------------------------------------------------------ */
+int or_packed_step(const void *logits, int dtype, int64_t row_stride, int B, int K, int W, int V,
+                   const int32_t *prev_draft, const int32_t *prev_len, const float *prev_q_at_draft,
+                   const void *prev_draft_logits, const int32_t *prev_q_offset, double T,
+                   uint64_t seed, uint64_t iter, const int64_t *pos_base, int32_t eos_id,
+                   const int32_t *remaining, int32_t *accept_len, int32_t *commit_len,
+                   int32_t *committed, int32_t *next_draft, int32_t *next_len,
+                   double *next_q_at_draft, double *confidence, int32_t *flags)
+{
+    int err = 0;
+    int R = K + W;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        int64_t pos0 = pos_base ? pos_base[b] : 0;
+        int n = prev_len[b];
+        int off = prev_q_offset ? prev_q_offset[b] : 0;
+        if (n < 0 || n > K - 1 || (T > 0.0 && (off < 0 || off + n > W))) {
+            err |= 1;
+            continue;
+        }
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        double *y = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t *C = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
+        int32_t *z = (int32_t *)malloc(sizeof(int32_t) * (size_t)W);
+        double *qz = (double *)malloc(sizeof(double) * (size_t)W);
+        int h = 0, c = -1, nflag = 0;
+        double gap = INFINITY;
+
+        /* ---- verification of D_{t-1} ---- */
+        if (T == 0.0) {
+            for (int i = 0; i <= n; ++i) {
+                load_row(logits, dtype, (int64_t)b * R + i, row_stride, V, x);
+                int v_i = or_argmax(x, V);
+                if (i < n && prev_draft[(int64_t)b * (K - 1) + i] == v_i) {
+                    ++h;
+                    continue;
+                }
+                c = v_i;
+                break;
+            }
+        } else {
+            int rejected = 0;
+            for (int i = 0; i < n && !rejected; ++i) {
+                int d = prev_draft[(int64_t)b * (K - 1) + i];
+                if (d < 0 || d >= V) {
+                    err |= 2;
+                    break;
+                }
+                load_row(logits, dtype, (int64_t)b * R + i, row_stride, V, x);
+                double Lp = or_lse(x, V, T);
+                double log_p = x[d] / T - Lp;
+                double log_q = log((double)prev_q_at_draft[(int64_t)b * (K - 1) + i]);
+                double alpha = or_accept_prob(log_p, log_q, OR_LOSSLESS, 0.0);
+                double u = or_uniform(or_key(seed, ST_ACCEPT, (uint64_t)b, pos0 + i, 0), 0);
+                if (fabs(u - alpha) < OR_FLAG_EPS)
+                    ++nflag;
+                if (u < alpha)
+                    ++h;
+                else
+                    rejected = 1;
+            }
+            uint64_t key = or_key(seed, ST_SAMPLE, (uint64_t)b, pos0 + h, 0);
+            load_row(logits, dtype, (int64_t)b * R + h, row_stride, V, x);
+            double Lp = or_lse(x, V, T);
+            if (h < n) {
+                /* correction from [p - Q]_+ with the stored proposal row */
+                load_row(prev_draft_logits, dtype, (int64_t)b * W + off + h, row_stride, V, y);
+                double Lq = or_lse(y, V, T);
+                or_residual_weights(x, y, V, T, T, Lp, Lq, OR_LOSSLESS, 0.0, w);
+                for (int v = 0; v < V; ++v)
+                    w[v] = w[v] > 0.0 ? log(w[v]) : -INFINITY;
+            } else {
+                for (int v = 0; v < V; ++v)
+                    w[v] = x[v] / T;
+            }
+            c = or_gumbel_argmax(w, V, key, &gap);
+            if (gap < OR_FLAG_EPS)
+                ++nflag;
+        }
+        for (int i = 0; i < h; ++i)
+            C[i] = prev_draft[(int64_t)b * (K - 1) + i];
+        C[h] = c;
+        int A = h + 1;
+        int a = A;
+        if (remaining && remaining[b] < a)
+            a = remaining[b] < 0 ? 0 : remaining[b];
+        if (eos_id >= 0)
+            for (int i = 0; i < A; ++i)
+                if (C[i] == eos_id) {
+                    if (i + 1 < a)
+                        a = i + 1;
+                    break;
+                }
+
+        /* ---- drafting Z_t from the same call ---- */
+        for (int j = 0; j < W; ++j) {
+            load_row(logits, dtype, (int64_t)b * R + K + j, row_stride, V, y);
+            double L1 = or_lse(y, V, 1.0);
+            int zm = or_argmax(y, V);
+            if (confidence)
+                confidence[(int64_t)b * W + j] = exp(y[zm] - L1);
+            if (T == 0.0) {
+                z[j] = zm;
+                qz[j] = 1.0;
+            } else {
+                double LT = or_lse(y, V, T);
+                for (int v = 0; v < V; ++v)
+                    w[v] = y[v] / T;
+                double g;
+                z[j] = or_gumbel_argmax(w, V, or_key(seed, ST_DRAFT, (uint64_t)b, pos0 + j, iter), &g);
+                qz[j] = exp(y[z[j]] / T - LT);
+                if (j >= a && g < OR_FLAG_EPS)
+                    ++nflag;
+            }
+        }
+
+        accept_len[b] = h;
+        commit_len[b] = a;
+        for (int i = 0; i < K; ++i)
+            committed[(int64_t)b * K + i] = i < a ? C[i] : -1;
+        int nl = W - a > 0 ? W - a : 0;
+        next_len[b] = nl;
+        for (int j = 0; j < W; ++j) {
+            next_draft[(int64_t)b * W + j] = j < nl ? z[a + j] : -1;
+            if (next_q_at_draft)
+                next_q_at_draft[(int64_t)b * W + j] = j < nl ? qz[a + j] : NAN;
+        }
+        if (flags)
+            flags[b] = nflag;
+        free(x);
+        free(y);
+        free(w);
+        free(C);
+        free(z);
+        free(qz);
+    }
+    return err ? -1 : 0;
+}
+
+/* Number of threads the parallel loops above use (for reporting). */
+int or_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
