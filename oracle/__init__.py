@@ -89,6 +89,12 @@ def _p(a):
     return None if a is None else a.ctypes.data_as(C.c_void_p)
 
 
+def f32(x: float) -> float:
+    """The value a C ``float`` parameter carries (temperatures and lambda are
+    passed to the library as fp32; the oracle uses the same numbers)."""
+    return float(np.float32(x))
+
+
 def _dtype_code(logits: np.ndarray) -> int:
     if logits.dtype == np.float32:
         return 0
@@ -217,8 +223,8 @@ def verify_sample(target, draft, draft_ids, draft_len=None, T_p=1.0, T_q=1.0, mo
         "tv": np.empty((B, K)) if want_tv else None, "flags": np.empty(B, np.int32),
     }
     rc = _L().or_verify_sample(
-        _p(target), _p(draft), _dtype_code(target), V, B, K, V, _p(ids), _p(dl), float(T_p),
-        float(T_q), int(mode), float(lam), int(seed) & (2**64 - 1), _p(pb),
+        _p(target), _p(draft), _dtype_code(target), V, B, K, V, _p(ids), _p(dl), f32(T_p),
+        f32(T_q), int(mode), f32(lam), int(seed) & (2**64 - 1), _p(pb),
         _p(out["accept_len"]), _p(out["next_token"]), _p(out["p_at_draft"]),
         _p(out["q_at_draft"]), _p(out["lse_p"]), _p(out["lse_q"]), _p(out["tv"]),
         _p(out["flags"]))
@@ -245,7 +251,7 @@ def verify_tree(node_logits, parent, node_pos, node_tok, T=0.0, seed=0, pos_base
     }
     rc = _L().or_verify_tree(
         _p(node_logits), _dtype_code(node_logits), V, B, N, V, _p(par), _p(pos), _p(tok),
-        float(T), int(seed) & (2**64 - 1), _p(pb), _p(out["path_len"]), _p(out["path_nodes"]),
+        f32(T), int(seed) & (2**64 - 1), _p(pb), _p(out["path_len"]), _p(out["path_nodes"]),
         int(max_depth), _p(out["commit_count"]), _p(out["match"]), _p(out["flags"]))
     if rc:
         raise ValueError("oracle: invalid tree inputs")
@@ -278,7 +284,7 @@ def packed_step(logits, K, W, prev_draft, prev_len, prev_q_at_draft=None,
     }
     rc = _L().or_packed_step(
         _p(logits), _dtype_code(logits), V, B, K, W, V, _p(pd), _p(pl), _p(pq), _p(pdl),
-        _p(off), float(T), int(seed) & (2**64 - 1), int(it) & (2**64 - 1), _p(pb), int(eos_id),
+        _p(off), f32(T), int(seed) & (2**64 - 1), int(it) & (2**64 - 1), _p(pb), int(eos_id),
         _p(rem), _p(out["accept_len"]), _p(out["commit_len"]), _p(out["committed"]),
         _p(out["next_draft"]), _p(out["next_len"]), _p(out["next_q_at_draft"]),
         _p(out["confidence"]), _p(out["flags"]))

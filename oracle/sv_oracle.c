@@ -74,15 +74,20 @@ uint64_t or_key(uint64_t seed, uint32_t stream, uint64_t seq, int64_t pos, uint6
     return k;
 }
 
-/* 52 random bits for vocabulary id v under row key k.  The top 16 bits are
- * one half of a 32-bit word shared by the pair (2j, 2j+1); the low 36 bits
- * come from a 64-bit mix of (k, v). */
+/* 52 random bits for vocabulary id v under row key k, most significant first:
+ *   8 bits: byte (v mod 4) of fmix32(low32(k) xor (v div 4) * 0x9E3779B9),
+ *   8 bits: byte (v mod 4) of fmix32(high32(k) xor (v div 4) * 0x85EBCA77),
+ *  36 bits: the top 36 bits of mix64(k xor v * 0xD1B54A32D192ED03).
+ * (Bytes are numbered from the least significant.)  Four consecutive ids
+ * share the two 32-bit words. */
 uint64_t or_bits52(uint64_t key, uint32_t v)
 {
-    uint32_t word = or_fmix32((uint32_t)key ^ ((v >> 1) * 0x9E3779B9U));
-    uint64_t prefix = (v & 1u) ? (uint64_t)(word >> 16) : (uint64_t)(word & 0xFFFFu);
+    uint32_t j = v >> 2, sh = 8u * (v & 3u);
+    uint32_t wa = or_fmix32((uint32_t)key ^ (j * 0x9E3779B9U));
+    uint32_t wb = or_fmix32((uint32_t)(key >> 32) ^ (j * 0x85EBCA77U));
+    uint64_t b0 = (wa >> sh) & 0xFFu, b1 = (wb >> sh) & 0xFFu;
     uint64_t suffix = or_mix64(key ^ ((uint64_t)v * 0xD1B54A32D192ED03ULL)) >> 28;
-    return (prefix << 36) | suffix;
+    return (b0 << 44) | (b1 << 36) | suffix;
 }
 
 /* Uniform in the open interval (0,1): u = (2m + 1) / 2^53, exact in fp64. */

@@ -307,7 +307,8 @@ def test_sample_lenient_reductions(orc):
 
 def test_sample_per_row_outputs(orc):
     rng = np.random.default_rng(12)
-    B, K, V, Tp, Tq = 3, 4, 30, 0.7, 1.3
+    B, K, V = 3, 4, 30
+    Tp, Tq = float(np.float32(0.7)), float(np.float32(1.3))  # temperatures are fp32 in the ABI
     x = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
     y = rng.normal(0, 2, (B, K, V)).astype(np.float32)
     ids = rng.integers(0, V, (B, K))

@@ -47,9 +47,12 @@ def test_uniform_chi_square(orc):
     counts, _ = np.histogram(u, bins=40, range=(0, 1))
     p = stats.chisquare(counts).pvalue
     assert p > 1e-4
-    # the prefix halves of one 32-bit word (v = 2j, 2j+1) are independent
-    pairs = np.histogram2d(u[0::2], u[1::2], bins=8, range=[[0, 1], [0, 1]])[0].ravel()
-    assert stats.chisquare(pairs).pvalue > 1e-4
+    # the four ids that share a hash word (v = 4j .. 4j+3) are independent
+    for a, b in ((0, 1), (0, 3), (1, 2)):
+        pairs = np.histogram2d(u[a::4], u[b::4], bins=8, range=[[0, 1], [0, 1]])[0].ravel()
+        assert stats.chisquare(pairs).pvalue > 1e-4
+    top = (np.floor(u * 256)).astype(int)
+    assert stats.chisquare(np.bincount(top, minlength=256)).pvalue > 1e-4
     assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.03
 
 
