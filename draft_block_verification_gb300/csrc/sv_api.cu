@@ -1,0 +1,526 @@
+// sv_api.cu -- host side of libsv: handle, argument checks, workspace and
+// launch orchestration for the four verify calls declared in sv.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "sv_gumbel.cuh"
+#include "sv_job.cuh"
+
+namespace sv {
+size_t pass_smem_bytes();
+size_t rescue_scratch_doubles(int B);
+cudaError_t pass_setup(int *blocks_per_sm);
+cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s);
+cudaError_t post_setup(int *blocks_per_sm);
+cudaError_t post_launch(const Job &j, int grid, int coop_grid, bool tv, cudaStream_t s);
+cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s);
+constexpr int kResidChunksHost = 8;
+}  // namespace sv
+
+using namespace sv;
+
+struct sv_handle {
+    int device = 0;
+    int sms = 0;
+    int pass_blocks = 1;   // resident streaming CTAs per SM
+    int post_blocks = 1;   // resident post-pass CTAs per SM
+    int *d_err = nullptr;
+    unsigned *d_ctl = nullptr;
+    float *d_gtab = nullptr;
+    char *ws = nullptr;
+    size_t ws_bytes = 0;
+    unsigned *cnt = nullptr;  // completion counters: always zero between calls
+    int cnt_B = 0;            // sequences the counter arena holds
+    int force_rescue = 0;
+    cudaEvent_t ev[2] = {nullptr, nullptr};  // caller-owned (SV_OPT_TIMING_EVENTS)
+    bool timing = false;
+    std::mutex mu;
+};
+
+namespace {
+
+// Upper bounds of G = -log(-log u), rounded up to fp32 with one more ulp of
+// slack: entry b < 256 bounds ids whose top 8 bits of u are b (u < (b+1)/256);
+// entry 256 + c bounds ids in the top bucket whose next 8 bits are c
+// (u < (65280 + c + 1)/65536).  The last entry of each level is +inf.
+static float up_f32(double g)
+{
+    float f = (float)g;
+    if ((double)f < g) f = nextafterf(f, INFINITY);
+    return nextafterf(f, INFINITY);
+}
+
+void gumbel_bound_table(float *t)
+{
+    for (int b = 0; b < kG8; ++b)
+        t[b] = (b == kG8 - 1) ? INFINITY : up_f32(-log(-log((double)(b + 1) / kG8)));
+    for (int c = 0; c < kG8; ++c)
+        t[kG8 + c] = (c == kG8 - 1) ? INFINITY
+                                    : up_f32(-log(-log((double)(65280 + c + 1) / 65536.0)));
+}
+
+sv_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return SV_OK;
+    if (e == cudaErrorMemoryAllocation) return SV_ERR_OOM;
+    return SV_ERR_CUDA;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t rp, rs, resid, rescue, dtmp, tvpart, rpart, total;
+};
+
+Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks)
+{
+    Layout L;
+    size_t o = 0;
+    L.rp = o;     o = align_up(o + (size_t)B * rows_per_seq * parts * sizeof(RowPart));
+    L.rs = o;     o = align_up(o + (size_t)B * rows_per_seq * sizeof(RowStat));
+    L.resid = o;  o = align_up(o + (size_t)B * sizeof(ResidEntry));
+    L.rescue = o; o = align_up(o + (size_t)B * sizeof(RescueEntry));
+    L.dtmp = o;   o = align_up(o + (size_t)B * std::max(W, 1) * sizeof(DraftTmp));
+    L.tvpart = o; o = align_up(o + (size_t)B * std::max(K, 1) * tv_chunks * sizeof(float));
+    L.rpart = o;  o = align_up(o + rescue_scratch_doubles(B) * sizeof(double));
+    L.total = o;
+    return L;
+}
+
+// Grow the workspace (stream-ordered); new memory is zeroed so that every
+// counter starts at zero.  Kernels return their counters to zero.
+sv_status ensure_ws(sv_handle *h, size_t bytes, cudaStream_t s)
+{
+    if (bytes <= h->ws_bytes) return SV_OK;
+    size_t nb = std::max(bytes, h->ws_bytes * 2);
+    if (h->ws) {
+        cudaError_t e = cudaFreeAsync(h->ws, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        h->ws = nullptr;
+        h->ws_bytes = 0;
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaMallocAsync(&p, nb, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaMemsetAsync(p, 0, nb, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    h->ws = (char *)p;
+    h->ws_bytes = nb;
+    return SV_OK;
+}
+
+// Counter arena: seq_done [Bcap], tvdone [kMaxK * Bcap], rdone [4 * Bcap].
+// The kernels return every counter they touch to zero, so the arena is zeroed
+// only when it is (re)allocated.
+constexpr int kCntPerSeq = 1 + kMaxK + 4;
+
+sv_status ensure_cnt(sv_handle *h, int B, cudaStream_t s)
+{
+    if (B <= h->cnt_B) return SV_OK;
+    int nb = std::max(B, 2 * h->cnt_B);
+    if (h->cnt) {
+        cudaError_t e = cudaFreeAsync(h->cnt, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        h->cnt = nullptr;
+        h->cnt_B = 0;
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaMallocAsync(&p, (size_t)nb * kCntPerSeq * sizeof(unsigned), s);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = cudaMemsetAsync(p, 0, (size_t)nb * kCntPerSeq * sizeof(unsigned), s);
+    if (e != cudaSuccess) return cuda_status(e);
+    h->cnt = (unsigned *)p;
+    h->cnt_B = nb;
+    return SV_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Shape checks shared by every logit tensor argument.
+bool logits_ok(const void *p, sv_dtype dt, int64_t rs, int V)
+{
+    if (!p || !aligned16(p)) return false;
+    if (dt != SV_F32 && dt != SV_BF16) return false;
+    int esz = dt == SV_BF16 ? 2 : 4;
+    if (V < 1 || (int64_t)V * esz % 16 != 0) return false;
+    if (rs < V || (rs * esz) % 16 != 0) return false;
+    if ((int64_t)V > (int64_t)1 << 30) return false;
+    return true;
+}
+
+void fill_common(Job &j, sv_handle *h, const void *src0, sv_dtype dt, int64_t rs, int V)
+{
+    memset(&j, 0, sizeof j);
+    j.dtype = dt;
+    j.src0 = (const char *)src0;
+    int esz = dt == SV_BF16 ? 2 : 4;
+    j.rs = rs * esz;
+    j.V = V;
+    j.nvec = (int)((int64_t)V * esz / 16);
+    j.err = h->d_err;
+    j.ctl = h->d_ctl;
+    j.gtab = h->d_gtab;
+    j.force_rescue = h->force_rescue;
+    j.c1 = 1.4426950408889634f;
+    j.eos = -1;
+}
+
+// Choose the row split and bind the workspace; returns the pass grid size.
+sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_chunks, int *grid)
+{
+    const int resident = h->sms * h->pass_blocks;
+    long long rows = (long long)j.B * rows_per_seq;
+    int max_parts = std::max(1, (j.nvec + kStageVecs - 1) / kStageVecs);
+    long long want = (4LL * resident + rows - 1) / std::max(rows, 1LL);
+    int parts = (int)std::min<long long>(std::max<long long>(want, 1), std::min(max_parts, 16));
+    j.rows_per_seq = rows_per_seq;
+    j.parts = parts;
+    j.part_vecs = (j.nvec + parts - 1) / parts;
+    j.parts = (j.nvec + j.part_vecs - 1) / j.part_vecs;  // no empty part
+    j.total_units = rows * j.parts;
+    j.tv_chunks = tv_chunks;
+    j.resid_chunks = kResidChunksHost;
+    Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks);
+    sv_status st = ensure_ws(h, L.total, s);
+    if (st != SV_OK) return st;
+    st = ensure_cnt(h, j.B, s);
+    if (st != SV_OK) return st;
+    j.seq_done = h->cnt;
+    j.tvdone = h->cnt + h->cnt_B;
+    j.rdone = h->cnt + (size_t)h->cnt_B * (1 + kMaxK);
+    char *w = h->ws;
+    j.rp = (RowPart *)(w + L.rp);
+    j.rs_stat = (RowStat *)(w + L.rs);
+    j.resid = (ResidEntry *)(w + L.resid);
+    j.rescue = (RescueEntry *)(w + L.rescue);
+    j.dtmp = (DraftTmp *)(w + L.dtmp);
+    j.tvpart = (float *)(w + L.tvpart);
+    j.rpart = (double *)(w + L.rpart);
+    *grid = (int)std::min<long long>(j.total_units, resident);
+    return SV_OK;
+}
+
+sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post, bool tv)
+{
+    if (h->timing) cudaEventRecord(h->ev[0], s);
+    cudaError_t e = pass_launch(j, grid, s);
+    if (h->timing) cudaEventRecord(h->ev[1], s);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (!post) return SV_OK;
+    return cuda_status(post_launch(j, h->sms * h->post_blocks, h->sms, tv, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *sv_status_string(sv_status s)
+{
+    switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_CUDA: return "CUDA runtime error";
+    case SV_ERR_OOM: return "out of device memory";
+    case SV_ERR_TIMEOUT: return "a bounded device wait expired";
+    case SV_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case SV_ERR_DEVICE_BOUNDS: return "token id, position or parent out of range";
+    }
+    return "unknown status";
+}
+
+sv_status sv_create(sv_handle **out)
+{
+    if (!out) return SV_ERR_INVALID_ARG;
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_UNSUPPORTED;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SV_ERR_UNSUPPORTED;
+    if (prop.major != 10 || prop.minor != 3) return SV_ERR_UNSUPPORTED;  // built for sm_103a
+    sv_handle *h = new sv_handle();
+    h->device = dev;
+    h->sms = prop.multiProcessorCount;
+    int nb = 0, pb = 0;
+    cudaError_t e = pass_setup(&nb);
+    h->pass_blocks = std::max(nb, 1);
+    if (e == cudaSuccess) e = post_setup(&pb);
+    h->post_blocks = std::max(1, std::min(pb, 2));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_ctl, C_NCTL * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_gtab, kGTab * sizeof(float));
+    if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->d_ctl, 0, C_NCTL * sizeof(unsigned));
+    if (e == cudaSuccess) {
+        float t[kGTab];
+        gumbel_bound_table(t);
+        e = cudaMemcpy(h->d_gtab, t, sizeof t, cudaMemcpyHostToDevice);
+    }
+    if (e != cudaSuccess) {
+        sv_destroy(h);
+        return cuda_status(e);
+    }
+    *out = h;
+    return SV_OK;
+}
+
+sv_status sv_destroy(sv_handle *h)
+{
+    if (!h) return SV_OK;
+    cudaDeviceSynchronize();
+    if (h->ws) cudaFree(h->ws);
+    if (h->cnt) cudaFree(h->cnt);
+    if (h->d_err) cudaFree(h->d_err);
+    if (h->d_ctl) cudaFree(h->d_ctl);
+    if (h->d_gtab) cudaFree(h->d_gtab);
+    delete h;
+    return SV_OK;
+}
+
+sv_status sv_sync_status(sv_handle *h, void *stream)
+{
+    if (!h) return SV_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    int code = 0;
+    e = cudaMemcpy(&code, h->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (code != 0) {
+        // A wait expired or an input was out of range: the counters may not
+        // have returned to zero, so clear them with the error word.
+        cudaMemset(h->d_err, 0, sizeof(int));
+        unsigned keep = 0;
+        cudaMemcpy(&keep, h->d_ctl + C_RESCUED, sizeof(unsigned), cudaMemcpyDeviceToHost);
+        cudaMemset(h->d_ctl, 0, C_NCTL * sizeof(unsigned));
+        cudaMemcpy(h->d_ctl + C_RESCUED, &keep, sizeof(unsigned), cudaMemcpyHostToDevice);
+        if (h->cnt) cudaMemset(h->cnt, 0, (size_t)h->cnt_B * kCntPerSeq * sizeof(unsigned));
+        cudaDeviceSynchronize();
+    }
+    return (sv_status)code;
+}
+
+sv_status sv_rescue_count(sv_handle *h, void *stream, int64_t *count)
+{
+    if (!h || !count) return SV_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    unsigned c = 0;
+    e = cudaMemcpy(&c, h->d_ctl + C_RESCUED, sizeof c, cudaMemcpyDeviceToHost);
+    *count = c;
+    return cuda_status(e);
+}
+
+sv_status sv_selftest(sv_handle *h, uint64_t seed, int64_t n, double *ratios, void *stream)
+{
+    if (!h || !ratios || n < 1) return SV_ERR_INVALID_ARG;
+    return cuda_status(selftest_run(seed, n, ratios, (cudaStream_t)stream));
+}
+
+sv_status sv_set_option(sv_handle *h, sv_option opt, int64_t value)
+{
+    if (!h) return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    switch (opt) {
+    case SV_OPT_FORCE_RESCUE:
+        h->force_rescue = value ? 1 : 0;
+        return SV_OK;
+    case SV_OPT_TIMING_EVENTS:
+        if (value == 0) {
+            h->timing = false;
+            return SV_OK;
+        }
+        memcpy(h->ev, (const void *)(intptr_t)value, sizeof h->ev);
+        h->timing = true;
+        return SV_OK;
+    }
+    return SV_ERR_INVALID_ARG;
+}
+
+sv_status sv_verify_greedy(sv_handle *h, const void *target, sv_dtype dtype, int64_t row_stride,
+                           int B, int K, int V, const int32_t *draft_ids,
+                           const int32_t *draft_len, int32_t *accept_len, int32_t *next_token,
+                           void *stream)
+{
+    if (!h || B < 0 || K < 0 || K > kMaxK) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!logits_ok(target, dtype, row_stride, V) || !accept_len || !next_token ||
+        (K > 0 && !draft_ids))
+        return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    Job j;
+    fill_common(j, h, target, dtype, row_stride, V);
+    j.kind = K_GREEDY;
+    j.B = B;
+    j.K = K;
+    j.ids = draft_ids;
+    j.lens = draft_len;
+    j.acc = accept_len;
+    j.next = next_token;
+    int grid;
+    sv_status st = plan(h, j, K + 1, s, 1, &grid);
+    if (st != SV_OK) return st;
+    return launch(h, j, grid, s, false, false);
+}
+
+sv_status sv_verify_sample(sv_handle *h, const void *target, const void *draft, sv_dtype dtype,
+                           int64_t row_stride, int B, int K, int V, const int32_t *draft_ids,
+                           const int32_t *draft_len, float T_p, float T_q, sv_accept_mode mode,
+                           float lam, uint64_t seed, const int64_t *pos_base,
+                           int32_t *accept_len, int32_t *next_token, float *p_at_draft,
+                           float *q_at_draft, float *lse_p, float *lse_q, float *tv,
+                           int32_t *flags, void *stream)
+{
+    if (!h || B < 0 || K < 0 || K > kMaxK) return SV_ERR_INVALID_ARG;
+    if (!(T_p >= 0.f) || !(T_q >= 0.f) || !isfinite(T_p) || !isfinite(T_q)) return SV_ERR_INVALID_ARG;
+    if (mode == SV_LENIENT_RATIO && !(lam >= 1.f && isfinite(lam))) return SV_ERR_INVALID_ARG;
+    if (mode == SV_LENIENT_LINEAR && !(lam >= 0.f && lam <= 1.f)) return SV_ERR_INVALID_ARG;
+    if (mode != SV_LOSSLESS && mode != SV_LENIENT_RATIO && mode != SV_LENIENT_LINEAR)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (T_p == 0.f) {  // greedy rule on the target rows
+        if (T_q != 0.f) return SV_ERR_INVALID_ARG;
+        return sv_verify_greedy(h, target, dtype, row_stride, B, K, V, draft_ids, draft_len,
+                                accept_len, next_token, stream);
+    }
+    if (T_q == 0.f) return SV_ERR_INVALID_ARG;
+    if (!logits_ok(target, dtype, row_stride, V) || !accept_len || !next_token ||
+        (K > 0 && (!draft_ids || !logits_ok(draft, dtype, row_stride, V))))
+        return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    Job j;
+    fill_common(j, h, target, dtype, row_stride, V);
+    j.kind = K_SAMPLE;
+    j.src1 = (const char *)draft;
+    j.B = B;
+    j.K = K;
+    j.Tp = T_p;
+    j.Tq = T_q;
+    j.cp = (float)(1.4426950408889634 / (double)T_p);
+    j.cq = (float)(1.4426950408889634 / (double)T_q);
+    j.invTp = (float)(1.0 / (double)T_p);
+    j.amode = mode;
+    j.lam = lam;
+    j.seed = seed;
+    j.ids = draft_ids;
+    j.lens = draft_len;
+    j.pos_base = pos_base;
+    j.acc = accept_len;
+    j.next = next_token;
+    j.flags = flags;
+    j.p_at = p_at_draft;
+    j.q_at = q_at_draft;
+    j.lse_p = lse_p;
+    j.lse_q = lse_q;
+    j.tv = tv;
+    const int tvc = (int)std::min<long long>(
+        16, std::max<long long>(1, (4LL * h->sms + (long long)B * std::max(K, 1) - 1) /
+                                       ((long long)B * std::max(K, 1))));
+    int grid;
+    sv_status st = plan(h, j, 2 * K + 1, s, tvc, &grid);
+    if (st != SV_OK) return st;
+    return launch(h, j, grid, s, true, tv != nullptr && K > 0);
+}
+
+sv_status sv_verify_tree(sv_handle *h, const void *node_logits, sv_dtype dtype, int64_t row_stride,
+                         int B, int N, int V, const int32_t *parent, const int32_t *node_pos,
+                         const int32_t *node_tok, float T, uint64_t seed,
+                         const int64_t *pos_base, int32_t *path_len, int32_t *path_nodes,
+                         int max_depth, int32_t *commit_count, uint8_t *match, int32_t *flags,
+                         void *stream)
+{
+    if (!h || B < 0 || N < 1 || N > kMaxN || max_depth < 0) return SV_ERR_INVALID_ARG;
+    if (!(T >= 0.f) || !isfinite(T)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!path_len || !commit_count || (max_depth > 0 && !path_nodes)) return SV_ERR_INVALID_ARG;
+    if (!logits_ok(node_logits, dtype, row_stride, V) || !parent || !node_pos || !node_tok)
+        return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    Job j;
+    fill_common(j, h, node_logits, dtype, row_stride, V);
+    j.kind = K_TREE;
+    j.B = B;
+    j.N = N;
+    j.Tp = T;
+    j.invTp = T > 0.f ? (float)(1.0 / (double)T) : 0.f;
+    j.seed = seed;
+    j.pos_base = pos_base;
+    j.parent = parent;
+    j.node_pos = node_pos;
+    j.node_tok = node_tok;
+    j.path_len = path_len;
+    j.path_nodes = path_nodes;
+    j.max_depth = max_depth;
+    j.commit_count = commit_count;
+    j.match = match;
+    j.flags = flags;
+    int grid;
+    sv_status st = plan(h, j, N, s, 1, &grid);
+    if (st != SV_OK) return st;
+    return launch(h, j, grid, s, false, false);
+}
+
+sv_status sv_packed_step(sv_handle *h, const void *logits, sv_dtype dtype, int64_t row_stride,
+                         int B, int K, int W, int V, const int32_t *prev_draft,
+                         const int32_t *prev_len, const float *prev_q_at_draft,
+                         const void *prev_draft_logits, const int32_t *prev_q_offset, float T,
+                         uint64_t seed, uint64_t iter, const int64_t *pos_base, int32_t eos_id,
+                         const int32_t *remaining, int32_t *accept_len, int32_t *commit_len,
+                         int32_t *committed, int32_t *next_draft, int32_t *next_len,
+                         float *next_q_at_draft, float *confidence, int32_t *flags,
+                         void *stream)
+{
+    if (!h || B < 0 || K < 1 || K > kMaxK || W < 1 || W > kMaxK) return SV_ERR_INVALID_ARG;
+    if (!(T >= 0.f) || !isfinite(T)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!logits_ok(logits, dtype, row_stride, V) || !prev_len || (K > 1 && !prev_draft) ||
+        !accept_len || !commit_len || !committed || !next_draft || !next_len)
+        return SV_ERR_INVALID_ARG;
+    if (T > 0.f && ((K > 1 && !prev_q_at_draft) || !prev_q_offset ||
+                    !logits_ok(prev_draft_logits, dtype, row_stride, V)))
+        return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    Job j;
+    fill_common(j, h, logits, dtype, row_stride, V);
+    j.kind = K_PACKED;
+    j.src2 = (const char *)prev_draft_logits;
+    j.B = B;
+    j.K = K;
+    j.W = W;
+    j.Tp = T;
+    j.Tq = T;
+    j.cp = T > 0.f ? (float)(1.4426950408889634 / (double)T) : 0.f;
+    j.cq = j.cp;
+    j.invTp = T > 0.f ? (float)(1.0 / (double)T) : 0.f;
+    j.seed = seed;
+    j.iter = iter;
+    j.pos_base = pos_base;
+    j.eos = eos_id;
+    j.remaining = remaining;
+    j.ids = prev_draft;
+    j.lens = prev_len;
+    j.prev_q = prev_q_at_draft;
+    j.prev_off = prev_q_offset;
+    j.acc = accept_len;
+    j.commit_len = commit_len;
+    j.committed = committed;
+    j.next_draft = next_draft;
+    j.next_len = next_len;
+    j.next_q = next_q_at_draft;
+    j.confidence = confidence;
+    j.flags = flags;
+    int grid;
+    sv_status st = plan(h, j, K + W, s, 1, &grid);
+    if (st != SV_OK) return st;
+    return launch(h, j, grid, s, T > 0.f, false);
+}
+
+}  // extern "C"

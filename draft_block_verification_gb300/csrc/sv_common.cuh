@@ -1,0 +1,240 @@
+// sv_common.cuh -- decision-step helpers shared by the streaming kernel and
+// the post-pass kernels (residual draw, total variation, fp64 path).
+#pragma once
+
+#include <math.h>
+
+#include "sv_gumbel.cuh"
+#include "sv_job.cuh"
+
+namespace sv {
+
+__device__ __forceinline__ int clamp_len(const Job &j, int b)
+{
+    int n = seq_len(j, b);
+    int hi = (j.kind == K_PACKED) ? j.K - 1 : j.K;
+    return min(max(n, 0), hi);
+}
+
+// ---------------------------------------------------------------------------
+// Row merging for the decision step.
+// ---------------------------------------------------------------------------
+struct RowM {
+    float m, mn;
+    int amax;
+    double L2b1, L2b2;  // base-2 log-sum-exp of x c1 and x c2: log2 sum_v 2^(x_v c)
+    Cand2 gc;           // Gumbel candidates of the row
+};
+
+constexpr double kLn2 = 0.6931471805599453;
+
+__device__ __forceinline__ RowPart load_part(const RowPart *p)
+{
+    RowPart r;
+    const uint4 *s = reinterpret_cast<const uint4 *>(p);
+    uint4 *d = reinterpret_cast<uint4 *>(&r);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(RowPart) / 16); ++i)
+        d[i] = __ldcg(s + i);
+    return r;
+}
+
+// Merge the unit records of one row.  Each record holds its unit max m_u and
+// s_u = sum 2^(x c - fl32(m_u c)); the row's base-2 log-sum-exp is
+// fl32(M c) + log2 sum_u s_u 2^(fl32(m_u c) - fl32(M c)), in fp64.
+static __device__ RowM merge_row(const Job &j, int b, int slot, float c1, float c2)
+{
+    const RowPart *p = j.rp + ((int64_t)b * j.rows_per_seq + slot) * j.parts;
+    RowM r;
+    r.m = -INFINITY;
+    r.mn = INFINITY;
+    r.amax = 0x7FFFFFFF;
+    r.gc.init();
+    for (int q = 0; q < j.parts; ++q) {
+        RowPart x = load_part(p + q);
+        if (x.m > r.m || (x.m == r.m && x.amax < r.amax)) {
+            r.m = x.m;
+            r.amax = x.amax;
+        }
+        r.mn = fminf(r.mn, x.mn);
+        Cand2 c;
+        c.hi1 = x.ghi1;
+        c.lo1 = x.glo1;
+        c.hi2 = x.ghi2;
+        c.lo2 = x.glo2;
+        c.hi3 = x.ghi3;
+        c.v1 = x.gv1;
+        c.v2 = x.gv2;
+        r.gc.merge(c);
+    }
+    const double M1 = (double)__fmul_rn(r.m, c1), M2 = (double)__fmul_rn(r.m, c2);
+    double S1 = 0.0, S2 = 0.0;
+    for (int q = 0; q < j.parts; ++q) {
+        RowPart x = load_part(p + q);
+        if (x.s1 > 0.f)
+            S1 += (double)x.s1 * exp2((double)__fmul_rn(x.m, c1) - M1);
+        if (x.s2 > 0.f)
+            S2 += (double)x.s2 * exp2((double)__fmul_rn(x.m, c2) - M2);
+    }
+    r.L2b1 = M1 + log2(S1);
+    r.L2b2 = M2 + log2(S2);
+    return r;
+}
+
+// Relative error bound of exp(L) for a row merged with temperature factor c.
+__device__ __forceinline__ double row_eps(const RowM &r, float c)
+{
+    double range = ((double)r.m - (double)r.mn) * (double)c;
+    double amax = fmax(fabs((double)r.m), fabs((double)r.mn)) * (double)c;
+    return lse_rel_bound_fma(2.0 * range, amax);
+}
+
+__device__ __forceinline__ const char *row_ptr(const Job &j, int b, int slot)
+{
+    return slot_row(j, b, slot);
+}
+
+__device__ __forceinline__ float load_logit(const Job &j, const char *row, int v)
+{
+    return j.dtype == SV_BF16 ? VecTraits<uint16_t>::load1(row, v) : VecTraits<float>::load1(row, v);
+}
+
+__device__ __forceinline__ double alpha_of(int mode, double r, double lam)
+{
+    double a = (mode == SV_LENIENT_RATIO) ? lam * r
+             : (mode == SV_LENIENT_LINEAR) ? (1.0 - lam) * r + lam
+                                           : r;
+    return a < 1.0 ? a : 1.0;
+}
+
+// ---------------------------------------------------------------------------
+// Level 3 of the Gumbel-max filter for a logit row (score x/T + G).
+// ---------------------------------------------------------------------------
+struct GRes {
+    int v;     // winner
+    int flag;  // best and second-best fp64 scores closer than 1e-9
+};
+
+__device__ __forceinline__ double exact_logit_score(const Job &j, const char *row, uint64_t key,
+                                                    double T, int v)
+{
+    float x = load_logit(j, row, v);
+    return (double)x / T + gumbel_of(uniform_at(key, (uint32_t)v));
+}
+
+// The best candidate's lower end beats every other upper end by > 1e-9.
+__device__ __forceinline__ bool gumbel_certified(const Cand2 &c)
+{
+    float other = fmaxf(c.hi2, c.hi3);
+    return c.v1 >= 0 && ((double)c.lo1 - (double)other > kFlagEps);
+}
+
+// Warp-level (all 32 lanes, uniform arguments).  Certified candidates return
+// at once; otherwise the two kept candidates are scored in fp64, and if some
+// other element's upper end still reaches within 1e-9 of the best (rare) the
+// whole row is rescanned with fp64 scores for everything its table bound
+// admits.
+static __device__ GRes resolve_logit_row(const Job &j, const char *row, uint64_t key, double T,
+                                         float invT, const Cand2 &c)
+{
+    if (gumbel_certified(c))
+        return GRes{c.v1, 0};
+    double s1 = (c.v1 >= 0) ? exact_logit_score(j, row, key, T, c.v1) : -INFINITY;
+    double s2 = (c.v2 >= 0) ? exact_logit_score(j, row, key, T, c.v2) : -INFINITY;
+    bool first = c.v2 < 0 || s1 > s2 || (s1 == s2 && c.v1 < c.v2);
+    double best = first ? s1 : s2, second = first ? s2 : s1;
+    if ((double)c.hi3 < best - kFlagEps)
+        return GRes{first ? c.v1 : c.v2, (best - second < kFlagEps) ? 1 : 0};
+    const int lane = threadIdx.x & 31;
+    const float thr = level1_thr(__double2float_rd(best - 2.0 * kFlagEps));
+    Top2 t;
+    t.init();
+    for (int v = lane; v < j.V; v += 32) {
+        uint32_t b0 = (word_a((uint32_t)key, (uint32_t)v >> 2) >> (8u * (v & 3))) & 0xFFu;
+        float x = load_logit(j, row, v);
+        if (fmaf(x, invT, gup_of(j.gtab, key, (uint32_t)v, b0)) < thr)
+            continue;
+        t.add((double)x / T + gumbel_of(u_of(bits52_of(key, (uint32_t)v, b0))), v);
+    }
+    warp_top2(t);
+    return GRes{t.i1, (t.s1 - t.s2 < kFlagEps) ? 1 : 0};
+}
+
+// Warp-level: each lane holds the candidates of one logit row (need = false
+// when it holds none); rows that are not certified are resolved one at a time
+// by the whole warp.  Returns the lane's winner and near-tie flag.
+static __device__ GRes resolve_lanes(const Job &j, const char *row, uint64_t key, double T,
+                                     float invT, const Cand2 &c, bool need)
+{
+    const int lane = threadIdx.x & 31;
+    GRes out{c.v1, 0};
+    unsigned m = __ballot_sync(0xFFFFFFFFu, need && !gumbel_certified(c));
+    while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const char *r2 = (const char *)__shfl_sync(0xFFFFFFFFu, (unsigned long long)row, src);
+        uint64_t k2 = __shfl_sync(0xFFFFFFFFu, (unsigned long long)key, src);
+        double T2 = __shfl_sync(0xFFFFFFFFu, T, src);
+        float i2 = __shfl_sync(0xFFFFFFFFu, invT, src);
+        Cand2 c2;
+        c2.hi1 = __shfl_sync(0xFFFFFFFFu, c.hi1, src);
+        c2.lo1 = __shfl_sync(0xFFFFFFFFu, c.lo1, src);
+        c2.hi2 = __shfl_sync(0xFFFFFFFFu, c.hi2, src);
+        c2.lo2 = __shfl_sync(0xFFFFFFFFu, c.lo2, src);
+        c2.hi3 = __shfl_sync(0xFFFFFFFFu, c.hi3, src);
+        c2.v1 = __shfl_sync(0xFFFFFFFFu, c.v1, src);
+        c2.v2 = __shfl_sync(0xFFFFFFFFu, c.v2, src);
+        GRes r = resolve_logit_row(j, r2, k2, T2, i2, c2);
+        if (lane == src)
+            out = r;
+    }
+    return out;
+}
+
+// Writes the stopping index, the committed tokens, the next draft and the
+// flags of a Packed-SS sequence once h is decided ([PackedSS] Alg. 1 lines
+// 6-10, Alg. 2 lines 8-13).  The correction c may still be unknown (c_known
+// false): it is then written later at committed[b, h] by the residual kernel;
+// an EOS at index h can only give a = h + 1, so a never depends on c.
+// Shared with the fp64 path.  Called by one full warp.
+static __device__ void packed_commit(const Job &j, int b, int h, int c, bool c_known, int flags_base)
+{
+    const int lane = threadIdx.x & 31;
+    const int Km1 = j.K - 1;
+    int d = (lane < h) ? __ldg(j.ids + (int64_t)b * Km1 + lane) : -1;
+    bool eos = (j.eos >= 0) && (lane < h) && (d == j.eos);
+    unsigned em = __ballot_sync(0xFFFFFFFFu, eos);
+    int a = h + 1;
+    if (j.remaining)
+        a = min(a, max(__ldg(j.remaining + b), 0));
+    if (em)
+        a = min(a, __ffs(em));  // first EOS at 1-indexed position i
+    if (c_known && j.eos >= 0 && c == j.eos)
+        a = min(a, h + 1);
+    if (lane < j.K) {
+        int tok = -1;
+        if (lane < a)
+            tok = (lane < h) ? d : (c_known ? c : -1);
+        j.committed[(int64_t)b * j.K + lane] = tok;
+    }
+    int nl = max(0, j.W - a);
+    int gf = 0;
+    if (lane < j.W) {
+        const float nan = __int_as_float(0x7FC00000);
+        int src = a + lane;
+        DraftTmp t = (lane < nl) ? j.dtmp[(int64_t)b * j.W + src] : DraftTmp{-1, 0, nan, 0.f};
+        j.next_draft[(int64_t)b * j.W + lane] = t.z;
+        if (j.next_q) j.next_q[(int64_t)b * j.W + lane] = (lane < nl) ? t.q : nan;
+        gf = (lane < nl) ? t.gflag : 0;
+    }
+    for (int o = 16; o; o >>= 1)
+        gf += __shfl_xor_sync(0xFFFFFFFFu, gf, o);
+    if (lane == 0) {
+        j.acc[b] = h;
+        j.commit_len[b] = a;
+        j.next_len[b] = nl;
+        if (j.flags) j.flags[b] = flags_base + gf;
+    }
+}
+
+}  // namespace sv

@@ -1,0 +1,442 @@
+// sv_dev.cuh -- device-side building blocks of libsv: the counter-based random
+// numbers, error latching, mbarrier / bulk-copy wrappers, per-row partial
+// records and warp reductions.
+//
+// Sources (short names used in comments):
+//   [PackedSS] "One Call Ahead: Packed Self-Speculative Decoding with Diffusion Drafting"
+//   [SPOT]     "On the SPOT: Enhancing Speculative Decoding for Diffusion Language Models
+//               via Commit-Order Prediction"
+//   [TwoTrade] "Speculative Diffusion is a Tale of Two Tradeoffs"
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// Launch geometry of the streaming kernel.
+// ---------------------------------------------------------------------------
+#ifndef SV_CONSUMER_WARPS
+#define SV_CONSUMER_WARPS 8
+#endif
+#ifndef SV_STAGES
+#define SV_STAGES 8
+#endif
+#ifndef SV_STAGE_BYTES
+#define SV_STAGE_BYTES 16384
+#endif
+#ifndef SV_SPIN_SLEEP_NS
+#define SV_SPIN_SLEEP_NS 64
+#endif
+#ifndef SV_MIN_BLOCKS
+#define SV_MIN_BLOCKS 1
+#endif
+constexpr int kConsumerWarps = SV_CONSUMER_WARPS;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kPassThreads = kConsumers + 32;     // + one producer warp
+constexpr int kStageBytes = SV_STAGE_BYTES;       // one bulk copy
+constexpr int kStageVecs = kStageBytes / 16;      // 16-byte vectors per stage
+constexpr int kVecsPerThread = kStageVecs / kConsumers;
+constexpr int kStages = SV_STAGES;
+static_assert(kVecsPerThread * kConsumers == kStageVecs, "stage must split evenly");
+constexpr int kMaxK = 32;
+constexpr int kMaxN = 64;
+constexpr double kFlagEps = 1e-9;                 // near-threshold window
+
+// Random-number streams.
+enum : uint32_t { kAccept = 1, kSample = 2, kDraft = 3, kTree = 4 };
+
+// Row work modes (bit set).
+enum : int { M_ARGMAX = 1, M_LSE = 2, M_LSE2 = 4, M_GUMBEL = 8 };
+
+// Entry-point kinds.
+enum : int { K_GREEDY = 0, K_SAMPLE = 1, K_TREE = 2, K_PACKED = 3 };
+
+// ---------------------------------------------------------------------------
+// Counter-based random numbers.  Written from the published definitions of
+// the two mixers: SplitMix64's output function (Steele, Lea & Flood) and the
+// MurmurHash3 32-bit finalizer (Appleby).
+//   key(seed, stream, seq, pos, iter): fold each field into a running 64-bit
+//     state through the SplitMix64 output function.
+//   For vocabulary id v the 52 random bits m are, most significant first:
+//     byte (v mod 4) of fmix32(low32(key) xor (v div 4) * 0x9E3779B9),
+//     byte (v mod 4) of fmix32(high32(key) xor (v div 4) * 0x85EBCA77),
+//     the top 36 bits of splitmix64(key xor v * 0xD1B54A32D192ED03);
+//   u = (2m + 1) 2^-53 (sv_gumbel.cuh).
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ uint64_t splitmix_out(uint64_t state)
+{
+    uint64_t z = state + 0x9E3779B97F4A7C15ull;
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z;
+}
+
+__host__ __device__ __forceinline__ uint32_t murmur_fmix(uint32_t x)
+{
+    x ^= x >> 16;
+    x *= 0x85EBCA6Bu;
+    x ^= x >> 13;
+    x *= 0xC2B2AE35u;
+    x ^= x >> 16;
+    return x;
+}
+
+__host__ __device__ __forceinline__ uint64_t rng_key(uint64_t seed, uint32_t stream, uint64_t seq,
+                                                     int64_t pos, uint64_t iter)
+{
+    uint64_t s = splitmix_out(seed);
+    s = splitmix_out(s ^ (uint64_t)stream);
+    s = splitmix_out(s ^ seq);
+    s = splitmix_out(s ^ (uint64_t)pos);
+    return splitmix_out(s ^ iter);
+}
+
+// Standard Gumbel by inversion, fp64.
+__device__ __forceinline__ double gumbel_of(double u)
+{
+    return -log(-log(u));
+}
+
+// ---------------------------------------------------------------------------
+// Error latch: the first non-OK status wins.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void latch(int *err, int code)
+{
+    atomicCAS(err, 0, code);
+}
+
+// Spin limits (iterations); every wait in libsv is bounded.
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk-copy wrappers (sm_90+ PTX).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; returns false when the limit expired.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try(bar, parity))
+            return true;
+        if (SV_SPIN_SLEEP_NS > 0 && i > 64)
+            __nanosleep(SV_SPIN_SLEEP_NS);
+    }
+    return false;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Fast 2^x (MUFU); relative error within 2^-21 over the range used here, which
+// the error bounds below assume and a GPU test measures.
+__device__ __forceinline__ float ex2f(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------
+// Ordered encoding of floats for unsigned atomicMax.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t f2ord(float f)
+{
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(uint32_t o)
+{
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// ---------------------------------------------------------------------------
+// Partial statistics of one unit (a contiguous part of one logit row).
+// ---------------------------------------------------------------------------
+struct __align__(16) RowPart {
+    float m;      // max logit of the part (raw value)
+    float mn;     // min logit of the part
+    float s1;     // sum 2^(x c1 - fl(m c1))
+    float s2;     // sum 2^(x c2 - fl(m c2))
+    int amax;     // lowest id attaining m
+    // Gumbel candidates (see Cand2 in sv_gumbel.cuh)
+    float ghi1, glo1, ghi2, glo2, ghi3;
+    int gv1, gv2;
+    int pad[4];
+};
+
+// Merged per-row statistics kept for the later kernels.
+struct __align__(16) RowStat {
+    double L1;    // natural log-sum-exp of x / T (the row's temperature)
+    double L2;    // base-2 log-sum-exp of x c, c = fl32(log2(e) / T)
+    float m;      // row max
+    float eps;    // bound on the relative error of exp(L1) (fp32 path)
+    int gidx;     // Gumbel-max winner
+    int gflag;    // its near-tie flag
+};
+
+// Top-2 bookkeeping of exact Gumbel scores; ties go to the lower id.
+struct Top2 {
+    double s1, s2;
+    int i1;
+    __device__ __forceinline__ void init()
+    {
+        s1 = -INFINITY;
+        s2 = -INFINITY;
+        i1 = -1;
+    }
+    __device__ __forceinline__ void add(double s, int i)
+    {
+        if (s > s1 || (s == s1 && i1 >= 0 && i < i1) || i1 < 0) {
+            if (i1 >= 0)
+                s2 = fmax(s2, s1);
+            s1 = s;
+            i1 = i;
+        } else {
+            s2 = fmax(s2, s);
+        }
+    }
+    __device__ __forceinline__ void merge(double os1, int oi1, double os2)
+    {
+        if (oi1 >= 0)
+            add(os1, oi1);
+        s2 = fmax(s2, os2);
+    }
+};
+
+__device__ __forceinline__ void warp_top2(Top2 &t)
+{
+    for (int o = 16; o; o >>= 1) {
+        double a = __shfl_xor_sync(0xFFFFFFFFu, t.s1, o);
+        double c = __shfl_xor_sync(0xFFFFFFFFu, t.s2, o);
+        int i = __shfl_xor_sync(0xFFFFFFFFu, t.i1, o);
+        t.merge(a, i, c);
+    }
+}
+
+// (value desc, index asc) argmax reduction over a warp.
+__device__ __forceinline__ void warp_argmax(float &v, int &i)
+{
+    for (int o = 16; o; o >>= 1) {
+        float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        int oi = __shfl_xor_sync(0xFFFFFFFFu, i, o);
+        if (ov > v || (ov == v && (unsigned)oi < (unsigned)i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+    for (int o = 16; o; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v)
+{
+    for (int o = 16; o; o >>= 1)
+        v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+    for (int o = 16; o; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sumd(double v)
+{
+    for (int o = 16; o; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Element access of a 16-byte vector.
+template <typename In>
+struct VecTraits;
+template <>
+struct VecTraits<uint16_t> {  // bf16 bit patterns
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &q, float (&f)[8])
+    {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(w[j] << 16);
+            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+    __device__ __forceinline__ static float load1(const void *row, int v)
+    {
+        uint16_t b = __ldg((const unsigned short *)row + v);
+        return __uint_as_float((uint32_t)b << 16);
+    }
+    // Packed (bf16x2) max and min over the 8 elements; invalid vectors give
+    // -inf / +inf.
+    __device__ __forceinline__ static uint32_t pmax(const uint4 &q)
+    {
+        return bmax(bmax(q.x, q.y), bmax(q.z, q.w));
+    }
+    __device__ __forceinline__ static uint32_t pmin(const uint4 &q)
+    {
+        return bmin(bmin(q.x, q.y), bmin(q.z, q.w));
+    }
+    __device__ __forceinline__ static uint32_t bmax(uint32_t a, uint32_t b)
+    {
+        __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    __device__ __forceinline__ static uint32_t bmin(uint32_t a, uint32_t b)
+    {
+        __nv_bfloat162 r = __hmin2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                   *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    static constexpr uint32_t kNegInf = 0xFF80FF80u, kPosInf = 0x7F807F80u;
+    // element i (run-time index) of the vector, without local memory
+    __device__ __forceinline__ static float elem(const uint4 &q, int i)
+    {
+        uint32_t w = (i < 2) ? q.x : (i < 4) ? q.y : (i < 6) ? q.z : q.w;
+        return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+    // largest of the 4 elements of group g (elements 4g .. 4g+3)
+    __device__ __forceinline__ static float group_max(const uint4 &q, int g)
+    {
+        uint32_t p = g == 0 ? bmax(q.x, q.y) : bmax(q.z, q.w);
+        return fmaxf(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ static float hi_of(uint32_t p)
+    {
+        return fmaxf(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ static float lo_of(uint32_t p)
+    {
+        return fminf(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+    }
+};
+template <>
+struct VecTraits<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &q, float (&f)[4])
+    {
+        f[0] = __uint_as_float(q.x);
+        f[1] = __uint_as_float(q.y);
+        f[2] = __uint_as_float(q.z);
+        f[3] = __uint_as_float(q.w);
+    }
+    __device__ __forceinline__ static float load1(const void *row, int v)
+    {
+        return __ldg((const float *)row + v);
+    }
+    __device__ __forceinline__ static uint32_t pmax(const uint4 &q)
+    {
+        return __float_as_uint(fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                     fmaxf(__uint_as_float(q.z), __uint_as_float(q.w))));
+    }
+    __device__ __forceinline__ static uint32_t pmin(const uint4 &q)
+    {
+        return __float_as_uint(fminf(fminf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                                     fminf(__uint_as_float(q.z), __uint_as_float(q.w))));
+    }
+    __device__ __forceinline__ static uint32_t bmax(uint32_t a, uint32_t b)
+    {
+        return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+    }
+    __device__ __forceinline__ static uint32_t bmin(uint32_t a, uint32_t b)
+    {
+        return __float_as_uint(fminf(__uint_as_float(a), __uint_as_float(b)));
+    }
+    static constexpr uint32_t kNegInf = 0xFF800000u, kPosInf = 0x7F800000u;
+    __device__ __forceinline__ static float group_max(const uint4 &q, int)
+    {
+        return __uint_as_float(pmax(q));
+    }
+    __device__ __forceinline__ static float elem(const uint4 &q, int i)
+    {
+        return __uint_as_float((i == 0) ? q.x : (i == 1) ? q.y : (i == 2) ? q.z : q.w);
+    }
+    __device__ __forceinline__ static float hi_of(uint32_t p) { return __uint_as_float(p); }
+    __device__ __forceinline__ static float lo_of(uint32_t p) { return __uint_as_float(p); }
+};
+
+// Relative error bounds of exp(L) for a row log-sum-exp L computed in fp32.
+//
+// Streaming kernel (terms 2^fl(x c - fl(m_ref c)), one FFMA each): ex2 per term
+// and the per-thread rescale (2 x 2^-21, plus one for slack); rounding of each
+// term's exponent |t| <= R = (max - min) c (ln 2 * 2^-24 * R); rounding of
+// c = log2(e)/T itself, which shifts every exponent by at most
+// 2^-24 * c * max|x| (ln 2 * 2^-24 * c * max|x|); and a summation depth of at
+// most 64 fp32 additions.
+__host__ __device__ __forceinline__ double lse_rel_bound_fma(double range_c, double absmax_c)
+{
+    return 3.0 * 0x1p-21 + 0.6931471805599453 * 0x1p-24 * (range_c + absmax_c) + 64.0 * 0x1p-24;
+}
+// Row passes that subtract first (terms 2^((x - m_ref) c)): exponent rounding
+// of 3 ulps of |t| <= R.
+__host__ __device__ __forceinline__ double lse_rel_bound(double range_c)
+{
+    return 3.0 * 0x1p-21 + 3.0 * 0.6931471805599453 * 0x1p-24 * range_c + 64.0 * 0x1p-24;
+}
+
+}  // namespace sv

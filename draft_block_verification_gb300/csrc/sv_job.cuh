@@ -1,0 +1,177 @@
+// sv_job.cuh -- kernel-parameter and workspace structures of libsv.
+#pragma once
+
+#include "sv_dev.cuh"
+
+namespace sv {
+
+// A sequence whose correction must be drawn from the residual [p - q]_+ of
+// one row pair, after the fast path proved every acceptance decision.
+struct __align__(16) ResidEntry {
+    int b;          // sequence
+    int h;          // position of the first rejection (row index)
+    int need_lq;    // 1: the q row's log-sum-exp is not known yet (Packed-SS)
+    int pad;
+    const char *prow;  // target row at position h
+    const char *qrow;  // proposal row at position h
+    double Lp, Lq;     // natural log-sum-exps of x/Tp and y/Tq
+    double epsp, epsq; // relative error bounds of exp(Lp), exp(Lq)
+};
+
+// A sequence that goes to the fp64 path.
+struct __align__(16) RescueEntry {
+    int b;
+    int kind;       // 0: acceptance decisions, 1: residual draw at position h
+    int h;          // kind 1: the rejected position; set for kind 0 by the fp64 path
+    int resid;      // the fp64 path draws a residual at position h
+    double Lp, Lq;  // fp64 log-sum-exps of the residual pair
+    int flags;      // near-threshold decisions found by the fp64 path so far
+    int pad[3];
+};
+
+// Per-draft-row results of a Packed-SS proposal, kept for the fp64 path.
+struct __align__(16) DraftTmp {
+    int z;
+    int gflag;
+    float q;
+    float pad;
+};
+
+// Control words in the workspace (all return to zero after each call).
+enum : int {
+    C_UNIT = 0,       // streaming kernel: next unit
+    C_EXIT = 1,       // streaming kernel: finished CTAs
+    C_RESID_N = 2,    // residual entries
+    C_RESCUE_N = 3,   // rescue entries
+    C_RWORK = 4,      // residual kernel: next work item
+    C_REXIT = 5,      // residual kernel: finished CTAs
+    C_TWORK = 6,      // total-variation kernel: next work item
+    C_TEXIT = 7,      // total-variation kernel: finished CTAs
+    C_GBAR = 8,       // fp64 kernel: grid barrier arrivals
+    C_GGEN = 9,       // fp64 kernel: grid barrier generation
+    C_GWORK = 10,     // fp64 kernel: next work item
+    C_ABORT = 11,     // fp64 kernel: a barrier timed out
+    C_RESCUED = 12,   // running count of rescued sequences (read by the host)
+    C_NCTL = 16
+};
+
+struct Job {
+    int kind, dtype;
+    const char *src0;   // target / node / packed logits
+    const char *src1;   // drafter logits (sample)
+    const char *src2;   // previous drafter logits (packed, T > 0)
+    int64_t rs;         // row stride, bytes
+    int V, nvec;        // vocabulary; 16-byte vectors per row
+    int B, K, N, W;
+    int rows_per_seq, parts, part_vecs;
+    long long total_units;
+    float Tp, Tq;       // temperatures (tree / packed: Tp = T)
+    float cp, cq, c1;   // log2(e)/Tp, log2(e)/Tq, log2(e)
+    float invTp;        // 1/Tp rounded to fp32 (Gumbel filter)
+    int amode;          // acceptance rule
+    float lam;
+    uint64_t seed, iter;
+    int eos;
+    int force_rescue;
+    int max_depth;
+    // inputs
+    const int32_t *ids, *lens;
+    const int64_t *pos_base;
+    const int32_t *parent, *node_pos, *node_tok;
+    const float *prev_q;
+    const int32_t *prev_off, *remaining;
+    // outputs
+    int32_t *acc, *next, *flags;
+    float *p_at, *q_at, *lse_p, *lse_q, *tv;
+    int32_t *path_len, *path_nodes, *commit_count;
+    uint8_t *match;
+    int32_t *commit_len, *committed, *next_draft, *next_len;
+    float *next_q, *confidence;
+    // workspace
+    RowPart *rp;        // [B * rows_per_seq * parts]
+    RowStat *rs_stat;   // [B * rows_per_seq]
+    unsigned *seq_done; // [B]
+    unsigned *ctl;      // [C_NCTL]
+    ResidEntry *resid;  // [B]
+    RescueEntry *rescue;// [B]
+    DraftTmp *dtmp;     // [B * W]
+    float *tvpart;      // [B * K * tv_chunks]
+    unsigned *tvdone;   // [B * K]
+    int tv_chunks;
+    double *rpart;      // residual / fp64 scratch
+    unsigned *rdone;    // [B * 64] per-entry chunk counters
+    int resid_chunks;
+    int *err;
+    const float *gtab;  // [kGTab] level-1 Gumbel bounds
+};
+
+// Row slot bookkeeping shared by the kernels.
+__device__ __forceinline__ int seq_len(const Job &j, int b)
+{
+    if (j.kind == K_TREE)
+        return j.N;
+    if (!j.lens)
+        return j.kind == K_PACKED ? 0 : j.K;
+    return __ldg(j.lens + b);
+}
+
+// Number of valid row slots of sequence b (clamped lengths).
+__device__ __forceinline__ int valid_slots(const Job &j, int b)
+{
+    switch (j.kind) {
+    case K_GREEDY: {
+        int n = min(max(seq_len(j, b), 0), j.K);
+        return n + 1;
+    }
+    case K_SAMPLE: {
+        int n = min(max(seq_len(j, b), 0), j.K);
+        return 2 * n + 1;
+    }
+    case K_TREE:
+        return j.N;
+    default: {
+        int n = min(max(seq_len(j, b), 0), j.K - 1);
+        return n + 1 + j.W;
+    }
+    }
+}
+
+__device__ __forceinline__ bool slot_valid(const Job &j, int b, int slot)
+{
+    switch (j.kind) {
+    case K_GREEDY:
+        return slot <= min(max(seq_len(j, b), 0), j.K);
+    case K_SAMPLE: {
+        int n = min(max(seq_len(j, b), 0), j.K);
+        return slot <= n || (slot > j.K && slot - j.K - 1 < n);
+    }
+    case K_TREE:
+        return true;
+    default: {
+        int n = min(max(seq_len(j, b), 0), j.K - 1);
+        return slot <= n || slot >= j.K;
+    }
+    }
+}
+
+__device__ __forceinline__ const char *slot_row(const Job &j, int b, int slot)
+{
+    switch (j.kind) {
+    case K_GREEDY:
+        return j.src0 + ((int64_t)b * (j.K + 1) + slot) * j.rs;
+    case K_SAMPLE:
+        return slot <= j.K ? j.src0 + ((int64_t)b * (j.K + 1) + slot) * j.rs
+                           : j.src1 + ((int64_t)b * j.K + (slot - j.K - 1)) * j.rs;
+    case K_TREE:
+        return j.src0 + ((int64_t)b * j.N + slot) * j.rs;
+    default:
+        return j.src0 + ((int64_t)b * (j.K + j.W) + slot) * j.rs;
+    }
+}
+
+__device__ __forceinline__ int64_t pos0_of(const Job &j, int b)
+{
+    return j.pos_base ? __ldg(j.pos_base + b) : 0;
+}
+
+}  // namespace sv

@@ -1,0 +1,1011 @@
+// sv_post.cu -- the kernels that run after the streaming pass:
+//   tv_kernel     total variation 1 - sum_v min(p_v, q_v) of every (p, q) row
+//                 pair ([TwoTrade] eq. 1), a second pass over both rows;
+//   resid_kernel  the correction drawn from the residual [p - q]_+ at the
+//                 first rejection ([PackedSS] Alg. 2 line 7; [SPOT] App. B
+//                 eq. 14), a second pass over one row pair per sequence;
+//   rescue_kernel the fp64 path for the rare sequences whose fp32 decisions
+//                 fell inside their error bound.
+#include <math.h>
+
+#include "sv_common.cuh"
+
+namespace sv {
+
+constexpr int kPostThreads = 256;
+constexpr int kPostWarps = kPostThreads / 32;
+constexpr int kResidChunks = 8;     // chunks per residual row pair
+constexpr int kRescueChunks = 16;   // chunks per row on the fp64 path
+constexpr int kMaxPairs = 32;
+
+struct PostShared {
+    float f[kPostWarps][4];
+    double d[kPostWarps][4];
+    int i[kPostWarps][2];
+    uint32_t thr;
+    unsigned item;
+    int flag;
+};
+
+// ---------------------------------------------------------------------------
+// Block reductions (all threads of the block call them).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_max(float v, PostShared &sm)
+{
+    v = warp_max(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sm.f[threadIdx.x >> 5][0] = v;
+    __syncthreads();
+    float r = -INFINITY;
+    for (int w = 0; w < kPostWarps; ++w) r = fmaxf(r, sm.f[w][0]);
+    return r;
+}
+__device__ __forceinline__ float block_min(float v, PostShared &sm)
+{
+    v = warp_min(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sm.f[threadIdx.x >> 5][1] = v;
+    __syncthreads();
+    float r = INFINITY;
+    for (int w = 0; w < kPostWarps; ++w) r = fminf(r, sm.f[w][1]);
+    return r;
+}
+__device__ __forceinline__ float block_sum(float v, PostShared &sm)
+{
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sm.f[threadIdx.x >> 5][2] = v;
+    __syncthreads();
+    float r = 0.f;
+    for (int w = 0; w < kPostWarps; ++w) r += sm.f[w][2];
+    return r;
+}
+__device__ __forceinline__ double block_sumd(double v, PostShared &sm)
+{
+    v = warp_sumd(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sm.d[threadIdx.x >> 5][0] = v;
+    __syncthreads();
+    double r = 0.0;
+    for (int w = 0; w < kPostWarps; ++w) r += sm.d[w][0];
+    return r;
+}
+
+template <typename In>
+__device__ __forceinline__ uint4 ldv(const char *row, int k)
+{
+    return __ldcs(reinterpret_cast<const uint4 *>(row) + k);
+}
+
+__device__ __forceinline__ int chunk_lo(int nvec, int c, int nc) { return (int)((int64_t)nvec * c / nc); }
+
+// ---------------------------------------------------------------------------
+// fp32 log-sum-exp partial of vectors [vb, ve) of one row (same arithmetic and
+// error model as the streaming kernel): returns max, min and
+// sum 2^((x - max) c).
+// ---------------------------------------------------------------------------
+template <typename In>
+__device__ void lse_chunk32(const char *row, int vb, int ve, float c, PostShared &sm, float &M,
+                            float &S, float &mn)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    float mref = -INFINITY, acc = 0.f, mx = -INFINITY, lo = INFINITY;
+    for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
+        float f[E];
+        VT::unpack(ldv<In>(row, k), f);
+        float cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            cm = fmaxf(cm, f[e]);
+            lo = fminf(lo, f[e]);
+        }
+        mx = fmaxf(mx, cm);
+        if (mref == -INFINITY) {
+            mref = cm;
+        } else if ((cm - mref) * c > 64.f) {
+            acc *= ex2f((mref - cm) * c);
+            mref = cm;
+        }
+        float t[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) t[e] = ex2f((f[e] - mref) * c);
+#pragma unroll
+        for (int w = E / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e) t[e] += t[e + w];
+        acc += t[0];
+    }
+    M = block_max(mx, sm);
+    mn = block_min(lo, sm);
+    float mine = (mref > -INFINITY) ? acc * ex2f((mref - M) * c) : 0.f;
+    S = block_sum(mine, sm);
+}
+
+// ---------------------------------------------------------------------------
+// Total variation.
+// ---------------------------------------------------------------------------
+template <typename In>
+__global__ void __launch_bounds__(kPostThreads) tv_kernel(const Job j)
+{
+    __shared__ PostShared sm;
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    const int TC = j.tv_chunks;
+    const unsigned items = (unsigned)j.B * j.K * TC;
+    for (;;) {
+        if (threadIdx.x == 0) sm.item = atomicAdd(j.ctl + C_TWORK, 1u);
+        __syncthreads();
+        unsigned it = sm.item;
+        __syncthreads();
+        if (it >= items) break;
+        int pair = it / TC, c = it - pair * TC;
+        int b = pair / j.K, i = pair - b * j.K;
+        if (i >= clamp_len(j, b)) continue;
+        const RowStat sp = j.rs_stat[(int64_t)b * j.rows_per_seq + i];
+        const RowStat sq = j.rs_stat[(int64_t)b * j.rows_per_seq + j.K + 1 + i];
+        const float lgp = (float)sp.L2, lgq = (float)sq.L2;
+        const char *prow = slot_row(j, b, i), *qrow = slot_row(j, b, j.K + 1 + i);
+        int vb = chunk_lo(j.nvec, c, TC), ve = chunk_lo(j.nvec, c + 1, TC);
+        float acc = 0.f;
+        for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
+            float x[E], y[E];
+            VT::unpack(ldv<In>(prow, k), x);
+            VT::unpack(ldv<In>(qrow, k), y);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                float fa = fmaf(x[e], j.cp, -lgp);  // log2 p_v
+                float fb = fmaf(y[e], j.cq, -lgq);  // log2 q_v
+                acc += ex2f(fminf(fa, fb));
+            }
+        }
+        float s = block_sum(acc, sm);
+        if (threadIdx.x == 0) {
+            j.tvpart[(int64_t)pair * TC + c] = s;
+            __threadfence();
+            unsigned old = atomicAdd(j.tvdone + pair, 1u);
+            if (old + 1u == (unsigned)TC) {
+                __threadfence();
+                double S = 0.0;
+                for (int q = 0; q < TC; ++q) S += (double)__ldcg(j.tvpart + (int64_t)pair * TC + q);
+                j.tv[(int64_t)b * j.K + i] = (float)(1.0 - S);
+                j.tvdone[pair] = 0u;
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(j.ctl + C_TEXIT, 1u) + 1u == gridDim.x) {
+            j.ctl[C_TWORK] = 0u;
+            j.ctl[C_TEXIT] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Residual draw.  At the first rejection, the correction is the Gumbel-max of
+// log w_v + G(v) with w = [p - q]_+ ([SPOT] App. B eq. 14; [PackedSS] Alg. 2
+// line 7).  With a = x/Tp, b = y/Tq and Delta = Lq - Lp,
+//   log w_v = a_v - Lp + log(1 - exp(b_v - a_v - Delta))   (when b - a < Delta);
+// dropping the common -Lp, every score is bracketed for Delta in [dlo, dhi]
+// (the log-sum-exps carry the fp32 error bound of the streaming pass, or the
+// fp64 rounding on the fp64 path).  The scan uses the three-level filter of
+// sv_gumbel.cuh: the table bound ignores log(1 - .) <= 0, survivors get fp32
+// intervals (fp64 ones on the fp64 path), and the two best candidates are
+// certified or re-scored in fp64.
+// ---------------------------------------------------------------------------
+struct RBest {  // fp64-interval tracker of the fp64 path
+    double lo, hi, hio;
+    int i;
+    __device__ __forceinline__ void init()
+    {
+        lo = -INFINITY;
+        hi = -INFINITY;
+        hio = -INFINITY;
+        i = -1;
+    }
+    __device__ __forceinline__ void add(double l, double h, int v)
+    {
+        if (i < 0 || l > lo || (l == lo && v < i)) {
+            if (i >= 0) hio = fmax(hio, hi);
+            lo = l;
+            hi = h;
+            i = v;
+        } else {
+            hio = fmax(hio, h);
+        }
+    }
+    __device__ __forceinline__ void merge(const RBest &o)
+    {
+        hio = fmax(hio, o.hio);
+        if (o.i >= 0) add(o.lo, o.hi, o.i);
+    }
+};
+
+__device__ __forceinline__ double log1mexp(double a)  // log(1 - e^a), a < 0
+{
+    return (a > -0.6931471805599453) ? log(-expm1(a)) : log1p(-exp(a));
+}
+
+struct RCtx {
+    const char *prow, *qrow;
+    double Tp, Tq, dlo, dhi;
+    float invTp, invTq, dlo32, dhi32;  // [dlo32, dhi32] contains [dlo, dhi]
+    uint64_t key;
+};
+
+// fp64 interval of the residual score of id v (Delta bracket only); false
+// when w_v = 0 for every Delta in the bracket.
+__device__ __forceinline__ bool resid_interval64(const RCtx &c, float x, float y, uint64_t m,
+                                                 double &lo, double &hi)
+{
+    double z = (double)x / c.Tp, w = (double)y / c.Tq;
+    double ah = w - z - c.dhi;
+    if (!(ah < 0.0))
+        return false;
+    double al = w - z - c.dlo;
+    double G = gumbel_of(u_of(m));
+    hi = z + log1mexp(ah) + G;
+    lo = (al < 0.0) ? z + log1mexp(al) + G : -INFINITY;
+    return true;
+}
+
+// log(1 - e^d), d < 0, in fp32 with a bound on its error: e = e^d carries
+// the ex2 error and the rounding of d log2(e); t = 1 - e is then off by at
+// most e (2^-21 + |d| 2^-22) + 2^-24 t, and lg2 adds 2^-22.
+__device__ __forceinline__ float log1mexp32(float d, float &err)
+{
+    const float e = ex2f(d * 1.44269504088896f);
+    const float t = 1.f - e;
+    const float r = 0.69314718055995f * lg2a(t);
+    // lg2.approx: error 2^-22 relative to max(1, |result|)
+    err = (e * (0x1p-21f + fabsf(d) * 0x1p-22f)) / t + (1.f + fabsf(r)) * 0x1p-21f;
+    return r;
+}
+
+// fp32 interval of the residual score; false when w_v = 0 for sure.
+__device__ __forceinline__ bool resid_interval32(const RCtx &c, float x, float y, uint64_t m,
+                                                 float &lo, float &hi)
+{
+    const float z = x * c.invTp, w = y * c.invTq;
+    const float dz = w - z;
+    const float edz = (fabsf(z) + fabsf(w)) * 0x1p-21f;
+    const float dmin = (dz - c.dhi32) - edz - fabsf(dz - c.dhi32) * 0x1p-22f;  // smallest d
+    const float dmax = (dz - c.dlo32) + edz + fabsf(dz - c.dlo32) * 0x1p-22f;  // largest d
+    if (dmin >= 0.f)
+        return false;
+    const float g = gumbel32(m);
+    float e1, lwh;
+    const float lw1 = log1mexp32(dmin, e1);
+    if (1.f - ex2f(dmin * 1.44269504088896f) > 0x1p-18f && e1 < 1.f)
+        lwh = lw1 + e1;
+    else {  // 1 - e^d <= -d
+        lwh = 0.69314718055995f * lg2a(-dmin);
+        lwh += (1.f + fabsf(lwh)) * 0x1p-20f;
+    }
+    float lwl = -INFINITY;
+    if (dmax < 0.f && 1.f - ex2f(dmax * 1.44269504088896f) > 0x1p-18f) {
+        float e2;
+        const float lw2 = log1mexp32(dmax, e2);
+        if (e2 < 1.f)
+            lwl = lw2 - e2;
+    }
+    const float sh = z + lwh + g, sl = z + lwl + g;
+    const float slack = (fabsf(z) + fabsf(sh)) * 0x1p-21f + kG32Err;
+    hi = sh + slack;
+    lo = sl - ((fabsf(z) + fabsf(sl)) * 0x1p-21f + kG32Err);
+    return true;
+}
+
+// fp32 test that w_v = 0 for every Delta in the bracket.
+__device__ __forceinline__ bool surely_zero(const RCtx &c, float x, float y)
+{
+    float a = x * c.invTp, b = y * c.invTq;
+    float d = (b - a) - c.dhi32;
+    return d > (fabsf(a) + fabsf(b) + fabsf(c.dhi32) + 1.f) * 0x1p-20f;
+}
+
+// Candidate trackers of the scan: fp32 intervals (Cand2) or fp64 intervals.
+struct Track32 {
+    Cand2 c;
+    float lomax, thr, thrS;
+    __device__ __forceinline__ void init()
+    {
+        c.init();
+        lomax = thr = thrS = -INFINITY;
+    }
+    __device__ __forceinline__ void raise(float t)
+    {
+        if (t > thr) {
+            thr = t;
+            thrS = level1_thr(t);
+        }
+    }
+    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint32_t b0)
+    {
+        if (surely_zero(ctx, x, y)) return;
+        float lo, hi;
+        if (!resid_interval32(ctx, x, y, bits52_of(ctx.key, v, b0), lo, hi) || hi < thr) return;
+        c.add(lo, hi, (int)v);
+        if (lo > lomax) {
+            lomax = lo;
+            raise(__fsub_rd(lo, 1e-9f));
+        }
+    }
+};
+struct Track64 {
+    RBest r;
+    float lomax, thr, thrS;
+    __device__ __forceinline__ void init()
+    {
+        r.init();
+        lomax = thr = thrS = -INFINITY;
+    }
+    __device__ __forceinline__ void raise(float t)
+    {
+        if (t > thr) {
+            thr = t;
+            thrS = level1_thr(t);
+        }
+    }
+    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint32_t b0)
+    {
+        if (surely_zero(ctx, x, y)) return;
+        double lo, hi;
+        if (!resid_interval64(ctx, x, y, bits52_of(ctx.key, v, b0), lo, hi)) return;
+        r.add(lo, hi, (int)v);
+        if (lo > -INFINITY && (float)lo > lomax) {
+            lomax = __double2float_rd(lo);
+            raise(__double2float_rd(lo - kFlagEps - (fabs(lo) + 41.0) * 0x1p-21));
+        }
+    }
+};
+
+__device__ __forceinline__ void block_rbest(RBest &r, PostShared &sm, RBest &out)
+{
+    for (int o = 16; o; o >>= 1) {
+        RBest q;
+        q.lo = __shfl_xor_sync(0xFFFFFFFFu, r.lo, o);
+        q.hi = __shfl_xor_sync(0xFFFFFFFFu, r.hi, o);
+        q.hio = __shfl_xor_sync(0xFFFFFFFFu, r.hio, o);
+        q.i = __shfl_xor_sync(0xFFFFFFFFu, r.i, o);
+        r.merge(q);
+    }
+    __syncthreads();
+    int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sm.d[w][0] = r.lo;
+        sm.d[w][1] = r.hi;
+        sm.d[w][2] = r.hio;
+        sm.i[w][0] = r.i;
+    }
+    __syncthreads();
+    out.init();
+    for (int q = 0; q < kPostWarps; ++q) {
+        RBest t;
+        t.lo = sm.d[q][0];
+        t.hi = sm.d[q][1];
+        t.hio = sm.d[q][2];
+        t.i = sm.i[q][0];
+        out.merge(t);
+    }
+}
+
+__device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out)
+{
+    warp_cand2(c);
+    __syncthreads();
+    int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sm.f[w][0] = c.hi1;
+        sm.f[w][1] = c.lo1;
+        sm.f[w][2] = c.hi2;
+        sm.f[w][3] = c.lo2;
+        sm.d[w][0] = c.hi3;
+        sm.i[w][0] = c.v1;
+        sm.i[w][1] = c.v2;
+    }
+    __syncthreads();
+    out.init();
+    for (int q = 0; q < kPostWarps; ++q) {
+        Cand2 t;
+        t.hi1 = sm.f[q][0];
+        t.lo1 = sm.f[q][1];
+        t.hi2 = sm.f[q][2];
+        t.lo2 = sm.f[q][3];
+        t.hi3 = (float)sm.d[q][0];
+        t.v1 = sm.i[q][0];
+        t.v2 = sm.i[q][1];
+        out.merge(t);
+    }
+}
+
+// Scan vectors [vb, ve) of the pair.  Seed: each warp adds the element with
+// the largest table bound among clearly positive weights (p > 1.07 q) of its
+// threads' first vectors; the CTA starts from the best threshold.
+template <typename In, typename Tr>
+__device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, PostShared &sm, Tr &tr)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    const uint32_t klo = (uint32_t)c.key;
+    tr.init();
+    int seedv = -1;
+    {
+        float bub = -INFINITY, bx = 0.f, by = 0.f;
+        int bv = -1;
+        uint32_t bb0 = 0;
+        int k = vb + threadIdx.x;
+        if (k < ve) {
+            float x[E], y[E];
+            VT::unpack(ldv<In>(c.prow, k), x);
+            VT::unpack(ldv<In>(c.qrow, k), y);
+            uint32_t v0 = (uint32_t)k * E;
+#pragma unroll
+            for (int g = 0; g < E / 4; ++g) {
+                uint32_t wa = word_a(klo, (v0 >> 2) + g);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float xv = x[4 * g + e], yv = y[4 * g + e];
+                    if (yv * c.invTq - xv * c.invTp - c.dhi32 > -0.07f) continue;
+                    uint32_t v = v0 + 4 * g + e, b0 = (wa >> (8 * e)) & 0xFFu;
+                    float ub = fmaf(xv, c.invTp, gup_of(gt, c.key, v, b0));
+                    if (ub > bub) {
+                        bub = ub;
+                        bv = (int)v;
+                        bx = xv;
+                        by = yv;
+                        bb0 = b0;
+                    }
+                }
+            }
+        }
+        float wv = bub;
+        int wi = bv;
+        warp_argmax(wv, wi);
+        if (threadIdx.x == 0) sm.thr = f2ord(-INFINITY);
+        __syncthreads();
+        if (bv >= 0 && bv == wi) {
+            seedv = bv;
+            tr.add(c, bx, by, (uint32_t)bv, bb0);
+            atomicMax(&sm.thr, f2ord(tr.thr));
+        }
+        __syncthreads();
+        tr.raise(ord2f(sm.thr));
+    }
+    const float gmax = g8max(gt);
+    float pub = tr.thr;
+    for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
+        const uint4 qx = ldv<In>(c.prow, k);
+        tr.raise(ord2f(*(volatile uint32_t *)&sm.thr));
+        const uint32_t v0 = (uint32_t)k * E;
+        bool any = false;
+        uint32_t was[E / 4];
+#pragma unroll
+        for (int g = 0; g < E / 4; ++g) {
+            was[g] = word_a(klo, (v0 >> 2) + g);
+            const bool top = ((~was[g] - 0x01010101u) & was[g] & 0x80808080u) != 0u;
+            any |= top || fmaf(VT::group_max(qx, g), c.invTp, gmax) >= tr.thrS;
+        }
+        if (!any) continue;
+        float x[E], y[E];
+        VT::unpack(qx, x);
+        VT::unpack(ldv<In>(c.qrow, k), y);
+#pragma unroll
+        for (int g = 0; g < E / 4; ++g)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t v = v0 + 4 * g + e, b0 = (was[g] >> (8 * e)) & 0xFFu;
+                if ((int)v == seedv) continue;
+                if (fmaf(x[4 * g + e], c.invTp, gup_of(gt, c.key, v, b0)) < tr.thrS) continue;
+                tr.add(c, x[4 * g + e], y[4 * g + e], v, b0);
+            }
+        if (tr.thr > pub) {
+            atomicMax(&sm.thr, f2ord(tr.thr));
+            pub = tr.thr;
+        }
+    }
+}
+
+__device__ __forceinline__ double *resid_rec(const Job &j, int e, int c)
+{
+    return j.rpart + ((int64_t)e * kResidChunks + c) * 8;
+}
+
+__device__ __forceinline__ void fill_ctx(const Job &j, RCtx &ctx, const char *prow, const char *qrow,
+                                         double D, double eD)
+{
+    ctx.prow = prow;
+    ctx.qrow = qrow;
+    ctx.Tp = j.Tp;
+    ctx.Tq = (j.kind == K_PACKED) ? j.Tp : j.Tq;
+    ctx.dlo = D - eD;
+    ctx.dhi = D + eD;
+    ctx.invTp = j.invTp;
+    ctx.invTq = (float)(1.0 / ctx.Tq);
+    ctx.dlo32 = __double2float_rd(ctx.dlo);
+    ctx.dhi32 = __double2float_ru(ctx.dhi);
+}
+
+template <typename In>
+__global__ void __launch_bounds__(kPostThreads) resid_kernel(const Job j)
+{
+    __shared__ PostShared sm;
+    __shared__ float gt[kGTab];
+    for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
+        gt[i] = __ldg(j.gtab + i);
+    __syncthreads();
+    const unsigned nE = *(volatile unsigned *)(j.ctl + C_RESID_N);
+    const unsigned nA = nE * kResidChunks;
+    for (;;) {
+        if (threadIdx.x == 0) sm.item = atomicAdd(j.ctl + C_RWORK, 1u);
+        __syncthreads();
+        unsigned it = sm.item;
+        __syncthreads();
+        if (it >= 2 * nA) break;
+        bool phaseA = it < nA;
+        if (!phaseA) it -= nA;
+        const int e = it / kResidChunks, c = it - e * kResidChunks;
+        unsigned *cnt = j.rdone + (int64_t)e * 4;
+        ResidEntry re = j.resid[e];
+        if (phaseA) {
+            // Proposal row's log-sum-exp (Packed-SS: the stored Q row).
+            if (!re.need_lq) continue;
+            float M, S, mn;
+            lse_chunk32<In>(re.qrow, chunk_lo(j.nvec, c, kResidChunks),
+                            chunk_lo(j.nvec, c + 1, kResidChunks), j.cp, sm, M, S, mn);
+            if (threadIdx.x == 0) {
+                double *rec = resid_rec(j, e, c);
+                rec[4] = M;
+                rec[5] = S;
+                rec[6] = mn;
+                __threadfence();
+                if (atomicAdd(cnt + 0, 1u) + 1u == (unsigned)kResidChunks) {
+                    __threadfence();
+                    double Mx = -INFINITY, mnn = INFINITY;
+                    for (int q = 0; q < kResidChunks; ++q) {
+                        Mx = fmax(Mx, __ldcg(resid_rec(j, e, q) + 4));
+                        mnn = fmin(mnn, __ldcg(resid_rec(j, e, q) + 6));
+                    }
+                    double St = 0.0;
+                    for (int q = 0; q < kResidChunks; ++q) {
+                        double *rq = resid_rec(j, e, q);
+                        St += __ldcg(rq + 5) * exp2((__ldcg(rq + 4) - Mx) * (double)j.cp);
+                    }
+                    j.resid[e].Lq = Mx / (double)j.Tp + log(St);
+                    j.resid[e].epsq = lse_rel_bound((Mx - mnn) * (double)j.cp);
+                    cnt[0] = 0u;
+                    __threadfence();
+                    atomicExch(cnt + 2, 1u);  // ready
+                }
+            }
+            continue;
+        }
+        if (re.need_lq) {
+            if (threadIdx.x == 0) {
+                uint32_t it2 = 0;
+                while (*(volatile unsigned *)(cnt + 2) == 0u) {
+                    if (++it2 > kSpinLimit) {
+                        latch(j.err, SV_ERR_TIMEOUT);
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+                __threadfence();
+            }
+            __syncthreads();
+            re.Lq = __ldcg(&j.resid[e].Lq);
+            re.epsq = __ldcg(&j.resid[e].epsq);
+        }
+        const double D = re.Lq - re.Lp;
+        const double eD = 1.001 * (re.epsp + re.epsq) + 1e-14 * (fabs(re.Lp) + fabs(re.Lq));
+        RCtx ctx;
+        fill_ctx(j, ctx, re.prow, re.qrow, D, eD);
+        ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
+        Track32 tr;
+        resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
+                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, sm, tr);
+        Cand2 best;
+        block_cand2(tr.c, sm, best);
+        if (threadIdx.x == 0) {
+            double *rec = resid_rec(j, e, c);
+            rec[0] = best.hi1;
+            rec[1] = best.lo1;
+            rec[2] = best.hi2;
+            rec[3] = best.lo2;
+            rec[4] = best.hi3;
+            rec[5] = (double)best.v1;
+            rec[6] = (double)best.v2;
+            __threadfence();
+            if (atomicAdd(cnt + 1, 1u) + 1u == (unsigned)kResidChunks) {
+                __threadfence();
+                Cand2 all;
+                all.init();
+                for (int q = 0; q < kResidChunks; ++q) {
+                    double *rq = resid_rec(j, e, q);
+                    Cand2 t;
+                    t.hi1 = (float)__ldcg(rq + 0);
+                    t.lo1 = (float)__ldcg(rq + 1);
+                    t.hi2 = (float)__ldcg(rq + 2);
+                    t.lo2 = (float)__ldcg(rq + 3);
+                    t.hi3 = (float)__ldcg(rq + 4);
+                    t.v1 = (int)__ldcg(rq + 5);
+                    t.v2 = (int)__ldcg(rq + 6);
+                    all.merge(t);
+                }
+                cnt[1] = 0u;
+                cnt[2] = 0u;
+                // certify in fp32, else re-score the two contenders in fp64
+                int win = -1;
+                if (gumbel_certified(all)) {
+                    win = all.v1;
+                } else if (all.v1 >= 0) {
+                    double l1 = -INFINITY, h1 = -INFINITY, l2 = -INFINITY, h2 = -INFINITY;
+                    float x1 = load_logit(j, re.prow, all.v1), y1 = load_logit(j, re.qrow, all.v1);
+                    resid_interval64(ctx, x1, y1, bits52_full(ctx.key, all.v1), l1, h1);
+                    if (all.v2 >= 0) {
+                        float x2 = load_logit(j, re.prow, all.v2), y2 = load_logit(j, re.qrow, all.v2);
+                        resid_interval64(ctx, x2, y2, bits52_full(ctx.key, all.v2), l2, h2);
+                    }
+                    const double others = (double)all.hi3;
+                    if (l1 > fmax(h2, others) + kFlagEps) win = all.v1;
+                    else if (l2 > fmax(h1, others) + kFlagEps) win = all.v2;
+                }
+                if (win >= 0 && !j.force_rescue) {
+                    if (j.kind == K_SAMPLE) {
+                        j.next[re.b] = win;
+                        if (j.flags) j.flags[re.b] = 0;
+                    } else if (re.h < j.commit_len[re.b]) {
+                        j.committed[(int64_t)re.b * j.K + re.h] = win;
+                    }
+                } else {
+                    unsigned k = atomicAdd(j.ctl + C_RESCUE_N, 1u);
+                    RescueEntry x;
+                    x.b = re.b;
+                    x.kind = 1;
+                    x.h = re.h;
+                    x.resid = 1;
+                    x.Lp = 0;
+                    x.Lq = 0;
+                    x.flags = 0;
+                    x.pad[0] = x.pad[1] = x.pad[2] = 0;
+                    j.rescue[k] = x;
+                }
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(j.ctl + C_REXIT, 1u) + 1u == gridDim.x) {
+            j.ctl[C_RWORK] = 0u;
+            j.ctl[C_REXIT] = 0u;
+            j.ctl[C_RESID_N] = 0u;
+            __threadfence();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fp64 path.  A cooperative launch (every CTA resident) with bounded grid
+// barriers between its phases:
+//   1. fp64 log-sum-exp of every row pair the listed sequences need;
+//   2. exact acceptance decisions, flags, and the position h of the
+//      correction (one warp per sequence);
+//   3. the residual draw at h with exact log-sum-exps;
+//   4. outputs.
+// ---------------------------------------------------------------------------
+__device__ bool grid_sync(const Job &j)
+{
+    __syncthreads();
+    int ok = 1;
+    if (threadIdx.x == 0) {
+        volatile unsigned *gen = j.ctl + C_GGEN;
+        volatile unsigned *ab = j.ctl + C_ABORT;
+        unsigned g = *gen;
+        __threadfence();
+        if (atomicAdd(j.ctl + C_GBAR, 1u) + 1u == gridDim.x) {
+            j.ctl[C_GBAR] = 0u;
+            __threadfence();
+            atomicAdd(j.ctl + C_GGEN, 1u);
+        } else {
+            uint32_t it = 0;
+            while (*gen == g) {
+                if (*ab || ++it > kSpinLimit) {
+                    latch(j.err, SV_ERR_TIMEOUT);
+                    atomicExch(j.ctl + C_ABORT, 1u);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(256);
+            }
+        }
+        __threadfence();
+    }
+    return __syncthreads_and(ok) != 0;
+}
+
+__device__ __forceinline__ double *lse64_rec(const Job &j, int e, int i, int r, int c)
+{
+    double *base = j.rpart + (int64_t)j.B * kResidChunks * 8;
+    return base + ((((int64_t)e * kMaxPairs + i) * 2 + r) * kRescueChunks + c) * 2;
+}
+__device__ __forceinline__ double *res64_rec(const Job &j, int e, int c)
+{
+    double *base = j.rpart + (int64_t)j.B * kResidChunks * 8 +
+                   (int64_t)j.B * kMaxPairs * 2 * kRescueChunks * 2;
+    return base + ((int64_t)e * kResidChunks + c) * 4;
+}
+
+__device__ __forceinline__ const char *pair_row(const Job &j, int b, int i, int r)
+{
+    if (r == 0) return slot_row(j, b, i);
+    if (j.kind == K_SAMPLE) return slot_row(j, b, j.K + 1 + i);
+    int off = __ldg(j.prev_off + b);
+    return j.src2 + ((int64_t)b * j.W + off + i) * j.rs;
+}
+
+// exact log-sum-exp of x / T over vectors [vb, ve): (max, sum exp((x - max)/T))
+template <typename In>
+__device__ void lse_chunk64(const char *row, int vb, int ve, double T, PostShared &sm, double &M,
+                            double &S)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    float mx = -INFINITY;
+    for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
+        float f[E];
+        VT::unpack(ldv<In>(row, k), f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) mx = fmaxf(mx, f[e]);
+    }
+    float m = block_max(mx, sm);
+    double md = (double)m / T, s = 0.0;
+    for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
+        float f[E];
+        VT::unpack(ldv<In>(row, k), f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) s += exp((double)f[e] / T - md);
+    }
+    M = md;
+    S = block_sumd(s, sm);
+}
+
+__device__ double merge64(const Job &j, int e, int i, int r)
+{
+    double M = -INFINITY;
+    for (int c = 0; c < kRescueChunks; ++c) M = fmax(M, __ldcg(lse64_rec(j, e, i, r, c)));
+    double S = 0.0;
+    for (int c = 0; c < kRescueChunks; ++c) {
+        double *q = lse64_rec(j, e, i, r, c);
+        S += __ldcg(q + 1) * exp(__ldcg(q) - M);
+    }
+    return M + log(S);
+}
+
+template <typename In>
+__global__ void __launch_bounds__(kPostThreads) rescue_kernel(const Job j)
+{
+    __shared__ PostShared sm;
+    __shared__ float gt[kGTab];
+    const unsigned nR = *(volatile unsigned *)(j.ctl + C_RESCUE_N);
+    if (nR == 0u) return;
+    for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
+        gt[i] = __ldg(j.gtab + i);
+    __syncthreads();
+    const double Tq = (j.kind == K_PACKED) ? (double)j.Tp : (double)j.Tq;
+
+    // ---- phase 1: fp64 log-sum-exps ----
+    const unsigned items1 = nR * kMaxPairs * 2 * kRescueChunks;
+    for (unsigned it = blockIdx.x; it < items1; it += gridDim.x) {
+        int c = it % kRescueChunks;
+        int r = (it / kRescueChunks) % 2;
+        int i = (it / (kRescueChunks * 2)) % kMaxPairs;
+        int e = it / (kRescueChunks * 2 * kMaxPairs);
+        RescueEntry re = j.rescue[e];
+        int lo = (re.kind == 0) ? 0 : re.h;
+        int hi = (re.kind == 0) ? clamp_len(j, re.b) : re.h + 1;
+        if (i < lo || i >= hi) continue;
+        double M, S;
+        lse_chunk64<In>(pair_row(j, re.b, i, r), chunk_lo(j.nvec, c, kRescueChunks),
+                        chunk_lo(j.nvec, c + 1, kRescueChunks), r == 0 ? (double)j.Tp : Tq, sm,
+                        M, S);
+        if (threadIdx.x == 0) {
+            double *q = lse64_rec(j, e, i, r, c);
+            q[0] = M;
+            q[1] = S;
+        }
+    }
+    if (!grid_sync(j)) return;
+
+    // ---- phase 2: exact decisions (one warp per sequence) ----
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kPostWarps + (threadIdx.x >> 5);
+    const int nw = gridDim.x * kPostWarps;
+    for (unsigned e = gw; e < nR; e += nw) {
+        RescueEntry re = j.rescue[e];
+        const int b = re.b;
+        const int n = clamp_len(j, b);
+        if (re.kind == 1) {
+            if (lane == 0) {
+                j.rescue[e].Lp = merge64(j, e, re.h, 0);
+                j.rescue[e].Lq = merge64(j, e, re.h, 1);
+                j.rescue[e].resid = 1;
+                j.rescue[e].flags = 0;
+            }
+            continue;
+        }
+        const int64_t p0 = pos0_of(j, b);
+        const int Ks = (j.kind == K_PACKED) ? j.K - 1 : j.K;
+        bool acc = false, fl = false;
+        double Lp = 0, Lq = 0;
+        if (lane < n) {
+            Lp = merge64(j, e, lane, 0);
+            Lq = merge64(j, e, lane, 1);
+            int d = __ldg(j.ids + (int64_t)b * Ks + lane);
+            double lp = -INFINITY, lq;
+            if (d >= 0 && d < j.V)
+                lp = (double)load_logit(j, slot_row(j, b, lane), d) / (double)j.Tp - Lp;
+            if (j.kind == K_PACKED) {
+                lq = log((double)__ldg(j.prev_q + (int64_t)b * Ks + lane));
+            } else {
+                lq = (d >= 0 && d < j.V)
+                         ? (double)load_logit(j, slot_row(j, b, j.K + 1 + lane), d) / Tq - Lq
+                         : 0.0;
+            }
+            double alpha = alpha_of(j.kind == K_PACKED ? SV_LOSSLESS : j.amode, exp(lp - lq),
+                                    j.lam);
+            double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0);
+            acc = u < alpha;
+            fl = fabs(u - alpha) < kFlagEps;
+        }
+        unsigned am = __ballot_sync(0xFFFFFFFFu, acc);
+        int h = (~am == 0u) ? 32 : __ffs(~am) - 1;
+        h = min(h, n);
+        unsigned reached = (h >= 31) ? 0xFFFFFFFFu : ((2u << h) - 1u);
+        int nfl = __popc(__ballot_sync(0xFFFFFFFFu, fl) & reached);
+        double Lph = __shfl_sync(0xFFFFFFFFu, Lp, h & 31);
+        double Lqh = __shfl_sync(0xFFFFFFFFu, Lq, h & 31);
+        if (h < n) {
+            if (lane == 0) {
+                j.rescue[e].h = h;
+                j.rescue[e].resid = 1;
+                j.rescue[e].Lp = Lph;
+                j.rescue[e].Lq = Lqh;
+                j.rescue[e].flags = nfl;
+                if (j.kind == K_SAMPLE) j.acc[b] = h;
+            }
+            continue;
+        }
+        // every draft accepted: the bonus token is the fast path's exact
+        // Gumbel-max of row n
+        if (j.kind == K_SAMPLE) {
+            if (lane == 0) {
+                RowStat sb = j.rs_stat[(int64_t)b * j.rows_per_seq + n];
+                j.acc[b] = n;
+                j.next[b] = sb.gidx;
+                if (j.flags) j.flags[b] = nfl + sb.gflag;
+                j.rescue[e].resid = 0;
+            }
+        } else {
+            RowM rb = merge_row(j, b, n, j.cp, 0.f);
+            GRes g = resolve_lanes(j, slot_row(j, b, n),
+                                   rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0), (double)j.Tp,
+                                   j.invTp, rb.gc, lane == 0);
+            if (lane == 0) j.rescue[e].resid = 0;
+            int c = __shfl_sync(0xFFFFFFFFu, g.v, 0);
+            int gf = __shfl_sync(0xFFFFFFFFu, g.flag, 0);
+            packed_commit(j, b, n, c, true, nfl + gf);
+        }
+    }
+    if (!grid_sync(j)) return;
+
+    // ---- phase 3: residual draws with exact log-sum-exps ----
+    const unsigned items3 = nR * kResidChunks;
+    for (unsigned it = blockIdx.x; it < items3; it += gridDim.x) {
+        int e = it / kResidChunks, c = it % kResidChunks;
+        RescueEntry re = j.rescue[e];
+        if (!re.resid) continue;
+        double D = re.Lq - re.Lp;
+        double eD = 1e-10 * (1.0 + fabs(re.Lp) + fabs(re.Lq));
+        RCtx ctx;
+        fill_ctx(j, ctx, pair_row(j, re.b, re.h, 0), pair_row(j, re.b, re.h, 1), D, eD);
+        ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
+        Track64 tr;
+        resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
+                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, sm, tr);
+        RBest best;
+        block_rbest(tr.r, sm, best);
+        if (threadIdx.x == 0) {
+            double *q = res64_rec(j, e, c);
+            q[0] = best.lo;
+            q[1] = best.hi;
+            q[2] = best.hio;
+            q[3] = (double)best.i;
+        }
+    }
+    if (!grid_sync(j)) return;
+
+    // ---- phase 4: outputs ----
+    for (unsigned e = gw; e < nR; e += nw) {
+        RescueEntry re = j.rescue[e];
+        if (!re.resid) continue;
+        int c = -1, fl = 0;
+        if (lane == 0) {
+            RBest all;
+            all.init();
+            for (int q = 0; q < kResidChunks; ++q) {
+                double *r = res64_rec(j, e, q);
+                RBest t;
+                t.lo = __ldcg(r + 0);
+                t.hi = __ldcg(r + 1);
+                t.hio = __ldcg(r + 2);
+                t.i = (int)__ldcg(r + 3);
+                all.merge(t);
+            }
+            c = all.i;
+            fl = (all.lo - all.hio < kFlagEps) ? 1 : 0;
+            if (c < 0) latch(j.err, SV_ERR_TIMEOUT);
+        }
+        c = __shfl_sync(0xFFFFFFFFu, c, 0);
+        fl = __shfl_sync(0xFFFFFFFFu, fl, 0);
+        if (j.kind == K_SAMPLE) {
+            if (lane == 0) {
+                j.acc[re.b] = re.h;
+                j.next[re.b] = c;
+                if (j.flags) j.flags[re.b] = re.flags + fl;
+            }
+        } else {
+            packed_commit(j, re.b, re.h, c, true, re.flags + fl);
+        }
+    }
+    if (!grid_sync(j)) return;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        j.ctl[C_RESCUED] += nR;
+        j.ctl[C_RESCUE_N] = 0u;
+        __threadfence();
+    }
+}
+
+// Host-side launchers.
+cudaError_t post_setup(int *blocks_per_sm)
+{
+    int a = 0, b = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rescue_kernel<uint16_t>,
+                                                                  kPostThreads, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rescue_kernel<float>, kPostThreads, 0);
+    *blocks_per_sm = a < b ? a : b;
+    return e;
+}
+
+cudaError_t post_launch(const Job &j, int grid, int coop_grid, bool tv, cudaStream_t s)
+{
+    const bool bf = j.dtype == SV_BF16;
+    if (tv) {
+        if (bf) tv_kernel<uint16_t><<<grid, kPostThreads, 0, s>>>(j);
+        else tv_kernel<float><<<grid, kPostThreads, 0, s>>>(j);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (bf) resid_kernel<uint16_t><<<grid, kPostThreads, 0, s>>>(j);
+    else resid_kernel<float><<<grid, kPostThreads, 0, s>>>(j);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // The fp64 path's grid barriers need every CTA resident: a cooperative
+    // launch guarantees it (or fails).  It returns at once when no sequence
+    // was listed.
+    Job jj = j;
+    void *args[] = {(void *)&jj};
+    return cudaLaunchCooperativeKernel(bf ? (const void *)rescue_kernel<uint16_t>
+                                          : (const void *)rescue_kernel<float>,
+                                       dim3(coop_grid), dim3(kPostThreads), args, 0, s);
+}
+
+size_t rescue_scratch_doubles(int B)
+{
+    return (size_t)B * kResidChunks * 8 + (size_t)B * kMaxPairs * 2 * kRescueChunks * 2 +
+           (size_t)B * kResidChunks * 4;
+}
+
+}  // namespace sv

@@ -1,0 +1,59 @@
+// sv_selftest.cu -- measures, on the device, the fp32 arithmetic that the
+// kernels' certified decisions rely on, against fp64:
+//   [0] max |G32 - G64| / kG32Err                 (Gumbel of sv_gumbel.cuh)
+//   [1] max |ex2(x) / 2^x - 1| / 2^-21            (x in [-126, 64])
+//   [2] max |lg2(x) - log2(x)| / (2^-22 max(1, |log2 x|))   (x in [2^-60, 2^8])
+// Uniforms are drawn from regions where the formulas are hardest: u
+// uniform, u within 2^-28 of 1, u below 2^-29, and u around 3/4.
+#include "sv_gumbel.cuh"
+
+namespace sv {
+
+__global__ void selftest_kernel(uint64_t seed, long long n, unsigned *out)
+{
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        uint64_t h = splitmix_out(seed ^ (uint64_t)i);
+        uint64_t m;
+        switch (i & 3) {
+        case 0: m = h >> 12; break;
+        case 1: m = ((1ull << 52) - 1) - (h >> 40); break;
+        case 2: m = h >> 40; break;
+        default: m = (3ull << 50) - (1ull << 23) + (h >> 40); break;
+        }
+        double g64 = gumbel_of(u_of(m));
+        float g32 = gumbel32(m);
+        r0 = fmaxf(r0, (float)(fabs((double)g32 - g64) / (double)kG32Err));
+        float x = -126.f + 190.f * (float)((h >> 11) & 0xFFFFF) * 0x1p-20f;
+        double e64 = exp2((double)x);
+        r1 = fmaxf(r1, (float)(fabs((double)ex2f(x) / e64 - 1.0) / 0x1p-21));
+        float y = exp2f(-60.f + 68.f * (float)(h & 0xFFFFF) * 0x1p-20f);
+        double l = log2((double)y);
+        r2 = fmaxf(r2, (float)(fabs((double)lg2a(y) - l) / (0x1p-22 * fmax(1.0, fabs(l)))));
+    }
+    atomicMax(out + 0, __float_as_uint(r0));
+    atomicMax(out + 1, __float_as_uint(r1));
+    atomicMax(out + 2, __float_as_uint(r2));
+}
+
+cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s)
+{
+    unsigned *d = nullptr;
+    cudaError_t e = cudaMallocAsync((void **)&d, 3 * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    cudaMemsetAsync(d, 0, 3 * sizeof(unsigned), s);
+    selftest_kernel<<<256, 256, 0, s>>>(seed, n, d);
+    unsigned h[3] = {0, 0, 0};
+    e = cudaMemcpyAsync(h, d, sizeof h, cudaMemcpyDeviceToHost, s);
+    cudaFreeAsync(d, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    for (int i = 0; i < 3; ++i) {
+        float f;
+        memcpy(&f, &h[i], sizeof f);
+        res[i] = f;
+    }
+    return e;
+}
+
+}  // namespace sv
