@@ -183,6 +183,21 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.part_vecs = (j.nvec + parts - 1) / parts;
     j.parts = (j.nvec + j.part_vecs - 1) / j.part_vecs;  // no empty part
     j.total_units = rows * j.parts;
+    // longest fp32 summation path: the chunk tree, one addition per stage of a
+    // unit, the warp sum and the sum over consumer warps (records are merged
+    // in fp64)
+    const int stages_per_unit = (j.part_vecs + kStageVecs - 1) / kStageVecs;
+    // plus the absolute error of log2 S in the row merge (below 2^-22)
+    j.eps_lse = lse_rel_bound_stream((double)j.V, 24.0 + stages_per_unit) + 0x1p-22;
+    // exact ratios (log2(e)/T) / fl32(log2(e)/T) and reciprocals, once per call
+    auto ratio = [](float c, float T) {
+        return (c > 0.f && T > 0.f) ? (1.4426950408889634 / (double)T) / (double)c : 1.0;
+    };
+    j.crp = ratio(j.cp, j.Tp);
+    j.crq = ratio(j.cq, j.Tq);
+    j.cr1 = ratio(j.c1, 1.f);
+    j.rTp = j.Tp > 0.f ? 1.0 / (double)j.Tp : 0.0;
+    j.rTq = j.Tq > 0.f ? 1.0 / (double)j.Tq : 0.0;
     j.tv_chunks = tv_chunks;
     j.resid_chunks = kResidChunksHost;
     Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks);

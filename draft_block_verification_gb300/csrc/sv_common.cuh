@@ -20,13 +20,15 @@ __device__ __forceinline__ int clamp_len(const Job &j, int b)
 // Row merging for the decision step.
 // ---------------------------------------------------------------------------
 struct RowM {
-    float m, mn;
+    float m;            // row max (modes that track it)
     int amax;
-    double L2b1, L2b2;  // base-2 log-sum-exp of x c1 and x c2: log2 sum_v 2^(x_v c)
+    double L2c1, L2c2;  // log2 sum_v 2^(x_v c) with the fp32 factors c1, c2
+    double L1a, L1b;    // natural log-sum-exps of x / T for the same two sums
     Cand2 gc;           // Gumbel candidates of the row
 };
 
 constexpr double kLn2 = 0.6931471805599453;
+constexpr double kLog2e = 1.4426950408889634;
 
 __device__ __forceinline__ RowPart load_part(const RowPart *p)
 {
@@ -39,24 +41,51 @@ __device__ __forceinline__ RowPart load_part(const RowPart *p)
     return r;
 }
 
-// Merge the unit records of one row.  Each record holds its unit max m_u and
-// s_u = sum 2^(x c - fl32(m_u c)); the row's base-2 log-sum-exp is
-// fl32(M c) + log2 sum_u s_u 2^(fl32(m_u c) - fl32(M c)), in fp64.
-static __device__ RowM merge_row(const Job &j, int b, int slot, float c1, float c2)
+// log2 S for S >= 0 with absolute error below 2^-22: S = m 2^k exactly with
+// m in [1/2, 1), and log2 m in fp32 (|log2 m| <= 1; log2f is within 1 ulp,
+// the rounding of m adds under 2^-23.5).  The fp64 library log2 would cost
+// hundreds of cycles per call on a part with a slow fp64 pipe.
+__device__ __forceinline__ double log2_fast(double S)
 {
-    const RowPart *p = j.rp + ((int64_t)b * j.rows_per_seq + slot) * j.parts;
+    int k;
+    const double m = frexp(S, &k);
+    return (double)k + (double)log2f((float)m);
+}
+
+// e^d in fp32 with relative error below 2^-21 for |d| < 87: d = h + l with
+// h = fl32(d), e^d = expf(h) (within 2 ulp) times 1 + l (|l| < 2^-24 |d|,
+// e^l - 1 - l below l^2).  Overflows to inf above, flushes to 0 below.
+__device__ __forceinline__ float exp_fast(double d)
+{
+    const float h = (float)d;
+    const float l = (float)(d - (double)h);
+    return expf(h) * (1.f + l);
+}
+
+// Merge the unit records of one row.  Record u holds s_u = sum 2^fl(x c - e_u)
+// with an integer e_u; with E = max_u e_u the row sum is
+// S = sum_u s_u 2^(e_u - E) (exact scalings), log2 sum 2^(x c) = E + log2 S,
+// and the natural log-sum-exp of x/T is ln2 (E c*/c + log2 S) (the exponent
+// shift x (c - c*) that is common to all terms taken out).  r1, r2 are the
+// ratios c*/c of the two sums (computed on the host in fp64); log2 S carries
+// the absolute error of log2_fast.
+static __device__ RowM merge_row(const Job &j, int b, int slot, double r1, double r2)
+{
+    const int nrec = j.parts;
+    const RowPart *p = j.rp + ((int64_t)b * j.rows_per_seq + slot) * nrec;
     RowM r;
     r.m = -INFINITY;
-    r.mn = INFINITY;
     r.amax = 0x7FFFFFFF;
     r.gc.init();
-    for (int q = 0; q < j.parts; ++q) {
+    float E1 = -INFINITY, E2 = -INFINITY;
+    for (int q = 0; q < nrec; ++q) {
         RowPart x = load_part(p + q);
         if (x.m > r.m || (x.m == r.m && x.amax < r.amax)) {
             r.m = x.m;
             r.amax = x.amax;
         }
-        r.mn = fminf(r.mn, x.mn);
+        E1 = fmaxf(E1, x.e1);
+        E2 = fmaxf(E2, x.e2);
         Cand2 c;
         c.hi1 = x.ghi1;
         c.lo1 = x.glo1;
@@ -67,26 +96,20 @@ static __device__ RowM merge_row(const Job &j, int b, int slot, float c1, float 
         c.v2 = x.gv2;
         r.gc.merge(c);
     }
-    const double M1 = (double)__fmul_rn(r.m, c1), M2 = (double)__fmul_rn(r.m, c2);
     double S1 = 0.0, S2 = 0.0;
-    for (int q = 0; q < j.parts; ++q) {
+    for (int q = 0; q < nrec; ++q) {
         RowPart x = load_part(p + q);
         if (x.s1 > 0.f)
-            S1 += (double)x.s1 * exp2((double)__fmul_rn(x.m, c1) - M1);
+            S1 += ldexp((double)x.s1, (int)(x.e1 - E1));
         if (x.s2 > 0.f)
-            S2 += (double)x.s2 * exp2((double)__fmul_rn(x.m, c2) - M2);
+            S2 += ldexp((double)x.s2, (int)(x.e2 - E2));
     }
-    r.L2b1 = M1 + log2(S1);
-    r.L2b2 = M2 + log2(S2);
+    const double l1 = log2_fast(S1), l2 = log2_fast(S2);
+    r.L2c1 = (double)E1 + l1;
+    r.L2c2 = (double)E2 + l2;
+    r.L1a = kLn2 * ((double)E1 * r1 + l1);
+    r.L1b = kLn2 * ((double)E2 * r2 + l2);
     return r;
-}
-
-// Relative error bound of exp(L) for a row merged with temperature factor c.
-__device__ __forceinline__ double row_eps(const RowM &r, float c)
-{
-    double range = ((double)r.m - (double)r.mn) * (double)c;
-    double amax = fmax(fabs((double)r.m), fabs((double)r.mn)) * (double)c;
-    return lse_rel_bound_fma(2.0 * range, amax);
 }
 
 __device__ __forceinline__ const char *row_ptr(const Job &j, int b, int slot)
@@ -134,7 +157,7 @@ __device__ __forceinline__ bool gumbel_certified(const Cand2 &c)
 // other element's upper end still reaches within 1e-9 of the best (rare) the
 // whole row is rescanned with fp64 scores for everything its table bound
 // admits.
-static __device__ GRes resolve_logit_row(const Job &j, const char *row, uint64_t key, double T,
+static __device__ __noinline__ GRes resolve_logit_row(const Job &j, const char *row, uint64_t key, double T,
                                          float invT, const Cand2 &c)
 {
     if (gumbel_certified(c))
@@ -163,7 +186,7 @@ static __device__ GRes resolve_logit_row(const Job &j, const char *row, uint64_t
 // Warp-level: each lane holds the candidates of one logit row (need = false
 // when it holds none); rows that are not certified are resolved one at a time
 // by the whole warp.  Returns the lane's winner and near-tie flag.
-static __device__ GRes resolve_lanes(const Job &j, const char *row, uint64_t key, double T,
+static __device__ __noinline__ GRes resolve_lanes(const Job &j, const char *row, uint64_t key, double T,
                                      float invT, const Cand2 &c, bool need)
 {
     const int lane = threadIdx.x & 31;

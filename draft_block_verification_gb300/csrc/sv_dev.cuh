@@ -37,7 +37,7 @@ namespace sv {
 #endif
 constexpr int kConsumerWarps = SV_CONSUMER_WARPS;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kPassThreads = kConsumers + 32;     // + one producer warp
+constexpr int kPassThreads = kConsumers + 64;     // + a producer and a finalizer warp
 constexpr int kStageBytes = SV_STAGE_BYTES;       // one bulk copy
 constexpr int kStageVecs = kStageBytes / 16;      // 16-byte vectors per stage
 constexpr int kVecsPerThread = kStageVecs / kConsumers;
@@ -50,8 +50,8 @@ constexpr double kFlagEps = 1e-9;                 // near-threshold window
 // Random-number streams.
 enum : uint32_t { kAccept = 1, kSample = 2, kDraft = 3, kTree = 4 };
 
-// Row work modes (bit set).
-enum : int { M_ARGMAX = 1, M_LSE = 2, M_LSE2 = 4, M_GUMBEL = 8 };
+// Row work modes (bit set).  M_MAX keeps the row max without its index.
+enum : int { M_ARGMAX = 1, M_LSE = 2, M_LSE2 = 4, M_GUMBEL = 8, M_MAX = 16 };
 
 // Entry-point kinds.
 enum : int { K_GREEDY = 0, K_SAMPLE = 1, K_TREE = 2, K_PACKED = 3 };
@@ -196,6 +196,32 @@ __device__ __forceinline__ float ex2f(float x)
     return y;
 }
 
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction per pair).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+        " mov.b64 c, {%6, %7};\n fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+        " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// 2^d for an integer-valued d <= 0, exactly (0 below the normal range).
+__device__ __forceinline__ float pow2_int(float d)
+{
+    return d < -126.f ? 0.f : __int_as_float((127 + (int)d) << 23);
+}
+
 // ---------------------------------------------------------------------------
 // Ordered encoding of floats for unsigned atomicMax.
 // ---------------------------------------------------------------------------
@@ -211,23 +237,25 @@ __device__ __forceinline__ float ord2f(uint32_t o)
 
 // ---------------------------------------------------------------------------
 // Partial statistics of one unit (a contiguous part of one logit row).
+// Log-sum-exps are kept as s = sum 2^fl(x c - e) with an integer-valued
+// reference exponent e, so that moving a sum to another reference is an exact
+// power-of-two scaling.
 // ---------------------------------------------------------------------------
 struct __align__(16) RowPart {
-    float m;      // max logit of the part (raw value)
-    float mn;     // min logit of the part
-    float s1;     // sum 2^(x c1 - fl(m c1))
-    float s2;     // sum 2^(x c2 - fl(m c2))
-    int amax;     // lowest id attaining m
+    float m;        // max logit of the part (modes that track it; else -inf)
+    float e1, e2;   // reference exponents of s1, s2 (-inf: empty sum)
+    float s1, s2;   // sum 2^fl(x c1 - e1), sum 2^fl(x c2 - e2)
+    int amax;       // lowest id attaining m (argmax mode)
     // Gumbel candidates (see Cand2 in sv_gumbel.cuh)
     float ghi1, glo1, ghi2, glo2, ghi3;
     int gv1, gv2;
-    int pad[4];
+    int pad[3];
 };
 
 // Merged per-row statistics kept for the later kernels.
 struct __align__(16) RowStat {
     double L1;    // natural log-sum-exp of x / T (the row's temperature)
-    double L2;    // base-2 log-sum-exp of x c, c = fl32(log2(e) / T)
+    double L2;    // log2 sum 2^(x c) with the fp32 factor c = fl32(log2(e) / T)
     float m;      // row max
     float eps;    // bound on the relative error of exp(L1) (fp32 path)
     int gidx;     // Gumbel-max winner
@@ -317,6 +345,16 @@ struct VecTraits;
 template <>
 struct VecTraits<uint16_t> {  // bf16 bit patterns
     static constexpr int N = 8;
+    static constexpr int P = 4;  // element pairs per vector (one 32-bit word each)
+    __device__ __forceinline__ static float2 pair(const uint4 &q, int i)
+    {
+        const uint32_t w = i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ static uint4 neg_inf_vec()
+    {
+        return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
     __device__ __forceinline__ static void unpack(const uint4 &q, float (&f)[8])
     {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -360,6 +398,17 @@ struct VecTraits<uint16_t> {  // bf16 bit patterns
         uint32_t w = (i < 2) ? q.x : (i < 4) ? q.y : (i < 6) ? q.z : q.w;
         return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
     }
+    // the raw data of group g (elements 4g .. 4g+3) in the first half of a vector
+    __device__ __forceinline__ static uint4 group_data(const uint4 &q, int g)
+    {
+        return g == 0 ? make_uint4(q.x, q.y, 0u, 0u) : make_uint4(q.z, q.w, 0u, 0u);
+    }
+    // element e (run-time index) of group data
+    __device__ __forceinline__ static float gelem(const uint4 &d, int e)
+    {
+        const uint32_t w = (e < 2) ? d.x : d.y;
+        return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
     // largest of the 4 elements of group g (elements 4g .. 4g+3)
     __device__ __forceinline__ static float group_max(const uint4 &q, int g)
     {
@@ -378,6 +427,16 @@ struct VecTraits<uint16_t> {  // bf16 bit patterns
 template <>
 struct VecTraits<float> {
     static constexpr int N = 4;
+    static constexpr int P = 2;
+    __device__ __forceinline__ static float2 pair(const uint4 &q, int i)
+    {
+        return i == 0 ? make_float2(__uint_as_float(q.x), __uint_as_float(q.y))
+                      : make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
+    }
+    __device__ __forceinline__ static uint4 neg_inf_vec()
+    {
+        return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    }
     __device__ __forceinline__ static void unpack(const uint4 &q, float (&f)[4])
     {
         f[0] = __uint_as_float(q.x);
@@ -416,21 +475,35 @@ struct VecTraits<float> {
     {
         return __uint_as_float((i == 0) ? q.x : (i == 1) ? q.y : (i == 2) ? q.z : q.w);
     }
+    __device__ __forceinline__ static uint4 group_data(const uint4 &q, int) { return q; }
+    __device__ __forceinline__ static float gelem(const uint4 &d, int e) { return elem(d, e); }
     __device__ __forceinline__ static float hi_of(uint32_t p) { return __uint_as_float(p); }
     __device__ __forceinline__ static float lo_of(uint32_t p) { return __uint_as_float(p); }
 };
 
 // Relative error bounds of exp(L) for a row log-sum-exp L computed in fp32.
 //
-// Streaming kernel (terms 2^fl(x c - fl(m_ref c)), one FFMA each): ex2 per term
-// and the per-thread rescale (2 x 2^-21, plus one for slack); rounding of each
-// term's exponent |t| <= R = (max - min) c (ln 2 * 2^-24 * R); rounding of
-// c = log2(e)/T itself, which shifts every exponent by at most
-// 2^-24 * c * max|x| (ln 2 * 2^-24 * c * max|x|); and a summation depth of at
-// most 64 fp32 additions.
-__host__ __device__ __forceinline__ double lse_rel_bound_fma(double range_c, double absmax_c)
+// Streaming kernel.  Terms are t = 2^fl(x c - e), one FFMA and one ex2 each,
+// with an integer reference e; a chunk whose partial sum reaches 2^20 moves
+// the reference up, so every exponent a = x c - e stays below kLseCap + 1.
+// Moves between references are exact powers of two.  With c = fl32(c*),
+// c* = log2(e)/T, the row's value is reported as E c*/c + log2 S (E the
+// reference of S), which leaves per term an exponent error of at most
+// 2^-24 |a| from the FFMA and 2^-24 |a| from c.  The row max has a >= -1, so
+// S >= 1/2, and with n terms:
+//   terms with a >= -24:       2^-21 (ex2) + 2 ln2 2^-24 max(kLseCap + 1, 24)
+//   terms with -48 <= a < -24: total weight <= n 2^-24, each off by at most
+//                              2^-21 + 2 ln2 2^-24 48
+//   terms with a < -48:        total weight <= n 2^-48
+// plus 2^-24 per fp32 addition on the longest summation path (depth), and
+// one 2^-21 of slack.
+constexpr float kLseCap = 20.f;
+__host__ __device__ __forceinline__ double lse_rel_bound_stream(double n, double depth)
 {
-    return 3.0 * 0x1p-21 + 0.6931471805599453 * 0x1p-24 * (range_c + absmax_c) + 64.0 * 0x1p-24;
+    const double u = 0x1p-24, ln2 = 0.6931471805599453;
+    const double near = 0x1p-21 + 2.0 * ln2 * u * 24.0;  // kLseCap + 1 <= 24
+    const double mid = 0x1p-21 + 2.0 * ln2 * u * 48.0;
+    return 2.0 * 0x1p-21 + near + 2.0 * n * u * mid + 2.0 * n * 0x1p-48 + 1.01 * depth * u;
 }
 // Row passes that subtract first (terms 2^((x - m_ref) c)): exponent rounding
 // of 3 ulps of |t| <= R.

@@ -68,6 +68,9 @@ struct Job {
     float Tp, Tq;       // temperatures (tree / packed: Tp = T)
     float cp, cq, c1;   // log2(e)/Tp, log2(e)/Tq, log2(e)
     float invTp;        // 1/Tp rounded to fp32 (Gumbel filter)
+    double eps_lse;     // relative error bound of exp(L) for streamed log-sum-exps
+    double crp, crq, cr1;  // (log2(e)/T) / c for cp, cq, c1 (exact ratios, fp64)
+    double rTp, rTq;    // 1/Tp, 1/Tq in fp64
     int amode;          // acceptance rule
     float lam;
     uint64_t seed, iter;

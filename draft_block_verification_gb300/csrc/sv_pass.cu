@@ -2,40 +2,31 @@
 //
 // One persistent CTA per SM streams logit rows from HBM exactly once.  A
 // producer warp takes work units (a contiguous part of one row) from a global
-// counter and moves them into an 8-stage shared-memory ring with bulk copies
-// (cp.async.bulk, completion on an mbarrier); eight consumer warps compute
-// the row statistics the verify rules need:
+// counter and moves them into a shared-memory ring with bulk copies
+// (cp.async.bulk, completion on an mbarrier); the consumer warps compute the
+// row statistics the verify rules need:
 //   - max / lowest-index argmax                 (greedy rules, [PackedSS] eq. 1)
-//   - sum 2^((x - m) c) for log-sum-exp at T    (p, q of [PackedSS] §2.2, [SPOT] eq. 2)
+//   - sum 2^(x c - e) for log-sum-exp at T      (p, q of [PackedSS] §2.2, [SPOT] eq. 2)
 //   - Gumbel-max with exact fp64 candidates     ([SPOT] eq. 4, eqs. 5-7)
-// The CTA that completes the last unit of a sequence runs that sequence's
-// decision step (prefix scan, stopping index, tree path) in one warp.
+// The producer prepares each unit's row mode one unit ahead, so the consumer
+// warps read everything they need from shared memory.  Consumer warps never
+// wait for one another or for global memory: at the end of a unit each drops
+// its warp-reduced partial into a shared-memory unit slot, and the Gumbel
+// threshold of a unit is shared through another slot.  A finalizer warp
+// merges the partials into the unit's record, counts records per sequence,
+// and runs a sequence's decision step (prefix scan, stopping index, tree
+// path) once its last record is in, so the ring never waits for any of it.
+// Each entry-point kind has its own kernel instance holding only the row
+// modes that kind uses.
 #include <math.h>
 
 #include "sv_common.cuh"
 
 namespace sv {
 
-struct StageMeta {
-    int unit;   // -1: end of work
-    int nv;     // 16-byte vectors in this stage
-    int vbase;  // row vector index of the stage's first vector
-    int first;  // first stage of its unit
-    int last;   // last stage of its unit
-    int pad[3];
-};
-
-struct PassShared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    StageMeta meta[kStages];
-    uint32_t thr[2];
-    float rf[kConsumerWarps][4];
-    int ri[kConsumerWarps][2];
-    float rg[kConsumerWarps][5];
-    int rgi[kConsumerWarps][2];
-    volatile int abort;
-};
+constexpr int kFinQ = 32;      // decision steps queued per CTA
+constexpr int kUnitSlots = 8;  // units whose partials wait for the finalizer
+constexpr int kGQ = 64;        // queued Gumbel groups per consumer warp
 
 struct RowMode {
     int mode;
@@ -44,20 +35,156 @@ struct RowMode {
     uint64_t key;
 };
 
-__device__ RowMode row_mode(const Job &j, int b, int slot)
+struct StageMeta {
+    int unit;         // -1: end of work
+    int nv;           // 16-byte vectors in this stage
+    int vbase;        // row vector index of the stage's first vector
+    int first, last;  // first / last stage of its unit
+    int lu;           // this CTA's running unit number
+    int b;            // sequence of the unit
+    unsigned expect;  // records that complete sequence b
+    RowMode rm;       // row mode of the unit
+};
+
+// One consumer warp's share of a unit.
+struct WarpPart {
+    float m;
+    int amax;
+    float e1, s1, e2, s2;
+    float hi1, lo1, hi2, lo2, hi3;
+    int v1, v2;
+    int pad[3];
+};
+
+struct PassShared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    StageMeta meta[kStages];
+    // Gumbel threshold of local unit lu, in slot lu % kStages: the ring holds
+    // stages of at most kStages - 1 other units when a unit starts, so no warp
+    // still uses the slot that unit takes over.
+    uint32_t thr[kStages];
+    volatile int abort;
+    // Gumbel groups that passed level 1, per consumer warp: raw data and
+    // (first id, hash word)
+    uint4 gqd[kConsumerWarps][kGQ];
+    uint2 gqm[kConsumerWarps][kGQ];
+    // unit slots: consumer warps write their partials and arrive on ubar; the
+    // finalizer merges them and arrives on ufree
+    uint64_t ubar[kUnitSlots];
+    uint64_t ufree[kUnitSlots];
+    WarpPart up[kUnitSlots][kConsumerWarps];
+    int uunit[kUnitSlots], ub[kUnitSlots];
+    unsigned uexpect[kUnitSlots];
+    volatile int nunits;     // units this CTA streamed (set when the producer is done)
+    volatile int prod_done;
+    int todo[kFinQ];         // sequences whose decision step is due (finalizer only)
+};
+
+// Per-sequence values a unit's bookkeeping needs, loaded one unit ahead.
+struct UnitPre {
+    int len;     // draft length as given (unclamped)
+    int64_t p0;  // absolute position of the sequence's first row
+    int np;      // tree: position of the node (T > 0)
+};
+
+// Unit order.  Rows that carry a Gumbel-max (a few times the work of a plain
+// row) are streamed first, H per sequence, so that the last units of the pass
+// are light ones and CTAs finish together; the other rows follow sequence by
+// sequence.  A unit is one part of one row.
+__device__ __forceinline__ int heavy_rows(const Job &j)
+{
+    if (j.kind == K_SAMPLE)
+        return 1;  // the bonus row
+    if (j.kind == K_PACKED && j.Tp != 0.f)
+        return 1 + j.W;  // the bonus row and the proposal rows
+    return 0;
+}
+
+// Sequence of unit u (needs no per-sequence data).
+__device__ __forceinline__ int unit_seq(const Job &j, long long u)
+{
+    const int H = heavy_rows(j);
+    const long long nh = (long long)j.B * H * j.parts;
+    if (u < nh)
+        return (int)(u / ((long long)H * j.parts));
+    return (int)((u - nh) / ((long long)(j.rows_per_seq - H) * j.parts));
+}
+
+// Row slot and part of unit u of sequence b with clamped length n.
+__device__ __forceinline__ void unit_map(const Job &j, long long u, int b, int n, int &slot,
+                                         int &part)
+{
+    const int H = heavy_rows(j);
+    const long long nh = (long long)j.B * H * j.parts;
+    if (u < nh) {
+        const long long rem = u - (long long)b * H * j.parts;
+        const int r = (int)(rem / j.parts);
+        part = (int)(rem - (long long)r * j.parts);
+        slot = r == 0 ? n : j.K + r - 1;
+    } else {
+        const long long rem = (u - nh) - (long long)b * (j.rows_per_seq - H) * j.parts;
+        const int r = (int)(rem / j.parts);
+        part = (int)(rem - (long long)r * j.parts);
+        slot = (H > 0 && r >= n) ? r + 1 : r;
+    }
+}
+
+__device__ __forceinline__ UnitPre unit_prefetch(const Job &j, long long u)
+{
+    UnitPre p{0, 0, 0};
+    if (u >= j.total_units)
+        return p;
+    const int b = unit_seq(j, u);
+    p.len = j.kind == K_TREE ? j.N : (j.lens ? __ldg(j.lens + b) : (j.kind == K_PACKED ? 0 : j.K));
+    p.p0 = j.pos_base ? __ldg(j.pos_base + b) : 0;
+    if (j.kind == K_TREE && j.Tp != 0.f) {
+        int slot, part;
+        unit_map(j, u, b, 0, slot, part);
+        p.np = __ldg(j.node_pos + (int64_t)b * j.N + slot);
+    }
+    return p;
+}
+
+__device__ __forceinline__ int clamp_n(const Job &j, int len)
+{
+    const int hi = (j.kind == K_PACKED) ? j.K - 1 : j.K;
+    return min(max(len, 0), hi);
+}
+
+// Row slots that exist for a sequence of clamped length n.
+__device__ __forceinline__ int valid_slots_n(const Job &j, int n)
+{
+    switch (j.kind) {
+    case K_GREEDY: return n + 1;
+    case K_SAMPLE: return 2 * n + 1;
+    case K_TREE: return j.N;
+    default: return n + 1 + j.W;
+    }
+}
+__device__ __forceinline__ bool slot_valid_n(const Job &j, int n, int slot)
+{
+    switch (j.kind) {
+    case K_GREEDY: return slot <= n;
+    case K_SAMPLE: return slot <= n || (slot > j.K && slot - j.K - 1 < n);
+    case K_TREE: return true;
+    default: return slot <= n || slot >= j.K;
+    }
+}
+
+__device__ __forceinline__ RowMode row_mode(const Job &j, int b, int slot, int n, int64_t p0,
+                                            int np)
 {
     RowMode r;
     r.mode = 0;
     r.c1 = r.c2 = r.invT = 0.f;
     r.T = 1.0;
     r.key = 0;
-    int64_t p0 = pos0_of(j, b);
     switch (j.kind) {
     case K_GREEDY:
         r.mode = M_ARGMAX;
         break;
-    case K_SAMPLE: {
-        int n = clamp_len(j, b);
+    case K_SAMPLE:
         r.mode = M_LSE;
         if (slot <= j.K) {
             r.c1 = j.cp;
@@ -71,7 +198,6 @@ __device__ RowMode row_mode(const Job &j, int b, int slot)
             r.c1 = j.cq;
         }
         break;
-    }
     case K_TREE:
         if (j.Tp == 0.f) {
             r.mode = M_ARGMAX;
@@ -79,12 +205,10 @@ __device__ RowMode row_mode(const Job &j, int b, int slot)
             r.mode = M_GUMBEL;
             r.invT = j.invTp;
             r.T = j.Tp;
-            int np = __ldg(j.node_pos + (int64_t)b * j.N + slot);
             r.key = rng_key(j.seed, kTree, (uint64_t)b, p0 + np, 0);
         }
         break;
-    default: {  // Packed-SS
-        int n = clamp_len(j, b);
+    default:  // Packed-SS
         if (slot < j.K) {
             if (j.Tp == 0.f) {
                 r.mode = M_ARGMAX;
@@ -99,12 +223,12 @@ __device__ RowMode row_mode(const Job &j, int b, int slot)
                 }
             }
         } else {
-            int jj = slot - j.K;
+            const int jj = slot - j.K;
             if (j.Tp == 0.f) {
                 r.mode = M_ARGMAX | M_LSE;  // confidence needs the T = 1 normaliser
                 r.c1 = j.c1;
             } else {
-                r.mode = M_GUMBEL | M_LSE;
+                r.mode = M_GUMBEL | M_LSE | M_MAX;
                 r.c1 = j.cp;
                 r.invT = j.invTp;
                 r.T = j.Tp;
@@ -116,39 +240,65 @@ __device__ RowMode row_mode(const Job &j, int b, int slot)
             }
         }
     }
-    }
     return r;
 }
 
+// Everything the producer needs to stream unit u (u < total_units).
+struct UnitInfo {
+    int rec;  // record index of the unit: (b * rows_per_seq + slot) * parts + part
+    int b, slot, part;
+    bool valid;
+    unsigned expect;
+    RowMode rm;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const Job &j, long long u, const UnitPre &p)
+{
+    UnitInfo i;
+    i.b = unit_seq(j, u);
+    const int n = j.kind == K_TREE ? j.N : clamp_n(j, p.len);
+    unit_map(j, u, i.b, n, i.slot, i.part);
+    i.rec = (int)(((long long)i.b * j.rows_per_seq + i.slot) * j.parts + i.part);
+    i.valid = slot_valid_n(j, n, i.slot);
+    i.expect = (unsigned)(valid_slots_n(j, n) * j.parts);
+    i.rm = row_mode(j, i.b, i.slot, n, p.p0, p.np);
+    return i;
+}
+
+// Gumbel part of a thread's state (passed by value to the out-of-line queue
+// screen, so that the state stays in registers).
+struct GState {
+    Cand2 c;           // candidates
+    float lomax;       // best lower end seen
+    float thr, thrS;   // level-2 and level-1 thresholds
+    int seedv;         // the seed candidate (warp-uniform)
+};
+
 // Per-thread running state of one unit.
 struct TState {
-    float mx, mn;
+    float e1, e2;      // integer reference exponents of the sums (-inf: none yet)
+    float2 acc1, acc2; // sums of 2^fl(x c - e), as fp32 pairs
+    float mx;          // running max
     int amax;
-    float mref;      // reference logit of the sums (a logit this thread has seen)
-    float mc1, mc2;  // fl(mref * c1), fl(mref * c2)
-    float acc1, acc2;
-    Cand2 c;         // Gumbel candidates
-    float lomax;     // best lower end seen
-    float thr, thrS; // level-2 and level-1 thresholds
-    float pub;       // threshold last published to the CTA
-    int seedv;
+    GState g;
+    float pub;         // threshold last published to the CTA
+    int gqn;           // groups in this warp's queue (warp-uniform)
 };
 
 __device__ __forceinline__ void tstate_init(TState &s)
 {
+    s.e1 = s.e2 = -INFINITY;
+    s.acc1 = s.acc2 = make_float2(0.f, 0.f);
     s.mx = -INFINITY;
-    s.mn = INFINITY;
     s.amax = 0x7FFFFFFF;
-    s.mref = -INFINITY;
-    s.mc1 = s.mc2 = 0.f;
-    s.acc1 = s.acc2 = 0.f;
-    s.c.init();
-    s.lomax = -INFINITY;
-    s.thr = s.thrS = s.pub = -INFINITY;
-    s.seedv = -1;
+    s.g.c.init();
+    s.g.lomax = -INFINITY;
+    s.g.thr = s.g.thrS = s.pub = -INFINITY;
+    s.g.seedv = -1;
+    s.gqn = 0;
 }
 
-__device__ __forceinline__ void raise_thr(TState &s, float t)
+__device__ __forceinline__ void raise_thr(GState &s, float t)
 {
     if (t > s.thr) {
         s.thr = t;
@@ -159,7 +309,7 @@ __device__ __forceinline__ void raise_thr(TState &s, float t)
 // Level 2: fp32 interval of x/T + G; candidates whose upper end reaches the
 // threshold are kept, and the best lower end raises the threshold (anything
 // below it - 1e-9 can neither win nor tie within 1e-9).
-__device__ __forceinline__ void gumbel_level2(float x, uint32_t v, uint32_t b0, TState &s,
+__device__ __forceinline__ void gumbel_level2(float x, uint32_t v, uint32_t b0, GState &s,
                                               const RowMode &rm)
 {
     const float2 iv = logit_interval_at(x, rm.invT, rm.key, v, b0);
@@ -173,147 +323,211 @@ __device__ __forceinline__ void gumbel_level2(float x, uint32_t v, uint32_t b0, 
     }
 }
 
-template <typename In, int MODE>
-__device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, int vbase, TState &s,
-                                         const RowMode &rm, const float *__restrict__ gt)
+// ---------------------------------------------------------------------------
+// One stage = one chunk: each consumer thread holds kVecsPerThread vectors.
+// Vectors past the end of the stage read as -inf, which adds nothing to a
+// sum and never wins a max.
+// ---------------------------------------------------------------------------
+using Chunk = uint4[kVecsPerThread];
+
+template <typename In>
+__device__ __forceinline__ void load_chunk(const uint4 *__restrict__ st, int nv, Chunk &q)
 {
-    using VT = VecTraits<In>;
-    constexpr int E = VT::N;
     const int t = threadIdx.x;
-    uint4 q[kVecsPerThread];
-    bool ok[kVecsPerThread];
 #pragma unroll
     for (int k = 0; k < kVecsPerThread; ++k) {
         int idx = t + k * kConsumers;
-        ok[k] = idx < nv;
-        q[k] = ok[k] ? st[idx] : make_uint4(0, 0, 0, 0);
-    }
-    if (MODE & (M_ARGMAX | M_LSE)) {
-        // chunk max / min on packed values (bf16x2 or fp32), as a short tree
-        uint32_t pm = VT::kNegInf, pn = VT::kPosInf;
-#pragma unroll
-        for (int k = 0; k < kVecsPerThread; ++k)
-            if (ok[k]) {
-                pm = VT::bmax(pm, VT::pmax(q[k]));
-                if (MODE & M_LSE)
-                    pn = VT::bmin(pn, VT::pmin(q[k]));
-            }
-        const float cm = VT::hi_of(pm);
-        if ((MODE & M_ARGMAX) && cm > s.mx) {
-            bool found = false;
-#pragma unroll
-            for (int k = 0; k < kVecsPerThread; ++k) {
-                float f[E];
-                VT::unpack(q[k], f);
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    if (!found && ok[k] && f[e] == cm) {
-                        found = true;
-                        s.amax = (vbase + t + k * kConsumers) * E + e;
-                    }
-            }
-        }
-        s.mx = fmaxf(s.mx, cm);
-        if ((MODE & M_LSE) && cm > -INFINITY) {
-            s.mn = fminf(s.mn, VT::lo_of(pn));
-            if (s.mref == -INFINITY) {
-                s.mref = cm;
-                s.mc1 = __fmul_rn(cm, rm.c1);
-                if (MODE & M_LSE2)
-                    s.mc2 = __fmul_rn(cm, rm.c2);
-            } else {
-                float cmax = (MODE & M_LSE2) ? fmaxf(rm.c1, rm.c2) : rm.c1;
-                if ((cm - s.mref) * cmax > 64.f) {  // keep every term below 2^64
-                    float n1 = __fmul_rn(cm, rm.c1);
-                    s.acc1 *= ex2f(s.mc1 - n1);
-                    s.mc1 = n1;
-                    if (MODE & M_LSE2) {
-                        float n2 = __fmul_rn(cm, rm.c2);
-                        s.acc2 *= ex2f(s.mc2 - n2);
-                        s.mc2 = n2;
-                    }
-                    s.mref = cm;
-                }
-            }
-            // one FFMA and one ex2 per term; stage partials summed as a tree
-            float part1[kVecsPerThread], part2[kVecsPerThread];
-#pragma unroll
-            for (int k = 0; k < kVecsPerThread; ++k) {
-                part1[k] = 0.f;
-                part2[k] = 0.f;
-                if (ok[k]) {
-                    float f[E], e1[E];
-                    VT::unpack(q[k], f);
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        e1[e] = ex2f(fmaf(f[e], rm.c1, -s.mc1));
-#pragma unroll
-                    for (int w = E / 2; w >= 1; w >>= 1)
-#pragma unroll
-                        for (int e = 0; e < w; ++e)
-                            e1[e] += e1[e + w];
-                    part1[k] = e1[0];
-                    if (MODE & M_LSE2) {
-                        float e2[E];
-#pragma unroll
-                        for (int e = 0; e < E; ++e)
-                            e2[e] = ex2f(fmaf(f[e], rm.c2, -s.mc2));
-#pragma unroll
-                        for (int w = E / 2; w >= 1; w >>= 1)
-#pragma unroll
-                            for (int e = 0; e < w; ++e)
-                                e2[e] += e2[e + w];
-                        part2[k] = e2[0];
-                    }
-                }
-            }
-#pragma unroll
-            for (int w = kVecsPerThread / 2; w >= 1; w >>= 1)
-#pragma unroll
-                for (int k = 0; k < w; ++k) {
-                    part1[k] += part1[k + w];
-                    part2[k] += part2[k + w];
-                }
-            s.acc1 += part1[0];
-            if (MODE & M_LSE2)
-                s.acc2 += part2[0];
-        }
-    }
-    if (MODE & M_GUMBEL) {
-        // level 1 on groups of 4 ids: one hash word; skip the group unless a
-        // byte is 0xFF (unbounded bucket) or its largest logit can reach the
-        // threshold with the largest finite bucket bound.
-        const uint32_t klo = (uint32_t)rm.key;
-        const float gmax = g8max(gt);
-#pragma unroll
-        for (int k = 0; k < kVecsPerThread; ++k)
-            if (ok[k]) {
-                const uint32_t v0 = (uint32_t)(vbase + t + k * kConsumers) * E;
-#pragma unroll
-                for (int g = 0; g < E / 4; ++g) {
-                    const uint32_t wa = word_a(klo, (v0 >> 2) + g);
-                    const bool top = ((~wa - 0x01010101u) & wa & 0x80808080u) != 0u;
-                    const float gx = VT::group_max(q[k], g);
-                    if (top || fmaf(gx, rm.invT, gmax) >= s.thrS) {
-                        // rare: per-id screen, deliberately not unrolled
-#pragma unroll 1
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t v = v0 + 4 * g + e;
-                            const uint32_t b0 = (wa >> (8 * e)) & 0xFFu;
-                            const float x = VT::elem(q[k], 4 * g + e);
-                            if ((int)v != s.seedv &&
-                                fmaf(x, rm.invT, gup_of(gt, rm.key, v, b0)) >= s.thrS)
-                                gumbel_level2(x, v, b0, s, rm);
-                        }
-                    }
-                }
-            }
+        q[k] = idx < nv ? st[idx] : VecTraits<In>::neg_inf_vec();
     }
 }
 
+template <typename In>
+__device__ __forceinline__ float chunk_max(const Chunk &q)
+{
+    using VT = VecTraits<In>;
+    uint32_t pm = VT::pmax(q[0]);
+#pragma unroll
+    for (int k = 1; k < kVecsPerThread; ++k)
+        pm = VT::bmax(pm, VT::pmax(q[k]));
+    return VT::hi_of(pm);
+}
+
+// Sum of 2^fl(x c - e) over the chunk: one packed FFMA per two elements, one
+// ex2 per element, a packed-add tree.
+template <typename In>
+__device__ __forceinline__ float2 lse_terms(const Chunk &q, float c, float e)
+{
+    using VT = VecTraits<In>;
+    constexpr int P = VT::P;  // element pairs per vector
+    float2 t[kVecsPerThread * P];
+    const float2 cc = make_float2(c, c), ne = make_float2(-e, -e);
+#pragma unroll
+    for (int k = 0; k < kVecsPerThread; ++k)
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            const float2 y = fma2(VT::pair(q[k], i), cc, ne);
+            t[k * P + i] = make_float2(ex2f(y.x), ex2f(y.y));
+        }
+#pragma unroll
+    for (int w = kVecsPerThread * P / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            t[i] = add2(t[i], t[i + w]);
+    return t[0];
+}
+
+// Adds the chunk to one log-sum-exp accumulator.  A partial sum of 2^20 or
+// more (or inf / NaN: no reference yet) moves the reference up to the chunk
+// max, rounded up to an integer, and rescales the accumulator exactly.
+template <typename In>
+__device__ __forceinline__ void lse_chunk(const Chunk &q, float c, float &e, float2 &acc)
+{
+    float2 part = lse_terms<In>(q, c, e);
+    if (!(part.x + part.y < 0x1p20f)) {
+        const float cm = chunk_max<In>(q);
+        if (cm == -INFINITY) {
+            part = make_float2(0.f, 0.f);
+        } else {
+            const float en = fmaxf(e, ceilf(__fmul_ru(cm, c)));
+            if (e > -INFINITY) {
+                const float sc = pow2_int(e - en);
+                acc.x *= sc;
+                acc.y *= sc;
+            }
+            e = en;
+            part = lse_terms<In>(q, c, e);
+        }
+    }
+    acc = add2(acc, part);
+}
+
+// Running max, and with ARG its lowest index: the first vector whose max is
+// the chunk max, then the first element of it that equals it (predicated
+// selects, no search loop).
+template <typename In, bool ARG>
+__device__ __forceinline__ void max_chunk(const Chunk &q, int vbase, TState &s)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    float vm[kVecsPerThread];
+#pragma unroll
+    for (int k = 0; k < kVecsPerThread; ++k)
+        vm[k] = VT::hi_of(VT::pmax(q[k]));
+    float cm = vm[0];
+#pragma unroll
+    for (int k = 1; k < kVecsPerThread; ++k)
+        cm = fmaxf(cm, vm[k]);
+    if (ARG && cm > s.mx) {
+        int kk = kVecsPerThread - 1;
+        uint4 v = q[kVecsPerThread - 1];
+#pragma unroll
+        for (int k = kVecsPerThread - 2; k >= 0; --k)
+            if (vm[k] == cm) {
+                kk = k;
+                v = q[k];
+            }
+        int ii = E - 1;
+#pragma unroll
+        for (int i = E - 2; i >= 0; --i)
+            if (VT::elem(v, i) == cm)
+                ii = i;
+        s.amax = (vbase + (int)threadIdx.x + kk * kConsumers) * E + ii;
+    }
+    s.mx = fmaxf(s.mx, cm);
+}
+
+// Level 1, per id, of the queued groups: the bound of G from the id's top
+// byte (and for a 0xFF top byte from its second byte); ids whose bound can
+// reach the threshold get the fp32 interval of level 2.  The warp takes the
+// queue 32 groups at a time, a group per lane.
+template <typename In>
+__device__ __noinline__ GState gumbel_flush(uint4 *__restrict__ qd, uint2 *__restrict__ qm, int n,
+                                            GState s, const RowMode &rm,
+                                            const float *__restrict__ gt)
+{
+    using VT = VecTraits<In>;
+    __syncwarp();
+    for (int i = (int)(threadIdx.x & 31); i < n; i += 32) {
+        const uint4 d = qd[i];
+        const uint2 mw = qm[i];
+#pragma unroll 1
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t v = mw.x + e;
+            const uint32_t b0 = (mw.y >> (8 * e)) & 0xFFu;
+            const float x = VT::gelem(d, e);
+            if ((int)v != s.seedv && fmaf(x, rm.invT, gup_of(gt, rm.key, v, b0)) >= s.thrS)
+                gumbel_level2(x, v, b0, s, rm);
+        }
+    }
+    __syncwarp();
+    return s;
+}
+
+// Level 1 on groups of 4 ids: one hash word; a group is queued only if a
+// byte is 0xFF (unbounded bucket) or its vector's largest logit can reach the
+// threshold with the largest finite bucket bound.  The queue is compacted
+// with a ballot, so a warp does not diverge per group.
+template <typename In>
+__device__ __forceinline__ void gumbel_chunk(const Chunk &q, int nv, int vbase, TState &s,
+                                             const RowMode &rm, const float *__restrict__ gt,
+                                             PassShared &sm)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N, G = E / 4;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const uint32_t klo = (uint32_t)rm.key;
+    const float gmax = g8max(gt);
+    uint4 *qd = sm.gqd[w];
+    uint2 *qm = sm.gqm[w];
+#pragma unroll
+    for (int k = 0; k < kVecsPerThread; ++k) {
+        const int idx = t + k * kConsumers;
+        const uint32_t j0 = (uint32_t)(vbase + idx) * G;
+        const bool hot = fmaf(VT::hi_of(VT::pmax(q[k])), rm.invT, gmax) >= s.g.thrS;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const uint32_t wa = word_a(klo, j0 + g);
+            const bool top = ((~wa - 0x01010101u) & wa & 0x80808080u) != 0u;
+            const bool pass = (top || hot) && idx < nv;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+            if (bal) {
+                if (pass) {
+                    const int r = s.gqn + __popc(bal & ((1u << lane) - 1u));
+                    qd[r] = VT::group_data(q[k], g);
+                    qm[r] = make_uint2((j0 + g) * 4u, wa);
+                }
+                s.gqn += __popc(bal);
+                if (s.gqn > kGQ - 32) {
+                    s.g = gumbel_flush<In>(qd, qm, s.gqn, s.g, rm, gt);
+                    s.gqn = 0;
+                }
+            }
+        }
+    }
+}
+
+template <typename In, int MODE>
+__device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, int vbase, TState &s,
+                                         const RowMode &rm, const float *__restrict__ gt,
+                                         PassShared &sm)
+{
+    Chunk q;
+    load_chunk<In>(st, nv, q);
+    if (MODE & (M_ARGMAX | M_MAX))
+        max_chunk<In, (MODE & M_ARGMAX) != 0>(q, vbase, s);
+    if (MODE & M_LSE)
+        lse_chunk<In>(q, rm.c1, s.e1, s.acc1);
+    if (MODE & M_LSE2)
+        lse_chunk<In>(q, rm.c2, s.e2, s.acc2);
+    if (MODE & M_GUMBEL)
+        gumbel_chunk<In>(q, nv, vbase, s, rm, gt, sm);
+}
+
 // First stage of a Gumbel unit: each warp scores in fp32 the element with the
-// largest table bound it holds, and the CTA starts from the best lower end of
-// these (a rigorous lower bound of the unit's maximum).
+// largest table bound among the first vector of each lane and starts from its
+// lower end (a rigorous lower bound of the unit's maximum), published to the
+// other warps.  The seed id is known to the whole warp, which keeps it out of
+// the queue.
 template <typename In>
 __device__ __forceinline__ void gumbel_seed(const uint4 *__restrict__ st, int nv, int vbase,
                                             TState &s, const RowMode &rm,
@@ -321,27 +535,26 @@ __device__ __forceinline__ void gumbel_seed(const uint4 *__restrict__ st, int nv
                                             int slot)
 {
     using VT = VecTraits<In>;
-    constexpr int E = VT::N;
+    constexpr int E = VT::N, G = E / 4;
     const int t = threadIdx.x;
     const uint32_t klo = (uint32_t)rm.key;
     float bub = -INFINITY, bx = 0.f;
     int bv = -1;
     uint32_t bb0 = 0;
-#pragma unroll 1
-    for (int k = 0; k < kVecsPerThread; ++k) {
-        int idx = t + k * kConsumers;
-        if (idx < nv) {
-            const uint4 q = st[idx];
-            uint32_t v0 = (uint32_t)(vbase + idx) * E;
-#pragma unroll 1
-            for (int i = 0; i < E; ++i) {
-                uint32_t v = v0 + i;
-                uint32_t b0 = (word_a(klo, v >> 2) >> (8 * (i & 3))) & 0xFFu;
-                float x = VT::elem(q, i);
-                float ub = fmaf(x, rm.invT, gup_of(gt, rm.key, v, b0));
+    if (t < nv) {
+        const uint4 q = st[t];
+        const uint32_t j0 = (uint32_t)(vbase + t) * G;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const uint32_t wa = word_a(klo, j0 + g);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t b0 = (wa >> (8 * e)) & 0xFFu;
+                const float x = VT::elem(q, 4 * g + e);
+                const float ub = fmaf(x, rm.invT, gt[b0]);  // +inf for a 0xFF byte
                 if (ub > bub) {
                     bub = ub;
-                    bv = (int)v;
+                    bv = (int)((j0 + g) * 4u + e);
                     bx = x;
                     bb0 = b0;
                 }
@@ -351,17 +564,17 @@ __device__ __forceinline__ void gumbel_seed(const uint4 *__restrict__ st, int nv
     float wv = bub;
     int wi = bv;
     warp_argmax(wv, wi);
+    s.g.seedv = wi;
     if (bv >= 0 && bv == wi) {
-        s.seedv = bv;
         const float2 iv = logit_interval_at(bx, rm.invT, rm.key, (uint32_t)bv, bb0);
         const float lo = iv.x, hi = iv.y;
-        s.c.add(lo, hi, bv);
-        s.lomax = lo;
-        raise_thr(s, __fsub_rd(lo, 1e-9f));
-        atomicMax(&sm.thr[slot], f2ord(s.thr));
+        s.g.c.add(lo, hi, bv);
+        s.g.lomax = lo;
+        raise_thr(s.g, __fsub_rd(lo, 1e-9f));
+        atomicMax(&sm.thr[slot], f2ord(s.g.thr));
     }
-    named_sync(1, kConsumers);
-    raise_thr(s, ord2f(*(volatile uint32_t *)&sm.thr[slot]));
+    __syncwarp();
+    raise_thr(s.g, ord2f(*(volatile uint32_t *)&sm.thr[slot]));
 }
 
 // ---------------------------------------------------------------------------
@@ -375,14 +588,14 @@ __device__ __forceinline__ void check_len(const Job &j, int b)
         latch(j.err, SV_ERR_DEVICE_BOUNDS);
 }
 
-__device__ void fin_greedy(const Job &j, int b)
+static __device__ __noinline__ void fin_greedy(const Job &j, int b)
 {
     const int lane = threadIdx.x & 31;
     int n = clamp_len(j, b);
     if (lane == 0) check_len(j, b);
     bool match = false;
     if (lane < n) {
-        RowM r = merge_row(j, b, lane, 0.f, 0.f);
+        RowM r = merge_row(j, b, lane, 1.0, 1.0);
         int d = __ldg(j.ids + (int64_t)b * j.K + lane);
         match = (d == r.amax);
     }
@@ -390,13 +603,13 @@ __device__ void fin_greedy(const Job &j, int b)
     int h = (~mm == 0u) ? 32 : __ffs(~mm) - 1;
     h = min(h, n);
     if (lane == 0) {
-        RowM r = merge_row(j, b, h, 0.f, 0.f);
+        RowM r = merge_row(j, b, h, 1.0, 1.0);
         j.acc[b] = h;
         j.next[b] = r.amax;
     }
 }
 
-__device__ void fin_sample(const Job &j, int b)
+static __device__ __noinline__ void fin_sample(const Job &j, int b)
 {
     const int lane = threadIdx.x & 31;
     int n = clamp_len(j, b);
@@ -405,12 +618,12 @@ __device__ void fin_sample(const Job &j, int b)
     bool acc = false, und = false;
     double Lp = 0, Lq = 0, ep = 0, eq = 0;
     if (lane < n) {
-        RowM rp = merge_row(j, b, lane, j.cp, 0.f);
-        RowM rq = merge_row(j, b, j.K + 1 + lane, j.cq, 0.f);
-        Lp = kLn2 * rp.L2b1;
-        Lq = kLn2 * rq.L2b1;
-        ep = row_eps(rp, j.cp);
-        eq = row_eps(rq, j.cq);
+        RowM rp = merge_row(j, b, lane, j.crp, 1.0);
+        RowM rq = merge_row(j, b, j.K + 1 + lane, j.crq, 1.0);
+        Lp = rp.L1a;
+        Lq = rq.L1a;
+        ep = j.eps_lse;
+        eq = j.eps_lse;
         int d = __ldg(j.ids + (int64_t)b * j.K + lane);
         double lp = -INFINITY, lq = 0.0;
         if (d < 0 || d >= j.V) {
@@ -418,11 +631,12 @@ __device__ void fin_sample(const Job &j, int b)
         } else {
             float xd = load_logit(j, row_ptr(j, b, lane), d);
             float yd = load_logit(j, row_ptr(j, b, j.K + 1 + lane), d);
-            lp = (double)xd / (double)j.Tp - Lp;
-            lq = (double)yd / (double)j.Tq - Lq;
+            lp = (double)xd * j.rTp - Lp;
+            lq = (double)yd * j.rTq - Lq;
         }
-        double r = exp(lp - lq);
-        double rel = 1.01 * (ep + eq) + 1e-15;
+        // r in fp32 (exp_fast: 2^-21); x * (1/T) for x / T: 1e-13 of slack
+        double r = (double)exp_fast(lp - lq);
+        double rel = 1.01 * (ep + eq) + 0x1p-21 + 1e-13;
         double alo = alpha_of(j.amode, r * (1.0 - rel), j.lam);
         double ahi = alpha_of(j.amode, r * (1.0 + rel), j.lam);
         double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0);
@@ -431,18 +645,18 @@ __device__ void fin_sample(const Job &j, int b)
         und = !(acc || rej) || j.force_rescue;
         if (j.force_rescue)
             acc = false;
-        if (j.p_at) j.p_at[(int64_t)b * j.K + lane] = (float)exp(lp);
-        if (j.q_at) j.q_at[(int64_t)b * j.K + lane] = (float)exp(lq);
+        if (j.p_at) j.p_at[(int64_t)b * j.K + lane] = exp_fast(lp);
+        if (j.q_at) j.q_at[(int64_t)b * j.K + lane] = exp_fast(lq);
         if (j.lse_p) j.lse_p[(int64_t)b * (j.K + 1) + lane] = (float)Lp;
         if (j.lse_q) j.lse_q[(int64_t)b * j.K + lane] = (float)Lq;
         RowStat *sp = j.rs_stat + (int64_t)b * j.rows_per_seq + lane;
         sp->L1 = Lp;
-        sp->L2 = rp.L2b1;
+        sp->L2 = rp.L2c1;
         sp->m = rp.m;
         sp->eps = (float)ep;
         RowStat *sq = j.rs_stat + (int64_t)b * j.rows_per_seq + j.K + 1 + lane;
         sq->L1 = Lq;
-        sq->L2 = rq.L2b1;
+        sq->L2 = rq.L2c1;
         sq->m = rq.m;
         sq->eps = (float)eq;
     } else if (lane < j.K) {
@@ -464,12 +678,12 @@ __device__ void fin_sample(const Job &j, int b)
     double eph = __shfl_sync(0xFFFFFFFFu, ep, f & 31);
     double eqh = __shfl_sync(0xFFFFFFFFu, eq, f & 31);
     // bonus row (always valid): its Gumbel-max with key (SAMPLE, pos + n)
-    RowM rb = merge_row(j, b, n, j.cp, 0.f);
+    RowM rb = merge_row(j, b, n, j.crp, 1.0);
     const char *rown = row_ptr(j, b, n);
     GRes gb = resolve_lanes(j, rown, rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0),
                             (double)j.Tp, j.invTp, rb.gc, lane == 0);
     if (lane == 0) {
-        double Lb = kLn2 * rb.L2b1;
+        double Lb = rb.L1a;
         if (j.lse_p) j.lse_p[(int64_t)b * (j.K + 1) + n] = (float)Lb;
         RowStat *sb = j.rs_stat + (int64_t)b * j.rows_per_seq + n;
         sb->L1 = Lb;
@@ -504,21 +718,37 @@ __device__ void fin_sample(const Job &j, int b)
     }
 }
 
-__device__ void fin_tree(const Job &j, int b)
+// Value v held for node a (lane a mod 32, half a div 32) by a warp holding
+// nodes lane and lane + 32.
+__device__ __forceinline__ int node_val(int v0, int v1, int a)
+{
+    const int x0 = __shfl_sync(0xFFFFFFFFu, v0, a & 31);
+    const int x1 = __shfl_sync(0xFFFFFFFFu, v1, a & 31);
+    return (a >> 5) ? x1 : x0;
+}
+
+static __device__ __noinline__ void fin_tree(const Job &j, int b)
 {
     const int lane = threadIdx.x & 31;
     const int64_t p0 = pos0_of(j, b);
-    unsigned mlo = 0, mhi = 0;
+    int par[2], ok[2], dep[2], anc[2];
     int nflag = 0;
     for (int half = 0; half < 2; ++half) {
-        int n = lane + 32 * half;
-        bool has = n < j.N;
-        RowM r = merge_row(j, b, has ? n : 0, 0.f, 0.f);
+        const int n = lane + 32 * half;
+        const bool has = n < j.N;
+        int pn = -1, np = 0;
+        if (has) {
+            pn = __ldg(j.parent + (int64_t)b * j.N + n);
+            np = __ldg(j.node_pos + (int64_t)b * j.N + n);
+        }
+        const bool bad = has && (pn < -1 || pn >= n || np < 0);
+        if (bad)
+            latch(j.err, SV_ERR_DEVICE_BOUNDS);
+        RowM r = merge_row(j, b, has ? n : 0, 1.0, 1.0);
         int win;
         if (j.Tp == 0.f) {
             win = r.amax;
         } else {
-            int np = has ? __ldg(j.node_pos + (int64_t)b * j.N + n) : 0;
             GRes g = resolve_lanes(j, row_ptr(j, b, has ? n : 0),
                                    rng_key(j.seed, kTree, (uint64_t)b, p0 + np, 0),
                                    (double)j.Tp, j.invTp, r.gc, has);
@@ -526,48 +756,66 @@ __device__ void fin_tree(const Job &j, int b)
             if (has)
                 nflag += g.flag;
         }
-        bool m = has && (win == __ldg(j.node_tok + (int64_t)b * j.N + n));
+        const bool m = has && (win == __ldg(j.node_tok + (int64_t)b * j.N + n));
         if (has && j.match) j.match[(int64_t)b * j.N + n] = m ? 1 : 0;
-        unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
-        if (half == 0) mlo = bal; else mhi = bal;
+        // a node with a bad parent index is treated as a root that is not
+        // accepted (depth 0, so its children sit at depth 1)
+        par[half] = (has && !bad) ? pn : -1;
+        ok[half] = (m && !bad) ? 1 : 0;
+        dep[half] = (has && !bad) ? 1 : 0;
+        anc[half] = par[half];
     }
     for (int o = 16; o; o >>= 1)
         nflag += __shfl_xor_sync(0xFFFFFFFFu, nflag, o);
-    if (lane == 0) {
-        uint64_t ok = 0;
-        uint8_t depth[kMaxN];
-        int best = -1, bestd = 0;
-        for (int n = 0; n < j.N; ++n) {
-            int par = __ldg(j.parent + (int64_t)b * j.N + n);
-            int np = __ldg(j.node_pos + (int64_t)b * j.N + n);
-            if (par < -1 || par >= n || np < 0) {
-                latch(j.err, SV_ERR_DEVICE_BOUNDS);
-                depth[n] = 0;
-                continue;
-            }
-            bool m = (n < 32) ? ((mlo >> n) & 1u) : ((mhi >> (n - 32)) & 1u);
-            bool okn = m && (par < 0 || ((ok >> par) & 1ull));
-            depth[n] = (uint8_t)(par < 0 ? 1 : depth[par] + 1);
-            if (okn) {
-                ok |= 1ull << n;
-                if (depth[n] > bestd) {
-                    bestd = depth[n];
-                    best = n;
-                }
-            }
+    // Pointer jumping over the parent links (parents precede their children,
+    // N <= 64): depth = nodes on the path from the root, ok = every node on it
+    // matched.
+    for (int it = 0; it < 6; ++it) {
+        int na[2], nd[2], no[2];
+        for (int half = 0; half < 2; ++half) {
+            const int a = anc[half] < 0 ? 0 : anc[half];
+            const int da = node_val(dep[0], dep[1], a);
+            const int oa = node_val(ok[0], ok[1], a);
+            const int aa = node_val(anc[0], anc[1], a);
+            const bool up = anc[half] >= 0;
+            nd[half] = up ? dep[half] + da : dep[half];
+            no[half] = up ? (ok[half] & oa) : ok[half];
+            na[half] = up ? aa : -1;
         }
+        for (int half = 0; half < 2; ++half) {
+            dep[half] = nd[half];
+            ok[half] = no[half];
+            anc[half] = na[half];
+        }
+    }
+    // deepest accepted node, lowest index among equals
+    int key = -1;
+    for (int half = 0; half < 2; ++half) {
+        const int n = lane + 32 * half;
+        if (n < j.N && ok[half])
+            key = max(key, (dep[half] << 8) | (255 - n));
+    }
+    for (int o = 16; o; o >>= 1)
+        key = max(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
+    const int best = key < 0 ? -1 : 255 - (key & 255);
+    const int bestd = key < 0 ? 0 : (key >> 8);
+    for (int k = lane; k < j.max_depth; k += 32)
+        j.path_nodes[(int64_t)b * j.max_depth + k] = -1;
+    __syncwarp();
+    // walk from the best node to the root (warp-uniform)
+    for (int n = best, d = bestd; n >= 0 && d > 0; --d) {
+        if (lane == 0 && d - 1 < j.max_depth)
+            j.path_nodes[(int64_t)b * j.max_depth + d - 1] = n;
+        n = node_val(par[0], par[1], n);
+    }
+    if (lane == 0) {
         j.path_len[b] = bestd;
         j.commit_count[b] = bestd + 1;
-        for (int k = 0; k < j.max_depth; ++k)
-            j.path_nodes[(int64_t)b * j.max_depth + k] = -1;
-        for (int n = best, d = bestd; n >= 0; n = __ldg(j.parent + (int64_t)b * j.N + n), --d)
-            if (d - 1 < j.max_depth)
-                j.path_nodes[(int64_t)b * j.max_depth + d - 1] = n;
         if (j.flags) j.flags[b] = nflag;
     }
 }
 
-__device__ void fin_packed(const Job &j, int b)
+static __device__ __noinline__ void fin_packed(const Job &j, int b)
 {
     const int lane = threadIdx.x & 31;
     const int n = clamp_len(j, b);
@@ -586,7 +834,7 @@ __device__ void fin_packed(const Job &j, int b)
     {
         const bool has = lane < j.W;
         const int slot = j.K + (has ? lane : 0);
-        RowM r = merge_row(j, b, slot, greedy ? j.c1 : j.cp, j.c1);
+        RowM r = greedy ? merge_row(j, b, slot, j.cr1, 1.0) : merge_row(j, b, slot, j.crp, j.cr1);
         GRes g{r.amax, 0};
         if (!greedy)
             g = resolve_lanes(j, row_ptr(j, b, slot),
@@ -600,15 +848,14 @@ __device__ void fin_packed(const Job &j, int b)
             t.z = r.amax;
             t.gflag = 0;
             t.q = 1.f;
-            conf = exp2((double)__fmul_rn(r.m, j.c1) - r.L2b1);
+            conf = exp_fast((double)r.m - r.L1a);
         } else {
             t.z = g.v;
             t.gflag = g.flag;
-            double LT = kLn2 * r.L2b1;
             float yz = load_logit(j, row_ptr(j, b, slot), t.z);
-            t.q = (float)exp((double)yz / (double)j.Tp - LT);
-            conf = (j.Tp == 1.f) ? exp2((double)__fmul_rn(r.m, j.cp) - r.L2b1)
-                                 : exp2((double)__fmul_rn(r.m, j.c1) - r.L2b2);
+            t.q = exp_fast((double)yz * j.rTp - r.L1a);
+            // confidence is the largest probability at T = 1
+            conf = exp_fast((double)r.m - ((j.Tp == 1.f) ? r.L1a : r.L1b));
         }
         if (has) {
             j.dtmp[(int64_t)b * j.W + lane] = t;
@@ -620,7 +867,7 @@ __device__ void fin_packed(const Job &j, int b)
     if (greedy) {
         int v = -1;
         if (lane <= n) {
-            RowM r = merge_row(j, b, lane, 0.f, 0.f);
+            RowM r = merge_row(j, b, lane, 1.0, 1.0);
             v = r.amax;
         }
         bool match = (lane < n) && (__ldg(j.ids + (int64_t)b * Km1 + lane) == v);
@@ -635,18 +882,20 @@ __device__ void fin_packed(const Job &j, int b)
     bool acc = false, und = false;
     double Lp = 0, ep = 0;
     if (lane < n) {
-        RowM rp = merge_row(j, b, lane, j.cp, 0.f);
-        Lp = kLn2 * rp.L2b1;
-        ep = row_eps(rp, j.cp);
+        RowM rp = merge_row(j, b, lane, j.crp, 1.0);
+        Lp = rp.L1a;
+        ep = j.eps_lse;
         int d = __ldg(j.ids + (int64_t)b * Km1 + lane);
         double lp = -INFINITY;
         if (d < 0 || d >= j.V)
             latch(j.err, SV_ERR_DEVICE_BOUNDS);
         else
-            lp = (double)load_logit(j, row_ptr(j, b, lane), d) / (double)j.Tp - Lp;
-        double lq = log((double)__ldg(j.prev_q + (int64_t)b * Km1 + lane));
-        double r = exp(lp - lq);
-        double rel = 1.01 * ep + 1e-15;
+            lp = (double)load_logit(j, row_ptr(j, b, lane), d) * j.rTp - Lp;
+        // log q in fp32 (logf within 1 ulp of |log q|): 2^-22 (1 + |log q|)
+        const float qd = __ldg(j.prev_q + (int64_t)b * Km1 + lane);
+        double lq = (double)logf(qd);
+        double r = (double)exp_fast(lp - lq);
+        double rel = 1.01 * ep + 0x1p-21 + 0x1p-22 * (1.0 + fabs(lq)) + 1e-13;
         double alo = fmin(1.0, r * (1.0 - rel)), ahi = fmin(1.0, r * (1.0 + rel));
         double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0);
         acc = u < alo - kFlagEps;
@@ -681,7 +930,7 @@ __device__ void fin_packed(const Job &j, int b)
         return;
     }
     if (f == n) {
-        RowM rb = merge_row(j, b, n, j.cp, 0.f);
+        RowM rb = merge_row(j, b, n, j.crp, 1.0);
         GRes g = resolve_lanes(j, row_ptr(j, b, n),
                                rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0), (double)j.Tp,
                                j.invTp, rb.gc, lane == 0);
@@ -712,155 +961,307 @@ __device__ void fin_packed(const Job &j, int b)
 // ---------------------------------------------------------------------------
 // The streaming kernel.
 // ---------------------------------------------------------------------------
-template <typename In, int MODE>
-__device__ __forceinline__ void run_chunk(const uint4 *st, const StageMeta &mt, TState &s,
-                                          const RowMode &rm, const float *gt, PassShared &sm,
-                                          int tslot)
+template <int KIND>
+__device__ __forceinline__ void fin_kind(const Job &j, int b)
 {
-    if ((MODE & M_GUMBEL) && mt.first)
-        gumbel_seed<In>(st, mt.nv, mt.vbase, s, rm, gt, sm, tslot);
-    do_chunk<In, MODE>(st, mt.nv, mt.vbase, s, rm, gt);
+    if constexpr (KIND == K_GREEDY)
+        fin_greedy(j, b);
+    else if constexpr (KIND == K_SAMPLE)
+        fin_sample(j, b);
+    else if constexpr (KIND == K_TREE)
+        fin_tree(j, b);
+    else
+        fin_packed(j, b);
 }
 
-template <typename In>
-__device__ __forceinline__ void dispatch_chunk(const uint4 *st, const StageMeta &mt, TState &s,
-                                               const RowMode &rm, const float *gt,
-                                               PassShared &sm, int tslot)
+// A thread's sum moved to the warp's reference E (exact scaling).
+__device__ __forceinline__ float rebased(float2 acc, float e, float E)
 {
-    switch (rm.mode) {
-    case M_ARGMAX: run_chunk<In, M_ARGMAX>(st, mt, s, rm, gt, sm, tslot); break;
-    case M_LSE: run_chunk<In, M_LSE>(st, mt, s, rm, gt, sm, tslot); break;
-    case M_LSE | M_GUMBEL: run_chunk<In, M_LSE | M_GUMBEL>(st, mt, s, rm, gt, sm, tslot); break;
-    case M_GUMBEL: run_chunk<In, M_GUMBEL>(st, mt, s, rm, gt, sm, tslot); break;
-    case M_ARGMAX | M_LSE: run_chunk<In, M_ARGMAX | M_LSE>(st, mt, s, rm, gt, sm, tslot); break;
-    case M_GUMBEL | M_LSE | M_LSE2:
-        run_chunk<In, M_GUMBEL | M_LSE | M_LSE2>(st, mt, s, rm, gt, sm, tslot);
-        break;
-    default: break;
-    }
+    return e > -INFINITY ? (acc.x + acc.y) * pow2_int(e - E) : 0.f;
 }
 
-// End of a unit: reduce the consumers' state into one RowPart record, and run
-// the decision step of the sequence if this was its last unit.
-__device__ void finish_unit(const Job &j, int unit, TState &s, const RowMode &rm,
-                            PassShared &sm, int tslot)
+// End of a unit for one consumer warp: reduce the warp's state and hand it to
+// the finalizer through unit slot lu % kUnitSlots.
+// Unit header values the consumers keep after the unit's stages are released.
+struct UnitHead {
+    int unit, lu, b;
+    unsigned expect;
+};
+
+__device__ __forceinline__ void finish_unit(const Job &j, const UnitHead &mt, TState &s,
+                                            const RowMode &rm, PassShared &sm)
 {
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int us = mt.lu % kUnitSlots;
     const bool gum = (rm.mode & M_GUMBEL) != 0;
+    const bool lse = (rm.mode & M_LSE) != 0, lse2 = (rm.mode & M_LSE2) != 0;
+    const bool hasmax = (rm.mode & (M_ARGMAX | M_MAX)) != 0;
     float mx = s.mx;
     int am = s.amax;
-    warp_argmax(mx, am);
-    float mn = warp_min(s.mn);
-    Cand2 g = s.c;
+    if (hasmax)
+        warp_argmax(mx, am);
+    Cand2 g = s.g.c;
     if (gum)
         warp_cand2(g);
-    if (lane == 0) {
-        sm.rf[w][0] = mx;
-        sm.rf[w][1] = mn;
-        sm.ri[w][0] = am;
-        sm.rg[w][0] = g.hi1;
-        sm.rg[w][1] = g.lo1;
-        sm.rg[w][2] = g.hi2;
-        sm.rg[w][3] = g.lo2;
-        sm.rg[w][4] = g.hi3;
-        sm.rgi[w][0] = g.v1;
-        sm.rgi[w][1] = g.v2;
+    float E1 = -INFINITY, E2 = -INFINITY, S1 = 0.f, S2 = 0.f;
+    if (lse) {
+        E1 = warp_max(s.e1);
+        S1 = warp_sum(rebased(s.acc1, s.e1, E1));
     }
-    named_sync(1, kConsumers);
-    float M = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < kConsumerWarps; ++q)
-        M = fmaxf(M, sm.rf[q][0]);
-    float t1 = 0.f, t2 = 0.f;
-    if ((rm.mode & M_LSE) && s.mref > -INFINITY) {
-        // terms were 2^(x c - mc); the unit record is relative to fl(M c)
-        t1 = s.acc1 * ex2f(s.mc1 - __fmul_rn(M, rm.c1));
-        if (rm.mode & M_LSE2)
-            t2 = s.acc2 * ex2f(s.mc2 - __fmul_rn(M, rm.c2));
-    }
-    float w1 = warp_sum(t1), w2 = warp_sum(t2);
-    float wmn = 0.f, wmx = 0.f;
-    int wam = 0;
-    Cand2 wg;
-    wg.init();
-    if (t == 0) {
-        wmx = -INFINITY;
-        wmn = INFINITY;
-        wam = 0x7FFFFFFF;
-        for (int q = 0; q < kConsumerWarps; ++q) {
-            float v = sm.rf[q][0];
-            int i = sm.ri[q][0];
-            if (v > wmx || (v == wmx && (unsigned)i < (unsigned)wam)) {
-                wmx = v;
-                wam = i;
-            }
-            wmn = fminf(wmn, sm.rf[q][1]);
-            if (gum) {
-                Cand2 o;
-                o.hi1 = sm.rg[q][0];
-                o.lo1 = sm.rg[q][1];
-                o.hi2 = sm.rg[q][2];
-                o.lo2 = sm.rg[q][3];
-                o.hi3 = sm.rg[q][4];
-                o.v1 = sm.rgi[q][0];
-                o.v2 = sm.rgi[q][1];
-                wg.merge(o);
-            }
-        }
-        sm.thr[tslot ^ 1] = f2ord(-INFINITY);  // next unit's threshold slot
+    if (lse2) {
+        E2 = warp_max(s.e2);
+        S2 = warp_sum(rebased(s.acc2, s.e2, E2));
     }
     if (lane == 0) {
-        sm.rf[w][2] = w1;
-        sm.rf[w][3] = w2;
-    }
-    named_sync(1, kConsumers);
-    if (w == 0) {
-        int last = 0, b = 0;
-        if (lane == 0) {
-            float S1 = 0.f, S2 = 0.f;
-            for (int q = 0; q < kConsumerWarps; ++q) {
-                S1 += sm.rf[q][2];
-                S2 += sm.rf[q][3];
-            }
-            RowPart r;
-            r.m = wmx;
-            r.mn = wmn;
-            r.s1 = S1;
-            r.s2 = S2;
-            r.amax = wam;
-            r.ghi1 = wg.hi1;
-            r.glo1 = wg.lo1;
-            r.ghi2 = wg.hi2;
-            r.glo2 = wg.lo2;
-            r.ghi3 = wg.hi3;
-            r.gv1 = wg.v1;
-            r.gv2 = wg.v2;
-            r.pad[0] = r.pad[1] = r.pad[2] = r.pad[3] = 0;
-            j.rp[unit] = r;
-            long long per_seq = (long long)j.rows_per_seq * j.parts;
-            b = (int)(unit / per_seq);
-            unsigned expect = (unsigned)(valid_slots(j, b) * j.parts);
-            __threadfence();
-            unsigned old = atomicAdd(j.seq_done + b, 1u);
-            last = (old + 1u == expect);
-            if (last)
-                __threadfence();
+        // the slot's previous unit must have been merged (normally long ago)
+        if (!mbar_wait(&sm.ufree[us], ((mt.lu / kUnitSlots) & 1) ^ 1))
+            latch(j.err, SV_ERR_TIMEOUT);
+        WarpPart &p = sm.up[us][w];
+        p.m = hasmax ? mx : -INFINITY;
+        p.amax = hasmax ? am : 0x7FFFFFFF;
+        p.e1 = E1;
+        p.s1 = S1;
+        p.e2 = E2;
+        p.s2 = S2;
+        p.hi1 = g.hi1;
+        p.lo1 = g.lo1;
+        p.hi2 = g.hi2;
+        p.lo2 = g.lo2;
+        p.hi3 = g.hi3;
+        p.v1 = g.v1;
+        p.v2 = g.v2;
+        if (w == 0) {
+            sm.uunit[us] = mt.unit;
+            sm.ub[us] = mt.b;
+            sm.uexpect[us] = mt.expect;
         }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        b = __shfl_sync(0xFFFFFFFFu, b, 0);
-        if (last) {
-            switch (j.kind) {
-            case K_GREEDY: fin_greedy(j, b); break;
-            case K_SAMPLE: fin_sample(j, b); break;
-            case K_TREE: fin_tree(j, b); break;
-            default: fin_packed(j, b); break;
+        mbar_arrive(&sm.ubar[us]);
+    }
+}
+
+// Merge the consumer warps' partials of local units cu .. cu + n - 1 (n <=
+// kUnitSlots, all complete), one unit per lane, into their records and count
+// them towards their sequences.  Returns a lane mask of the units whose record
+// completed a sequence; lane i's seq is its unit's sequence.  Whole warp.
+__device__ __forceinline__ unsigned merge_units(const Job &j, PassShared &sm, int cu, int n,
+                                                int &seq)
+{
+    const int lane = threadIdx.x & 31;
+    bool done = false;
+    seq = -1;
+    if (lane < n) {
+        const int us = (cu + lane) % kUnitSlots;
+        float m = -INFINITY, e1 = -INFINITY, e2 = -INFINITY;
+        int am = 0x7FFFFFFF;
+        Cand2 g;
+        g.init();
+#pragma unroll 1
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const WarpPart &p = sm.up[us][w];
+            if (p.m > m || (p.m == m && (unsigned)p.amax < (unsigned)am)) {
+                m = p.m;
+                am = p.amax;
             }
+            e1 = fmaxf(e1, p.e1);
+            e2 = fmaxf(e2, p.e2);
+            Cand2 o;
+            o.hi1 = p.hi1;
+            o.lo1 = p.lo1;
+            o.hi2 = p.hi2;
+            o.lo2 = p.lo2;
+            o.hi3 = p.hi3;
+            o.v1 = p.v1;
+            o.v2 = p.v2;
+            g.merge(o);
+        }
+        float S1 = 0.f, S2 = 0.f;
+#pragma unroll 1
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const WarpPart &p = sm.up[us][w];
+            if (p.s1 > 0.f) S1 += p.s1 * pow2_int(p.e1 - e1);
+            if (p.s2 > 0.f) S2 += p.s2 * pow2_int(p.e2 - e2);
+        }
+        const int unit = sm.uunit[us], b = sm.ub[us];
+        const unsigned expect = sm.uexpect[us];
+        seq = b;
+        RowPart r;
+        r.m = m;
+        r.e1 = e1;
+        r.e2 = e2;
+        r.s1 = S1;
+        r.s2 = S2;
+        r.amax = am;
+        r.ghi1 = g.hi1;
+        r.glo1 = g.lo1;
+        r.ghi2 = g.hi2;
+        r.glo2 = g.lo2;
+        r.ghi3 = g.hi3;
+        r.gv1 = g.v1;
+        r.gv2 = g.v2;
+        r.pad[0] = r.pad[1] = r.pad[2] = 0;
+        j.rp[unit] = r;
+        __threadfence();
+        const unsigned old = atomicAdd(j.seq_done + b, 1u);
+        done = (old + 1u == expect);
+        if (done)
+            __threadfence();  // acquire: every record of the sequence is visible
+        mbar_arrive(&sm.ufree[us]);
+    }
+    return __ballot_sync(0xFFFFFFFFu, done);
+}
+
+// The finalizer warp: merges unit partials in local-unit order, all units
+// that are complete at once, and runs the decision steps of completed
+// sequences, until the producer is done and every unit it streamed is
+// merged.  Waits are bounded by a spin limit that restarts whenever work is
+// found.
+template <int KIND>
+__device__ void finalizer_loop(const Job &j, PassShared &sm)
+{
+    const int lane = threadIdx.x & 31;
+    int cu = 0, qh = 0, qt = 0;
+    uint32_t spin = 0;
+    for (;;) {
+        // complete slots from cu on (each lane tests one; a completed phase
+        // stays complete until the slot is freed)
+        const int u = cu + lane;
+        const bool rdy = lane < kUnitSlots && mbar_try(&sm.ubar[u % kUnitSlots],
+                                                       (u / kUnitSlots) & 1);
+        const unsigned rm = __ballot_sync(0xFFFFFFFFu, rdy);
+        const int n = __ffs(~rm) - 1;  // leading complete slots
+        if (n > 0) {
+            int seq;
+            unsigned dm = merge_units(j, sm, cu, n, seq);
+            while (dm) {
+                const int i = __ffs(dm) - 1;
+                dm &= dm - 1;
+                const int b = __shfl_sync(0xFFFFFFFFu, seq, i);
+                if (qt - qh < kFinQ) {
+                    if (lane == 0)
+                        sm.todo[qt % kFinQ] = b;
+                    ++qt;
+                } else {
+                    fin_kind<KIND>(j, b);
+                }
+            }
+            __syncwarp();
+            cu += n;
+            spin = 0;
+            continue;
+        }
+        if (qh < qt) {
+            const int b = sm.todo[qh % kFinQ];
+            ++qh;
+            fin_kind<KIND>(j, b);
+            spin = 0;
+            continue;
+        }
+        int fin = 0;
+        if (lane == 0)
+            fin = sm.prod_done && cu >= sm.nunits;
+        if (__shfl_sync(0xFFFFFFFFu, fin, 0))
+            break;
+        if (++spin > kSpinLimit) {
+            if (lane == 0)
+                latch(j.err, SV_ERR_TIMEOUT);
+            break;
+        }
+        if (spin > 64)
+            __nanosleep(SV_SPIN_SLEEP_NS);
+    }
+}
+
+// Streams one unit whose first stage is ready in `stage`: every stage of the
+// unit with the row mode fixed at compile time, then the unit's partial.
+// Returns false if a wait timed out or the producer aborted.
+template <typename In, int MODE>
+__device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, const float *gt,
+                          int &stage, uint32_t &phase, const RowMode &rm)
+{
+    const int lane = threadIdx.x & 31;
+    const StageMeta &m0 = sm.meta[stage];
+    const UnitHead uh{m0.unit, m0.lu, m0.b, m0.expect};
+    const int tslot = uh.lu % kStages;
+    TState s;
+    tstate_init(s);
+    bool first = true;
+    for (;;) {
+        const StageMeta &mt = sm.meta[stage];
+        const int nv = mt.nv, vbase = mt.vbase, last = mt.last;
+        const uint4 *st = reinterpret_cast<const uint4 *>(stages + (size_t)stage * kStageBytes);
+        if (MODE & M_GUMBEL) {
+            raise_thr(s.g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
+            if (first)
+                gumbel_seed<In>(st, nv, vbase, s, rm, gt, sm, tslot);
+        }
+        do_chunk<In, MODE>(st, nv, vbase, s, rm, gt, sm);
+        if ((MODE & M_GUMBEL) && s.g.thr > s.pub) {
+            atomicMax(&sm.thr[tslot], f2ord(s.g.thr));
+            s.pub = s.g.thr;
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.empty[stage]);
+        if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        if (last)
+            break;
+        first = false;
+        if (!mbar_wait(&sm.full[stage], phase)) {
+            latch(j.err, SV_ERR_TIMEOUT);
+            return false;
+        }
+        if (sm.meta[stage].unit != uh.unit)  // the producer aborted
+            return false;
+    }
+    if ((MODE & M_GUMBEL) && s.gqn > 0) {
+        const int w = threadIdx.x >> 5;
+        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqm[w], s.gqn, s.g, rm, gt);
+        s.gqn = 0;
+    }
+    finish_unit(j, uh, s, rm, sm);
+    return true;
+}
+
+// Only the row modes of entry-point kind KIND are instantiated.
+template <typename In, int KIND>
+__device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsigned char *stages,
+                                              const float *gt, int &stage, uint32_t &phase,
+                                              const RowMode &rm)
+{
+    const int m = rm.mode;
+    if constexpr (KIND == K_GREEDY) {
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
+    } else if constexpr (KIND == K_SAMPLE) {
+        if (m & M_GUMBEL)
+            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
+    } else if constexpr (KIND == K_TREE) {
+        if (m & M_GUMBEL)
+            return unit_loop<In, M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
+    } else {
+        switch (m) {
+        case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
+        case M_LSE: return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
+        case M_LSE | M_GUMBEL:
+            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
+        case M_ARGMAX | M_LSE:
+            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm);
+        case M_GUMBEL | M_LSE | M_MAX:
+            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm);
+        default:
+            return unit_loop<In, M_GUMBEL | M_LSE | M_LSE2 | M_MAX>(j, sm, stages, gt, stage,
+                                                                     phase, rm);
         }
     }
 }
 
-template <typename In>
-__global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS) pass_kernel(const Job j)
+template <typename In, int KIND>
+__global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
+    pass_kernel(const __grid_constant__ Job j)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     PassShared &sm = *reinterpret_cast<PassShared *>(smem_raw);
@@ -873,60 +1274,82 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS) pass_kernel(const
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
         }
-        sm.thr[0] = f2ord(-INFINITY);
-        sm.thr[1] = f2ord(-INFINITY);
+        for (int s = 0; s < kStages; ++s)
+            sm.thr[s] = f2ord(-INFINITY);
+        for (int q = 0; q < kUnitSlots; ++q) {
+            mbar_init(&sm.ubar[q], kConsumerWarps);
+            mbar_init(&sm.ufree[q], 1);
+        }
         sm.abort = 0;
+        sm.nunits = 0;
+        sm.prod_done = 0;
         mbar_fence_init();
     }
     for (int i = t; i < kGTab; i += blockDim.x)
         gt[i] = __ldg(j.gtab + i);
     __syncthreads();
 
-    const long long per_seq = (long long)j.rows_per_seq * j.parts;
-    if (t >= kConsumers) {
+    if (t >= kConsumers + 32) {
+        // ---------------- finalizer warp ----------------
+        finalizer_loop<KIND>(j, sm);
+    } else if (t >= kConsumers) {
         // ---------------- producer warp ----------------
+        // Lane 0 streams unit `cur` while the next unit's index and per-
+        // sequence values are already in flight.
         if (t == kConsumers) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t pend = 0, pend_par = 0;  // stages with a copy not yet re-acquired
+            int lu = 0;                       // local unit number
             bool ok = true;
-            for (;;) {
-                long long u = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
-                if (u >= j.total_units)
-                    break;
-                int b = (int)(u / per_seq);
-                int rem = (int)(u - (long long)b * per_seq);
-                int slot = rem / j.parts, part = rem - slot * j.parts;
-                if (!slot_valid(j, b, slot))
-                    continue;
-                const char *row = slot_row(j, b, slot);
-                int vs = part * j.part_vecs;
-                int ve = min(j.nvec, vs + j.part_vecs);
-                for (int v = vs; v < ve; v += kStageVecs) {
-                    int nv = min(kStageVecs, ve - v);
-                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u)) {
-                        ok = false;
+            long long cu = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
+            long long nu = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
+            UnitPre cp = unit_prefetch(j, cu);
+            while (cu < j.total_units) {
+                const UnitPre np = unit_prefetch(j, nu);  // consumed next round
+                const long long nn = nu < j.total_units ? (long long)atomicAdd(j.ctl + C_UNIT, 1u)
+                                                        : nu;
+                const UnitInfo ui = unit_info(j, cu, cp);
+                if (ui.valid) {
+                    const char *row = slot_row(j, ui.b, ui.slot);
+                    const int vs = ui.part * j.part_vecs;
+                    const int ve = min(j.nvec, vs + j.part_vecs);
+                    for (int v = vs; v < ve; v += kStageVecs) {
+                        const int nv = min(kStageVecs, ve - v);
+                        if (!mbar_wait(&sm.empty[stage], phase ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        pend &= ~(1u << stage);  // the consumers released it: its copy landed
+                        StageMeta &mt = sm.meta[stage];
+                        mt.unit = ui.rec;
+                        mt.nv = nv;
+                        mt.vbase = v;
+                        mt.first = (v == vs);
+                        mt.last = (v + kStageVecs >= ve);
+                        mt.lu = lu;
+                        mt.b = ui.b;
+                        mt.expect = ui.expect;
+                        mt.rm = ui.rm;
+                        if (v == vs)
+                            sm.thr[lu % kStages] = f2ord(-INFINITY);
+                        mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
+                        bulk_g2s(stages + (size_t)stage * kStageBytes, row + (int64_t)v * 16,
+                                 (uint32_t)nv * 16u, &sm.full[stage]);
+                        pend |= 1u << stage;
+                        pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok)
                         break;
-                    }
-                    pend &= ~(1u << stage);  // the consumers released it: its copy landed
-                    StageMeta &mt = sm.meta[stage];
-                    mt.unit = (int)u;
-                    mt.nv = nv;
-                    mt.vbase = v;
-                    mt.first = (v == vs);
-                    mt.last = (v + kStageVecs >= ve);
-                    mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
-                    bulk_g2s(stages + (size_t)stage * kStageBytes, row + (int64_t)v * 16,
-                             (uint32_t)nv * 16u, &sm.full[stage]);
-                    pend |= 1u << stage;
-                    pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    ++lu;
                 }
-                if (!ok)
-                    break;
+                cu = nu;
+                cp = np;
+                nu = nn;
             }
             if (ok && mbar_wait(&sm.empty[stage], phase ^ 1u)) {
                 pend &= ~(1u << stage);
@@ -939,6 +1362,10 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS) pass_kernel(const
                 sm.meta[stage].unit = -1;
                 mbar_arrive(&sm.full[stage]);
             }
+            // units the consumers will hand to the finalizer
+            sm.nunits = lu;
+            __threadfence_block();
+            sm.prod_done = 1;
             // Every copy this warp issued must land before the CTA exits; a
             // stage whose copy was consumed has completed that phase, so the
             // wait returns at once.
@@ -950,47 +1377,16 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS) pass_kernel(const
         // ---------------- consumer warps ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int tslot = 0;
-        TState s;
-        RowMode rm;
-        rm.mode = 0;
-        tstate_init(s);
         for (;;) {
             if (!mbar_wait(&sm.full[stage], phase)) {
                 latch(j.err, SV_ERR_TIMEOUT);
                 break;
             }
-            StageMeta mt = sm.meta[stage];
-            if (mt.unit < 0 || sm.abort)
+            if (sm.meta[stage].unit < 0 || sm.abort)
                 break;
-            if (mt.first) {
-                int b = (int)(mt.unit / per_seq);
-                int rem = (int)(mt.unit - (long long)b * per_seq);
-                rm = row_mode(j, b, rem / j.parts);
-                tstate_init(s);
-            }
-            if (rm.mode & M_GUMBEL)
-                raise_thr(s, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
-            const uint4 *st = reinterpret_cast<const uint4 *>(stages + (size_t)stage * kStageBytes);
-            if (j.dtype == SV_BF16)
-                dispatch_chunk<uint16_t>(st, mt, s, rm, gt, sm, tslot);
-            else
-                dispatch_chunk<float>(st, mt, s, rm, gt, sm, tslot);
-            if ((rm.mode & M_GUMBEL) && s.thr > s.pub) {
-                atomicMax(&sm.thr[tslot], f2ord(s.thr));
-                s.pub = s.thr;
-            }
-            __syncwarp();
-            if ((t & 31) == 0)
-                mbar_arrive(&sm.empty[stage]);
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (mt.last) {
-                finish_unit(j, mt.unit, s, rm, sm, tslot);
-                tslot ^= 1;
-            }
+            const RowMode rm = sm.meta[stage].rm;
+            if (!unit_dispatch<In, KIND>(j, sm, stages, gt, stage, phase, rm))
+                break;
         }
     }
     __syncthreads();
@@ -1016,27 +1412,60 @@ size_t pass_smem_bytes()
     return a + b + (size_t)kStages * kStageBytes;
 }
 
+template <typename In, int KIND>
+static cudaError_t set_smem(int smem)
+{
+    return cudaFuncSetAttribute(pass_kernel<In, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem);
+}
+
 // Host-side launchers (the kernels are templates of this translation unit).
 cudaError_t pass_setup(int *blocks_per_sm)
 {
     const int smem = (int)pass_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(pass_kernel<uint16_t>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(pass_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, pass_kernel<uint16_t>,
-                                                          kPassThreads, smem);
+    cudaError_t e = cudaSuccess;
+    cudaError_t (*fns[])(int) = {
+        set_smem<uint16_t, K_GREEDY>, set_smem<uint16_t, K_SAMPLE>, set_smem<uint16_t, K_TREE>,
+        set_smem<uint16_t, K_PACKED>, set_smem<float, K_GREEDY>,   set_smem<float, K_SAMPLE>,
+        set_smem<float, K_TREE>,      set_smem<float, K_PACKED>};
+    for (auto f : fns)
+        if (e == cudaSuccess)
+            e = f(smem);
+    // the grid is sized for the instance with the fewest resident CTAs
+    const void *ks[] = {
+        (const void *)pass_kernel<uint16_t, K_GREEDY>, (const void *)pass_kernel<uint16_t, K_SAMPLE>,
+        (const void *)pass_kernel<uint16_t, K_TREE>,   (const void *)pass_kernel<uint16_t, K_PACKED>,
+        (const void *)pass_kernel<float, K_GREEDY>,    (const void *)pass_kernel<float, K_SAMPLE>,
+        (const void *)pass_kernel<float, K_TREE>,      (const void *)pass_kernel<float, K_PACKED>};
+    int best = 1 << 30;
+    for (const void *k : ks) {
+        int n = 0;
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kPassThreads, smem);
+        best = n < best ? n : best;
+    }
+    *blocks_per_sm = best;
     return e;
+}
+
+template <typename In>
+static void launch_in(const Job &j, int grid, cudaStream_t s)
+{
+    const size_t smem = pass_smem_bytes();
+    switch (j.kind) {
+    case K_GREEDY: pass_kernel<In, K_GREEDY><<<grid, kPassThreads, smem, s>>>(j); break;
+    case K_SAMPLE: pass_kernel<In, K_SAMPLE><<<grid, kPassThreads, smem, s>>>(j); break;
+    case K_TREE: pass_kernel<In, K_TREE><<<grid, kPassThreads, smem, s>>>(j); break;
+    default: pass_kernel<In, K_PACKED><<<grid, kPassThreads, smem, s>>>(j); break;
+    }
 }
 
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s)
 {
     if (j.dtype == SV_BF16)
-        pass_kernel<uint16_t><<<grid, kPassThreads, pass_smem_bytes(), s>>>(j);
+        launch_in<uint16_t>(j, grid, s);
     else
-        pass_kernel<float><<<grid, kPassThreads, pass_smem_bytes(), s>>>(j);
+        launch_in<float>(j, grid, s);
     return cudaGetLastError();
 }
 

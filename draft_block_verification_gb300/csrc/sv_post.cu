@@ -126,7 +126,7 @@ __device__ void lse_chunk32(const char *row, int vb, int ve, float c, PostShared
 // Total variation.
 // ---------------------------------------------------------------------------
 template <typename In>
-__global__ void __launch_bounds__(kPostThreads) tv_kernel(const Job j)
+__global__ void __launch_bounds__(kPostThreads) tv_kernel(const __grid_constant__ Job j)
 {
     __shared__ PostShared sm;
     using VT = VecTraits<In>;
@@ -529,7 +529,7 @@ __device__ __forceinline__ void fill_ctx(const Job &j, RCtx &ctx, const char *pr
 }
 
 template <typename In>
-__global__ void __launch_bounds__(kPostThreads) resid_kernel(const Job j)
+__global__ void __launch_bounds__(kPostThreads) resid_kernel(const __grid_constant__ Job j)
 {
     __shared__ PostShared sm;
     __shared__ float gt[kGTab];
@@ -784,7 +784,7 @@ __device__ double merge64(const Job &j, int e, int i, int r)
 }
 
 template <typename In>
-__global__ void __launch_bounds__(kPostThreads) rescue_kernel(const Job j)
+__global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_constant__ Job j)
 {
     __shared__ PostShared sm;
     __shared__ float gt[kGTab];
@@ -888,7 +888,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const Job j)
                 j.rescue[e].resid = 0;
             }
         } else {
-            RowM rb = merge_row(j, b, n, j.cp, 0.f);
+            RowM rb = merge_row(j, b, n, j.crp, 1.0);
             GRes g = resolve_lanes(j, slot_row(j, b, n),
                                    rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0), (double)j.Tp,
                                    j.invTp, rb.gc, lane == 0);
