@@ -57,6 +57,9 @@ def lib():
         L.sv_selftest.argtypes = [vp, u64, i64, C.POINTER(C.c_double), vp]
         L.sv_verify_greedy.restype = i32
         L.sv_verify_greedy.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.sv_verify_greedy_static.restype = i32
+        L.sv_verify_greedy_static.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp,
+                                              vp]
         L.sv_verify_sample.restype = i32
         L.sv_verify_sample.argtypes = [vp, vp, vp, i32, i64, i32, i32, i32, vp, vp, f32, f32,
                                        i32, f32, u64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -204,6 +207,28 @@ def sv_verify_greedy(target, draft_ids, draft_len=None, *, handle=None, stream=N
     _check(lib().sv_verify_greedy(h.ptr, _p(target), code, rs, B, K, V, _p(ids), _p(dl),
                                   _p(acc), _p(nxt), _stream(stream, dev)), "sv_verify_greedy")
     return acc, nxt
+
+
+def sv_verify_greedy_static(target, draft_ids, draft_len=None, *, stream=None, accept_len=None,
+                            next_token=None, status=None):
+    """Greedy verification with the library's fixed scratch (no device
+    allocation by the library; see sv.h).  Returns (accept_len, next_token,
+    status); status[0] holds the first device-side error of the call, 0 if
+    none.  Pass preallocated outputs to keep the call free of allocations on
+    the Python side as well."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    code, rs = _rows(target, "target")
+    ids = _i32(draft_ids, (B, K), "draft_ids", dev)
+    dl = _i32(draft_len, (B,), "draft_len", dev)
+    acc = _out(accept_len, (B,), torch.int32, dev)
+    nxt = _out(next_token, (B,), torch.int32, dev)
+    st = _out(status, (1,), torch.int32, dev)
+    _check(lib().sv_verify_greedy_static(_p(target), code, rs, B, K, V, _p(ids), _p(dl), _p(acc),
+                                         _p(nxt), _p(st), _stream(stream, dev)),
+           "sv_verify_greedy_static")
+    return acc, nxt, st
 
 
 def sv_verify_sample(target, draft, draft_ids, draft_len=None, *, T_p=1.0, T_q=1.0,

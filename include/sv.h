@@ -115,6 +115,32 @@ sv_status sv_verify_greedy(sv_handle *h, const void *target, sv_dtype dtype, int
                            void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Greedy verification without any device allocation.  The papers have no
+ * counterpart: this is a deployment variant of sv_verify_greedy, same inputs,
+ * outputs and results, for callers that cannot let a library allocate device
+ * memory -- a serving engine that reserves all free memory for its own pools
+ * (a KV cache, say) up front, or a memory-capped process in which an
+ * allocation in the middle of a step could fail or stall on the allocator.
+ * No handle: the scratch is one fixed device array of about 2.1 MB per device
+ * that ships with the library.
+ *   status [1] int32, device, out: written 0 at the start of the call (in
+ *          stream order), then the first device-side error (SV_ERR_TIMEOUT,
+ *          SV_ERR_DEVICE_BOUNDS) if one occurs.  Nothing else needs to start
+ *          at zero: the call clears its own counters.
+ * Limits: B <= 4096 and B * (K + 1) <= 32768; larger shapes return
+ * SV_ERR_UNSUPPORTED with nothing enqueued.  Other argument errors return
+ * SV_ERR_INVALID_ARG as in sv_verify_greedy.
+ * Calls on one device share the scratch and must not overlap: issue them on
+ * one stream, or order the streams with events.  The first call on a device
+ * looks up the scratch and sets kernel attributes; make it before any stream
+ * capture.
+ * ------------------------------------------------------------------------- */
+sv_status sv_verify_greedy_static(const void *target, sv_dtype dtype, int64_t row_stride, int B,
+                                  int K, int V, const int32_t *draft_ids,
+                                  const int32_t *draft_len, int32_t *accept_len,
+                                  int32_t *next_token, int32_t *status, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Speculative sampling: lossless, ratio-lenient or linear-lenient acceptance
  * ([PackedSS] §2.2 and Alg. 2; [TwoTrade] §2 and Alg. 1; [SPOT] App. B).
  *   target [B, K+1, V], draft [B, K, V]: logits of the target p and the

@@ -57,3 +57,15 @@ def test_binding_exports_the_c_names():
     import draft_block_verification_gb300 as dbv
     for n in ("sv_verify_greedy", "sv_verify_sample", "sv_verify_tree", "sv_packed_step"):
         assert callable(getattr(dbv, n))
+
+
+def test_static_greedy_rejects_bad_arguments_on_the_host(lib):
+    vp = C.c_void_p
+    lib.sv_verify_greedy_static.restype = C.c_int
+    # a missing status word, or a negative batch, is refused before any CUDA call
+    rc = lib.sv_verify_greedy_static(vp(0), 1, C.c_int64(8), 1, 1, 8, vp(0), vp(0), vp(0),
+                                     vp(0), vp(0), vp(0))
+    assert rc == 1  # SV_ERR_INVALID_ARG
+    rc = lib.sv_verify_greedy_static(vp(16), 1, C.c_int64(8), -1, 1, 8, vp(16), vp(0), vp(16),
+                                     vp(16), vp(16), vp(0))
+    assert rc == 1
