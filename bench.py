@@ -79,7 +79,8 @@ def _profiled_traffic():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons (200 ms)."""
+    """nvidia-smi sampling of SM clocks and throttle reasons every 50 ms; the
+    timed region starts only after the first sample arrived."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -90,10 +91,12 @@ class Clocks:
         self.p = None
 
     def __enter__(self):
+        self.first = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.first = self.p.stdout.readline()  # sampler is running
         except OSError:
             self.p = None
         return self
@@ -146,46 +149,65 @@ def _barrier(dist, dev):
     torch.cuda.synchronize(dev)
 
 
-def cpu_baseline(cfg, seconds_budget=20.0):
-    """Time the fp64 oracle, as it stands, on a bounded sample of the workload
-    (a prefix of the batch, generated on the CPU with the same recipe)."""
-    import oracle
-    oracle.build()
-    B = cfg["B"]
-    sample_b = B
-    # one sequence is ~33 rows of V fp64 work; keep the sample within budget
-    si = datagen.sample_inputs(sample_b, cfg["K"], cfg["V"], dtype=cfg["dtype"], seed=cfg["seed"],
+def _oracle_inputs(cfg, nseq):
+    si = datagen.sample_inputs(nseq, cfg["K"], cfg["V"], dtype=cfg["dtype"], seed=cfg["seed"],
                                sigma=cfg["sigma"], T=cfg["T"], device="cpu")
-    tgt = datagen.to_numpy_logits(si.target)
-    drf = datagen.to_numpy_logits(si.draft)
-    ids = si.draft_ids.numpy()
+    return (datagen.to_numpy_logits(si.target), datagen.to_numpy_logits(si.draft),
+            si.draft_ids.numpy())
+
+
+def _oracle_call(cfg, inputs):
+    import oracle
+    tgt, drf, ids = inputs
     t0 = time.perf_counter()
     oracle.verify_sample(tgt, drf, ids, seed=cfg["seed"], want_tv=False)
-    dt = time.perf_counter() - t0
-    rows = sample_b * cfg["K"]
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, nseq=None, inputs=None):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload:
+    the first nseq sequences of the batch (all of them by default), generated
+    on the CPU with the same recipe."""
+    import oracle
+    oracle.build()
+    nseq = nseq or cfg["B"]
+    inputs = inputs or _oracle_inputs(cfg, nseq)
+    dt = _oracle_call(cfg, inputs)
+    rows = nseq * cfg["K"]
     return {"value": rows / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d sequences x %d drafts x V=%d (%s), one sv_verify_sample-equivalent "
-                      "oracle call, %.2f s wall" % (sample_b, cfg["K"], cfg["V"], cfg["dtype"], dt)}
+            "sample": "%d of %d sequences x %d drafts x V=%d (%s), one oracle verify call, "
+                      "%.3f s wall" % (nseq, cfg["B"], cfg["K"], cfg["V"], cfg["dtype"], dt)}
 
 
 def run_reference(args):
+    """The reference arm is the CPU oracle (the pages ship no code): every step
+    verifies a sample of the workload, sized so that the whole run stays
+    within about two minutes."""
     dist, rank, ws = _dist()
     cfg = datagen.CONFIGS[WORKLOAD]
     if rank != 0:
         return
+    import oracle
+    oracle.build()
+    full = _oracle_inputs(cfg, cfg["B"])
+    t_full = _oracle_call(cfg, full)
+    n_calls = max(1, args.warmup + args.steps)
+    nseq = int(max(1, min(cfg["B"], cfg["B"] * 120.0 / (n_calls * max(t_full, 1e-6)))))
+    inputs = full if nseq == cfg["B"] else tuple(a[:nseq] for a in full)
     vals = []
     cb = None
-    for _ in range(args.warmup + args.steps):
-        cb = cpu_baseline(cfg)
+    for _ in range(n_calls):
+        cb = cpu_baseline(cfg, nseq, inputs)
         vals.append(cb["value"])
     value = statistics.median(vals[args.warmup:]) if args.steps else cb["value"]
     cb["value"] = value
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * cfg["B"] * cfg["K"] / value, "higher_is_better": True,
+            "ms_per_step": 1000.0 * nseq * cfg["K"] / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "B": cfg["B"], "K": cfg["K"], "V": cfg["V"],
-                       "logits": cfg["dtype"], "T": cfg["T"], "l2": "inputs larger than L2"},
+                       "logits": cfg["dtype"], "T": cfg["T"], "l2": "inputs larger than L2",
+                       "sample_sequences_per_step": nseq},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -199,7 +221,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dbv.build()
-    cfg = datagen.CONFIGS[WORKLOAD]
+    cfg = dict(datagen.CONFIGS[WORKLOAD])
+    if args.batch:
+        cfg["B"] = args.batch
     B, K, V = cfg["B"], cfg["K"], cfg["V"]
     si = datagen.sample_inputs(B, K, V, dtype=cfg["dtype"], seed=cfg["seed"], sigma=cfg["sigma"],
                                T=cfg["T"], device=dev)
@@ -269,9 +293,11 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "K": K, "V": V, "logits": "bf16",
+        "config": {"workload": WORKLOAD if B == datagen.CONFIGS[WORKLOAD]["B"] else
+                   "%s with B=%d" % (WORKLOAD, B), "B": B, "K": K, "V": V, "logits": "bf16",
                    "T": cfg["T"], "mode": "lossless", "outputs": "accept_len, next_token, "
-                   "p/q at draft ids, lse", "l2": "inputs larger than L2 (541.75 MB/step)"},
+                   "p/q at draft ids, lse",
+                   "l2": "inputs larger than L2 (%.2f MB/step)" % (B * (2 * K + 1) * V * 2 / 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _profiled_traffic(),
                      "peak_source": peak_kind, "kernel": "pass_kernel", "kernel_ms": kern_ms,
@@ -291,10 +317,12 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the number of sequences (small cases for ncu captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

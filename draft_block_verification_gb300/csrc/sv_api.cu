@@ -16,8 +16,9 @@ size_t pass_smem_bytes();
 size_t rescue_scratch_doubles(int B);
 cudaError_t pass_setup(int *blocks_per_sm);
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s);
-cudaError_t post_setup(int *blocks_per_sm);
-cudaError_t post_launch(const Job &j, int grid, int coop_grid, bool tv, cudaStream_t s);
+cudaError_t post_setup(int occ[2]);
+cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
+                        cudaStream_t s);
 cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s);
 constexpr int kResidChunksHost = 8;
 }  // namespace sv
@@ -28,7 +29,8 @@ struct sv_handle {
     int device = 0;
     int sms = 0;
     int pass_blocks = 1;   // resident streaming CTAs per SM
-    int post_blocks = 1;   // resident post-pass CTAs per SM
+    int post_blocks = 1;   // resident residual-kernel CTAs per SM
+    int tv_blocks = 1;     // resident total-variation CTAs per SM
     int *d_err = nullptr;
     unsigned *d_ctl = nullptr;
     float *d_gtab = nullptr;
@@ -227,7 +229,8 @@ sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post
     if (h->timing) cudaEventRecord(h->ev[1], s);
     if (e != cudaSuccess) return cuda_status(e);
     if (!post) return SV_OK;
-    return cuda_status(post_launch(j, h->sms * h->post_blocks, h->sms, tv, s));
+    return cuda_status(
+        post_launch(j, h->sms * h->tv_blocks, h->sms * h->post_blocks, h->sms, tv, s));
 }
 
 }  // namespace
@@ -260,11 +263,12 @@ sv_status sv_create(sv_handle **out)
     sv_handle *h = new sv_handle();
     h->device = dev;
     h->sms = prop.multiProcessorCount;
-    int nb = 0, pb = 0;
+    int nb = 0, pb[2] = {0, 0};
     cudaError_t e = pass_setup(&nb);
     h->pass_blocks = std::max(nb, 1);
-    if (e == cudaSuccess) e = post_setup(&pb);
-    h->post_blocks = std::max(1, std::min(pb, 2));
+    if (e == cudaSuccess) e = post_setup(pb);
+    h->tv_blocks = std::max(1, pb[0]);
+    h->post_blocks = std::max(1, pb[1]);
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_ctl, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_gtab, kGTab * sizeof(float));

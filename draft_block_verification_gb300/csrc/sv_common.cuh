@@ -21,6 +21,7 @@ __device__ __forceinline__ int clamp_len(const Job &j, int b)
 // ---------------------------------------------------------------------------
 struct RowM {
     float m;            // row max (modes that track it)
+    float xd;           // logit at the row's draft token (NaN if not recorded)
     int amax;
     double L2c1, L2c2;  // log2 sum_v 2^(x_v c) with the fp32 factors c1, c2
     double L1a, L1b;    // natural log-sum-exps of x / T for the same two sums
@@ -75,17 +76,36 @@ static __device__ RowM merge_row(const Job &j, int b, int slot, double r1, doubl
     const RowPart *p = j.rp + ((int64_t)b * j.rows_per_seq + slot) * nrec;
     RowM r;
     r.m = -INFINITY;
+    r.xd = __int_as_float(0x7FC00000);
     r.amax = 0x7FFFFFFF;
     r.gc.init();
+    // one pass over the records (each read once); a larger exponent moves the
+    // running sum by an exact power of two
     float E1 = -INFINITY, E2 = -INFINITY;
+    double S1 = 0.0, S2 = 0.0;
     for (int q = 0; q < nrec; ++q) {
         RowPart x = load_part(p + q);
         if (x.m > r.m || (x.m == r.m && x.amax < r.amax)) {
             r.m = x.m;
             r.amax = x.amax;
         }
-        E1 = fmaxf(E1, x.e1);
-        E2 = fmaxf(E2, x.e2);
+        r.xd = fmaxf(r.xd, x.xd);
+        if (x.s1 > 0.f) {
+            if (x.e1 > E1) {
+                S1 = (E1 > -INFINITY ? ldexp(S1, (int)(E1 - x.e1)) : 0.0) + (double)x.s1;
+                E1 = x.e1;
+            } else {
+                S1 += ldexp((double)x.s1, (int)(x.e1 - E1));
+            }
+        }
+        if (x.s2 > 0.f) {
+            if (x.e2 > E2) {
+                S2 = (E2 > -INFINITY ? ldexp(S2, (int)(E2 - x.e2)) : 0.0) + (double)x.s2;
+                E2 = x.e2;
+            } else {
+                S2 += ldexp((double)x.s2, (int)(x.e2 - E2));
+            }
+        }
         Cand2 c;
         c.hi1 = x.ghi1;
         c.lo1 = x.glo1;
@@ -95,14 +115,6 @@ static __device__ RowM merge_row(const Job &j, int b, int slot, double r1, doubl
         c.v1 = x.gv1;
         c.v2 = x.gv2;
         r.gc.merge(c);
-    }
-    double S1 = 0.0, S2 = 0.0;
-    for (int q = 0; q < nrec; ++q) {
-        RowPart x = load_part(p + q);
-        if (x.s1 > 0.f)
-            S1 += ldexp((double)x.s1, (int)(x.e1 - E1));
-        if (x.s2 > 0.f)
-            S2 += ldexp((double)x.s2, (int)(x.e2 - E2));
     }
     const double l1 = log2_fast(S1), l2 = log2_fast(S2);
     r.L2c1 = (double)E1 + l1;

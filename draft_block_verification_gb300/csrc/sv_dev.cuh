@@ -249,7 +249,8 @@ struct __align__(16) RowPart {
     // Gumbel candidates (see Cand2 in sv_gumbel.cuh)
     float ghi1, glo1, ghi2, glo2, ghi3;
     int gv1, gv2;
-    int pad[3];
+    float xd;       // logit at the row's draft token, if the unit holds it (else NaN)
+    int pad[2];
 };
 
 // Merged per-row statistics kept for the later kernels.

@@ -43,6 +43,8 @@ struct StageMeta {
     int lu;           // this CTA's running unit number
     int b;            // sequence of the unit
     unsigned expect;  // records that complete sequence b
+    int xid;          // vocabulary id whose logit the unit records (-1: none)
+    int pad[3];
     RowMode rm;       // row mode of the unit
 };
 
@@ -53,7 +55,8 @@ struct WarpPart {
     float e1, s1, e2, s2;
     float hi1, lo1, hi2, lo2, hi3;
     int v1, v2;
-    int pad[3];
+    float xd;  // logit at the draft token (the one lane that held it), else NaN
+    int pad[2];
 };
 
 struct PassShared {
@@ -83,9 +86,10 @@ struct PassShared {
 
 // Per-sequence values a unit's bookkeeping needs, loaded one unit ahead.
 struct UnitPre {
-    int len;     // draft length as given (unclamped)
-    int64_t p0;  // absolute position of the sequence's first row
-    int np;      // tree: position of the node (T > 0)
+    int len;       // draft length as given (unclamped)
+    int64_t p0;    // absolute position of the sequence's first row
+    int np;        // tree: position of the node (T > 0)
+    int ida, idb;  // draft tokens of the two slots a light unit can map to
 };
 
 // Unit order.  Rows that carry a Gumbel-max (a few times the work of a plain
@@ -130,12 +134,41 @@ __device__ __forceinline__ void unit_map(const Job &j, long long u, int b, int n
     }
 }
 
+// Draft position whose token the row in `slot` is tested on (sample: target
+// and drafter rows; Packed-SS at T > 0: verify rows), or -1.
+__device__ __forceinline__ int draft_pos(const Job &j, int slot)
+{
+    if (j.kind == K_SAMPLE)
+        return slot < j.K ? slot : (slot > j.K ? slot - j.K - 1 : -1);
+    if (j.kind == K_PACKED && j.Tp != 0.f)
+        return slot < j.K - 1 ? slot : -1;
+    return -1;
+}
+
+__device__ __forceinline__ int draft_token(const Job &j, int b, int slot)
+{
+    const int pos = draft_pos(j, slot);
+    if (pos < 0 || !j.ids)
+        return -1;
+    const int per = j.kind == K_PACKED ? j.K - 1 : j.K;
+    return __ldg(j.ids + (int64_t)b * per + pos);
+}
+
 __device__ __forceinline__ UnitPre unit_prefetch(const Job &j, long long u)
 {
-    UnitPre p{0, 0, 0};
+    UnitPre p{0, 0, 0, -1, -1};
     if (u >= j.total_units)
         return p;
     const int b = unit_seq(j, u);
+    const int H = heavy_rows(j);
+    const long long nh = (long long)j.B * H * j.parts;
+    if (H > 0 && u >= nh) {
+        // a light unit's slot is r or r + 1 (the bonus slot is skipped)
+        const long long rem = (u - nh) - (long long)b * (j.rows_per_seq - H) * j.parts;
+        const int r = (int)(rem / j.parts);
+        p.ida = draft_token(j, b, r);
+        p.idb = draft_token(j, b, r + 1);
+    }
     p.len = j.kind == K_TREE ? j.N : (j.lens ? __ldg(j.lens + b) : (j.kind == K_PACKED ? 0 : j.K));
     p.p0 = j.pos_base ? __ldg(j.pos_base + b) : 0;
     if (j.kind == K_TREE && j.Tp != 0.f) {
@@ -249,6 +282,7 @@ struct UnitInfo {
     int b, slot, part;
     bool valid;
     unsigned expect;
+    int xid;  // draft token whose logit the unit records, or -1
     RowMode rm;
 };
 
@@ -259,6 +293,20 @@ __device__ __forceinline__ UnitInfo unit_info(const Job &j, long long u, const U
     const int n = j.kind == K_TREE ? j.N : clamp_n(j, p.len);
     unit_map(j, u, i.b, n, i.slot, i.part);
     i.rec = (int)(((long long)i.b * j.rows_per_seq + i.slot) * j.parts + i.part);
+    i.xid = -1;
+    const int H = heavy_rows(j);
+    if (H > 0 && u >= (long long)j.B * H * j.parts) {
+        const int pos = draft_pos(j, i.slot);
+        if (pos >= 0 && pos < n) {
+            const long long rem =
+                (u - (long long)j.B * H * j.parts) - (long long)i.b * (j.rows_per_seq - H) * j.parts;
+            const int d = (i.slot == (int)(rem / j.parts)) ? p.ida : p.idb;
+            if (d < 0 || d >= j.V)
+                latch(j.err, SV_ERR_DEVICE_BOUNDS);  // tested as probability 0
+            else
+                i.xid = d;
+        }
+    }
     i.valid = slot_valid_n(j, n, i.slot);
     i.expect = (unsigned)(valid_slots_n(j, n) * j.parts);
     i.rm = row_mode(j, i.b, i.slot, n, p.p0, p.np);
@@ -283,6 +331,7 @@ struct TState {
     GState g;
     float pub;         // threshold last published to the CTA
     int gqn;           // groups in this warp's queue (warp-uniform)
+    float xd;          // logit at the unit's draft token (its owner thread), else NaN
 };
 
 __device__ __forceinline__ void tstate_init(TState &s)
@@ -296,6 +345,7 @@ __device__ __forceinline__ void tstate_init(TState &s)
     s.g.thr = s.g.thrS = s.pub = -INFINITY;
     s.g.seedv = -1;
     s.gqn = 0;
+    s.xd = __int_as_float(0x7FC00000);
 }
 
 __device__ __forceinline__ void raise_thr(GState &s, float t)
@@ -612,27 +662,30 @@ static __device__ __noinline__ void fin_greedy(const Job &j, int b)
 static __device__ __noinline__ void fin_sample(const Job &j, int b)
 {
     const int lane = threadIdx.x & 31;
-    int n = clamp_len(j, b);
-    if (lane == 0) check_len(j, b);
+    // Every load of the step is independent of the draft length, so they are
+    // issued together: the length, the position base and the unit records of
+    // target rows 0..K (lane i) and drafter rows (lane i < K).  Records of rows
+    // beyond the length are not used.  The logits at the draft tokens were
+    // recorded during the stream.
+    const int len = seq_len(j, b);
     const int64_t p0 = pos0_of(j, b);
+    RowM rp, rq;
+    rp.gc.init();
+    rq.gc.init();
+    if (lane <= j.K) rp = merge_row(j, b, lane, j.crp, 1.0);
+    if (lane < j.K) rq = merge_row(j, b, j.K + 1 + lane, j.crq, 1.0);
+    const int n = min(max(len, 0), j.K);
+    if (lane == 0 && (len < 0 || len > j.K)) latch(j.err, SV_ERR_DEVICE_BOUNDS);
     bool acc = false, und = false;
-    double Lp = 0, Lq = 0, ep = 0, eq = 0;
+    double Lp = 0, Lq = 0;
+    const double ep = j.eps_lse, eq = j.eps_lse;
     if (lane < n) {
-        RowM rp = merge_row(j, b, lane, j.crp, 1.0);
-        RowM rq = merge_row(j, b, j.K + 1 + lane, j.crq, 1.0);
         Lp = rp.L1a;
         Lq = rq.L1a;
-        ep = j.eps_lse;
-        eq = j.eps_lse;
-        int d = __ldg(j.ids + (int64_t)b * j.K + lane);
         double lp = -INFINITY, lq = 0.0;
-        if (d < 0 || d >= j.V) {
-            latch(j.err, SV_ERR_DEVICE_BOUNDS);
-        } else {
-            float xd = load_logit(j, row_ptr(j, b, lane), d);
-            float yd = load_logit(j, row_ptr(j, b, j.K + 1 + lane), d);
-            lp = (double)xd * j.rTp - Lp;
-            lq = (double)yd * j.rTq - Lq;
+        if (!isnan(rp.xd) && !isnan(rq.xd)) {  // NaN: the draft token was out of range
+            lp = (double)rp.xd * j.rTp - Lp;
+            lq = (double)rq.xd * j.rTq - Lq;
         }
         // r in fp32 (exp_fast: 2^-21); x * (1/T) for x / T: 1e-13 of slack
         double r = (double)exp_fast(lp - lq);
@@ -677,19 +730,22 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
     double Lqh = __shfl_sync(0xFFFFFFFFu, Lq, f & 31);
     double eph = __shfl_sync(0xFFFFFFFFu, ep, f & 31);
     double eqh = __shfl_sync(0xFFFFFFFFu, eq, f & 31);
-    // bonus row (always valid): its Gumbel-max with key (SAMPLE, pos + n)
-    RowM rb = merge_row(j, b, n, j.crp, 1.0);
-    const char *rown = row_ptr(j, b, n);
-    GRes gb = resolve_lanes(j, rown, rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0),
-                            (double)j.Tp, j.invTp, rb.gc, lane == 0);
+    // bonus row n (always valid): its Gumbel-max with key (SAMPLE, pos + n),
+    // resolved by the lane that holds its record
+    GRes g = resolve_lanes(j, row_ptr(j, b, lane <= j.K ? lane : 0),
+                           rng_key(j.seed, kSample, (uint64_t)b, p0 + lane, 0), (double)j.Tp,
+                           j.invTp, rp.gc, lane == n);
+    const int gbv = __shfl_sync(0xFFFFFFFFu, g.v, n);
+    const int gbf = __shfl_sync(0xFFFFFFFFu, g.flag, n);
+    const double Lb = __shfl_sync(0xFFFFFFFFu, rp.L1a, n);
+    const float mb = __shfl_sync(0xFFFFFFFFu, rp.m, n);
     if (lane == 0) {
-        double Lb = rb.L1a;
         if (j.lse_p) j.lse_p[(int64_t)b * (j.K + 1) + n] = (float)Lb;
         RowStat *sb = j.rs_stat + (int64_t)b * j.rows_per_seq + n;
         sb->L1 = Lb;
-        sb->m = rb.m;
-        sb->gidx = gb.v;
-        sb->gflag = gb.flag;
+        sb->m = mb;
+        sb->gidx = gbv;
+        sb->gflag = gbf;
         if (rescue) {
             unsigned e = atomicAdd(j.ctl + C_RESCUE_N, 1u);
             j.rescue[e].b = b;
@@ -697,8 +753,8 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
             j.rescue[e].h = 0;
         } else if (f == n) {
             j.acc[b] = n;
-            j.next[b] = gb.v;
-            if (j.flags) j.flags[b] = gb.flag;
+            j.next[b] = gbv;
+            if (j.flags) j.flags[b] = gbf;
         } else {
             j.acc[b] = f;
             unsigned e = atomicAdd(j.ctl + C_RESID_N, 1u);
@@ -885,12 +941,11 @@ static __device__ __noinline__ void fin_packed(const Job &j, int b)
         RowM rp = merge_row(j, b, lane, j.crp, 1.0);
         Lp = rp.L1a;
         ep = j.eps_lse;
-        int d = __ldg(j.ids + (int64_t)b * Km1 + lane);
+        // the logit at the draft token was recorded during the stream (NaN:
+        // the token was out of range, already reported)
         double lp = -INFINITY;
-        if (d < 0 || d >= j.V)
-            latch(j.err, SV_ERR_DEVICE_BOUNDS);
-        else
-            lp = (double)load_logit(j, row_ptr(j, b, lane), d) * j.rTp - Lp;
+        if (!isnan(rp.xd))
+            lp = (double)rp.xd * j.rTp - Lp;
         // log q in fp32 (logf within 1 ulp of |log q|): 2^-22 (1 + |log q|)
         const float qd = __ldg(j.prev_q + (int64_t)b * Km1 + lane);
         double lq = (double)logf(qd);
@@ -986,6 +1041,7 @@ __device__ __forceinline__ float rebased(float2 acc, float e, float E)
 struct UnitHead {
     int unit, lu, b;
     unsigned expect;
+    int xid;
 };
 
 __device__ __forceinline__ void finish_unit(const Job &j, const UnitHead &mt, TState &s,
@@ -1003,6 +1059,7 @@ __device__ __forceinline__ void finish_unit(const Job &j, const UnitHead &mt, TS
     Cand2 g = s.g.c;
     if (gum)
         warp_cand2(g);
+    const float xd = warp_max(s.xd);  // NaN except at one lane (fmaxf drops NaN)
     float E1 = -INFINITY, E2 = -INFINITY, S1 = 0.f, S2 = 0.f;
     if (lse) {
         E1 = warp_max(s.e1);
@@ -1030,6 +1087,7 @@ __device__ __forceinline__ void finish_unit(const Job &j, const UnitHead &mt, TS
         p.hi3 = g.hi3;
         p.v1 = g.v1;
         p.v2 = g.v2;
+        p.xd = xd;
         if (w == 0) {
             sm.uunit[us] = mt.unit;
             sm.ub[us] = mt.b;
@@ -1052,6 +1110,7 @@ __device__ __forceinline__ unsigned merge_units(const Job &j, PassShared &sm, in
     if (lane < n) {
         const int us = (cu + lane) % kUnitSlots;
         float m = -INFINITY, e1 = -INFINITY, e2 = -INFINITY;
+        float xd = __int_as_float(0x7FC00000);
         int am = 0x7FFFFFFF;
         Cand2 g;
         g.init();
@@ -1064,6 +1123,7 @@ __device__ __forceinline__ unsigned merge_units(const Job &j, PassShared &sm, in
             }
             e1 = fmaxf(e1, p.e1);
             e2 = fmaxf(e2, p.e2);
+            xd = fmaxf(xd, p.xd);
             Cand2 o;
             o.hi1 = p.hi1;
             o.lo1 = p.lo1;
@@ -1098,7 +1158,8 @@ __device__ __forceinline__ unsigned merge_units(const Job &j, PassShared &sm, in
         r.ghi3 = g.hi3;
         r.gv1 = g.v1;
         r.gv2 = g.v2;
-        r.pad[0] = r.pad[1] = r.pad[2] = 0;
+        r.xd = xd;
+        r.pad[0] = r.pad[1] = 0;
         j.rp[unit] = r;
         __threadfence();
         const unsigned old = atomicAdd(j.seq_done + b, 1u);
@@ -1180,7 +1241,7 @@ __device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, c
 {
     const int lane = threadIdx.x & 31;
     const StageMeta &m0 = sm.meta[stage];
-    const UnitHead uh{m0.unit, m0.lu, m0.b, m0.expect};
+    const UnitHead uh{m0.unit, m0.lu, m0.b, m0.expect, m0.xid};
     const int tslot = uh.lu % kStages;
     TState s;
     tstate_init(s);
@@ -1195,6 +1256,13 @@ __device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, c
                 gumbel_seed<In>(st, nv, vbase, s, rm, gt, sm, tslot);
         }
         do_chunk<In, MODE>(st, nv, vbase, s, rm, gt, sm);
+        if (uh.xid >= 0) {
+            // the thread that holds the draft token's vector records its logit
+            constexpr int E = VecTraits<In>::N;
+            const int iv = uh.xid / E - vbase;
+            if (iv >= 0 && iv < nv && (int)threadIdx.x == iv % kConsumers)
+                s.xd = VecTraits<In>::elem(st[iv], uh.xid % E);
+        }
         if ((MODE & M_GUMBEL) && s.g.thr > s.pub) {
             atomicMax(&sm.thr[tslot], f2ord(s.g.thr));
             s.pub = s.g.thr;
@@ -1330,6 +1398,7 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
                         mt.lu = lu;
                         mt.b = ui.b;
                         mt.expect = ui.expect;
+                        mt.xid = ui.xid;
                         mt.rm = ui.rm;
                         if (v == vs)
                             sm.thr[lu % kStages] = f2ord(-INFINITY);

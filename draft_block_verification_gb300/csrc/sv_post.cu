@@ -17,6 +17,7 @@ constexpr int kPostWarps = kPostThreads / 32;
 constexpr int kResidChunks = 8;     // chunks per residual row pair
 constexpr int kRescueChunks = 16;   // chunks per row on the fp64 path
 constexpr int kMaxPairs = 32;
+constexpr int kLoadsAhead = 4;      // vectors per row each thread loads before using them
 
 struct PostShared {
     float f[kPostWarps][4];
@@ -71,10 +72,17 @@ __device__ __forceinline__ double block_sumd(double v, PostShared &sm)
     return r;
 }
 
+// Streaming 16-byte load.  Volatile so that the compiler keeps a batch of
+// them ahead of their uses (memory-level parallelism) instead of sinking each
+// load to its first use.
 template <typename In>
 __device__ __forceinline__ uint4 ldv(const char *row, int k)
 {
-    return __ldcs(reinterpret_cast<const uint4 *>(row) + k);
+    uint4 r;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(reinterpret_cast<const uint4 *>(row) + k));
+    return r;
 }
 
 __device__ __forceinline__ int chunk_lo(int nvec, int c, int nc) { return (int)((int64_t)nvec * c / nc); }
@@ -91,9 +99,19 @@ __device__ void lse_chunk32(const char *row, int vb, int ve, float c, PostShared
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
     float mref = -INFINITY, acc = 0.f, mx = -INFINITY, lo = INFINITY;
-    for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
+    for (int k0 = vb + threadIdx.x; k0 < ve; k0 += kLoadsAhead * blockDim.x) {
+      uint4 qv[kLoadsAhead];
+#pragma unroll
+      for (int u = 0; u < kLoadsAhead; ++u) {
+        const int k = k0 + u * blockDim.x;
+        qv[u] = k < ve ? ldv<In>(row, k) : VT::neg_inf_vec();
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadsAhead; ++u) {
+        if (k0 + u * (int)blockDim.x >= ve)
+            break;
         float f[E];
-        VT::unpack(ldv<In>(row, k), f);
+        VT::unpack(qv[u], f);
         float cm = -INFINITY;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -115,6 +133,7 @@ __device__ void lse_chunk32(const char *row, int vb, int ve, float c, PostShared
 #pragma unroll
             for (int e = 0; e < w; ++e) t[e] += t[e + w];
         acc += t[0];
+      }
     }
     M = block_max(mx, sm);
     mn = block_min(lo, sm);
@@ -148,15 +167,26 @@ __global__ void __launch_bounds__(kPostThreads) tv_kernel(const __grid_constant_
         const char *prow = slot_row(j, b, i), *qrow = slot_row(j, b, j.K + 1 + i);
         int vb = chunk_lo(j.nvec, c, TC), ve = chunk_lo(j.nvec, c + 1, TC);
         float acc = 0.f;
-        for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
-            float x[E], y[E];
-            VT::unpack(ldv<In>(prow, k), x);
-            VT::unpack(ldv<In>(qrow, k), y);
+        // several vectors of both rows in flight per thread before any use
+        for (int k0 = vb + threadIdx.x; k0 < ve; k0 += kLoadsAhead * blockDim.x) {
+            uint4 px[kLoadsAhead], qy[kLoadsAhead];
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                float fa = fmaf(x[e], j.cp, -lgp);  // log2 p_v
-                float fb = fmaf(y[e], j.cq, -lgq);  // log2 q_v
-                acc += ex2f(fminf(fa, fb));
+            for (int u = 0; u < kLoadsAhead; ++u) {
+                const int k = k0 + u * blockDim.x;
+                px[u] = k < ve ? ldv<In>(prow, k) : VT::neg_inf_vec();
+                qy[u] = k < ve ? ldv<In>(qrow, k) : VT::neg_inf_vec();
+            }
+#pragma unroll
+            for (int u = 0; u < kLoadsAhead; ++u) {
+                float x[E], y[E];
+                VT::unpack(px[u], x);
+                VT::unpack(qy[u], y);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    float fa = fmaf(x[e], j.cp, -lgp);  // log2 p_v
+                    float fb = fmaf(y[e], j.cq, -lgq);  // log2 q_v
+                    acc += ex2f(fminf(fa, fb));         // -inf padding adds 0
+                }
             }
         }
         float s = block_sum(acc, sm);
@@ -421,6 +451,29 @@ __device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out
     }
 }
 
+// Level 1 per id and level 2 for one vector whose group test passed.
+template <typename In, typename Tr>
+__device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, int k,
+                                             const uint32_t (&was)[VecTraits<In>::N / 4],
+                                             int seedv, const float *gt, Tr &tr)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    const uint32_t v0 = (uint32_t)k * E;
+    float x[E], y[E];
+    VT::unpack(qx, x);
+    VT::unpack(ldv<In>(c.qrow, k), y);
+#pragma unroll 1
+    for (int i = 0; i < E; ++i) {
+        const int g = i >> 2, e = i & 3;
+        const uint32_t v = v0 + i, b0 = (was[g] >> (8 * e)) & 0xFFu;
+        if ((int)v == seedv) continue;
+        const float xi = VT::elem(qx, i);
+        if (fmaf(xi, c.invTp, gup_of(gt, c.key, v, b0)) < tr.thrS) continue;
+        tr.add(c, xi, VT::elem(ldv<In>(c.qrow, k), i), v, b0);
+    }
+}
+
 // Scan vectors [vb, ve) of the pair.  Seed: each warp adds the element with
 // the largest table bound among clearly positive weights (p > 1.07 q) of its
 // threads' first vectors; the CTA starts from the best threshold.
@@ -476,31 +529,31 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, PostS
     }
     const float gmax = g8max(gt);
     float pub = tr.thr;
-    for (int k = vb + threadIdx.x; k < ve; k += blockDim.x) {
-        const uint4 qx = ldv<In>(c.prow, k);
-        tr.raise(ord2f(*(volatile uint32_t *)&sm.thr));
-        const uint32_t v0 = (uint32_t)k * E;
-        bool any = false;
-        uint32_t was[E / 4];
+    for (int k0 = vb + threadIdx.x; k0 < ve; k0 += kLoadsAhead * blockDim.x) {
+        uint4 px[kLoadsAhead];
 #pragma unroll
-        for (int g = 0; g < E / 4; ++g) {
-            was[g] = word_a(klo, (v0 >> 2) + g);
-            const bool top = ((~was[g] - 0x01010101u) & was[g] & 0x80808080u) != 0u;
-            any |= top || fmaf(VT::group_max(qx, g), c.invTp, gmax) >= tr.thrS;
+        for (int u = 0; u < kLoadsAhead; ++u) {
+            const int k = k0 + u * blockDim.x;
+            px[u] = k < ve ? ldv<In>(c.prow, k) : VT::neg_inf_vec();
         }
-        if (!any) continue;
-        float x[E], y[E];
-        VT::unpack(qx, x);
-        VT::unpack(ldv<In>(c.qrow, k), y);
+        tr.raise(ord2f(*(volatile uint32_t *)&sm.thr));
 #pragma unroll
-        for (int g = 0; g < E / 4; ++g)
+        for (int u = 0; u < kLoadsAhead; ++u) {
+            const int k = k0 + u * blockDim.x;
+            if (k >= ve)
+                break;
+            const uint32_t v0 = (uint32_t)k * E;
+            bool any = false;
+            uint32_t was[E / 4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t v = v0 + 4 * g + e, b0 = (was[g] >> (8 * e)) & 0xFFu;
-                if ((int)v == seedv) continue;
-                if (fmaf(x[4 * g + e], c.invTp, gup_of(gt, c.key, v, b0)) < tr.thrS) continue;
-                tr.add(c, x[4 * g + e], y[4 * g + e], v, b0);
+            for (int g = 0; g < E / 4; ++g) {
+                was[g] = word_a(klo, (v0 >> 2) + g);
+                const bool top = ((~was[g] - 0x01010101u) & was[g] & 0x80808080u) != 0u;
+                any |= top || fmaf(VT::group_max(px[u], g), c.invTp, gmax) >= tr.thrS;
             }
+            if (any)
+                resid_vector<In>(c, px[u], k, was, seedv, gt, tr);
+        }
         if (tr.thr > pub) {
             atomicMax(&sm.thr, f2ord(tr.thr));
             pub = tr.thr;
@@ -968,28 +1021,38 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
 }
 
 // Host-side launchers.
-cudaError_t post_setup(int *blocks_per_sm)
+// Resident CTAs per SM of the total-variation kernel (occ[0]) and of the
+// residual kernel (occ[1]); both take work items from a counter, so their
+// grids fill the GPU.
+cudaError_t post_setup(int occ[2])
 {
-    int a = 0, b = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rescue_kernel<uint16_t>,
+    int a = 0, b = 0, c = 0, d = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, tv_kernel<uint16_t>,
                                                                   kPostThreads, 0);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rescue_kernel<float>, kPostThreads, 0);
-    *blocks_per_sm = a < b ? a : b;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tv_kernel<float>, kPostThreads, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, resid_kernel<uint16_t>,
+                                                          kPostThreads, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, resid_kernel<float>, kPostThreads, 0);
+    occ[0] = a < b ? a : b;
+    occ[1] = c < d ? c : d;
     return e;
 }
 
-cudaError_t post_launch(const Job &j, int grid, int coop_grid, bool tv, cudaStream_t s)
+cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
+                        cudaStream_t s)
 {
     const bool bf = j.dtype == SV_BF16;
     if (tv) {
-        if (bf) tv_kernel<uint16_t><<<grid, kPostThreads, 0, s>>>(j);
-        else tv_kernel<float><<<grid, kPostThreads, 0, s>>>(j);
+        if (bf) tv_kernel<uint16_t><<<tv_grid, kPostThreads, 0, s>>>(j);
+        else tv_kernel<float><<<tv_grid, kPostThreads, 0, s>>>(j);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (bf) resid_kernel<uint16_t><<<grid, kPostThreads, 0, s>>>(j);
-    else resid_kernel<float><<<grid, kPostThreads, 0, s>>>(j);
+    if (bf) resid_kernel<uint16_t><<<resid_grid, kPostThreads, 0, s>>>(j);
+    else resid_kernel<float><<<resid_grid, kPostThreads, 0, s>>>(j);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // The fp64 path's grid barriers need every CTA resident: a cooperative
