@@ -33,7 +33,8 @@ struct sv_handle {
     int tv_blocks = 1;     // resident total-variation CTAs per SM
     int *d_err = nullptr;
     unsigned *d_ctl = nullptr;
-    float *d_gtab = nullptr;
+    float *d_gtab = nullptr;      // [kGTab] G bounds of ordinary ids
+    uint64_t *d_skip = nullptr;   // [kSkipN] skip thresholds
     char *ws = nullptr;
     size_t ws_bytes = 0;
     unsigned *cnt = nullptr;  // completion counters: always zero between calls
@@ -46,10 +47,10 @@ struct sv_handle {
 
 namespace {
 
-// Upper bounds of G = -log(-log u), rounded up to fp32 with one more ulp of
-// slack: entry b < 256 bounds ids whose top 8 bits of u are b (u < (b+1)/256);
-// entry 256 + c bounds ids in the top bucket whose next 8 bits are c
-// (u < (65280 + c + 1)/65536).  The last entry of each level is +inf.
+// Upper bounds of G = -log(-log u) for ordinary ids, rounded up to fp32 with
+// one more ulp of slack: entry c bounds ids whose fine bits start with the
+// byte c, i.e. w < (c + 1)/256 and u = w 255/256 < (c + 1) 255 / 65536.  The
+// last entry bounds every ordinary id (u < 255/256).
 static float up_f32(double g)
 {
     float f = (float)g;
@@ -59,11 +60,46 @@ static float up_f32(double g)
 
 void gumbel_bound_table(float *t)
 {
-    for (int b = 0; b < kG8; ++b)
-        t[b] = (b == kG8 - 1) ? INFINITY : up_f32(-log(-log((double)(b + 1) / kG8)));
-    for (int c = 0; c < kG8; ++c)
-        t[kG8 + c] = (c == kG8 - 1) ? INFINITY
-                                    : up_f32(-log(-log((double)(65280 + c + 1) / 65536.0)));
+    for (int c = 0; c < kGTab; ++c)
+        t[c] = up_f32(-log(-log((double)(c + 1) * 255.0 / 65536.0)));
+}
+
+// Skip thresholds C_g = ceil(2^64 (255/256)^g), g = 1..256 (entry 0 unused):
+// 255^g as a little-endian byte string; C_g = 255^g * 256^(8-g) for g <= 8,
+// else 255^g / 256^(g-8) rounded up (its bytes below 256^(g-8) dropped).
+void skip_table(uint64_t *C)
+{
+    uint8_t n[272];
+    memset(n, 0, sizeof n);
+    n[0] = 1;
+    int len = 1;
+    C[0] = 0;
+    for (int g = 1; g <= 256; ++g) {
+        unsigned carry = 0;
+        for (int i = 0; i < len; ++i) {
+            const unsigned t = n[i] * 255u + carry;
+            n[i] = (uint8_t)(t & 255u);
+            carry = t >> 8;
+        }
+        while (carry) {
+            n[len++] = (uint8_t)(carry & 255u);
+            carry >>= 8;
+        }
+        uint64_t v = 0;
+        if (g <= 8) {
+            for (int i = len - 1; i >= 0; --i)
+                v = (v << 8) | n[i];
+            C[g] = v << (8 * (8 - g));
+        } else {
+            const int drop = g - 8;
+            bool rest = false;
+            for (int i = 0; i < drop && i < len; ++i)
+                rest |= n[i] != 0;
+            for (int i = len - 1; i >= drop; --i)
+                v = (v << 8) | n[i];
+            C[g] = v + (rest ? 1 : 0);
+        }
+    }
 }
 
 sv_status cuda_status(cudaError_t e)
@@ -167,6 +203,7 @@ void fill_common(Job &j, sv_handle *h, const void *src0, sv_dtype dt, int64_t rs
     j.err = h->d_err;
     j.ctl = h->d_ctl;
     j.gtab = h->d_gtab;
+    j.skip = h->d_skip;
     j.force_rescue = h->force_rescue;
     j.c1 = 1.4426950408889634f;
     j.eos = -1;
@@ -272,12 +309,16 @@ sv_status sv_create(sv_handle **out)
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_ctl, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_gtab, kGTab * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_skip, kSkipN * sizeof(uint64_t));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_ctl, 0, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) {
         float t[kGTab];
         gumbel_bound_table(t);
         e = cudaMemcpy(h->d_gtab, t, sizeof t, cudaMemcpyHostToDevice);
+        uint64_t c[kSkipN];
+        skip_table(c);
+        if (e == cudaSuccess) e = cudaMemcpy(h->d_skip, c, sizeof c, cudaMemcpyHostToDevice);
     }
     if (e != cudaSuccess) {
         sv_destroy(h);
@@ -296,6 +337,7 @@ sv_status sv_destroy(sv_handle *h)
     if (h->d_err) cudaFree(h->d_err);
     if (h->d_ctl) cudaFree(h->d_ctl);
     if (h->d_gtab) cudaFree(h->d_gtab);
+    if (h->d_skip) cudaFree(h->d_skip);
     delete h;
     return SV_OK;
 }

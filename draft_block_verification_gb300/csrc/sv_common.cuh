@@ -154,7 +154,7 @@ __device__ __forceinline__ double exact_logit_score(const Job &j, const char *ro
                                                     double T, int v)
 {
     float x = load_logit(j, row, v);
-    return (double)x / T + gumbel_of(uniform_at(key, (uint32_t)v));
+    return (double)x / T + gumbel64(fine52(key, (uint32_t)v), is_top(key, (uint32_t)v, j.skip));
 }
 
 // The best candidate's lower end beats every other upper end by > 1e-9.
@@ -185,11 +185,12 @@ static __device__ __noinline__ GRes resolve_logit_row(const Job &j, const char *
     Top2 t;
     t.init();
     for (int v = lane; v < j.V; v += 32) {
-        uint32_t b0 = (word_a((uint32_t)key, (uint32_t)v >> 2) >> (8u * (v & 3))) & 0xFFu;
-        float x = load_logit(j, row, v);
-        if (fmaf(x, invT, gup_of(j.gtab, key, (uint32_t)v, b0)) < thr)
+        const float x = load_logit(j, row, v);
+        const uint64_t m = fine52(key, (uint32_t)v);
+        const bool top = is_top(key, (uint32_t)v, j.skip);
+        if (!top && fmaf(x, invT, __ldg(j.gtab + (int)(m >> 44))) < thr)
             continue;
-        t.add((double)x / T + gumbel_of(u_of(bits52_of(key, (uint32_t)v, b0))), v);
+        t.add((double)x / T + gumbel64(m, top), v);
     }
     warp_top2(t);
     return GRes{t.i1, (t.s1 - t.s2 < kFlagEps) ? 1 : 0};

@@ -57,16 +57,14 @@ enum : int { M_ARGMAX = 1, M_LSE = 2, M_LSE2 = 4, M_GUMBEL = 8, M_MAX = 16 };
 enum : int { K_GREEDY = 0, K_SAMPLE = 1, K_TREE = 2, K_PACKED = 3 };
 
 // ---------------------------------------------------------------------------
-// Counter-based random numbers.  Written from the published definitions of
-// the two mixers: SplitMix64's output function (Steele, Lea & Flood) and the
-// MurmurHash3 32-bit finalizer (Appleby).
+// Counter-based random numbers, written from the published definition of
+// SplitMix64 (Steele, Lea & Flood): its output function, and its stream
+// (output n + 1 of the generator seeded with s is the output function of
+// s + n * 0x9E3779B97F4A7C15).
 //   key(seed, stream, seq, pos, iter): fold each field into a running 64-bit
-//     state through the SplitMix64 output function.
-//   For vocabulary id v the 52 random bits m are, most significant first:
-//     byte (v mod 4) of fmix32(low32(key) xor (v div 4) * 0x9E3779B9),
-//     byte (v mod 4) of fmix32(high32(key) xor (v div 4) * 0x85EBCA77),
-//     the top 36 bits of splitmix64(key xor v * 0xD1B54A32D192ED03);
-//   u = (2m + 1) 2^-53 (sv_gumbel.cuh).
+//     state through the output function.
+//   The uniforms of a row are read from the stream seeded with the row key
+//   (the layout is described in sv_gumbel.cuh).
 // ---------------------------------------------------------------------------
 __host__ __device__ __forceinline__ uint64_t splitmix_out(uint64_t state)
 {
@@ -79,16 +77,6 @@ __host__ __device__ __forceinline__ uint64_t splitmix_out(uint64_t state)
     return z;
 }
 
-__host__ __device__ __forceinline__ uint32_t murmur_fmix(uint32_t x)
-{
-    x ^= x >> 16;
-    x *= 0x85EBCA6Bu;
-    x ^= x >> 13;
-    x *= 0xC2B2AE35u;
-    x ^= x >> 16;
-    return x;
-}
-
 __host__ __device__ __forceinline__ uint64_t rng_key(uint64_t seed, uint32_t stream, uint64_t seq,
                                                      int64_t pos, uint64_t iter)
 {
@@ -97,12 +85,6 @@ __host__ __device__ __forceinline__ uint64_t rng_key(uint64_t seed, uint32_t str
     s = splitmix_out(s ^ seq);
     s = splitmix_out(s ^ (uint64_t)pos);
     return splitmix_out(s ^ iter);
-}
-
-// Standard Gumbel by inversion, fp64.
-__device__ __forceinline__ double gumbel_of(double u)
-{
-    return -log(-log(u));
 }
 
 // ---------------------------------------------------------------------------

@@ -1,69 +1,131 @@
-// sv_gumbel.cuh -- Gumbel-max over a vocabulary row with a three-level filter.
+// sv_gumbel.cuh -- the uniforms of a row and Gumbel-max over a vocabulary row.
 //
-// The sample is argmax_v s_v, s_v = z_v + G(key, v) (z = x/T for a logit row,
-// or the residual log-weight of [SPOT] App. B eq. 14), with G = -log(-log u)
-// ([SPOT] eq. 4, the Gumbel-argmax identity eqs. 5-7).  u's 52 random bits are
-// laid out so that a whole row can be screened cheaply:
-//   level 1: one 32-bit hash per 4 ids gives each id the top 8 bits of u,
-//            bounding G by a 256-entry table; a group of 4 is skipped unless
-//            one of its bytes is 0xFF or its largest logit can still reach
-//            the running threshold;
-//   level 2: survivors get G in fp32 with a proved interval, and s_v an
-//            interval [lo, hi];
-//   level 3: the two candidates with the largest upper ends are certified
-//            (lower end of the best > upper end of every other + 1e-9), or
-//            evaluated in fp64 when their intervals overlap.
+// Uniforms.  All randomness of a row is read from the SplitMix64 stream
+// seeded with the row key k (stream_at(k, n) = output n + 1).  The ids are
+// split into blocks of 256.  Which ids of a block fall into the top 1/256 of
+// the unit interval ("top" ids) is drawn as i.i.d. Bernoulli(1/256) trials by
+// geometric skipping: draw i of block b is M = stream_at(k, b * 2^16 + i); its
+// gap is the number of g in 1..256 with M < C_g, C_g = ceil(2^64 (255/256)^g)
+// (so P(gap >= g) = (255/256)^g to within 2^-64); the first top offset is
+// gap_0, each next one the previous plus 1 + gap_i.  The 52 fine bits of id v
+// are m = stream_at(k, 2^40 + v) >> 12, w = (2m + 1) / 2^53, and
+// u = w * 255/256 for an ordinary id, 1 - u = (1 - w) / 256 for a top id.
+//
+// Gumbel-max.  The sample is argmax_v s_v, s_v = z_v + G(v) (z = x/T for a
+// logit row, or the residual log-weight of [SPOT] App. B eq. 14), with
+// G = -log(-log u) ([SPOT] eq. 4, the Gumbel-argmax identity eqs. 5-7).  The
+// layout makes a row cheap to screen:
+//   top ids (about one per block) are found from a couple of draws per block
+//   and scored first, which gives a threshold close to the row's maximum;
+//   an ordinary id has G < G(255/256) = 5.5414..., so a vector of ids whose
+//   largest score bound stays below the threshold is skipped at once; ids of
+//   the few vectors that pass are bounded by the top byte of their fine bits
+//   (a 256-entry table), and survivors get G in fp32 with a proved interval;
+//   the two candidates with the largest upper ends are certified (lower end
+//   of the best > upper end of every other + 1e-9), or evaluated in fp64.
 #pragma once
 
 #include "sv_dev.cuh"
 
 namespace sv {
 
-constexpr int kG8 = 256;            // coarse table: G at the top of each 8-bit bucket
-constexpr int kGTab = 2 * kG8;      // + the 256 sub-buckets of the top bucket
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+constexpr int kGTab = 256;   // G bounds of an ordinary id by the top byte of its fine bits
+constexpr int kSkipN = 257;  // skip thresholds C_1..C_256 (entry 0 unused)
 // |G32 - G| bound for the fp32 evaluation below (about 8x the analysis: the
 // two lg2.approx calls and the argument rounding give under 2^-20; a GPU
 // self-test measures it).
 constexpr float kG32Err = 0x1p-17f;
 
-__device__ __forceinline__ uint32_t word_a(uint32_t klo, uint32_t j)
+__host__ __device__ __forceinline__ uint64_t stream_at(uint64_t key, uint64_t n)
 {
-    return murmur_fmix(klo ^ (j * 0x9E3779B9u));
-}
-__device__ __forceinline__ uint32_t word_b(uint32_t khi, uint32_t j)
-{
-    return murmur_fmix(khi ^ (j * 0x85EBCA77u));
+    return splitmix_out(key + n * kGamma);
 }
 
-// 52 random bits of id v whose top byte b0 is known.
-__device__ __forceinline__ uint64_t bits52_of(uint64_t key, uint32_t v, uint32_t b0)
+// The 52 fine bits of id v.
+__device__ __forceinline__ uint64_t fine52(uint64_t key, uint32_t v)
 {
-    uint32_t b1 = (word_b((uint32_t)(key >> 32), v >> 2) >> (8u * (v & 3u))) & 0xFFu;
-    uint64_t low = splitmix_out(key ^ ((uint64_t)v * 0xD1B54A32D192ED03ull)) >> 28;
-    return ((uint64_t)b0 << 44) | ((uint64_t)b1 << 36) | low;
-}
-__device__ __forceinline__ uint64_t bits52_full(uint64_t key, uint32_t v)
-{
-    uint32_t b0 = (word_a((uint32_t)key, v >> 2) >> (8u * (v & 3u))) & 0xFFu;
-    return bits52_of(key, v, b0);
-}
-__device__ __forceinline__ double u_of(uint64_t m)
-{
-    return (double)(2 * m + 1) * 0x1p-53;
-}
-__device__ __forceinline__ double uniform_at(uint64_t key, uint32_t v)
-{
-    return u_of(bits52_full(key, v));
+    return stream_at(key, (1ull << 40) + v) >> 12;
 }
 
-// Level-1 bound of G for id v: byte b0 of word a; if b0 == 255, the next
-// byte (word b) selects a sub-bucket.  The table is rounded up.
-__device__ __forceinline__ float gup_of(const float *tab, uint64_t key, uint32_t v, uint32_t b0)
+// Gap of a skip draw: the largest g in 0..256 with M < C_g (C decreasing,
+// C_0 taken as 2^64).  Estimated from log2 of u = M / 2^64 (g is about
+// log(u) / log(255/256)) and then corrected against the exact thresholds, so
+// the result is exact; the correction loops usually run zero times.
+__device__ __forceinline__ int skip_gap(uint64_t M, const uint64_t *__restrict__ C)
 {
-    if (b0 != 255u)
-        return tab[b0];
-    uint32_t b1 = (word_b((uint32_t)(key >> 32), v >> 2) >> (8u * (v & 3u))) & 0xFFu;
-    return tab[kG8 + b1];
+    float u = __uint2float_rn((uint32_t)(M >> 40)) * 0x1p-24f + 0x1p-25f;
+    float l2;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(u));
+    // 1 / log2(255/256) = -177.0989; u < 1 so the estimate is >= 0
+    int g = (int)fminf(l2 * -177.09888f, 256.f);
+    g = max(0, min(g, 256));
+    while (g < 256 && M < C[g + 1])
+        ++g;
+    while (g > 0 && M >= C[g])
+        --g;
+    return g;
+}
+
+// Offset of the next top id of block beta after draw i (pos: the previous
+// offset, -1 before the first draw).
+__device__ __forceinline__ int next_top(uint64_t key, uint32_t beta, int i, int pos,
+                                        const uint64_t *__restrict__ C)
+{
+    return pos + 1 + skip_gap(stream_at(key, ((uint64_t)beta << 16) | (uint32_t)i), C);
+}
+
+// Top ids among offsets o0 .. o0 + n - 1 of block beta, as a bit mask (n <= 32).
+__device__ __forceinline__ uint32_t top_mask(uint64_t key, uint32_t beta, int o0, int n,
+                                             const uint64_t *__restrict__ C)
+{
+    uint32_t msk = 0;
+    int pos = -1;
+    for (int i = 0; i < 257; ++i) {  // offsets grow by at least one per draw
+        pos = next_top(key, beta, i, pos, C);
+        if (pos >= o0 + n)
+            break;
+        if (pos >= o0)
+            msk |= 1u << (pos - o0);
+    }
+    return msk;
+}
+
+__device__ __forceinline__ bool is_top(uint64_t key, uint32_t v, const uint64_t *__restrict__ C)
+{
+    return top_mask(key, v >> 8, (int)(v & 255u), 1, C) != 0u;
+}
+
+// u and 1 - u as integers over 2^61 (both exact).
+__device__ __forceinline__ void u_parts(uint64_t m, bool top, uint64_t &un, uint64_t &dn)
+{
+    if (top) {
+        dn = (1ull << 53) - 2 * m - 1;
+        un = (1ull << 61) - dn;
+    } else {
+        un = 255ull * (2 * m + 1);
+        dn = (1ull << 61) - un;
+    }
+}
+
+// The uniform and the Gumbel value in fp64 (the same expressions as the
+// definition, so the values are reproducible bit for bit).
+__device__ __forceinline__ double uniform64(uint64_t m, bool top)
+{
+    const double w = (double)(2 * m + 1) * 0x1p-53;
+    return top ? 1.0 - (1.0 - w) / 256.0 : w * (255.0 / 256.0);
+}
+__device__ __forceinline__ double gumbel64(uint64_t m, bool top)
+{
+    const double w = (double)(2 * m + 1) * 0x1p-53;
+    if (top)
+        return -log(-log1p(-((1.0 - w) / 256.0)));
+    return -log(-log(w * (255.0 / 256.0)));
+}
+__device__ __forceinline__ double uniform_at(uint64_t key, uint32_t v,
+                                             const uint64_t *__restrict__ C)
+{
+    return uniform64(fine52(key, v), is_top(key, v, C));
 }
 
 __device__ __forceinline__ float lg2a(float x)
@@ -73,19 +135,21 @@ __device__ __forceinline__ float lg2a(float x)
     return y;
 }
 
-// G = -ln(E), E = -ln(u), u = (2m+1) 2^-53, in fp32.  For u < 3/4, E comes
-// from lg2 of u (u is exact to 2^-24).  For u >= 3/4, 1 - u is exact as the
-// integer 2^53 - 2m - 1 and E = -ln(1 - d) = 2 atanh(d / (2 - d)) by its odd
-// series in s = d/(2-d) <= 1/7, truncated after s^9 (relative error < 4e-10).
-__device__ __forceinline__ float gumbel32(uint64_t m)
+// G = -ln(E), E = -ln(u), in fp32.  For u < 3/4, E comes from lg2 of u (u is
+// exact to 2^-24).  For u >= 3/4, d = 1 - u is exact as an integer over 2^61
+// and E = -ln(1 - d) = 2 atanh(d / (2 - d)) by its odd series in
+// s = d/(2-d) <= 1/7, truncated after s^9 (relative error < 4e-10).
+__device__ __forceinline__ float gumbel32(uint64_t m, bool top)
 {
     const float ln2 = 0.693147180559945f;
+    uint64_t un, dn;
+    u_parts(m, top, un, dn);
     float E;
-    if (m < (3ull << 50)) {
-        float u = __ull2float_rn(2 * m + 1) * 0x1p-53f;
+    if (un < (3ull << 59)) {
+        float u = __ull2float_rn(un) * 0x1p-61f;
         E = -ln2 * lg2a(u);
     } else {
-        float d = __ull2float_rn((1ull << 53) - 2 * m - 1) * 0x1p-53f;
+        float d = __ull2float_rn(dn) * 0x1p-61f;
         float s = __fdiv_rn(d, 2.f - d);
         float s2 = s * s;
         float p = fmaf(s2, 1.f / 9.f, 1.f / 7.f);
@@ -97,8 +161,8 @@ __device__ __forceinline__ float gumbel32(uint64_t m)
     return -ln2 * lg2a(E);
 }
 
-// Largest finite entry of the coarse table (b0 = 254), for the group test.
-__device__ __forceinline__ float g8max(const float *tab) { return tab[kG8 - 2]; }
+// Bound of G over every ordinary id (the table's last entry).
+__device__ __forceinline__ float g_ordinary_max(const float *tab) { return tab[kGTab - 1]; }
 
 // Threshold used against level-1 (table) bounds: an fp32 bound ub of an
 // exact score satisfies exact <= ub + (|ub| + 40) 2^-21, so comparing ub with
@@ -163,13 +227,22 @@ __device__ __forceinline__ void warp_cand2(Cand2 &c)
 }
 
 // fp32 interval (lo, hi) of the Gumbel-perturbed logit x/T + G for id v with
-// top byte b0.  Out of line: it runs for a few ids per row, and inlining it
-// into the unrolled streaming loops would flood the instruction cache.
-static __device__ __noinline__ float2 logit_interval_at(float x, float invT, uint64_t key, uint32_t v,
-                                                        uint32_t b0)
+// fine bits m (top: whether v is a top id).
+__device__ __forceinline__ float2 logit_interval_m(float x, float invT, uint64_t m, bool top)
 {
     float z = x * invT;
-    float g = gumbel32(bits52_of(key, v, b0));
+    float g = gumbel32(m, top);
+    float s = z + g;
+    float e = (fabsf(z) + fabsf(s)) * 0x1p-21f + kG32Err;
+    return make_float2(s - e, s + e);
+}
+
+// The same for id v.  Out of line: it runs for a few ids per row.
+static __device__ __noinline__ float2 logit_interval_at(float x, float invT, uint64_t key, uint32_t v,
+                                                        bool top)
+{
+    float z = x * invT;
+    float g = gumbel32(fine52(key, v), top);
     float s = z + g;
     float e = (fabsf(z) + fabsf(s)) * 0x1p-21f + kG32Err;
     return make_float2(s - e, s + e);

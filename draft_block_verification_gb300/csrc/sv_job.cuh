@@ -105,7 +105,8 @@ struct Job {
     unsigned *rdone;    // [B * 64] per-entry chunk counters
     int resid_chunks;
     int *err;
-    const float *gtab;  // [kGTab] level-1 Gumbel bounds
+    const float *gtab;     // [kGTab] G bounds of ordinary ids
+    const uint64_t *skip;  // [kSkipN] skip thresholds of the top-id draws
 };
 
 // Row slot bookkeeping shared by the kernels.

@@ -26,7 +26,8 @@ namespace sv {
 
 constexpr int kFinQ = 32;      // decision steps queued per CTA
 constexpr int kUnitSlots = 8;  // units whose partials wait for the finalizer
-constexpr int kGQ = 64;        // queued Gumbel groups per consumer warp
+constexpr int kGQ = 64;        // queued Gumbel vectors per consumer warp
+constexpr int kSeedCap = 2048; // top ids gathered per seeding round
 
 struct RowMode {
     int mode;
@@ -44,7 +45,13 @@ struct StageMeta {
     int b;            // sequence of the unit
     unsigned expect;  // records that complete sequence b
     int xid;          // vocabulary id whose logit the unit records (-1: none)
-    int pad[3];
+    int vend;         // end (vector index) of the unit's part of the row
+    const char *row;  // the unit's logit row
+    // first stage: the next unit this CTA streams, if it carries a Gumbel-max
+    // (its top ids are prefetched while this unit streams)
+    const char *nrow;
+    uint64_t nkey;
+    int nrec, nlo, nhi, npad;
     RowMode rm;       // row mode of the unit
 };
 
@@ -68,10 +75,11 @@ struct PassShared {
     // still uses the slot that unit takes over.
     uint32_t thr[kStages];
     volatile int abort;
-    // Gumbel groups that passed level 1, per consumer warp: raw data and
-    // (first id, hash word)
+    // Gumbel vectors that passed level 1, per consumer warp: raw data and
+    // the vector's index in the row
     uint4 gqd[kConsumerWarps][kGQ];
-    uint2 gqm[kConsumerWarps][kGQ];
+    uint32_t gqv[kConsumerWarps][kGQ];
+    uint64_t skip[kSkipN];   // skip thresholds of the top-id draws
     // unit slots: consumer warps write their partials and arrive on ubar; the
     // finalizer merges them and arrives on ufree
     uint64_t ubar[kUnitSlots];
@@ -79,6 +87,13 @@ struct PassShared {
     WarpPart up[kUnitSlots][kConsumerWarps];
     int uunit[kUnitSlots], ub[kUnitSlots];
     unsigned uexpect[kUnitSlots];
+    // top ids of a unit being seeded, and their logits' 32-bit words (copied
+    // ahead, one unit early); buffer lu & 1 belongs to local unit lu
+    uint32_t seed_ids[2][kSeedCap];
+    uint32_t seed_x[2][kSeedCap];
+    int seed_cnt[2];     // ids listed in a buffer
+    int seed_n;
+    int seed_more;
     volatile int nunits;     // units this CTA streamed (set when the producer is done)
     volatile int prod_done;
     int todo[kFinQ];         // sequences whose decision step is due (finalizer only)
@@ -319,7 +334,6 @@ struct GState {
     Cand2 c;           // candidates
     float lomax;       // best lower end seen
     float thr, thrS;   // level-2 and level-1 thresholds
-    int seedv;         // the seed candidate (warp-uniform)
 };
 
 // Per-thread running state of one unit.
@@ -343,7 +357,6 @@ __device__ __forceinline__ void tstate_init(TState &s)
     s.g.c.init();
     s.g.lomax = -INFINITY;
     s.g.thr = s.g.thrS = s.pub = -INFINITY;
-    s.g.seedv = -1;
     s.gqn = 0;
     s.xd = __int_as_float(0x7FC00000);
 }
@@ -359,10 +372,10 @@ __device__ __forceinline__ void raise_thr(GState &s, float t)
 // Level 2: fp32 interval of x/T + G; candidates whose upper end reaches the
 // threshold are kept, and the best lower end raises the threshold (anything
 // below it - 1e-9 can neither win nor tie within 1e-9).
-__device__ __forceinline__ void gumbel_level2(float x, uint32_t v, uint32_t b0, GState &s,
+__device__ __forceinline__ void gumbel_level2(float x, uint32_t v, bool top, GState &s,
                                               const RowMode &rm)
 {
-    const float2 iv = logit_interval_at(x, rm.invT, rm.key, v, b0);
+    const float2 iv = logit_interval_at(x, rm.invT, rm.key, v, top);
     const float lo = iv.x, hi = iv.y;
     if (hi < s.thr)
         return;
@@ -486,71 +499,68 @@ __device__ __forceinline__ void max_chunk(const Chunk &q, int vbase, TState &s)
     s.mx = fmaxf(s.mx, cm);
 }
 
-// Level 1, per id, of the queued groups: the bound of G from the id's top
-// byte (and for a 0xFF top byte from its second byte); ids whose bound can
-// reach the threshold get the fp32 interval of level 2.  The warp takes the
-// queue 32 groups at a time, a group per lane.
+// Per-id screen of the queued vectors, 32 at a time, a vector per lane: its
+// top ids are skipped (the seeding warp scored every top id of the unit);
+// an ordinary id is bounded by the top byte of its fine bits, and survivors
+// get the fp32 interval of level 2.
 template <typename In>
-__device__ __noinline__ GState gumbel_flush(uint4 *__restrict__ qd, uint2 *__restrict__ qm, int n,
-                                            GState s, const RowMode &rm,
-                                            const float *__restrict__ gt)
+__device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
+                                            const uint32_t *__restrict__ qv, int n, GState s,
+                                            const RowMode &rm, const float *__restrict__ gt,
+                                            const uint64_t *__restrict__ skip)
 {
     using VT = VecTraits<In>;
+    constexpr int E = VT::N;
     __syncwarp();
     for (int i = (int)(threadIdx.x & 31); i < n; i += 32) {
         const uint4 d = qd[i];
-        const uint2 mw = qm[i];
+        const uint32_t v0 = qv[i] * E;
+        const uint32_t tm = top_mask(rm.key, v0 >> 8, (int)(v0 & 255u), E, skip);
 #pragma unroll 1
-        for (int e = 0; e < 4; ++e) {
-            const uint32_t v = mw.x + e;
-            const uint32_t b0 = (mw.y >> (8 * e)) & 0xFFu;
-            const float x = VT::gelem(d, e);
-            if ((int)v != s.seedv && fmaf(x, rm.invT, gup_of(gt, rm.key, v, b0)) >= s.thrS)
-                gumbel_level2(x, v, b0, s, rm);
+        for (int e = 0; e < E; ++e) {
+            if ((tm >> e) & 1u)
+                continue;
+            const uint32_t v = v0 + e;
+            const float x = VT::elem(d, e);
+            const uint64_t m = fine52(rm.key, v);
+            if (fmaf(x, rm.invT, gt[(int)(m >> 44)]) >= s.thrS)
+                gumbel_level2(x, v, false, s, rm);
         }
     }
     __syncwarp();
     return s;
 }
 
-// Level 1 on groups of 4 ids: one hash word; a group is queued only if a
-// byte is 0xFF (unbounded bucket) or its vector's largest logit can reach the
-// threshold with the largest finite bucket bound.  The queue is compacted
-// with a ballot, so a warp does not diverge per group.
+// Level 1 on whole vectors: an ordinary id's G stays below the table's last
+// entry, so a vector is queued only if its largest logit can reach the
+// threshold with that bound.  The queue is compacted with a ballot, so a warp
+// does not diverge per vector.
 template <typename In>
 __device__ __forceinline__ void gumbel_chunk(const Chunk &q, int nv, int vbase, TState &s,
                                              const RowMode &rm, const float *__restrict__ gt,
-                                             PassShared &sm)
+                                             const uint64_t *__restrict__ skip, PassShared &sm)
 {
     using VT = VecTraits<In>;
-    constexpr int E = VT::N, G = E / 4;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const uint32_t klo = (uint32_t)rm.key;
-    const float gmax = g8max(gt);
+    const float gmax = g_ordinary_max(gt);
     uint4 *qd = sm.gqd[w];
-    uint2 *qm = sm.gqm[w];
+    uint32_t *qv = sm.gqv[w];
 #pragma unroll
     for (int k = 0; k < kVecsPerThread; ++k) {
         const int idx = t + k * kConsumers;
-        const uint32_t j0 = (uint32_t)(vbase + idx) * G;
-        const bool hot = fmaf(VT::hi_of(VT::pmax(q[k])), rm.invT, gmax) >= s.g.thrS;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const uint32_t wa = word_a(klo, j0 + g);
-            const bool top = ((~wa - 0x01010101u) & wa & 0x80808080u) != 0u;
-            const bool pass = (top || hot) && idx < nv;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
-            if (bal) {
-                if (pass) {
-                    const int r = s.gqn + __popc(bal & ((1u << lane) - 1u));
-                    qd[r] = VT::group_data(q[k], g);
-                    qm[r] = make_uint2((j0 + g) * 4u, wa);
-                }
-                s.gqn += __popc(bal);
-                if (s.gqn > kGQ - 32) {
-                    s.g = gumbel_flush<In>(qd, qm, s.gqn, s.g, rm, gt);
-                    s.gqn = 0;
-                }
+        const bool pass =
+            fmaf(VT::hi_of(VT::pmax(q[k])), rm.invT, gmax) >= s.g.thrS && idx < nv;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+        if (bal) {
+            if (pass) {
+                const int r = s.gqn + __popc(bal & ((1u << lane) - 1u));
+                qd[r] = q[k];
+                qv[r] = (uint32_t)(vbase + idx);
+            }
+            s.gqn += __popc(bal);
+            if (s.gqn > kGQ - 32) {
+                s.g = gumbel_flush<In>(qd, qv, s.gqn, s.g, rm, gt, skip);
+                s.gqn = 0;
             }
         }
     }
@@ -570,61 +580,7 @@ __device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, i
     if (MODE & M_LSE2)
         lse_chunk<In>(q, rm.c2, s.e2, s.acc2);
     if (MODE & M_GUMBEL)
-        gumbel_chunk<In>(q, nv, vbase, s, rm, gt, sm);
-}
-
-// First stage of a Gumbel unit: each warp scores in fp32 the element with the
-// largest table bound among the first vector of each lane and starts from its
-// lower end (a rigorous lower bound of the unit's maximum), published to the
-// other warps.  The seed id is known to the whole warp, which keeps it out of
-// the queue.
-template <typename In>
-__device__ __forceinline__ void gumbel_seed(const uint4 *__restrict__ st, int nv, int vbase,
-                                            TState &s, const RowMode &rm,
-                                            const float *__restrict__ gt, PassShared &sm,
-                                            int slot)
-{
-    using VT = VecTraits<In>;
-    constexpr int E = VT::N, G = E / 4;
-    const int t = threadIdx.x;
-    const uint32_t klo = (uint32_t)rm.key;
-    float bub = -INFINITY, bx = 0.f;
-    int bv = -1;
-    uint32_t bb0 = 0;
-    if (t < nv) {
-        const uint4 q = st[t];
-        const uint32_t j0 = (uint32_t)(vbase + t) * G;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const uint32_t wa = word_a(klo, j0 + g);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t b0 = (wa >> (8 * e)) & 0xFFu;
-                const float x = VT::elem(q, 4 * g + e);
-                const float ub = fmaf(x, rm.invT, gt[b0]);  // +inf for a 0xFF byte
-                if (ub > bub) {
-                    bub = ub;
-                    bv = (int)((j0 + g) * 4u + e);
-                    bx = x;
-                    bb0 = b0;
-                }
-            }
-        }
-    }
-    float wv = bub;
-    int wi = bv;
-    warp_argmax(wv, wi);
-    s.g.seedv = wi;
-    if (bv >= 0 && bv == wi) {
-        const float2 iv = logit_interval_at(bx, rm.invT, rm.key, (uint32_t)bv, bb0);
-        const float lo = iv.x, hi = iv.y;
-        s.g.c.add(lo, hi, bv);
-        s.g.lomax = lo;
-        raise_thr(s.g, __fsub_rd(lo, 1e-9f));
-        atomicMax(&sm.thr[slot], f2ord(s.g.thr));
-    }
-    __syncwarp();
-    raise_thr(s.g, ord2f(*(volatile uint32_t *)&sm.thr[slot]));
+        gumbel_chunk<In>(q, nv, vbase, s, rm, gt, sm.skip, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -692,7 +648,7 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
         double rel = 1.01 * (ep + eq) + 0x1p-21 + 1e-13;
         double alo = alpha_of(j.amode, r * (1.0 - rel), j.lam);
         double ahi = alpha_of(j.amode, r * (1.0 + rel), j.lam);
-        double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0);
+        double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
         acc = u < alo - kFlagEps;
         bool rej = u >= ahi + kFlagEps;
         und = !(acc || rej) || j.force_rescue;
@@ -952,7 +908,7 @@ static __device__ __noinline__ void fin_packed(const Job &j, int b)
         double r = (double)exp_fast(lp - lq);
         double rel = 1.01 * ep + 0x1p-21 + 0x1p-22 * (1.0 + fabs(lq)) + 1e-13;
         double alo = fmin(1.0, r * (1.0 - rel)), ahi = fmin(1.0, r * (1.0 + rel));
-        double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0);
+        double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
         acc = u < alo - kFlagEps;
         und = !(acc || u >= ahi + kFlagEps) || j.force_rescue;
         if (j.force_rescue)
@@ -1232,12 +1188,193 @@ __device__ void finalizer_loop(const Job &j, PassShared &sm)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Seeding of Gumbel units by the consumer threads.  Every top id of a unit's
+// id range is found (a couple of skip draws per block of 256 ids; threads take
+// blocks in turn and list the ids in shared memory), its logit is copied to
+// shared memory (cp.async, issued one unit ahead when the producer names the
+// next unit), and it is scored in an fp32 interval.  The top ids join the
+// candidates and the best lower end - 1e-9 starts the unit's shared
+// threshold; the consumers' scan then skips top ids.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// The aligned 32-bit word that holds the logit of id v, and the logit in it.
+template <typename In>
+__device__ __forceinline__ const void *logit_word(const char *row, uint32_t v)
+{
+    return row + (sizeof(In) == 2 ? (((size_t)v * 2) & ~(size_t)3) : (size_t)v * 4);
+}
+template <typename In>
+__device__ __forceinline__ float logit_of_word(uint32_t w, uint32_t v)
+{
+    if (sizeof(In) == 2)
+        return __uint_as_float((v & 1u) ? (w & 0xFFFF0000u) : (w << 16));
+    return __uint_as_float(w);
+}
+
+// Lists the top ids of [lo, hi) in buffer b; false if they did not all fit
+// (the count is then larger than the list).  Every consumer thread calls it.
+__device__ __noinline__ bool seed_list(PassShared &sm, int b, uint64_t key, int lo, int hi)
+{
+    const int t = threadIdx.x;
+    if (t == 0)
+        sm.seed_n = 0;
+    named_sync(1, kConsumers);
+    const uint32_t bhi = (uint32_t)(hi - 1) >> 8;
+    uint32_t beta = ((uint32_t)lo >> 8) + t;
+    int pos = -1, i = 0;
+    while (beta <= bhi) {
+        pos = next_top(key, beta, i++, pos, sm.skip);
+        const uint32_t v = beta * 256u + (uint32_t)pos;
+        if (pos > 255 || v >= (uint32_t)hi) {  // block done
+            beta += kConsumers;
+            pos = -1;
+            i = 0;
+        } else if (v >= (uint32_t)lo) {
+            const int idx = atomicAdd(&sm.seed_n, 1);
+            if (idx < kSeedCap)
+                sm.seed_ids[b][idx] = v;
+        }
+    }
+    named_sync(1, kConsumers);
+    const int n = sm.seed_n;
+    if (t == 0)
+        sm.seed_cnt[b] = min(n, kSeedCap);
+    return n <= kSeedCap;
+}
+
+// Starts the copies of the listed ids' logit words into buffer b.
+template <typename In>
+__device__ __forceinline__ void seed_copy(PassShared &sm, int b, const char *row)
+{
+    const int n = min(sm.seed_n, kSeedCap);
+    for (int e = threadIdx.x; e < n; e += kConsumers)
+        cp_async4(&sm.seed_x[b][e], logit_word<In>(row, sm.seed_ids[b][e]));
+    cp_async_commit();
+}
+
+// Scores buffer b (its copies must have been started) and starts the unit's
+// threshold.
+template <typename In>
+__device__ __noinline__ GState seed_eval(PassShared &sm, int b, GState g, const RowMode &rm,
+                                         int tslot)
+{
+    cp_async_wait_all();
+    named_sync(1, kConsumers);  // every thread's copies have landed
+    const int n = sm.seed_cnt[b];
+    for (int e = threadIdx.x; e < n; e += kConsumers) {
+        const uint32_t v = sm.seed_ids[b][e];
+        const float2 iv = logit_interval_m(logit_of_word<In>(sm.seed_x[b][e], v), rm.invT,
+                                           fine52(rm.key, v), true);
+        g.c.add(iv.x, iv.y, (int)v);
+        if (iv.x > g.lomax) {
+            g.lomax = iv.x;
+            raise_thr(g, __fsub_rd(iv.x, 1e-9f));
+        }
+    }
+    atomicMax(&sm.thr[tslot], f2ord(g.thr));
+    named_sync(1, kConsumers);
+    raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
+    return g;
+}
+
+// Seeding without a prefetched list: in rounds of at most kSeedCap ids,
+// loading the logits directly (the fallback for units with more top ids than
+// a list holds).
+template <typename In>
+__device__ __noinline__ GState seed_rounds(PassShared &sm, int b, const char *row, int lo, int hi,
+                                           GState g, const RowMode &rm, int tslot)
+{
+    using VT = VecTraits<In>;
+    constexpr uint32_t kNone = 0xFFFFFFFFu;
+    constexpr int kPer = kSeedCap / kConsumers;
+    const int t = threadIdx.x;
+    const uint32_t bhi = (uint32_t)(hi - 1) >> 8;
+    uint32_t beta = ((uint32_t)lo >> 8) + t;
+    int pos = -1, i = 0;
+    bool more = beta <= bhi;
+    uint32_t pend = kNone;  // a top id found but not listed yet
+    for (;;) {
+        if (t == 0) {
+            sm.seed_n = 0;
+            sm.seed_more = 0;
+        }
+        named_sync(1, kConsumers);
+        for (;;) {
+            if (pend != kNone) {
+                const int idx = atomicAdd(&sm.seed_n, 1);
+                if (idx >= kSeedCap)
+                    break;  // the list is full: keep it for the next round
+                sm.seed_ids[b][idx] = pend;
+                pend = kNone;
+            }
+            if (!more)
+                break;
+            pos = next_top(rm.key, beta, i++, pos, sm.skip);
+            const uint32_t v = beta * 256u + (uint32_t)pos;
+            if (pos > 255 || v >= (uint32_t)hi) {  // block done
+                beta += kConsumers;
+                pos = -1;
+                i = 0;
+                more = beta <= bhi;
+            } else if (v >= (uint32_t)lo) {
+                pend = v;
+            }
+        }
+        if (more || pend != kNone)
+            sm.seed_more = 1;
+        named_sync(1, kConsumers);
+        const int n = min(sm.seed_n, kSeedCap);
+        uint32_t id[kPer];
+        float x[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int e = t + k * kConsumers;
+            id[k] = e < n ? sm.seed_ids[b][e] : kNone;
+            x[k] = id[k] != kNone ? VT::load1(row, (int)id[k]) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+            if (id[k] != kNone) {
+                const float2 iv =
+                    logit_interval_m(x[k], rm.invT, fine52(rm.key, id[k]), true);
+                g.c.add(iv.x, iv.y, (int)id[k]);
+                if (iv.x > g.lomax) {
+                    g.lomax = iv.x;
+                    raise_thr(g, __fsub_rd(iv.x, 1e-9f));
+                }
+            }
+        const int again = sm.seed_more;
+        named_sync(1, kConsumers);  // the list is reused by the next round
+        if (!again)
+            break;
+    }
+    atomicMax(&sm.thr[tslot], f2ord(g.thr));
+    named_sync(1, kConsumers);
+    raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
+    return g;
+}
+
 // Streams one unit whose first stage is ready in `stage`: every stage of the
 // unit with the row mode fixed at compile time, then the unit's partial.
 // Returns false if a wait timed out or the producer aborted.
 template <typename In, int MODE>
-__device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, const float *gt,
-                          int &stage, uint32_t &phase, const RowMode &rm)
+__device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages,
+                                          const float *gt, int &stage, uint32_t &phase,
+                                          const RowMode &rm, int &pf_next)
 {
     const int lane = threadIdx.x & 31;
     const StageMeta &m0 = sm.meta[stage];
@@ -1245,16 +1382,35 @@ __device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, c
     const int tslot = uh.lu % kStages;
     TState s;
     tstate_init(s);
-    bool first = true;
+    constexpr int E = VecTraits<In>::N;
+    const int sb = uh.lu & 1;  // this unit's seed buffer
+    if (MODE & M_GUMBEL) {
+        if (pf_next == uh.unit) {
+            s.g = seed_eval<In>(sm, sb, s.g, rm, tslot);  // listed and copied a unit ago
+        } else if (seed_list(sm, sb, rm.key, m0.vbase * E, m0.vend * E)) {
+            seed_copy<In>(sm, sb, m0.row);
+            s.g = seed_eval<In>(sm, sb, s.g, rm, tslot);
+        } else {
+            s.g = seed_rounds<In>(sm, sb, m0.row, m0.vbase * E, m0.vend * E, s.g, rm, tslot);
+        }
+    }
+    if (m0.nrec >= 0) {
+        // the next unit carries a Gumbel-max: list its top ids and start
+        // their copies now, so that they land while this unit streams
+        const int nb = sb ^ 1;
+        const bool fits = seed_list(sm, nb, m0.nkey, m0.nlo, m0.nhi);
+        if (fits)
+            seed_copy<In>(sm, nb, m0.nrow);
+        pf_next = fits ? m0.nrec : -1;  // the same on every consumer thread
+    } else {
+        pf_next = -1;
+    }
     for (;;) {
         const StageMeta &mt = sm.meta[stage];
         const int nv = mt.nv, vbase = mt.vbase, last = mt.last;
         const uint4 *st = reinterpret_cast<const uint4 *>(stages + (size_t)stage * kStageBytes);
-        if (MODE & M_GUMBEL) {
+        if (MODE & M_GUMBEL)
             raise_thr(s.g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
-            if (first)
-                gumbel_seed<In>(st, nv, vbase, s, rm, gt, sm, tslot);
-        }
         do_chunk<In, MODE>(st, nv, vbase, s, rm, gt, sm);
         if (uh.xid >= 0) {
             // the thread that holds the draft token's vector records its logit
@@ -1276,7 +1432,6 @@ __device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, c
         }
         if (last)
             break;
-        first = false;
         if (!mbar_wait(&sm.full[stage], phase)) {
             latch(j.err, SV_ERR_TIMEOUT);
             return false;
@@ -1286,7 +1441,7 @@ __device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, c
     }
     if ((MODE & M_GUMBEL) && s.gqn > 0) {
         const int w = threadIdx.x >> 5;
-        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqm[w], s.gqn, s.g, rm, gt);
+        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqv[w], s.gqn, s.g, rm, gt, sm.skip);
         s.gqn = 0;
     }
     finish_unit(j, uh, s, rm, sm);
@@ -1297,32 +1452,32 @@ __device__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages, c
 template <typename In, int KIND>
 __device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsigned char *stages,
                                               const float *gt, int &stage, uint32_t &phase,
-                                              const RowMode &rm)
+                                              const RowMode &rm, int &pf_next)
 {
     const int m = rm.mode;
     if constexpr (KIND == K_GREEDY) {
-        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
     } else if constexpr (KIND == K_SAMPLE) {
         if (m & M_GUMBEL)
-            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
-        return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
+            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
+        return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
     } else if constexpr (KIND == K_TREE) {
         if (m & M_GUMBEL)
-            return unit_loop<In, M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
-        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
+            return unit_loop<In, M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
     } else {
         switch (m) {
-        case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
-        case M_LSE: return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
+        case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+        case M_LSE: return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
         case M_LSE | M_GUMBEL:
-            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
+            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
         case M_ARGMAX | M_LSE:
-            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm);
+            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
         case M_GUMBEL | M_LSE | M_MAX:
-            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm);
+            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
         default:
             return unit_loop<In, M_GUMBEL | M_LSE | M_LSE2 | M_MAX>(j, sm, stages, gt, stage,
-                                                                     phase, rm);
+                                                                     phase, rm, pf_next);
         }
     }
 }
@@ -1355,6 +1510,9 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
     }
     for (int i = t; i < kGTab; i += blockDim.x)
         gt[i] = __ldg(j.gtab + i);
+    if (j.skip)
+        for (int i = t; i < kSkipN; i += blockDim.x)
+            sm.skip[i] = __ldg(j.skip + i);
     __syncthreads();
 
     if (t >= kConsumers + 32) {
@@ -1362,26 +1520,39 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         finalizer_loop<KIND>(j, sm);
     } else if (t >= kConsumers) {
         // ---------------- producer warp ----------------
-        // Lane 0 streams unit `cur` while the next unit's index and per-
-        // sequence values are already in flight.
+        // Lane 0 streams unit `cu`.  Two units are prepared ahead: the next
+        // unit's info is ready while this one streams (its per-sequence values
+        // were loaded a unit earlier), so the first stage can name it.
         if (t == kConsumers) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t pend = 0, pend_par = 0;  // stages with a copy not yet re-acquired
             int lu = 0;                       // local unit number
             bool ok = true;
+            const int E = j.dtype == SV_BF16 ? 8 : 4;
             long long cu = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
             long long nu = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
-            UnitPre cp = unit_prefetch(j, cu);
+            const UnitPre cp0 = unit_prefetch(j, cu);
+            UnitPre np = unit_prefetch(j, nu);
+            long long nnu = nu < j.total_units ? (long long)atomicAdd(j.ctl + C_UNIT, 1u) : nu;
+            UnitInfo ci;
+            ci.valid = false;
+            if (cu < j.total_units)
+                ci = unit_info(j, cu, cp0);
             while (cu < j.total_units) {
-                const UnitPre np = unit_prefetch(j, nu);  // consumed next round
-                const long long nn = nu < j.total_units ? (long long)atomicAdd(j.ctl + C_UNIT, 1u)
-                                                        : nu;
-                const UnitInfo ui = unit_info(j, cu, cp);
-                if (ui.valid) {
-                    const char *row = slot_row(j, ui.b, ui.slot);
-                    const int vs = ui.part * j.part_vecs;
+                UnitInfo ni;
+                ni.valid = false;
+                if (nu < j.total_units)
+                    ni = unit_info(j, nu, np);
+                const UnitPre nnp = unit_prefetch(j, nnu);
+                const long long n3 =
+                    nnu < j.total_units ? (long long)atomicAdd(j.ctl + C_UNIT, 1u) : nnu;
+                if (ci.valid) {
+                    const char *row = slot_row(j, ci.b, ci.slot);
+                    const int vs = ci.part * j.part_vecs;
                     const int ve = min(j.nvec, vs + j.part_vecs);
+                    // the next streamed unit (the next valid one) if it seeds
+                    const bool nseed = ni.valid && (ni.rm.mode & M_GUMBEL);
                     for (int v = vs; v < ve; v += kStageVecs) {
                         const int nv = min(kStageVecs, ve - v);
                         if (!mbar_wait(&sm.empty[stage], phase ^ 1u)) {
@@ -1390,18 +1561,30 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
                         }
                         pend &= ~(1u << stage);  // the consumers released it: its copy landed
                         StageMeta &mt = sm.meta[stage];
-                        mt.unit = ui.rec;
+                        mt.unit = ci.rec;
                         mt.nv = nv;
                         mt.vbase = v;
                         mt.first = (v == vs);
                         mt.last = (v + kStageVecs >= ve);
                         mt.lu = lu;
-                        mt.b = ui.b;
-                        mt.expect = ui.expect;
-                        mt.xid = ui.xid;
-                        mt.rm = ui.rm;
-                        if (v == vs)
+                        mt.b = ci.b;
+                        mt.expect = ci.expect;
+                        mt.xid = ci.xid;
+                        mt.row = row;
+                        mt.vend = ve;
+                        mt.rm = ci.rm;
+                        mt.nrec = -1;
+                        if (v == vs) {
                             sm.thr[lu % kStages] = f2ord(-INFINITY);
+                            if (nseed) {
+                                const int nvs = ni.part * j.part_vecs;
+                                mt.nrec = ni.rec;
+                                mt.nrow = slot_row(j, ni.b, ni.slot);
+                                mt.nkey = ni.rm.key;
+                                mt.nlo = nvs * E;
+                                mt.nhi = min(j.nvec, nvs + j.part_vecs) * E;
+                            }
+                        }
                         mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
                         bulk_g2s(stages + (size_t)stage * kStageBytes, row + (int64_t)v * 16,
                                  (uint32_t)nv * 16u, &sm.full[stage]);
@@ -1416,9 +1599,11 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
                         break;
                     ++lu;
                 }
+                ci = ni;
                 cu = nu;
-                cp = np;
-                nu = nn;
+                nu = nnu;
+                np = nnp;
+                nnu = n3;
             }
             if (ok && mbar_wait(&sm.empty[stage], phase ^ 1u)) {
                 pend &= ~(1u << stage);
@@ -1446,6 +1631,7 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         // ---------------- consumer warps ----------------
         int stage = 0;
         uint32_t phase = 0;
+        int pf_next = -1;  // record of the next unit whose top ids were prefetched
         for (;;) {
             if (!mbar_wait(&sm.full[stage], phase)) {
                 latch(j.err, SV_ERR_TIMEOUT);
@@ -1454,9 +1640,10 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             if (sm.meta[stage].unit < 0 || sm.abort)
                 break;
             const RowMode rm = sm.meta[stage].rm;
-            if (!unit_dispatch<In, KIND>(j, sm, stages, gt, stage, phase, rm))
+            if (!unit_dispatch<In, KIND>(j, sm, stages, gt, stage, phase, rm, pf_next))
                 break;
         }
+        cp_async_wait_all();  // no copy may be in flight when the CTA exits
     }
     __syncthreads();
     if (t == 0) {

@@ -268,14 +268,14 @@ struct RCtx {
 // fp64 interval of the residual score of id v (Delta bracket only); false
 // when w_v = 0 for every Delta in the bracket.
 __device__ __forceinline__ bool resid_interval64(const RCtx &c, float x, float y, uint64_t m,
-                                                 double &lo, double &hi)
+                                                 bool top, double &lo, double &hi)
 {
     double z = (double)x / c.Tp, w = (double)y / c.Tq;
     double ah = w - z - c.dhi;
     if (!(ah < 0.0))
         return false;
     double al = w - z - c.dlo;
-    double G = gumbel_of(u_of(m));
+    double G = gumbel64(m, top);
     hi = z + log1mexp(ah) + G;
     lo = (al < 0.0) ? z + log1mexp(al) + G : -INFINITY;
     return true;
@@ -296,7 +296,7 @@ __device__ __forceinline__ float log1mexp32(float d, float &err)
 
 // fp32 interval of the residual score; false when w_v = 0 for sure.
 __device__ __forceinline__ bool resid_interval32(const RCtx &c, float x, float y, uint64_t m,
-                                                 float &lo, float &hi)
+                                                 bool top, float &lo, float &hi)
 {
     const float z = x * c.invTp, w = y * c.invTq;
     const float dz = w - z;
@@ -305,7 +305,7 @@ __device__ __forceinline__ bool resid_interval32(const RCtx &c, float x, float y
     const float dmax = (dz - c.dlo32) + edz + fabsf(dz - c.dlo32) * 0x1p-22f;  // largest d
     if (dmin >= 0.f)
         return false;
-    const float g = gumbel32(m);
+    const float g = gumbel32(m, top);
     float e1, lwh;
     const float lw1 = log1mexp32(dmin, e1);
     if (1.f - ex2f(dmin * 1.44269504088896f) > 0x1p-18f && e1 < 1.f)
@@ -352,11 +352,12 @@ struct Track32 {
             thrS = level1_thr(t);
         }
     }
-    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint32_t b0)
+    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint64_t m,
+                                        bool top)
     {
         if (surely_zero(ctx, x, y)) return;
         float lo, hi;
-        if (!resid_interval32(ctx, x, y, bits52_of(ctx.key, v, b0), lo, hi) || hi < thr) return;
+        if (!resid_interval32(ctx, x, y, m, top, lo, hi) || hi < thr) return;
         c.add(lo, hi, (int)v);
         if (lo > lomax) {
             lomax = lo;
@@ -379,11 +380,12 @@ struct Track64 {
             thrS = level1_thr(t);
         }
     }
-    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint32_t b0)
+    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint64_t m,
+                                        bool top)
     {
         if (surely_zero(ctx, x, y)) return;
         double lo, hi;
-        if (!resid_interval64(ctx, x, y, bits52_of(ctx.key, v, b0), lo, hi)) return;
+        if (!resid_interval64(ctx, x, y, m, top, lo, hi)) return;
         r.add(lo, hi, (int)v);
         if (lo > -INFINITY && (float)lo > lomax) {
             lomax = __double2float_rd(lo);
@@ -451,83 +453,65 @@ __device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out
     }
 }
 
-// Level 1 per id and level 2 for one vector whose group test passed.
+// Per-id screen of one vector whose bound reached the threshold: top ids are
+// skipped (the seed phase scored every top id of the chunk); an ordinary id
+// is bounded by the top byte of its fine bits.
 template <typename In, typename Tr>
 __device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, int k,
-                                             const uint32_t (&was)[VecTraits<In>::N / 4],
-                                             int seedv, const float *gt, Tr &tr)
+                                             const float *gt, const uint64_t *skip, Tr &tr)
 {
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
     const uint32_t v0 = (uint32_t)k * E;
-    float x[E], y[E];
-    VT::unpack(qx, x);
-    VT::unpack(ldv<In>(c.qrow, k), y);
+    const uint32_t tm = top_mask(c.key, v0 >> 8, (int)(v0 & 255u), E, skip);
+    const uint4 qy = ldv<In>(c.qrow, k);
 #pragma unroll 1
     for (int i = 0; i < E; ++i) {
-        const int g = i >> 2, e = i & 3;
-        const uint32_t v = v0 + i, b0 = (was[g] >> (8 * e)) & 0xFFu;
-        if ((int)v == seedv) continue;
+        if ((tm >> i) & 1u)
+            continue;
+        const uint32_t v = v0 + i;
         const float xi = VT::elem(qx, i);
-        if (fmaf(xi, c.invTp, gup_of(gt, c.key, v, b0)) < tr.thrS) continue;
-        tr.add(c, xi, VT::elem(ldv<In>(c.qrow, k), i), v, b0);
+        const uint64_t m = fine52(c.key, v);
+        if (fmaf(xi, c.invTp, gt[(int)(m >> 44)]) < tr.thrS)
+            continue;
+        tr.add(c, xi, VT::elem(qy, i), v, m, false);
     }
 }
 
-// Scan vectors [vb, ve) of the pair.  Seed: each warp adds the element with
-// the largest table bound among clearly positive weights (p > 1.07 q) of its
-// threads' first vectors; the CTA starts from the best threshold.
+// Scan vectors [vb, ve) of the pair.  Seed: the CTA scores every top id of
+// the chunk first (a couple of skip draws per block of 256 ids), which sets a
+// threshold close to the chunk's best; then each vector whose largest logit
+// can reach it with the ordinary-id bound is screened per id.  (Scores drop
+// the common -Lp, and log w <= x/T - Lp, so x/T + G bounds a score.)
 template <typename In, typename Tr>
-__device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, PostShared &sm, Tr &tr)
+__device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const uint64_t *skip,
+                           PostShared &sm, Tr &tr)
 {
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
-    const uint32_t klo = (uint32_t)c.key;
     tr.init();
-    int seedv = -1;
+    if (threadIdx.x == 0) sm.thr = f2ord(-INFINITY);
+    __syncthreads();
     {
-        float bub = -INFINITY, bx = 0.f, by = 0.f;
-        int bv = -1;
-        uint32_t bb0 = 0;
-        int k = vb + threadIdx.x;
-        if (k < ve) {
-            float x[E], y[E];
-            VT::unpack(ldv<In>(c.prow, k), x);
-            VT::unpack(ldv<In>(c.qrow, k), y);
-            uint32_t v0 = (uint32_t)k * E;
-#pragma unroll
-            for (int g = 0; g < E / 4; ++g) {
-                uint32_t wa = word_a(klo, (v0 >> 2) + g);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float xv = x[4 * g + e], yv = y[4 * g + e];
-                    if (yv * c.invTq - xv * c.invTp - c.dhi32 > -0.07f) continue;
-                    uint32_t v = v0 + 4 * g + e, b0 = (wa >> (8 * e)) & 0xFFu;
-                    float ub = fmaf(xv, c.invTp, gup_of(gt, c.key, v, b0));
-                    if (ub > bub) {
-                        bub = ub;
-                        bv = (int)v;
-                        bx = xv;
-                        by = yv;
-                        bb0 = b0;
-                    }
-                }
+        const uint32_t lo = (uint32_t)vb * E, hi = (uint32_t)ve * E;
+        for (uint32_t beta = (lo >> 8) + threadIdx.x; beta <= ((hi - 1) >> 8); beta += blockDim.x) {
+            int pos = -1;
+            for (int i = 0; i < 257; ++i) {
+                pos = next_top(c.key, beta, i, pos, skip);
+                const uint32_t v = beta * 256u + (uint32_t)pos;
+                if (pos > 255 || v >= hi)
+                    break;
+                if (v < lo)
+                    continue;
+                tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v,
+                       fine52(c.key, v), true);
             }
         }
-        float wv = bub;
-        int wi = bv;
-        warp_argmax(wv, wi);
-        if (threadIdx.x == 0) sm.thr = f2ord(-INFINITY);
-        __syncthreads();
-        if (bv >= 0 && bv == wi) {
-            seedv = bv;
-            tr.add(c, bx, by, (uint32_t)bv, bb0);
-            atomicMax(&sm.thr, f2ord(tr.thr));
-        }
+        atomicMax(&sm.thr, f2ord(tr.thr));
         __syncthreads();
         tr.raise(ord2f(sm.thr));
     }
-    const float gmax = g8max(gt);
+    const float gmax = gt[kGTab - 1];
     float pub = tr.thr;
     for (int k0 = vb + threadIdx.x; k0 < ve; k0 += kLoadsAhead * blockDim.x) {
         uint4 px[kLoadsAhead];
@@ -542,17 +526,8 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, PostS
             const int k = k0 + u * blockDim.x;
             if (k >= ve)
                 break;
-            const uint32_t v0 = (uint32_t)k * E;
-            bool any = false;
-            uint32_t was[E / 4];
-#pragma unroll
-            for (int g = 0; g < E / 4; ++g) {
-                was[g] = word_a(klo, (v0 >> 2) + g);
-                const bool top = ((~was[g] - 0x01010101u) & was[g] & 0x80808080u) != 0u;
-                any |= top || fmaf(VT::group_max(px[u], g), c.invTp, gmax) >= tr.thrS;
-            }
-            if (any)
-                resid_vector<In>(c, px[u], k, was, seedv, gt, tr);
+            if (fmaf(VT::hi_of(VT::pmax(px[u])), c.invTp, gmax) >= tr.thrS)
+                resid_vector<In>(c, px[u], k, gt, skip, tr);
         }
         if (tr.thr > pub) {
             atomicMax(&sm.thr, f2ord(tr.thr));
@@ -658,7 +633,7 @@ __global__ void __launch_bounds__(kPostThreads) resid_kernel(const __grid_consta
         ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
         Track32 tr;
         resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
-                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, sm, tr);
+                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, j.skip, sm, tr);
         Cand2 best;
         block_cand2(tr.c, sm, best);
         if (threadIdx.x == 0) {
@@ -696,10 +671,12 @@ __global__ void __launch_bounds__(kPostThreads) resid_kernel(const __grid_consta
                 } else if (all.v1 >= 0) {
                     double l1 = -INFINITY, h1 = -INFINITY, l2 = -INFINITY, h2 = -INFINITY;
                     float x1 = load_logit(j, re.prow, all.v1), y1 = load_logit(j, re.qrow, all.v1);
-                    resid_interval64(ctx, x1, y1, bits52_full(ctx.key, all.v1), l1, h1);
+                    resid_interval64(ctx, x1, y1, fine52(ctx.key, all.v1),
+                                     is_top(ctx.key, all.v1, j.skip), l1, h1);
                     if (all.v2 >= 0) {
                         float x2 = load_logit(j, re.prow, all.v2), y2 = load_logit(j, re.qrow, all.v2);
-                        resid_interval64(ctx, x2, y2, bits52_full(ctx.key, all.v2), l2, h2);
+                        resid_interval64(ctx, x2, y2, fine52(ctx.key, all.v2),
+                                         is_top(ctx.key, all.v2, j.skip), l2, h2);
                     }
                     const double others = (double)all.hi3;
                     if (l1 > fmax(h2, others) + kFlagEps) win = all.v1;
@@ -908,7 +885,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
             }
             double alpha = alpha_of(j.kind == K_PACKED ? SV_LOSSLESS : j.amode, exp(lp - lq),
                                     j.lam);
-            double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0);
+            double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
             acc = u < alpha;
             fl = fabs(u - alpha) < kFlagEps;
         }
@@ -966,7 +943,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
         Track64 tr;
         resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
-                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, sm, tr);
+                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, j.skip, sm, tr);
         RBest best;
         block_rbest(tr.r, sm, best);
         if (threadIdx.x == 0) {

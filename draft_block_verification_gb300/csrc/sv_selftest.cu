@@ -3,8 +3,10 @@
 //   [0] max |G32 - G64| / kG32Err                 (Gumbel of sv_gumbel.cuh)
 //   [1] max |ex2(x) / 2^x - 1| / 2^-21            (x in [-126, 64])
 //   [2] max |lg2(x) - log2(x)| / (2^-22 max(1, |log2 x|))   (x in [2^-60, 2^8])
-// Uniforms are drawn from regions where the formulas are hardest: u
-// uniform, u within 2^-28 of 1, u below 2^-29, and u around 3/4.
+// Fine bits are drawn, for ordinary and top ids alike, from regions where the
+// formulas are hardest: uniform, w within 2^-28 of 1 (u next to 255/256, or
+// 1 - u near 2^-61 for a top id), w below 2^-29, and u around 3/4 (the
+// switch between the two evaluations of -log u).
 #include "sv_gumbel.cuh"
 
 namespace sv {
@@ -16,14 +18,15 @@ __global__ void selftest_kernel(uint64_t seed, long long n, unsigned *out)
          i += (long long)gridDim.x * blockDim.x) {
         uint64_t h = splitmix_out(seed ^ (uint64_t)i);
         uint64_t m;
+        const bool top = (i >> 2) & 1;
         switch (i & 3) {
         case 0: m = h >> 12; break;
         case 1: m = ((1ull << 52) - 1) - (h >> 40); break;
         case 2: m = h >> 40; break;
-        default: m = (3ull << 50) - (1ull << 23) + (h >> 40); break;
+        default: m = (3ull << 58) / 255ull / 2ull - (1ull << 23) + (h >> 40); break;
         }
-        double g64 = gumbel_of(u_of(m));
-        float g32 = gumbel32(m);
+        double g64 = gumbel64(m, top);
+        float g32 = gumbel32(m, top);
         r0 = fmaxf(r0, (float)(fabs((double)g32 - g64) / (double)kG32Err));
         float x = -126.f + 190.f * (float)((h >> 11) & 0xFFFFF) * 0x1p-20f;
         double e64 = exp2((double)x);

@@ -54,9 +54,11 @@ def _L():
         u64, u32, i64, i32, dbl = C.c_uint64, C.c_uint32, C.c_int64, C.c_int, C.c_double
         vp = C.c_void_p
         lib.or_mix64.restype, lib.or_mix64.argtypes = u64, [u64]
-        lib.or_fmix32.restype, lib.or_fmix32.argtypes = u32, [u32]
         lib.or_key.restype, lib.or_key.argtypes = u64, [u64, u32, u64, i64, u64]
-        lib.or_bits52.restype, lib.or_bits52.argtypes = u64, [u64, u32]
+        lib.or_fine52.restype, lib.or_fine52.argtypes = u64, [u64, u32]
+        lib.or_is_top.restype, lib.or_is_top.argtypes = i32, [u64, u32]
+        lib.or_skip_threshold.restype, lib.or_skip_threshold.argtypes = u64, [i32]
+        lib.or_row_uniforms.restype, lib.or_row_uniforms.argtypes = None, [u64, i32, vp, vp]
         lib.or_uniform.restype, lib.or_uniform.argtypes = dbl, [u64, u32]
         lib.or_gumbel.restype, lib.or_gumbel.argtypes = dbl, [u64, u32]
         lib.or_lse.restype, lib.or_lse.argtypes = dbl, [vp, i32, dbl]
@@ -126,20 +128,35 @@ def mix64(x: int) -> int:
     return int(_L().or_mix64(x & (2**64 - 1)))
 
 
-def fmix32(x: int) -> int:
-    return int(_L().or_fmix32(x & (2**32 - 1)))
-
-
 def key(seed: int, stream: int, seq: int, pos: int, it: int = 0) -> int:
     return int(_L().or_key(seed & (2**64 - 1), stream, seq & (2**64 - 1), pos, it & (2**64 - 1)))
 
 
-def bits52(k: int, v: int) -> int:
-    return int(_L().or_bits52(k, v))
+def fine52(k: int, v: int) -> int:
+    """The 52 fine bits m of id v: w = (2m + 1) / 2^53."""
+    return int(_L().or_fine52(k, v))
+
+
+def is_top(k: int, v: int) -> bool:
+    """Whether id v falls in the top 1/256 of the unit interval under key k."""
+    return bool(_L().or_is_top(k, v))
+
+
+def skip_threshold(g: int) -> int:
+    """C_g = ceil(2^64 (255/256)^g), the skip thresholds (g = 1..256)."""
+    return int(_L().or_skip_threshold(g))
 
 
 def uniform(k: int, v: int) -> float:
     return float(_L().or_uniform(k, v))
+
+
+def row_uniforms(k: int, V: int):
+    """(u[V], top[V]) of ids 0..V-1 under key k."""
+    u = np.empty(V)
+    top = np.empty(V, np.uint8)
+    _L().or_row_uniforms(k, V, _p(u), _p(top))
+    return u, top.astype(bool)
 
 
 def gumbel(k: int, v: int) -> float:

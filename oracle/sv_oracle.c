@@ -52,17 +52,6 @@ uint64_t or_mix64(uint64_t x)
     return z ^ (z >> 31);
 }
 
-/* MurmurHash3 32-bit finalizer (Appleby, public domain). */
-uint32_t or_fmix32(uint32_t h)
-{
-    h ^= h >> 16;
-    h *= 0x85EBCA6BU;
-    h ^= h >> 13;
-    h *= 0xC2B2AE35U;
-    h ^= h >> 16;
-    return h;
-}
-
 /* Row key: a chain of the 64-bit mixer over the counter fields. */
 uint64_t or_key(uint64_t seed, uint32_t stream, uint64_t seq, int64_t pos, uint64_t iter)
 {
@@ -74,32 +63,138 @@ uint64_t or_key(uint64_t seed, uint32_t stream, uint64_t seq, int64_t pos, uint6
     return k;
 }
 
-/* 52 random bits for vocabulary id v under row key k, most significant first:
- *   8 bits: byte (v mod 4) of fmix32(low32(k) xor (v div 4) * 0x9E3779B9),
- *   8 bits: byte (v mod 4) of fmix32(high32(k) xor (v div 4) * 0x85EBCA77),
- *  36 bits: the top 36 bits of mix64(k xor v * 0xD1B54A32D192ED03).
- * (Bytes are numbered from the least significant.)  Four consecutive ids
- * share the two 32-bit words. */
-uint64_t or_bits52(uint64_t key, uint32_t v)
+/* Uniforms of a row (row key k, vocabulary id v).  All randomness of a row is
+ * read from the SplitMix64 stream seeded with k: output number n + 1 is
+ * S(k, n) = or_mix64(k + n * 0x9E3779B97F4A7C15).
+ *
+ * The ids are split into blocks of 256 (block b = v div 256).  Which ids of a
+ * block fall into the top 1/256 of the unit interval ("top" ids) is drawn as
+ * i.i.d. Bernoulli(1/256) trials by geometric skipping (the number of failures
+ * before each success is geometric; the classical skip method for Bernoulli
+ * sequences): draw i of block b is M = S(k, b * 2^16 + i), its gap is the
+ * number of g in 1..256 with M < C_g, C_g = ceil(2^64 (255/256)^g), so that
+ * P(gap >= g) = C_g / 2^64 = (255/256)^g to within 2^-64; the first top
+ * offset is gap_0 and each next one is the previous plus 1 + gap_i, until an
+ * offset passes 255.
+ * Fine bits: m = S(k, 2^40 + v) >> 12 (52 bits), w = (2m + 1) / 2^53.
+ * Uniform: u = w * 255/256 for an ordinary id, and 1 - u = (1 - w) / 256
+ * (exact) for a top id, so that u is uniform on (0, 1) and G = -log(-log u)
+ * is standard Gumbel. */
+static uint64_t or_stream(uint64_t k, uint64_t n)
 {
-    uint32_t j = v >> 2, sh = 8u * (v & 3u);
-    uint32_t wa = or_fmix32((uint32_t)key ^ (j * 0x9E3779B9U));
-    uint32_t wb = or_fmix32((uint32_t)(key >> 32) ^ (j * 0x85EBCA77U));
-    uint64_t b0 = (wa >> sh) & 0xFFu, b1 = (wb >> sh) & 0xFFu;
-    uint64_t suffix = or_mix64(key ^ ((uint64_t)v * 0xD1B54A32D192ED03ULL)) >> 28;
-    return (b0 << 44) | (b1 << 36) | suffix;
+    return or_mix64(k + n * 0x9E3779B97F4A7C15ULL);
 }
 
-/* Uniform in the open interval (0,1): u = (2m + 1) / 2^53, exact in fp64. */
+/* C_g for g = 1..256 (index 0 unused), exact: 255^g as a multi-word integer,
+ * times 2^(64 - 8g), rounded up. */
+static uint64_t or_skip_c[257];
+static int or_skip_ready = 0;
+
+static void or_skip_init(void)
+{
+    if (or_skip_ready)
+        return;
+    uint32_t big[80];              /* 255^g, base 2^32, least significant first */
+    memset(big, 0, sizeof big);
+    big[0] = 1;
+    int len = 1;
+    for (int g = 1; g <= 256; ++g) {
+        uint64_t carry = 0;
+        for (int i = 0; i < len; ++i) {
+            uint64_t t = (uint64_t)big[i] * 255u + carry;
+            big[i] = (uint32_t)t;
+            carry = t >> 32;
+        }
+        if (carry)
+            big[len++] = (uint32_t)carry;
+        int shift = 8 * g - 64;        /* value = 255^g / 2^shift */
+        if (shift <= 0) {
+            uint64_t v = (uint64_t)big[0] | ((len > 1 ? (uint64_t)big[1] : 0) << 32);
+            or_skip_c[g] = v << (-shift);
+        } else {
+            /* floor(255^g / 2^shift), plus one if any dropped bit is set */
+            int w = shift / 32, r = shift % 32, dropped = 0;
+            for (int i = 0; i < w && i < len; ++i)
+                dropped |= big[i] != 0;
+            if (r && w < len && (big[w] & ((1u << r) - 1u)))
+                dropped = 1;
+            uint64_t v = 0;
+            for (int i = 0; i < 3; ++i) {
+                int idx = w + i;
+                uint64_t limb = idx < len ? big[idx] : 0;
+                if (r == 0) {
+                    if (i < 2) v |= limb << (32 * i);
+                } else {
+                    if (i == 0) v |= limb >> r;
+                    else if (i == 1) v |= limb << (32 - r);
+                    else v |= limb << (64 - r);
+                }
+            }
+            or_skip_c[g] = v + (uint64_t)dropped;
+        }
+    }
+    or_skip_ready = 1;
+}
+
+uint64_t or_skip_threshold(int g)
+{
+    or_skip_init();
+    return (g >= 1 && g <= 256) ? or_skip_c[g] : 0;
+}
+
+static int or_gap(uint64_t M)
+{
+    int g = 0;
+    while (g < 256 && M < or_skip_c[g + 1])
+        ++g;
+    return g;
+}
+
+/* 1 if v is a top id of its block under key k. */
+int or_is_top(uint64_t key, uint32_t v)
+{
+    or_skip_init();
+    const uint64_t b = v >> 8;
+    const int o = (int)(v & 255u);
+    int pos = -1;
+    for (uint64_t i = 0;; ++i) {
+        pos += or_gap(or_stream(key, (b << 16) | i)) + 1;
+        if (pos >= o)
+            return pos == o;
+    }
+}
+
+uint64_t or_fine52(uint64_t key, uint32_t v)
+{
+    return or_stream(key, (1ULL << 40) + v) >> 12;
+}
+
+/* Uniform in (0,1) (see above). */
 double or_uniform(uint64_t key, uint32_t v)
 {
-    return (double)(2 * or_bits52(key, v) + 1) * 0x1p-53;
+    const double w = (double)(2 * or_fine52(key, v) + 1) * 0x1p-53;
+    if (or_is_top(key, v))
+        return 1.0 - (1.0 - w) / 256.0;
+    return w * (255.0 / 256.0);
 }
 
-/* Standard Gumbel by inversion: G = -log(-log u). */
+/* Uniforms and top flags of ids 0..V-1 (for tests). */
+void or_row_uniforms(uint64_t key, int V, double *u, uint8_t *top)
+{
+    for (int v = 0; v < V; ++v) {
+        u[v] = or_uniform(key, (uint32_t)v);
+        top[v] = (uint8_t)or_is_top(key, (uint32_t)v);
+    }
+}
+
+/* Standard Gumbel by inversion, G = -log(-log u); for a top id from the exact
+ * 1 - u as -log(-log1p(-(1 - u))). */
 double or_gumbel(uint64_t key, uint32_t v)
 {
-    return -log(-log(or_uniform(key, v)));
+    const double w = (double)(2 * or_fine52(key, v) + 1) * 0x1p-53;
+    if (or_is_top(key, v))
+        return -log(-log1p(-((1.0 - w) / 256.0)));
+    return -log(-log(w * (255.0 / 256.0)));
 }
 
 /* ------------------------------------------------------------------------ */

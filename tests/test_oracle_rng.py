@@ -1,8 +1,10 @@
 """Pins of the oracle's counter-based random numbers.
 
-The mixers are pinned by published test vectors (tests/golden); the derived
-uniforms and Gumbels by their distributions (closed-form moments, chi-square
-goodness of fit) and by the exactness of the (2m+1)/2^53 construction.
+The mixer is pinned by published test vectors (tests/golden); the skip
+thresholds by an independent exact-integer computation; the top-id process by
+its binomial law per block of 256 ids; the uniforms and Gumbels by their
+distributions (closed-form moments, chi-square goodness of fit) and by the
+exactness of the (2m+1)/2^53 construction.
 """
 import math
 import os
@@ -29,30 +31,62 @@ def test_published_mixer_vectors(orc, fn, x, y):
     assert getattr(orc, fn)(x) == y
 
 
+def test_skip_thresholds_are_exact(orc):
+    # C_g = ceil(2^64 (255/256)^g), here with Python's exact integers
+    for g in range(1, 257):
+        exact = -((-(2**64) * 255**g) // 256**g)
+        assert orc.skip_threshold(g) == exact, g
+
+
 def test_uniform_is_open_interval_and_exact(orc):
-    for s in range(50):
+    for s in range(40):
         k = orc.key(s, orc.ST_SAMPLE, s * 7, s * 13, 0)
-        for v in (0, 1, 2, 3, 1000, 151935):
+        for v in (0, 1, 2, 3, 255, 256, 1000, 151935):
             u = orc.uniform(k, v)
             assert 0.0 < u < 1.0
-            m2 = u * 2.0 ** 53           # must be the odd integer 2m + 1
-            assert m2 == int(m2) and int(m2) % 2 == 1
-            assert int(m2) // 2 == orc.bits52(k, v)
+            m = orc.fine52(k, v)
+            assert 0 <= m < 2**52
+            w = (2 * m + 1) * 2.0**-53
+            if orc.is_top(k, v):
+                assert u >= 255 / 256 and 1.0 - u == pytest.approx((1.0 - w) / 256, abs=2**-53)
+            else:
+                assert u < 255 / 256 and u == w * (255 / 256)
+
+
+def test_top_ids_are_bernoulli_per_block(orc):
+    # counts per block of 256 ids ~ Binomial(256, 1/256); offsets uniform
+    counts, offsets = [], []
+    for s in range(120):
+        k = orc.key(1000 + s, orc.ST_TREE, s, 3 * s, 0)
+        _, top = orc.row_uniforms(k, 256 * 40)
+        t = top.reshape(40, 256)
+        counts.extend(t.sum(1).tolist())
+        offsets.extend(np.nonzero(t)[1].tolist())
+    counts = np.array(counts)
+    n = counts.size
+    p = [stats.binom.pmf(c, 256, 1 / 256) for c in range(3)]
+    p.append(1.0 - sum(p))
+    obs = [np.sum(counts == 0), np.sum(counts == 1), np.sum(counts == 2), np.sum(counts >= 3)]
+    assert stats.chisquare(obs, np.array(p) * n).pvalue > 1e-4
+    assert abs(counts.mean() - 1.0) < 4 * math.sqrt(255 / 256 / n)
+    assert stats.chisquare(np.bincount(np.array(offsets) // 16, minlength=16)).pvalue > 1e-4
 
 
 def test_uniform_chi_square(orc):
-    n = 40000
+    n = 60000
     k = orc.key(123, orc.ST_SAMPLE, 0, 0, 0)
-    u = np.array([orc.uniform(k, v) for v in range(n)])
+    u, top = orc.row_uniforms(k, n)
     counts, _ = np.histogram(u, bins=40, range=(0, 1))
-    p = stats.chisquare(counts).pvalue
-    assert p > 1e-4
-    # the four ids that share a hash word (v = 4j .. 4j+3) are independent
-    for a, b in ((0, 1), (0, 3), (1, 2)):
-        pairs = np.histogram2d(u[a::4], u[b::4], bins=8, range=[[0, 1], [0, 1]])[0].ravel()
+    assert stats.chisquare(counts).pvalue > 1e-4
+    # the top bucket [255/256, 1) holds exactly the top ids, and a fine
+    # histogram inside it is flat
+    assert np.array_equal(u >= 255 / 256, top)
+    inner = (u[top] - 255 / 256) * 256
+    assert stats.chisquare(np.histogram(inner, bins=8, range=(0, 1))[0]).pvalue > 1e-4
+    # neighbours (inside and across blocks) are independent
+    for lag in (1, 2, 255, 256):
+        pairs = np.histogram2d(u[:-lag], u[lag:], bins=8, range=[[0, 1], [0, 1]])[0].ravel()
         assert stats.chisquare(pairs).pvalue > 1e-4
-    top = (np.floor(u * 256)).astype(int)
-    assert stats.chisquare(np.bincount(top, minlength=256)).pvalue > 1e-4
     assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.03
 
 
@@ -62,8 +96,7 @@ def test_uniform_across_keys(orc):
                   for b in range(200) for i in range(100)])
     counts, _ = np.histogram(u, bins=20, range=(0, 1))
     assert stats.chisquare(counts).pvalue > 1e-4
-    ks = stats.kstest(u, "uniform").pvalue
-    assert ks > 1e-4
+    assert stats.kstest(u, "uniform").pvalue > 1e-4
 
 
 def test_keys_differ_by_every_field(orc):
@@ -85,3 +118,5 @@ def test_gumbel_moments(orc):
     assert abs(g.mean() - 0.5772156649015329) < 4 * math.sqrt(math.pi ** 2 / 6 / g.size)
     assert abs(g.var() - math.pi ** 2 / 6) < 0.05
     assert stats.kstest(g, "gumbel_r").pvalue > 1e-4
+    # the upper tail comes from the top ids: P(G > 5.5414) = 1/256
+    assert abs(np.mean(g > -math.log(-math.log(255 / 256))) - 1 / 256) < 4 * math.sqrt(1 / 256 / g.size)
