@@ -38,7 +38,7 @@ import datagen  # noqa: E402
 WORKLOAD = "lossless_t1"
 METRIC = "verified draft rows/sec and logits HBM GB/s (fraction of GB300 peak), 1 GPU"
 PROFILE = os.path.join(ROOT, "profiles", "pass_kernel_lossless_t1.md")
-KERNEL_SOURCES = ["sv_pass.cu", "sv_common.cuh", "sv_dev.cuh", "sv_job.cuh"]
+KERNEL_SOURCES = ["sv_pass.cu", "sv_common.cuh", "sv_dev.cuh", "sv_gumbel.cuh", "sv_job.cuh"]
 
 
 def _peaks():

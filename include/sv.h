@@ -25,15 +25,18 @@
  * - Integer outputs are int32; accept lengths count draft tokens.  Float
  *   outputs are fp32; entries that do not exist for a sequence (beyond its
  *   draft length) are written as NaN (floats) or -1 (token ids).
- * - Random numbers come from a counter-based generator: for a row key
- *   k = key(seed, stream, sequence b, absolute position, call index) and a
- *   vocabulary id v, u(k, v) = (2m + 1) / 2^53 with 52 random bits m, and
- *   G(k, v) = -log(-log u).  Streams: ACCEPT = 1 (acceptance uniforms,
- *   v = 0), SAMPLE = 2 (corrections and bonus tokens), DRAFT = 3 (Packed-SS
+ * - Random numbers come from a counter-based generator: a row key
+ *   k = key(seed, stream, sequence b, absolute position, call index) seeds a
+ *   SplitMix64 stream; every uniform u(k, v) of the row (vocabulary id v) is
+ *   read from that stream, and G(k, v) = -log(-log u).  Which ids land in
+ *   the top 1/256 of (0, 1) is an i.i.d. Bernoulli(1/256) process drawn by
+ *   geometric skipping in blocks of 256 ids; 52 fine bits m per id place u
+ *   at w * 255/256 (other ids) or 1 - (1 - w)/256 (top ids), w =
+ *   (2m + 1) / 2^53.  Streams: ACCEPT = 1 (acceptance uniforms, v = 0),
+ *   SAMPLE = 2 (corrections and bonus tokens), DRAFT = 3 (Packed-SS
  *   proposals, keyed by the call index), TREE = 4 (coupled noise shared by
- *   every tree node at the same absolute position).  The bit layout is given
- *   in the library's design notes and is fixed: equal arguments give equal
- *   results on any GB300.
+ *   every tree node at the same absolute position).  The layout is fixed:
+ *   equal arguments give equal results on any GB300.
  * - Decisions are exact with respect to fp64 arithmetic on the upcast logits:
  *   the kernels decide in fp32 with a proved error bound and recompute in
  *   fp64 whenever a decision falls inside that bound.  A decision whose fp64
