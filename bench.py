@@ -1,11 +1,12 @@
 """Benchmark of the verify step on GB300.
 
-One step = one sv_verify_sample call (lossless rejection sampling at T = 1:
-streaming pass over every target and drafter row, residual draw, fp64 path)
-over the lossless workload: B = 64 sequences, K = 16 draft tokens, V = 128256,
-bf16 logits (541.75 MB of logits per step, larger than the 126 MB L2, so every
-step streams from HBM).  Inputs are seeded synthetic tensors resident on the
-GPU before the timed region.
+One step = one verify call over one batch of a named workload (default: the
+lossless workload -- sv_verify_sample at T = 1 over B = 64 sequences, K = 16
+draft tokens, V = 128256, bf16 logits, 541.75 MB of logits per step, larger
+than the 126 MB L2, so every step streams from HBM).  A call runs the whole
+verify path: the streaming pass over every required row, the decisions, the
+residual draw and the fp64 check.  Inputs are seeded synthetic tensors
+resident on the GPU before the timed region.
 
 Prints ONE JSON line (rank 0): verified draft rows/s for the whole job, the
 roofline of the streaming kernel against the measured HBM copy bandwidth, the
@@ -13,6 +14,8 @@ end-to-end rate through the C ABI with host buffers, the CPU oracle baseline
 and the SM clocks sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload lossless_t1|lenient_sweep|tree|packed|greedy_tiny]
+                  [--T t] [--sigma s] [--lam l] [--mode lossless|ratio|linear]
 Multi-GPU (torchrun): every rank verifies its own full batch (weak scaling, no
 collective on the data path); value = all ranks' rows / max time over ranks.
 """
@@ -38,6 +41,7 @@ import datagen  # noqa: E402
 WORKLOAD = "lossless_t1"
 METRIC = "verified draft rows/sec and logits HBM GB/s (fraction of GB300 peak), 1 GPU"
 PROFILE = os.path.join(ROOT, "profiles", "pass_kernel_lossless_t1.md")
+L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["sv_pass.cu", "sv_common.cuh", "sv_dev.cuh", "sv_gumbel.cuh", "sv_job.cuh"]
 
 
@@ -146,37 +150,196 @@ def _max_over_ranks(dist, x, dev):
 def _barrier(dist, dev):
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize(dev)
+    if dev.type == "cuda":
+        torch.cuda.synchronize(dev)
 
 
-def _oracle_inputs(cfg, nseq):
-    si = datagen.sample_inputs(nseq, cfg["K"], cfg["V"], dtype=cfg["dtype"], seed=cfg["seed"],
-                               sigma=cfg["sigma"], T=cfg["T"], device="cpu")
-    return (datagen.to_numpy_logits(si.target), datagen.to_numpy_logits(si.draft),
-            si.draft_ids.numpy())
+def job_rate(world_size, units_per_rank, ms_max):
+    """Whole-job throughput: every rank processed units_per_rank units; the
+    job took the slowest rank's time (ms)."""
+    return world_size * units_per_rank / (ms_max / 1000.0)
 
 
-def _oracle_call(cfg, inputs):
-    import oracle
-    tgt, drf, ids = inputs
-    t0 = time.perf_counter()
-    oracle.verify_sample(tgt, drf, ids, seed=cfg["seed"], want_tv=False)
-    return time.perf_counter() - t0
+# ---------------------------------------------------------------------------
+# Workloads.  Each is one verify call on seeded synthetic inputs of the shapes
+# and distributions the method is measured on.
+# ---------------------------------------------------------------------------
+class Workload:
+    """One verify call of a named workload: inputs, the call through the
+    library, the same call through the oracle, and the algorithmic bytes of
+    the streaming kernel (required logit rows x V x element size)."""
+
+    def __init__(self, name, args):
+        self.name = name
+        self.cfg = dict(datagen.CONFIGS[name])
+        self.kind = self.cfg["kind"]
+        c = self.cfg
+        if args.batch:
+            c["B"] = args.batch
+        pick = lambda v, d: d if v is None else v
+        if self.kind == "sample":
+            # one point of the sweep (the lossless workload has a single point)
+            self.T = pick(args.T, c["T"] if not isinstance(c["T"], tuple) else 1.0)
+            self.sigma = pick(args.sigma, c["sigma"] if not isinstance(c["sigma"], tuple) else 1.0)
+            self.mode = {"lossless": 0, "ratio": 1, "linear": 2}[
+                args.mode or ("lossless" if name == "lossless_t1" else "ratio")]
+            self.lam = pick(args.lam, 1.0 if self.mode == 0 else 2.0)
+            if self.mode == 2 and args.lam is None:
+                self.lam = 0.5  # mu = 1 - 1/lambda at lambda = 2
+        elif self.kind in ("tree", "packed"):
+            self.T = pick(args.T, 1.0)
+        else:
+            self.T = 0.0
+        self.esz = 2 if c["dtype"] == "bf16" else 4
+
+    def point(self):
+        c = self.cfg
+        d = {"workload": self.name}
+        if self.kind == "sample":
+            d.update(B=c["B"], K=c["K"], V=c["V"], T=self.T, sigma=self.sigma,
+                     mode=["lossless", "ratio", "linear"][self.mode], lam=self.lam)
+        elif self.kind == "greedy":
+            d.update(B=c["B"], K=c["K"], V=c["V"])
+        elif self.kind == "tree":
+            d.update(B=c["B"], N=c["N"], V=c["V"], T=self.T, max_depth=c["max_depth"],
+                     max_children=c["max_children"])
+        else:
+            d.update(B=c["B"], K=c["K"], W=c["W"], V=c["V"], T=self.T)
+        d["logits"] = c["dtype"]
+        return d
+
+    def inputs(self, device, nseq=None):
+        c = self.cfg
+        B = nseq or c["B"]
+        if self.kind == "sample":
+            si = datagen.sample_inputs(B, c["K"], c["V"], dtype=c["dtype"], seed=c["seed"],
+                                       sigma=self.sigma, T=self.T, device=device)
+            return {"target": si.target, "draft": si.draft, "draft_ids": si.draft_ids}
+        if self.kind == "greedy":
+            gi = datagen.greedy_inputs(B, c["K"], c["V"], dtype=c["dtype"], seed=c["seed"],
+                                       device=device)
+            return {"target": gi.target, "draft_ids": gi.draft_ids, "draft_len": gi.draft_len}
+        if self.kind == "tree":
+            ti = datagen.tree_inputs(B, c["N"], c["V"], dtype=c["dtype"], seed=c["seed"],
+                                     L=c["L"], max_depth=c["max_depth"],
+                                     max_children=c["max_children"], device=device)
+            return {"node_logits": ti.node_logits, "parent": ti.parent, "node_pos": ti.node_pos,
+                    "node_tok": ti.node_tok}
+        pi = datagen.packed_inputs(B, c["K"], c["W"], c["V"], dtype=c["dtype"], seed=c["seed"],
+                                   T=self.T, device=device)
+        d = {"logits": pi.logits, "prev_draft": pi.prev_draft, "prev_len": pi.prev_len}
+        if self.T > 0:
+            d.update(prev_q_at_draft=pi.prev_q_at_draft, prev_draft_logits=pi.prev_draft_logits,
+                     prev_q_offset=pi.prev_q_offset)
+        return d
+
+    def call(self, dbv, inp, h):
+        c = self.cfg
+        if self.kind == "sample":
+            return dbv.sv_verify_sample(inp["target"], inp["draft"], inp["draft_ids"], T_p=self.T,
+                                        T_q=self.T, mode=self.mode, lam=self.lam, seed=c["seed"],
+                                        handle=h)
+        if self.kind == "greedy":
+            acc, nxt = dbv.sv_verify_greedy(inp["target"], inp["draft_ids"], inp["draft_len"],
+                                            handle=h)
+            return {"accept_len": acc, "next_token": nxt}
+        if self.kind == "tree":
+            return dbv.sv_verify_tree(inp["node_logits"], inp["parent"], inp["node_pos"],
+                                      inp["node_tok"], T=self.T, seed=c["seed"], handle=h)
+        return dbv.sv_packed_step(inp["logits"], c["K"], c["W"], inp["prev_draft"],
+                                  inp["prev_len"], prev_q_at_draft=inp.get("prev_q_at_draft"),
+                                  prev_draft_logits=inp.get("prev_draft_logits"),
+                                  prev_q_offset=inp.get("prev_q_offset"), T=self.T,
+                                  seed=c["seed"], it=1, handle=h)
+
+    def oracle_call(self, inp):
+        """The same call through the oracle; inputs as returned by inputs() on
+        the CPU.  Returns the wall time in seconds."""
+        import oracle
+        c = self.cfg
+        n = lambda t: t.numpy()
+        lg = datagen.to_numpy_logits
+        t0 = time.perf_counter()
+        if self.kind == "sample":
+            oracle.verify_sample(lg(inp["target"]), lg(inp["draft"]), n(inp["draft_ids"]),
+                                 T_p=self.T, T_q=self.T, mode=self.mode, lam=self.lam,
+                                 seed=c["seed"], want_tv=False)
+        elif self.kind == "greedy":
+            oracle.verify_greedy(lg(inp["target"]), n(inp["draft_ids"]), n(inp["draft_len"]))
+        elif self.kind == "tree":
+            oracle.verify_tree(lg(inp["node_logits"]), n(inp["parent"]), n(inp["node_pos"]),
+                               n(inp["node_tok"]), T=self.T, seed=c["seed"])
+        else:
+            pdl = inp.get("prev_draft_logits")
+            oracle.packed_step(lg(inp["logits"]), c["K"], c["W"], n(inp["prev_draft"]),
+                               n(inp["prev_len"]),
+                               prev_q_at_draft=None if pdl is None else n(inp["prev_q_at_draft"]),
+                               prev_draft_logits=None if pdl is None else lg(pdl),
+                               prev_q_offset=None if pdl is None else n(inp["prev_q_offset"]),
+                               T=self.T, seed=c["seed"], it=1)
+        return time.perf_counter() - t0
+
+    def units(self, inp):
+        """Verified draft rows of one call (the metric's unit)."""
+        c = self.cfg
+        if self.kind in ("sample", "greedy"):
+            if "draft_len" in inp:
+                return int(inp["draft_len"].sum().item())
+            return int(inp["draft_ids"].shape[0]) * c["K"]
+        if self.kind == "tree":
+            return int(inp["parent"].numel())
+        return int(inp["prev_len"].sum().item())
+
+    def alg_bytes(self, inp):
+        """Bytes of logits the streaming kernel must read: every row the
+        verify rule needs, once."""
+        c = self.cfg
+        row = c["V"] * self.esz
+        if self.kind == "sample":
+            B = inp["target"].shape[0]
+            return B * (2 * c["K"] + 1) * row
+        if self.kind == "greedy":
+            return int((inp["draft_len"].long() + 1).sum().item()) * row
+        if self.kind == "tree":
+            return int(inp["parent"].numel()) * row
+        B = inp["logits"].shape[0]
+        return int((inp["prev_len"].long() + 1).sum().item() + B * c["W"]) * row
+
+    def launches(self):
+        """Library kernels per call: the streaming pass, plus the residual
+        pass and the fp64 check after a sampling call."""
+        return 3 if (self.kind == "sample" or (self.kind == "packed" and self.T > 0)) else 1
 
 
-def cpu_baseline(cfg, nseq=None, inputs=None):
-    """Time the fp64 oracle, as it stands, on a bounded sample of the workload:
-    the first nseq sequences of the batch (all of them by default), generated
-    on the CPU with the same recipe."""
+def _cpu_sample(w, seconds, nmax=None):
+    """Inputs for the oracle on the CPU: as many sequences of the workload as
+    fit in about `seconds` of oracle time (measured on one sequence)."""
     import oracle
     oracle.build()
-    nseq = nseq or cfg["B"]
-    inputs = inputs or _oracle_inputs(cfg, nseq)
-    dt = _oracle_call(cfg, inputs)
-    rows = nseq * cfg["K"]
-    return {"value": rows / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d of %d sequences x %d drafts x V=%d (%s), one oracle verify call, "
-                      "%.3f s wall" % (nseq, cfg["B"], cfg["K"], cfg["V"], cfg["dtype"], dt)}
+    B = nmax or w.cfg["B"]
+    one = w.inputs("cpu", 1)
+    t1 = max(w.oracle_call(one), 1e-4)
+    nseq = int(max(1, min(B, seconds / t1)))
+    return nseq, (one if nseq == 1 else w.inputs("cpu", nseq))
+
+
+def cpu_baseline(w, seconds=15.0):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload
+    (the first sequences of a batch drawn on the CPU with the same recipe),
+    repeating the call until about `seconds` have passed."""
+    import oracle
+    nseq, inp = _cpu_sample(w, seconds / 3)
+    times = []
+    t_end = time.perf_counter() + seconds
+    while True:
+        times.append(w.oracle_call(inp))
+        if time.perf_counter() >= t_end or len(times) >= 50:
+            break
+    dt = statistics.median(times)
+    units = w.units(inp)
+    return {"value": units / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d of %d sequences of %s, %d oracle calls, median %.3f s wall"
+                      % (nseq, w.cfg["B"], w.name, len(times), dt)}
 
 
 def run_reference(args):
@@ -184,34 +347,36 @@ def run_reference(args):
     verifies a sample of the workload, sized so that the whole run stays
     within about two minutes."""
     dist, rank, ws = _dist()
-    cfg = datagen.CONFIGS[WORKLOAD]
     if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
         return
+    w = Workload(args.workload, args)
     import oracle
-    oracle.build()
-    full = _oracle_inputs(cfg, cfg["B"])
-    t_full = _oracle_call(cfg, full)
     n_calls = max(1, args.warmup + args.steps)
-    nseq = int(max(1, min(cfg["B"], cfg["B"] * 120.0 / (n_calls * max(t_full, 1e-6)))))
-    inputs = full if nseq == cfg["B"] else tuple(a[:nseq] for a in full)
+    nseq, inp = _cpu_sample(w, 100.0 / n_calls)
     vals = []
-    cb = None
     for _ in range(n_calls):
-        cb = cpu_baseline(cfg, nseq, inputs)
-        vals.append(cb["value"])
-    value = statistics.median(vals[args.warmup:]) if args.steps else cb["value"]
-    cb["value"] = value
+        vals.append(w.units(inp) / w.oracle_call(inp))
+    value = statistics.median(vals[args.warmup:]) if args.steps else vals[-1]
+    cb = {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": "%d of %d sequences of %s per step" % (nseq, w.cfg["B"], w.name)}
+    cfg = w.point()
+    cfg.update(sample_sequences_per_step=nseq)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * nseq * cfg["K"] / value, "higher_is_better": True,
+            "ms_per_step": 1000.0 * w.units(inp) / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": cfg["B"], "K": cfg["K"], "V": cfg["V"],
-                       "logits": cfg["dtype"], "T": cfg["T"], "l2": "inputs larger than L2",
-                       "sample_sequences_per_step": nseq},
-            "cpu_baseline": cb,
+            "config": cfg, "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _tensors(out):
+    return [t for t in (out.values() if isinstance(out, dict) else out) if torch.is_tensor(t)]
 
 
 def run_ours(args):
@@ -221,16 +386,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dbv.build()
-    cfg = dict(datagen.CONFIGS[WORKLOAD])
-    if args.batch:
-        cfg["B"] = args.batch
-    B, K, V = cfg["B"], cfg["K"], cfg["V"]
-    si = datagen.sample_inputs(B, K, V, dtype=cfg["dtype"], seed=cfg["seed"], sigma=cfg["sigma"],
-                               T=cfg["T"], device=dev)
+    w = Workload(args.workload, args)
+    inp = w.inputs(dev)
     h = dbv.default_handle(dev)
     stream = torch.cuda.current_stream(dev)
-    call = lambda: dbv.sv_verify_sample(si.target, si.draft, si.draft_ids, T_p=cfg["T"],
-                                        T_q=cfg["T"], seed=cfg["seed"], handle=h)
+    call = lambda: w.call(dbv, inp, h)
     for _ in range(max(args.warmup, 3)):
         call()
     h.sync_status()
@@ -243,42 +403,52 @@ def run_ours(args):
         b.record(stream)
     torch.cuda.synchronize(dev)
     ptrs = [np.array([e[0].cuda_event, e[1].cuda_event], dtype=np.uint64) for e in evs]
-    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Inputs smaller than a few L2s: flush L2 between steps (a write of twice
+    # its size, outside the per-step events) and time each step on its own.
+    flush = None
+    if w.alg_bytes(inp) < 3 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps if flush is not None else 1)]
     with Clocks(local) as clk:
         _barrier(dist, dev)
-        t_start.record(stream)
+        if flush is None:
+            steps_ev[0][0].record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(float(i))
+                steps_ev[i][0].record(stream)
             h.set_option(dbv.SV_OPT_TIMING_EVENTS, int(ptrs[i].ctypes.data))
             call()
-        t_stop.record(stream)
+            if flush is not None:
+                steps_ev[i][1].record(stream)
+        if flush is None:
+            steps_ev[0][1].record(stream)
         _barrier(dist, dev)
     h.set_option(dbv.SV_OPT_TIMING_EVENTS, 0)
     h.sync_status()
-    ms = t_start.elapsed_time(t_stop) / args.steps
+    ms = sum(a.elapsed_time(b) for a, b in steps_ev) / args.steps
     ms = _max_over_ranks(dist, ms, dev)
     kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    rows = B * K
-    value = ws * rows / (ms / 1000.0)
-    alg_bytes = B * (2 * K + 1) * V * 2
+    units = w.units(inp)
+    value = job_rate(ws, units, ms)
+    alg_bytes = w.alg_bytes(inp)
     peak, peak_kind = _peaks()
     achieved = alg_bytes / (kern_ms / 1000.0) / 1e9
 
     # end to end: pinned host inputs -> device, the call, results -> host
-    host = [t.detach().cpu().pin_memory() for t in (si.target, si.draft, si.draft_ids)]
-    dst = [torch.empty_like(t, device=dev) for t in host]
-    h2d = sum(t.numel() * t.element_size() for t in host)
+    host = {k: t.detach().cpu().pin_memory() for k, t in inp.items()}
+    dst = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
     out_bytes = 0
     _barrier(dist, dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_steps = max(2, min(args.steps, 5))
     e0.record(stream)
     for _ in range(e_steps):
-        for d, s in zip(dst, host):
-            d.copy_(s, non_blocking=True)
-        out = dbv.sv_verify_sample(dst[0], dst[1], dst[2], T_p=cfg["T"], T_q=cfg["T"],
-                                   seed=cfg["seed"], handle=h)
-        res = [out[k].to("cpu", non_blocking=True) for k in ("accept_len", "next_token",
-                                                             "p_at_draft", "q_at_draft")]
+        for k, t in host.items():
+            dst[k].copy_(t, non_blocking=True)
+        res = [t.to("cpu", non_blocking=True) for t in _tensors(w.call(dbv, dst, h))]
         out_bytes = sum(r.numel() * r.element_size() for r in res)
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -289,26 +459,27 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         return
+    cfg = w.point()
+    cfg["l2"] = ("inputs larger than L2 (%.2f MB of logits/step)" % (alg_bytes / 1e6)
+                 if flush is None else "L2 flushed between steps (%.2f MB of logits/step)"
+                 % (alg_bytes / 1e6))
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if B == datagen.CONFIGS[WORKLOAD]["B"] else
-                   "%s with B=%d" % (WORKLOAD, B), "B": B, "K": K, "V": V, "logits": "bf16",
-                   "T": cfg["T"], "mode": "lossless", "outputs": "accept_len, next_token, "
-                   "p/q at draft ids, lse",
-                   "l2": "inputs larger than L2 (%.2f MB/step)" % (B * (2 * K + 1) * V * 2 / 1e6)},
+        "scaling": "weak", "vs_baseline": None, "dtype": w.cfg["dtype"], "data": "synthetic",
+        "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": _profiled_traffic(),
+                     "frac": achieved / peak,
+                     "traffic": _profiled_traffic() if args.workload == WORKLOAD else None,
                      "peak_source": peak_kind, "kernel": "pass_kernel", "kernel_ms": kern_ms,
                      "alg_bytes_per_launch": alg_bytes},
-        "e2e": {"value": ws * rows / (e_ms / 1000.0), "unit": "rows/s",
+        "e2e": {"value": job_rate(ws, units, e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": w.launches() * args.steps,
         "clocks": clk.summary(),
     }
     if ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg)
+        line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -323,6 +494,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the number of sequences (small cases for ncu captures)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(datagen.CONFIGS),
+                    help="which verify workload one step runs (default: %s)" % WORKLOAD)
+    ap.add_argument("--T", type=float, default=None, help="temperature (sample, tree, packed)")
+    ap.add_argument("--sigma", type=float, default=None, help="drafter noise (sample)")
+    ap.add_argument("--lam", type=float, default=None, help="lambda (ratio) or mu (linear)")
+    ap.add_argument("--mode", default=None, choices=["lossless", "ratio", "linear"])
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
