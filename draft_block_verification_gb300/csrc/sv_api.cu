@@ -227,7 +227,7 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     // in fp64)
     const int stages_per_unit = (j.part_vecs + kStageVecs - 1) / kStageVecs;
     // plus the absolute error of log2 S in the row merge (below 2^-22)
-    j.eps_lse = lse_rel_bound_stream((double)j.V, 24.0 + stages_per_unit) + 0x1p-22;
+    j.eps_lse = lse_rel_bound_stream((double)j.V, kLseSumDepth + 2.0 + stages_per_unit) + 0x1p-22;
     // exact ratios (log2(e)/T) / fl32(log2(e)/T) and reciprocals, once per call
     auto ratio = [](float c, float T) {
         return (c > 0.f && T > 0.f) ? (1.4426950408889634 / (double)T) / (double)c : 1.0;

@@ -18,16 +18,20 @@
 namespace sv {
 
 // ---------------------------------------------------------------------------
-// Launch geometry of the streaming kernel.
+// Launch geometry of the streaming kernel: one CTA per SM with 12 consumer
+// warps, each thread taking 6 16-byte vectors of a 36 KB stage, and a ring of
+// 4 stages (144 KB in flight per SM).  Chosen by measurement on GB300 among
+// 8-16 consumer warps and 16-36 KB stages: more consumer warps hide the
+// per-element dependency chains, larger stages halve the per-stage overhead.
 // ---------------------------------------------------------------------------
 #ifndef SV_CONSUMER_WARPS
-#define SV_CONSUMER_WARPS 8
+#define SV_CONSUMER_WARPS 12
 #endif
 #ifndef SV_STAGES
-#define SV_STAGES 8
+#define SV_STAGES 4
 #endif
 #ifndef SV_STAGE_BYTES
-#define SV_STAGE_BYTES 16384
+#define SV_STAGE_BYTES 36864
 #endif
 #ifndef SV_SPIN_SLEEP_NS
 #define SV_SPIN_SLEEP_NS 64
@@ -43,6 +47,12 @@ constexpr int kStageVecs = kStageBytes / 16;      // 16-byte vectors per stage
 constexpr int kVecsPerThread = kStageVecs / kConsumers;
 constexpr int kStages = SV_STAGES;
 static_assert(kVecsPerThread * kConsumers == kStageVecs, "stage must split evenly");
+constexpr int ceil_log2(int n) { return n <= 1 ? 0 : 1 + ceil_log2((n + 1) / 2); }
+// Longest fp32 summation path of a unit's log-sum-exp partial, one addition
+// per stage aside: the pairwise tree of a chunk (up to 4 element pairs per
+// vector), the x + y of the packed pair, the warp sum and the sequential sum
+// over the consumer warps.
+constexpr int kLseSumDepth = ceil_log2(kVecsPerThread * 4) + 1 + 5 + (kConsumerWarps - 1);
 constexpr int kMaxK = 32;
 constexpr int kMaxN = 64;
 constexpr double kFlagEps = 1e-9;                 // near-threshold window

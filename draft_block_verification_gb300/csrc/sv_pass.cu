@@ -431,20 +431,29 @@ __device__ __forceinline__ float2 lse_terms(const Chunk &q, float c, float e)
             const float2 y = fma2(VT::pair(q[k], i), cc, ne);
             t[k * P + i] = make_float2(ex2f(y.x), ex2f(y.y));
         }
+    // pairwise tree over any number of terms (depth ceil(log2 N))
+    constexpr int N = kVecsPerThread * P;
 #pragma unroll
-    for (int w = kVecsPerThread * P / 2; w >= 1; w >>= 1)
+    for (int w = 1; w < N; w <<= 1)
 #pragma unroll
-        for (int i = 0; i < w; ++i)
+        for (int i = 0; i + w < N; i += 2 * w)
             t[i] = add2(t[i], t[i + w]);
     return t[0];
 }
 
-// Adds the chunk to one log-sum-exp accumulator.  A partial sum of 2^20 or
-// more (or inf / NaN: no reference yet) moves the reference up to the chunk
-// max, rounded up to an integer, and rescales the accumulator exactly.
+// Adds the chunk to one log-sum-exp accumulator.  The first chunk with an
+// element sets the reference to its max, rounded up to an integer; later, a
+// partial sum of 2^20 or more moves the reference up to the chunk max and
+// rescales the accumulator exactly.
 template <typename In>
 __device__ __forceinline__ void lse_chunk(const Chunk &q, float c, float &e, float2 &acc)
 {
+    if (e == -INFINITY) {
+        const float cm = chunk_max<In>(q);
+        if (cm == -INFINITY)
+            return;  // no element yet
+        e = ceilf(__fmul_ru(cm, c));
+    }
     float2 part = lse_terms<In>(q, c, e);
     if (!(part.x + part.y < 0x1p20f)) {
         const float cm = chunk_max<In>(q);
@@ -1300,7 +1309,7 @@ __device__ __noinline__ GState seed_rounds(PassShared &sm, int b, const char *ro
 {
     using VT = VecTraits<In>;
     constexpr uint32_t kNone = 0xFFFFFFFFu;
-    constexpr int kPer = kSeedCap / kConsumers;
+    constexpr int kPer = (kSeedCap + kConsumers - 1) / kConsumers;
     const int t = threadIdx.x;
     const uint32_t bhi = (uint32_t)(hi - 1) >> 8;
     uint32_t beta = ((uint32_t)lo >> 8) + t;

@@ -457,14 +457,13 @@ __device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out
 // skipped (the seed phase scored every top id of the chunk); an ordinary id
 // is bounded by the top byte of its fine bits.
 template <typename In, typename Tr>
-__device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, int k,
-                                             const float *gt, const uint64_t *skip, Tr &tr)
+__device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, const uint4 &qy,
+                                             int k, const float *gt, const uint64_t *skip, Tr &tr)
 {
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
     const uint32_t v0 = (uint32_t)k * E;
     const uint32_t tm = top_mask(c.key, v0 >> 8, (int)(v0 & 255u), E, skip);
-    const uint4 qy = ldv<In>(c.qrow, k);
 #pragma unroll 1
     for (int i = 0; i < E; ++i) {
         if ((tm >> i) & 1u)
@@ -478,6 +477,42 @@ __device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, int
     }
 }
 
+// Seed of a scan over vectors [vb, ve): the CTA scores every top id of the
+// range (a couple of skip draws per block of 256 ids) and shares the best
+// lower end as the threshold.
+template <typename In, typename Tr>
+__device__ __forceinline__ void resid_seed(const RCtx &c, int vb, int ve, const uint64_t *skip,
+                                           PostShared &sm, Tr &tr)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    if (threadIdx.x == 0) sm.thr = f2ord(-INFINITY);
+    __syncthreads();
+    const uint32_t lo = (uint32_t)vb * E, hi = (uint32_t)ve * E;
+    for (uint32_t beta = (lo >> 8) + threadIdx.x; beta <= ((hi - 1) >> 8); beta += blockDim.x) {
+        int pos = -1;
+        for (int i = 0; i < 257; ++i) {
+            pos = next_top(c.key, beta, i, pos, skip);
+            const uint32_t v = beta * 256u + (uint32_t)pos;
+            if (pos > 255 || v >= hi)
+                break;
+            if (v < lo)
+                continue;
+            tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v, fine52(c.key, v),
+                   true);
+        }
+    }
+    atomicMax(&sm.thr, f2ord(tr.thr));
+    __syncthreads();
+    tr.raise(ord2f(sm.thr));
+}
+
+// Resident residual CTAs per SM: several items in flight per SM hide the
+// latency chain of one item (loads, seed, screen, merge).
+#ifndef SV_RESID_MIN_BLOCKS
+#define SV_RESID_MIN_BLOCKS 4
+#endif
+
 // Scan vectors [vb, ve) of the pair.  Seed: the CTA scores every top id of
 // the chunk first (a couple of skip draws per block of 256 ids), which sets a
 // threshold close to the chunk's best; then each vector whose largest logit
@@ -488,29 +523,8 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const
                            PostShared &sm, Tr &tr)
 {
     using VT = VecTraits<In>;
-    constexpr int E = VT::N;
     tr.init();
-    if (threadIdx.x == 0) sm.thr = f2ord(-INFINITY);
-    __syncthreads();
-    {
-        const uint32_t lo = (uint32_t)vb * E, hi = (uint32_t)ve * E;
-        for (uint32_t beta = (lo >> 8) + threadIdx.x; beta <= ((hi - 1) >> 8); beta += blockDim.x) {
-            int pos = -1;
-            for (int i = 0; i < 257; ++i) {
-                pos = next_top(c.key, beta, i, pos, skip);
-                const uint32_t v = beta * 256u + (uint32_t)pos;
-                if (pos > 255 || v >= hi)
-                    break;
-                if (v < lo)
-                    continue;
-                tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v,
-                       fine52(c.key, v), true);
-            }
-        }
-        atomicMax(&sm.thr, f2ord(tr.thr));
-        __syncthreads();
-        tr.raise(ord2f(sm.thr));
-    }
+    resid_seed<In>(c, vb, ve, skip, sm, tr);
     const float gmax = gt[kGTab - 1];
     float pub = tr.thr;
     for (int k0 = vb + threadIdx.x; k0 < ve; k0 += kLoadsAhead * blockDim.x) {
@@ -527,7 +541,7 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const
             if (k >= ve)
                 break;
             if (fmaf(VT::hi_of(VT::pmax(px[u])), c.invTp, gmax) >= tr.thrS)
-                resid_vector<In>(c, px[u], k, gt, skip, tr);
+                resid_vector<In>(c, px[u], ldv<In>(c.qrow, k), k, gt, skip, tr);
         }
         if (tr.thr > pub) {
             atomicMax(&sm.thr, f2ord(tr.thr));
@@ -556,24 +570,130 @@ __device__ __forceinline__ void fill_ctx(const Job &j, RCtx &ctx, const char *pr
     ctx.dhi32 = __double2float_ru(ctx.dhi);
 }
 
+// One item of the residual pass: chunk c of the row pair of entry e.  Scans
+// the chunk, stores its candidates, and the last chunk of the pair to finish
+// merges them and draws the correction.
 template <typename In>
-__global__ void __launch_bounds__(kPostThreads) resid_kernel(const __grid_constant__ Job j)
+__device__ __forceinline__ void resid_item(const Job &j, PostShared &sm, const float *gt,
+                                           const uint64_t *skip, int e, int c,
+                                           const ResidEntry &re)
+{
+    unsigned *cnt = j.rdone + (int64_t)e * 4;
+    const double D = re.Lq - re.Lp;
+    const double eD = 1.001 * (re.epsp + re.epsq) + 1e-14 * (fabs(re.Lp) + fabs(re.Lq));
+    RCtx ctx;
+    fill_ctx(j, ctx, re.prow, re.qrow, D, eD);
+    ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
+    Track32 tr;
+    resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
+                   chunk_lo(j.nvec, c + 1, kResidChunks), gt, skip, sm, tr);
+    Cand2 best;
+    block_cand2(tr.c, sm, best);
+    if (threadIdx.x == 0) {
+        double *rec = resid_rec(j, e, c);
+        rec[0] = best.hi1;
+        rec[1] = best.lo1;
+        rec[2] = best.hi2;
+        rec[3] = best.lo2;
+        rec[4] = best.hi3;
+        rec[5] = (double)best.v1;
+        rec[6] = (double)best.v2;
+        __threadfence();
+        sm.flag = atomicAdd(cnt + 1, 1u) + 1u == (unsigned)kResidChunks;
+    }
+    __syncthreads();
+    const bool last = sm.flag != 0;
+    __syncthreads();  // sm.flag is reused by the next item
+    if (!last || threadIdx.x >= 32)
+        return;
+    // The pair's last chunk: the first warp gathers the chunk records in
+    // parallel (lane q holds record q) and merges them.
+    __threadfence();
+    const int lane = threadIdx.x;
+    Cand2 all;
+    all.init();
+    for (int q = lane; q < kResidChunks; q += 32) {
+        const double *rq = resid_rec(j, e, q);
+        Cand2 t;
+        t.hi1 = (float)__ldcg(rq + 0);
+        t.lo1 = (float)__ldcg(rq + 1);
+        t.hi2 = (float)__ldcg(rq + 2);
+        t.lo2 = (float)__ldcg(rq + 3);
+        t.hi3 = (float)__ldcg(rq + 4);
+        t.v1 = (int)__ldcg(rq + 5);
+        t.v2 = (int)__ldcg(rq + 6);
+        all.merge(t);
+    }
+    warp_cand2(all);
+    if (lane != 0)
+        return;
+    cnt[1] = 0u;
+    cnt[2] = 0u;
+    // certify in fp32, else re-score the two contenders in fp64
+    int win = -1;
+    if (gumbel_certified(all)) {
+        win = all.v1;
+    } else if (all.v1 >= 0) {
+        double l1 = -INFINITY, h1 = -INFINITY, l2 = -INFINITY, h2 = -INFINITY;
+        float x1 = load_logit(j, re.prow, all.v1), y1 = load_logit(j, re.qrow, all.v1);
+        resid_interval64(ctx, x1, y1, fine52(ctx.key, all.v1), is_top(ctx.key, all.v1, skip),
+                         l1, h1);
+        if (all.v2 >= 0) {
+            float x2 = load_logit(j, re.prow, all.v2), y2 = load_logit(j, re.qrow, all.v2);
+            resid_interval64(ctx, x2, y2, fine52(ctx.key, all.v2),
+                             is_top(ctx.key, all.v2, skip), l2, h2);
+        }
+        const double others = (double)all.hi3;
+        if (l1 > fmax(h2, others) + kFlagEps) win = all.v1;
+        else if (l2 > fmax(h1, others) + kFlagEps) win = all.v2;
+    }
+    if (win >= 0 && !j.force_rescue) {
+        if (j.kind == K_SAMPLE) {
+            j.next[re.b] = win;
+            if (j.flags) j.flags[re.b] = 0;
+        } else if (re.h < j.commit_len[re.b]) {
+            j.committed[(int64_t)re.b * j.K + re.h] = win;
+        }
+    } else {
+        unsigned k = atomicAdd(j.ctl + C_RESCUE_N, 1u);
+        RescueEntry x;
+        x.b = re.b;
+        x.kind = 1;
+        x.h = re.h;
+        x.resid = 1;
+        x.Lp = 0;
+        x.Lq = 0;
+        x.flags = 0;
+        x.pad[0] = x.pad[1] = x.pad[2] = 0;
+        j.rescue[k] = x;
+    }
+}
+
+template <typename In>
+__global__ void __launch_bounds__(kPostThreads, SV_RESID_MIN_BLOCKS) resid_kernel(const __grid_constant__ Job j)
 {
     __shared__ PostShared sm;
     __shared__ float gt[kGTab];
+    __shared__ uint64_t skip[kSkipN];  // skip thresholds of the top-id draws
     for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
         gt[i] = __ldg(j.gtab + i);
+    for (int i = threadIdx.x; i < kSkipN; i += blockDim.x)
+        skip[i] = __ldg(j.skip + i);
     __syncthreads();
     const unsigned nE = *(volatile unsigned *)(j.ctl + C_RESID_N);
     const unsigned nA = nE * kResidChunks;
+    // CTAs take items from a counter.  Packed-SS items come in two phases
+    // (the stored proposal rows' log-sum-exps first); sampling calls have
+    // only the residual scans.
+    const bool twophase = j.kind != K_SAMPLE;
     for (;;) {
         if (threadIdx.x == 0) sm.item = atomicAdd(j.ctl + C_RWORK, 1u);
         __syncthreads();
         unsigned it = sm.item;
         __syncthreads();
-        if (it >= 2 * nA) break;
-        bool phaseA = it < nA;
-        if (!phaseA) it -= nA;
+        if (it >= (twophase ? 2 * nA : nA)) break;
+        const bool phaseA = twophase && it < nA;
+        if (twophase && !phaseA) it -= nA;
         const int e = it / kResidChunks, c = it - e * kResidChunks;
         unsigned *cnt = j.rdone + (int64_t)e * 4;
         ResidEntry re = j.resid[e];
@@ -626,84 +746,7 @@ __global__ void __launch_bounds__(kPostThreads) resid_kernel(const __grid_consta
             re.Lq = __ldcg(&j.resid[e].Lq);
             re.epsq = __ldcg(&j.resid[e].epsq);
         }
-        const double D = re.Lq - re.Lp;
-        const double eD = 1.001 * (re.epsp + re.epsq) + 1e-14 * (fabs(re.Lp) + fabs(re.Lq));
-        RCtx ctx;
-        fill_ctx(j, ctx, re.prow, re.qrow, D, eD);
-        ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
-        Track32 tr;
-        resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
-                       chunk_lo(j.nvec, c + 1, kResidChunks), gt, j.skip, sm, tr);
-        Cand2 best;
-        block_cand2(tr.c, sm, best);
-        if (threadIdx.x == 0) {
-            double *rec = resid_rec(j, e, c);
-            rec[0] = best.hi1;
-            rec[1] = best.lo1;
-            rec[2] = best.hi2;
-            rec[3] = best.lo2;
-            rec[4] = best.hi3;
-            rec[5] = (double)best.v1;
-            rec[6] = (double)best.v2;
-            __threadfence();
-            if (atomicAdd(cnt + 1, 1u) + 1u == (unsigned)kResidChunks) {
-                __threadfence();
-                Cand2 all;
-                all.init();
-                for (int q = 0; q < kResidChunks; ++q) {
-                    double *rq = resid_rec(j, e, q);
-                    Cand2 t;
-                    t.hi1 = (float)__ldcg(rq + 0);
-                    t.lo1 = (float)__ldcg(rq + 1);
-                    t.hi2 = (float)__ldcg(rq + 2);
-                    t.lo2 = (float)__ldcg(rq + 3);
-                    t.hi3 = (float)__ldcg(rq + 4);
-                    t.v1 = (int)__ldcg(rq + 5);
-                    t.v2 = (int)__ldcg(rq + 6);
-                    all.merge(t);
-                }
-                cnt[1] = 0u;
-                cnt[2] = 0u;
-                // certify in fp32, else re-score the two contenders in fp64
-                int win = -1;
-                if (gumbel_certified(all)) {
-                    win = all.v1;
-                } else if (all.v1 >= 0) {
-                    double l1 = -INFINITY, h1 = -INFINITY, l2 = -INFINITY, h2 = -INFINITY;
-                    float x1 = load_logit(j, re.prow, all.v1), y1 = load_logit(j, re.qrow, all.v1);
-                    resid_interval64(ctx, x1, y1, fine52(ctx.key, all.v1),
-                                     is_top(ctx.key, all.v1, j.skip), l1, h1);
-                    if (all.v2 >= 0) {
-                        float x2 = load_logit(j, re.prow, all.v2), y2 = load_logit(j, re.qrow, all.v2);
-                        resid_interval64(ctx, x2, y2, fine52(ctx.key, all.v2),
-                                         is_top(ctx.key, all.v2, j.skip), l2, h2);
-                    }
-                    const double others = (double)all.hi3;
-                    if (l1 > fmax(h2, others) + kFlagEps) win = all.v1;
-                    else if (l2 > fmax(h1, others) + kFlagEps) win = all.v2;
-                }
-                if (win >= 0 && !j.force_rescue) {
-                    if (j.kind == K_SAMPLE) {
-                        j.next[re.b] = win;
-                        if (j.flags) j.flags[re.b] = 0;
-                    } else if (re.h < j.commit_len[re.b]) {
-                        j.committed[(int64_t)re.b * j.K + re.h] = win;
-                    }
-                } else {
-                    unsigned k = atomicAdd(j.ctl + C_RESCUE_N, 1u);
-                    RescueEntry x;
-                    x.b = re.b;
-                    x.kind = 1;
-                    x.h = re.h;
-                    x.resid = 1;
-                    x.Lp = 0;
-                    x.Lq = 0;
-                    x.flags = 0;
-                    x.pad[0] = x.pad[1] = x.pad[2] = 0;
-                    j.rescue[k] = x;
-                }
-            }
-        }
+        resid_item<In>(j, sm, gt, skip, e, c, re);
     }
     if (threadIdx.x == 0) {
         __threadfence();
