@@ -41,7 +41,7 @@ namespace sv {
 #endif
 constexpr int kConsumerWarps = SV_CONSUMER_WARPS;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kPassThreads = kConsumers + 64;     // + a producer and a finalizer warp
+constexpr int kPassThreads = kConsumers + 96;     // + producer, finalizer and planner warps
 constexpr int kStageBytes = SV_STAGE_BYTES;       // one bulk copy
 constexpr int kStageVecs = kStageBytes / 16;      // 16-byte vectors per stage
 constexpr int kVecsPerThread = kStageVecs / kConsumers;
@@ -137,6 +137,19 @@ __device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
                  : "memory");
+}
+
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)

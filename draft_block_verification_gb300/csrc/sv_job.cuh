@@ -102,7 +102,7 @@ struct Job {
     unsigned *tvdone;   // [B * K]
     int tv_chunks;
     double *rpart;      // residual / fp64 scratch
-    unsigned *rdone;    // [B * 64] per-entry chunk counters
+    unsigned *rdone;    // [B * 4] per-entry counters
     int resid_chunks;
     int *err;
     const float *gtab;     // [kGTab] G bounds of ordinary ids

@@ -55,6 +55,21 @@ struct StageMeta {
     RowMode rm;       // row mode of the unit
 };
 
+// The planner warp's plan of the units this CTA streams next, handed to the
+// producer through a small queue: everything the producer needs, so that no
+// global-memory latency sits between two units' copies.
+constexpr int kPlanQ = 8;
+struct PlanEntry {
+    int kind;         // 0: part of a row, -1: no more units
+    int rec, b;       // record; sequence
+    unsigned expect;  // records that complete sequence b
+    int xid;          // vocabulary id whose logit the unit records (-1: none)
+    int vs, ve;       // the unit's vectors [vs, ve) of the row
+    int pad;
+    const char *row;  // the unit's logit row
+    RowMode rm;
+};
+
 // One consumer warp's share of a unit.
 struct WarpPart {
     float m;
@@ -94,6 +109,8 @@ struct PassShared {
     int seed_cnt[2];     // ids listed in a buffer
     int seed_n;
     int seed_more;
+    PlanEntry plan[kPlanQ];
+    uint64_t plan_full[kPlanQ], plan_empty[kPlanQ];
     volatile int nunits;     // units this CTA streamed (set when the producer is done)
     volatile int prod_done;
     int todo[kFinQ];         // sequences whose decision step is due (finalizer only)
@@ -1392,9 +1409,13 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
     TState s;
     tstate_init(s);
     constexpr int E = VecTraits<In>::N;
-    const int sb = uh.lu & 1;  // this unit's seed buffer
+    // pf_next: (record << 1 | buffer) of the unit whose top ids were listed
+    // and copied a unit ago, or -1.  Residual units may stream between a unit
+    // and the one it prefetched for, so the buffer travels with the record.
+    const bool pre = pf_next >= 0 && (pf_next >> 1) == uh.unit;
+    const int sb = pre ? (pf_next & 1) : (pf_next >= 0 ? (pf_next & 1) ^ 1 : 0);
     if (MODE & M_GUMBEL) {
-        if (pf_next == uh.unit) {
+        if (pre) {
             s.g = seed_eval<In>(sm, sb, s.g, rm, tslot);  // listed and copied a unit ago
         } else if (seed_list(sm, sb, rm.key, m0.vbase * E, m0.vend * E)) {
             seed_copy<In>(sm, sb, m0.row);
@@ -1410,7 +1431,7 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
         const bool fits = seed_list(sm, nb, m0.nkey, m0.nlo, m0.nhi);
         if (fits)
             seed_copy<In>(sm, nb, m0.nrow);
-        pf_next = fits ? m0.nrec : -1;  // the same on every consumer thread
+        pf_next = fits ? (m0.nrec << 1) | nb : -1;  // the same on every consumer thread
     } else {
         pf_next = -1;
     }
@@ -1491,6 +1512,58 @@ __device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsi
     }
 }
 
+// ---------------------------------------------------------------------------
+// The planner warp (lane 0): takes units from the global counter, loads their
+// per-sequence values and works out their row modes and records, and queues
+// them for the producer -- kPlanQ units ahead, so the producer never waits on
+// global memory between two units.  Ends the queue with a kind -1 entry.
+// ---------------------------------------------------------------------------
+template <int KIND>
+__device__ void planner_loop(const Job &j, PassShared &sm)
+{
+    if ((threadIdx.x & 31) != 0)
+        return;
+    long long n = 0;  // entries queued
+    bool ok = true;
+    auto push = [&](const PlanEntry &pe) {
+        const int q = (int)(n % kPlanQ);
+        if (!mbar_wait(&sm.plan_empty[q], (uint32_t)((n / kPlanQ) & 1) ^ 1u)) {
+            ok = false;
+            return;
+        }
+        sm.plan[q] = pe;
+        mbar_arrive(&sm.plan_full[q]);  // release: the producer sees the entry
+        ++n;
+    };
+    long long u = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
+    UnitPre pre = unit_prefetch(j, u);
+    while (ok && u < j.total_units) {
+        const long long un = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
+        const UnitPre pn = unit_prefetch(j, un);
+        const UnitInfo ci = unit_info(j, u, pre);
+        if (ci.valid) {
+            PlanEntry pe;
+            pe.kind = 0;
+            pe.rec = ci.rec;
+            pe.b = ci.b;
+            pe.expect = ci.expect;
+            pe.xid = ci.xid;
+            pe.vs = ci.part * j.part_vecs;
+            pe.ve = min(j.nvec, pe.vs + j.part_vecs);
+            pe.row = slot_row(j, ci.b, ci.slot);
+            pe.rm = ci.rm;
+            push(pe);
+        }
+        u = un;
+        pre = pn;
+    }
+    if (!ok)
+        latch(j.err, SV_ERR_TIMEOUT);
+    PlanEntry end;
+    end.kind = -1;
+    push(end);
+}
+
 template <typename In, int KIND>
 __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
     pass_kernel(const __grid_constant__ Job j)
@@ -1512,6 +1585,10 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             mbar_init(&sm.ubar[q], kConsumerWarps);
             mbar_init(&sm.ufree[q], 1);
         }
+        for (int q = 0; q < kPlanQ; ++q) {
+            mbar_init(&sm.plan_full[q], 1);
+            mbar_init(&sm.plan_empty[q], 1);
+        }
         sm.abort = 0;
         sm.nunits = 0;
         sm.prod_done = 0;
@@ -1524,14 +1601,18 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             sm.skip[i] = __ldg(j.skip + i);
     __syncthreads();
 
-    if (t >= kConsumers + 32) {
+    if (t >= kConsumers + 64) {
+        // ---------------- planner warp ----------------
+        planner_loop<KIND>(j, sm);
+    } else if (t >= kConsumers + 32) {
         // ---------------- finalizer warp ----------------
         finalizer_loop<KIND>(j, sm);
     } else if (t >= kConsumers) {
         // ---------------- producer warp ----------------
-        // Lane 0 streams unit `cu`.  Two units are prepared ahead: the next
-        // unit's info is ready while this one streams (its per-sequence values
-        // were loaded a unit earlier), so the first stage can name it.
+        // Lane 0 streams the planned units in order.  The entry after the
+        // current one is read too: if it carries a Gumbel-max, the current
+        // unit's first stage names it, so that the consumers list and copy
+        // its top ids while this unit streams.
         if (t == kConsumers) {
             int stage = 0;
             uint32_t phase = 0;
@@ -1539,80 +1620,68 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             int lu = 0;                       // local unit number
             bool ok = true;
             const int E = j.dtype == SV_BF16 ? 8 : 4;
-            long long cu = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
-            long long nu = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
-            const UnitPre cp0 = unit_prefetch(j, cu);
-            UnitPre np = unit_prefetch(j, nu);
-            long long nnu = nu < j.total_units ? (long long)atomicAdd(j.ctl + C_UNIT, 1u) : nu;
-            UnitInfo ci;
-            ci.valid = false;
-            if (cu < j.total_units)
-                ci = unit_info(j, cu, cp0);
-            while (cu < j.total_units) {
-                UnitInfo ni;
-                ni.valid = false;
-                if (nu < j.total_units)
-                    ni = unit_info(j, nu, np);
-                const UnitPre nnp = unit_prefetch(j, nnu);
-                const long long n3 =
-                    nnu < j.total_units ? (long long)atomicAdd(j.ctl + C_UNIT, 1u) : nnu;
-                if (ci.valid) {
-                    const char *row = slot_row(j, ci.b, ci.slot);
-                    const int vs = ci.part * j.part_vecs;
-                    const int ve = min(j.nvec, vs + j.part_vecs);
-                    // the next streamed unit (the next valid one) if it seeds
-                    const bool nseed = ni.valid && (ni.rm.mode & M_GUMBEL);
-                    for (int v = vs; v < ve; v += kStageVecs) {
-                        const int nv = min(kStageVecs, ve - v);
-                        if (!mbar_wait(&sm.empty[stage], phase ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        pend &= ~(1u << stage);  // the consumers released it: its copy landed
-                        StageMeta &mt = sm.meta[stage];
-                        mt.unit = ci.rec;
-                        mt.nv = nv;
-                        mt.vbase = v;
-                        mt.first = (v == vs);
-                        mt.last = (v + kStageVecs >= ve);
-                        mt.lu = lu;
-                        mt.b = ci.b;
-                        mt.expect = ci.expect;
-                        mt.xid = ci.xid;
-                        mt.row = row;
-                        mt.vend = ve;
-                        mt.rm = ci.rm;
-                        mt.nrec = -1;
-                        if (v == vs) {
-                            sm.thr[lu % kStages] = f2ord(-INFINITY);
-                            if (nseed) {
-                                const int nvs = ni.part * j.part_vecs;
-                                mt.nrec = ni.rec;
-                                mt.nrow = slot_row(j, ni.b, ni.slot);
-                                mt.nkey = ni.rm.key;
-                                mt.nlo = nvs * E;
-                                mt.nhi = min(j.nvec, nvs + j.part_vecs) * E;
-                            }
-                        }
-                        mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
-                        bulk_g2s(stages + (size_t)stage * kStageBytes, row + (int64_t)v * 16,
-                                 (uint32_t)nv * 16u, &sm.full[stage]);
-                        pend |= 1u << stage;
-                        pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
+            for (long long pi = 0;; ++pi) {
+                const int q = (int)(pi % kPlanQ);
+                if (!mbar_wait(&sm.plan_full[q], (uint32_t)((pi / kPlanQ) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const PlanEntry &ce = sm.plan[q];
+                if (ce.kind < 0)
+                    break;
+                // The next entry only if it is already queued: waiting for it
+                // here could wait on a decision that needs this very unit.
+                const int q1 = (int)((pi + 1) % kPlanQ);
+                const bool have_next =
+                    mbar_test(&sm.plan_full[q1], (uint32_t)(((pi + 1) / kPlanQ) & 1));
+                const PlanEntry &ne = sm.plan[q1];
+                const int step = kStageVecs;
+                const bool nseed = have_next && ne.kind == 0 && (ne.rm.mode & M_GUMBEL);
+                for (int v = ce.vs; v < ce.ve; v += step) {
+                    const int nv = min(step, ce.ve - v);
+                    if (!mbar_wait(&sm.empty[stage], phase ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    pend &= ~(1u << stage);  // the consumers released it: its copy landed
+                    StageMeta &mt = sm.meta[stage];
+                    mt.unit = ce.rec;
+                    mt.nv = nv;
+                    mt.vbase = v;
+                    mt.first = (v == ce.vs);
+                    mt.last = (v + step >= ce.ve);
+                    mt.lu = lu;
+                    mt.b = ce.b;
+                    mt.expect = ce.expect;
+                    mt.xid = ce.xid;
+                    mt.row = ce.row;
+                    mt.vend = ce.ve;
+                    mt.rm = ce.rm;
+                    mt.nrec = -1;
+                    if (v == ce.vs) {
+                        sm.thr[lu % kStages] = f2ord(-INFINITY);
+                        if (nseed) {
+                            mt.nrec = ne.rec;
+                            mt.nrow = ne.row;
+                            mt.nkey = ne.rm.key;
+                            mt.nlo = ne.vs * E;
+                            mt.nhi = ne.ve * E;
                         }
                     }
-                    if (!ok)
-                        break;
-                    ++lu;
+                    mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
+                    bulk_g2s(stages + (size_t)stage * kStageBytes, ce.row + (int64_t)v * 16,
+                             (uint32_t)nv * 16u, &sm.full[stage]);
+                    pend |= 1u << stage;
+                    pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                ci = ni;
-                cu = nu;
-                nu = nnu;
-                np = nnp;
-                nnu = n3;
+                if (!ok)
+                    break;
+                ++lu;
+                mbar_arrive(&sm.plan_empty[q]);  // the planner may reuse the slot
             }
             if (ok && mbar_wait(&sm.empty[stage], phase ^ 1u)) {
                 pend &= ~(1u << stage);
@@ -1640,7 +1709,7 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         // ---------------- consumer warps ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int pf_next = -1;  // record of the next unit whose top ids were prefetched
+        int pf_next = -1;  // (record << 1 | buffer) of a unit whose top ids were prefetched
         for (;;) {
             if (!mbar_wait(&sm.full[stage], phase)) {
                 latch(j.err, SV_ERR_TIMEOUT);

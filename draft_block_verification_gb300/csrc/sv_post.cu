@@ -8,7 +8,7 @@
 //                 fell inside their error bound.
 #include <math.h>
 
-#include "sv_common.cuh"
+#include "sv_resid.cuh"
 
 namespace sv {
 
@@ -214,16 +214,10 @@ __global__ void __launch_bounds__(kPostThreads) tv_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
-// Residual draw.  At the first rejection, the correction is the Gumbel-max of
-// log w_v + G(v) with w = [p - q]_+ ([SPOT] App. B eq. 14; [PackedSS] Alg. 2
-// line 7).  With a = x/Tp, b = y/Tq and Delta = Lq - Lp,
-//   log w_v = a_v - Lp + log(1 - exp(b_v - a_v - Delta))   (when b - a < Delta);
-// dropping the common -Lp, every score is bracketed for Delta in [dlo, dhi]
-// (the log-sum-exps carry the fp32 error bound of the streaming pass, or the
-// fp64 rounding on the fp64 path).  The scan uses the three-level filter of
-// sv_gumbel.cuh: the table bound ignores log(1 - .) <= 0, survivors get fp32
-// intervals (fp64 ones on the fp64 path), and the two best candidates are
-// certified or re-scored in fp64.
+// Residual pass (the scores and their intervals are in sv_resid.cuh): one
+// row pair per sequence that rejected, in chunks scanned by different CTAs
+// and merged by the last one; Packed-SS calls first need the stored
+// proposal row's log-sum-exp.
 // ---------------------------------------------------------------------------
 struct RBest {  // fp64-interval tracker of the fp64 path
     double lo, hi, hio;
@@ -253,118 +247,7 @@ struct RBest {  // fp64-interval tracker of the fp64 path
     }
 };
 
-__device__ __forceinline__ double log1mexp(double a)  // log(1 - e^a), a < 0
-{
-    return (a > -0.6931471805599453) ? log(-expm1(a)) : log1p(-exp(a));
-}
-
-struct RCtx {
-    const char *prow, *qrow;
-    double Tp, Tq, dlo, dhi;
-    float invTp, invTq, dlo32, dhi32;  // [dlo32, dhi32] contains [dlo, dhi]
-    uint64_t key;
-};
-
-// fp64 interval of the residual score of id v (Delta bracket only); false
-// when w_v = 0 for every Delta in the bracket.
-__device__ __forceinline__ bool resid_interval64(const RCtx &c, float x, float y, uint64_t m,
-                                                 bool top, double &lo, double &hi)
-{
-    double z = (double)x / c.Tp, w = (double)y / c.Tq;
-    double ah = w - z - c.dhi;
-    if (!(ah < 0.0))
-        return false;
-    double al = w - z - c.dlo;
-    double G = gumbel64(m, top);
-    hi = z + log1mexp(ah) + G;
-    lo = (al < 0.0) ? z + log1mexp(al) + G : -INFINITY;
-    return true;
-}
-
-// log(1 - e^d), d < 0, in fp32 with a bound on its error: e = e^d carries
-// the ex2 error and the rounding of d log2(e); t = 1 - e is then off by at
-// most e (2^-21 + |d| 2^-22) + 2^-24 t, and lg2 adds 2^-22.
-__device__ __forceinline__ float log1mexp32(float d, float &err)
-{
-    const float e = ex2f(d * 1.44269504088896f);
-    const float t = 1.f - e;
-    const float r = 0.69314718055995f * lg2a(t);
-    // lg2.approx: error 2^-22 relative to max(1, |result|)
-    err = (e * (0x1p-21f + fabsf(d) * 0x1p-22f)) / t + (1.f + fabsf(r)) * 0x1p-21f;
-    return r;
-}
-
-// fp32 interval of the residual score; false when w_v = 0 for sure.
-__device__ __forceinline__ bool resid_interval32(const RCtx &c, float x, float y, uint64_t m,
-                                                 bool top, float &lo, float &hi)
-{
-    const float z = x * c.invTp, w = y * c.invTq;
-    const float dz = w - z;
-    const float edz = (fabsf(z) + fabsf(w)) * 0x1p-21f;
-    const float dmin = (dz - c.dhi32) - edz - fabsf(dz - c.dhi32) * 0x1p-22f;  // smallest d
-    const float dmax = (dz - c.dlo32) + edz + fabsf(dz - c.dlo32) * 0x1p-22f;  // largest d
-    if (dmin >= 0.f)
-        return false;
-    const float g = gumbel32(m, top);
-    float e1, lwh;
-    const float lw1 = log1mexp32(dmin, e1);
-    if (1.f - ex2f(dmin * 1.44269504088896f) > 0x1p-18f && e1 < 1.f)
-        lwh = lw1 + e1;
-    else {  // 1 - e^d <= -d
-        lwh = 0.69314718055995f * lg2a(-dmin);
-        lwh += (1.f + fabsf(lwh)) * 0x1p-20f;
-    }
-    float lwl = -INFINITY;
-    if (dmax < 0.f && 1.f - ex2f(dmax * 1.44269504088896f) > 0x1p-18f) {
-        float e2;
-        const float lw2 = log1mexp32(dmax, e2);
-        if (e2 < 1.f)
-            lwl = lw2 - e2;
-    }
-    const float sh = z + lwh + g, sl = z + lwl + g;
-    const float slack = (fabsf(z) + fabsf(sh)) * 0x1p-21f + kG32Err;
-    hi = sh + slack;
-    lo = sl - ((fabsf(z) + fabsf(sl)) * 0x1p-21f + kG32Err);
-    return true;
-}
-
-// fp32 test that w_v = 0 for every Delta in the bracket.
-__device__ __forceinline__ bool surely_zero(const RCtx &c, float x, float y)
-{
-    float a = x * c.invTp, b = y * c.invTq;
-    float d = (b - a) - c.dhi32;
-    return d > (fabsf(a) + fabsf(b) + fabsf(c.dhi32) + 1.f) * 0x1p-20f;
-}
-
-// Candidate trackers of the scan: fp32 intervals (Cand2) or fp64 intervals.
-struct Track32 {
-    Cand2 c;
-    float lomax, thr, thrS;
-    __device__ __forceinline__ void init()
-    {
-        c.init();
-        lomax = thr = thrS = -INFINITY;
-    }
-    __device__ __forceinline__ void raise(float t)
-    {
-        if (t > thr) {
-            thr = t;
-            thrS = level1_thr(t);
-        }
-    }
-    __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint64_t m,
-                                        bool top)
-    {
-        if (surely_zero(ctx, x, y)) return;
-        float lo, hi;
-        if (!resid_interval32(ctx, x, y, m, top, lo, hi) || hi < thr) return;
-        c.add(lo, hi, (int)v);
-        if (lo > lomax) {
-            lomax = lo;
-            raise(__fsub_rd(lo, 1e-9f));
-        }
-    }
-};
+// fp64-interval candidate tracker of the fp64 path.
 struct Track64 {
     RBest r;
     float lomax, thr, thrS;
@@ -453,30 +336,6 @@ __device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out
     }
 }
 
-// Per-id screen of one vector whose bound reached the threshold: top ids are
-// skipped (the seed phase scored every top id of the chunk); an ordinary id
-// is bounded by the top byte of its fine bits.
-template <typename In, typename Tr>
-__device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, const uint4 &qy,
-                                             int k, const float *gt, const uint64_t *skip, Tr &tr)
-{
-    using VT = VecTraits<In>;
-    constexpr int E = VT::N;
-    const uint32_t v0 = (uint32_t)k * E;
-    const uint32_t tm = top_mask(c.key, v0 >> 8, (int)(v0 & 255u), E, skip);
-#pragma unroll 1
-    for (int i = 0; i < E; ++i) {
-        if ((tm >> i) & 1u)
-            continue;
-        const uint32_t v = v0 + i;
-        const float xi = VT::elem(qx, i);
-        const uint64_t m = fine52(c.key, v);
-        if (fmaf(xi, c.invTp, gt[(int)(m >> 44)]) < tr.thrS)
-            continue;
-        tr.add(c, xi, VT::elem(qy, i), v, m, false);
-    }
-}
-
 // Seed of a scan over vectors [vb, ve): the CTA scores every top id of the
 // range (a couple of skip draws per block of 256 ids) and shares the best
 // lower end as the threshold.
@@ -488,20 +347,8 @@ __device__ __forceinline__ void resid_seed(const RCtx &c, int vb, int ve, const 
     constexpr int E = VT::N;
     if (threadIdx.x == 0) sm.thr = f2ord(-INFINITY);
     __syncthreads();
-    const uint32_t lo = (uint32_t)vb * E, hi = (uint32_t)ve * E;
-    for (uint32_t beta = (lo >> 8) + threadIdx.x; beta <= ((hi - 1) >> 8); beta += blockDim.x) {
-        int pos = -1;
-        for (int i = 0; i < 257; ++i) {
-            pos = next_top(c.key, beta, i, pos, skip);
-            const uint32_t v = beta * 256u + (uint32_t)pos;
-            if (pos > 255 || v >= hi)
-                break;
-            if (v < lo)
-                continue;
-            tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v, fine52(c.key, v),
-                   true);
-        }
-    }
+    seed_top_ids<In>(c, (uint32_t)vb * E, (uint32_t)ve * E, skip, (int)threadIdx.x,
+                     (int)blockDim.x, tr);
     atomicMax(&sm.thr, f2ord(tr.thr));
     __syncthreads();
     tr.raise(ord2f(sm.thr));
@@ -555,20 +402,6 @@ __device__ __forceinline__ double *resid_rec(const Job &j, int e, int c)
     return j.rpart + ((int64_t)e * kResidChunks + c) * 8;
 }
 
-__device__ __forceinline__ void fill_ctx(const Job &j, RCtx &ctx, const char *prow, const char *qrow,
-                                         double D, double eD)
-{
-    ctx.prow = prow;
-    ctx.qrow = qrow;
-    ctx.Tp = j.Tp;
-    ctx.Tq = (j.kind == K_PACKED) ? j.Tp : j.Tq;
-    ctx.dlo = D - eD;
-    ctx.dhi = D + eD;
-    ctx.invTp = j.invTp;
-    ctx.invTq = (float)(1.0 / ctx.Tq);
-    ctx.dlo32 = __double2float_rd(ctx.dlo);
-    ctx.dhi32 = __double2float_ru(ctx.dhi);
-}
 
 // One item of the residual pass: chunk c of the row pair of entry e.  Scans
 // the chunk, stores its candidates, and the last chunk of the pair to finish
@@ -579,11 +412,8 @@ __device__ __forceinline__ void resid_item(const Job &j, PostShared &sm, const f
                                            const ResidEntry &re)
 {
     unsigned *cnt = j.rdone + (int64_t)e * 4;
-    const double D = re.Lq - re.Lp;
-    const double eD = 1.001 * (re.epsp + re.epsq) + 1e-14 * (fabs(re.Lp) + fabs(re.Lq));
     RCtx ctx;
-    fill_ctx(j, ctx, re.prow, re.qrow, D, eD);
-    ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
+    resid_ctx(j, re, ctx);
     Track32 tr;
     resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
                    chunk_lo(j.nvec, c + 1, kResidChunks), gt, skip, sm, tr);
@@ -629,44 +459,7 @@ __device__ __forceinline__ void resid_item(const Job &j, PostShared &sm, const f
         return;
     cnt[1] = 0u;
     cnt[2] = 0u;
-    // certify in fp32, else re-score the two contenders in fp64
-    int win = -1;
-    if (gumbel_certified(all)) {
-        win = all.v1;
-    } else if (all.v1 >= 0) {
-        double l1 = -INFINITY, h1 = -INFINITY, l2 = -INFINITY, h2 = -INFINITY;
-        float x1 = load_logit(j, re.prow, all.v1), y1 = load_logit(j, re.qrow, all.v1);
-        resid_interval64(ctx, x1, y1, fine52(ctx.key, all.v1), is_top(ctx.key, all.v1, skip),
-                         l1, h1);
-        if (all.v2 >= 0) {
-            float x2 = load_logit(j, re.prow, all.v2), y2 = load_logit(j, re.qrow, all.v2);
-            resid_interval64(ctx, x2, y2, fine52(ctx.key, all.v2),
-                             is_top(ctx.key, all.v2, skip), l2, h2);
-        }
-        const double others = (double)all.hi3;
-        if (l1 > fmax(h2, others) + kFlagEps) win = all.v1;
-        else if (l2 > fmax(h1, others) + kFlagEps) win = all.v2;
-    }
-    if (win >= 0 && !j.force_rescue) {
-        if (j.kind == K_SAMPLE) {
-            j.next[re.b] = win;
-            if (j.flags) j.flags[re.b] = 0;
-        } else if (re.h < j.commit_len[re.b]) {
-            j.committed[(int64_t)re.b * j.K + re.h] = win;
-        }
-    } else {
-        unsigned k = atomicAdd(j.ctl + C_RESCUE_N, 1u);
-        RescueEntry x;
-        x.b = re.b;
-        x.kind = 1;
-        x.h = re.h;
-        x.resid = 1;
-        x.Lp = 0;
-        x.Lq = 0;
-        x.flags = 0;
-        x.pad[0] = x.pad[1] = x.pad[2] = 0;
-        j.rescue[k] = x;
-    }
+    resid_resolve(j, re, ctx, all, skip);
 }
 
 template <typename In>
