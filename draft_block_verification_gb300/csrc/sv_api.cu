@@ -29,7 +29,6 @@ struct sv_handle {
     int device = 0;
     int sms = 0;
     int pass_blocks = 1;   // resident streaming CTAs per SM
-    int post_blocks = 1;   // resident residual-kernel CTAs per SM
     int tv_blocks = 1;     // resident total-variation CTAs per SM
     int *d_err = nullptr;
     unsigned *d_ctl = nullptr;
@@ -267,7 +266,7 @@ sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post
     if (e != cudaSuccess) return cuda_status(e);
     if (!post) return SV_OK;
     return cuda_status(
-        post_launch(j, h->sms * h->tv_blocks, h->sms * h->post_blocks, h->sms, tv, s));
+        post_launch(j, h->sms * h->tv_blocks, j.B * kResidChunksHost, h->sms, tv, s));
 }
 
 }  // namespace
@@ -305,7 +304,6 @@ sv_status sv_create(sv_handle **out)
     h->pass_blocks = std::max(nb, 1);
     if (e == cudaSuccess) e = post_setup(pb);
     h->tv_blocks = std::max(1, pb[0]);
-    h->post_blocks = std::max(1, pb[1]);
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_ctl, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_gtab, kGTab * sizeof(float));

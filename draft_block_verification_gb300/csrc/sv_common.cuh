@@ -273,4 +273,20 @@ static __device__ void packed_commit(const Job &j, int b, int h, int c, bool c_k
     }
 }
 
+// Launch configuration that allows programmatic dependent launch: the
+// kernel may be scheduled while the previous kernel of the stream finishes
+// (it calls pdl_wait before it touches global memory).
+inline void pdl_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&at)[1], dim3 grid,
+                       dim3 block, size_t smem, cudaStream_t s)
+{
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+}
+
 }  // namespace sv

@@ -187,6 +187,24 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Programmatic dependent launch (sm_90+).  pdl_wait blocks until the kernel
+// that precedes this one in the stream has completed and its writes are
+// visible (a no-op for a kernel launched without the attribute); every
+// kernel of the library calls it before it touches global memory.
+// pdl_trigger lets the next kernel of the stream be scheduled early: its
+// CTAs take SM resources as this kernel's CTAs exit and then wait in
+// pdl_wait, which hides the launch gap.  A kernel triggers only once all its
+// CTAs are running, so the next kernel can never take resources that this
+// kernel's own CTAs still need.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_sync(int id, int nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -114,6 +114,7 @@ struct PassShared {
     volatile int nunits;     // units this CTA streamed (set when the producer is done)
     volatile int prod_done;
     int todo[kFinQ];         // sequences whose decision step is due (finalizer only)
+    int fin_qh, fin_qt;      // decision steps the finalizer left for the whole CTA
 };
 
 // Per-sequence values a unit's bookkeeping needs, loaded one unit ahead.
@@ -1156,8 +1157,11 @@ __device__ __forceinline__ unsigned merge_units(const Job &j, PassShared &sm, in
 // The finalizer warp: merges unit partials in local-unit order, all units
 // that are complete at once, and runs the decision steps of completed
 // sequences, until the producer is done and every unit it streamed is
-// merged.  Waits are bounded by a spin limit that restarts whenever work is
-// found.
+// merged.  Once the producer is done it only queues decision steps: the
+// steps still queued when it returns are run by every warp of the CTA at
+// once (end_decisions), so that a CTA that completes several sequences at the
+// end of the pass does not run their steps one after another.  Waits are
+// bounded by a spin limit that restarts whenever work is found.
 template <int KIND>
 __device__ void finalizer_loop(const Job &j, PassShared &sm)
 {
@@ -1180,6 +1184,7 @@ __device__ void finalizer_loop(const Job &j, PassShared &sm)
                 dm &= dm - 1;
                 const int b = __shfl_sync(0xFFFFFFFFu, seq, i);
                 if (qt - qh < kFinQ) {
+                    __syncwarp();  // every lane has read the slot it may overwrite
                     if (lane == 0)
                         sm.todo[qt % kFinQ] = b;
                     ++qt;
@@ -1192,7 +1197,11 @@ __device__ void finalizer_loop(const Job &j, PassShared &sm)
             spin = 0;
             continue;
         }
-        if (qh < qt) {
+        int pdone = 0;
+        if (lane == 0)
+            pdone = sm.prod_done;
+        pdone = __shfl_sync(0xFFFFFFFFu, pdone, 0);
+        if (qh < qt && !pdone) {
             const int b = sm.todo[qh % kFinQ];
             ++qh;
             fin_kind<KIND>(j, b);
@@ -1201,7 +1210,7 @@ __device__ void finalizer_loop(const Job &j, PassShared &sm)
         }
         int fin = 0;
         if (lane == 0)
-            fin = sm.prod_done && cu >= sm.nunits;
+            fin = pdone && cu >= sm.nunits;
         if (__shfl_sync(0xFFFFFFFFu, fin, 0))
             break;
         if (++spin > kSpinLimit) {
@@ -1212,6 +1221,22 @@ __device__ void finalizer_loop(const Job &j, PassShared &sm)
         if (spin > 64)
             __nanosleep(SV_SPIN_SLEEP_NS);
     }
+    __syncwarp();
+    if (lane == 0) {
+        sm.fin_qh = qh;
+        sm.fin_qt = qt;
+    }
+}
+
+// The decision steps the finalizer left queued, a warp per step (every warp
+// of the CTA calls it after the CTA-wide barrier that follows the loops).
+template <int KIND>
+__device__ __forceinline__ void end_decisions(const Job &j, PassShared &sm)
+{
+    constexpr int kWarps = kPassThreads / 32;
+    const int qh = sm.fin_qh, qt = sm.fin_qt;
+    for (int i = qh + (int)(threadIdx.x >> 5); i < qt; i += kWarps)
+        fin_kind<KIND>(j, sm.todo[i % kFinQ]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1538,6 +1563,15 @@ __device__ void planner_loop(const Job &j, PassShared &sm)
     long long u = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
     UnitPre pre = unit_prefetch(j, u);
     while (ok && u < j.total_units) {
+        // Near the end of the pass, claim a unit only once the producer has
+        // taken all but one queued entry: units claimed ahead are this CTA's
+        // alone, and a deep queue at the end would leave CTAs finishing
+        // several units apart.
+        if (j.total_units - u < 2LL * gridDim.x && n >= 2 &&
+            !mbar_wait(&sm.plan_empty[(n - 2) % kPlanQ], (uint32_t)(((n - 2) / kPlanQ) & 1))) {
+            ok = false;
+            break;
+        }
         const long long un = (long long)atomicAdd(j.ctl + C_UNIT, 1u);
         const UnitPre pn = unit_prefetch(j, un);
         const UnitInfo ci = unit_info(j, u, pre);
@@ -1592,8 +1626,11 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         sm.abort = 0;
         sm.nunits = 0;
         sm.prod_done = 0;
+        sm.fin_qh = sm.fin_qt = 0;
         mbar_fence_init();
     }
+    pdl_wait();
+    pdl_trigger();
     for (int i = t; i < kGTab; i += blockDim.x)
         gt[i] = __ldg(j.gtab + i);
     if (j.skip)
@@ -1724,6 +1761,8 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         cp_async_wait_all();  // no copy may be in flight when the CTA exits
     }
     __syncthreads();
+    end_decisions<KIND>(j, sm);
+    __syncthreads();
     if (t == 0) {
         __threadfence();
         unsigned old = atomicAdd(j.ctl + C_EXIT, 1u);
@@ -1783,24 +1822,22 @@ cudaError_t pass_setup(int *blocks_per_sm)
 }
 
 template <typename In>
-static void launch_in(const Job &j, int grid, cudaStream_t s)
+static cudaError_t launch_in(const Job &j, int grid, cudaStream_t s)
 {
-    const size_t smem = pass_smem_bytes();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    pdl_config(cfg, at, dim3(grid), dim3(kPassThreads), pass_smem_bytes(), s);
     switch (j.kind) {
-    case K_GREEDY: pass_kernel<In, K_GREEDY><<<grid, kPassThreads, smem, s>>>(j); break;
-    case K_SAMPLE: pass_kernel<In, K_SAMPLE><<<grid, kPassThreads, smem, s>>>(j); break;
-    case K_TREE: pass_kernel<In, K_TREE><<<grid, kPassThreads, smem, s>>>(j); break;
-    default: pass_kernel<In, K_PACKED><<<grid, kPassThreads, smem, s>>>(j); break;
+    case K_GREEDY: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_GREEDY>, j);
+    case K_SAMPLE: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_SAMPLE>, j);
+    case K_TREE: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_TREE>, j);
+    default: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_PACKED>, j);
     }
 }
 
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s)
 {
-    if (j.dtype == SV_BF16)
-        launch_in<uint16_t>(j, grid, s);
-    else
-        launch_in<float>(j, grid, s);
-    return cudaGetLastError();
+    return j.dtype == SV_BF16 ? launch_in<uint16_t>(j, grid, s) : launch_in<float>(j, grid, s);
 }
 
 }  // namespace sv

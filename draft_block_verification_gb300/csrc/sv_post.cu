@@ -7,6 +7,7 @@
 //   rescue_kernel the fp64 path for the rare sequences whose fp32 decisions
 //                 fell inside their error bound.
 #include <math.h>
+#include <stddef.h>
 
 #include "sv_resid.cuh"
 
@@ -148,6 +149,8 @@ template <typename In>
 __global__ void __launch_bounds__(kPostThreads) tv_kernel(const __grid_constant__ Job j)
 {
     __shared__ PostShared sm;
+    pdl_wait();
+    pdl_trigger();
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
     const int TC = j.tv_chunks;
@@ -307,6 +310,8 @@ __device__ __forceinline__ void block_rbest(RBest &r, PostShared &sm, RBest &out
     }
 }
 
+// Merged candidates of the CTA, in thread 0's `out` (the other threads get an
+// empty set).
 __device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out)
 {
     warp_cand2(c);
@@ -323,6 +328,8 @@ __device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out
     }
     __syncthreads();
     out.init();
+    if (threadIdx.x != 0)
+        return;
     for (int q = 0; q < kPostWarps; ++q) {
         Cand2 t;
         t.hi1 = sm.f[q][0];
@@ -397,154 +404,322 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const
     }
 }
 
-__device__ __forceinline__ double *resid_rec(const Job &j, int e, int c)
-{
-    return j.rpart + ((int64_t)e * kResidChunks + c) * 8;
-}
+// Vectors per warp queued for the per-id screen of the residual scan.
+constexpr int kRQ = 64;
+constexpr int kScanAhead = 8;  // vectors per thread loaded together
 
+constexpr int kSeedPer = 4;  // listed top ids each thread scores from registers
+constexpr int kSeedList = kSeedPer * kPostThreads;
 
-// One item of the residual pass: chunk c of the row pair of entry e.  Scans
-// the chunk, stores its candidates, and the last chunk of the pair to finish
-// merges them and draws the correction.
+struct ResidQueue {
+    uint4 d[kPostWarps][kRQ];
+    int v[kPostWarps][kRQ];
+    uint32_t ids[kSeedList];  // top ids of the row
+    int nids;
+};
+
+// Scores every top id of ids [lo, hi) into tr.  First the CTA lists them in
+// shared memory (threads take blocks of 256 ids in turn: a couple of skip
+// draws each); then each thread loads the logits of its share of the list at
+// once, into registers, and scores them, so a thread waits for one round of
+// loads.  Ids past the list's capacity (far beyond the expected count) are
+// scored where they are found.
 template <typename In>
-__device__ __forceinline__ void resid_item(const Job &j, PostShared &sm, const float *gt,
-                                           const uint64_t *skip, int e, int c,
-                                           const ResidEntry &re)
+__device__ __forceinline__ void seed_range(const RCtx &c, uint32_t lo, uint32_t hi,
+                                           const uint64_t *skip, ResidQueue &q, Track32 &tr)
 {
-    unsigned *cnt = j.rdone + (int64_t)e * 4;
-    RCtx ctx;
-    resid_ctx(j, re, ctx);
-    Track32 tr;
-    resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),
-                   chunk_lo(j.nvec, c + 1, kResidChunks), gt, skip, sm, tr);
-    Cand2 best;
-    block_cand2(tr.c, sm, best);
-    if (threadIdx.x == 0) {
-        double *rec = resid_rec(j, e, c);
-        rec[0] = best.hi1;
-        rec[1] = best.lo1;
-        rec[2] = best.hi2;
-        rec[3] = best.lo2;
-        rec[4] = best.hi3;
-        rec[5] = (double)best.v1;
-        rec[6] = (double)best.v2;
-        __threadfence();
-        sm.flag = atomicAdd(cnt + 1, 1u) + 1u == (unsigned)kResidChunks;
+    using VT = VecTraits<In>;
+    const int t = threadIdx.x;
+    if (t == 0) q.nids = 0;
+    __syncthreads();
+    const uint32_t b1 = hi > lo ? ((hi - 1u) >> 8) + 1u : 0u;
+    for (uint32_t beta = (lo >> 8) + (uint32_t)t; beta < b1; beta += kPostThreads) {
+        int pos = -1;
+        for (int i = 0; i < kSkipN; ++i) {
+            pos = next_top(c.key, beta, i, pos, skip);
+            const uint32_t v = beta * 256u + (uint32_t)pos;
+            if (pos > 255 || v >= hi)
+                break;
+            if (v < lo)
+                continue;
+            const int slot = atomicAdd(&q.nids, 1);
+            if (slot < kSeedList)
+                q.ids[slot] = v;
+            else
+                tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v,
+                       fine52(c.key, v), true);
+        }
     }
     __syncthreads();
-    const bool last = sm.flag != 0;
-    __syncthreads();  // sm.flag is reused by the next item
-    if (!last || threadIdx.x >= 32)
-        return;
-    // The pair's last chunk: the first warp gathers the chunk records in
-    // parallel (lane q holds record q) and merges them.
-    __threadfence();
-    const int lane = threadIdx.x;
-    Cand2 all;
-    all.init();
-    for (int q = lane; q < kResidChunks; q += 32) {
-        const double *rq = resid_rec(j, e, q);
-        Cand2 t;
-        t.hi1 = (float)__ldcg(rq + 0);
-        t.lo1 = (float)__ldcg(rq + 1);
-        t.hi2 = (float)__ldcg(rq + 2);
-        t.lo2 = (float)__ldcg(rq + 3);
-        t.hi3 = (float)__ldcg(rq + 4);
-        t.v1 = (int)__ldcg(rq + 5);
-        t.v2 = (int)__ldcg(rq + 6);
-        all.merge(t);
+    const int n = min(q.nids, kSeedList);
+    uint32_t id[kSeedPer];
+    float x[kSeedPer], y[kSeedPer];
+#pragma unroll
+    for (int r = 0; r < kSeedPer; ++r) {
+        const int i = t + r * kPostThreads;
+        id[r] = i < n ? q.ids[i] : 0xFFFFFFFFu;
+        x[r] = y[r] = 0.f;
+        if (i < n) {
+            x[r] = VT::load1(c.prow, (int)id[r]);
+            y[r] = VT::load1(c.qrow, (int)id[r]);
+        }
     }
-    warp_cand2(all);
-    if (lane != 0)
-        return;
-    cnt[1] = 0u;
-    cnt[2] = 0u;
-    resid_resolve(j, re, ctx, all, skip);
+#pragma unroll
+    for (int r = 0; r < kSeedPer; ++r)
+        if (id[r] != 0xFFFFFFFFu)
+            tr.add(c, x[r], y[r], id[r], fine52(c.key, id[r]), true);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Per-id screen of a warp's queued vectors, one vector per lane.
+template <typename In>
+__device__ __forceinline__ void resid_flush(const RCtx &c, const ResidQueue &q, int n,
+                                            const float *gt, const uint64_t *skip, Track32 &tr)
+{
+    const int w = threadIdx.x >> 5;
+    __syncwarp();
+    for (int i = (int)(threadIdx.x & 31); i < n; i += 32) {
+        const int k = q.v[w][i];
+        resid_vector<In>(c, q.d[w][i], ldv<In>(c.qrow, k), k, gt, skip, tr);
+    }
+    __syncwarp();
+}
+
+
+// ---------------------------------------------------------------------------
+// The residual pass.  One thread-block cluster of kResidChunks CTAs per
+// residual entry; CTA r of the cluster scans chunk r of the entry's row pair.
+// The CTAs of a cluster talk through distributed shared memory: they share
+// their Gumbel thresholds while they scan (remote max-reductions into every
+// peer's word), the proposal row's log-sum-exp of a Packed-SS entry (each CTA
+// computes its chunk's partial), and their candidates at the end, which CTA 0
+// merges to draw the correction.  No global memory round trip sits between
+// the chunks of an entry.
+// ---------------------------------------------------------------------------
+struct ClusterSlot {
+    uint32_t thr;        // best published threshold (ordered float)
+    float lse[3];        // Packed-SS: this chunk's (max, scaled sum, min) of the q row
+    Cand2 cand;          // this chunk's candidates
+    double Lq, epsq;     // Packed-SS: the merged log-sum-exp, broadcast in the CTA
+};
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void peer_max(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t peer_ld_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float peer_ld_f32(uint32_t addr)
+{
+    return __uint_as_float(peer_ld_u32(addr));
+}
+// Cluster barrier (every thread of every CTA of the cluster); arrive has
+// release and wait acquire semantics, so shared-memory writes before it are
+// visible to the whole cluster after it.
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Publishes a warp's best threshold to every CTA of the cluster (lanes 0 ..
+// kResidChunks - 1 each update one peer) when it beats what the warp
+// published before.
+__device__ __forceinline__ void publish_thr(const Track32 &tr, ClusterSlot &cs, uint32_t &pub)
+{
+    const uint32_t w = __reduce_max_sync(0xFFFFFFFFu, f2ord(tr.thr));
+    if (w > pub) {
+        const int lane = threadIdx.x & 31;
+        if (lane < kResidChunks) peer_max(peer_addr(&cs.thr, (uint32_t)lane), w);
+        pub = w;
+    }
+}
+
+// Fast-path scan of vectors [vb, ve) of the pair.  The chunk of both rows is
+// prefetched into L2 (by the caller) while the CTA scores the chunk's top
+// ids.  The CTAs of the cluster share thresholds: each publishes its best
+// lower end - 1e-9 and raises its own threshold to the largest published
+// one, so every chunk is screened against (nearly) the best of the whole
+// row.  That is safe: the id behind a published value is a candidate of its
+// own chunk, so an id whose upper end stays below it can neither win nor
+// come within 1e-9 of the winner.  A vector whose largest logit can reach the
+// threshold with the ordinary-id bound is queued (compacted with a ballot)
+// and the queue is screened per id with a vector per lane, so a warp does
+// not diverge per vector.
+template <typename In>
+__device__ void resid_scan_fast(const RCtx &c, int vb, int ve, ClusterSlot &cs, const float *gt,
+                                const uint64_t *skip, ResidQueue &q, Track32 &tr)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    tr.init();
+    seed_range<In>(c, (uint32_t)vb * E, (uint32_t)ve * E, skip, q, tr);
+    uint32_t pub = 0u;
+    publish_thr(tr, cs, pub);
+    const float gmax = gt[kGTab - 1];
+    int qn = 0;
+    for (int base = vb; base < ve; base += kScanAhead * kPostThreads) {
+        uint4 px[kScanAhead];
+#pragma unroll
+        for (int u = 0; u < kScanAhead; ++u) {
+            const int k = base + t + u * kPostThreads;
+            px[u] = k < ve ? ldv<In>(c.prow, k) : VT::neg_inf_vec();
+        }
+        tr.raise(ord2f(*(volatile uint32_t *)&cs.thr));
+#pragma unroll
+        for (int u = 0; u < kScanAhead; ++u) {
+            const int k = base + t + u * kPostThreads;
+            const bool pass = fmaf(VT::hi_of(VT::pmax(px[u])), c.invTp, gmax) >= tr.thrS;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
+            if (bal) {
+                if (pass) {
+                    const int r = qn + __popc(bal & ((1u << lane) - 1u));
+                    q.d[w][r] = px[u];
+                    q.v[w][r] = k;
+                }
+                qn += __popc(bal);
+                if (qn > kRQ - 32) {
+                    resid_flush<In>(c, q, qn, gt, skip, tr);
+                    qn = 0;
+                    tr.raise(ord2f(*(volatile uint32_t *)&cs.thr));
+                }
+            }
+        }
+        publish_thr(tr, cs, pub);
+    }
+    if (qn) resid_flush<In>(c, q, qn, gt, skip, tr);
 }
 
 template <typename In>
-__global__ void __launch_bounds__(kPostThreads, SV_RESID_MIN_BLOCKS) resid_kernel(const __grid_constant__ Job j)
+__global__ void __cluster_dims__(kResidChunks, 1, 1)
+    __launch_bounds__(kPostThreads, SV_RESID_MIN_BLOCKS) resid_kernel(const __grid_constant__ Job j)
 {
     __shared__ PostShared sm;
+    __shared__ ResidQueue q;
+    __shared__ ClusterSlot cs;
     __shared__ float gt[kGTab];
     __shared__ uint64_t skip[kSkipN];  // skip thresholds of the top-id draws
-    for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
-        gt[i] = __ldg(j.gtab + i);
-    for (int i = threadIdx.x; i < kSkipN; i += blockDim.x)
-        skip[i] = __ldg(j.skip + i);
-    __syncthreads();
+    const int t = threadIdx.x;
+    const uint32_t rank = cluster_rank();
+    const int e = (int)(blockIdx.x / kResidChunks), c = (int)rank;
+    pdl_wait();
+    pdl_trigger();
     const unsigned nE = *(volatile unsigned *)(j.ctl + C_RESID_N);
-    const unsigned nA = nE * kResidChunks;
-    // CTAs take items from a counter.  Packed-SS items come in two phases
-    // (the stored proposal rows' log-sum-exps first); sampling calls have
-    // only the residual scans.
-    const bool twophase = j.kind != K_SAMPLE;
-    for (;;) {
-        if (threadIdx.x == 0) sm.item = atomicAdd(j.ctl + C_RWORK, 1u);
-        __syncthreads();
-        unsigned it = sm.item;
-        __syncthreads();
-        if (it >= (twophase ? 2 * nA : nA)) break;
-        const bool phaseA = twophase && it < nA;
-        if (twophase && !phaseA) it -= nA;
-        const int e = it / kResidChunks, c = it - e * kResidChunks;
-        unsigned *cnt = j.rdone + (int64_t)e * 4;
-        ResidEntry re = j.resid[e];
-        if (phaseA) {
-            // Proposal row's log-sum-exp (Packed-SS: the stored Q row).
-            if (!re.need_lq) continue;
-            float M, S, mn;
-            lse_chunk32<In>(re.qrow, chunk_lo(j.nvec, c, kResidChunks),
-                            chunk_lo(j.nvec, c + 1, kResidChunks), j.cp, sm, M, S, mn);
-            if (threadIdx.x == 0) {
-                double *rec = resid_rec(j, e, c);
-                rec[4] = M;
-                rec[5] = S;
-                rec[6] = mn;
-                __threadfence();
-                if (atomicAdd(cnt + 0, 1u) + 1u == (unsigned)kResidChunks) {
-                    __threadfence();
-                    double Mx = -INFINITY, mnn = INFINITY;
-                    for (int q = 0; q < kResidChunks; ++q) {
-                        Mx = fmax(Mx, __ldcg(resid_rec(j, e, q) + 4));
-                        mnn = fmin(mnn, __ldcg(resid_rec(j, e, q) + 6));
-                    }
-                    double St = 0.0;
-                    for (int q = 0; q < kResidChunks; ++q) {
-                        double *rq = resid_rec(j, e, q);
-                        St += __ldcg(rq + 5) * exp2((__ldcg(rq + 4) - Mx) * (double)j.cp);
-                    }
-                    j.resid[e].Lq = Mx / (double)j.Tp + log(St);
-                    j.resid[e].epsq = lse_rel_bound((Mx - mnn) * (double)j.cp);
-                    cnt[0] = 0u;
-                    __threadfence();
-                    atomicExch(cnt + 2, 1u);  // ready
-                }
+    if ((unsigned)e < nE) {  // the same for every CTA of the cluster
+        const ResidEntry re0 = j.resid[e];
+        const int vb = chunk_lo(j.nvec, c, kResidChunks), ve = chunk_lo(j.nvec, c + 1, kResidChunks);
+        if (t == 0) {
+            cs.thr = f2ord(-INFINITY);
+            if (ve > vb) {
+                prefetch_l2(reinterpret_cast<const uint4 *>(re0.prow) + vb, (uint32_t)(ve - vb) * 16u);
+                if (!re0.need_lq)
+                    prefetch_l2(reinterpret_cast<const uint4 *>(re0.qrow) + vb,
+                                (uint32_t)(ve - vb) * 16u);
             }
-            continue;
         }
+        for (int i = t; i < kGTab; i += blockDim.x)
+            gt[i] = __ldg(j.gtab + i);
+        for (int i = t; i < kSkipN; i += blockDim.x)
+            skip[i] = __ldg(j.skip + i);
+        ResidEntry re = re0;
         if (re.need_lq) {
-            if (threadIdx.x == 0) {
-                uint32_t it2 = 0;
-                while (*(volatile unsigned *)(cnt + 2) == 0u) {
-                    if (++it2 > kSpinLimit) {
-                        latch(j.err, SV_ERR_TIMEOUT);
-                        break;
-                    }
-                    __nanosleep(128);
-                }
-                __threadfence();
+            // Packed-SS: the stored proposal row's log-sum-exp, a partial per
+            // chunk, merged by every CTA from its peers' partials.
+            float M, S, mn;
+            lse_chunk32<In>(re.qrow, vb, ve, j.cp, sm, M, S, mn);
+            if (t == 0) {
+                cs.lse[0] = M;
+                cs.lse[1] = S;
+                cs.lse[2] = mn;
             }
             __syncthreads();
-            re.Lq = __ldcg(&j.resid[e].Lq);
-            re.epsq = __ldcg(&j.resid[e].epsq);
+            cluster_arrive();
+            cluster_wait();
+            if (t == 0) {
+                double Mx = -INFINITY, mnn = INFINITY, St = 0.0;
+                float pm[kResidChunks], ps[kResidChunks];
+                for (int r = 0; r < kResidChunks; ++r) {
+                    pm[r] = peer_ld_f32(peer_addr(&cs.lse[0], (uint32_t)r));
+                    ps[r] = peer_ld_f32(peer_addr(&cs.lse[1], (uint32_t)r));
+                    Mx = fmax(Mx, (double)pm[r]);
+                    mnn = fmin(mnn, (double)peer_ld_f32(peer_addr(&cs.lse[2], (uint32_t)r)));
+                }
+                for (int r = 0; r < kResidChunks; ++r)
+                    St += (double)ps[r] * exp2(((double)pm[r] - Mx) * (double)j.cp);
+                cs.Lq = Mx / (double)j.Tp + log(St);
+                cs.epsq = lse_rel_bound((Mx - mnn) * (double)j.cp);
+            }
+            __syncthreads();
+            re.Lq = cs.Lq;
+            re.epsq = cs.epsq;
+            if (t == 0 && ve > vb)
+                prefetch_l2(reinterpret_cast<const uint4 *>(re.qrow) + vb, (uint32_t)(ve - vb) * 16u);
+        } else {
+            __syncthreads();
+            cluster_arrive();  // cs.thr of every CTA is set before anyone publishes
+            cluster_wait();
         }
-        resid_item<In>(j, sm, gt, skip, e, c, re);
+        RCtx ctx;
+        resid_ctx(j, re, ctx);
+        Track32 tr;
+        resid_scan_fast<In>(ctx, vb, ve, cs, gt, skip, q, tr);
+        Cand2 best;
+        block_cand2(tr.c, sm, best);
+        if (t == 0) cs.cand = best;
+        __syncthreads();
+        cluster_arrive();
+        cluster_wait();
+        if (rank == 0 && t < 32) {
+            // CTA 0's first warp merges the chunks' candidates (lane r reads
+            // CTA r's) and draws the correction.
+            Cand2 all;
+            all.init();
+            if (t < kResidChunks) {
+                const uint32_t a = peer_addr(&cs.cand, (uint32_t)t);
+                all.hi1 = peer_ld_f32(a + offsetof(Cand2, hi1));
+                all.lo1 = peer_ld_f32(a + offsetof(Cand2, lo1));
+                all.hi2 = peer_ld_f32(a + offsetof(Cand2, hi2));
+                all.lo2 = peer_ld_f32(a + offsetof(Cand2, lo2));
+                all.hi3 = peer_ld_f32(a + offsetof(Cand2, hi3));
+                all.v1 = (int)peer_ld_u32(a + offsetof(Cand2, v1));
+                all.v2 = (int)peer_ld_u32(a + offsetof(Cand2, v2));
+            }
+            warp_cand2(all);
+            if (t == 0) resid_resolve(j, re, ctx, all, skip);
+        }
+        // No CTA leaves while CTA 0 may still read its shared memory.
+        cluster_arrive();
+        cluster_wait();
     }
-    if (threadIdx.x == 0) {
+    if (t == 0) {
         __threadfence();
         if (atomicAdd(j.ctl + C_REXIT, 1u) + 1u == gridDim.x) {
-            j.ctl[C_RWORK] = 0u;
             j.ctl[C_REXIT] = 0u;
             j.ctl[C_RESID_N] = 0u;
             __threadfence();
@@ -654,6 +829,9 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
 {
     __shared__ PostShared sm;
     __shared__ float gt[kGTab];
+    // No pdl_trigger: the grid barriers below need every CTA of this grid
+    // resident, so the next kernel is scheduled only once this one exits.
+    pdl_wait();
     const unsigned nR = *(volatile unsigned *)(j.ctl + C_RESCUE_N);
     if (nR == 0u) return;
     for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
@@ -858,15 +1036,18 @@ cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid
                         cudaStream_t s)
 {
     const bool bf = j.dtype == SV_BF16;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    cudaError_t e;
     if (tv) {
-        if (bf) tv_kernel<uint16_t><<<tv_grid, kPostThreads, 0, s>>>(j);
-        else tv_kernel<float><<<tv_grid, kPostThreads, 0, s>>>(j);
-        cudaError_t e = cudaGetLastError();
+        pdl_config(cfg, at, dim3(tv_grid), dim3(kPostThreads), 0, s);
+        e = bf ? cudaLaunchKernelEx(&cfg, tv_kernel<uint16_t>, j)
+               : cudaLaunchKernelEx(&cfg, tv_kernel<float>, j);
         if (e != cudaSuccess) return e;
     }
-    if (bf) resid_kernel<uint16_t><<<resid_grid, kPostThreads, 0, s>>>(j);
-    else resid_kernel<float><<<resid_grid, kPostThreads, 0, s>>>(j);
-    cudaError_t e = cudaGetLastError();
+    pdl_config(cfg, at, dim3(resid_grid), dim3(kPostThreads), 0, s);
+    e = bf ? cudaLaunchKernelEx(&cfg, resid_kernel<uint16_t>, j)
+           : cudaLaunchKernelEx(&cfg, resid_kernel<float>, j);
     if (e != cudaSuccess) return e;
     // The fp64 path's grid barriers need every CTA resident: a cooperative
     // launch guarantees it (or fails).  It returns at once when no sequence
