@@ -266,7 +266,7 @@ sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post
     if (e != cudaSuccess) return cuda_status(e);
     if (!post) return SV_OK;
     return cuda_status(
-        post_launch(j, h->sms * h->tv_blocks, j.B * kResidChunksHost, h->sms, tv, s));
+        post_launch(j, h->sms * h->tv_blocks, std::min(j.B, h->sms), h->sms, tv, s));
 }
 
 }  // namespace

@@ -361,12 +361,6 @@ __device__ __forceinline__ void resid_seed(const RCtx &c, int vb, int ve, const 
     tr.raise(ord2f(sm.thr));
 }
 
-// Resident residual CTAs per SM: several items in flight per SM hide the
-// latency chain of one item (loads, seed, screen, merge).
-#ifndef SV_RESID_MIN_BLOCKS
-#define SV_RESID_MIN_BLOCKS 4
-#endif
-
 // Scan vectors [vb, ve) of the pair.  Seed: the CTA scores every top id of
 // the chunk first (a couple of skip draws per block of 256 ids), which sets a
 // threshold close to the chunk's best; then each vector whose largest logit
@@ -404,60 +398,140 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const
     }
 }
 
-// Vectors per warp queued for the per-id screen of the residual scan.
-constexpr int kRQ = 64;
+// ---------------------------------------------------------------------------
+// The residual pass: one CTA of kResidThreads threads per residual entry
+// scans the entry's whole row pair, so no CTA waits for another: the row's
+// top ids set one threshold for the whole row, and the candidates are merged
+// inside the CTA.
+// ---------------------------------------------------------------------------
+constexpr int kResidThreads = 1024;
+constexpr int kResidWarps = kResidThreads / 32;
+constexpr int kRQ = 64;        // vectors per warp queued for the per-id screen
 constexpr int kScanAhead = 8;  // vectors per thread loaded together
+constexpr int kSeedPer = 2;    // listed top ids each thread scores from registers
+constexpr int kSeedList = kSeedPer * kResidThreads;
 
-constexpr int kSeedPer = 4;  // listed top ids each thread scores from registers
-constexpr int kSeedList = kSeedPer * kPostThreads;
-
-struct ResidQueue {
-    uint4 d[kPostWarps][kRQ];
-    int v[kPostWarps][kRQ];
-    uint32_t ids[kSeedList];  // top ids of the row
+struct ResidShared {
+    int qv[kResidWarps][kRQ];  // queued vectors (row vector index) per warp
+    uint32_t ids[kSeedList];   // top ids of the row
     int nids;
+    uint32_t thr;              // the CTA's Gumbel threshold (ordered float)
+    float f[kResidWarps][5];   // block reductions
+    int iv[kResidWarps][2];
+    double Lq, epsq;           // Packed-SS: the proposal row's log-sum-exp
 };
 
-// Scores every top id of ids [lo, hi) into tr.  First the CTA lists them in
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// fp32 log-sum-exp of a whole row with the CTA (the arithmetic and error
+// model of lse_chunk32): max, min and sum 2^((x - max) c).
+template <typename In>
+__device__ void resid_lse32(const char *row, int nvec, float c, ResidShared &rs, float &M,
+                            float &S, float &mn)
+{
+    using VT = VecTraits<In>;
+    constexpr int E = VT::N;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    float mref = -INFINITY, acc = 0.f, mx = -INFINITY, lo = INFINITY;
+    for (int base = 0; base < nvec; base += kScanAhead * kResidThreads) {
+        uint4 qv[kScanAhead];
+#pragma unroll
+        for (int u = 0; u < kScanAhead; ++u) {
+            const int k = base + t + u * kResidThreads;
+            qv[u] = k < nvec ? ldv<In>(row, k) : VT::neg_inf_vec();
+        }
+#pragma unroll
+        for (int u = 0; u < kScanAhead; ++u) {
+            float f[E];
+            VT::unpack(qv[u], f);
+            float cm = -INFINITY, cl = INFINITY;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                cm = fmaxf(cm, f[e]);
+                cl = fminf(cl, f[e]);
+            }
+            if (cm == -INFINITY)
+                continue;  // past the end of the row
+            lo = fminf(lo, cl);
+            mx = fmaxf(mx, cm);
+            if (mref == -INFINITY) {
+                mref = cm;
+            } else if ((cm - mref) * c > 64.f) {
+                acc *= ex2f((mref - cm) * c);
+                mref = cm;
+            }
+            float tt[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) tt[e] = ex2f((f[e] - mref) * c);
+#pragma unroll
+            for (int h = E / 2; h >= 1; h >>= 1)
+#pragma unroll
+                for (int e = 0; e < h; ++e) tt[e] += tt[e + h];
+            acc += tt[0];
+        }
+    }
+    const float wm = warp_max(mx), wl = warp_min(lo);
+    if (lane == 0) {
+        rs.f[w][0] = wm;
+        rs.f[w][1] = wl;
+    }
+    __syncthreads();
+    float bm = -INFINITY, bl = INFINITY;
+    for (int q = 0; q < kResidWarps; ++q) {
+        bm = fmaxf(bm, rs.f[q][0]);
+        bl = fminf(bl, rs.f[q][1]);
+    }
+    const float mine = (mref > -INFINITY) ? acc * ex2f((mref - bm) * c) : 0.f;
+    const float ws = warp_sum(mine);
+    __syncthreads();
+    if (lane == 0) rs.f[w][2] = ws;
+    __syncthreads();
+    float bs = 0.f;
+    for (int q = 0; q < kResidWarps; ++q) bs += rs.f[q][2];
+    M = bm;
+    S = bs;
+    mn = bl;
+}
+
+// Scores every top id of ids [0, V) into tr.  First the CTA lists them in
 // shared memory (threads take blocks of 256 ids in turn: a couple of skip
 // draws each); then each thread loads the logits of its share of the list at
 // once, into registers, and scores them, so a thread waits for one round of
-// loads.  Ids past the list's capacity (far beyond the expected count) are
+// loads.  Ids past the list's capacity (far beyond the expected V/256) are
 // scored where they are found.
 template <typename In>
-__device__ __forceinline__ void seed_range(const RCtx &c, uint32_t lo, uint32_t hi,
-                                           const uint64_t *skip, ResidQueue &q, Track32 &tr)
+__device__ __forceinline__ void seed_row(const RCtx &c, uint32_t V, const uint64_t *skip,
+                                         ResidShared &rs, Track32 &tr)
 {
     using VT = VecTraits<In>;
     const int t = threadIdx.x;
-    if (t == 0) q.nids = 0;
-    __syncthreads();
-    const uint32_t b1 = hi > lo ? ((hi - 1u) >> 8) + 1u : 0u;
-    for (uint32_t beta = (lo >> 8) + (uint32_t)t; beta < b1; beta += kPostThreads) {
+    const uint32_t nb = (V + 255u) >> 8;
+    for (uint32_t beta = (uint32_t)t; beta < nb; beta += kResidThreads) {
         int pos = -1;
         for (int i = 0; i < kSkipN; ++i) {
             pos = next_top(c.key, beta, i, pos, skip);
             const uint32_t v = beta * 256u + (uint32_t)pos;
-            if (pos > 255 || v >= hi)
+            if (pos > 255 || v >= V)
                 break;
-            if (v < lo)
-                continue;
-            const int slot = atomicAdd(&q.nids, 1);
+            const int slot = atomicAdd(&rs.nids, 1);
             if (slot < kSeedList)
-                q.ids[slot] = v;
+                rs.ids[slot] = v;
             else
                 tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v,
                        fine52(c.key, v), true);
         }
     }
     __syncthreads();
-    const int n = min(q.nids, kSeedList);
+    const int n = min(rs.nids, kSeedList);
     uint32_t id[kSeedPer];
     float x[kSeedPer], y[kSeedPer];
 #pragma unroll
     for (int r = 0; r < kSeedPer; ++r) {
-        const int i = t + r * kPostThreads;
-        id[r] = i < n ? q.ids[i] : 0xFFFFFFFFu;
+        const int i = t + r * kResidThreads;
+        id[r] = i < n ? rs.ids[i] : 0xFFFFFFFFu;
         x[r] = y[r] = 0.f;
         if (i < n) {
             x[r] = VT::load1(c.prow, (int)id[r]);
@@ -470,252 +544,152 @@ __device__ __forceinline__ void seed_range(const RCtx &c, uint32_t lo, uint32_t 
             tr.add(c, x[r], y[r], id[r], fine52(c.key, id[r]), true);
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Per-id screen of a warp's queued vectors, one vector per lane.
 template <typename In>
-__device__ __forceinline__ void resid_flush(const RCtx &c, const ResidQueue &q, int n,
+__device__ __forceinline__ void resid_flush(const RCtx &c, const ResidShared &rs, int n,
                                             const float *gt, const uint64_t *skip, Track32 &tr)
 {
     const int w = threadIdx.x >> 5;
     __syncwarp();
     for (int i = (int)(threadIdx.x & 31); i < n; i += 32) {
-        const int k = q.v[w][i];
-        resid_vector<In>(c, q.d[w][i], ldv<In>(c.qrow, k), k, gt, skip, tr);
+        const int k = rs.qv[w][i];
+        resid_vector<In>(c, ldv<In>(c.prow, k), ldv<In>(c.qrow, k), k, gt, skip, tr);
     }
     __syncwarp();
 }
 
-
-// ---------------------------------------------------------------------------
-// The residual pass.  One thread-block cluster of kResidChunks CTAs per
-// residual entry; CTA r of the cluster scans chunk r of the entry's row pair.
-// The CTAs of a cluster talk through distributed shared memory: they share
-// their Gumbel thresholds while they scan (remote max-reductions into every
-// peer's word), the proposal row's log-sum-exp of a Packed-SS entry (each CTA
-// computes its chunk's partial), and their candidates at the end, which CTA 0
-// merges to draw the correction.  No global memory round trip sits between
-// the chunks of an entry.
-// ---------------------------------------------------------------------------
-struct ClusterSlot {
-    uint32_t thr;        // best published threshold (ordered float)
-    float lse[3];        // Packed-SS: this chunk's (max, scaled sum, min) of the q row
-    Cand2 cand;          // this chunk's candidates
-    double Lq, epsq;     // Packed-SS: the merged log-sum-exp, broadcast in the CTA
-};
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void peer_max(uint32_t addr, uint32_t v)
-{
-    asm volatile("red.relaxed.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v)
-                 : "memory");
-}
-__device__ __forceinline__ uint32_t peer_ld_u32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float peer_ld_f32(uint32_t addr)
-{
-    return __uint_as_float(peer_ld_u32(addr));
-}
-// Cluster barrier (every thread of every CTA of the cluster); arrive has
-// release and wait acquire semantics, so shared-memory writes before it are
-// visible to the whole cluster after it.
-__device__ __forceinline__ void cluster_arrive()
-{
-    asm volatile("barrier.cluster.arrive.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait()
-{
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-
-// Publishes a warp's best threshold to every CTA of the cluster (lanes 0 ..
-// kResidChunks - 1 each update one peer) when it beats what the warp
-// published before.
-__device__ __forceinline__ void publish_thr(const Track32 &tr, ClusterSlot &cs, uint32_t &pub)
+// The warp's best threshold into the CTA's word, when it beats what the
+// warp published before.
+__device__ __forceinline__ void publish_thr(const Track32 &tr, ResidShared &rs, uint32_t &pub)
 {
     const uint32_t w = __reduce_max_sync(0xFFFFFFFFu, f2ord(tr.thr));
     if (w > pub) {
-        const int lane = threadIdx.x & 31;
-        if (lane < kResidChunks) peer_max(peer_addr(&cs.thr, (uint32_t)lane), w);
+        if ((threadIdx.x & 31) == 0) atomicMax(&rs.thr, w);
         pub = w;
     }
 }
 
-// Fast-path scan of vectors [vb, ve) of the pair.  The chunk of both rows is
-// prefetched into L2 (by the caller) while the CTA scores the chunk's top
-// ids.  The CTAs of the cluster share thresholds: each publishes its best
-// lower end - 1e-9 and raises its own threshold to the largest published
-// one, so every chunk is screened against (nearly) the best of the whole
-// row.  That is safe: the id behind a published value is a candidate of its
-// own chunk, so an id whose upper end stays below it can neither win nor
-// come within 1e-9 of the winner.  A vector whose largest logit can reach the
-// threshold with the ordinary-id bound is queued (compacted with a ballot)
-// and the queue is screened per id with a vector per lane, so a warp does
-// not diverge per vector.
+// Gumbel-max over the residual scores of the whole row pair (the row was
+// prefetched into L2 by the caller while the CTA scores the row's top ids).
+// A vector whose largest logit can reach the threshold with the ordinary-id
+// bound is queued (compacted with a ballot) and the queue is screened per id
+// with a vector per lane, so a warp does not diverge per vector.
 template <typename In>
-__device__ void resid_scan_fast(const RCtx &c, int vb, int ve, ClusterSlot &cs, const float *gt,
-                                const uint64_t *skip, ResidQueue &q, Track32 &tr)
+__device__ void resid_scan_row(const RCtx &c, int nvec, uint32_t V, const float *gt,
+                               const uint64_t *skip, ResidShared &rs, Track32 &tr)
 {
     using VT = VecTraits<In>;
-    constexpr int E = VT::N;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     tr.init();
-    seed_range<In>(c, (uint32_t)vb * E, (uint32_t)ve * E, skip, q, tr);
+    seed_row<In>(c, V, skip, rs, tr);
     uint32_t pub = 0u;
-    publish_thr(tr, cs, pub);
+    publish_thr(tr, rs, pub);
+    __syncthreads();
     const float gmax = gt[kGTab - 1];
     int qn = 0;
-    for (int base = vb; base < ve; base += kScanAhead * kPostThreads) {
+    for (int base = 0; base < nvec; base += kScanAhead * kResidThreads) {
         uint4 px[kScanAhead];
 #pragma unroll
         for (int u = 0; u < kScanAhead; ++u) {
-            const int k = base + t + u * kPostThreads;
-            px[u] = k < ve ? ldv<In>(c.prow, k) : VT::neg_inf_vec();
+            const int k = base + t + u * kResidThreads;
+            px[u] = k < nvec ? ldv<In>(c.prow, k) : VT::neg_inf_vec();
         }
-        tr.raise(ord2f(*(volatile uint32_t *)&cs.thr));
+        tr.raise(ord2f(*(volatile uint32_t *)&rs.thr));
 #pragma unroll
         for (int u = 0; u < kScanAhead; ++u) {
-            const int k = base + t + u * kPostThreads;
+            const int k = base + t + u * kResidThreads;
             const bool pass = fmaf(VT::hi_of(VT::pmax(px[u])), c.invTp, gmax) >= tr.thrS;
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
             if (bal) {
-                if (pass) {
-                    const int r = qn + __popc(bal & ((1u << lane) - 1u));
-                    q.d[w][r] = px[u];
-                    q.v[w][r] = k;
-                }
+                if (pass) rs.qv[w][qn + __popc(bal & ((1u << lane) - 1u))] = k;
                 qn += __popc(bal);
                 if (qn > kRQ - 32) {
-                    resid_flush<In>(c, q, qn, gt, skip, tr);
+                    resid_flush<In>(c, rs, qn, gt, skip, tr);
                     qn = 0;
-                    tr.raise(ord2f(*(volatile uint32_t *)&cs.thr));
+                    tr.raise(ord2f(*(volatile uint32_t *)&rs.thr));
                 }
             }
         }
-        publish_thr(tr, cs, pub);
+        publish_thr(tr, rs, pub);
     }
-    if (qn) resid_flush<In>(c, q, qn, gt, skip, tr);
+    if (qn) resid_flush<In>(c, rs, qn, gt, skip, tr);
+}
+
+// The CTA's merged candidates, in thread 0's `out`.
+__device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared &rs, Cand2 &out)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    warp_cand2(c);
+    if (lane == 0) {
+        rs.f[w][0] = c.hi1;
+        rs.f[w][1] = c.lo1;
+        rs.f[w][2] = c.hi2;
+        rs.f[w][3] = c.lo2;
+        rs.f[w][4] = c.hi3;
+        rs.iv[w][0] = c.v1;
+        rs.iv[w][1] = c.v2;
+    }
+    __syncthreads();
+    out.init();
+    if (w == 0) {
+        if (lane < kResidWarps) {
+            out.hi1 = rs.f[lane][0];
+            out.lo1 = rs.f[lane][1];
+            out.hi2 = rs.f[lane][2];
+            out.lo2 = rs.f[lane][3];
+            out.hi3 = rs.f[lane][4];
+            out.v1 = rs.iv[lane][0];
+            out.v2 = rs.iv[lane][1];
+        }
+        warp_cand2(out);
+    }
 }
 
 template <typename In>
-__global__ void __cluster_dims__(kResidChunks, 1, 1)
-    __launch_bounds__(kPostThreads, SV_RESID_MIN_BLOCKS) resid_kernel(const __grid_constant__ Job j)
+__global__ void __launch_bounds__(kResidThreads, 1) resid_kernel(const __grid_constant__ Job j)
 {
-    __shared__ PostShared sm;
-    __shared__ ResidQueue q;
-    __shared__ ClusterSlot cs;
+    __shared__ ResidShared rs;
     __shared__ float gt[kGTab];
     __shared__ uint64_t skip[kSkipN];  // skip thresholds of the top-id draws
     const int t = threadIdx.x;
-    const uint32_t rank = cluster_rank();
-    const int e = (int)(blockIdx.x / kResidChunks), c = (int)rank;
     pdl_wait();
     pdl_trigger();
     const unsigned nE = *(volatile unsigned *)(j.ctl + C_RESID_N);
-    if ((unsigned)e < nE) {  // the same for every CTA of the cluster
-        const ResidEntry re0 = j.resid[e];
-        const int vb = chunk_lo(j.nvec, c, kResidChunks), ve = chunk_lo(j.nvec, c + 1, kResidChunks);
-        if (t == 0) {
-            cs.thr = f2ord(-INFINITY);
-            if (ve > vb) {
-                prefetch_l2(reinterpret_cast<const uint4 *>(re0.prow) + vb, (uint32_t)(ve - vb) * 16u);
-                if (!re0.need_lq)
-                    prefetch_l2(reinterpret_cast<const uint4 *>(re0.qrow) + vb,
-                                (uint32_t)(ve - vb) * 16u);
-            }
-        }
-        for (int i = t; i < kGTab; i += blockDim.x)
+    if (blockIdx.x < nE) {
+        for (int i = t; i < kGTab; i += kResidThreads)
             gt[i] = __ldg(j.gtab + i);
-        for (int i = t; i < kSkipN; i += blockDim.x)
+        for (int i = t; i < kSkipN; i += kResidThreads)
             skip[i] = __ldg(j.skip + i);
-        ResidEntry re = re0;
+    }
+    for (unsigned e = blockIdx.x; e < nE; e += gridDim.x) {
+        ResidEntry re = j.resid[e];
+        if (t == 0) {
+            prefetch_l2(re.prow, (uint32_t)j.nvec * 16u);
+            prefetch_l2(re.qrow, (uint32_t)j.nvec * 16u);
+            rs.nids = 0;
+            rs.thr = f2ord(-INFINITY);
+        }
+        __syncthreads();
         if (re.need_lq) {
-            // Packed-SS: the stored proposal row's log-sum-exp, a partial per
-            // chunk, merged by every CTA from its peers' partials.
+            // Packed-SS: the stored proposal row's log-sum-exp.
             float M, S, mn;
-            lse_chunk32<In>(re.qrow, vb, ve, j.cp, sm, M, S, mn);
+            resid_lse32<In>(re.qrow, j.nvec, j.cp, rs, M, S, mn);
             if (t == 0) {
-                cs.lse[0] = M;
-                cs.lse[1] = S;
-                cs.lse[2] = mn;
+                rs.Lq = (double)M / (double)j.Tp + log((double)S);
+                rs.epsq = lse_rel_bound(((double)M - (double)mn) * (double)j.cp);
             }
             __syncthreads();
-            cluster_arrive();
-            cluster_wait();
-            if (t == 0) {
-                double Mx = -INFINITY, mnn = INFINITY, St = 0.0;
-                float pm[kResidChunks], ps[kResidChunks];
-                for (int r = 0; r < kResidChunks; ++r) {
-                    pm[r] = peer_ld_f32(peer_addr(&cs.lse[0], (uint32_t)r));
-                    ps[r] = peer_ld_f32(peer_addr(&cs.lse[1], (uint32_t)r));
-                    Mx = fmax(Mx, (double)pm[r]);
-                    mnn = fmin(mnn, (double)peer_ld_f32(peer_addr(&cs.lse[2], (uint32_t)r)));
-                }
-                for (int r = 0; r < kResidChunks; ++r)
-                    St += (double)ps[r] * exp2(((double)pm[r] - Mx) * (double)j.cp);
-                cs.Lq = Mx / (double)j.Tp + log(St);
-                cs.epsq = lse_rel_bound((Mx - mnn) * (double)j.cp);
-            }
-            __syncthreads();
-            re.Lq = cs.Lq;
-            re.epsq = cs.epsq;
-            if (t == 0 && ve > vb)
-                prefetch_l2(reinterpret_cast<const uint4 *>(re.qrow) + vb, (uint32_t)(ve - vb) * 16u);
-        } else {
-            __syncthreads();
-            cluster_arrive();  // cs.thr of every CTA is set before anyone publishes
-            cluster_wait();
+            re.Lq = rs.Lq;
+            re.epsq = rs.epsq;
         }
         RCtx ctx;
         resid_ctx(j, re, ctx);
         Track32 tr;
-        resid_scan_fast<In>(ctx, vb, ve, cs, gt, skip, q, tr);
-        Cand2 best;
-        block_cand2(tr.c, sm, best);
-        if (t == 0) cs.cand = best;
-        __syncthreads();
-        cluster_arrive();
-        cluster_wait();
-        if (rank == 0 && t < 32) {
-            // CTA 0's first warp merges the chunks' candidates (lane r reads
-            // CTA r's) and draws the correction.
-            Cand2 all;
-            all.init();
-            if (t < kResidChunks) {
-                const uint32_t a = peer_addr(&cs.cand, (uint32_t)t);
-                all.hi1 = peer_ld_f32(a + offsetof(Cand2, hi1));
-                all.lo1 = peer_ld_f32(a + offsetof(Cand2, lo1));
-                all.hi2 = peer_ld_f32(a + offsetof(Cand2, hi2));
-                all.lo2 = peer_ld_f32(a + offsetof(Cand2, lo2));
-                all.hi3 = peer_ld_f32(a + offsetof(Cand2, hi3));
-                all.v1 = (int)peer_ld_u32(a + offsetof(Cand2, v1));
-                all.v2 = (int)peer_ld_u32(a + offsetof(Cand2, v2));
-            }
-            warp_cand2(all);
-            if (t == 0) resid_resolve(j, re, ctx, all, skip);
-        }
-        // No CTA leaves while CTA 0 may still read its shared memory.
-        cluster_arrive();
-        cluster_wait();
+        resid_scan_row<In>(ctx, j.nvec, (uint32_t)j.V, gt, skip, rs, tr);
+        Cand2 all;
+        resid_cand2(tr.c, rs, all);
+        if (t == 0) resid_resolve(j, re, ctx, all, skip);
+        __syncthreads();  // rs is reused by the next entry
     }
     if (t == 0) {
         __threadfence();
@@ -1024,9 +998,10 @@ cudaError_t post_setup(int occ[2])
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tv_kernel<float>, kPostThreads, 0);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, resid_kernel<uint16_t>,
-                                                          kPostThreads, 0);
+                                                          kResidThreads, 0);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, resid_kernel<float>, kPostThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, resid_kernel<float>, kResidThreads,
+                                                          0);
     occ[0] = a < b ? a : b;
     occ[1] = c < d ? c : d;
     return e;
@@ -1045,7 +1020,7 @@ cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid
                : cudaLaunchKernelEx(&cfg, tv_kernel<float>, j);
         if (e != cudaSuccess) return e;
     }
-    pdl_config(cfg, at, dim3(resid_grid), dim3(kPostThreads), 0, s);
+    pdl_config(cfg, at, dim3(resid_grid), dim3(kResidThreads), 0, s);
     e = bf ? cudaLaunchKernelEx(&cfg, resid_kernel<uint16_t>, j)
            : cudaLaunchKernelEx(&cfg, resid_kernel<float>, j);
     if (e != cudaSuccess) return e;
