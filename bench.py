@@ -186,6 +186,9 @@ class Workload:
             self.lam = pick(args.lam, 1.0 if self.mode == 0 else 2.0)
             if self.mode == 2 and args.lam is None:
                 self.lam = 0.5  # mu = 1 - 1/lambda at lambda = 2
+            # the lenient sweep reports the per-row TV(p, q) as well (a second
+            # pass over every row pair); --no-tv leaves it out
+            self.tv = name == "lenient_sweep" and not args.no_tv
         elif self.kind in ("tree", "packed"):
             self.T = pick(args.T, 1.0)
         else:
@@ -197,7 +200,7 @@ class Workload:
         d = {"workload": self.name}
         if self.kind == "sample":
             d.update(B=c["B"], K=c["K"], V=c["V"], T=self.T, sigma=self.sigma,
-                     mode=["lossless", "ratio", "linear"][self.mode], lam=self.lam)
+                     mode=["lossless", "ratio", "linear"][self.mode], lam=self.lam, tv=self.tv)
         elif self.kind == "greedy":
             d.update(B=c["B"], K=c["K"], V=c["V"])
         elif self.kind == "tree":
@@ -238,7 +241,7 @@ class Workload:
         if self.kind == "sample":
             return dbv.sv_verify_sample(inp["target"], inp["draft"], inp["draft_ids"], T_p=self.T,
                                         T_q=self.T, mode=self.mode, lam=self.lam, seed=c["seed"],
-                                        handle=h)
+                                        want_tv=self.tv, handle=h)
         if self.kind == "greedy":
             acc, nxt = dbv.sv_verify_greedy(inp["target"], inp["draft_ids"], inp["draft_len"],
                                             handle=h)
@@ -263,7 +266,7 @@ class Workload:
         if self.kind == "sample":
             oracle.verify_sample(lg(inp["target"]), lg(inp["draft"]), n(inp["draft_ids"]),
                                  T_p=self.T, T_q=self.T, mode=self.mode, lam=self.lam,
-                                 seed=c["seed"], want_tv=False)
+                                 seed=c["seed"], want_tv=self.tv)
         elif self.kind == "greedy":
             oracle.verify_greedy(lg(inp["target"]), n(inp["draft_ids"]), n(inp["draft_len"]))
         elif self.kind == "tree":
@@ -307,8 +310,11 @@ class Workload:
 
     def launches(self):
         """Library kernels per call: the streaming pass, plus the residual
-        pass and the fp64 check after a sampling call."""
-        return 3 if (self.kind == "sample" or (self.kind == "packed" and self.T > 0)) else 1
+        pass and the fp64 check after a sampling call (and the TV pass when
+        TV is asked for)."""
+        if self.kind == "sample":
+            return 4 if self.tv else 3
+        return 3 if (self.kind == "packed" and self.T > 0) else 1
 
 
 def _cpu_sample(w, seconds, nmax=None):
@@ -509,6 +515,8 @@ def main():
     ap.add_argument("--sigma", type=float, default=None, help="drafter noise (sample)")
     ap.add_argument("--lam", type=float, default=None, help="lambda (ratio) or mu (linear)")
     ap.add_argument("--mode", default=None, choices=["lossless", "ratio", "linear"])
+    ap.add_argument("--no-tv", action="store_true",
+                    help="lenient sweep: leave out the per-row TV pass")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
