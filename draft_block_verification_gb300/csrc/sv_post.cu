@@ -598,7 +598,10 @@ __device__ void resid_scan_row(const RCtx &c, int nvec, uint32_t V, const float 
 #pragma unroll
         for (int u = 0; u < kScanAhead; ++u) {
             const int k = base + t + u * kResidThreads;
-            const bool pass = fmaf(VT::hi_of(VT::pmax(px[u])), c.invTp, gmax) >= tr.thrS;
+            // (k < nvec: past the row's end there is no vector, and with no
+            // threshold yet a -inf bound would still compare >= -inf)
+            const bool pass =
+                k < nvec && fmaf(VT::hi_of(VT::pmax(px[u])), c.invTp, gmax) >= tr.thrS;
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
             if (bal) {
                 if (pass) rs.qv[w][qn + __popc(bal & ((1u << lane) - 1u))] = k;
