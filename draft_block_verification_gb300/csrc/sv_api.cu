@@ -20,7 +20,6 @@ cudaError_t post_setup(int occ[2]);
 cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
                         cudaStream_t s);
 cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s);
-constexpr int kResidChunksHost = 8;
 }  // namespace sv
 
 using namespace sv;
@@ -151,10 +150,10 @@ sv_status ensure_ws(sv_handle *h, size_t bytes, cudaStream_t s)
     return SV_OK;
 }
 
-// Counter arena: seq_done [Bcap], tvdone [kMaxK * Bcap], rdone [4 * Bcap].
+// Counter arena: seq_done [Bcap], tvdone [kMaxK * Bcap].
 // The kernels return every counter they touch to zero, so the arena is zeroed
 // only when it is (re)allocated.
-constexpr int kCntPerSeq = 1 + kMaxK + 4;
+constexpr int kCntPerSeq = 1 + kMaxK;
 
 sv_status ensure_cnt(sv_handle *h, int B, cudaStream_t s)
 {
@@ -237,7 +236,6 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.rTp = j.Tp > 0.f ? 1.0 / (double)j.Tp : 0.0;
     j.rTq = j.Tq > 0.f ? 1.0 / (double)j.Tq : 0.0;
     j.tv_chunks = tv_chunks;
-    j.resid_chunks = kResidChunksHost;
     Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks);
     sv_status st = ensure_ws(h, L.total, s);
     if (st != SV_OK) return st;
@@ -245,7 +243,6 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     if (st != SV_OK) return st;
     j.seq_done = h->cnt;
     j.tvdone = h->cnt + h->cnt_B;
-    j.rdone = h->cnt + (size_t)h->cnt_B * (1 + kMaxK);
     char *w = h->ws;
     j.rp = (RowPart *)(w + L.rp);
     j.rs_stat = (RowStat *)(w + L.rs);

@@ -43,7 +43,7 @@ enum : int {
     C_EXIT = 1,       // streaming kernel: finished CTAs
     C_RESID_N = 2,    // residual entries
     C_RESCUE_N = 3,   // rescue entries
-    C_RWORK = 4,      // residual kernel: next work item
+    // 4: unused
     C_REXIT = 5,      // residual kernel: finished CTAs
     C_TWORK = 6,      // total-variation kernel: next work item
     C_TEXIT = 7,      // total-variation kernel: finished CTAs
@@ -102,8 +102,6 @@ struct Job {
     unsigned *tvdone;   // [B * K]
     int tv_chunks;
     double *rpart;      // residual / fp64 scratch
-    unsigned *rdone;    // [B * 4] per-entry counters
-    int resid_chunks;
     int *err;
     const float *gtab;     // [kGTab] G bounds of ordinary ids
     const uint64_t *skip;  // [kSkipN] skip thresholds of the top-id draws

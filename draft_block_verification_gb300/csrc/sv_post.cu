@@ -667,8 +667,10 @@ __global__ void __launch_bounds__(kResidThreads, 1) resid_kernel(const __grid_co
     for (unsigned e = blockIdx.x; e < nE; e += gridDim.x) {
         ResidEntry re = j.resid[e];
         if (t == 0) {
+            // the p row streams whole; the q row is read only where a
+            // candidate needs it (or whole, for a Packed-SS log-sum-exp)
             prefetch_l2(re.prow, (uint32_t)j.nvec * 16u);
-            prefetch_l2(re.qrow, (uint32_t)j.nvec * 16u);
+            if (re.need_lq) prefetch_l2(re.qrow, (uint32_t)j.nvec * 16u);
             rs.nids = 0;
             rs.thr = f2ord(-INFINITY);
         }

@@ -113,15 +113,13 @@ struct Track32 {
             thrS = level1_thr(t);
         }
     }
-    // keep = false: id v belongs to another item's range; it only raises the
-    // threshold (its own item keeps it as a candidate).
     __device__ __forceinline__ void add(const RCtx &ctx, float x, float y, uint32_t v, uint64_t m,
-                                        bool top, bool keep = true)
+                                        bool top)
     {
         if (surely_zero(ctx, x, y)) return;
         float lo, hi;
         if (!resid_interval32(ctx, x, y, m, top, lo, hi) || hi < thr) return;
-        if (keep) c.add(lo, hi, (int)v);
+        c.add(lo, hi, (int)v);
         if (lo > lomax) {
             lomax = lo;
             raise(__fsub_rd(lo, 1e-9f));
