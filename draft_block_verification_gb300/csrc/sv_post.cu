@@ -15,7 +15,7 @@ namespace sv {
 
 constexpr int kPostThreads = 256;
 constexpr int kPostWarps = kPostThreads / 32;
-constexpr int kResidChunks = 8;     // chunks per residual row pair
+constexpr int kResidChunks = 8;     // chunks per residual row pair on the fp64 path
 constexpr int kRescueChunks = 16;   // chunks per row on the fp64 path
 constexpr int kMaxPairs = 32;
 constexpr int kLoadsAhead = 4;      // vectors per row each thread loads before using them
@@ -991,9 +991,9 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
 }
 
 // Host-side launchers.
-// Resident CTAs per SM of the total-variation kernel (occ[0]) and of the
-// residual kernel (occ[1]); both take work items from a counter, so their
-// grids fill the GPU.
+// Resident CTAs per SM of the total-variation kernel (occ[0], which takes
+// work items from a counter, so its grid fills the GPU) and of the residual
+// kernel (occ[1]; its grid is one CTA per sequence, at most one per SM).
 cudaError_t post_setup(int occ[2])
 {
     int a = 0, b = 0, c = 0, d = 0;

@@ -127,7 +127,7 @@ struct Track32 {
     }
 };
 // Per-id screen of one vector whose bound reached the threshold: top ids are
-// skipped (the seed phase scored every top id of the chunk); an ordinary id
+// skipped (the seed phase scored every top id of the scanned range); an ordinary id
 // is bounded by the top byte of its fine bits.
 template <typename In, typename Tr>
 __device__ __forceinline__ void resid_vector(const RCtx &c, const uint4 &qx, const uint4 &qy,
