@@ -211,19 +211,58 @@ struct Cand2 {
     __device__ __forceinline__ float lomax() const { return fmaxf(lo1, lo2); }
 };
 
+// The warp's best candidate by (upper end desc, id asc) when each lane
+// offers (hi, v, lo), v = -1 for none: two 32-bit warp reductions and a
+// ballot.  hi, v and lo become the winner's in every lane; returns the
+// winning lane, or -1 when no lane offers a candidate.
+__device__ __forceinline__ int warp_best(float &hi, int &v, float &lo)
+{
+    const uint32_t h = f2ord(hi);
+    const uint32_t hm = __reduce_max_sync(0xFFFFFFFFu, h);
+    const bool top = h == hm && v >= 0;
+    const int vm = __reduce_min_sync(0xFFFFFFFFu, top ? v : 0x7FFFFFFF);
+    const unsigned wins = __ballot_sync(0xFFFFFFFFu, top && v == vm);
+    if (wins == 0u) {
+        hi = ord2f(hm);
+        v = -1;
+        lo = -INFINITY;
+        return -1;
+    }
+    const int wl = __ffs(wins) - 1;
+    hi = __shfl_sync(0xFFFFFFFFu, hi, wl);
+    v = __shfl_sync(0xFFFFFFFFu, v, wl);
+    lo = __shfl_sync(0xFFFFFFFFu, lo, wl);
+    return wl;
+}
+
+// The warp's merged candidates in every lane: its top two by (upper end
+// desc, id asc) and the largest upper end of every other candidate.  Each
+// lane holds its own top two and hi3, with distinct ids across lanes.  Every
+// lane of the warp calls it.
 __device__ __forceinline__ void warp_cand2(Cand2 &c)
 {
-    for (int o = 16; o; o >>= 1) {
-        Cand2 p;
-        p.hi1 = __shfl_xor_sync(0xFFFFFFFFu, c.hi1, o);
-        p.lo1 = __shfl_xor_sync(0xFFFFFFFFu, c.lo1, o);
-        p.hi2 = __shfl_xor_sync(0xFFFFFFFFu, c.hi2, o);
-        p.lo2 = __shfl_xor_sync(0xFFFFFFFFu, c.lo2, o);
-        p.hi3 = __shfl_xor_sync(0xFFFFFFFFu, c.hi3, o);
-        p.v1 = __shfl_xor_sync(0xFFFFFFFFu, c.v1, o);
-        p.v2 = __shfl_xor_sync(0xFFFFFFFFu, c.v2, o);
-        c.merge(p);
-    }
+    const int lane = threadIdx.x & 31;
+    float h1 = c.hi1, l1 = c.lo1;
+    int v1 = c.v1;
+    const int w1 = warp_best(h1, v1, l1);
+    // each lane's best remaining candidate
+    float h2 = lane == w1 ? c.hi2 : c.hi1, l2 = lane == w1 ? c.lo2 : c.lo1;
+    int v2 = lane == w1 ? c.v2 : c.v1;
+    const int w2 = warp_best(h2, v2, l2);
+    // the largest upper end left in each lane once the two kept are out
+    float rest = c.v1 >= 0 ? c.hi1 : -INFINITY;
+    if (lane == w1 && lane == w2)
+        rest = c.v2 >= 0 ? c.hi3 : -INFINITY;
+    else if (lane == w1 || lane == w2)
+        rest = fmaxf(c.v2 >= 0 ? c.hi2 : -INFINITY, c.hi3);
+    const uint32_t r = __reduce_max_sync(0xFFFFFFFFu, f2ord(rest));
+    c.hi1 = h1;
+    c.lo1 = l1;
+    c.v1 = v1;
+    c.hi2 = h2;
+    c.lo2 = l2;
+    c.v2 = v2;
+    c.hi3 = fmaxf(ord2f(r), -INFINITY);
 }
 
 // fp32 interval (lo, hi) of the Gumbel-perturbed logit x/T + G for id v with

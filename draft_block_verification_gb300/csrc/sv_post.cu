@@ -310,38 +310,6 @@ __device__ __forceinline__ void block_rbest(RBest &r, PostShared &sm, RBest &out
     }
 }
 
-// Merged candidates of the CTA, in thread 0's `out` (the other threads get an
-// empty set).
-__device__ __forceinline__ void block_cand2(Cand2 &c, PostShared &sm, Cand2 &out)
-{
-    warp_cand2(c);
-    __syncthreads();
-    int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        sm.f[w][0] = c.hi1;
-        sm.f[w][1] = c.lo1;
-        sm.f[w][2] = c.hi2;
-        sm.f[w][3] = c.lo2;
-        sm.d[w][0] = c.hi3;
-        sm.i[w][0] = c.v1;
-        sm.i[w][1] = c.v2;
-    }
-    __syncthreads();
-    out.init();
-    if (threadIdx.x != 0)
-        return;
-    for (int q = 0; q < kPostWarps; ++q) {
-        Cand2 t;
-        t.hi1 = sm.f[q][0];
-        t.lo1 = sm.f[q][1];
-        t.hi2 = sm.f[q][2];
-        t.lo2 = sm.f[q][3];
-        t.hi3 = (float)sm.d[q][0];
-        t.v1 = sm.i[q][0];
-        t.v2 = sm.i[q][1];
-        out.merge(t);
-    }
-}
 
 // Seed of a scan over vectors [vb, ve): the CTA scores every top id of the
 // range (a couple of skip draws per block of 256 ids) and shares the best
@@ -618,58 +586,11 @@ __device__ void resid_scan_row(const RCtx &c, int nvec, uint32_t V, const float 
     if (qn) resid_flush<In>(c, rs, qn, gt, skip, tr);
 }
 
-// The best candidate of a warp by (upper end desc, id asc), when each lane
-// offers (hi, v, lo): two 32-bit reductions and a ballot.  Returns the
-// winning lane (every lane gets the same); hi, v and lo become the winner's.
-__device__ __forceinline__ int warp_best(float &hi, int &v, float &lo)
-{
-    const uint32_t h = f2ord(hi);
-    const uint32_t hm = __reduce_max_sync(0xFFFFFFFFu, h);
-    const bool top = h == hm;
-    // id -1 (no candidate) only ties with other empty lanes
-    const int vm = __reduce_min_sync(0xFFFFFFFFu, top ? v : 0x7FFFFFFF);
-    const int wl = __ffs(__ballot_sync(0xFFFFFFFFu, top && v == vm)) - 1;
-    hi = __shfl_sync(0xFFFFFFFFu, hi, wl);
-    v = __shfl_sync(0xFFFFFFFFu, v, wl);
-    lo = __shfl_sync(0xFFFFFFFFu, lo, wl);
-    return wl;
-}
-
-// warp_cand2 with reductions instead of a shuffle tree: the warp's top two
-// candidates by (upper end desc, id asc) and the largest upper end of every
-// other candidate, in every lane.  Each lane holds its own top two (hi1 >=
-// hi2) and hi3.
-__device__ __forceinline__ void warp_cand2_redux(Cand2 &c)
-{
-    const int lane = threadIdx.x & 31;
-    float h1 = c.hi1, l1 = c.lo1;
-    int v1 = c.v1;
-    const int w1 = warp_best(h1, v1, l1);
-    // each lane's best remaining candidate
-    float h2 = lane == w1 ? c.hi2 : c.hi1, l2 = lane == w1 ? c.lo2 : c.lo1;
-    int v2 = lane == w1 ? c.v2 : c.v1;
-    const int w2 = warp_best(h2, v2, l2);
-    // the largest upper end left in each lane once the two kept are out
-    float rest = c.hi1;
-    if (lane == w1 && lane == w2)
-        rest = c.hi3;
-    else if (lane == w1 || lane == w2)
-        rest = fmaxf(c.hi2, c.hi3);
-    const uint32_t r = __reduce_max_sync(0xFFFFFFFFu, f2ord(rest));
-    c.hi1 = h1;
-    c.lo1 = l1;
-    c.v1 = v1;
-    c.hi2 = h2;
-    c.lo2 = l2;
-    c.v2 = v2;
-    c.hi3 = ord2f(r);
-}
-
 // The CTA's merged candidates, in thread 0's `out`.
 __device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared &rs, Cand2 &out)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    warp_cand2_redux(c);
+    warp_cand2(c);
     if (lane == 0) {
         rs.f[w][0] = c.hi1;
         rs.f[w][1] = c.lo1;
@@ -691,7 +612,7 @@ __device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared &rs, Cand2 &ou
             out.v1 = rs.iv[lane][0];
             out.v2 = rs.iv[lane][1];
         }
-        warp_cand2_redux(out);
+        warp_cand2(out);
     }
 }
 
