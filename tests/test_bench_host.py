@@ -83,3 +83,28 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_workload_launch_counts_and_tv_flag():
+    """Library kernels per step that `gpu_launches` reports: the lenient sweep
+    computes the per-row TV by default (one more kernel), --no-tv leaves it
+    out; the other workloads are unchanged."""
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+
+    def args(**kw):
+        d = dict(batch=None, T=None, sigma=None, lam=None, mode=None, no_tv=False)
+        d.update(kw)
+        return argparse.Namespace(**d)
+
+    w = bench.Workload("lenient_sweep", args())
+    assert w.tv and w.launches() == 4 and w.point()["tv"] is True
+    w = bench.Workload("lenient_sweep", args(no_tv=True))
+    assert not w.tv and w.launches() == 3 and w.point()["tv"] is False
+    w = bench.Workload("lossless_t1", args())
+    assert not w.tv and w.launches() == 3
+    assert bench.Workload("tree", args(T=1.0)).launches() == 1
+    assert bench.Workload("packed", args(T=1.0)).launches() == 3
+    assert bench.Workload("packed", args(T=0.0)).launches() == 1
+    assert bench.Workload("greedy_tiny", args()).launches() == 1
