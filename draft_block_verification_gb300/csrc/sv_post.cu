@@ -217,10 +217,12 @@ __global__ void __launch_bounds__(kPostThreads) tv_kernel(const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
-// Residual pass (the scores and their intervals are in sv_resid.cuh): one
-// row pair per sequence that rejected, in chunks scanned by different CTAs
-// and merged by the last one; Packed-SS calls first need the stored
-// proposal row's log-sum-exp.
+// Residual draws (the scores and their intervals are in sv_resid.cuh): one
+// row pair per sequence that rejected.  The fast path (resid_kernel, below)
+// gives each pair one CTA; the fp64 path scans a pair in chunks on different
+// CTAs (resid_scan with the fp64 tracker) and merges them after a grid
+// barrier.  Packed-SS calls first need the stored proposal row's
+// log-sum-exp.
 // ---------------------------------------------------------------------------
 struct RBest {  // fp64-interval tracker of the fp64 path
     double lo, hi, hio;
@@ -329,11 +331,12 @@ __device__ __forceinline__ void resid_seed(const RCtx &c, int vb, int ve, const 
     tr.raise(ord2f(sm.thr));
 }
 
-// Scan vectors [vb, ve) of the pair.  Seed: the CTA scores every top id of
-// the chunk first (a couple of skip draws per block of 256 ids), which sets a
-// threshold close to the chunk's best; then each vector whose largest logit
-// can reach it with the ordinary-id bound is screened per id.  (Scores drop
-// the common -Lp, and log w <= x/T - Lp, so x/T + G bounds a score.)
+// Scan vectors [vb, ve) of the pair (the fp64 path's chunks).  Seed: the CTA
+// scores every top id of the chunk first (a couple of skip draws per block of
+// 256 ids), which sets a threshold close to the chunk's best; then each
+// vector whose largest logit can reach it with the ordinary-id bound is
+// screened per id.  (Scores drop the common -Lp, and log w <= x/T - Lp, so
+// x/T + G bounds a score.)
 template <typename In, typename Tr>
 __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const uint64_t *skip,
                            PostShared &sm, Tr &tr)
