@@ -1,12 +1,13 @@
 """Benchmark of the verify step on GB300.
 
 One step = one verify call over one batch of a named workload (default: the
-lossless workload -- sv_verify_sample at T = 1 over B = 64 sequences, K = 16
-draft tokens, V = 128256, bf16 logits, 541.75 MB of logits per step, larger
-than the 126 MB L2, so every step streams from HBM).  A call runs the whole
-verify path: the streaming pass over every required row, the decisions, the
-residual draw and the fp64 check.  Inputs are seeded synthetic tensors
-resident on the GPU before the timed region.
+Packed-SS step at T = 1 -- sv_packed_step over B = 256 sequences, K = 32
+verify rows and W = 32 proposal rows per sequence, V = 151936, bf16 logits;
+the call reads the required rows, about 3.7 GB per step, far larger than the
+126 MB L2, so every step streams from HBM).  A call runs the whole verify
+path: the streaming pass over every required row, the decisions, the
+residual draw from the stored proposal rows and the fp64 check.  Inputs are
+seeded synthetic tensors resident on the GPU before the timed region.
 
 Prints ONE JSON line (rank 0): verified draft rows/s for the whole job, the
 roofline of the streaming kernel against the measured HBM copy bandwidth, the
@@ -14,7 +15,7 @@ end-to-end rate through the C ABI with host buffers, the CPU oracle baseline
 and the SM clocks sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload lossless_t1|lenient_sweep|tree|packed|greedy_tiny]
+                  [--workload packed|lossless_t1|lenient_sweep|tree|greedy_tiny]
                   [--T t] [--sigma s] [--lam l] [--mode lossless|ratio|linear]
 Multi-GPU (torchrun): every rank verifies its own full batch (weak scaling, no
 collective on the data path); value = all ranks' rows / max time over ranks.
@@ -38,9 +39,8 @@ import torch  # noqa: E402
 
 import datagen  # noqa: E402
 
-WORKLOAD = "lossless_t1"
+WORKLOAD = "packed"
 METRIC = "verified draft rows/sec and logits HBM GB/s (fraction of GB300 peak), 1 GPU"
-PROFILE = os.path.join(ROOT, "profiles", "pass_kernel_lossless_t1.md")
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["sv_pass.cu", "sv_common.cuh", "sv_dev.cuh", "sv_gumbel.cuh", "sv_job.cuh"]
 
@@ -62,11 +62,18 @@ def _kernel_hash():
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic():
+def _profile_path(w):
+    """The committed ncu summary of the streaming kernel on this workload."""
+    t = "" if w.kind == "greedy" else "_t%g" % w.T
+    return os.path.join(ROOT, "profiles", "pass_kernel_%s%s.md" % (w.name, t))
+
+
+def _profiled_traffic(w):
     """DRAM bytes per launch of the streaming kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+    summary of this workload, if it was taken on the current kernel source;
+    else None."""
     try:
-        text = open(PROFILE).read()
+        text = open(_profile_path(w)).read()
     except OSError:
         return None
     vals = {}
@@ -83,8 +90,11 @@ def _profiled_traffic():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons every 50 ms; the
-    timed region starts only after the first sample arrived."""
+    """nvidia-smi sampling of SM clocks and throttle reasons every 20 ms.  The
+    timed region starts only after the first sample arrived; that sample is
+    kept (taken just before the region), so that a region shorter than the
+    sampling interval still has a clock record; `in_region` counts the
+    samples taken while it ran."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -98,7 +108,7 @@ class Clocks:
         self.first = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.first = self.p.stdout.readline()  # sampler is running
         except OSError:
@@ -107,14 +117,17 @@ class Clocks:
 
     def __exit__(self, *a):
         self.rows = []
+        self.in_region = 0
         if self.p is None:
             return
         self.p.terminate()
         out, _ = self.p.communicate(timeout=10)
-        for line in out.splitlines():
+        lines = ([self.first] if self.first else []) + out.splitlines()
+        for i, line in enumerate(lines):
             f = [x.strip() for x in line.split(",")]
             if len(f) >= 9:
                 self.rows.append(f)
+                self.in_region += 1 if i > 0 else 0
 
     def summary(self):
         rows = getattr(self, "rows", [])
@@ -126,7 +139,7 @@ class Clocks:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "in_region": getattr(self, "in_region", 0)}
 
 
 def _dist():
@@ -158,6 +171,31 @@ def job_rate(world_size, units_per_rank, ms_max):
     """Whole-job throughput: every rank processed units_per_rank units; the
     job took the slowest rank's time (ms)."""
     return world_size * units_per_rank / (ms_max / 1000.0)
+
+
+def _percentiles(xs):
+    """Median, 10th and 90th percentiles (ms) of per-step times."""
+    a = np.asarray(xs, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
+def _cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 # ---------------------------------------------------------------------------
@@ -308,6 +346,22 @@ class Workload:
         B = inp["logits"].shape[0]
         return int((inp["prev_len"].long() + 1).sum().item() + B * c["W"]) * row
 
+    def decisions(self, out):
+        """Per-call decision summary of a call's outputs: near-threshold flags,
+        mean accepted draft tokens per sequence (tree: mean accepted path
+        depth), and for Packed-SS the mean stopping index a."""
+        t = lambda k: out[k].detach().float().cpu() if isinstance(out, dict) and k in out else None
+        d = {}
+        if self.kind == "tree":
+            d["mean_path_len"] = float(t("path_len").mean())
+        else:
+            d["mean_accept_len"] = float(t("accept_len").mean())
+        if self.kind == "packed":
+            d["mean_commit_len"] = float(t("commit_len").mean())
+        f = t("flags")
+        d["flags"] = None if f is None else int(f.sum())
+        return d
+
     def launches(self):
         """Library kernels per call: the streaming pass, plus the residual
         pass and the fp64 check after a sampling call (and the TV pass when
@@ -344,6 +398,7 @@ def cpu_baseline(w, seconds=15.0):
     dt = statistics.median(times)
     units = w.units(inp)
     return {"value": units / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "cpu_model": _cpu_model(),
             "sample": "%d of %d sequences of %s, %d oracle calls, median %.3f s wall"
                       % (nseq, w.cfg["B"], w.name, len(times), dt)}
 
@@ -366,6 +421,7 @@ def run_reference(args):
         vals.append(w.units(inp) / w.oracle_call(inp))
     value = statistics.median(vals[args.warmup:]) if args.steps else vals[-1]
     cb = {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "cpu_model": _cpu_model(),
           "sample": "%d of %d sequences of %s per step" % (nseq, w.cfg["B"], w.name)}
     cfg = w.point()
     cfg.update(sample_sequences_per_step=nseq)
@@ -414,23 +470,20 @@ def run_ours(args):
     flush = None
     if w.alg_bytes(inp) < 3 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    # one event pair per step (start, end) on the launching stream
     steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps if flush is not None else 1)]
+                for _ in range(args.steps)]
     with Clocks(local) as clk:
         _barrier(dist, dev)
-        if flush is None:
-            steps_ev[0][0].record(stream)
         for i in range(args.steps):
             if flush is not None:
                 flush.fill_(float(i))
-                steps_ev[i][0].record(stream)
-            call()
-            if flush is not None:
-                steps_ev[i][1].record(stream)
-        if flush is None:
-            steps_ev[0][1].record(stream)
+            steps_ev[i][0].record(stream)
+            out = call()
+            steps_ev[i][1].record(stream)
         _barrier(dist, dev)
     h.sync_status()
+    dec = w.decisions(out)
     # The streaming kernel's own duration: the same steps again, with the
     # library recording an event pair around that kernel on the call's stream
     # (kept out of the timed steps above, where events between the kernels
@@ -442,7 +495,8 @@ def run_ours(args):
         call()
     h.set_option(dbv.SV_OPT_TIMING_EVENTS, 0)
     h.sync_status()
-    ms = sum(a.elapsed_time(b) for a, b in steps_ev) / args.steps
+    step_ms = [a.elapsed_time(b) for a, b in steps_ev]
+    ms = sum(step_ms) / args.steps
     ms = _max_over_ranks(dist, ms, dev)
     kern_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     units = w.units(inp)
@@ -485,11 +539,13 @@ def run_ours(args):
         "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": _profiled_traffic() if args.workload == WORKLOAD else None,
+                     "traffic": _profiled_traffic(w),
                      "peak_source": peak_kind, "kernel": "pass_kernel", "kernel_ms": kern_ms,
                      "alg_bytes_per_launch": alg_bytes},
         "e2e": {"value": job_rate(ws, units, e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},
+        "step_ms": _percentiles(step_ms),
+        "decisions": dec,
         "gpu_launches": w.launches() * args.steps,
         "clocks": clk.summary(),
     }

@@ -17,7 +17,9 @@
 // Calls on one device share that scratch, so they must not overlap: issue
 // them on one stream, or order streams with events.  The first call on a
 // device looks up the scratch address (cudaGetSymbolAddress) and sets the
-// kernel attributes; make that first call before any stream capture.
+// kernel attributes; make that first call before any stream capture.  A
+// set-up that fails with a CUDA error is not remembered: the next call on
+// that device tries again.
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -53,8 +55,8 @@ constexpr size_t kScratchBytes = kTabOff + kGTab * sizeof(float);
 static __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
 
 struct DeviceSetup {
-    bool done = false;
-    sv_status status = SV_OK;
+    bool done = false;            // set up successfully, or found unsupported
+    sv_status status = SV_OK;     // SV_OK or SV_ERR_UNSUPPORTED once done
     unsigned char *scratch = nullptr;
     int sms = 0;
     int blocks_per_sm = 1;
@@ -63,34 +65,38 @@ struct DeviceSetup {
 std::mutex g_setup_mu;
 DeviceSetup g_setup[kStaticMaxDevices];
 
-// Once per device, with that device current.
+// Once per device, with that device current.  Only a completed set-up and
+// the finding that the device is not an sm_103 part are remembered: a CUDA
+// error (for example a first call made inside a stream capture) is returned
+// as SV_ERR_CUDA and the next call tries again.
 sv_status setup_device(int dev, DeviceSetup **out)
 {
     std::lock_guard<std::mutex> lk(g_setup_mu);
     DeviceSetup &d = g_setup[dev];
-    if (!d.done) {
-        d.done = true;
-        cudaDeviceProp prop;
-        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 ||
-            prop.minor != 3) {
-            d.status = SV_ERR_UNSUPPORTED;  // built for sm_103a only
-        } else {
-            d.sms = prop.multiProcessorCount;
-            void *p = nullptr;
-            cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-            int nb = 0;
-            if (e == cudaSuccess)
-                e = pass_setup(&nb);
-            if (e != cudaSuccess || p == nullptr) {
-                d.status = SV_ERR_CUDA;
-            } else {
-                d.scratch = (unsigned char *)p;
-                d.blocks_per_sm = std::max(nb, 1);
-            }
-        }
-    }
     *out = &d;
-    return d.status;
+    if (d.done)
+        return d.status;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return SV_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) {  // built for sm_103a only
+        d.status = SV_ERR_UNSUPPORTED;
+        d.done = true;
+        return d.status;
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    int nb = 0;
+    if (e == cudaSuccess)
+        e = pass_setup(&nb);
+    if (e != cudaSuccess || p == nullptr)
+        return SV_ERR_CUDA;
+    d.sms = prop.multiProcessorCount;
+    d.scratch = (unsigned char *)p;
+    d.blocks_per_sm = std::max(nb, 1);
+    d.status = SV_OK;
+    d.done = true;
+    return SV_OK;
 }
 
 bool logits_ok_static(const void *p, sv_dtype dt, int64_t rs, int V)
@@ -112,6 +118,10 @@ extern "C" sv_status sv_verify_greedy_static(const void *target, sv_dtype dtype,
                                              int32_t *status, void *stream)
 {
     if (B < 0 || K < 0 || K > kMaxK || !status) return SV_ERR_INVALID_ARG;
+    if (B == 0)  // nothing to verify; the status word still reads 0
+        return cudaMemsetAsync(status, 0, sizeof(int32_t), (cudaStream_t)stream) == cudaSuccess
+                   ? SV_OK
+                   : SV_ERR_CUDA;
     if (!logits_ok_static(target, dtype, row_stride, V) || !accept_len || !next_token ||
         (K > 0 && !draft_ids))
         return SV_ERR_INVALID_ARG;
@@ -130,7 +140,6 @@ extern "C" sv_status sv_verify_greedy_static(const void *target, sv_dtype dtype,
     cudaError_t e = cudaMemsetAsync(cnt, 0, ((size_t)C_NCTL + B) * sizeof(unsigned), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
     if (e != cudaSuccess) return SV_ERR_CUDA;
-    if (B == 0) return SV_OK;
 
     Job j;
     memset(&j, 0, sizeof j);

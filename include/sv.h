@@ -130,13 +130,15 @@ sv_status sv_verify_greedy(sv_handle *h, const void *target, sv_dtype dtype, int
  *          stream order), then the first device-side error (SV_ERR_TIMEOUT,
  *          SV_ERR_DEVICE_BOUNDS) if one occurs.  Nothing else needs to start
  *          at zero: the call clears its own counters.
+ * B = 0 only writes 0 to status (the logit and id pointers may be NULL).
  * Limits: B <= 4096 and B * (K + 1) <= 32768; larger shapes return
  * SV_ERR_UNSUPPORTED with nothing enqueued.  Other argument errors return
  * SV_ERR_INVALID_ARG as in sv_verify_greedy.
  * Calls on one device share the scratch and must not overlap: issue them on
  * one stream, or order the streams with events.  The first call on a device
  * looks up the scratch and sets kernel attributes; make it before any stream
- * capture.
+ * capture.  If that set-up fails with a CUDA error the call returns
+ * SV_ERR_CUDA and the next call on the device tries the set-up again.
  * ------------------------------------------------------------------------- */
 sv_status sv_verify_greedy_static(const void *target, sv_dtype dtype, int64_t row_stride, int B,
                                   int K, int V, const int32_t *draft_ids,

@@ -197,14 +197,26 @@ def test_tree_full_size(dbv, T):
     ti = datagen.tree_inputs(c["B"], c["N"], c["V"], dtype="bf16", seed=c["seed"], L=c["L"],
                              max_depth=c["max_depth"], max_children=c["max_children"],
                              device=DEV)
-    out = dbv.sv_verify_tree(ti.node_logits, ti.parent, ti.node_pos, ti.node_tok, T=T,
+    # the drafter's tokens: at T = 0 the workload's own (argmax w.p. 0.8); at
+    # T > 0 the oracle's coupled-noise winner of each node w.p. 0.8, so that the
+    # trees hold deep accepted paths at full vocabulary size too
+    # (the first 8 trees; crafting costs the oracle a full row per node)
+    tok = ti.node_tok
+    if T > 0:
+        S = 8
+        crafted = craft_tree_tokens(np_logits(ti.node_logits[:S]), cpu(ti.node_pos[:S]), T,
+                                    c["seed"], np.random.default_rng(5))
+        tok = tok.clone()
+        tok[:S] = torch.from_numpy(crafted).to(DEV)
+    out = dbv.sv_verify_tree(ti.node_logits, ti.parent, ti.node_pos, tok, T=T,
                              seed=c["seed"], max_depth=8)
     ref = oracle.verify_tree(np_logits(ti.node_logits), cpu(ti.parent), cpu(ti.node_pos),
-                             cpu(ti.node_tok), T=T, seed=c["seed"], max_depth=8)
+                             cpu(tok), T=T, seed=c["seed"], max_depth=8)
     keep = ref["flags"] == 0
     assert np.array_equal(cpu(out["flags"]), ref["flags"])
     for k in ("path_len", "path_nodes", "match", "commit_count"):
         assert np.array_equal(cpu(out[k])[keep], ref[k][keep]), k
+    assert ref["path_len"][:8].max() >= 2 and ref["match"][:8].mean() > 0.5
 
 
 # ------------------------------------------------------------------ Packed-SS

@@ -120,3 +120,40 @@ def test_gumbel_moments(orc):
     assert stats.kstest(g, "gumbel_r").pvalue > 1e-4
     # the upper tail comes from the top ids: P(G > 5.5414) = 1/256
     assert abs(np.mean(g > -math.log(-math.log(255 / 256))) - 1 / 256) < 4 * math.sqrt(1 / 256 / g.size)
+
+
+FROZEN = os.path.join(os.path.dirname(__file__), "golden", "rng_frozen_vectors.txt")
+
+
+def _frozen():
+    rows, key = [], None
+    for line in open(FROZEN):
+        f = line.split("#")[0].split()
+        if not f:
+            continue
+        if f[0] == "key":
+            key = tuple(int(x) for x in f[1:6]) + (int(f[6], 16),)
+        else:
+            rows.append((key, int(f[1]), int(f[2]), int(f[3], 16), float.fromhex(f[4]),
+                         float.fromhex(f[5])))
+    return rows
+
+
+def test_frozen_vectors_cover_the_layout():
+    rows = _frozen()
+    assert len(rows) >= 32
+    assert {k[1] for k, *_ in rows} == {1, 2, 3, 4}       # every stream
+    assert any(top for _, v, top, *_ in rows if v >= 151808)  # a top id in the last block
+    assert sum(top for _, _, top, *_ in rows) >= 9           # top ids of every key
+    assert any(k[4] >= 2**32 for k, *_ in rows) and any(k[3] >= 2**40 for k, *_ in rows)
+
+
+def test_oracle_matches_frozen_vectors(orc):
+    """The oracle's key, top flag, fine bits, uniform and Gumbel value, bit for
+    bit, against values frozen from an earlier build of the same layout."""
+    for (seed, st, seq, pos, it, k), v, top, m, u, g in _frozen():
+        assert orc.key(seed, st, seq, pos, it) == k
+        assert int(orc.is_top(k, v)) == top, (k, v)
+        assert orc.fine52(k, v) == m, (k, v)
+        assert orc.uniform(k, v) == u, (k, v)
+        assert orc.gumbel(k, v) == g, (k, v)

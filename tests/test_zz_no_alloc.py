@@ -71,6 +71,31 @@ def test_status_reports_device_errors_and_next_call_starts_clean(dbv):
     assert torch.equal(acc, ref_acc) and torch.equal(nxt, ref_nxt)
 
 
+@pytest.mark.parametrize("B,K,V,dtype,ragged", [(4096, 7, 64, "bf16", True),
+                                                 (4096, 7, 1032, "f32", False),
+                                                 (300, 0, 4104, "bf16", False)])
+def test_capacity_limit_and_no_draft_tokens(dbv, B, K, V, dtype, ragged):
+    """At the limit (B = 4096 and B * (K + 1) = 32768 rows: one part per row,
+    every record and counter of the scratch in use) and with no draft tokens,
+    the results equal the handle path's on two calls in a row."""
+    target, ids, dl = _case(B, K, V, dtype, B + K, ragged)
+    ref_acc, ref_nxt = dbv.sv_verify_greedy(target, ids, dl)
+    for _ in range(2):
+        acc, nxt, st = dbv.sv_verify_greedy_static(target, ids, dl)
+        torch.cuda.synchronize()
+        assert int(st[0]) == 0
+        assert torch.equal(acc, ref_acc) and torch.equal(nxt, ref_nxt)
+
+
+def test_empty_batch(dbv):
+    dev = torch.device("cuda", 0)
+    target = torch.zeros((0, 4, 64), dtype=torch.bfloat16, device=dev)
+    ids = torch.zeros((0, 3), dtype=torch.int32, device=dev)
+    acc, nxt, st = dbv.sv_verify_greedy_static(target, ids)
+    torch.cuda.synchronize()
+    assert acc.numel() == 0 and nxt.numel() == 0 and int(st[0]) == 0
+
+
 @pytest.mark.parametrize("B,K", [(4097, 0), (1025, 31)])
 def test_rejects_shapes_beyond_the_scratch(dbv, B, K):
     dev = torch.device("cuda", 0)
