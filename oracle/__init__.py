@@ -25,7 +25,7 @@ _LIBDIR = os.path.join(_HERE, "_lib")
 _LIBPATH = os.path.join(_LIBDIR, "liboracle.so")
 _lib = None
 
-LOSSLESS, RATIO, LINEAR = 0, 1, 2
+LOSSLESS, RATIO, LINEAR, CACTUS = 0, 1, 2, 3
 ST_ACCEPT, ST_SAMPLE, ST_DRAFT, ST_TREE = 1, 2, 3, 4
 FLAG_EPS = 1e-9
 
@@ -68,7 +68,10 @@ def _L():
         lib.or_accept_prob.restype = dbl
         lib.or_accept_prob.argtypes = [dbl, dbl, i32, dbl]
         lib.or_residual_weights.restype = None
-        lib.or_residual_weights.argtypes = [vp, vp, i32, dbl, dbl, dbl, dbl, i32, dbl, vp]
+        lib.or_residual_weights.argtypes = [vp, vp, i32, dbl, dbl, dbl, dbl, i32, dbl, dbl, vp]
+        lib.or_cactus_gamma.restype, lib.or_cactus_gamma.argtypes = dbl, [dbl, dbl]
+        lib.or_residual_scale.restype = dbl
+        lib.or_residual_scale.argtypes = [dbl, i32, dbl]
         lib.or_tv.restype, lib.or_tv.argtypes = dbl, [vp, vp, i32, dbl, dbl, dbl, dbl]
         lib.or_verify_greedy.restype = i32
         lib.or_verify_greedy.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]
@@ -187,13 +190,26 @@ def accept_prob(log_p: float, log_q: float, mode: int = LOSSLESS, lam: float = 1
     return float(_L().or_accept_prob(log_p, log_q, mode, lam))
 
 
-def residual_weights(x, y, Tp: float, Tq: float, mode: int = LOSSLESS, lam: float = 1.0):
-    """Unnormalised residual weights for target logits x and drafter logits y."""
+def cactus_gamma(p: float, delta: float) -> float:
+    """gamma*: the modified Cactus target probability of the drafted token."""
+    return float(_L().or_cactus_gamma(float(p), float(delta)))
+
+
+def residual_scale(log_pd: float, mode: int = LOSSLESS, lam: float = 1.0) -> float:
+    """c = (1 - gamma*) / (1 - p(d)) for CACTUS (1 for the other modes)."""
+    return float(_L().or_residual_scale(float(log_pd), int(mode), float(lam)))
+
+
+def residual_weights(x, y, Tp: float, Tq: float, mode: int = LOSSLESS, lam: float = 1.0,
+                     d: int = None):
+    """Unnormalised residual weights for target logits x and drafter logits y
+    (d: the rejected draft token, which the CACTUS weights depend on)."""
     x = np.ascontiguousarray(x, dtype=np.float64)
     y = np.ascontiguousarray(y, dtype=np.float64)
     w = np.empty_like(x)
     Lp, Lq = lse(x, Tp), lse(y, Tq)
-    _L().or_residual_weights(_p(x), _p(y), x.size, Tp, Tq, Lp, Lq, mode, lam, _p(w))
+    c = 1.0 if d is None else residual_scale(x[d] / Tp - Lp, mode, lam)
+    _L().or_residual_weights(_p(x), _p(y), x.size, Tp, Tq, Lp, Lq, mode, lam, c, _p(w))
     return w
 
 

@@ -29,7 +29,7 @@
 #include <string.h>
 
 enum { OR_F32 = 0, OR_BF16 = 1 };
-enum { OR_LOSSLESS = 0, OR_RATIO = 1, OR_LINEAR = 2 };
+enum { OR_LOSSLESS = 0, OR_RATIO = 1, OR_LINEAR = 2, OR_CACTUS = 3 };
 /* Random-number streams (READING: the pages only ask for independent uniforms
  * and Gumbels; [PackedSS] App. B.2 "Conditioning information" requires draft
  * sampling, acceptance tests and corrections to use independent numbers). */
@@ -277,16 +277,77 @@ int or_gumbel_argmax(const double *score, int V, uint64_t key, double *gap)
     return best;
 }
 
+/* Modified Cactus ([TwoTrade] App. E).  Given the target probability p of
+ * the drafted token y and the KL budget delta, the modified target puts
+ * gamma* on y, the largest gamma with
+ *   Phi(gamma) = gamma log(gamma/p) + (1-gamma) log((1-gamma)/(1-p)) <= delta
+ * (eq. 17), and rescales every other token by (1-gamma*)/(1-p).  Phi is 0 at
+ * gamma = p, grows on [p, 1] and reaches log(1/p) at 1, so gamma* is 1 when
+ * delta >= log(1/p) and otherwise the root of Phi(gamma) = delta above p.
+ * The page solves it with Newton's method; so does this function, started
+ * from the page's second-order (Taylor) solution p + sqrt(2 delta p (1-p))
+ * (eq. 18) and kept inside a shrinking bracket [lo, hi] around the root (a
+ * step that would leave it is replaced by the bracket's midpoint).
+ * READING: p = 0 (a token the target cannot produce) keeps gamma* = 0. */
+double or_cactus_gamma(double p, double delta)
+{
+    if (!(p > 0.0))
+        return 0.0;
+    if (p >= 1.0)
+        return 1.0;
+    if (!(delta > 0.0))
+        return p;
+    if (delta >= -log(p))
+        return 1.0;
+    double lo = p, hi = 1.0;
+    double g = p + sqrt(2.0 * delta * p * (1.0 - p));
+    if (!(g > lo && g < hi))
+        g = 0.5 * (lo + hi);
+    /* log(gamma/p) and log((1-gamma)/(1-p)) as log1p of (gamma-p)/p and of
+     * (p-gamma)/(1-p): both quotients are near 1 when gamma is near p (small
+     * delta), where their plain logs would lose most of the digits */
+    for (int it = 0; it < 200; ++it) {
+        double l0 = log1p((g - p) / p);
+        double l1 = log1p((p - g) / (1.0 - p));
+        double phi = g * l0 + (1.0 - g) * l1;
+        double f = phi - delta;
+        if (f == 0.0)
+            break;
+        if (f > 0.0)
+            hi = g;
+        else
+            lo = g;
+        double d1 = l0 - l1; /* Phi'(gamma) */
+        double gn = g - f / d1;
+        if (!(gn > lo && gn < hi))
+            gn = 0.5 * (lo + hi);
+        if (gn == g || hi - lo <= 2e-16 * hi)
+            break;
+        g = gn;
+    }
+    return g;
+}
+
 /* Acceptance probability of a draft token from log p(d) and log q(d).
  *   LOSSLESS: min{1, p/q}                      [PackedSS] §2.2; [TwoTrade] §2
  *   RATIO:    min{1, lam p/q}, lam >= 1         READING of the "predefined
  *             ratio" lenience named in [TwoTrade] §1
  *   LINEAR:   min{1, ptilde/q}, ptilde = (1-mu)p + mu q, mu = lam in [0,1]
- *                                              [TwoTrade] eq. (5), Alg. 1 */
+ *                                              [TwoTrade] eq. (5), Alg. 1
+ *   CACTUS:   min{1, gamma* / q}, delta = lam >= 0 [TwoTrade] App. E
+ *             (gamma* = p when delta = 0, which is then the lossless rule
+ *             to the last bit) */
 double or_accept_prob(double log_p, double log_q, int mode, double lam)
 {
-    double r = exp(log_p - log_q);
     double a;
+    if (mode == OR_CACTUS) {
+        double p = exp(log_p);
+        double g = or_cactus_gamma(p, lam);
+        double lg = (g == p) ? log_p : log(g);
+        a = exp(lg - log_q);
+        return a < 1.0 ? a : 1.0;
+    }
+    double r = exp(log_p - log_q);
     if (mode == OR_RATIO)
         a = lam * r;
     else if (mode == OR_LINEAR)
@@ -296,19 +357,42 @@ double or_accept_prob(double log_p, double log_q, int mode, double lam)
     return a < 1.0 ? a : 1.0;
 }
 
+/* The factor c = (1 - gamma*)/(1 - p(d)) by which the modified Cactus
+ * target rescales every token other than the drafted one d ([TwoTrade]
+ * App. E); 1 for the other modes.  READING: p(d) = 1 (gamma* = 1, so d is
+ * always accepted and no residual is drawn) gives 0. */
+double or_residual_scale(double log_pd, int mode, double lam)
+{
+    if (mode != OR_CACTUS)
+        return 1.0;
+    double p = exp(log_pd);
+    if (p >= 1.0)
+        return 0.0;
+    double g = or_cactus_gamma(p, lam);
+    return (g == p) ? 1.0 : (1.0 - g) / (1.0 - p);
+}
+
 /* Residual weights (unnormalised) used after the first rejection.
  *   LOSSLESS: [p - q]_+                         [PackedSS] §2.2, Alg. 2
  *   LINEAR:   [ptilde - q]_+                    [TwoTrade] Alg. 1
  *   RATIO:    [p - q]_+  (READING: the lenience changes only the test;
  *             parity unpinned for lam > 1)
- * p and q are the normalised rows exp(x/Tp - Lp) and exp(y/Tq - Lq). */
+ *   CACTUS:   [ptilde - q]_+ with ptilde = c p off the drafted token d and
+ *             gamma* on it ([TwoTrade] App. E); c = or_residual_scale().
+ *             A rejection implies gamma* < q(d), and c p(d) <= p(d) <= gamma*,
+ *             so both ptilde(d) - q(d) and c p(d) - q(d) are negative: the
+ *             weight of every id, d included, is [c p - q]_+.
+ * p and q are the normalised rows exp(x/Tp - Lp) and exp(y/Tq - Lq); c is
+ * the residual scale (1 for the other modes). */
 void or_residual_weights(const double *x, const double *y, int V, double Tp, double Tq,
-                         double Lp, double Lq, int mode, double lam, double *w)
+                         double Lp, double Lq, int mode, double lam, double c, double *w)
 {
     for (int v = 0; v < V; ++v) {
         double p = exp(x[v] / Tp - Lp);
         double q = exp(y[v] / Tq - Lq);
-        double pt = (mode == OR_LINEAR) ? (1.0 - lam) * p + lam * q : p;
+        double pt = (mode == OR_LINEAR) ? (1.0 - lam) * p + lam * q
+                  : (mode == OR_CACTUS) ? c * p
+                                        : p;
         double d = pt - q;
         w[v] = d > 0.0 ? d : 0.0;
     }
@@ -448,7 +532,9 @@ int or_verify_sample(const void *target, const void *draft, int dtype, int64_t r
         if (h < n) {
             load_row(draft, dtype, (int64_t)b * K + h, row_stride, V, y);
             double Lq = or_lse(y, V, Tq);
-            or_residual_weights(x, y, V, Tp, Tq, Lp, Lq, mode, lam, w);
+            int dh = draft_ids[(int64_t)b * K + h];
+            double scale = or_residual_scale(x[dh] / Tp - Lp, mode, lam);
+            or_residual_weights(x, y, V, Tp, Tq, Lp, Lq, mode, lam, scale, w);
             for (int v = 0; v < V; ++v)
                 w[v] = w[v] > 0.0 ? log(w[v]) : -INFINITY;
             c = or_gumbel_argmax(w, V, key, &gap);
@@ -629,7 +715,7 @@ int or_packed_step(const void *logits, int dtype, int64_t row_stride, int B, int
                 /* correction from [p - Q]_+ with the stored proposal row */
                 load_row(prev_draft_logits, dtype, (int64_t)b * W + off + h, row_stride, V, y);
                 double Lq = or_lse(y, V, T);
-                or_residual_weights(x, y, V, T, T, Lp, Lq, OR_LOSSLESS, 0.0, w);
+                or_residual_weights(x, y, V, T, T, Lp, Lq, OR_LOSSLESS, 0.0, 1.0, w);
                 for (int v = 0; v < V; ++v)
                     w[v] = w[v] > 0.0 ? log(w[v]) : -INFINITY;
             } else {
