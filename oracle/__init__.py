@@ -85,6 +85,9 @@ def _L():
         lib.or_packed_step.argtypes = [vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                        dbl, u64, u64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                        vp]
+        lib.or_verify_spot.restype = i32
+        lib.or_verify_spot.argtypes = [vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, dbl,
+                                       u64, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
         lib.or_num_threads.restype, lib.or_num_threads.argtypes = i32, []
         _lib = lib
     return _lib
@@ -323,4 +326,36 @@ def packed_step(logits, K, W, prev_draft, prev_len, prev_q_at_draft=None,
         _p(out["confidence"]), _p(out["flags"]))
     if rc:
         raise ValueError("oracle: invalid packed-step inputs")
+    return out
+
+
+def verify_spot(state_logits, parent, node_pos, node_tok, root_mask, T=0.0, seed=0,
+                pos_base=None, max_depth=None):
+    """SPOT state-equality verification with the target's position selection.
+    state_logits [B, 1+N, L, V]; parent/node_pos/node_tok [B, N]; root_mask [B]
+    (bit s set: block position s is masked in the root state)."""
+    state_logits = np.ascontiguousarray(state_logits)
+    B, S, L, V = state_logits.shape
+    N = S - 1
+    par, pos, tok = (_i32(a, (B, N)) for a in (parent, node_pos, node_tok))
+    rm = np.ascontiguousarray(np.asarray(root_mask, dtype=np.uint64).reshape(B))
+    if max_depth is None:
+        max_depth = max(N, 1)
+    pb = _i64(pos_base)
+    out = {
+        "path_len": np.empty(B, np.int32), "path_nodes": np.empty((B, max_depth), np.int32),
+        "commit_count": np.empty(B, np.int32), "commit_pos": np.empty(B, np.int32),
+        "commit_tok": np.empty(B, np.int32), "match": np.empty((B, max(N, 1)), np.uint8),
+        "state_pos": np.empty((B, S), np.int32), "state_tok": np.empty((B, S), np.int32),
+        "flags": np.empty(B, np.int32),
+    }
+    rc = _L().or_verify_spot(
+        _p(state_logits), _dtype_code(state_logits), V, B, N, L, V, _p(par), _p(pos), _p(tok),
+        _p(rm), f32(T), int(seed) & (2**64 - 1), _p(pb), _p(out["path_len"]),
+        _p(out["path_nodes"]), int(max_depth), _p(out["commit_count"]), _p(out["commit_pos"]),
+        _p(out["commit_tok"]), _p(out["match"]), _p(out["state_pos"]), _p(out["state_tok"]),
+        _p(out["flags"]))
+    if rc:
+        raise ValueError("oracle: invalid SPOT tree inputs")
+    out["match"] = out["match"][:, :N]
     return out

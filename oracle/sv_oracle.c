@@ -412,6 +412,147 @@ double or_tv(const double *x, const double *y, int V, double Tp, double Tq, doub
 }
 
 /* ------------------------------------------------------------------------ */
+/* State-equality verification of a SPOT draft tree with the target's own    */
+/* position selection, [SPOT] App. A.1 ("Position selection", "Greedy        */
+/* transition", "Shared Gumbel representation", "State-equality verifier"),  */
+/* §4.3 eq. (4).                                                             */
+/*   A block state holds L positions, each a token or masked.  The root      */
+/*   state's masked positions are the bits of root_mask[b]; tree node n     */
+/*   commits token node_tok[n] at the masked position node_pos[n] of its     */
+/*   parent's state (parent[b,n] in [-1, n-1], -1 = the root), so its own    */
+/*   state has that position filled.  State 0 is the root, state 1 + n the   */
+/*   state of node n.                                                        */
+/*   state_logits [B, 1+N, L, V]: row (b, state, s) is the target's          */
+/*   conditional at that state for position s (read for masked s only).      */
+/*   The target's transition Phi(state), for a state with a masked position: */
+/*     s* = argmax over masked s of max_v p_s(v), p_s = softmax(row) at      */
+/*          temperature 1 (the model's own conditional); lowest s on exact   */
+/*          ties (READING of "a fixed deterministic tie-breaking rule");     */
+/*     v* = argmax_v row_{s*}(v) at T = 0; at T > 0 the Gumbel-max of        */
+/*          row_{s*}/T with the row G(seed, TREE, b, pos_base + s*, 0, .),   */
+/*          shared by every state at that absolute position.                 */
+/*   A child is accepted when its commitment equals Phi of its parent's      */
+/*   state; the verifier walks from the root through accepted children (the */
+/*   lowest index among equal children, READING) and commits Phi of the      */
+/*   last state reached, unless that state has no masked position left.      */
+/* Outputs: path_len, path_nodes [B, max_depth] (-1 padded), commit_count   */
+/* (path_len + 1, or path_len at a full block), commit_pos / commit_tok      */
+/* (Phi of the last state, -1 at a full block), match [B, N] (the node's     */
+/* commitment equals Phi of its parent's state), state_pos / state_tok       */
+/* [B, 1+N] (Phi of every state, -1 for a full one; may be NULL), flags [B]: */
+/* decisions within 1e-9 over all states (0 < best - runner-up confidence    */
+/* < 1e-9 for s*, a Gumbel-max top-two gap below 1e-9 for v*).               */
+/* ------------------------------------------------------------------------ */
+int or_verify_spot(const void *state_logits, int dtype, int64_t row_stride, int B, int N, int L,
+                   int V, const int32_t *parent, const int32_t *node_pos,
+                   const int32_t *node_tok, const uint64_t *root_mask, double T, uint64_t seed,
+                   const int64_t *pos_base, int32_t *path_len, int32_t *path_nodes, int max_depth,
+                   int32_t *commit_count, int32_t *commit_pos, int32_t *commit_tok,
+                   uint8_t *match, int32_t *state_pos, int32_t *state_tok, int32_t *flags)
+{
+    if (L < 1 || L > 64 || N < 0)
+        return -1;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        const int S = N + 1;
+        const uint64_t all = (L == 64) ? ~0ULL : ((1ULL << L) - 1);
+        uint64_t *mask = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)S);
+        int *ps = (int *)malloc(sizeof(int) * (size_t)S);  /* s* of each state */
+        int *pv = (int *)malloc(sizeof(int) * (size_t)S);  /* v* of each state */
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        const int64_t pos0 = pos_base ? pos_base[b] : 0;
+        int nflag = 0;
+        /* masked positions of every state */
+        mask[0] = root_mask[b] & all;
+        for (int n = 0; n < N; ++n) {
+            const int par = parent[(int64_t)b * N + n], s = node_pos[(int64_t)b * N + n];
+            if (par < -1 || par >= n || s < 0 || s >= L || !((mask[par + 1] >> s) & 1ULL)) {
+                err |= 1;
+                mask[n + 1] = 0;
+                continue;
+            }
+            mask[n + 1] = mask[par + 1] & ~(1ULL << s);
+        }
+        /* Phi of every state */
+        for (int st = 0; st < S; ++st) {
+            ps[st] = pv[st] = -1;
+            if (mask[st] == 0)
+                continue;
+            double c1 = -INFINITY, c2 = -INFINITY;
+            for (int s = 0; s < L; ++s) {
+                if (!((mask[st] >> s) & 1ULL))
+                    continue;
+                load_row(state_logits, dtype, ((int64_t)b * S + st) * L + s, row_stride, V, x);
+                const double conf = exp(x[or_argmax(x, V)] - or_lse(x, V, 1.0));
+                if (conf > c1) {
+                    c2 = c1;
+                    c1 = conf;
+                    ps[st] = s;
+                } else if (conf > c2) {
+                    c2 = conf;
+                }
+            }
+            if (c1 - c2 > 0.0 && c1 - c2 < OR_FLAG_EPS)
+                ++nflag;
+            load_row(state_logits, dtype, ((int64_t)b * S + st) * L + ps[st], row_stride, V, x);
+            if (T == 0.0) {
+                pv[st] = or_argmax(x, V);
+            } else {
+                double gap;
+                for (int v = 0; v < V; ++v)
+                    x[v] = x[v] / T;
+                pv[st] = or_gumbel_argmax(
+                    x, V, or_key(seed, ST_TREE, (uint64_t)b, pos0 + ps[st], 0), &gap);
+                if (gap < OR_FLAG_EPS)
+                    ++nflag;
+            }
+        }
+        /* match bits; the walk from the root */
+        for (int n = 0; n < N; ++n) {
+            const int par = parent[(int64_t)b * N + n];
+            const int m = par >= -1 && par < n && ps[par + 1] >= 0 &&
+                          node_pos[(int64_t)b * N + n] == ps[par + 1] &&
+                          node_tok[(int64_t)b * N + n] == pv[par + 1];
+            if (match)
+                match[(int64_t)b * N + n] = (uint8_t)m;
+        }
+        for (int k = 0; k < max_depth; ++k)
+            path_nodes[(int64_t)b * max_depth + k] = -1;
+        int y = -1, len = 0; /* y: the node whose state was reached (-1: root) */
+        for (;;) {
+            int next = -1;
+            for (int n = y + 1; n < N && next < 0; ++n)
+                if (parent[(int64_t)b * N + n] == y && ps[y + 1] >= 0 &&
+                    node_pos[(int64_t)b * N + n] == ps[y + 1] &&
+                    node_tok[(int64_t)b * N + n] == pv[y + 1])
+                    next = n;
+            if (next < 0)
+                break;
+            if (len < max_depth)
+                path_nodes[(int64_t)b * max_depth + len] = next;
+            ++len;
+            y = next;
+        }
+        path_len[b] = len;
+        commit_pos[b] = ps[y + 1];
+        commit_tok[b] = pv[y + 1];
+        commit_count[b] = len + (ps[y + 1] >= 0 ? 1 : 0);
+        for (int st = 0; st < S; ++st) {
+            if (state_pos) state_pos[(int64_t)b * S + st] = ps[st];
+            if (state_tok) state_tok[(int64_t)b * S + st] = pv[st];
+        }
+        if (flags)
+            flags[b] = nflag;
+        free(x);
+        free(pv);
+        free(ps);
+        free(mask);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Greedy verification, [PackedSS] §3.1 eqs. (1)-(2), Alg. 1 lines 3, 5-6.   */
 /* target: [B, K+1, V] rows; draft_ids: [B, K]; draft_len: [B] or NULL (=K). */
 /* ------------------------------------------------------------------------ */
