@@ -88,6 +88,9 @@ def _L():
         lib.or_verify_spot.restype = i32
         lib.or_verify_spot.argtypes = [vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, dbl,
                                        u64, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+        lib.or_packed_anyorder_step.restype = i32
+        lib.or_packed_anyorder_step.argtypes = [vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp,
+                                                vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.or_num_threads.restype, lib.or_num_threads.argtypes = i32, []
         _lib = lib
     return _lib
@@ -358,4 +361,27 @@ def verify_spot(state_logits, parent, node_pos, node_tok, root_mask, T=0.0, seed
     if rc:
         raise ValueError("oracle: invalid SPOT tree inputs")
     out["match"] = out["match"][:, :N]
+    return out
+
+
+def packed_anyorder_step(logits, Kv, W, u, win_pos, order, draft, end_pos, eos_id=-1):
+    """One any-order Packed-SS iteration (greedy); logits [B, Kv + W, V];
+    u [B]; win_pos, order, draft [B, W]; end_pos [B].  See sv_oracle.c."""
+    logits = np.ascontiguousarray(logits)
+    B, R, V = logits.shape
+    if R != Kv + W:
+        raise ValueError("logits must be [B, Kv + W, V]")
+    u, end = _i32(u, (B,)), _i32(end_pos, (B,))
+    wp, od, dr = (_i32(a, (B, W)) for a in (win_pos, order, draft))
+    out = {"accept_len": np.empty(B, np.int32), "commit_len": np.empty(B, np.int32),
+           "commit_pos": np.empty((B, W), np.int32), "commit_tok": np.empty((B, W), np.int32),
+           "end_pos": np.empty(B, np.int32), "next_draft": np.empty((B, W), np.int32),
+           "score": np.empty((B, W)), "next_order": np.empty((B, W), np.int32)}
+    rc = _L().or_packed_anyorder_step(
+        _p(logits), _dtype_code(logits), V, B, Kv, W, V, _p(u), _p(wp), _p(od), _p(dr), _p(end),
+        int(eos_id), _p(out["accept_len"]), _p(out["commit_len"]), _p(out["commit_pos"]),
+        _p(out["commit_tok"]), _p(out["end_pos"]), _p(out["next_draft"]), _p(out["score"]),
+        _p(out["next_order"]))
+    if rc:
+        raise ValueError("oracle: invalid any-order step inputs")
     return out

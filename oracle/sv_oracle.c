@@ -553,6 +553,138 @@ int or_verify_spot(const void *state_logits, int dtype, int64_t row_stride, int 
 }
 
 /* ------------------------------------------------------------------------ */
+/* One iteration of Packed-SS with any-order greedy decoding, [PackedSS]     */
+/* App. C "Procedure", Alg. 3 lines 6-15, eq. (8); confidence scores of       */
+/* App. E.6 "Confidence scores".                                             */
+/*   The active window U_t holds u <= W unresolved output positions,         */
+/*   win_pos[b, 0..u-1] (ascending).  order[b, r] is the index into the      */
+/*   window of the position checked at rank r (pi_t, a permutation of        */
+/*   0..u-1).  draft[b, i] is the draft token at win_pos[i], or -1 if the    */
+/*   position has none.                                                      */
+/*   kappa = the number of leading ranks whose position has a draft token.   */
+/*   logits [B, Kv + W, V]: verify row r (r < min(kappa+1, u) <= Kv) is the  */
+/*   verifier's prediction at rank r, given the drafts of ranks < r;         */
+/*   proposal row Kv + i (i < u) is the drafter's row at win_pos[i].         */
+/*     v_r = argmax verify row r (eq. 8); h = the leading ranks r < kappa    */
+/*     with draft = v_r; A = min(h + 1, u); C = (win_pos[order[r]], v_r),    */
+/*     r < A; an accepted EOS at position j lowers the end E to min(E, j),   */
+/*     and pairs beyond E are dropped (lines 11-12).                         */
+/*     z_i = argmax proposal row i; score_i = its softmax probability at     */
+/*     temperature 1 (the probability of the draft token when proposed).     */
+/*     Retained positions J: window positions <= E that were not accepted;   */
+/*     next_draft[i] = z_i on J, else -1 (line 15).                          */
+/*     next_order: the window indices of J by decreasing score, ties by      */
+/*     position (App. E.6), -1 padded.                                       */
+/* Outputs: accept_len (h), commit_len (pairs kept), commit_pos / commit_tok */
+/* [B, W] (rank order, -1 padded), end_out (E), next_draft [B, W], score     */
+/* [B, W] (every proposal row i < u; NaN beyond), next_order [B, W].         */
+/* ------------------------------------------------------------------------ */
+int or_packed_anyorder_step(const void *logits, int dtype, int64_t row_stride, int B, int Kv,
+                            int W, int V, const int32_t *u_in, const int32_t *win_pos,
+                            const int32_t *order, const int32_t *draft, const int32_t *end_in,
+                            int32_t eos_id, int32_t *accept_len, int32_t *commit_len,
+                            int32_t *commit_pos, int32_t *commit_tok, int32_t *end_out,
+                            int32_t *next_draft, double *score, int32_t *next_order)
+{
+    if (W < 1 || W > 64 || Kv < 0)
+        return -1;
+    int err = 0;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        const int R = Kv + W;
+        const int u = u_in[b];
+        const int32_t *wp = win_pos + (int64_t)b * W, *od = order + (int64_t)b * W;
+        const int32_t *dr = draft + (int64_t)b * W;
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        int seen[64] = {0};
+        int bad = u < 0 || u > W;
+        for (int r = 0; r < u && !bad; ++r) {
+            bad |= od[r] < 0 || od[r] >= u || seen[od[r]];
+            if (!bad)
+                seen[od[r]] = 1;
+        }
+        int kappa = 0;
+        while (!bad && kappa < u && dr[od[kappa]] >= 0)
+            ++kappa;
+        const int nreq = (kappa + 1 < u) ? kappa + 1 : u;
+        if (bad || nreq > Kv) {
+            err |= 1;
+            free(x);
+            continue;
+        }
+        /* verifier predictions, rank order (line 7) */
+        int v[64];
+        for (int r = 0; r < nreq; ++r) {
+            load_row(logits, dtype, (int64_t)b * R + r, row_stride, V, x);
+            v[r] = or_argmax(x, V);
+        }
+        /* matches, accepted count (lines 9-10) */
+        int h = 0;
+        while (h < kappa && dr[od[h]] == v[h])
+            ++h;
+        const int A = (h + 1 < u) ? h + 1 : u;
+        /* the end position E after accepted EOS tokens (line 11) */
+        int E = end_in[b];
+        for (int r = 0; r < A; ++r)
+            if (eos_id >= 0 && v[r] == eos_id && wp[od[r]] < E)
+                E = wp[od[r]];
+        /* accepted pairs within E, in rank order (lines 12-13) */
+        int kept = 0, acc[64] = {0};
+        for (int r = 0; r < W; ++r) {
+            commit_pos[(int64_t)b * W + r] = -1;
+            commit_tok[(int64_t)b * W + r] = -1;
+        }
+        for (int r = 0; r < A; ++r) {
+            if (wp[od[r]] > E)
+                continue;
+            acc[od[r]] = 1;
+            commit_pos[(int64_t)b * W + kept] = wp[od[r]];
+            commit_tok[(int64_t)b * W + kept] = v[r];
+            ++kept;
+        }
+        /* proposals and their scores (line 8; App. E.6) */
+        double sc[64];
+        int z[64];
+        for (int i = 0; i < W; ++i) {
+            sc[i] = NAN;
+            z[i] = -1;
+            if (i >= u)
+                continue;
+            load_row(logits, dtype, (int64_t)b * R + Kv + i, row_stride, V, x);
+            z[i] = or_argmax(x, V);
+            sc[i] = exp(x[z[i]] - or_lse(x, V, 1.0));
+        }
+        /* retained draft positions and the next draft (lines 14-15) */
+        int nj = 0, jl[64];
+        for (int i = 0; i < W; ++i) {
+            const int keep = i < u && !acc[i] && wp[i] <= E;
+            next_draft[(int64_t)b * W + i] = keep ? z[i] : -1;
+            score[(int64_t)b * W + i] = sc[i];
+            if (keep)
+                jl[nj++] = i;
+        }
+        /* confidence order of the retained positions: decreasing score, ties
+         * by position (insertion sort, stable on the ascending positions) */
+        for (int a = 1; a < nj; ++a) {
+            const int t = jl[a];
+            int c = a - 1;
+            while (c >= 0 && sc[jl[c]] < sc[t]) {
+                jl[c + 1] = jl[c];
+                --c;
+            }
+            jl[c + 1] = t;
+        }
+        for (int i = 0; i < W; ++i)
+            next_order[(int64_t)b * W + i] = i < nj ? jl[i] : -1;
+        accept_len[b] = h;
+        commit_len[b] = kept;
+        end_out[b] = E;
+        free(x);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Greedy verification, [PackedSS] §3.1 eqs. (1)-(2), Alg. 1 lines 3, 5-6.   */
 /* target: [B, K+1, V] rows; draft_ids: [B, K]; draft_len: [B] or NULL (=K). */
 /* ------------------------------------------------------------------------ */
