@@ -219,7 +219,7 @@ class Workload:
             # one point of the sweep (the lossless workload has a single point)
             self.T = pick(args.T, c["T"] if not isinstance(c["T"], tuple) else 1.0)
             self.sigma = pick(args.sigma, c["sigma"] if not isinstance(c["sigma"], tuple) else 1.0)
-            self.mode = {"lossless": 0, "ratio": 1, "linear": 2}[
+            self.mode = {"lossless": 0, "ratio": 1, "linear": 2, "cactus": 3}[
                 args.mode or ("lossless" if name == "lossless_t1" else "ratio")]
             self.lam = pick(args.lam, 1.0 if self.mode == 0 else 2.0)
             if self.mode == 2 and args.lam is None:
@@ -227,8 +227,10 @@ class Workload:
             # the lenient sweep reports the per-row TV(p, q) as well (a second
             # pass over every row pair); --no-tv leaves it out
             self.tv = name == "lenient_sweep" and not args.no_tv
-        elif self.kind in ("tree", "packed"):
+        elif self.kind in ("tree", "packed", "spot"):
             self.T = pick(args.T, 1.0)
+        elif self.kind == "anyorder":
+            self.T = 0.0  # Alg. 3 is greedy
         else:
             self.T = 0.0
         self.esz = 2 if c["dtype"] == "bf16" else 4
@@ -238,12 +240,18 @@ class Workload:
         d = {"workload": self.name}
         if self.kind == "sample":
             d.update(B=c["B"], K=c["K"], V=c["V"], T=self.T, sigma=self.sigma,
-                     mode=["lossless", "ratio", "linear"][self.mode], lam=self.lam, tv=self.tv)
+                     mode=["lossless", "ratio", "linear", "cactus"][self.mode], lam=self.lam,
+                     tv=self.tv)
         elif self.kind == "greedy":
             d.update(B=c["B"], K=c["K"], V=c["V"])
         elif self.kind == "tree":
             d.update(B=c["B"], N=c["N"], V=c["V"], T=self.T, max_depth=c["max_depth"],
                      max_children=c["max_children"])
+        elif self.kind == "spot":
+            d.update(B=c["B"], N=c["N"], L=c["L"], V=c["V"], T=self.T, max_depth=c["max_depth"],
+                     max_children=c["max_children"])
+        elif self.kind == "anyorder":
+            d.update(B=c["B"], Kv=c["K"], W=c["W"], V=c["V"], T=0.0)
         else:
             d.update(B=c["B"], K=c["K"], W=c["W"], V=c["V"], T=self.T)
         d["logits"] = c["dtype"]
@@ -266,6 +274,17 @@ class Workload:
                                      max_children=c["max_children"], device=device)
             return {"node_logits": ti.node_logits, "parent": ti.parent, "node_pos": ti.node_pos,
                     "node_tok": ti.node_tok}
+        if self.kind == "anyorder":
+            ai = datagen.anyorder_inputs(B, c["K"], c["W"], c["V"], dtype=c["dtype"],
+                                         seed=c["seed"], device=device)
+            return {"logits": ai.logits, "u": ai.u, "win_pos": ai.win_pos, "order": ai.order,
+                    "draft": ai.draft, "end_pos": ai.end_pos}
+        if self.kind == "spot":
+            si = datagen.spot_inputs(B, c["N"], c["L"], c["V"], dtype=c["dtype"], seed=c["seed"],
+                                     max_depth=c["max_depth"], max_children=c["max_children"],
+                                     device=device)
+            return {"state_logits": si.state_logits, "parent": si.parent,
+                    "node_pos": si.node_pos, "node_tok": si.node_tok, "root_mask": si.root_mask}
         pi = datagen.packed_inputs(B, c["K"], c["W"], c["V"], dtype=c["dtype"], seed=c["seed"],
                                    T=self.T, device=device)
         d = {"logits": pi.logits, "prev_draft": pi.prev_draft, "prev_len": pi.prev_len}
@@ -287,6 +306,14 @@ class Workload:
         if self.kind == "tree":
             return dbv.sv_verify_tree(inp["node_logits"], inp["parent"], inp["node_pos"],
                                       inp["node_tok"], T=self.T, seed=c["seed"], handle=h)
+        if self.kind == "anyorder":
+            return dbv.sv_packed_anyorder_step(inp["logits"], c["K"], c["W"], inp["u"],
+                                               inp["win_pos"], inp["order"], inp["draft"],
+                                               inp["end_pos"], handle=h)
+        if self.kind == "spot":
+            return dbv.sv_verify_spot(inp["state_logits"], inp["parent"], inp["node_pos"],
+                                      inp["node_tok"], inp["root_mask"], T=self.T,
+                                      seed=c["seed"], handle=h)
         return dbv.sv_packed_step(inp["logits"], c["K"], c["W"], inp["prev_draft"],
                                   inp["prev_len"], prev_q_at_draft=inp.get("prev_q_at_draft"),
                                   prev_draft_logits=inp.get("prev_draft_logits"),
@@ -310,6 +337,14 @@ class Workload:
         elif self.kind == "tree":
             oracle.verify_tree(lg(inp["node_logits"]), n(inp["parent"]), n(inp["node_pos"]),
                                n(inp["node_tok"]), T=self.T, seed=c["seed"])
+        elif self.kind == "anyorder":
+            oracle.packed_anyorder_step(lg(inp["logits"]), c["K"], c["W"], n(inp["u"]),
+                                        n(inp["win_pos"]), n(inp["order"]), n(inp["draft"]),
+                                        n(inp["end_pos"]))
+        elif self.kind == "spot":
+            oracle.verify_spot(lg(inp["state_logits"]), n(inp["parent"]), n(inp["node_pos"]),
+                               n(inp["node_tok"]), n(inp["root_mask"]).astype(np.uint64),
+                               T=self.T, seed=c["seed"])
         else:
             pdl = inp.get("prev_draft_logits")
             oracle.packed_step(lg(inp["logits"]), c["K"], c["W"], n(inp["prev_draft"]),
@@ -327,8 +362,10 @@ class Workload:
             if "draft_len" in inp:
                 return int(inp["draft_len"].sum().item())
             return int(inp["draft_ids"].shape[0]) * c["K"]
-        if self.kind == "tree":
+        if self.kind in ("tree", "spot"):
             return int(inp["parent"].numel())
+        if self.kind == "anyorder":
+            return int(sum(k for k, _ in self.anyorder_rows(inp)))
         return int(inp["prev_len"].sum().item())
 
     def alg_bytes(self, inp):
@@ -343,8 +380,37 @@ class Workload:
             return int((inp["draft_len"].long() + 1).sum().item()) * row
         if self.kind == "tree":
             return int(inp["parent"].numel()) * row
+        if self.kind == "spot":
+            return self.spot_rows(inp) * row
+        if self.kind == "anyorder":
+            return int(sum(min(k + 1, u) + u for k, u in self.anyorder_rows(inp))) * row
         B = inp["logits"].shape[0]
         return int((inp["prev_len"].long() + 1).sum().item() + B * c["W"]) * row
+
+    def anyorder_rows(self, inp):
+        """(kappa, u) of every sequence of an any-order call: kappa verified
+        draft tokens; min(kappa + 1, u) verify rows and u proposal rows read."""
+        u = inp["u"].cpu().numpy()
+        od, dr = inp["order"].cpu().numpy(), inp["draft"].cpu().numpy()
+        out = []
+        for b in range(len(u)):
+            k = 0
+            while k < u[b] and dr[b, od[b, k]] >= 0:
+                k += 1
+            out.append((k, int(u[b])))
+        return out
+
+    def spot_rows(self, inp):
+        """Rows a SPOT call streams: every masked position of every state."""
+        m = inp["root_mask"].cpu().numpy().astype(np.uint64)
+        par, pos = inp["parent"].cpu().numpy(), inp["node_pos"].cpu().numpy()
+        total = 0
+        for b in range(par.shape[0]):
+            masks = [int(m[b])]
+            for n in range(par.shape[1]):
+                masks.append(masks[par[b, n] + 1] & ~(1 << int(pos[b, n])))
+            total += sum(bin(x).count("1") for x in masks)
+        return total
 
     def decisions(self, out):
         """Per-call decision summary of a call's outputs: near-threshold flags,
@@ -352,7 +418,7 @@ class Workload:
         depth), and for Packed-SS the mean stopping index a."""
         t = lambda k: out[k].detach().float().cpu() if isinstance(out, dict) and k in out else None
         d = {}
-        if self.kind == "tree":
+        if self.kind in ("tree", "spot"):
             d["mean_path_len"] = float(t("path_len").mean())
         else:
             d["mean_accept_len"] = float(t("accept_len").mean())
@@ -368,6 +434,8 @@ class Workload:
         TV is asked for)."""
         if self.kind == "sample":
             return 4 if self.tv else 3
+        if self.kind in ("spot", "anyorder"):
+            return 2  # the per-sequence preparation, then the streaming pass
         return 3 if (self.kind == "packed" and self.T > 0) else 1
 
 
@@ -569,8 +637,9 @@ def main():
                     help="which verify workload one step runs (default: %s)" % WORKLOAD)
     ap.add_argument("--T", type=float, default=None, help="temperature (sample, tree, packed)")
     ap.add_argument("--sigma", type=float, default=None, help="drafter noise (sample)")
-    ap.add_argument("--lam", type=float, default=None, help="lambda (ratio) or mu (linear)")
-    ap.add_argument("--mode", default=None, choices=["lossless", "ratio", "linear"])
+    ap.add_argument("--lam", type=float, default=None,
+                    help="lambda (ratio), mu (linear) or the KL budget delta (cactus)")
+    ap.add_argument("--mode", default=None, choices=["lossless", "ratio", "linear", "cactus"])
     ap.add_argument("--no-tv", action="store_true",
                     help="lenient sweep: leave out the per-row TV pass")
     args = ap.parse_args()

@@ -28,6 +28,13 @@ CONFIGS = {
                  max_depth=8, max_children=4, T=(0.0, 1.0)),
     "packed": dict(kind="packed", B=256, K=32, W=32, V=151936, dtype="bf16", seed=4,
                    T=(0.0, 1.0)),
+    # any-order Packed-SS steps: windows of 32 unresolved positions checked
+    # in a random rank order, drafts at 90% of them
+    "anyorder": dict(kind="anyorder", B=256, K=32, W=32, V=151936, dtype="bf16", seed=6),
+    # SPOT trees with the target's own position selection: 32 trees of 8
+    # drafted states over a 32-position block that starts fully masked
+    "spot": dict(kind="spot", B=32, N=8, L=32, V=151936, dtype="bf16", seed=5,
+                 max_depth=8, max_children=4, T=(0.0, 1.0)),
 }
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -217,3 +224,103 @@ def to_numpy_logits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(t.dtype)
+
+
+@dataclasses.dataclass
+class SpotInputs:
+    state_logits: torch.Tensor  # [B, 1+N, L, V]
+    parent: torch.Tensor        # [B, N] int32, -1 = child of the root
+    node_pos: torch.Tensor      # [B, N] int32, a masked position of the parent's state
+    node_tok: torch.Tensor      # [B, N] int32
+    root_mask: torch.Tensor     # [B] int64, bit s = position s masked at the root
+    masks: np.ndarray           # [B, 1+N] host-side masks of every state
+
+
+def spot_trees(B, N, L, max_depth=8, max_children=4, seed=5, root_masked=None):
+    """Random SPOT draft trees (host numpy): the root state has root_masked
+    masked positions (all L by default, else a uniform subset); node n picks
+    a uniform parent among the root and the earlier nodes that have a masked
+    position left, depth below max_depth and fewer than max_children
+    children, and commits at a uniform masked position of that parent's
+    state."""
+    rng = np.random.default_rng(seed)
+    parent = np.full((B, N), -1, np.int32)
+    pos = np.zeros((B, N), np.int32)
+    masks = np.zeros((B, N + 1), np.uint64)
+    k = L if root_masked is None else root_masked
+    for b in range(B):
+        m0 = 0
+        for s in rng.choice(L, size=k, replace=False):
+            m0 |= 1 << int(s)
+        masks[b, 0] = m0
+        depth = np.zeros(N + 1, np.int64)
+        children = np.zeros(N + 1, np.int64)
+        for n in range(N):
+            cand = [a for a in range(n + 1) if int(masks[b, a]) != 0 and depth[a] < max_depth
+                    and children[a] < max_children]
+            a = cand[rng.integers(len(cand))]
+            free = [s for s in range(L) if (int(masks[b, a]) >> s) & 1]
+            s = free[rng.integers(len(free))]
+            parent[b, n] = a - 1
+            pos[b, n] = s
+            masks[b, n + 1] = int(masks[b, a]) & ~(1 << s)
+            depth[n + 1] = depth[a] + 1
+            children[a] += 1
+    return parent, pos, masks
+
+
+def spot_inputs(B, N, L, V, dtype="bf16", seed=5, max_depth=8, max_children=4, p_match=0.8,
+                root_masked=None, device="cpu") -> SpotInputs:
+    """SPOT workload: rows N(0, 2^2) for every (state, position); node tokens
+    = the largest entry of the parent state's row at the node's position with
+    probability p_match, else a uniform other id."""
+    parent, pos, masks = spot_trees(B, N, L, max_depth, max_children, seed, root_masked)
+    g = _gen(seed, device)
+    logits = _normal((B, N + 1, L, V), 2.0, g, device).to(_TORCH_DTYPE[dtype])
+    t = lambda a: torch.as_tensor(a, dtype=torch.int32, device=device)
+    par_state = torch.as_tensor(parent.astype(np.int64) + 1, device=device)
+    rows = logits[torch.arange(B, device=device)[:, None], par_state,
+                  torch.as_tensor(pos.astype(np.int64), device=device)] if N > 0 else None
+    tok = _pick_tokens(rows, p_match, g, device) if N > 0 else \
+        torch.zeros((B, 0), dtype=torch.int32, device=device)
+    rm = torch.as_tensor(masks[:, 0].astype(np.int64), device=device)
+    return SpotInputs(logits, t(parent), t(pos), tok, rm, masks)
+
+
+@dataclasses.dataclass
+class AnyOrderInputs:
+    logits: torch.Tensor   # [B, Kv + W, V]
+    u: torch.Tensor        # [B] int32
+    win_pos: torch.Tensor  # [B, W] int32, ascending output positions
+    order: torch.Tensor    # [B, W] int32, window index of each rank
+    draft: torch.Tensor    # [B, W] int32, -1 = no draft
+    end_pos: torch.Tensor  # [B] int32
+
+
+def anyorder_inputs(B, Kv, W, V, dtype="bf16", seed=6, p_draft=0.9, p_match=0.8, ragged=False,
+                    device="cpu") -> AnyOrderInputs:
+    """Any-order Packed-SS state: u unresolved window positions (W, or uniform
+    in 1..W when ragged) at ascending output positions with random gaps, a
+    random rank order, a draft token at each position with probability
+    p_draft -- at rank r the largest entry of verify row r with probability
+    p_match, else a uniform other id -- and rows N(0, 2^2)."""
+    rng = np.random.default_rng(seed)
+    g = _gen(seed, device)
+    logits = _normal((B, Kv + W, V), 2.0, g, device).to(_TORCH_DTYPE[dtype])
+    best = logits[:, :Kv].float().argmax(-1).cpu().numpy()
+    u = rng.integers(1, W + 1, B) if ragged else np.full(B, W)
+    wp = np.full((B, W), -1, np.int32)
+    od = np.full((B, W), -1, np.int32)
+    dr = np.full((B, W), -1, np.int32)
+    for b in range(B):
+        n = int(u[b])
+        wp[b, :n] = np.sort(rng.choice(np.arange(1, 4 * W + 1), n, replace=False))
+        od[b, :n] = rng.permutation(n)
+        for r in range(n):
+            if rng.random() < p_draft:
+                if r < Kv and rng.random() < p_match:
+                    dr[b, od[b, r]] = best[b, r]
+                else:
+                    dr[b, od[b, r]] = int(rng.integers(V))
+    t = lambda a: torch.as_tensor(a, dtype=torch.int32, device=device)
+    return AnyOrderInputs(logits, t(u), t(wp), t(od), t(dr), t(np.full(B, 10 ** 6)))

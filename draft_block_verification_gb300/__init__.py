@@ -23,7 +23,7 @@ from ._build import LIBPATH, build  # noqa: F401  (build is part of the API)
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_CUDA, SV_ERR_OOM = 0, 1, 2, 3
 SV_ERR_TIMEOUT, SV_ERR_UNSUPPORTED, SV_ERR_DEVICE_BOUNDS = 4, 5, 6
 SV_F32, SV_BF16 = 0, 1
-SV_LOSSLESS, SV_LENIENT_RATIO, SV_LENIENT_LINEAR = 0, 1, 2
+SV_LOSSLESS, SV_LENIENT_RATIO, SV_LENIENT_LINEAR, SV_LENIENT_CACTUS = 0, 1, 2, 3
 SV_OPT_FORCE_RESCUE, SV_OPT_TIMING_EVENTS = 1, 2
 
 _lib = None
@@ -55,6 +55,7 @@ def lib():
         L.sv_set_option.restype, L.sv_set_option.argtypes = i32, [vp, i32, i64]
         L.sv_selftest.restype = i32
         L.sv_selftest.argtypes = [vp, u64, i64, C.POINTER(C.c_double), vp]
+        L.sv_wait_selftest.restype, L.sv_wait_selftest.argtypes = i32, [vp, i64, vp]
         L.sv_verify_greedy.restype = i32
         L.sv_verify_greedy.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, vp, vp]
         L.sv_verify_greedy_static.restype = i32
@@ -66,6 +67,12 @@ def lib():
         L.sv_verify_tree.restype = i32
         L.sv_verify_tree.argtypes = [vp, vp, i32, i64, i32, i32, i32, vp, vp, vp, f32, u64, vp,
                                      vp, vp, i32, vp, vp, vp, vp]
+        L.sv_verify_spot.restype = i32
+        L.sv_verify_spot.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, f32,
+                                     u64, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.sv_packed_anyorder_step.restype = i32
+        L.sv_packed_anyorder_step.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp,
+                                              vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.sv_packed_step.restype = i32
         L.sv_packed_step.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                      f32, u64, u64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -125,6 +132,12 @@ class Handle:
         _check(lib().sv_selftest(self.ptr, int(seed), int(n), r, _stream(stream, self.device)),
                "sv_selftest")
         return list(r)
+
+    def wait_selftest(self, limit: int = 1000, stream=None):
+        """Enqueue the self-test whose bounded waits run out: the next
+        sync_status raises SVError with SV_ERR_TIMEOUT."""
+        _check(lib().sv_wait_selftest(self.ptr, int(limit), _stream(stream, self.device)),
+               "sv_wait_selftest")
 
     def set_option(self, opt: int, value: int):
         _check(lib().sv_set_option(self.ptr, int(opt), int(value)), "sv_set_option")
@@ -288,6 +301,63 @@ def sv_verify_tree(node_logits, parent, node_pos, node_tok, *, T=0.0, seed=0, po
         int(seed) & (2**64 - 1), _p(pos_base), _p(out["path_len"]), _p(out["path_nodes"]), md,
         _p(out["commit_count"]), _p(out["match"]), _p(out["flags"]), _stream(stream, dev)),
         "sv_verify_tree")
+    return out
+
+
+def sv_verify_spot(state_logits, parent, node_pos, node_tok, root_mask, *, T=0.0, seed=0,
+                   pos_base=None, max_depth=None, handle=None, stream=None):
+    """SPOT verification with the target's position selection (see sv.h):
+    state_logits [B, 1+N, L, V]; parent/node_pos/node_tok [B, N] int32;
+    root_mask [B] int64 (bit s: position s is masked in the root state)."""
+    B, S, L, V = state_logits.shape
+    N = S - 1
+    dev = state_logits.device
+    code, rs = _rows(state_logits, "state_logits")
+    h = handle or default_handle(dev)
+    par = _i32(parent, (B, N), "parent", dev) if N > 0 else None
+    pos = _i32(node_pos, (B, N), "node_pos", dev) if N > 0 else None
+    tok = _i32(node_tok, (B, N), "node_tok", dev) if N > 0 else None
+    if (root_mask.dtype != torch.int64 or not root_mask.is_cuda or root_mask.device != dev
+            or not root_mask.is_contiguous() or tuple(root_mask.shape) != (B,)):
+        raise ValueError("root_mask must be a contiguous int64 CUDA tensor of shape [B]")
+    if pos_base is not None and (pos_base.dtype != torch.int64 or not pos_base.is_cuda):
+        raise ValueError("pos_base must be an int64 CUDA tensor")
+    md = max(N, 1) if max_depth is None else int(max_depth)
+    i = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
+    out = {"path_len": i(B), "path_nodes": i(B, md), "commit_count": i(B), "commit_pos": i(B),
+           "commit_tok": i(B), "match": torch.empty((B, N), dtype=torch.uint8, device=dev),
+           "state_pos": i(B, S), "state_tok": i(B, S), "flags": i(B)}
+    _check(lib().sv_verify_spot(
+        h.ptr, _p(state_logits), code, rs, B, N, L, V, _p(par), _p(pos), _p(tok),
+        _p(root_mask), float(T), int(seed) & (2**64 - 1), _p(pos_base), _p(out["path_len"]),
+        _p(out["path_nodes"]), md, _p(out["commit_count"]), _p(out["commit_pos"]),
+        _p(out["commit_tok"]), _p(out["match"]) if N > 0 else None, _p(out["state_pos"]),
+        _p(out["state_tok"]), _p(out["flags"]), _stream(stream, dev)), "sv_verify_spot")
+    return out
+
+
+def sv_packed_anyorder_step(logits, Kv, W, u, win_pos, order, draft, end_pos, *, eos_id=-1,
+                            handle=None, stream=None):
+    """One any-order Packed-SS iteration (see sv.h); logits [B, Kv + W, V];
+    u, end_pos [B]; win_pos, order, draft [B, W] (int32 CUDA tensors)."""
+    B, R, V = logits.shape
+    if R != Kv + W:
+        raise ValueError("logits must be [B, Kv + W, V]")
+    dev = logits.device
+    code, rs = _rows(logits, "logits")
+    h = handle or default_handle(dev)
+    uu, end = _i32(u, (B,), "u", dev), _i32(end_pos, (B,), "end_pos", dev)
+    wp, od, dr = (_i32(a, (B, W), n, dev) for a, n in ((win_pos, "win_pos"), (order, "order"),
+                                                        (draft, "draft")))
+    i = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
+    out = {"accept_len": i(B), "commit_len": i(B), "commit_pos": i(B, W), "commit_tok": i(B, W),
+           "end_pos": i(B), "next_draft": i(B, W),
+           "score": torch.empty((B, W), dtype=torch.float32, device=dev), "next_order": i(B, W)}
+    _check(lib().sv_packed_anyorder_step(
+        h.ptr, _p(logits), code, rs, B, Kv, W, V, _p(uu), _p(wp), _p(od), _p(dr), _p(end),
+        int(eos_id), _p(out["accept_len"]), _p(out["commit_len"]), _p(out["commit_pos"]),
+        _p(out["commit_tok"]), _p(out["end_pos"]), _p(out["next_draft"]), _p(out["score"]),
+        _p(out["next_order"]), _stream(stream, dev)), "sv_packed_anyorder_step")
     return out
 
 

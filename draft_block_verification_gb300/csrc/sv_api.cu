@@ -16,10 +16,13 @@ size_t pass_smem_bytes();
 size_t rescue_scratch_doubles(int B);
 cudaError_t pass_setup(int *blocks_per_sm);
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s);
+cudaError_t spot_prep_launch(const Job &j, cudaStream_t s);
+cudaError_t anyorder_prep_launch(const Job &j, cudaStream_t s);
 cudaError_t post_setup(int occ[2]);
 cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
                         cudaStream_t s);
 cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s);
+cudaError_t wait_selftest_run(int *err, const unsigned *word, uint32_t limit, cudaStream_t s);
 }  // namespace sv
 
 using namespace sv;
@@ -42,6 +45,32 @@ struct sv_handle {
     bool timing = false;
     std::mutex mu;
 };
+
+namespace sv {
+// Host fault injection for failure-path tests.  SV_FAULT_INJECT holds
+// "call:code[,call:code...]"; a listed entry point returns the status
+// `code` (1..6) at its launch point -- after its argument checks, before it
+// enqueues anything -- without touching the GPU.  Unset, empty or malformed
+// entries inject nothing.  The variable is read at every call.
+sv_status fault_injected(const char *call)
+{
+    const char *env = getenv("SV_FAULT_INJECT");
+    if (!env || !*env) return SV_OK;
+    const size_t n = strlen(call);
+    for (const char *p = env; *p;) {
+        const char *end = strchr(p, ',');
+        const size_t len = end ? (size_t)(end - p) : strlen(p);
+        if (len > n + 1 && strncmp(p, call, n) == 0 && p[n] == ':') {
+            char *stop = nullptr;
+            const long code = strtol(p + n + 1, &stop, 10);
+            if (stop == p + len && code >= 1 && code <= 6) return (sv_status)code;
+        }
+        if (!end) break;
+        p = end + 1;
+    }
+    return SV_OK;
+}
+}  // namespace sv
 
 namespace {
 
@@ -110,10 +139,10 @@ sv_status cuda_status(cudaError_t e)
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t rp, rs, resid, rescue, dtmp, tvpart, rpart, total;
+    size_t rp, rs, resid, rescue, dtmp, tvpart, rpart, smask, svalid, total;
 };
 
-Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks)
+Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks, int states)
 {
     Layout L;
     size_t o = 0;
@@ -124,6 +153,8 @@ Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks)
     L.dtmp = o;   o = align_up(o + (size_t)B * std::max(W, 1) * sizeof(DraftTmp));
     L.tvpart = o; o = align_up(o + (size_t)B * std::max(K, 1) * tv_chunks * sizeof(float));
     L.rpart = o;  o = align_up(o + rescue_scratch_doubles(B) * sizeof(double));
+    L.smask = o;  o = align_up(o + (size_t)B * states * sizeof(uint64_t));
+    L.svalid = o; o = align_up(o + (size_t)B * sizeof(unsigned));
     L.total = o;
     return L;
 }
@@ -236,7 +267,8 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.rTp = j.Tp > 0.f ? 1.0 / (double)j.Tp : 0.0;
     j.rTq = j.Tq > 0.f ? 1.0 / (double)j.Tq : 0.0;
     j.tv_chunks = tv_chunks;
-    Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks);
+    Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks,
+                      j.kind == K_SPOT ? j.N + 1 : (j.kind == K_ANYORDER ? 1 : 0));
     sv_status st = ensure_ws(h, L.total, s);
     if (st != SV_OK) return st;
     st = ensure_cnt(h, j.B, s);
@@ -251,12 +283,18 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.dtmp = (DraftTmp *)(w + L.dtmp);
     j.tvpart = (float *)(w + L.tvpart);
     j.rpart = (double *)(w + L.rpart);
+    j.smask = (uint64_t *)(w + L.smask);
+    j.svalid = (unsigned *)(w + L.svalid);
     *grid = (int)std::min<long long>(j.total_units, resident);
     return SV_OK;
 }
 
 sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post, bool tv)
 {
+    if (j.kind == K_SPOT || j.kind == K_ANYORDER) {
+        cudaError_t e = j.kind == K_SPOT ? spot_prep_launch(j, s) : anyorder_prep_launch(j, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     if (h->timing) cudaEventRecord(h->ev[0], s);
     cudaError_t e = pass_launch(j, grid, s);
     if (h->timing) cudaEventRecord(h->ev[1], s);
@@ -288,6 +326,7 @@ sv_status sv_create(sv_handle **out)
 {
     if (!out) return SV_ERR_INVALID_ARG;
     *out = nullptr;
+    if (sv_status fi = fault_injected("sv_create")) return fi;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_UNSUPPORTED;
     cudaDeviceProp prop;
@@ -377,6 +416,16 @@ sv_status sv_selftest(sv_handle *h, uint64_t seed, int64_t n, double *ratios, vo
     return cuda_status(selftest_run(seed, n, ratios, (cudaStream_t)stream));
 }
 
+sv_status sv_wait_selftest(sv_handle *h, int64_t limit, void *stream)
+{
+    if (!h || limit < 0 || limit > (int64_t)kSpinLimit) return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    // the word waited on is the handle's control word C_RESCUED, which only
+    // the fp64 path changes, and never while this kernel runs on the stream
+    return cuda_status(wait_selftest_run(h->d_err, h->d_ctl + C_RESCUED, (uint32_t)limit,
+                                         (cudaStream_t)stream));
+}
+
 sv_status sv_set_option(sv_handle *h, sv_option opt, int64_t value)
 {
     if (!h) return SV_ERR_INVALID_ARG;
@@ -416,6 +465,7 @@ sv_status sv_verify_greedy(sv_handle *h, const void *target, sv_dtype dtype, int
     j.K = K;
     j.ids = draft_ids;
     j.lens = draft_len;
+    if (sv_status fi = fault_injected("sv_verify_greedy")) return fi;
     j.acc = accept_len;
     j.next = next_token;
     int grid;
@@ -436,7 +486,9 @@ sv_status sv_verify_sample(sv_handle *h, const void *target, const void *draft, 
     if (!(T_p >= 0.f) || !(T_q >= 0.f) || !isfinite(T_p) || !isfinite(T_q)) return SV_ERR_INVALID_ARG;
     if (mode == SV_LENIENT_RATIO && !(lam >= 1.f && isfinite(lam))) return SV_ERR_INVALID_ARG;
     if (mode == SV_LENIENT_LINEAR && !(lam >= 0.f && lam <= 1.f)) return SV_ERR_INVALID_ARG;
-    if (mode != SV_LOSSLESS && mode != SV_LENIENT_RATIO && mode != SV_LENIENT_LINEAR)
+    if (mode == SV_LENIENT_CACTUS && !(lam >= 0.f && isfinite(lam))) return SV_ERR_INVALID_ARG;
+    if (mode != SV_LOSSLESS && mode != SV_LENIENT_RATIO && mode != SV_LENIENT_LINEAR &&
+        mode != SV_LENIENT_CACTUS)
         return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
     if (T_p == 0.f) {  // greedy rule on the target rows
@@ -478,6 +530,7 @@ sv_status sv_verify_sample(sv_handle *h, const void *target, const void *draft, 
     const int tvc = (int)std::min<long long>(
         16, std::max<long long>(1, (4LL * h->sms + (long long)B * std::max(K, 1) - 1) /
                                        ((long long)B * std::max(K, 1))));
+    if (sv_status fi = fault_injected("sv_verify_sample")) return fi;
     int grid;
     sv_status st = plan(h, j, 2 * K + 1, s, tvc, &grid);
     if (st != SV_OK) return st;
@@ -517,8 +570,102 @@ sv_status sv_verify_tree(sv_handle *h, const void *node_logits, sv_dtype dtype, 
     j.commit_count = commit_count;
     j.match = match;
     j.flags = flags;
+    if (sv_status fi = fault_injected("sv_verify_tree")) return fi;
     int grid;
     sv_status st = plan(h, j, N, s, 1, &grid);
+    if (st != SV_OK) return st;
+    return launch(h, j, grid, s, false, false);
+}
+
+sv_status sv_verify_spot(sv_handle *h, const void *state_logits, sv_dtype dtype,
+                         int64_t row_stride, int B, int N, int L, int V, const int32_t *parent,
+                         const int32_t *node_pos, const int32_t *node_tok,
+                         const uint64_t *root_mask, float T, uint64_t seed,
+                         const int64_t *pos_base, int32_t *path_len, int32_t *path_nodes,
+                         int max_depth, int32_t *commit_count, int32_t *commit_pos,
+                         int32_t *commit_tok, uint8_t *match, int32_t *state_pos,
+                         int32_t *state_tok, int32_t *flags, void *stream)
+{
+    if (!h || B < 0 || N < 0 || N > kMaxN || L < 1 || L > kMaxL || max_depth < 0)
+        return SV_ERR_INVALID_ARG;
+    if (!(T >= 0.f) || !isfinite(T)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!path_len || !commit_count || !commit_pos || !commit_tok || !root_mask ||
+        (max_depth > 0 && !path_nodes) || (N > 0 && (!parent || !node_pos || !node_tok)))
+        return SV_ERR_INVALID_ARG;
+    if (!logits_ok(state_logits, dtype, row_stride, V)) return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    Job j;
+    fill_common(j, h, state_logits, dtype, row_stride, V);
+    j.kind = K_SPOT;
+    j.B = B;
+    j.N = N;
+    j.L = L;
+    j.Tp = T;
+    j.invTp = T > 0.f ? (float)(1.0 / (double)T) : 0.f;
+    j.seed = seed;
+    j.pos_base = pos_base;
+    j.parent = parent;
+    j.node_pos = node_pos;
+    j.node_tok = node_tok;
+    j.root_mask = root_mask;
+    j.path_len = path_len;
+    j.path_nodes = path_nodes;
+    j.max_depth = max_depth;
+    j.commit_count = commit_count;
+    j.commit_pos = commit_pos;
+    j.commit_tok = commit_tok;
+    j.match = match;
+    j.state_pos = state_pos;
+    j.state_tok = state_tok;
+    j.flags = flags;
+    if (sv_status fi = fault_injected("sv_verify_spot")) return fi;
+    int grid;
+    sv_status st = plan(h, j, (N + 1) * L, s, 1, &grid);
+    if (st != SV_OK) return st;
+    return launch(h, j, grid, s, false, false);
+}
+
+sv_status sv_packed_anyorder_step(sv_handle *h, const void *logits, sv_dtype dtype,
+                                  int64_t row_stride, int B, int Kv, int W, int V,
+                                  const int32_t *u, const int32_t *win_pos, const int32_t *order,
+                                  const int32_t *draft, const int32_t *end_pos, int32_t eos_id,
+                                  int32_t *accept_len, int32_t *commit_len, int32_t *commit_pos,
+                                  int32_t *commit_tok, int32_t *end_out, int32_t *next_draft,
+                                  float *score, int32_t *next_order, void *stream)
+{
+    if (!h || B < 0 || Kv < 1 || Kv > kMaxK || W < 1 || W > kMaxK) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!logits_ok(logits, dtype, row_stride, V) || !u || !win_pos || !order || !draft ||
+        !end_pos || !accept_len || !commit_len || !commit_pos || !commit_tok || !end_out ||
+        !next_draft || !next_order)
+        return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    Job j;
+    fill_common(j, h, logits, dtype, row_stride, V);
+    j.kind = K_ANYORDER;
+    j.B = B;
+    j.K = Kv;
+    j.W = W;
+    j.lens = u;
+    j.win_pos = win_pos;
+    j.order = order;
+    j.ids = draft;
+    j.end_in = end_pos;
+    j.eos = eos_id;
+    j.acc = accept_len;
+    j.commit_len = commit_len;
+    j.commit_pos = commit_pos;
+    j.commit_tok = commit_tok;
+    j.end_out = end_out;
+    j.next_draft = next_draft;
+    j.confidence = score;
+    j.next_order = next_order;
+    if (sv_status fi = fault_injected("sv_packed_anyorder_step")) return fi;
+    int grid;
+    sv_status st = plan(h, j, Kv + W, s, 1, &grid);
     if (st != SV_OK) return st;
     return launch(h, j, grid, s, false, false);
 }
@@ -573,6 +720,7 @@ sv_status sv_packed_step(sv_handle *h, const void *logits, sv_dtype dtype, int64
     j.next_q = next_q_at_draft;
     j.confidence = confidence;
     j.flags = flags;
+    if (sv_status fi = fault_injected("sv_packed_step")) return fi;
     int grid;
     sv_status st = plan(h, j, K + W, s, 1, &grid);
     if (st != SV_OK) return st;

@@ -143,6 +143,110 @@ __device__ __forceinline__ double alpha_of(int mode, double r, double lam)
 }
 
 // ---------------------------------------------------------------------------
+// Modified Cactus lenience ([TwoTrade] App. E).  The drafted token y with
+// target probability p gets gamma*: the largest gamma in [p, 1] with
+//   Phi(gamma) = gamma log(gamma/p) + (1-gamma) log((1-gamma)/(1-p)) <= delta
+// (eq. 17); every other token is scaled by c = (1-gamma*)/(1-p).  Phi rises
+// from 0 at p to log(1/p) at 1, so gamma* = 1 when delta >= log(1/p).
+// ---------------------------------------------------------------------------
+// Phi(g) - delta in fp64, with both logs taken as log1p of small quotients
+// (g near p when delta is small); *scale receives the size of its terms.
+__device__ __forceinline__ double cactus_f(double g, double p, double delta, double *d1,
+                                           double *scale)
+{
+    const double a = log1p((g - p) / p);          // log(g / p)
+    const double b = log1p((p - g) / (1.0 - p));  // log((1 - g) / (1 - p))
+    *d1 = a - b;                                  // Phi'(g)
+    *scale = fabs(g * a) + fabs((1.0 - g) * b) + delta;
+    return g * a + (1.0 - g) * b - delta;
+}
+
+// gamma* by Newton's method (the page's solver), started at the page's
+// second-order solution p + sqrt(2 delta p (1-p)) and kept inside the
+// bracket of the root by bisection steps.  Returns a verified bracket
+// [*glo, *ghi] of gamma*: the Newton point widened by 1e-10 relative on each
+// side, each side checked to lie on its side of the root with a margin of
+// 64 roundings of Phi's terms.  false when the check fails (the caller then
+// treats the decision as undecided).  fp64; a few hundred cycles per step on
+// this part's fp64 pipe, run for the few draft positions of one sequence.
+static __device__ __noinline__ bool cactus_bracket(double p, double delta, double *glo, double *ghi)
+{
+    if (!(p > 0.0)) {
+        *glo = *ghi = 0.0;
+        return true;
+    }
+    if (p >= 1.0 || delta >= -log(p)) {  // Phi(1) = log(1/p)
+        *glo = *ghi = 1.0;
+        return p >= 1.0 || delta > -log(p) * (1.0 + 1e-15);
+    }
+    if (!(delta > 0.0)) {
+        *glo = *ghi = p;
+        return true;
+    }
+    double lo = p, hi = 1.0;
+    double g = p + sqrt(2.0 * delta * p * (1.0 - p));
+    if (!(g > lo && g < hi))
+        g = 0.5 * (lo + hi);
+    for (int it = 0; it < 64; ++it) {
+        double d1, sc;
+        const double f = cactus_f(g, p, delta, &d1, &sc);
+        if (f > 0.0)
+            hi = g;
+        else
+            lo = g;
+        double gn = g - f / d1;
+        if (!(gn > lo && gn < hi))
+            gn = 0.5 * (lo + hi);
+        if (gn == g || hi - lo <= 4e-16 * hi)
+            break;
+        g = gn;
+    }
+    const double a = fmax(p, g * (1.0 - 1e-10)), b = fmin(1.0, g * (1.0 + 1e-10));
+    double d1, sa, sb;
+    const double fa = cactus_f(a, p, delta, &d1, &sa);
+    bool ok = a == p || fa < -64.0 * 0x1p-53 * sa;
+    if (b < 1.0) {
+        const double fb = cactus_f(b, p, delta, &d1, &sb);
+        ok = ok && fb > 64.0 * 0x1p-53 * sb;
+    }
+    *glo = a;
+    *ghi = b;
+    return ok;
+}
+
+// Acceptance probability min{1, gamma* / q} in fp64 from log p(d), log q(d)
+// (the fp64 path); gamma* is the middle of its bracket.
+__device__ __forceinline__ double cactus_alpha64(double lp, double lq, double delta)
+{
+    const double p = exp(lp);
+    double glo, ghi;
+    cactus_bracket(p, delta, &glo, &ghi);
+    const double g = 0.5 * (glo + ghi);
+    const double a = exp((g == p ? lp : log(g)) - lq);
+    return a < 1.0 ? a : 1.0;
+}
+
+// log c = log((1 - gamma*)/(1 - p)) for the residual in fp64 (the fp64 path).
+__device__ __forceinline__ double cactus_log_scale64(double lp, double delta)
+{
+    const double p = exp(lp);
+    double glo, ghi;
+    cactus_bracket(p, delta, &glo, &ghi);
+    const double g = 0.5 * (glo + ghi);
+    if (g == p)
+        return 0.0;
+    return log1p(-g) - log1p(-p);
+}
+
+// Acceptance probability of any rule in fp64 (the fp64 path).
+__device__ __forceinline__ double alpha_exact(int mode, double lp, double lq, double lam)
+{
+    if (mode == SV_LENIENT_CACTUS)
+        return cactus_alpha64(lp, lq, lam);
+    return alpha_of(mode, exp(lp - lq), lam);
+}
+
+// ---------------------------------------------------------------------------
 // Level 3 of the Gumbel-max filter for a logit row (score x/T + G).
 // ---------------------------------------------------------------------------
 struct GRes {

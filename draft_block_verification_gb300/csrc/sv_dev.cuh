@@ -68,7 +68,8 @@ enum : uint32_t { kAccept = 1, kSample = 2, kDraft = 3, kTree = 4 };
 enum : int { M_ARGMAX = 1, M_LSE = 2, M_LSE2 = 4, M_GUMBEL = 8, M_MAX = 16 };
 
 // Entry-point kinds.
-enum : int { K_GREEDY = 0, K_SAMPLE = 1, K_TREE = 2, K_PACKED = 3 };
+enum : int { K_GREEDY = 0, K_SAMPLE = 1, K_TREE = 2, K_PACKED = 3, K_SPOT = 4, K_ANYORDER = 5 };
+constexpr int kMaxL = 32;  // SPOT: positions per block state (one lane each)
 
 // ---------------------------------------------------------------------------
 // Counter-based random numbers, written from the published definition of
@@ -168,16 +169,35 @@ __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Bounded wait; returns false when the limit expired.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// Bounded wait of at most `limit` tries; returns false when the limit
+// expired.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t *bar, uint32_t parity, uint32_t limit)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try(bar, parity))
             return true;
         if (SV_SPIN_SLEEP_NS > 0 && i > 64)
             __nanosleep(SV_SPIN_SLEEP_NS);
     }
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    return mbar_wait_n(bar, parity, kSpinLimit);
+}
+
+// Bounded wait for a global word to leave the value `old` (the form of the
+// grid barrier of the fp64 path), giving up after `limit` tries or when *ab
+// is set; returns false when it gave up.
+__device__ __forceinline__ bool spin_until_change(const volatile unsigned *word, unsigned old,
+                                                  const volatile unsigned *ab, uint32_t limit)
+{
+    for (uint32_t it = 0; *word == old; ++it) {
+        if ((ab && *ab) || it >= limit)
+            return false;
+        __nanosleep(256);
+    }
+    return true;
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
@@ -209,10 +229,6 @@ __device__ __forceinline__ void pdl_trigger()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ void named_sync(int id, int nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 // Fast 2^x (MUFU); relative error within 2^-21 over the range used here, which
 // the error bounds below assume and a GPU test measures.

@@ -16,6 +16,8 @@ struct __align__(16) ResidEntry {
     const char *qrow;  // proposal row at position h
     double Lp, Lq;     // natural log-sum-exps of x/Tp and y/Tq
     double epsp, epsq; // relative error bounds of exp(Lp), exp(Lq)
+    double lclo, lchi; // bracket of log c: the residual is [c p - q]_+ (c = 1
+                       // but for the modified Cactus rule)
 };
 
 // A sequence that goes to the fp64 path.
@@ -90,6 +92,14 @@ struct Job {
     uint8_t *match;
     int32_t *commit_len, *committed, *next_draft, *next_len;
     float *next_q, *confidence;
+    // SPOT (K_SPOT): L positions per block state, root masks, Phi outputs
+    int L;
+    const uint64_t *root_mask;
+    int32_t *commit_pos, *commit_tok, *state_pos, *state_tok;
+    // any-order Packed-SS (K_ANYORDER): window positions, rank order, end
+    // position in and out, the next confidence order
+    const int32_t *win_pos, *order, *end_in;
+    int32_t *end_out, *next_order;
     // workspace
     RowPart *rp;        // [B * rows_per_seq * parts]
     RowStat *rs_stat;   // [B * rows_per_seq]
@@ -102,6 +112,9 @@ struct Job {
     unsigned *tvdone;   // [B * K]
     int tv_chunks;
     double *rpart;      // residual / fp64 scratch
+    uint64_t *smask;    // SPOT: masked positions of every state [B * (N + 1)];
+                        // any-order: verify rows needed per sequence [B]
+    unsigned *svalid;   // SPOT, any-order: rows to stream per sequence [B]
     int *err;
     const float *gtab;     // [kGTab] G bounds of ordinary ids
     const uint64_t *skip;  // [kSkipN] skip thresholds of the top-id draws
@@ -110,7 +123,7 @@ struct Job {
 // Row slot bookkeeping shared by the kernels.
 __device__ __forceinline__ int seq_len(const Job &j, int b)
 {
-    if (j.kind == K_TREE)
+    if (j.kind == K_TREE || j.kind == K_SPOT)
         return j.N;
     if (!j.lens)
         return j.kind == K_PACKED ? 0 : j.K;
@@ -131,6 +144,9 @@ __device__ __forceinline__ int valid_slots(const Job &j, int b)
     }
     case K_TREE:
         return j.N;
+    case K_SPOT:
+    case K_ANYORDER:
+        return (int)__ldg(j.svalid + b);
     default: {
         int n = min(max(seq_len(j, b), 0), j.K - 1);
         return n + 1 + j.W;
@@ -149,6 +165,12 @@ __device__ __forceinline__ bool slot_valid(const Job &j, int b, int slot)
     }
     case K_TREE:
         return true;
+    case K_SPOT:
+        return ((__ldg(j.smask + (int64_t)b * (j.N + 1) + slot / j.L) >> (slot % j.L)) & 1ull) != 0;
+    case K_ANYORDER: {
+        const int u = min(max(seq_len(j, b), 0), j.W);
+        return slot < (int)__ldg(j.smask + b) || (slot >= j.K && slot - j.K < u);
+    }
     default: {
         int n = min(max(seq_len(j, b), 0), j.K - 1);
         return slot <= n || slot >= j.K;
@@ -166,6 +188,10 @@ __device__ __forceinline__ const char *slot_row(const Job &j, int b, int slot)
                            : j.src1 + ((int64_t)b * j.K + (slot - j.K - 1)) * j.rs;
     case K_TREE:
         return j.src0 + ((int64_t)b * j.N + slot) * j.rs;
+    case K_SPOT:  // slot = state * L + position
+        return j.src0 + ((int64_t)b * (j.N + 1) * j.L + slot) * j.rs;
+    case K_ANYORDER:
+        return j.src0 + ((int64_t)b * (j.K + j.W) + slot) * j.rs;
     default:
         return j.src0 + ((int64_t)b * (j.K + j.W) + slot) * j.rs;
     }

@@ -109,6 +109,9 @@ struct PassShared {
     int seed_cnt[2];     // ids listed in a buffer
     int seed_n;
     int seed_more;
+    // barrier among the consumer warps (see csync) and each warp's phase
+    uint64_t csync;
+    uint32_t cph[kConsumerWarps];
     PlanEntry plan[kPlanQ];
     uint64_t plan_full[kPlanQ], plan_empty[kPlanQ];
     volatile int nunits;     // units this CTA streamed (set when the producer is done)
@@ -123,6 +126,8 @@ struct UnitPre {
     int64_t p0;    // absolute position of the sequence's first row
     int np;        // tree: position of the node (T > 0)
     int ida, idb;  // draft tokens of the two slots a light unit can map to
+    uint64_t smask;   // SPOT: masked positions of the unit's state
+    unsigned svalid;  // SPOT: rows the tree streams
 };
 
 // Unit order.  Rows that carry a Gumbel-max (a few times the work of a plain
@@ -189,7 +194,7 @@ __device__ __forceinline__ int draft_token(const Job &j, int b, int slot)
 
 __device__ __forceinline__ UnitPre unit_prefetch(const Job &j, long long u)
 {
-    UnitPre p{0, 0, 0, -1, -1};
+    UnitPre p{0, 0, 0, -1, -1, 0ull, 0u};
     if (u >= j.total_units)
         return p;
     const int b = unit_seq(j, u);
@@ -208,6 +213,16 @@ __device__ __forceinline__ UnitPre unit_prefetch(const Job &j, long long u)
         int slot, part;
         unit_map(j, u, b, 0, slot, part);
         p.np = __ldg(j.node_pos + (int64_t)b * j.N + slot);
+    }
+    if (j.kind == K_SPOT) {
+        int slot, part;
+        unit_map(j, u, b, 0, slot, part);
+        p.smask = __ldg(j.smask + (int64_t)b * (j.N + 1) + slot / j.L);
+        p.svalid = __ldg(j.svalid + b);
+    }
+    if (j.kind == K_ANYORDER) {
+        p.smask = __ldg(j.smask + b);  // verify rows needed
+        p.svalid = __ldg(j.svalid + b);
     }
     return p;
 }
@@ -272,6 +287,30 @@ __device__ __forceinline__ RowMode row_mode(const Job &j, int b, int slot, int n
             r.invT = j.invTp;
             r.T = j.Tp;
             r.key = rng_key(j.seed, kTree, (uint64_t)b, p0 + np, 0);
+        }
+        break;
+    case K_ANYORDER:
+        // verify rows: the argmax; proposal rows: the argmax and the
+        // log-sum-exp at temperature 1 of their confidence
+        if (slot < j.K) {
+            r.mode = M_ARGMAX;
+        } else {
+            r.mode = M_ARGMAX | M_LSE;
+            r.c1 = j.c1;
+        }
+        break;
+    case K_SPOT:
+        // the confidence max_v softmax(x)_v needs the row max and its
+        // log-sum-exp at temperature 1; the token, the argmax (T = 0) or the
+        // coupled-noise Gumbel-max at the row's absolute position (T > 0)
+        r.c1 = j.c1;
+        if (j.Tp == 0.f) {
+            r.mode = M_ARGMAX | M_LSE;
+        } else {
+            r.mode = M_GUMBEL | M_LSE | M_MAX;
+            r.invT = j.invTp;
+            r.T = j.Tp;
+            r.key = rng_key(j.seed, kTree, (uint64_t)b, p0 + slot % j.L, 0);
         }
         break;
     default:  // Packed-SS
@@ -340,8 +379,17 @@ __device__ __forceinline__ UnitInfo unit_info(const Job &j, long long u, const U
                 i.xid = d;
         }
     }
-    i.valid = slot_valid_n(j, n, i.slot);
-    i.expect = (unsigned)(valid_slots_n(j, n) * j.parts);
+    if (j.kind == K_SPOT) {
+        i.valid = ((p.smask >> (i.slot % j.L)) & 1ull) != 0;
+        i.expect = p.svalid * (unsigned)j.parts;
+    } else if (j.kind == K_ANYORDER) {
+        const int u = min(max(p.len, 0), j.W);
+        i.valid = i.slot < (int)p.smask || (i.slot >= j.K && i.slot - j.K < u);
+        i.expect = p.svalid * (unsigned)j.parts;
+    } else {
+        i.valid = slot_valid_n(j, n, i.slot);
+        i.expect = (unsigned)(valid_slots_n(j, n) * j.parts);
+    }
     i.rm = row_mode(j, i.b, i.slot, n, p.p0, p.np);
     return i;
 }
@@ -661,6 +709,7 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
     if (lane == 0 && (len < 0 || len > j.K)) latch(j.err, SV_ERR_DEVICE_BOUNDS);
     bool acc = false, und = false;
     double Lp = 0, Lq = 0;
+    double lclo = 0.0, lchi = 0.0;  // bracket of log c (modified Cactus residual)
     const double ep = j.eps_lse, eq = j.eps_lse;
     if (lane < n) {
         Lp = rp.L1a;
@@ -675,6 +724,19 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
         double rel = 1.01 * (ep + eq) + 0x1p-21 + 1e-13;
         double alo = alpha_of(j.amode, r * (1.0 - rel), j.lam);
         double ahi = alpha_of(j.amode, r * (1.0 + rel), j.lam);
+        if (j.amode == SV_LENIENT_CACTUS && r * (1.0 - rel) < 1.0) {
+            // gamma* grows with p: bracket p and q, then gamma* at both ends
+            // of p's bracket; alpha = gamma* / q and c = (1 - gamma*)/(1 - p)
+            const double plo = exp(lp - 1.01 * ep - 1e-13), phi = exp(lp + 1.01 * ep + 1e-13);
+            const double qlo = exp(lq - 1.01 * eq - 1e-13), qhi = exp(lq + 1.01 * eq + 1e-13);
+            double g0, g1, g2, g3;
+            const bool ok = cactus_bracket(plo, (double)j.lam, &g0, &g1) &&
+                            cactus_bracket(phi, (double)j.lam, &g2, &g3);
+            alo = ok ? fmin(1.0, g0 / qhi) : 0.0;
+            ahi = ok ? fmin(1.0, g3 / qlo) : 1.0;
+            lclo = (g3 < 1.0) ? log1p(-g3) - log1p(-plo) : -INFINITY;
+            lchi = log1p(-g0) - log1p(-phi);
+        }
         double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
         acc = u < alo - kFlagEps;
         bool rej = u >= ahi + kFlagEps;
@@ -713,6 +775,8 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
     double Lqh = __shfl_sync(0xFFFFFFFFu, Lq, f & 31);
     double eph = __shfl_sync(0xFFFFFFFFu, ep, f & 31);
     double eqh = __shfl_sync(0xFFFFFFFFu, eq, f & 31);
+    const double lcloh = __shfl_sync(0xFFFFFFFFu, lclo, f & 31);
+    const double lchih = __shfl_sync(0xFFFFFFFFu, lchi, f & 31);
     // bonus row n (always valid): its Gumbel-max with key (SAMPLE, pos + n),
     // resolved by the lane that holds its record
     GRes g = resolve_lanes(j, row_ptr(j, b, lane <= j.K ? lane : 0),
@@ -752,6 +816,8 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
             re.Lq = Lqh;
             re.epsp = eph;
             re.epsq = eqh;
+            re.lclo = lcloh;
+            re.lchi = lchih;
             j.resid[e] = re;
         }
     }
@@ -992,7 +1058,283 @@ static __device__ __noinline__ void fin_packed(const Job &j, int b)
         re.Lq = 0.0;
         re.epsp = eph;
         re.epsq = 0.0;
+        re.lclo = re.lchi = 0.0;
         j.resid[e] = re;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// SPOT decision step ([SPOT] App. A.1): the target's transition Phi at every
+// state of the tree (position s* by the largest probability over the state's
+// masked positions, then its token), the match bit of every node, and the
+// walk from the root through accepted children.  One warp; lane a holds
+// states a, a + 32 and a + 64.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int state_val(const int (&v)[3], int a)
+{
+    const int x0 = __shfl_sync(0xFFFFFFFFu, v[0], a & 31);
+    const int x1 = __shfl_sync(0xFFFFFFFFu, v[1], a & 31);
+    const int x2 = __shfl_sync(0xFFFFFFFFu, v[2], a & 31);
+    return (a >> 5) == 0 ? x0 : ((a >> 5) == 1 ? x1 : x2);
+}
+
+// max_v softmax(x)_v = 1 / sum_v exp(x_v - max x) of one row in fp64, by the
+// whole warp: the rare states whose fp32 confidences do not separate their
+// best position by the 1e-9 window.
+static __device__ __noinline__ double conf64_row(const Job &j, const char *row)
+{
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY;
+    for (int v = lane; v < j.V; v += 32)
+        m = fmaxf(m, load_logit(j, row, v));
+    m = warp_max(m);
+    double sum = 0.0;
+    for (int v = lane; v < j.V; v += 32)
+        sum += exp((double)load_logit(j, row, v) - (double)m);
+    return 1.0 / warp_sumd(sum);
+}
+
+static __device__ __noinline__ void fin_spot(const Job &j, int b)
+{
+    const int lane = threadIdx.x & 31;
+    const int S = j.N + 1, L = j.L;
+    const int64_t p0 = pos0_of(j, b);
+    // relative error of a confidence exp(m - L1) from the streamed sums
+    const double e = 1.01 * j.eps_lse + 0x1p-21 + 1e-13;
+    int sp[3], sv[3], nflag = 0;
+    for (int r = 0; r < 3; ++r) {
+        const int st = lane + 32 * r;
+        const uint64_t mk = st < S ? __ldg(j.smask + (int64_t)b * S + st) : 0ull;
+        // best position by fp32 confidence (lowest s among equal values) and
+        // the largest upper end among the other masked positions
+        float bc = -1.f;
+        double blo = 0.0, bhi = 0.0, ohi = -1.0;
+        int bs = -1, bam = -1;
+        Cand2 bgc;
+        bgc.init();
+        for (int s = 0; s < L; ++s) {
+            if (!((mk >> s) & 1ull))
+                continue;
+            const RowM rm = merge_row(j, b, st * L + s, j.cr1, 1.0);
+            const float c = exp_fast((double)rm.m - rm.L1a);
+            const double lo = (double)c * (1.0 - e), hi = (double)c * (1.0 + e);
+            if (c > bc) {
+                if (bs >= 0)
+                    ohi = fmax(ohi, bhi);
+                bc = c;
+                blo = lo;
+                bhi = hi;
+                bs = s;
+                bam = rm.amax;
+                bgc = rm.gc;
+            } else {
+                ohi = fmax(ohi, hi);
+            }
+        }
+        // settled in fp32 when the best's lower end clears every other upper
+        // end by the flag window; else the contenders in fp64, by the warp
+        const bool unsure = bs >= 0 && ohi >= 0.0 && blo - ohi < kFlagEps;
+        unsigned um = __ballot_sync(0xFFFFFFFFu, unsure);
+        while (um) {
+            const int src = __ffs(um) - 1;
+            um &= um - 1;
+            const int ost = src + 32 * r;
+            const uint64_t omk = __shfl_sync(0xFFFFFFFFu, mk, src);
+            const double oblo = __shfl_sync(0xFFFFFFFFu, blo, src);
+            // contenders: masked positions whose upper end reaches the best's
+            // lower end - 1e-9 (lane = position)
+            bool cont = false;
+            if (lane < L && ((omk >> lane) & 1ull)) {
+                const RowM rm = merge_row(j, b, ost * L + lane, j.cr1, 1.0);
+                const double c = (double)exp_fast((double)rm.m - rm.L1a);
+                cont = c * (1.0 + e) >= oblo - kFlagEps;
+            }
+            unsigned cm = __ballot_sync(0xFFFFFFFFu, cont);
+            double c1 = -1.0, c2 = -1.0;
+            int s1 = -1;
+            while (cm) {  // ascending positions: the lowest wins exact ties
+                const int s = __ffs(cm) - 1;
+                cm &= cm - 1;
+                const double c = conf64_row(j, row_ptr(j, b, ost * L + s));
+                if (c > c1) {
+                    c2 = c1;
+                    c1 = c;
+                    s1 = s;
+                } else if (c > c2) {
+                    c2 = c;
+                }
+            }
+            if (lane == src) {
+                bs = s1;
+                if (c1 - c2 > 0.0 && c1 - c2 < kFlagEps)
+                    ++nflag;
+            }
+        }
+        // the token at s*: its row's argmax (T = 0) or coupled-noise
+        // Gumbel-max (T > 0)
+        const bool has = bs >= 0;
+        const RowM rb = (has && unsure) ? merge_row(j, b, st * L + bs, j.cr1, 1.0) : RowM{};
+        if (has && unsure) {
+            bam = rb.amax;
+            bgc = rb.gc;
+        }
+        int v = has ? bam : -1;
+        if (j.Tp != 0.f) {
+            const GRes g = resolve_lanes(j, row_ptr(j, b, has ? st * L + bs : 0),
+                                         rng_key(j.seed, kTree, (uint64_t)b, p0 + (has ? bs : 0), 0),
+                                         (double)j.Tp, j.invTp, bgc, has);
+            v = has ? g.v : -1;
+            if (has)
+                nflag += g.flag;
+        }
+        sp[r] = bs;
+        sv[r] = v;
+        if (st < S) {
+            if (j.state_pos) j.state_pos[(int64_t)b * S + st] = bs;
+            if (j.state_tok) j.state_tok[(int64_t)b * S + st] = v;
+        }
+    }
+    // match bits: a node's commitment equals Phi of its parent's state
+    bool mt[2];
+    int par[2];
+    for (int h = 0; h < 2; ++h) {
+        const int n = lane + 32 * h;
+        const bool in = n < j.N;
+        par[h] = in ? __ldg(j.parent + (int64_t)b * j.N + n) : -2;
+        const int pos = in ? __ldg(j.node_pos + (int64_t)b * j.N + n) : -1;
+        const int tok = in ? __ldg(j.node_tok + (int64_t)b * j.N + n) : -1;
+        const bool ok = in && par[h] >= -1 && par[h] < n;
+        const int a = ok ? par[h] + 1 : 0;
+        const int ps = state_val(sp, a), pv = state_val(sv, a);
+        mt[h] = ok && ps >= 0 && pos == ps && tok == pv;
+        if (in && j.match) j.match[(int64_t)b * j.N + n] = mt[h] ? 1 : 0;
+    }
+    for (int k = lane; k < j.max_depth; k += 32)
+        j.path_nodes[(int64_t)b * j.max_depth + k] = -1;
+    __syncwarp();
+    // the walk: the lowest-index accepted child of the state reached
+    int y = -1, len = 0;
+    for (int it = 0; it < j.N; ++it) {
+        const unsigned c0 = __ballot_sync(0xFFFFFFFFu, mt[0] && par[0] == y);
+        const unsigned c1 = __ballot_sync(0xFFFFFFFFu, mt[1] && par[1] == y);
+        if (!c0 && !c1)
+            break;
+        const int nx = c0 ? __ffs(c0) - 1 : 32 + __ffs(c1) - 1;
+        if (lane == 0 && len < j.max_depth)
+            j.path_nodes[(int64_t)b * j.max_depth + len] = nx;
+        ++len;
+        y = nx;
+    }
+    const int cs = state_val(sp, y + 1), ct = state_val(sv, y + 1);
+    for (int o = 16; o; o >>= 1)
+        nflag += __shfl_xor_sync(0xFFFFFFFFu, nflag, o);
+    if (lane == 0) {
+        j.path_len[b] = len;
+        j.commit_count[b] = len + (cs >= 0 ? 1 : 0);
+        j.commit_pos[b] = cs;
+        j.commit_tok[b] = ct;
+        if (j.flags) j.flags[b] = nflag;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Any-order Packed-SS decision step ([PackedSS] App. C, Alg. 3 lines 6-15,
+// eq. 8; scores of App. E.6).  One warp; lane r is rank r of the verify
+// order and also window index r.
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ void fin_anyorder(const Job &j, int b)
+{
+    const int lane = threadIdx.x & 31;
+    const int W = j.W;
+    const int u = min(max(__ldg(j.lens + b), 0), W);
+    const int nreq = (int)__ldg(j.smask + b);
+    const int32_t *wp = j.win_pos + (int64_t)b * W, *od = j.order + (int64_t)b * W;
+    const int32_t *dr = j.ids + (int64_t)b * W;
+    // rank r: its window index, position and draft; kappa = leading ranks
+    // with a draft (the preparation checked that order is a permutation)
+    const int oi = lane < u ? __ldg(od + lane) : 0;
+    const int pos = lane < u ? __ldg(wp + oi) : 0;
+    const int d = lane < u ? __ldg(dr + oi) : -1;
+    const unsigned hasd = __ballot_sync(0xFFFFFFFFu, lane < u && d >= 0);
+    const int kappa = min((~hasd == 0u) ? 32 : __ffs(~hasd) - 1, u);
+    int v = -1;
+    if (lane < nreq)
+        v = merge_row(j, b, lane, 1.0, 1.0).amax;  // eq. 8: the verifier's argmax
+    const unsigned mm = __ballot_sync(0xFFFFFFFFu, lane < kappa && d == v);
+    const int h = min((~mm == 0u) ? 32 : __ffs(~mm) - 1, kappa);
+    const int A = min(h + 1, u);
+    // an accepted EOS at position p lowers the end to min(E, p)
+    const int E0 = __ldg(j.end_in + b);
+    int ecut = 0x7FFFFFFF;
+    if (lane < A && j.eos >= 0 && v == j.eos)
+        ecut = pos;
+    const int E = min(E0, __reduce_min_sync(0xFFFFFFFFu, ecut));
+    // accepted pairs within E, rank order
+    const bool keep = lane < A && pos <= E;
+    const unsigned km = __ballot_sync(0xFFFFFFFFu, keep);
+    const int kept = __popc(km);
+    const int slot = __popc(km & ((1u << lane) - 1u));
+    if (keep) {
+        j.commit_pos[(int64_t)b * W + slot] = pos;
+        j.commit_tok[(int64_t)b * W + slot] = v;
+    }
+    if (lane >= kept && lane < W) {
+        j.commit_pos[(int64_t)b * W + lane] = -1;
+        j.commit_tok[(int64_t)b * W + lane] = -1;
+    }
+    const unsigned accd = __reduce_or_sync(0xFFFFFFFFu, keep ? (1u << oi) : 0u);
+    // proposals (window index = lane): argmax, and its probability at
+    // temperature 1 with a relative error bound
+    const double e = 1.01 * j.eps_lse + 0x1p-21 + 1e-13;
+    int z = -1;
+    double sc = -1.0;
+    if (lane < u) {
+        const RowM rm = merge_row(j, b, j.K + lane, j.cr1, 1.0);
+        z = rm.amax;
+        sc = (double)exp_fast((double)rm.m - rm.L1a);
+    }
+    const int wpos = lane < u ? __ldg(wp + lane) : 0x7FFFFFFF;
+    const bool ret = lane < u && !((accd >> lane) & 1u) && wpos <= E;
+    // scores whose intervals overlap another retained score's are recomputed
+    // in fp64 (by the warp), so that the order below is exact
+    bool unsure = false;
+    for (int o = 0; o < 32; ++o) {
+        const double so = __shfl_sync(0xFFFFFFFFu, sc, o);
+        const bool ro = __shfl_sync(0xFFFFFFFFu, ret, o);
+        if (ret && ro && o != lane && fabs(sc - so) <= (sc + so) * e)
+            unsure = true;
+    }
+    unsigned um = __ballot_sync(0xFFFFFFFFu, unsure);
+    while (um) {
+        const int src = __ffs(um) - 1;
+        um &= um - 1;
+        const double c = conf64_row(j, row_ptr(j, b, j.K + src));
+        if (lane == src)
+            sc = c;
+    }
+    // rank of each retained position: decreasing score, ties by position
+    int rank = 0;
+    for (int o = 0; o < 32; ++o) {
+        const double so = __shfl_sync(0xFFFFFFFFu, sc, o);
+        const bool ro = __shfl_sync(0xFFFFFFFFu, ret, o);
+        if (ro && (so > sc || (so == sc && o < lane)))
+            ++rank;
+    }
+    const int nret = __popc(__ballot_sync(0xFFFFFFFFu, ret));
+    if (lane < W) {
+        j.next_draft[(int64_t)b * W + lane] = ret ? z : -1;
+        if (j.confidence)
+            j.confidence[(int64_t)b * W + lane] =
+                lane < u ? (float)sc : __int_as_float(0x7FC00000);
+        if (ret)
+            j.next_order[(int64_t)b * W + rank] = lane;
+        if (lane >= nret)
+            j.next_order[(int64_t)b * W + lane] = -1;
+    }
+    if (lane == 0) {
+        j.acc[b] = h;
+        j.commit_len[b] = kept;
+        j.end_out[b] = E;
     }
 }
 
@@ -1008,6 +1350,10 @@ __device__ __forceinline__ void fin_kind(const Job &j, int b)
         fin_sample(j, b);
     else if constexpr (KIND == K_TREE)
         fin_tree(j, b);
+    else if constexpr (KIND == K_SPOT)
+        fin_spot(j, b);
+    else if constexpr (KIND == K_ANYORDER)
+        fin_anyorder(j, b);
     else
         fin_packed(j, b);
 }
@@ -1276,14 +1622,59 @@ __device__ __forceinline__ float logit_of_word(uint32_t w, uint32_t v)
     return __uint_as_float(w);
 }
 
+// Barrier among the consumer warps on an mbarrier (kConsumerWarps arrivals)
+// with a bounded wait.  A hardware barrier would wait without end for a warp
+// that gave up after an expired wait; this one gives up too (latching
+// SV_ERR_TIMEOUT), and the CTA's abort flag then makes every later wait
+// return at once and the consumers leave the stream.  Every consumer thread
+// calls it; returns false when the barrier did not complete.  The mbarrier's
+// release / acquire order the consumers' shared-memory accesses around it.
+__device__ __noinline__ bool csync(PassShared &sm, const Job &j)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t ph = sm.cph[w];
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(&sm.csync);
+    bool ok = false;
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try(&sm.csync, ph)) {
+            ok = true;
+            break;
+        }
+        if (sm.abort)
+            break;
+        if (SV_SPIN_SLEEP_NS > 0 && i > 64)
+            __nanosleep(SV_SPIN_SLEEP_NS);
+    }
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    if (lane == 0) {
+        sm.cph[w] = ph ^ 1u;
+        if (!ok) {
+            latch(j.err, SV_ERR_TIMEOUT);
+            sm.abort = 1;
+        }
+    }
+    __syncwarp();
+    return ok;
+}
+
 // Lists the top ids of [lo, hi) in buffer b; false if they did not all fit
-// (the count is then larger than the list).  Every consumer thread calls it.
-__device__ __noinline__ bool seed_list(PassShared &sm, int b, uint64_t key, int lo, int hi)
+// (the count is then larger than the list).  *listed receives the number of
+// ids in the list, the same in every thread.  Every consumer thread calls
+// it.  After a barrier that did not complete the list is left empty.
+__device__ __noinline__ bool seed_list(PassShared &sm, const Job &j, int b, uint64_t key, int lo,
+                                       int hi, int *listed)
 {
     const int t = threadIdx.x;
+    *listed = 0;
     if (t == 0)
         sm.seed_n = 0;
-    named_sync(1, kConsumers);
+    if (!csync(sm, j)) {
+        if (t == 0)
+            sm.seed_cnt[b] = 0;
+        return true;
+    }
     const uint32_t bhi = (uint32_t)(hi - 1) >> 8;
     uint32_t beta = ((uint32_t)lo >> 8) + t;
     int pos = -1, i = 0;
@@ -1300,18 +1691,18 @@ __device__ __noinline__ bool seed_list(PassShared &sm, int b, uint64_t key, int 
                 sm.seed_ids[b][idx] = v;
         }
     }
-    named_sync(1, kConsumers);
-    const int n = sm.seed_n;
+    const bool ok = csync(sm, j);
+    const int n = ok ? sm.seed_n : 0;
+    *listed = min(n, kSeedCap);
     if (t == 0)
         sm.seed_cnt[b] = min(n, kSeedCap);
     return n <= kSeedCap;
 }
 
-// Starts the copies of the listed ids' logit words into buffer b.
+// Starts the copies of the n listed ids' logit words into buffer b.
 template <typename In>
-__device__ __forceinline__ void seed_copy(PassShared &sm, int b, const char *row)
+__device__ __forceinline__ void seed_copy(PassShared &sm, int b, const char *row, int n)
 {
-    const int n = min(sm.seed_n, kSeedCap);
     for (int e = threadIdx.x; e < n; e += kConsumers)
         cp_async4(&sm.seed_x[b][e], logit_word<In>(row, sm.seed_ids[b][e]));
     cp_async_commit();
@@ -1320,12 +1711,12 @@ __device__ __forceinline__ void seed_copy(PassShared &sm, int b, const char *row
 // Scores buffer b (its copies must have been started) and starts the unit's
 // threshold.
 template <typename In>
-__device__ __noinline__ GState seed_eval(PassShared &sm, int b, GState g, const RowMode &rm,
-                                         int tslot)
+__device__ __noinline__ GState seed_eval(PassShared &sm, const Job &j, int b, GState g,
+                                         const RowMode &rm, int tslot)
 {
     cp_async_wait_all();
-    named_sync(1, kConsumers);  // every thread's copies have landed
-    const int n = sm.seed_cnt[b];
+    const bool ok = csync(sm, j);  // every thread's copies have landed
+    const int n = ok ? min(max(sm.seed_cnt[b], 0), kSeedCap) : 0;
     for (int e = threadIdx.x; e < n; e += kConsumers) {
         const uint32_t v = sm.seed_ids[b][e];
         const float2 iv = logit_interval_m(logit_of_word<In>(sm.seed_x[b][e], v), rm.invT,
@@ -1337,8 +1728,8 @@ __device__ __noinline__ GState seed_eval(PassShared &sm, int b, GState g, const 
         }
     }
     atomicMax(&sm.thr[tslot], f2ord(g.thr));
-    named_sync(1, kConsumers);
-    raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
+    if (csync(sm, j))
+        raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
     return g;
 }
 
@@ -1346,8 +1737,8 @@ __device__ __noinline__ GState seed_eval(PassShared &sm, int b, GState g, const 
 // loading the logits directly (the fallback for units with more top ids than
 // a list holds).
 template <typename In>
-__device__ __noinline__ GState seed_rounds(PassShared &sm, int b, const char *row, int lo, int hi,
-                                           GState g, const RowMode &rm, int tslot)
+__device__ __noinline__ GState seed_rounds(PassShared &sm, const Job &j, int b, const char *row,
+                                           int lo, int hi, GState g, const RowMode &rm, int tslot)
 {
     using VT = VecTraits<In>;
     constexpr uint32_t kNone = 0xFFFFFFFFu;
@@ -1363,7 +1754,8 @@ __device__ __noinline__ GState seed_rounds(PassShared &sm, int b, const char *ro
             sm.seed_n = 0;
             sm.seed_more = 0;
         }
-        named_sync(1, kConsumers);
+        if (!csync(sm, j))
+            return g;
         for (;;) {
             if (pend != kNone) {
                 const int idx = atomicAdd(&sm.seed_n, 1);
@@ -1387,7 +1779,8 @@ __device__ __noinline__ GState seed_rounds(PassShared &sm, int b, const char *ro
         }
         if (more || pend != kNone)
             sm.seed_more = 1;
-        named_sync(1, kConsumers);
+        if (!csync(sm, j))
+            return g;
         const int n = min(sm.seed_n, kSeedCap);
         uint32_t id[kPer];
         float x[kPer];
@@ -1409,13 +1802,14 @@ __device__ __noinline__ GState seed_rounds(PassShared &sm, int b, const char *ro
                 }
             }
         const int again = sm.seed_more;
-        named_sync(1, kConsumers);  // the list is reused by the next round
+        if (!csync(sm, j))  // the list is reused by the next round
+            return g;
         if (!again)
             break;
     }
     atomicMax(&sm.thr[tslot], f2ord(g.thr));
-    named_sync(1, kConsumers);
-    raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
+    if (csync(sm, j))
+        raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
     return g;
 }
 
@@ -1439,23 +1833,24 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
     // and the one it prefetched for, so the buffer travels with the record.
     const bool pre = pf_next >= 0 && (pf_next >> 1) == uh.unit;
     const int sb = pre ? (pf_next & 1) : (pf_next >= 0 ? (pf_next & 1) ^ 1 : 0);
+    int listed = 0;
     if (MODE & M_GUMBEL) {
         if (pre) {
-            s.g = seed_eval<In>(sm, sb, s.g, rm, tslot);  // listed and copied a unit ago
-        } else if (seed_list(sm, sb, rm.key, m0.vbase * E, m0.vend * E)) {
-            seed_copy<In>(sm, sb, m0.row);
-            s.g = seed_eval<In>(sm, sb, s.g, rm, tslot);
+            s.g = seed_eval<In>(sm, j, sb, s.g, rm, tslot);  // listed and copied a unit ago
+        } else if (seed_list(sm, j, sb, rm.key, m0.vbase * E, m0.vend * E, &listed)) {
+            seed_copy<In>(sm, sb, m0.row, listed);
+            s.g = seed_eval<In>(sm, j, sb, s.g, rm, tslot);
         } else {
-            s.g = seed_rounds<In>(sm, sb, m0.row, m0.vbase * E, m0.vend * E, s.g, rm, tslot);
+            s.g = seed_rounds<In>(sm, j, sb, m0.row, m0.vbase * E, m0.vend * E, s.g, rm, tslot);
         }
     }
     if (m0.nrec >= 0) {
         // the next unit carries a Gumbel-max: list its top ids and start
         // their copies now, so that they land while this unit streams
         const int nb = sb ^ 1;
-        const bool fits = seed_list(sm, nb, m0.nkey, m0.nlo, m0.nhi);
+        const bool fits = seed_list(sm, j, nb, m0.nkey, m0.nlo, m0.nhi, &listed);
         if (fits)
-            seed_copy<In>(sm, nb, m0.nrow);
+            seed_copy<In>(sm, nb, m0.nrow, listed);
         pf_next = fits ? (m0.nrec << 1) | nb : -1;  // the same on every consumer thread
     } else {
         pf_next = -1;
@@ -1491,7 +1886,7 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
             latch(j.err, SV_ERR_TIMEOUT);
             return false;
         }
-        if (sm.meta[stage].unit != uh.unit)  // the producer aborted
+        if (sm.meta[stage].unit != uh.unit || sm.abort)  // the producer or a consumer aborted
             return false;
     }
     if ((MODE & M_GUMBEL) && s.gqn > 0) {
@@ -1520,6 +1915,15 @@ __device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsi
         if (m & M_GUMBEL)
             return unit_loop<In, M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
         return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+    } else if constexpr (KIND == K_ANYORDER) {
+        if (m & M_LSE)
+            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+    } else if constexpr (KIND == K_SPOT) {
+        if (m & M_GUMBEL)
+            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm,
+                                                           pf_next);
+        return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
     } else {
         switch (m) {
         case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
@@ -1623,6 +2027,11 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             mbar_init(&sm.plan_full[q], 1);
             mbar_init(&sm.plan_empty[q], 1);
         }
+        mbar_init(&sm.csync, kConsumerWarps);
+        for (int w = 0; w < kConsumerWarps; ++w)
+            sm.cph[w] = 0u;
+        sm.seed_cnt[0] = sm.seed_cnt[1] = 0;
+        sm.seed_n = 0;
         sm.abort = 0;
         sm.nunits = 0;
         sm.prod_done = 0;
@@ -1799,8 +2208,9 @@ cudaError_t pass_setup(int *blocks_per_sm)
     cudaError_t e = cudaSuccess;
     cudaError_t (*fns[])(int) = {
         set_smem<uint16_t, K_GREEDY>, set_smem<uint16_t, K_SAMPLE>, set_smem<uint16_t, K_TREE>,
-        set_smem<uint16_t, K_PACKED>, set_smem<float, K_GREEDY>,   set_smem<float, K_SAMPLE>,
-        set_smem<float, K_TREE>,      set_smem<float, K_PACKED>};
+        set_smem<uint16_t, K_PACKED>, set_smem<uint16_t, K_SPOT>,   set_smem<uint16_t, K_ANYORDER>,
+        set_smem<float, K_GREEDY>,    set_smem<float, K_SAMPLE>,    set_smem<float, K_TREE>,
+        set_smem<float, K_PACKED>,    set_smem<float, K_SPOT>,      set_smem<float, K_ANYORDER>};
     for (auto f : fns)
         if (e == cudaSuccess)
             e = f(smem);
@@ -1808,8 +2218,10 @@ cudaError_t pass_setup(int *blocks_per_sm)
     const void *ks[] = {
         (const void *)pass_kernel<uint16_t, K_GREEDY>, (const void *)pass_kernel<uint16_t, K_SAMPLE>,
         (const void *)pass_kernel<uint16_t, K_TREE>,   (const void *)pass_kernel<uint16_t, K_PACKED>,
+        (const void *)pass_kernel<uint16_t, K_SPOT>,   (const void *)pass_kernel<uint16_t, K_ANYORDER>,
         (const void *)pass_kernel<float, K_GREEDY>,    (const void *)pass_kernel<float, K_SAMPLE>,
-        (const void *)pass_kernel<float, K_TREE>,      (const void *)pass_kernel<float, K_PACKED>};
+        (const void *)pass_kernel<float, K_TREE>,      (const void *)pass_kernel<float, K_PACKED>,
+        (const void *)pass_kernel<float, K_SPOT>,      (const void *)pass_kernel<float, K_ANYORDER>};
     int best = 1 << 30;
     for (const void *k : ks) {
         int n = 0;
@@ -1831,8 +2243,126 @@ static cudaError_t launch_in(const Job &j, int grid, cudaStream_t s)
     case K_GREEDY: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_GREEDY>, j);
     case K_SAMPLE: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_SAMPLE>, j);
     case K_TREE: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_TREE>, j);
+    case K_SPOT: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_SPOT>, j);
+    case K_ANYORDER: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_ANYORDER>, j);
     default: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_PACKED>, j);
     }
+}
+
+// SPOT preparation, one thread per tree: the masked positions of every state
+// (the root's from root_mask; a node's state is its parent's with the
+// node's position filled) and the number of rows the tree streams.  A node
+// whose parent index is out of range, or whose position is not masked in its
+// parent's state, latches SV_ERR_DEVICE_BOUNDS and gets a full state.  A
+// tree with nothing masked anywhere has no row to stream, so its outputs
+// are written here: nothing accepted and nothing committed.
+__global__ void __launch_bounds__(128) spot_prep_kernel(const __grid_constant__ Job j)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= j.B)
+        return;
+    const int S = j.N + 1;
+    const uint64_t all = j.L >= 64 ? ~0ull : ((1ull << j.L) - 1ull);
+    uint64_t *mk = j.smask + (int64_t)b * S;
+    uint64_t m0 = __ldg(j.root_mask + b) & all;
+    mk[0] = m0;
+    unsigned cnt = (unsigned)__popcll(m0);
+    for (int n = 0; n < j.N; ++n) {
+        const int par = __ldg(j.parent + (int64_t)b * j.N + n);
+        const int pos = __ldg(j.node_pos + (int64_t)b * j.N + n);
+        uint64_t m = 0ull;
+        if (par < -1 || par >= n || pos < 0 || pos >= j.L ||
+            !((mk[par + 1] >> pos) & 1ull))
+            latch(j.err, SV_ERR_DEVICE_BOUNDS);
+        else
+            m = mk[par + 1] & ~(1ull << pos);
+        mk[n + 1] = m;
+        cnt += (unsigned)__popcll(m);
+    }
+    j.svalid[b] = cnt;
+    if (cnt == 0u) {
+        j.path_len[b] = 0;
+        j.commit_count[b] = 0;
+        j.commit_pos[b] = -1;
+        j.commit_tok[b] = -1;
+        if (j.flags) j.flags[b] = 0;
+        for (int k = 0; k < j.max_depth; ++k)
+            j.path_nodes[(int64_t)b * j.max_depth + k] = -1;
+        for (int n = 0; n < j.N && j.match; ++n)
+            j.match[(int64_t)b * j.N + n] = 0;
+        for (int st = 0; st < S; ++st) {
+            if (j.state_pos) j.state_pos[(int64_t)b * S + st] = -1;
+            if (j.state_tok) j.state_tok[(int64_t)b * S + st] = -1;
+        }
+    }
+}
+
+cudaError_t spot_prep_launch(const Job &j, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    pdl_config(cfg, at, dim3((j.B + 127) / 128), dim3(128), 0, s);
+    return cudaLaunchKernelEx(&cfg, spot_prep_kernel, j);
+}
+
+// Any-order preparation, one thread per sequence: checks that the first u
+// entries of the order are a permutation of the window indices, finds kappa
+// (the leading ranks with a draft token), the verify rows needed (min(kappa
+// + 1, u), which must not exceed the K verify rows given) and the rows to
+// stream.  Bad inputs latch SV_ERR_DEVICE_BOUNDS and stream nothing; a
+// sequence with nothing to stream gets its outputs here.
+__global__ void __launch_bounds__(128) anyorder_prep_kernel(const __grid_constant__ Job j)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= j.B)
+        return;
+    const int W = j.W;
+    const int uin = __ldg(j.lens + b);
+    bool bad = uin < 0 || uin > W;
+    const int u = bad ? 0 : uin;
+    unsigned seen = 0u;
+    int kappa = 0;
+    bool run = true;
+    for (int r = 0; r < u; ++r) {
+        const int oi = __ldg(j.order + (int64_t)b * W + r);
+        if (oi < 0 || oi >= u || ((seen >> oi) & 1u)) {
+            bad = true;
+            break;
+        }
+        seen |= 1u << oi;
+        run = run && __ldg(j.ids + (int64_t)b * W + oi) >= 0;
+        kappa += run ? 1 : 0;
+    }
+    const int nreq = min(kappa + 1, u);
+    bad = bad || nreq > j.K;
+    if (bad)
+        latch(j.err, SV_ERR_DEVICE_BOUNDS);
+    j.smask[b] = bad ? 0ull : (uint64_t)nreq;
+    j.svalid[b] = bad ? 0u : (unsigned)(nreq + u);
+    if (bad || u == 0) {
+        j.acc[b] = 0;
+        j.commit_len[b] = 0;
+        j.end_out[b] = __ldg(j.end_in + b);
+        for (int i = 0; i < W; ++i) {
+            j.commit_pos[(int64_t)b * W + i] = -1;
+            j.commit_tok[(int64_t)b * W + i] = -1;
+            j.next_draft[(int64_t)b * W + i] = -1;
+            j.next_order[(int64_t)b * W + i] = -1;
+            if (j.confidence) j.confidence[(int64_t)b * W + i] = __int_as_float(0x7FC00000);
+        }
+    }
+}
+
+cudaError_t anyorder_prep_launch(const Job &j, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    pdl_config(cfg, at, dim3((j.B + 127) / 128), dim3(128), 0, s);
+    return cudaLaunchKernelEx(&cfg, anyorder_prep_kernel, j);
 }
 
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s)

@@ -699,17 +699,10 @@ __device__ bool grid_sync(const Job &j)
             j.ctl[C_GBAR] = 0u;
             __threadfence();
             atomicAdd(j.ctl + C_GGEN, 1u);
-        } else {
-            uint32_t it = 0;
-            while (*gen == g) {
-                if (*ab || ++it > kSpinLimit) {
-                    latch(j.err, SV_ERR_TIMEOUT);
-                    atomicExch(j.ctl + C_ABORT, 1u);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(256);
-            }
+        } else if (!spin_until_change(gen, g, ab, kSpinLimit)) {
+            latch(j.err, SV_ERR_TIMEOUT);
+            atomicExch(j.ctl + C_ABORT, 1u);
+            ok = 0;
         }
         __threadfence();
     }
@@ -820,9 +813,18 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         RescueEntry re = j.rescue[e];
         const int b = re.b;
         const int n = clamp_len(j, b);
+        const bool cactus = j.kind == K_SAMPLE && j.amode == SV_LENIENT_CACTUS;
         if (re.kind == 1) {
             if (lane == 0) {
-                j.rescue[e].Lp = merge64(j, e, re.h, 0);
+                double Lp = merge64(j, e, re.h, 0);
+                if (cactus) {
+                    // the residual [c p - q]_+ is [p - q]_+ with Lp lowered by log c
+                    const int d = __ldg(j.ids + (int64_t)b * j.K + re.h);
+                    const double lp =
+                        (double)load_logit(j, slot_row(j, b, re.h), d) / (double)j.Tp - Lp;
+                    Lp -= cactus_log_scale64(lp, (double)j.lam);
+                }
+                j.rescue[e].Lp = Lp;
                 j.rescue[e].Lq = merge64(j, e, re.h, 1);
                 j.rescue[e].resid = 1;
                 j.rescue[e].flags = 0;
@@ -832,7 +834,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         const int64_t p0 = pos0_of(j, b);
         const int Ks = (j.kind == K_PACKED) ? j.K - 1 : j.K;
         bool acc = false, fl = false;
-        double Lp = 0, Lq = 0;
+        double Lp = 0, Lq = 0, lc = 0.0;
         if (lane < n) {
             Lp = merge64(j, e, lane, 0);
             Lq = merge64(j, e, lane, 1);
@@ -847,8 +849,10 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
                          ? (double)load_logit(j, slot_row(j, b, j.K + 1 + lane), d) / Tq - Lq
                          : 0.0;
             }
-            double alpha = alpha_of(j.kind == K_PACKED ? SV_LOSSLESS : j.amode, exp(lp - lq),
-                                    j.lam);
+            double alpha = alpha_exact(j.kind == K_PACKED ? SV_LOSSLESS : j.amode, lp, lq,
+                                       (double)j.lam);
+            if (cactus)
+                lc = cactus_log_scale64(lp, (double)j.lam);
             double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
             acc = u < alpha;
             fl = fabs(u - alpha) < kFlagEps;
@@ -860,6 +864,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         int nfl = __popc(__ballot_sync(0xFFFFFFFFu, fl) & reached);
         double Lph = __shfl_sync(0xFFFFFFFFu, Lp, h & 31);
         double Lqh = __shfl_sync(0xFFFFFFFFu, Lq, h & 31);
+        Lph -= __shfl_sync(0xFFFFFFFFu, lc, h & 31);  // Cactus: the residual's scale c
         if (h < n) {
             if (lane == 0) {
                 j.rescue[e].h = h;

@@ -212,11 +212,17 @@ __device__ __forceinline__ void seed_top_ids(const RCtx &c, uint32_t lo, uint32_
 }
 
 // Context of the residual draw of entry re.
+// The weights [c p - q]_+ are those of [p - q]_+ with Lp lowered by log c,
+// so the bracket of Delta = Lq - Lp widens by the bracket of log c.
 __device__ __forceinline__ void resid_ctx(const Job &j, const ResidEntry &re, RCtx &ctx)
 {
     const double D = re.Lq - re.Lp;
     const double eD = 1.001 * (re.epsp + re.epsq) + 1e-14 * (fabs(re.Lp) + fabs(re.Lq));
     fill_ctx(j, ctx, re.prow, re.qrow, D, eD);
+    ctx.dlo += re.lclo;
+    ctx.dhi += re.lchi;
+    ctx.dlo32 = __double2float_rd(ctx.dlo);
+    ctx.dhi32 = __double2float_ru(ctx.dhi);
     ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
 }
 

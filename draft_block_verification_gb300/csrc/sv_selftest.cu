@@ -59,4 +59,36 @@ cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s
     return e;
 }
 
+// Waits that run out: warp 0 waits on an mbarrier that nothing arrives at,
+// warp 1 waits for a global word that nothing changes (the grid-barrier
+// form), each with the bounded-wait primitives the kernels use and at most
+// `limit` tries.  Each latches SV_ERR_TIMEOUT in *err when its wait expires
+// and returns; nothing else is touched, so the context stays usable.
+__global__ void wait_selftest_kernel(int *err, const unsigned *word, uint32_t limit)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int w = threadIdx.x >> 5;
+    bool ok = true;
+    if (w == 0)
+        ok = mbar_wait_n(&bar, 0, limit);  // phase 0 never completes
+    else if (w == 1 && threadIdx.x == 32)
+        ok = spin_until_change(word, *word, nullptr, limit);
+    if (!ok)
+        latch(err, SV_ERR_TIMEOUT);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_arrive(&bar);  // complete the phase before the CTA exits
+}
+
+cudaError_t wait_selftest_run(int *err, const unsigned *word, uint32_t limit, cudaStream_t s)
+{
+    wait_selftest_kernel<<<1, 64, 0, s>>>(err, word, limit);
+    return cudaGetLastError();
+}
+
 }  // namespace sv

@@ -30,6 +30,7 @@
 #include "sv_job.cuh"
 
 namespace sv {
+sv_status fault_injected(const char *call);
 size_t pass_smem_bytes();
 cudaError_t pass_setup(int *blocks_per_sm);
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s);
@@ -127,6 +128,7 @@ extern "C" sv_status sv_verify_greedy_static(const void *target, sv_dtype dtype,
         return SV_ERR_INVALID_ARG;
     const long long rows = (long long)B * (K + 1);
     if (B > kStaticMaxSeqs || rows > kStaticMaxRows) return SV_ERR_UNSUPPORTED;
+    if (sv_status fi = fault_injected("sv_verify_greedy_static")) return fi;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices)
         return SV_ERR_UNSUPPORTED;

@@ -44,6 +44,14 @@
  *   Gumbel-max winner less than 1e-9 ahead of the runner-up) is counted in
  *   the optional `flags` output.
  * - K (draft tokens), W (packed width) <= 32; N (tree nodes) <= 64.
+ * - Fault injection for tests of a caller's failure handling: the
+ *   environment variable SV_FAULT_INJECT="call:code[,call:code...]" makes
+ *   each listed entry point (sv_create, sv_verify_greedy,
+ *   sv_verify_greedy_static, sv_verify_sample, sv_verify_tree,
+ *   sv_verify_spot, sv_packed_step, sv_packed_anyorder_step) return the
+ *   status `code` (1..6) at its launch point,
+ *   after its argument checks and before anything is enqueued.  It is read
+ *   at every call; unset, nothing is injected.
  */
 #ifndef SV_H
 #define SV_H
@@ -73,9 +81,17 @@ typedef enum {
     SV_LENIENT_RATIO = 1,  /* accept w.p. min{1, lam p(d)/q(d)}, lam >= 1;
                               residual [p-q]_+ (the "predefined ratio" lenience
                               named in [TwoTrade] §1) */
-    SV_LENIENT_LINEAR = 2  /* target ptilde = (1-lam) p + lam q, lam in [0,1]:
+    SV_LENIENT_LINEAR = 2, /* target ptilde = (1-lam) p + lam q, lam in [0,1]:
                               accept w.p. min{1, ptilde(d)/q(d)}, residual
                               [ptilde-q]_+ ([TwoTrade] eq. 5, Alg. 1) */
+    SV_LENIENT_CACTUS = 3  /* modified Cactus, KL budget delta = lam >= 0:
+                              gamma* = the largest gamma with
+                              gamma log(gamma/p(d)) + (1-gamma)
+                              log((1-gamma)/(1-p(d))) <= delta (solved by
+                              Newton's method); accept w.p.
+                              min{1, gamma* / q(d)}; residual [c p - q]_+ with
+                              c = (1-gamma*)/(1-p(d)) ([TwoTrade] App. E,
+                              eq. 17); delta = 0 is the lossless rule */
 } sv_accept_mode;
 
 typedef struct sv_handle sv_handle;
@@ -158,7 +174,7 @@ sv_status sv_verify_greedy_static(const void *target, sv_dtype dtype, int64_t ro
  *   weights with key (seed, SAMPLE, b, pos_base + h, 0); bonus when all n are
  *   accepted: Gumbel-max of x_n / T_p with key (seed, SAMPLE, b, pos_base + n, 0).
  *   lam: lambda >= 1 for SV_LENIENT_RATIO, mu in [0,1] for SV_LENIENT_LINEAR,
- *   ignored for SV_LOSSLESS.
+ *   the KL budget delta >= 0 for SV_LENIENT_CACTUS, ignored for SV_LOSSLESS.
  * Outputs (NULL to skip the optional ones):
  *   accept_len [B], next_token [B];
  *   p_at_draft, q_at_draft [B, K]: p_i(d_i), q_i(d_i);
@@ -201,6 +217,52 @@ sv_status sv_verify_tree(sv_handle *h, const void *node_logits, sv_dtype dtype, 
                          void *stream);
 
 /* ---------------------------------------------------------------------------
+ * SPOT verification with the target's own position selection ([SPOT] App.
+ * A.1 "Position selection", "Greedy transition", "Shared Gumbel
+ * representation", "State-equality verifier"; §4.3 eq. 4).
+ *   A block state has L <= 32 positions, each holding a token or masked.
+ *   root_mask [B] (uint64, device): bit s set = position s is masked in the
+ *     root state (bits at or above L are ignored).
+ *   parent [B, N] in [-1, n-1] (-1 = the root), node_pos [B, N], node_tok
+ *     [B, N] (N <= 64; may be NULL when N = 0): node n commits token
+ *     node_tok at position node_pos, which must be masked in its parent's
+ *     state; the node's own state has it filled.  State 0 is the root,
+ *     state 1 + n the state of node n.
+ *   state_logits [B, 1+N, L, V]: row (b, state, s) is the target's
+ *     conditional at that state for position s.  Only rows of masked
+ *     positions are read.
+ *   The target's transition Phi(state): s* = the masked position with the
+ *     largest max_v softmax(row)_v (the model's own probabilities, at
+ *     temperature 1; lowest position on exact ties), then the token
+ *     argmax_v row_{s*} (T = 0) or argmax_v row_{s*}/T + G(key(seed, TREE,
+ *     b, pos_base + s*, 0), v) (T > 0: the noise row of an absolute position
+ *     is shared by every state).
+ *   A child is accepted when its commitment equals Phi of its parent's
+ *   state; the walk from the root follows accepted children (the lowest
+ *   index among equal children) and then commits Phi of the state reached.
+ * Outputs: path_len [B] (accepted nodes), path_nodes [B, max_depth] (-1
+ *   padded), commit_count [B] (path_len + 1, or path_len when the state
+ *   reached has nothing masked), commit_pos / commit_tok [B] (Phi of the
+ *   state reached; -1 when nothing is masked), match [B, N] (optional,
+ *   uint8: the node equals Phi of its parent's state), state_pos /
+ *   state_tok [B, 1+N] (optional: Phi of every state, -1 where nothing is
+ *   masked), flags [B] (optional: decisions within 1e-9 -- a confidence
+ *   runner-up less than 1e-9 behind s*, or a Gumbel-max top-two gap below
+ *   1e-9 -- over all states).
+ * Errors: SV_ERR_INVALID_ARG (shapes, L > 32, N > 64, T < 0); latched
+ *   SV_ERR_DEVICE_BOUNDS for a parent out of range or a position that is
+ *   not masked in the parent's state.
+ * ------------------------------------------------------------------------- */
+sv_status sv_verify_spot(sv_handle *h, const void *state_logits, sv_dtype dtype,
+                         int64_t row_stride, int B, int N, int L, int V, const int32_t *parent,
+                         const int32_t *node_pos, const int32_t *node_tok,
+                         const uint64_t *root_mask, float T, uint64_t seed,
+                         const int64_t *pos_base, int32_t *path_len, int32_t *path_nodes,
+                         int max_depth, int32_t *commit_count, int32_t *commit_pos,
+                         int32_t *commit_tok, uint8_t *match, int32_t *state_pos,
+                         int32_t *state_tok, int32_t *flags, void *stream);
+
+/* ---------------------------------------------------------------------------
  * One Packed-SS iteration: verify the previous draft and propose the next
  * block from the same model call ([PackedSS] §3.1 Alg. 1, §3.2 Alg. 2).
  *   logits [B, K+W, V]: rows 0..K-1 are verify rows (row i predicts absolute
@@ -235,6 +297,43 @@ sv_status sv_packed_step(sv_handle *h, const void *logits, sv_dtype dtype, int64
                          void *stream);
 
 /* ---------------------------------------------------------------------------
+ * One iteration of Packed-SS with any-order greedy verification ([PackedSS]
+ * App. C "Procedure", Alg. 3 lines 6-15, eq. 8; confidence scores of App.
+ * E.6 "Confidence scores").
+ *   u [B] in [0, W]: unresolved positions of the active window;
+ *   win_pos [B, W]: those output positions, ascending (first u entries);
+ *   order [B, W]: pi_t, the window index checked at each rank (its first u
+ *     entries a permutation of 0..u-1);
+ *   draft [B, W]: the draft token at each window position, -1 if none;
+ *   end_pos [B]: E, the last output position to generate.
+ *   kappa = the number of leading ranks whose position has a draft token.
+ *   logits [B, Kv + W, V]: verify row r (r < min(kappa + 1, u), which must
+ *     be <= Kv) is the verifier's prediction at rank r given the draft tokens
+ *     of the earlier ranks; proposal row Kv + i (i < u) is the drafter's row
+ *     at win_pos[i].  Other rows are not read.
+ *   v_r = argmax of verify row r (lowest id on ties); h = the leading ranks
+ *   r < kappa whose draft equals v_r; A = min(h + 1, u); the pairs
+ *   (win_pos[order[r]], v_r), r < A, are accepted; an accepted eos_id at
+ *   position p lowers E to min(E, p) and pairs beyond E are dropped.
+ * Outputs: accept_len [B] (h), commit_len [B] (pairs kept), commit_pos /
+ *   commit_tok [B, W] (rank order, -1 padded), end_out [B] (E),
+ *   next_draft [B, W] (argmax of proposal row i at window positions that
+ *   stay unresolved and <= E, else -1), score [B, W] (optional: the
+ *   probability at temperature 1 of each proposal row's argmax, NaN beyond
+ *   u), next_order [B, W] (the window indices with a next draft, by
+ *   decreasing score, ties by position; -1 padded).
+ * Errors: SV_ERR_INVALID_ARG; latched SV_ERR_DEVICE_BOUNDS for u outside
+ *   [0, W], an order that is not a permutation, or min(kappa + 1, u) > Kv.
+ * ------------------------------------------------------------------------- */
+sv_status sv_packed_anyorder_step(sv_handle *h, const void *logits, sv_dtype dtype,
+                                  int64_t row_stride, int B, int Kv, int W, int V,
+                                  const int32_t *u, const int32_t *win_pos, const int32_t *order,
+                                  const int32_t *draft, const int32_t *end_pos, int32_t eos_id,
+                                  int32_t *accept_len, int32_t *commit_len, int32_t *commit_pos,
+                                  int32_t *commit_tok, int32_t *end_out, int32_t *next_draft,
+                                  float *score, int32_t *next_order, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Options (testing and measurement).
  *   SV_OPT_FORCE_RESCUE (value 0/1): decide every sampled sequence on the
  *     fp64 path, as if every fast decision fell inside its error bound.
@@ -254,6 +353,17 @@ sv_status sv_set_option(sv_handle *h, sv_option opt, int64_t value);
  * Every ratio must stay below 1 for the error bounds the kernels use.
  * ------------------------------------------------------------------------- */
 sv_status sv_selftest(sv_handle *h, uint64_t seed, int64_t n, double *ratios, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Self-test of the bounded waits (enqueued on `stream`, asynchronous).  One
+ * small kernel waits, with at most `limit` tries each (0 <= limit <= 2^24,
+ * the kernels' own limit), on an mbarrier that nothing arrives at and on a
+ * device word that nothing changes -- the two wait forms every kernel of the
+ * library uses.  Both waits expire, the kernel latches SV_ERR_TIMEOUT in the
+ * handle and returns, so the next sv_sync_status returns SV_ERR_TIMEOUT and
+ * the handle stays usable.  Errors: SV_ERR_INVALID_ARG, SV_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+sv_status sv_wait_selftest(sv_handle *h, int64_t limit, void *stream);
 
 #ifdef __cplusplus
 }

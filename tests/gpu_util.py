@@ -75,3 +75,42 @@ def craft_tree_tokens(node_logits_np, pos, T, seed, rng, p=0.8, pos_base=None):
                 k = oracle.key(seed, oracle.ST_TREE, b, pb + int(pos[b, n]), 0)
                 tok[b, n] = oracle.gumbel_argmax(x / Tf, k)[0]
     return tok
+
+
+def craft_spot_tree(rows_np, root_mask, N, T, seed, rng, p=0.7, pos_base=None,
+                    max_children=4):
+    """A SPOT tree for given state rows [B, 1+N, L, V]: node n takes a uniform
+    parent among the states with a masked position left and fewer than
+    max_children children; with probability p it commits the oracle's own
+    transition Phi of that parent state (so that paths are deep), else a
+    uniform masked position and a uniform token.  Returns (parent, node_pos,
+    node_tok) as int32 arrays [B, N]."""
+    B, S, L, V = rows_np.shape
+    parent = np.full((B, N), -1, np.int32)
+    pos = np.zeros((B, N), np.int32)
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        masks = [int(root_mask[b])]
+        kids = [0] * (N + 1)
+        pb = 0 if pos_base is None else int(pos_base[b])
+        for n in range(N):
+            cand = [a for a in range(n + 1) if masks[a] and kids[a] < max_children]
+            a = cand[rng.integers(len(cand))]
+            if rng.random() < p:
+                r = oracle.verify_spot(rows_np[b:b + 1, a:a + 1], np.zeros((1, 0)),
+                                       np.zeros((1, 0)), np.zeros((1, 0)),
+                                       np.array([masks[a]], np.uint64), T=T, seed=seed,
+                                       pos_base=np.array([pb]))
+                s, v = int(r["commit_pos"][0]), int(r["commit_tok"][0])
+                # the row of state a at position s is row (b, a, s): the call above
+                # saw it as sequence 0, so its noise key used sequence 0, not b
+                if T > 0:
+                    k = oracle.key(seed, oracle.ST_TREE, b, pb + s, 0)
+                    v = oracle.gumbel_argmax(bits_to_f64(rows_np[b, a, s]) / oracle.f32(T), k)[0]
+            else:
+                free = [x for x in range(L) if (masks[a] >> x) & 1]
+                s, v = free[rng.integers(len(free))], int(rng.integers(V))
+            parent[b, n], pos[b, n], tok[b, n] = a - 1, s, v
+            masks.append(masks[a] & ~(1 << s))
+            kids[a] += 1
+    return parent, pos, tok

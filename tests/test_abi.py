@@ -69,3 +69,24 @@ def test_static_greedy_rejects_bad_arguments_on_the_host(lib):
     rc = lib.sv_verify_greedy_static(vp(16), 1, C.c_int64(8), -1, 1, 8, vp(16), vp(0), vp(16),
                                      vp(16), vp(16), vp(0))
     assert rc == 1
+
+
+def test_fault_injection_hook_answers_without_a_gpu(lib, monkeypatch):
+    """SV_FAULT_INJECT makes the listed call return the given status before it
+    touches the GPU: sv_create reports an injected SV_ERR_OOM (3) instead of
+    whatever the device would have answered; malformed or unlisted entries
+    inject nothing."""
+    vp = C.c_void_p
+    lib.sv_create.restype = C.c_int
+    h = vp(0)
+    monkeypatch.setenv("SV_FAULT_INJECT", "sv_verify_tree:2,sv_create:3")
+    assert lib.sv_create(C.byref(h)) == 3 and not h.value
+    monkeypatch.setenv("SV_FAULT_INJECT", "sv_create:5")
+    assert lib.sv_create(C.byref(h)) == 5
+    # a NULL out-pointer is still an argument error, checked first
+    assert lib.sv_create(vp(0)) == 1
+    monkeypatch.setenv("SV_FAULT_INJECT", "sv_create:9,sv_create,sv_creat:3,sv_create:2x")
+    rc = lib.sv_create(C.byref(h))
+    assert rc not in (2, 3, 9)  # nothing injected: the device's own answer
+    if rc == 0:
+        lib.sv_destroy(h)

@@ -8,8 +8,8 @@ import torch
 
 import datagen
 import oracle
-from gpu_util import (DEV, RTOL, assert_float_close, compare_sample, cpu, craft_tree_tokens,
-                      np_logits)
+from gpu_util import (DEV, RTOL, assert_float_close, compare_sample, cpu, craft_spot_tree,
+                      craft_tree_tokens, np_logits)
 
 pytestmark = pytest.mark.gpu
 
@@ -73,6 +73,11 @@ SAMPLE_CASES = [
     ("f32", 4, 3, 2048, 2, 0.875, 1.3, 0.9, 1.0, False),
     ("bf16", 3, 32, 2056, 0, 1.0, 1.0, 1.0, 0.5, True),
     ("bf16", 4, 0, 1024, 0, 1.0, 1.0, 1.0, 0.5, False),
+    # modified Cactus: KL budget delta = lam
+    ("bf16", 6, 7, 12288, 3, 0.05, 1.0, 1.0, 1.0, False),
+    ("f32", 5, 4, 4100, 3, 0.5, 0.7, 0.7, 1.0, True),
+    ("bf16", 4, 5, 8200, 3, 3.0, 1.0, 1.0, 0.5, False),
+    ("bf16", 4, 5, 8200, 3, 0.0, 1.0, 1.0, 0.5, True),
 ]
 
 
@@ -91,8 +96,9 @@ def test_sample_parity(dbv, dtype, B, K, V, mode, lam, Tp, Tq, sigma, ragged):
     dbv.default_handle().sync_status()
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_sample_fp64_path(dbv, dtype):
+@pytest.mark.parametrize("dtype,mode,lam", [("bf16", 0, 1.0), ("f32", 0, 1.0), ("bf16", 3, 0.2),
+                                            ("f32", 3, 1.5)])
+def test_sample_fp64_path(dbv, dtype, mode, lam):
     """Force every sequence through the fp64 path; it must agree too."""
     si = datagen.sample_inputs(10, 6, 4104, dtype=dtype, seed=5, sigma=1.0, ragged=True)
     h = dbv.Handle()
@@ -100,14 +106,25 @@ def test_sample_fp64_path(dbv, dtype):
         h.set_option(dbv.SV_OPT_FORCE_RESCUE, 1)
         before = h.rescue_count()
         out = dbv.sv_verify_sample(_g(si.target), _g(si.draft), _g(si.draft_ids),
-                                   _g(si.draft_len), seed=3, want_tv=True, handle=h)
+                                   _g(si.draft_len), mode=mode, lam=lam, seed=3, want_tv=True,
+                                   handle=h)
         h.sync_status()
         assert h.rescue_count() - before == 10
     finally:
         h.close()
     ref = oracle.verify_sample(np_logits(si.target), np_logits(si.draft), si.draft_ids.numpy(),
-                               si.draft_len.numpy(), seed=3)
+                               si.draft_len.numpy(), mode=mode, lam=lam, seed=3)
     compare_sample(out, ref, dtype)
+
+
+def test_sample_cactus_zero_budget_is_lossless(dbv):
+    """The modified Cactus rule with delta = 0 gives the lossless results."""
+    si = datagen.sample_inputs(12, 8, 8200, dtype="bf16", seed=44, sigma=1.0, ragged=True)
+    args = (_g(si.target), _g(si.draft), _g(si.draft_ids), _g(si.draft_len))
+    a = dbv.sv_verify_sample(*args, mode=3, lam=0.0, seed=6, want_tv=True)
+    b = dbv.sv_verify_sample(*args, mode=0, seed=6, want_tv=True)
+    for k in a:
+        assert torch.equal(a[k].nan_to_num(), b[k].nan_to_num()), k
 
 
 def test_sample_error_model(dbv):
@@ -155,7 +172,8 @@ def test_sample_full_size_lossless(dbv):
     assert n >= c["B"] - 1
 
 
-@pytest.mark.parametrize("sigma,T,mode,lam", [(1.0, 0.7, 1, 4.0), (0.25, 1.0, 2, 0.75)])
+@pytest.mark.parametrize("sigma,T,mode,lam", [(1.0, 0.7, 1, 4.0), (0.25, 1.0, 2, 0.75),
+                                            (1.0, 1.0, 3, 0.1)])
 def test_sample_full_size_lenient(dbv, sigma, T, mode, lam):
     """Two points of the lenient sweep at full size (B = 128, K = 16, V = 151936)."""
     c = datagen.CONFIGS["lenient_sweep"]
@@ -217,6 +235,200 @@ def test_tree_full_size(dbv, T):
     for k in ("path_len", "path_nodes", "match", "commit_count"):
         assert np.array_equal(cpu(out[k])[keep], ref[k][keep]), k
     assert ref["path_len"][:8].max() >= 2 and ref["match"][:8].mean() > 0.5
+
+
+# ------------------------------------------------------------------ SPOT
+
+SPOT_KEYS = ("path_len", "path_nodes", "commit_count", "commit_pos", "commit_tok", "match",
+             "state_pos", "state_tok")
+
+
+def _spot_both(dbv, rows, parent, pos, tok, root_mask, T, seed, pos_base, md):
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    out = dbv.sv_verify_spot(rows.to(DEV), g(parent), g(pos), g(tok),
+                             g(root_mask.astype(np.int64)), T=T, seed=seed, pos_base=g(pos_base),
+                             max_depth=md)
+    ref = oracle.verify_spot(np_logits(rows), parent, pos, tok, root_mask.astype(np.uint64),
+                             T=T, seed=seed, pos_base=pos_base, max_depth=md)
+    return out, ref
+
+
+def _compare_spot(out, ref):
+    assert np.array_equal(cpu(out["flags"]), ref["flags"])
+    keep = ref["flags"] == 0
+    for k in SPOT_KEYS:
+        assert np.array_equal(cpu(out[k])[keep], ref[k][keep]), k
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0, 0.7])
+@pytest.mark.parametrize("dtype,B,N,L,V,masked", [("bf16", 4, 10, 8, 2056, None),
+                                                  ("f32", 3, 20, 16, 4100, 11),
+                                                  ("bf16", 2, 0, 5, 1024, None),
+                                                  ("bf16", 2, 64, 32, 1032, None)])
+def test_spot_parity(dbv, T, dtype, B, N, L, V, masked):
+    g = torch.Generator().manual_seed(N * 7 + L)
+    rows = (torch.randn((B, N + 1, L, V), generator=g) * 2).to(
+        torch.bfloat16 if dtype == "bf16" else torch.float32)
+    rng = np.random.default_rng(N + L)
+    root = np.zeros(B, np.uint64)
+    for b in range(B):
+        for x in rng.choice(L, size=L if masked is None else masked, replace=False):
+            root[b] |= np.uint64(1 << int(x))
+    pos_base = np.arange(B, dtype=np.int64) * 64 + 9
+    parent, pos, tok = craft_spot_tree(np_logits(rows), root, N, T, 17, rng, pos_base=pos_base)
+    md = max(N, 1)
+    out, ref = _spot_both(dbv, rows, parent, pos, tok, root, T, 17, pos_base, md)
+    _compare_spot(out, ref)
+    if N >= 10:
+        assert ref["path_len"].max() >= 2
+
+
+def test_spot_confidence_ties_and_unmasked_rows(dbv):
+    """Equal rows at two masked positions: the lower position wins, unflagged;
+    a huge peak at an unmasked position is never read."""
+    L, V = 6, 1024
+    rows = torch.randn((1, 1, L, V)) * 2
+    rows[0, 0, 4] = rows[0, 0, 1]
+    rows[0, 0, 1, 3] = 12.0
+    rows[0, 0, 4, 3] = 12.0
+    rows[0, 0, 2, 5] = 1000.0  # unmasked below
+    root = np.array([0b110011], np.uint64)
+    e = np.zeros((1, 0), np.int32)
+    out, ref = _spot_both(dbv, rows, e, e, e, root, 0.0, 1, np.zeros(1, np.int64), 1)
+    _compare_spot(out, ref)
+    assert int(cpu(out["commit_pos"])[0]) == 1 and int(cpu(out["flags"])[0]) == 0
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_spot_full_size(dbv, T):
+    """The SPOT workload at full size: 32 trees of 8 drafted states over a
+    32-position block, V = 151936 bf16 (the first 8 trees follow the target's
+    own transitions with probability 0.7, so that paths are deep)."""
+    c = datagen.CONFIGS["spot"]
+    si = datagen.spot_inputs(c["B"], c["N"], c["L"], c["V"], dtype="bf16", seed=c["seed"],
+                             device=DEV)
+    rows_np = np_logits(si.state_logits)
+    root = cpu(si.root_mask).astype(np.uint64)
+    parent, pos, tok = cpu(si.parent), cpu(si.node_pos), cpu(si.node_tok)
+    S = 8
+    p8, q8, t8 = craft_spot_tree(rows_np[:S], root[:S], c["N"], T, c["seed"],
+                                 np.random.default_rng(3))
+    parent, pos, tok = parent.copy(), pos.copy(), tok.copy()
+    parent[:S], pos[:S], tok[:S] = p8, q8, t8
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    out = dbv.sv_verify_spot(si.state_logits, g(parent), g(pos), g(tok), si.root_mask, T=T,
+                             seed=c["seed"], max_depth=c["N"])
+    ref = oracle.verify_spot(rows_np, parent, pos, tok, root, T=T, seed=c["seed"],
+                             max_depth=c["N"])
+    _compare_spot(out, ref)
+    assert ref["path_len"][:S].max() >= 2
+
+
+def test_spot_position_not_masked_is_latched(dbv):
+    rows = torch.randn((2, 3, 4, 1024), device=DEV)
+    par = torch.tensor([[-1, 0], [-1, 0]], dtype=torch.int32, device=DEV)
+    pos = torch.tensor([[1, 1], [1, 2]], dtype=torch.int32, device=DEV)  # tree 0: 1 twice
+    tok = torch.zeros((2, 2), dtype=torch.int32, device=DEV)
+    root = torch.full((2,), 0b1111, dtype=torch.int64, device=DEV)
+    h = dbv.Handle()
+    try:
+        dbv.sv_verify_spot(rows, par, pos, tok, root, handle=h)
+        with pytest.raises(dbv.SVError) as e:
+            h.sync_status()
+        assert e.value.status == dbv.SV_ERR_DEVICE_BOUNDS
+        pos[0, 1] = 3
+        out = dbv.sv_verify_spot(rows, par, pos, tok, root, handle=h)
+        h.sync_status()
+        ref = oracle.verify_spot(np_logits(rows), cpu(par), cpu(pos), cpu(tok),
+                                 cpu(root).astype(np.uint64))
+        _compare_spot(out, ref)
+    finally:
+        h.close()
+
+
+# ------------------------------------------------------------------ any-order Packed-SS
+
+AO_KEYS = ("accept_len", "commit_len", "commit_pos", "commit_tok", "end_pos", "next_draft",
+           "next_order")
+
+
+def _anyorder_both(dbv, ai, Kv, W, eos=-1, end=None):
+    end = ai.end_pos if end is None else end
+    out = dbv.sv_packed_anyorder_step(ai.logits.to(DEV), Kv, W, ai.u.to(DEV), ai.win_pos.to(DEV),
+                                      ai.order.to(DEV), ai.draft.to(DEV), end.to(DEV), eos_id=eos)
+    ref = oracle.packed_anyorder_step(np_logits(ai.logits), Kv, W, cpu(ai.u), cpu(ai.win_pos),
+                                      cpu(ai.order), cpu(ai.draft), cpu(end), eos_id=eos)
+    return out, ref
+
+
+def _compare_anyorder(out, ref, dtype):
+    for k in AO_KEYS:
+        assert np.array_equal(cpu(out[k]), ref[k]), k
+    assert_float_close(cpu(out["score"]), ref["score"], RTOL[dtype], 0.0, "score")
+
+
+@pytest.mark.parametrize("dtype,B,Kv,W,V,ragged,p_draft", [
+    ("bf16", 6, 8, 8, 4104, True, 0.9), ("f32", 4, 5, 5, 2048, False, 1.0),
+    ("bf16", 3, 32, 32, 1032, True, 0.95), ("bf16", 5, 1, 1, 1024, False, 0.5),
+    ("bf16", 4, 6, 6, 2056, True, 0.0)])
+def test_anyorder_parity(dbv, dtype, B, Kv, W, V, ragged, p_draft):
+    ai = datagen.anyorder_inputs(B, Kv, W, V, dtype=dtype, seed=B * 10 + W, p_draft=p_draft,
+                                 ragged=ragged)
+    out, ref = _anyorder_both(dbv, ai, Kv, W)
+    _compare_anyorder(out, ref, dtype)
+    # an accepted EOS cuts the end: the first accepted token becomes EOS
+    eos = int(ref["commit_tok"][0, 0])
+    end = torch.full((B,), 3 * W, dtype=torch.int32)
+    out, ref = _anyorder_both(dbv, ai, Kv, W, eos=eos, end=end)
+    _compare_anyorder(out, ref, dtype)
+    assert ref["end_pos"][0] <= ref["commit_pos"][0, 0]
+
+
+def test_anyorder_ties_in_scores(dbv):
+    """Equal proposal rows give equal scores: the retained positions keep
+    their textual order among themselves."""
+    ai = datagen.anyorder_inputs(3, 4, 4, 1024, dtype="bf16", seed=9, p_draft=0.0)
+    ai.logits[:, 4:] = ai.logits[:, 4:5]
+    out, ref = _anyorder_both(dbv, ai, 4, 4)
+    _compare_anyorder(out, ref, "bf16")
+    assert cpu(out["next_order"])[0, :3].tolist() == [1, 2, 3]
+
+
+@pytest.mark.parametrize("which", ["not_a_permutation", "too_few_rows"])
+def test_anyorder_bad_inputs_are_latched(dbv, which):
+    ai = datagen.anyorder_inputs(2, 4, 4, 1024, dtype="bf16", seed=3, p_draft=1.0)
+    Kv = 4
+    if which == "not_a_permutation":
+        ai.order[1, 1] = ai.order[1, 0]
+    else:
+        Kv = 2  # all four positions have drafts: min(kappa + 1, u) = 4 verify rows
+        ai.logits = torch.cat([ai.logits[:, :2], ai.logits[:, 4:]], 1)
+    h = dbv.Handle()
+    try:
+        dbv.sv_packed_anyorder_step(ai.logits.to(DEV), Kv, 4, ai.u.to(DEV), ai.win_pos.to(DEV),
+                                    ai.order.to(DEV), ai.draft.to(DEV), ai.end_pos.to(DEV),
+                                    handle=h)
+        with pytest.raises(dbv.SVError) as e:
+            h.sync_status()
+        assert e.value.status == dbv.SV_ERR_DEVICE_BOUNDS
+    finally:
+        h.close()
+
+
+def test_anyorder_full_size(dbv):
+    """The any-order workload at full size (B = 256, 32 + 32 rows, V = 151936),
+    against the oracle on the first 24 sequences."""
+    c = datagen.CONFIGS["anyorder"]
+    ai = datagen.anyorder_inputs(c["B"], c["K"], c["W"], c["V"], dtype="bf16", seed=c["seed"],
+                                 device=DEV)
+    out = dbv.sv_packed_anyorder_step(ai.logits, c["K"], c["W"], ai.u, ai.win_pos, ai.order,
+                                      ai.draft, ai.end_pos)
+    S = 24
+    ref = oracle.packed_anyorder_step(np_logits(ai.logits[:S]), c["K"], c["W"], cpu(ai.u[:S]),
+                                      cpu(ai.win_pos[:S]), cpu(ai.order[:S]), cpu(ai.draft[:S]),
+                                      cpu(ai.end_pos[:S]))
+    _compare_anyorder({k: v[:S] for k, v in out.items()}, ref, "bf16")
+    assert ref["accept_len"].max() >= 2
 
 
 # ------------------------------------------------------------------ Packed-SS
