@@ -72,7 +72,7 @@ def lib():
                                      u64, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.sv_packed_anyorder_step.restype = i32
         L.sv_packed_anyorder_step.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp,
-                                              vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                              vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         L.sv_packed_step.restype = i32
         L.sv_packed_step.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                      f32, u64, u64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -352,12 +352,12 @@ def sv_packed_anyorder_step(logits, Kv, W, u, win_pos, order, draft, end_pos, *,
     i = lambda *shape: torch.empty(shape, dtype=torch.int32, device=dev)
     out = {"accept_len": i(B), "commit_len": i(B), "commit_pos": i(B, W), "commit_tok": i(B, W),
            "end_pos": i(B), "next_draft": i(B, W),
-           "score": torch.empty((B, W), dtype=torch.float32, device=dev), "next_order": i(B, W)}
+           "score": torch.empty((B, W), dtype=torch.float32, device=dev)}
     _check(lib().sv_packed_anyorder_step(
         h.ptr, _p(logits), code, rs, B, Kv, W, V, _p(uu), _p(wp), _p(od), _p(dr), _p(end),
         int(eos_id), _p(out["accept_len"]), _p(out["commit_len"]), _p(out["commit_pos"]),
         _p(out["commit_tok"]), _p(out["end_pos"]), _p(out["next_draft"]), _p(out["score"]),
-        _p(out["next_order"]), _stream(stream, dev)), "sv_packed_anyorder_step")
+        _stream(stream, dev)), "sv_packed_anyorder_step")
     return out
 
 

@@ -18,6 +18,7 @@ cudaError_t pass_setup(int *blocks_per_sm);
 cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s);
 cudaError_t spot_prep_launch(const Job &j, cudaStream_t s);
 cudaError_t anyorder_prep_launch(const Job &j, cudaStream_t s);
+cudaError_t seed_launch(const Job &j, int grid, cudaStream_t s);
 cudaError_t post_setup(int occ[2]);
 cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
                         cudaStream_t s);
@@ -139,10 +140,11 @@ sv_status cuda_status(cudaError_t e)
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t rp, rs, resid, rescue, dtmp, tvpart, rpart, smask, svalid, total;
+    size_t rp, rs, resid, rescue, dtmp, tvpart, rpart, smask, svalid, seeds, total;
 };
 
-Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks, int states)
+Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks, int states,
+              size_t seed_recs)
 {
     Layout L;
     size_t o = 0;
@@ -155,6 +157,7 @@ Layout layout(int B, int rows_per_seq, int parts, int K, int W, int tv_chunks, i
     L.rpart = o;  o = align_up(o + rescue_scratch_doubles(B) * sizeof(double));
     L.smask = o;  o = align_up(o + (size_t)B * states * sizeof(uint64_t));
     L.svalid = o; o = align_up(o + (size_t)B * sizeof(unsigned));
+    L.seeds = o;  o = align_up(o + seed_recs * sizeof(SeedRec));
     L.total = o;
     return L;
 }
@@ -267,8 +270,23 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.rTp = j.Tp > 0.f ? 1.0 / (double)j.Tp : 0.0;
     j.rTq = j.Tq > 0.f ? 1.0 / (double)j.Tq : 0.0;
     j.tv_chunks = tv_chunks;
+    // seed records: one per chunk of seed_bpw blocks of 256 ids of every
+    // Gumbel-max row.  A warp lists a chunk with its lanes kept busy by
+    // handing out blocks, so larger chunks waste fewer trips; the largest
+    // size that still gives every SM a full wave of seed warps (8 CTAs of 8
+    // warps) is taken, 32 blocks when even that size does not.
+    const int nblk = (j.V + 255) / 256;
+    const long long grows = (long long)j.B * gumbel_rows(j);
+    j.seed_bpw = 32;
+    for (int bpw = 128; bpw > 32; bpw /= 2)
+        if (grows * ((nblk + bpw - 1) / bpw) >= 64LL * h->sms) {
+            j.seed_bpw = bpw;
+            break;
+        }
+    j.seed_chunks = (nblk + j.seed_bpw - 1) / j.seed_bpw;
+    const size_t seed_recs = (size_t)j.B * gumbel_rows(j) * j.seed_chunks;
     Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks,
-                      j.kind == K_SPOT ? j.N + 1 : (j.kind == K_ANYORDER ? 1 : 0));
+                      j.kind == K_SPOT ? j.N + 1 : (j.kind == K_ANYORDER ? 1 : 0), seed_recs);
     sv_status st = ensure_ws(h, L.total, s);
     if (st != SV_OK) return st;
     st = ensure_cnt(h, j.B, s);
@@ -285,17 +303,27 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.rpart = (double *)(w + L.rpart);
     j.smask = (uint64_t *)(w + L.smask);
     j.svalid = (unsigned *)(w + L.svalid);
+    j.seeds = seed_recs ? (SeedRec *)(w + L.seeds) : nullptr;
     *grid = (int)std::min<long long>(j.total_units, resident);
     return SV_OK;
 }
 
+// The timing events (SV_OPT_TIMING_EVENTS) bracket the streaming pass with
+// the kernels that prepare it (state masks, seed records).
 sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post, bool tv)
 {
+    if (h->timing) cudaEventRecord(h->ev[0], s);
     if (j.kind == K_SPOT || j.kind == K_ANYORDER) {
         cudaError_t e = j.kind == K_SPOT ? spot_prep_launch(j, s) : anyorder_prep_launch(j, s);
         if (e != cudaSuccess) return cuda_status(e);
     }
-    if (h->timing) cudaEventRecord(h->ev[0], s);
+    if (j.seeds) {
+        // enough warps for every chunk, at most 8 CTAs of 256 threads per SM
+        const long long warps = (long long)j.B * gumbel_rows(j) * j.seed_chunks;
+        const int grid = (int)std::min<long long>((warps + 7) / 8, 8LL * h->sms);
+        cudaError_t e = seed_launch(j, std::max(grid, 1), s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     cudaError_t e = pass_launch(j, grid, s);
     if (h->timing) cudaEventRecord(h->ev[1], s);
     if (e != cudaSuccess) return cuda_status(e);
@@ -633,13 +661,13 @@ sv_status sv_packed_anyorder_step(sv_handle *h, const void *logits, sv_dtype dty
                                   const int32_t *draft, const int32_t *end_pos, int32_t eos_id,
                                   int32_t *accept_len, int32_t *commit_len, int32_t *commit_pos,
                                   int32_t *commit_tok, int32_t *end_out, int32_t *next_draft,
-                                  float *score, int32_t *next_order, void *stream)
+                                  float *score, void *stream)
 {
     if (!h || B < 0 || Kv < 1 || Kv > kMaxK || W < 1 || W > kMaxK) return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
     if (!logits_ok(logits, dtype, row_stride, V) || !u || !win_pos || !order || !draft ||
         !end_pos || !accept_len || !commit_len || !commit_pos || !commit_tok || !end_out ||
-        !next_draft || !next_order)
+        !next_draft)
         return SV_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(h->mu);
     cudaStream_t s = (cudaStream_t)stream;
@@ -662,7 +690,6 @@ sv_status sv_packed_anyorder_step(sv_handle *h, const void *logits, sv_dtype dty
     j.end_out = end_out;
     j.next_draft = next_draft;
     j.confidence = score;
-    j.next_order = next_order;
     if (sv_status fi = fault_injected("sv_packed_anyorder_step")) return fi;
     int grid;
     sv_status st = plan(h, j, Kv + W, s, 1, &grid);

@@ -116,6 +116,28 @@ static __device__ RowM merge_row(const Job &j, int b, int slot, double r1, doubl
         c.v2 = x.gv2;
         r.gc.merge(c);
     }
+    // a Gumbel-max row's top ids were scored before the stream (seed
+    // records, one per chunk of the row); the stream skipped them
+    if (j.seeds) {
+        const int k = gumbel_index(j, slot, clamp_len(j, b));
+        if (k >= 0) {
+            const SeedRec *sr =
+                j.seeds + ((int64_t)b * gumbel_rows(j) + k) * j.seed_chunks;
+            for (int q = 0; q < j.seed_chunks; ++q) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(sr + q));
+                const float4 c4 = __ldcg(reinterpret_cast<const float4 *>(sr + q) + 1);
+                Cand2 c;
+                c.hi1 = a.y;
+                c.lo1 = a.z;
+                c.hi2 = a.w;
+                c.lo2 = c4.x;
+                c.hi3 = c4.y;
+                c.v1 = __float_as_int(c4.z);
+                c.v2 = __float_as_int(c4.w);
+                r.gc.merge(c);
+            }
+        }
+    }
     const double l1 = log2_fast(S1), l2 = log2_fast(S2);
     r.L2c1 = (double)E1 + l1;
     r.L2c2 = (double)E2 + l2;
@@ -212,6 +234,73 @@ static __device__ __noinline__ bool cactus_bracket(double p, double delta, doubl
     *glo = a;
     *ghi = b;
     return ok;
+}
+
+// Newton's method for gamma* in fp32 (the same steps and logs as
+// cactus_bracket), for the fast path's bracket below.
+__device__ __forceinline__ float cactus_newton32(float p, float delta)
+{
+    float lo = p, hi = 1.f;
+    float g = p + sqrtf(2.f * delta * p * (1.f - p));
+    if (!(g > lo && g < hi))
+        g = 0.5f * (lo + hi);
+    for (int it = 0; it < 24; ++it) {
+        const float a = log1pf((g - p) / p), b = log1pf((p - g) / (1.f - p));
+        const float f = g * a + (1.f - g) * b - delta;
+        if (f > 0.f)
+            hi = g;
+        else
+            lo = g;
+        float gn = g - f / (a - b);
+        if (!(gn > lo && gn < hi))
+            gn = 0.5f * (lo + hi);
+        if (gn == g)
+            break;
+        g = gn;
+    }
+    return g;
+}
+
+// Bracket [*glo, *ghi] of gamma*(p) for every p in [plo, phi] (gamma* grows
+// with p): the fp32 Newton points at plo and phi, widened by 2^-14
+// relative, each checked in fp64 to lie on its side of its root (margin of
+// 64 roundings of Phi's terms).  Two fp64 evaluations of Phi in all; falls
+// back to the fp64 Newton of cactus_bracket when a check fails.  false when
+// no bracket could be certified.
+static __device__ __noinline__ bool cactus_bracket_fast(double plo, double phi, double delta,
+                                                 double *glo, double *ghi)
+{
+    double d1, sc;
+    bool ok_lo, ok_hi;
+    if (!(plo > 0.0) || !(delta > 0.0) || delta >= -log(plo)) {
+        double a, b;
+        ok_lo = cactus_bracket(plo, delta, glo, &a);
+    } else {
+        *glo = fmax(plo, (double)cactus_newton32((float)plo, (float)delta) * (1.0 - 0x1p-14));
+        const double f = cactus_f(*glo, plo, delta, &d1, &sc);
+        ok_lo = *glo == plo || f < -64.0 * 0x1p-53 * sc;
+        if (!ok_lo) {
+            double a;
+            ok_lo = cactus_bracket(plo, delta, glo, &a);
+        }
+    }
+    if (phi >= 1.0 || !(delta > 0.0) || delta >= -log(phi)) {
+        double a;
+        ok_hi = cactus_bracket(phi, delta, &a, ghi);
+    } else {
+        *ghi = fmin(1.0, (double)cactus_newton32((float)fmin(phi, 1.0), (float)delta) *
+                             (1.0 + 0x1p-14));
+        ok_hi = *ghi >= 1.0;
+        if (!ok_hi) {
+            const double f = cactus_f(*ghi, phi, delta, &d1, &sc);
+            ok_hi = f > 64.0 * 0x1p-53 * sc;
+        }
+        if (!ok_hi) {
+            double a;
+            ok_hi = cactus_bracket(phi, delta, &a, ghi);
+        }
+    }
+    return ok_lo && ok_hi;
 }
 
 // Acceptance probability min{1, gamma* / q} in fp64 from log p(d), log q(d)

@@ -53,10 +53,10 @@ constexpr int kStages = SV_STAGES;
 static_assert(kVecsPerThread * kConsumers == kStageVecs, "stage must split evenly");
 constexpr int ceil_log2(int n) { return n <= 1 ? 0 : 1 + ceil_log2((n + 1) / 2); }
 // Longest fp32 summation path of a unit's log-sum-exp partial, one addition
-// per stage aside: the pairwise tree of a chunk (up to 4 element pairs per
-// vector), the x + y of the packed pair, the warp sum and the sequential sum
-// over the consumer warps.
-constexpr int kLseSumDepth = ceil_log2(kVecsPerThread * 4) + 1 + 5 + (kConsumerWarps - 1);
+// per stage aside: the pairwise tree of a vector's element pairs (up to 4),
+// the chain over the chunk's vectors, the x + y of the packed pair, the warp
+// sum and the sequential sum over the consumer warps.
+constexpr int kLseSumDepth = 2 + (kVecsPerThread - 1) + 1 + 5 + (kConsumerWarps - 1);
 constexpr int kMaxK = 32;
 constexpr int kMaxN = 64;
 constexpr double kFlagEps = 1e-9;                 // near-threshold window

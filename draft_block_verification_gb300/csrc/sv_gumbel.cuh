@@ -165,11 +165,13 @@ __device__ __forceinline__ float gumbel32(uint64_t m, bool top)
 __device__ __forceinline__ float g_ordinary_max(const float *tab) { return tab[kGTab - 1]; }
 
 // Threshold used against level-1 (table) bounds: an fp32 bound ub of an
-// exact score satisfies exact <= ub + (|ub| + 40) 2^-21, so comparing ub with
-// thr - (|thr| + 41) 2^-21 never drops an element that can reach thr.
+// exact score satisfies exact <= ub + (|ub| + 40) 2^-21, so an element whose
+// ub is at most thr - (|thr| + 41) 2^-21 stays at least about 2^-21 below thr
+// and cannot reach it.  The threshold is rounded down at each step, so the
+// fp32 value never exceeds that real bound.
 __device__ __forceinline__ float level1_thr(float thr)
 {
-    return thr - (fabsf(thr) + 41.f) * 0x1p-21f;
+    return __fsub_rd(thr, __fmul_ru(__fadd_ru(fabsf(thr), 41.f), 0x1p-21f));
 }
 
 // Candidates with the two largest upper ends, and the largest upper end of

@@ -20,6 +20,16 @@ struct __align__(16) ResidEntry {
                        // but for the modified Cactus rule)
 };
 
+// One seed record: the top ids (the ids whose uniform lies in the top 1/256)
+// of one chunk of a Gumbel-max row, scored before the stream: the chunk's
+// threshold (best lower end - 1e-9) and its candidates (Cand2 fields).
+struct __align__(16) SeedRec {
+    float thr;
+    float hi1, lo1, hi2, lo2, hi3;
+    int v1, v2;
+};
+// blocks of 256 ids per seed record: one or two per lane (seed_bpw)
+
 // A sequence that goes to the fp64 path.
 struct __align__(16) RescueEntry {
     int b;
@@ -97,9 +107,9 @@ struct Job {
     const uint64_t *root_mask;
     int32_t *commit_pos, *commit_tok, *state_pos, *state_tok;
     // any-order Packed-SS (K_ANYORDER): window positions, rank order, end
-    // position in and out, the next confidence order
+    // position in and out
     const int32_t *win_pos, *order, *end_in;
-    int32_t *end_out, *next_order;
+    int32_t *end_out;
     // workspace
     RowPart *rp;        // [B * rows_per_seq * parts]
     RowStat *rs_stat;   // [B * rows_per_seq]
@@ -112,6 +122,9 @@ struct Job {
     unsigned *tvdone;   // [B * K]
     int tv_chunks;
     double *rpart;      // residual / fp64 scratch
+    SeedRec *seeds;     // [gumbel rows * seed_chunks] (see gumbel_rows)
+    int seed_chunks;    // seed records per Gumbel-max row
+    int seed_bpw;       // blocks of 256 ids per seed record (32, 64 or 128)
     uint64_t *smask;    // SPOT: masked positions of every state [B * (N + 1)];
                         // any-order: verify rows needed per sequence [B]
     unsigned *svalid;   // SPOT, any-order: rows to stream per sequence [B]
@@ -200,6 +213,45 @@ __device__ __forceinline__ const char *slot_row(const Job &j, int b, int slot)
 __device__ __forceinline__ int64_t pos0_of(const Job &j, int b)
 {
     return j.pos_base ? __ldg(j.pos_base + b) : 0;
+}
+
+// Gumbel-max rows: per sequence, the bonus row of a sampling call; the
+// bonus row and the W proposal rows of a Packed-SS step at T > 0; every node
+// row of a tree at T > 0; every (state, position) row of a SPOT call at
+// T > 0.  Row k of sequence b has index b * gumbel_rows(j) + k.
+__host__ __device__ __forceinline__ int gumbel_rows(const Job &j)
+{
+    switch (j.kind) {
+    case K_SAMPLE: return 1;
+    case K_PACKED: return j.Tp != 0.f ? 1 + j.W : 0;
+    case K_TREE: return j.Tp != 0.f ? j.N : 0;
+    case K_SPOT: return j.Tp != 0.f ? (j.N + 1) * j.L : 0;
+    default: return 0;
+    }
+}
+
+// Row slot of Gumbel-max row k of sequence b (n: the sequence's clamped
+// draft length, which places the bonus row).
+__device__ __forceinline__ int gumbel_slot(const Job &j, int k, int n)
+{
+    if (j.kind == K_SAMPLE) return n;
+    if (j.kind == K_PACKED) return k == 0 ? n : j.K + k - 1;
+    return k;  // tree, SPOT
+}
+
+// Index k of the Gumbel-max row in `slot` of a sequence with clamped draft
+// length n, or -1 when that row carries no Gumbel-max.
+__device__ __forceinline__ int gumbel_index(const Job &j, int slot, int n)
+{
+    switch (j.kind) {
+    case K_SAMPLE: return slot == n ? 0 : -1;
+    case K_PACKED:
+        if (j.Tp == 0.f) return -1;
+        return slot == n ? 0 : (slot >= j.K ? 1 + slot - j.K : -1);
+    case K_TREE:
+    case K_SPOT: return j.Tp != 0.f ? slot : -1;
+    default: return -1;
+    }
 }
 
 }  // namespace sv

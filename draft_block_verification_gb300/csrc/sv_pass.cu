@@ -27,11 +27,11 @@ namespace sv {
 constexpr int kFinQ = 32;      // decision steps queued per CTA
 constexpr int kUnitSlots = 8;  // units whose partials wait for the finalizer
 constexpr int kGQ = 64;        // queued Gumbel vectors per consumer warp
-constexpr int kSeedCap = 2048; // top ids gathered per seeding round
 
 struct RowMode {
     int mode;
     float c1, c2, invT;
+    float thr0;       // Gumbel-max rows: the threshold the row's seed records give
     double T;
     uint64_t key;
 };
@@ -45,13 +45,8 @@ struct StageMeta {
     int b;            // sequence of the unit
     unsigned expect;  // records that complete sequence b
     int xid;          // vocabulary id whose logit the unit records (-1: none)
-    int vend;         // end (vector index) of the unit's part of the row
+    int pad;
     const char *row;  // the unit's logit row
-    // first stage: the next unit this CTA streams, if it carries a Gumbel-max
-    // (its top ids are prefetched while this unit streams)
-    const char *nrow;
-    uint64_t nkey;
-    int nrec, nlo, nhi, npad;
     RowMode rm;       // row mode of the unit
 };
 
@@ -94,6 +89,7 @@ struct PassShared {
     // the vector's index in the row
     uint4 gqd[kConsumerWarps][kGQ];
     uint32_t gqv[kConsumerWarps][kGQ];
+    Cand2 gcand[kConsumerWarps];  // each consumer warp's Gumbel candidates of its unit
     uint64_t skip[kSkipN];   // skip thresholds of the top-id draws
     // unit slots: consumer warps write their partials and arrive on ubar; the
     // finalizer merges them and arrives on ufree
@@ -102,16 +98,6 @@ struct PassShared {
     WarpPart up[kUnitSlots][kConsumerWarps];
     int uunit[kUnitSlots], ub[kUnitSlots];
     unsigned uexpect[kUnitSlots];
-    // top ids of a unit being seeded, and their logits' 32-bit words (copied
-    // ahead, one unit early); buffer lu & 1 belongs to local unit lu
-    uint32_t seed_ids[2][kSeedCap];
-    uint32_t seed_x[2][kSeedCap];
-    int seed_cnt[2];     // ids listed in a buffer
-    int seed_n;
-    int seed_more;
-    // barrier among the consumer warps (see csync) and each warp's phase
-    uint64_t csync;
-    uint32_t cph[kConsumerWarps];
     PlanEntry plan[kPlanQ];
     uint64_t plan_full[kPlanQ], plan_empty[kPlanQ];
     volatile int nunits;     // units this CTA streamed (set when the producer is done)
@@ -259,6 +245,7 @@ __device__ __forceinline__ RowMode row_mode(const Job &j, int b, int slot, int n
     RowMode r;
     r.mode = 0;
     r.c1 = r.c2 = r.invT = 0.f;
+    r.thr0 = -INFINITY;
     r.T = 1.0;
     r.key = 0;
     switch (j.kind) {
@@ -391,14 +378,20 @@ __device__ __forceinline__ UnitInfo unit_info(const Job &j, long long u, const U
         i.expect = (unsigned)(valid_slots_n(j, n) * j.parts);
     }
     i.rm = row_mode(j, i.b, i.slot, n, p.p0, p.np);
+    if ((i.rm.mode & M_GUMBEL) && j.seeds) {
+        const int k = gumbel_index(j, i.slot, n);
+        const SeedRec *sr = j.seeds + ((int64_t)i.b * gumbel_rows(j) + k) * j.seed_chunks;
+        for (int q = 0; q < j.seed_chunks; ++q)
+            i.rm.thr0 = fmaxf(i.rm.thr0, __ldcg(&sr[q].thr));
+    }
     return i;
 }
 
-// Gumbel part of a thread's state (passed by value to the out-of-line queue
-// screen, so that the state stays in registers).
+// Gumbel part of a thread's state: the thresholds only (passed by value to
+// the out-of-line queue screen, so that they stay in registers).  The
+// candidates are kept per warp in shared memory (PassShared::gcand), written
+// only by that screen, so that the stream loop does not hold them.
 struct GState {
-    Cand2 c;           // candidates
-    float lomax;       // best lower end seen
     float thr, thrS;   // level-2 and level-1 thresholds
 };
 
@@ -420,8 +413,6 @@ __device__ __forceinline__ void tstate_init(TState &s)
     s.acc1 = s.acc2 = make_float2(0.f, 0.f);
     s.mx = -INFINITY;
     s.amax = 0x7FFFFFFF;
-    s.g.c.init();
-    s.g.lomax = -INFINITY;
     s.g.thr = s.g.thrS = s.pub = -INFINITY;
     s.gqn = 0;
     s.xd = __int_as_float(0x7FC00000);
@@ -436,20 +427,17 @@ __device__ __forceinline__ void raise_thr(GState &s, float t)
 }
 
 // Level 2: fp32 interval of x/T + G; candidates whose upper end reaches the
-// threshold are kept, and the best lower end raises the threshold (anything
+// threshold are kept, and their lower end raises the threshold (anything
 // below it - 1e-9 can neither win nor tie within 1e-9).
 __device__ __forceinline__ void gumbel_level2(float x, uint32_t v, bool top, GState &s,
-                                              const RowMode &rm)
+                                              Cand2 &c, const RowMode &rm)
 {
     const float2 iv = logit_interval_at(x, rm.invT, rm.key, v, top);
     const float lo = iv.x, hi = iv.y;
     if (hi < s.thr)
         return;
-    s.c.add(lo, hi, (int)v);
-    if (lo > s.lomax) {
-        s.lomax = lo;
-        raise_thr(s, __fsub_rd(lo, 1e-9f));
-    }
+    c.add(lo, hi, (int)v);
+    raise_thr(s, __fsub_rd(lo, 1e-9f));
 }
 
 // ---------------------------------------------------------------------------
@@ -482,29 +470,32 @@ __device__ __forceinline__ float chunk_max(const Chunk &q)
 }
 
 // Sum of 2^fl(x c - e) over the chunk: one packed FFMA per two elements, one
-// ex2 per element, a packed-add tree.
+// ex2 per element; a pairwise tree over each vector's element pairs, and the
+// vectors' sums chained in order (so that a vector's registers are free once
+// it is summed).
 template <typename In>
 __device__ __forceinline__ float2 lse_terms(const Chunk &q, float c, float e)
 {
     using VT = VecTraits<In>;
     constexpr int P = VT::P;  // element pairs per vector
-    float2 t[kVecsPerThread * P];
     const float2 cc = make_float2(c, c), ne = make_float2(-e, -e);
+    float2 part = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kVecsPerThread; ++k)
+    for (int k = 0; k < kVecsPerThread; ++k) {
+        float2 t[P];
 #pragma unroll
         for (int i = 0; i < P; ++i) {
             const float2 y = fma2(VT::pair(q[k], i), cc, ne);
-            t[k * P + i] = make_float2(ex2f(y.x), ex2f(y.y));
+            t[i] = make_float2(ex2f(y.x), ex2f(y.y));
         }
-    // pairwise tree over any number of terms (depth ceil(log2 N))
-    constexpr int N = kVecsPerThread * P;
 #pragma unroll
-    for (int w = 1; w < N; w <<= 1)
+        for (int w = 1; w < P; w <<= 1)
 #pragma unroll
-        for (int i = 0; i + w < N; i += 2 * w)
-            t[i] = add2(t[i], t[i + w]);
-    return t[0];
+            for (int i = 0; i + w < P; i += 2 * w)
+                t[i] = add2(t[i], t[i + w]);
+        part = k == 0 ? t[0] : add2(part, t[0]);
+    }
+    return part;
 }
 
 // Adds the chunk to one log-sum-exp accumulator.  The first chunk with an
@@ -575,17 +566,21 @@ __device__ __forceinline__ void max_chunk(const Chunk &q, int vbase, TState &s)
 }
 
 // Per-id screen of the queued vectors, 32 at a time, a vector per lane: its
-// top ids are skipped (the seeding warp scored every top id of the unit);
-// an ordinary id is bounded by the top byte of its fine bits, and survivors
-// get the fp32 interval of level 2.
+// top ids are skipped (the seed kernel scored every top id of the row); an
+// ordinary id is bounded by the top byte of its fine bits, and survivors get
+// the fp32 interval of level 2.  The lanes' candidates are merged into the
+// warp's (wc, in shared memory), and every lane leaves with the warp's best
+// threshold.  Whole warp.
 template <typename In>
 __device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
                                             const uint32_t *__restrict__ qv, int n, GState s,
                                             const RowMode &rm, const float *__restrict__ gt,
-                                            const uint64_t *__restrict__ skip)
+                                            const uint64_t *__restrict__ skip, Cand2 *wc)
 {
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
+    Cand2 c;
+    c.init();
     __syncwarp();
     for (int i = (int)(threadIdx.x & 31); i < n; i += 32) {
         const uint4 d = qd[i];
@@ -599,32 +594,38 @@ __device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
             const float x = VT::elem(d, e);
             const uint64_t m = fine52(rm.key, v);
             if (fmaf(x, rm.invT, gt[(int)(m >> 44)]) >= s.thrS)
-                gumbel_level2(x, v, false, s, rm);
+                gumbel_level2(x, v, false, s, c, rm);
         }
     }
+    warp_cand2(c);
+    if ((threadIdx.x & 31) == 0)
+        wc->merge(c);
+    raise_thr(s, warp_max(s.thr));
     __syncwarp();
     return s;
 }
 
-// Level 1 on whole vectors: an ordinary id's G stays below the table's last
-// entry, so a vector is queued only if its largest logit can reach the
-// threshold with that bound.  The queue is compacted with a ballot, so a warp
-// does not diverge per vector.
+// Level 1 on whole vectors: an ordinary id's G stays below gmax (the table's
+// last entry), so a vector is queued only if its largest logit can reach the
+// threshold with that bound.  The comparison is strict: a bound equal to the
+// level-1 threshold stays below thr (the threshold's margin exceeds the
+// bound's rounding slack), and the -inf padding of a short stage never passes,
+// not even a threshold of -inf.  The queue is compacted with a ballot, so a
+// warp does not diverge per vector.
 template <typename In>
-__device__ __forceinline__ void gumbel_chunk(const Chunk &q, int nv, int vbase, TState &s,
-                                             const RowMode &rm, const float *__restrict__ gt,
+__device__ __forceinline__ void gumbel_chunk(const Chunk &q, int vbase, TState &s,
+                                             const RowMode &rm, float gmax,
+                                             const float *__restrict__ gt,
                                              const uint64_t *__restrict__ skip, PassShared &sm)
 {
     using VT = VecTraits<In>;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const float gmax = g_ordinary_max(gt);
     uint4 *qd = sm.gqd[w];
     uint32_t *qv = sm.gqv[w];
 #pragma unroll
     for (int k = 0; k < kVecsPerThread; ++k) {
         const int idx = t + k * kConsumers;
-        const bool pass =
-            fmaf(VT::hi_of(VT::pmax(q[k])), rm.invT, gmax) >= s.g.thrS && idx < nv;
+        const bool pass = fmaf(VT::hi_of(VT::pmax(q[k])), rm.invT, gmax) > s.g.thrS;
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
         if (bal) {
             if (pass) {
@@ -634,7 +635,7 @@ __device__ __forceinline__ void gumbel_chunk(const Chunk &q, int nv, int vbase, 
             }
             s.gqn += __popc(bal);
             if (s.gqn > kGQ - 32) {
-                s.g = gumbel_flush<In>(qd, qv, s.gqn, s.g, rm, gt, skip);
+                s.g = gumbel_flush<In>(qd, qv, s.gqn, s.g, rm, gt, skip, &sm.gcand[w]);
                 s.gqn = 0;
             }
         }
@@ -643,8 +644,8 @@ __device__ __forceinline__ void gumbel_chunk(const Chunk &q, int nv, int vbase, 
 
 template <typename In, int MODE>
 __device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, int vbase, TState &s,
-                                         const RowMode &rm, const float *__restrict__ gt,
-                                         PassShared &sm)
+                                         const RowMode &rm, float gmax,
+                                         const float *__restrict__ gt, PassShared &sm)
 {
     Chunk q;
     load_chunk<In>(st, nv, q);
@@ -655,7 +656,7 @@ __device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, i
     if (MODE & M_LSE2)
         lse_chunk<In>(q, rm.c2, s.e2, s.acc2);
     if (MODE & M_GUMBEL)
-        gumbel_chunk<In>(q, nv, vbase, s, rm, gt, sm.skip, sm);
+        gumbel_chunk<In>(q, vbase, s, rm, gmax, gt, sm.skip, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -724,20 +725,21 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
         double rel = 1.01 * (ep + eq) + 0x1p-21 + 1e-13;
         double alo = alpha_of(j.amode, r * (1.0 - rel), j.lam);
         double ahi = alpha_of(j.amode, r * (1.0 + rel), j.lam);
-        if (j.amode == SV_LENIENT_CACTUS && r * (1.0 - rel) < 1.0) {
-            // gamma* grows with p: bracket p and q, then gamma* at both ends
-            // of p's bracket; alpha = gamma* / q and c = (1 - gamma*)/(1 - p)
+        double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
+        // Cactus: gamma* >= p gives alpha >= the lossless alpha (alo, ahi
+        // above), so a sure lossless accept is a sure accept; other lanes
+        // bracket gamma* over p's bracket (it grows with p), then alpha =
+        // gamma* / q and the residual scale c = (1 - gamma*)/(1 - p)
+        if (j.amode == SV_LENIENT_CACTUS && !(u < alo - kFlagEps)) {
             const double plo = exp(lp - 1.01 * ep - 1e-13), phi = exp(lp + 1.01 * ep + 1e-13);
             const double qlo = exp(lq - 1.01 * eq - 1e-13), qhi = exp(lq + 1.01 * eq + 1e-13);
-            double g0, g1, g2, g3;
-            const bool ok = cactus_bracket(plo, (double)j.lam, &g0, &g1) &&
-                            cactus_bracket(phi, (double)j.lam, &g2, &g3);
+            double g0, g3;
+            const bool ok = cactus_bracket_fast(plo, phi, (double)j.lam, &g0, &g3);
             alo = ok ? fmin(1.0, g0 / qhi) : 0.0;
             ahi = ok ? fmin(1.0, g3 / qlo) : 1.0;
             lclo = (g3 < 1.0) ? log1p(-g3) - log1p(-plo) : -INFINITY;
             lchi = log1p(-g0) - log1p(-phi);
         }
-        double u = uniform_at(rng_key(j.seed, kAccept, (uint64_t)b, p0 + lane, 0), 0, j.skip);
         acc = u < alo - kFlagEps;
         bool rej = u >= ahi + kFlagEps;
         und = !(acc || rej) || j.force_rescue;
@@ -1078,20 +1080,69 @@ __device__ __forceinline__ int state_val(const int (&v)[3], int a)
     return (a >> 5) == 0 ? x0 : ((a >> 5) == 1 ? x1 : x2);
 }
 
-// max_v softmax(x)_v = 1 / sum_v exp(x_v - max x) of one row in fp64, by the
-// whole warp: the rare states whose fp32 confidences do not separate their
-// best position by the 1e-9 window.
-static __device__ __noinline__ double conf64_row(const Job &j, const char *row)
+// max_v softmax(x)_v = 1 / S, S = sum_v exp(x_v - max x), of one row, by the
+// whole warp (16-byte loads), for the rare states whose streamed confidences
+// do not separate their best position by the 1e-9 window.
+//   conf_row_refined: S from CUDA's expf (documented within 2 ulp) with a
+//     compensated fp32 sum per lane and an fp64 sum over the lanes: the
+//     interval [*lo, *hi] of the confidence has relative half-width 5e-7.
+//   conf_row64: S in fp64 (exp of the fp64 difference), for contenders that
+//     the refined intervals still do not separate.
+template <bool EXACT>
+static __device__ __noinline__ double conf_row_sum(const Job &j, const char *row, float *mout)
 {
     const int lane = threadIdx.x & 31;
+    const uint4 *r4 = reinterpret_cast<const uint4 *>(row);
+    const bool bf = j.dtype == SV_BF16;
     float m = -INFINITY;
-    for (int v = lane; v < j.V; v += 32)
-        m = fmaxf(m, load_logit(j, row, v));
+    for (int k = lane; k < j.nvec; k += 32) {
+        const uint4 q = __ldg(r4 + k);
+        m = fmaxf(m, bf ? VecTraits<uint16_t>::hi_of(VecTraits<uint16_t>::pmax(q))
+                        : VecTraits<float>::hi_of(VecTraits<float>::pmax(q)));
+    }
     m = warp_max(m);
-    double sum = 0.0;
-    for (int v = lane; v < j.V; v += 32)
-        sum += exp((double)load_logit(j, row, v) - (double)m);
-    return 1.0 / warp_sumd(sum);
+    *mout = m;
+    double sd = 0.0;
+    float sf = 0.f, cf = 0.f;  // compensated fp32 sum
+    for (int k = lane; k < j.nvec; k += 32) {
+        const uint4 q = __ldg(r4 + k);
+        float f[8];
+        int ne = 8;
+        if (bf) {
+            VecTraits<uint16_t>::unpack(q, f);
+        } else {
+            float g[4];
+            VecTraits<float>::unpack(q, g);
+            for (int e = 0; e < 4; ++e) f[e] = g[e];
+            ne = 4;
+        }
+        for (int e = 0; e < ne; ++e) {
+            if (EXACT) {
+                sd += exp((double)f[e] - (double)m);
+            } else {
+                const float y = expf(f[e] - m) - cf;  // f - m is exact for bf16 and fp32
+                const float t = sf + y;
+                cf = (t - sf) - y;
+                sf = t;
+            }
+        }
+    }
+    return warp_sumd(EXACT ? sd : (double)sf);
+}
+
+static __device__ __forceinline__ void conf_row_refined(const Job &j, const char *row, double *lo,
+                                                        double *hi)
+{
+    float m;
+    const double S = conf_row_sum<false>(j, row, &m);
+    *lo = 1.0 / (S * (1.0 + 5e-7));
+    *hi = 1.0 / (S * (1.0 - 5e-7));
+}
+
+static __device__ __forceinline__ double conf_row64(const Job &j, const char *row)
+{
+    float m;
+    return 1.0 / conf_row_sum<true>(j, row, &m);
 }
 
 static __device__ __noinline__ void fin_spot(const Job &j, int b)
@@ -1101,97 +1152,112 @@ static __device__ __noinline__ void fin_spot(const Job &j, int b)
     const int64_t p0 = pos0_of(j, b);
     // relative error of a confidence exp(m - L1) from the streamed sums
     const double e = 1.01 * j.eps_lse + 0x1p-21 + 1e-13;
-    int sp[3], sv[3], nflag = 0;
-    for (int r = 0; r < 3; ++r) {
-        const int st = lane + 32 * r;
-        const uint64_t mk = st < S ? __ldg(j.smask + (int64_t)b * S + st) : 0ull;
-        // best position by fp32 confidence (lowest s among equal values) and
-        // the largest upper end among the other masked positions
-        float bc = -1.f;
-        double blo = 0.0, bhi = 0.0, ohi = -1.0;
-        int bs = -1, bam = -1;
-        Cand2 bgc;
-        bgc.init();
-        for (int s = 0; s < L; ++s) {
-            if (!((mk >> s) & 1ull))
-                continue;
-            const RowM rm = merge_row(j, b, st * L + s, j.cr1, 1.0);
-            const float c = exp_fast((double)rm.m - rm.L1a);
-            const double lo = (double)c * (1.0 - e), hi = (double)c * (1.0 + e);
-            if (c > bc) {
-                if (bs >= 0)
-                    ohi = fmax(ohi, bhi);
-                bc = c;
-                blo = lo;
-                bhi = hi;
-                bs = s;
-                bam = rm.amax;
-                bgc = rm.gc;
-            } else {
-                ohi = fmax(ohi, hi);
-            }
+    // sp[r], sv[r]: Phi of state lane + 32 r (position, token)
+    int sp[3] = {-1, -1, -1}, sv[3] = {-1, -1, -1}, nflag = 0;
+    for (int st = 0; st < S; ++st) {
+        const uint64_t mk = __ldg(j.smask + (int64_t)b * S + st);
+        if (mk == 0ull)
+            continue;
+        // lane = position: its row's confidence interval
+        const bool has = lane < L && ((mk >> lane) & 1ull);
+        float c = -1.f;
+        double lo = -1.0, hi = -1.0;
+        int am = -1;
+        if (has) {
+            const RowM rm = merge_row(j, b, st * L + lane, j.cr1, 1.0);
+            c = exp_fast((double)rm.m - rm.L1a);
+            lo = (double)c * (1.0 - e);
+            hi = (double)c * (1.0 + e);
+            am = rm.amax;
         }
-        // settled in fp32 when the best's lower end clears every other upper
-        // end by the flag window; else the contenders in fp64, by the warp
-        const bool unsure = bs >= 0 && ohi >= 0.0 && blo - ohi < kFlagEps;
-        unsigned um = __ballot_sync(0xFFFFFFFFu, unsure);
-        while (um) {
-            const int src = __ffs(um) - 1;
-            um &= um - 1;
-            const int ost = src + 32 * r;
-            const uint64_t omk = __shfl_sync(0xFFFFFFFFu, mk, src);
-            const double oblo = __shfl_sync(0xFFFFFFFFu, blo, src);
-            // contenders: masked positions whose upper end reaches the best's
-            // lower end - 1e-9 (lane = position)
-            bool cont = false;
-            if (lane < L && ((omk >> lane) & 1ull)) {
-                const RowM rm = merge_row(j, b, ost * L + lane, j.cr1, 1.0);
-                const double c = (double)exp_fast((double)rm.m - rm.L1a);
-                cont = c * (1.0 + e) >= oblo - kFlagEps;
-            }
-            unsigned cm = __ballot_sync(0xFFFFFFFFu, cont);
-            double c1 = -1.0, c2 = -1.0;
-            int s1 = -1;
-            while (cm) {  // ascending positions: the lowest wins exact ties
-                const int s = __ffs(cm) - 1;
-                cm &= cm - 1;
-                const double c = conf64_row(j, row_ptr(j, b, ost * L + s));
-                if (c > c1) {
-                    c2 = c1;
-                    c1 = c;
-                    s1 = s;
-                } else if (c > c2) {
-                    c2 = c;
+        // the best by (confidence desc, position asc) and the largest upper
+        // end among the other masked positions
+        const uint32_t cm = __reduce_max_sync(0xFFFFFFFFu, f2ord(c));
+        const unsigned tie = __ballot_sync(0xFFFFFFFFu, has && f2ord(c) == cm);
+        int bs = __ffs(tie) - 1;
+        const double blo = __shfl_sync(0xFFFFFFFFu, lo, bs);
+        const float oh = (has && lane != bs) ? __double2float_ru(hi) : -1.f;
+        const double ohi = (double)ord2f(__reduce_max_sync(0xFFFFFFFFu, f2ord(oh)));
+        int v = __shfl_sync(0xFFFFFFFFu, am, bs);
+        if (ohi >= 0.0 && __double2float_rd(blo) - ohi < kFlagEps) {
+            // not separated by the streamed bounds: the contenders get the
+            // refined intervals (lane = position); those still within reach
+            // of the best are recomputed in fp64
+            unsigned ct = __ballot_sync(0xFFFFFFFFu, has && hi >= blo - kFlagEps);
+            double rlo = -1.0, rhi = -1.0;
+            for (unsigned cm2 = ct; cm2; cm2 &= cm2 - 1) {
+                const int s = __ffs(cm2) - 1;
+                double a0, a1;
+                conf_row_refined(j, row_ptr(j, b, st * L + s), &a0, &a1);
+                if (lane == s) {
+                    rlo = a0;
+                    rhi = a1;
                 }
             }
-            if (lane == src) {
-                bs = s1;
-                if (c1 - c2 > 0.0 && c1 - c2 < kFlagEps)
+            // the best refined lower end and whether another upper end
+            // comes within 1e-9 of it
+            double best = -1.0;
+            int s1 = -1;
+            for (int o = 0; o < 32; ++o) {
+                const double x = __shfl_sync(0xFFFFFFFFu, rlo, o);
+                if ((ct >> o) & 1u && x > best) {
+                    best = x;
+                    s1 = o;
+                }
+            }
+            const bool close = ((ct >> lane) & 1u) && lane != s1 && rhi >= best - kFlagEps;
+            const unsigned cl = __ballot_sync(0xFFFFFFFFu, close);
+            if (cl) {
+                unsigned cx = cl | (1u << s1);
+                double c1 = -1.0, c2 = -1.0;
+                s1 = -1;
+                while (cx) {  // ascending positions: the lowest wins exact ties
+                    const int s = __ffs(cx) - 1;
+                    cx &= cx - 1;
+                    const double x = conf_row64(j, row_ptr(j, b, st * L + s));
+                    if (x > c1) {
+                        c2 = c1;
+                        c1 = x;
+                        s1 = s;
+                    } else if (x > c2) {
+                        c2 = x;
+                    }
+                }
+                if (lane == 0 && c1 - c2 > 0.0 && c1 - c2 < kFlagEps)
                     ++nflag;
             }
+            bs = s1;
+            v = __shfl_sync(0xFFFFFFFFu, am, bs);
         }
-        // the token at s*: its row's argmax (T = 0) or coupled-noise
-        // Gumbel-max (T > 0)
-        const bool has = bs >= 0;
-        const RowM rb = (has && unsure) ? merge_row(j, b, st * L + bs, j.cr1, 1.0) : RowM{};
-        if (has && unsure) {
-            bam = rb.amax;
-            bgc = rb.gc;
+        if (lane == (st & 31)) {
+            sp[st >> 5] = bs;
+            sv[st >> 5] = v;  // the argmax; replaced by the Gumbel-max at T > 0
         }
-        int v = has ? bam : -1;
-        if (j.Tp != 0.f) {
-            const GRes g = resolve_lanes(j, row_ptr(j, b, has ? st * L + bs : 0),
-                                         rng_key(j.seed, kTree, (uint64_t)b, p0 + (has ? bs : 0), 0),
-                                         (double)j.Tp, j.invTp, bgc, has);
-            v = has ? g.v : -1;
+    }
+    // T > 0: the token at s* is the coupled-noise Gumbel-max of that row
+    if (j.Tp != 0.f) {
+        for (int r = 0; r < 3; ++r) {
+            const int st = lane + 32 * r;
+            const bool has = st < S && sp[r] >= 0;
+            Cand2 gc;
+            gc.init();
             if (has)
+                gc = merge_row(j, b, st * L + sp[r], j.cr1, 1.0).gc;
+            const GRes g = resolve_lanes(j, row_ptr(j, b, has ? st * L + sp[r] : 0),
+                                         rng_key(j.seed, kTree, (uint64_t)b,
+                                                 p0 + (has ? sp[r] : 0), 0),
+                                         (double)j.Tp, j.invTp, gc, has);
+            if (has) {
+                sv[r] = g.v;
                 nflag += g.flag;
+            }
         }
-        sp[r] = bs;
-        sv[r] = v;
+    }
+    for (int r = 0; r < 3; ++r) {
+        const int st = lane + 32 * r;
         if (st < S) {
-            if (j.state_pos) j.state_pos[(int64_t)b * S + st] = bs;
-            if (j.state_tok) j.state_tok[(int64_t)b * S + st] = v;
+            if (j.state_pos) j.state_pos[(int64_t)b * S + st] = sp[r];
+            if (j.state_tok) j.state_tok[(int64_t)b * S + st] = sv[r];
         }
     }
     // match bits: a node's commitment equals Phi of its parent's state
@@ -1240,7 +1306,8 @@ static __device__ __noinline__ void fin_spot(const Job &j, int b)
 // ---------------------------------------------------------------------------
 // Any-order Packed-SS decision step ([PackedSS] App. C, Alg. 3 lines 6-15,
 // eq. 8; scores of App. E.6).  One warp; lane r is rank r of the verify
-// order and also window index r.
+// order and also window index r.  The scores are returned for the caller's
+// order policy, which ranks the next window (App. C "Procedure").
 // ---------------------------------------------------------------------------
 static __device__ __noinline__ void fin_anyorder(const Job &j, int b)
 {
@@ -1284,8 +1351,7 @@ static __device__ __noinline__ void fin_anyorder(const Job &j, int b)
     }
     const unsigned accd = __reduce_or_sync(0xFFFFFFFFu, keep ? (1u << oi) : 0u);
     // proposals (window index = lane): argmax, and its probability at
-    // temperature 1 with a relative error bound
-    const double e = 1.01 * j.eps_lse + 0x1p-21 + 1e-13;
+    // temperature 1
     int z = -1;
     double sc = -1.0;
     if (lane < u) {
@@ -1295,41 +1361,11 @@ static __device__ __noinline__ void fin_anyorder(const Job &j, int b)
     }
     const int wpos = lane < u ? __ldg(wp + lane) : 0x7FFFFFFF;
     const bool ret = lane < u && !((accd >> lane) & 1u) && wpos <= E;
-    // scores whose intervals overlap another retained score's are recomputed
-    // in fp64 (by the warp), so that the order below is exact
-    bool unsure = false;
-    for (int o = 0; o < 32; ++o) {
-        const double so = __shfl_sync(0xFFFFFFFFu, sc, o);
-        const bool ro = __shfl_sync(0xFFFFFFFFu, ret, o);
-        if (ret && ro && o != lane && fabs(sc - so) <= (sc + so) * e)
-            unsure = true;
-    }
-    unsigned um = __ballot_sync(0xFFFFFFFFu, unsure);
-    while (um) {
-        const int src = __ffs(um) - 1;
-        um &= um - 1;
-        const double c = conf64_row(j, row_ptr(j, b, j.K + src));
-        if (lane == src)
-            sc = c;
-    }
-    // rank of each retained position: decreasing score, ties by position
-    int rank = 0;
-    for (int o = 0; o < 32; ++o) {
-        const double so = __shfl_sync(0xFFFFFFFFu, sc, o);
-        const bool ro = __shfl_sync(0xFFFFFFFFu, ret, o);
-        if (ro && (so > sc || (so == sc && o < lane)))
-            ++rank;
-    }
-    const int nret = __popc(__ballot_sync(0xFFFFFFFFu, ret));
     if (lane < W) {
         j.next_draft[(int64_t)b * W + lane] = ret ? z : -1;
         if (j.confidence)
             j.confidence[(int64_t)b * W + lane] =
                 lane < u ? (float)sc : __int_as_float(0x7FC00000);
-        if (ret)
-            j.next_order[(int64_t)b * W + rank] = lane;
-        if (lane >= nret)
-            j.next_order[(int64_t)b * W + lane] = -1;
     }
     if (lane == 0) {
         j.acc[b] = h;
@@ -1385,9 +1421,12 @@ __device__ __forceinline__ void finish_unit(const Job &j, const UnitHead &mt, TS
     int am = s.amax;
     if (hasmax)
         warp_argmax(mx, am);
-    Cand2 g = s.g.c;
-    if (gum)
-        warp_cand2(g);
+    Cand2 g;
+    g.init();
+    if (gum) {
+        __syncwarp();
+        g = sm.gcand[w];
+    }
     const float xd = warp_max(s.xd);  // NaN except at one lane (fmaxf drops NaN)
     float E1 = -INFINITY, E2 = -INFINITY, S1 = 0.f, S2 = 0.f;
     if (lse) {
@@ -1585,241 +1624,13 @@ __device__ __forceinline__ void end_decisions(const Job &j, PassShared &sm)
         fin_kind<KIND>(j, sm.todo[i % kFinQ]);
 }
 
-// ---------------------------------------------------------------------------
-// Seeding of Gumbel units by the consumer threads.  Every top id of a unit's
-// id range is found (a couple of skip draws per block of 256 ids; threads take
-// blocks in turn and list the ids in shared memory), its logit is copied to
-// shared memory (cp.async, issued one unit ahead when the producer names the
-// next unit), and it is scored in an fp32 interval.  The top ids join the
-// candidates and the best lower end - 1e-9 starts the unit's shared
-// threshold; the consumers' scan then skips top ids.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async4(void *dst, const void *src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// The aligned 32-bit word that holds the logit of id v, and the logit in it.
-template <typename In>
-__device__ __forceinline__ const void *logit_word(const char *row, uint32_t v)
-{
-    return row + (sizeof(In) == 2 ? (((size_t)v * 2) & ~(size_t)3) : (size_t)v * 4);
-}
-template <typename In>
-__device__ __forceinline__ float logit_of_word(uint32_t w, uint32_t v)
-{
-    if (sizeof(In) == 2)
-        return __uint_as_float((v & 1u) ? (w & 0xFFFF0000u) : (w << 16));
-    return __uint_as_float(w);
-}
-
-// Barrier among the consumer warps on an mbarrier (kConsumerWarps arrivals)
-// with a bounded wait.  A hardware barrier would wait without end for a warp
-// that gave up after an expired wait; this one gives up too (latching
-// SV_ERR_TIMEOUT), and the CTA's abort flag then makes every later wait
-// return at once and the consumers leave the stream.  Every consumer thread
-// calls it; returns false when the barrier did not complete.  The mbarrier's
-// release / acquire order the consumers' shared-memory accesses around it.
-__device__ __noinline__ bool csync(PassShared &sm, const Job &j)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t ph = sm.cph[w];
-    __syncwarp();
-    if (lane == 0)
-        mbar_arrive(&sm.csync);
-    bool ok = false;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try(&sm.csync, ph)) {
-            ok = true;
-            break;
-        }
-        if (sm.abort)
-            break;
-        if (SV_SPIN_SLEEP_NS > 0 && i > 64)
-            __nanosleep(SV_SPIN_SLEEP_NS);
-    }
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    if (lane == 0) {
-        sm.cph[w] = ph ^ 1u;
-        if (!ok) {
-            latch(j.err, SV_ERR_TIMEOUT);
-            sm.abort = 1;
-        }
-    }
-    __syncwarp();
-    return ok;
-}
-
-// Lists the top ids of [lo, hi) in buffer b; false if they did not all fit
-// (the count is then larger than the list).  *listed receives the number of
-// ids in the list, the same in every thread.  Every consumer thread calls
-// it.  After a barrier that did not complete the list is left empty.
-__device__ __noinline__ bool seed_list(PassShared &sm, const Job &j, int b, uint64_t key, int lo,
-                                       int hi, int *listed)
-{
-    const int t = threadIdx.x;
-    *listed = 0;
-    if (t == 0)
-        sm.seed_n = 0;
-    if (!csync(sm, j)) {
-        if (t == 0)
-            sm.seed_cnt[b] = 0;
-        return true;
-    }
-    const uint32_t bhi = (uint32_t)(hi - 1) >> 8;
-    uint32_t beta = ((uint32_t)lo >> 8) + t;
-    int pos = -1, i = 0;
-    while (beta <= bhi) {
-        pos = next_top(key, beta, i++, pos, sm.skip);
-        const uint32_t v = beta * 256u + (uint32_t)pos;
-        if (pos > 255 || v >= (uint32_t)hi) {  // block done
-            beta += kConsumers;
-            pos = -1;
-            i = 0;
-        } else if (v >= (uint32_t)lo) {
-            const int idx = atomicAdd(&sm.seed_n, 1);
-            if (idx < kSeedCap)
-                sm.seed_ids[b][idx] = v;
-        }
-    }
-    const bool ok = csync(sm, j);
-    const int n = ok ? sm.seed_n : 0;
-    *listed = min(n, kSeedCap);
-    if (t == 0)
-        sm.seed_cnt[b] = min(n, kSeedCap);
-    return n <= kSeedCap;
-}
-
-// Starts the copies of the n listed ids' logit words into buffer b.
-template <typename In>
-__device__ __forceinline__ void seed_copy(PassShared &sm, int b, const char *row, int n)
-{
-    for (int e = threadIdx.x; e < n; e += kConsumers)
-        cp_async4(&sm.seed_x[b][e], logit_word<In>(row, sm.seed_ids[b][e]));
-    cp_async_commit();
-}
-
-// Scores buffer b (its copies must have been started) and starts the unit's
-// threshold.
-template <typename In>
-__device__ __noinline__ GState seed_eval(PassShared &sm, const Job &j, int b, GState g,
-                                         const RowMode &rm, int tslot)
-{
-    cp_async_wait_all();
-    const bool ok = csync(sm, j);  // every thread's copies have landed
-    const int n = ok ? min(max(sm.seed_cnt[b], 0), kSeedCap) : 0;
-    for (int e = threadIdx.x; e < n; e += kConsumers) {
-        const uint32_t v = sm.seed_ids[b][e];
-        const float2 iv = logit_interval_m(logit_of_word<In>(sm.seed_x[b][e], v), rm.invT,
-                                           fine52(rm.key, v), true);
-        g.c.add(iv.x, iv.y, (int)v);
-        if (iv.x > g.lomax) {
-            g.lomax = iv.x;
-            raise_thr(g, __fsub_rd(iv.x, 1e-9f));
-        }
-    }
-    atomicMax(&sm.thr[tslot], f2ord(g.thr));
-    if (csync(sm, j))
-        raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
-    return g;
-}
-
-// Seeding without a prefetched list: in rounds of at most kSeedCap ids,
-// loading the logits directly (the fallback for units with more top ids than
-// a list holds).
-template <typename In>
-__device__ __noinline__ GState seed_rounds(PassShared &sm, const Job &j, int b, const char *row,
-                                           int lo, int hi, GState g, const RowMode &rm, int tslot)
-{
-    using VT = VecTraits<In>;
-    constexpr uint32_t kNone = 0xFFFFFFFFu;
-    constexpr int kPer = (kSeedCap + kConsumers - 1) / kConsumers;
-    const int t = threadIdx.x;
-    const uint32_t bhi = (uint32_t)(hi - 1) >> 8;
-    uint32_t beta = ((uint32_t)lo >> 8) + t;
-    int pos = -1, i = 0;
-    bool more = beta <= bhi;
-    uint32_t pend = kNone;  // a top id found but not listed yet
-    for (;;) {
-        if (t == 0) {
-            sm.seed_n = 0;
-            sm.seed_more = 0;
-        }
-        if (!csync(sm, j))
-            return g;
-        for (;;) {
-            if (pend != kNone) {
-                const int idx = atomicAdd(&sm.seed_n, 1);
-                if (idx >= kSeedCap)
-                    break;  // the list is full: keep it for the next round
-                sm.seed_ids[b][idx] = pend;
-                pend = kNone;
-            }
-            if (!more)
-                break;
-            pos = next_top(rm.key, beta, i++, pos, sm.skip);
-            const uint32_t v = beta * 256u + (uint32_t)pos;
-            if (pos > 255 || v >= (uint32_t)hi) {  // block done
-                beta += kConsumers;
-                pos = -1;
-                i = 0;
-                more = beta <= bhi;
-            } else if (v >= (uint32_t)lo) {
-                pend = v;
-            }
-        }
-        if (more || pend != kNone)
-            sm.seed_more = 1;
-        if (!csync(sm, j))
-            return g;
-        const int n = min(sm.seed_n, kSeedCap);
-        uint32_t id[kPer];
-        float x[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int e = t + k * kConsumers;
-            id[k] = e < n ? sm.seed_ids[b][e] : kNone;
-            x[k] = id[k] != kNone ? VT::load1(row, (int)id[k]) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k)
-            if (id[k] != kNone) {
-                const float2 iv =
-                    logit_interval_m(x[k], rm.invT, fine52(rm.key, id[k]), true);
-                g.c.add(iv.x, iv.y, (int)id[k]);
-                if (iv.x > g.lomax) {
-                    g.lomax = iv.x;
-                    raise_thr(g, __fsub_rd(iv.x, 1e-9f));
-                }
-            }
-        const int again = sm.seed_more;
-        if (!csync(sm, j))  // the list is reused by the next round
-            return g;
-        if (!again)
-            break;
-    }
-    atomicMax(&sm.thr[tslot], f2ord(g.thr));
-    if (csync(sm, j))
-        raise_thr(g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
-    return g;
-}
-
 // Streams one unit whose first stage is ready in `stage`: every stage of the
 // unit with the row mode fixed at compile time, then the unit's partial.
 // Returns false if a wait timed out or the producer aborted.
 template <typename In, int MODE>
 __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned char *stages,
                                           const float *gt, int &stage, uint32_t &phase,
-                                          const RowMode &rm, int &pf_next)
+                                          const RowMode &rm)
 {
     const int lane = threadIdx.x & 31;
     const StageMeta &m0 = sm.meta[stage];
@@ -1827,33 +1638,13 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
     const int tslot = uh.lu % kStages;
     TState s;
     tstate_init(s);
-    constexpr int E = VecTraits<In>::N;
-    // pf_next: (record << 1 | buffer) of the unit whose top ids were listed
-    // and copied a unit ago, or -1.  Residual units may stream between a unit
-    // and the one it prefetched for, so the buffer travels with the record.
-    const bool pre = pf_next >= 0 && (pf_next >> 1) == uh.unit;
-    const int sb = pre ? (pf_next & 1) : (pf_next >= 0 ? (pf_next & 1) ^ 1 : 0);
-    int listed = 0;
+    // a Gumbel-max row starts from the threshold of its top ids, scored
+    // before the stream (the screen below skips them)
+    const float gmax = (MODE & M_GUMBEL) ? g_ordinary_max(gt) : 0.f;
     if (MODE & M_GUMBEL) {
-        if (pre) {
-            s.g = seed_eval<In>(sm, j, sb, s.g, rm, tslot);  // listed and copied a unit ago
-        } else if (seed_list(sm, j, sb, rm.key, m0.vbase * E, m0.vend * E, &listed)) {
-            seed_copy<In>(sm, sb, m0.row, listed);
-            s.g = seed_eval<In>(sm, j, sb, s.g, rm, tslot);
-        } else {
-            s.g = seed_rounds<In>(sm, j, sb, m0.row, m0.vbase * E, m0.vend * E, s.g, rm, tslot);
-        }
-    }
-    if (m0.nrec >= 0) {
-        // the next unit carries a Gumbel-max: list its top ids and start
-        // their copies now, so that they land while this unit streams
-        const int nb = sb ^ 1;
-        const bool fits = seed_list(sm, j, nb, m0.nkey, m0.nlo, m0.nhi, &listed);
-        if (fits)
-            seed_copy<In>(sm, nb, m0.nrow, listed);
-        pf_next = fits ? (m0.nrec << 1) | nb : -1;  // the same on every consumer thread
-    } else {
-        pf_next = -1;
+        raise_thr(s.g, rm.thr0);
+        if (lane == 0)
+            sm.gcand[threadIdx.x >> 5].init();
     }
     for (;;) {
         const StageMeta &mt = sm.meta[stage];
@@ -1861,7 +1652,7 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
         const uint4 *st = reinterpret_cast<const uint4 *>(stages + (size_t)stage * kStageBytes);
         if (MODE & M_GUMBEL)
             raise_thr(s.g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
-        do_chunk<In, MODE>(st, nv, vbase, s, rm, gt, sm);
+        do_chunk<In, MODE>(st, nv, vbase, s, rm, gmax, gt, sm);
         if (uh.xid >= 0) {
             // the thread that holds the draft token's vector records its logit
             constexpr int E = VecTraits<In>::N;
@@ -1891,7 +1682,7 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
     }
     if ((MODE & M_GUMBEL) && s.gqn > 0) {
         const int w = threadIdx.x >> 5;
-        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqv[w], s.gqn, s.g, rm, gt, sm.skip);
+        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqv[w], s.gqn, s.g, rm, gt, sm.skip, &sm.gcand[w]);
         s.gqn = 0;
     }
     finish_unit(j, uh, s, rm, sm);
@@ -1902,41 +1693,40 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
 template <typename In, int KIND>
 __device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsigned char *stages,
                                               const float *gt, int &stage, uint32_t &phase,
-                                              const RowMode &rm, int &pf_next)
+                                              const RowMode &rm)
 {
     const int m = rm.mode;
     if constexpr (KIND == K_GREEDY) {
-        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
     } else if constexpr (KIND == K_SAMPLE) {
         if (m & M_GUMBEL)
-            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
-        return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
     } else if constexpr (KIND == K_TREE) {
         if (m & M_GUMBEL)
-            return unit_loop<In, M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
-        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
     } else if constexpr (KIND == K_ANYORDER) {
         if (m & M_LSE)
-            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
-        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
     } else if constexpr (KIND == K_SPOT) {
         if (m & M_GUMBEL)
-            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm,
-                                                           pf_next);
-        return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm);
+        return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm);
     } else {
         switch (m) {
-        case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
-        case M_LSE: return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
+        case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
+        case M_LSE: return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
         case M_LSE | M_GUMBEL:
-            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
         case M_ARGMAX | M_LSE:
-            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm);
         case M_GUMBEL | M_LSE | M_MAX:
-            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm, pf_next);
+            return unit_loop<In, M_GUMBEL | M_LSE | M_MAX>(j, sm, stages, gt, stage, phase, rm);
         default:
             return unit_loop<In, M_GUMBEL | M_LSE | M_LSE2 | M_MAX>(j, sm, stages, gt, stage,
-                                                                     phase, rm, pf_next);
+                                                                     phase, rm);
         }
     }
 }
@@ -2027,11 +1817,6 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             mbar_init(&sm.plan_full[q], 1);
             mbar_init(&sm.plan_empty[q], 1);
         }
-        mbar_init(&sm.csync, kConsumerWarps);
-        for (int w = 0; w < kConsumerWarps; ++w)
-            sm.cph[w] = 0u;
-        sm.seed_cnt[0] = sm.seed_cnt[1] = 0;
-        sm.seed_n = 0;
         sm.abort = 0;
         sm.nunits = 0;
         sm.prod_done = 0;
@@ -2065,7 +1850,6 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             uint32_t pend = 0, pend_par = 0;  // stages with a copy not yet re-acquired
             int lu = 0;                       // local unit number
             bool ok = true;
-            const int E = j.dtype == SV_BF16 ? 8 : 4;
             for (long long pi = 0;; ++pi) {
                 const int q = (int)(pi % kPlanQ);
                 if (!mbar_wait(&sm.plan_full[q], (uint32_t)((pi / kPlanQ) & 1))) {
@@ -2075,14 +1859,7 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
                 const PlanEntry &ce = sm.plan[q];
                 if (ce.kind < 0)
                     break;
-                // The next entry only if it is already queued: waiting for it
-                // here could wait on a decision that needs this very unit.
-                const int q1 = (int)((pi + 1) % kPlanQ);
-                const bool have_next =
-                    mbar_test(&sm.plan_full[q1], (uint32_t)(((pi + 1) / kPlanQ) & 1));
-                const PlanEntry &ne = sm.plan[q1];
                 const int step = kStageVecs;
-                const bool nseed = have_next && ne.kind == 0 && (ne.rm.mode & M_GUMBEL);
                 for (int v = ce.vs; v < ce.ve; v += step) {
                     const int nv = min(step, ce.ve - v);
                     if (!mbar_wait(&sm.empty[stage], phase ^ 1u)) {
@@ -2101,19 +1878,9 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
                     mt.expect = ce.expect;
                     mt.xid = ce.xid;
                     mt.row = ce.row;
-                    mt.vend = ce.ve;
                     mt.rm = ce.rm;
-                    mt.nrec = -1;
-                    if (v == ce.vs) {
+                    if (v == ce.vs)
                         sm.thr[lu % kStages] = f2ord(-INFINITY);
-                        if (nseed) {
-                            mt.nrec = ne.rec;
-                            mt.nrow = ne.row;
-                            mt.nkey = ne.rm.key;
-                            mt.nlo = ne.vs * E;
-                            mt.nhi = ne.ve * E;
-                        }
-                    }
                     mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
                     bulk_g2s(stages + (size_t)stage * kStageBytes, ce.row + (int64_t)v * 16,
                              (uint32_t)nv * 16u, &sm.full[stage]);
@@ -2155,7 +1922,6 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         // ---------------- consumer warps ----------------
         int stage = 0;
         uint32_t phase = 0;
-        int pf_next = -1;  // (record << 1 | buffer) of a unit whose top ids were prefetched
         for (;;) {
             if (!mbar_wait(&sm.full[stage], phase)) {
                 latch(j.err, SV_ERR_TIMEOUT);
@@ -2164,10 +1930,9 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             if (sm.meta[stage].unit < 0 || sm.abort)
                 break;
             const RowMode rm = sm.meta[stage].rm;
-            if (!unit_dispatch<In, KIND>(j, sm, stages, gt, stage, phase, rm, pf_next))
+            if (!unit_dispatch<In, KIND>(j, sm, stages, gt, stage, phase, rm))
                 break;
         }
-        cp_async_wait_all();  // no copy may be in flight when the CTA exits
     }
     __syncthreads();
     end_decisions<KIND>(j, sm);
@@ -2247,6 +2012,154 @@ static cudaError_t launch_in(const Job &j, int grid, cudaStream_t s)
     case K_ANYORDER: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_ANYORDER>, j);
     default: return cudaLaunchKernelEx(&cfg, pass_kernel<In, K_PACKED>, j);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Seed kernel.  Before the stream, every top id (an id whose uniform lies in
+// the top 1/256, about one per block of 256 ids) of every Gumbel-max row of
+// the call is found by its skip draws, its logit is loaded, and it is scored
+// in an fp32 interval.  One warp takes one chunk of seed_bpw blocks of one
+// row and writes the chunk's seed record: the best lower end - 1e-9 (a
+// threshold no winner can fall below) and the chunk's candidates.
+//
+// The warp first lists the chunk's top ids in shared memory: each lane walks
+// one block a draw at a time and, when its block ends, takes the next block
+// of the chunk, so that the lanes stay busy although blocks hold different
+// numbers of top ids; new ids are appended with a ballot.  The list is then
+// scored with every lane converged, two ids a lane with both logit loads in
+// flight.  Warps never wait for one another, so the kernel runs at full
+// occupancy; the streaming pass starts every Gumbel-max unit from its row's
+// threshold and skips top ids, and the decision step merges the seed records
+// into the row's candidates.
+// ---------------------------------------------------------------------------
+constexpr int kSeedThreads = 256;
+constexpr int kSeedList = 64;  // listed top ids a warp scores at once (two a lane)
+
+template <typename In>
+__device__ __forceinline__ void seed_score(const uint32_t *ids, int n, const char *row,
+                                           const RowMode &rm, Cand2 &c, float &lomax)
+{
+    using VT = VecTraits<In>;
+    const int lane = threadIdx.x & 31;
+    const bool a = lane < n, b = lane + 32 < n;
+    const uint32_t va = a ? ids[lane] : 0u, vb = b ? ids[lane + 32] : 0u;
+    const float xa = a ? VT::load1(row, (int)va) : 0.f;
+    const float xb = b ? VT::load1(row, (int)vb) : 0.f;
+    if (a) {
+        const float2 iv = logit_interval_m(xa, rm.invT, fine52(rm.key, va), true);
+        c.add(iv.x, iv.y, (int)va);
+        lomax = fmaxf(lomax, iv.x);
+    }
+    if (b) {
+        const float2 iv = logit_interval_m(xb, rm.invT, fine52(rm.key, vb), true);
+        c.add(iv.x, iv.y, (int)vb);
+        lomax = fmaxf(lomax, iv.x);
+    }
+}
+
+template <typename In>
+__global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constant__ Job j)
+{
+    __shared__ uint64_t skip[kSkipN];
+    __shared__ uint32_t idl[kSeedThreads / 32][kSeedList];
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < kSkipN; i += blockDim.x)
+        skip[i] = __ldg(j.skip + i);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    constexpr int kWarps = kSeedThreads / 32;
+    const int H = gumbel_rows(j);
+    const uint32_t nblk = ((uint32_t)j.V + 255u) >> 8;
+    const long long items = (long long)j.B * H * j.seed_chunks;
+    uint32_t *ids = idl[wl];
+    for (long long it = (long long)blockIdx.x * kWarps + wl; it < items;
+         it += (long long)gridDim.x * kWarps) {
+        const int chunk = (int)(it % j.seed_chunks);
+        const long long g = it / j.seed_chunks;
+        const int b = (int)(g / H), k = (int)(g % H);
+        const int n = clamp_len(j, b);
+        const int slot = gumbel_slot(j, k, n);
+        bool valid = true;
+        int np = 0;
+        if (j.kind == K_SPOT)
+            valid = ((__ldg(j.smask + (int64_t)b * (j.N + 1) + slot / j.L) >> (slot % j.L)) &
+                     1ull) != 0;
+        if (j.kind == K_TREE)
+            np = __ldg(j.node_pos + (int64_t)b * j.N + slot);
+        SeedRec r;
+        r.thr = r.hi1 = r.lo1 = r.hi2 = r.lo2 = r.hi3 = -INFINITY;
+        r.v1 = r.v2 = -1;
+        if (valid) {  // warp-uniform
+            const RowMode rm = row_mode(j, b, slot, n, pos0_of(j, b), np);
+            const char *row = slot_row(j, b, slot);
+            Cand2 c;
+            c.init();
+            float lomax = -INFINITY;
+            const uint32_t b0 = (uint32_t)chunk * (uint32_t)j.seed_bpw;
+            const uint32_t bend = min(b0 + (uint32_t)j.seed_bpw, nblk);
+            uint32_t nextb = b0 + 32u;  // next block to hand out (warp-uniform)
+            uint32_t beta = b0 + (uint32_t)lane;
+            bool act = beta < bend;
+            int pos = -1, i = 0, cnt = 0;
+            // Each draw moves its lane's offset up by at least one, so a block
+            // ends within 257 draws and the loop within 257 * seed_bpw trips.
+            while (__any_sync(0xFFFFFFFFu, act)) {
+                bool got = false, done = false;
+                uint32_t v = 0u;
+                if (act) {
+                    pos = next_top(rm.key, beta, i++, pos, skip);
+                    v = beta * 256u + (uint32_t)pos;
+                    got = pos <= 255 && v < (uint32_t)j.V;
+                    done = !got;
+                }
+                const unsigned gm = __ballot_sync(0xFFFFFFFFu, got);
+                if (got)
+                    ids[cnt + __popc(gm & lt)] = v;
+                cnt += __popc(gm);
+                const unsigned dm = __ballot_sync(0xFFFFFFFFu, done);
+                if (done) {
+                    beta = nextb + (uint32_t)__popc(dm & lt);
+                    act = beta < bend;
+                    pos = -1;
+                    i = 0;
+                }
+                nextb += (uint32_t)__popc(dm);
+                if (cnt > kSeedList - 32) {  // room for one more trip's ids
+                    __syncwarp();
+                    seed_score<In>(ids, cnt, row, rm, c, lomax);
+                    __syncwarp();
+                    cnt = 0;
+                }
+            }
+            __syncwarp();
+            if (cnt > 0)
+                seed_score<In>(ids, cnt, row, rm, c, lomax);
+            __syncwarp();
+            warp_cand2(c);
+            lomax = warp_max(lomax);
+            r.thr = lomax > -INFINITY ? __fsub_rd(lomax, 1e-9f) : -INFINITY;
+            r.hi1 = c.hi1;
+            r.lo1 = c.lo1;
+            r.hi2 = c.hi2;
+            r.lo2 = c.lo2;
+            r.hi3 = c.hi3;
+            r.v1 = c.v1;
+            r.v2 = c.v2;
+        }
+        if (lane == 0)
+            j.seeds[it] = r;
+    }
+}
+
+cudaError_t seed_launch(const Job &j, int grid, cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    pdl_config(cfg, at, dim3(grid), dim3(kSeedThreads), 0, s);
+    return j.dtype == SV_BF16 ? cudaLaunchKernelEx(&cfg, seed_kernel<uint16_t>, j)
+                              : cudaLaunchKernelEx(&cfg, seed_kernel<float>, j);
 }
 
 // SPOT preparation, one thread per tree: the masked positions of every state
@@ -2351,7 +2264,6 @@ __global__ void __launch_bounds__(128) anyorder_prep_kernel(const __grid_constan
             j.commit_pos[(int64_t)b * W + i] = -1;
             j.commit_tok[(int64_t)b * W + i] = -1;
             j.next_draft[(int64_t)b * W + i] = -1;
-            j.next_order[(int64_t)b * W + i] = -1;
             if (j.confidence) j.confidence[(int64_t)b * W + i] = __int_as_float(0x7FC00000);
         }
     }

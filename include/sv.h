@@ -320,8 +320,8 @@ sv_status sv_packed_step(sv_handle *h, const void *logits, sv_dtype dtype, int64
  *   next_draft [B, W] (argmax of proposal row i at window positions that
  *   stay unresolved and <= E, else -1), score [B, W] (optional: the
  *   probability at temperature 1 of each proposal row's argmax, NaN beyond
- *   u), next_order [B, W] (the window indices with a next draft, by
- *   decreasing score, ties by position; -1 padded).
+ *   u; the confidence scores by which a caller's order policy ranks the
+ *   next window, App. E.6).
  * Errors: SV_ERR_INVALID_ARG; latched SV_ERR_DEVICE_BOUNDS for u outside
  *   [0, W], an order that is not a permutation, or min(kappa + 1, u) > Kv.
  * ------------------------------------------------------------------------- */
@@ -331,15 +331,17 @@ sv_status sv_packed_anyorder_step(sv_handle *h, const void *logits, sv_dtype dty
                                   const int32_t *draft, const int32_t *end_pos, int32_t eos_id,
                                   int32_t *accept_len, int32_t *commit_len, int32_t *commit_pos,
                                   int32_t *commit_tok, int32_t *end_out, int32_t *next_draft,
-                                  float *score, int32_t *next_order, void *stream);
+                                  float *score, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Options (testing and measurement).
  *   SV_OPT_FORCE_RESCUE (value 0/1): decide every sampled sequence on the
  *     fp64 path, as if every fast decision fell inside its error bound.
  *   SV_OPT_TIMING_EVENTS: value is a pointer to two cudaEvent_t (start, stop)
- *     recorded around the streaming kernel of the next calls (0 = off);
- *     the events stay owned by the caller.
+ *     recorded around the streaming pass of the next calls, together with
+ *     the kernels that prepare it (SPOT state masks, any-order preparation,
+ *     the seed records of Gumbel-max rows); 0 = off.  The events stay owned
+ *     by the caller.
  * ------------------------------------------------------------------------- */
 typedef enum { SV_OPT_FORCE_RESCUE = 1, SV_OPT_TIMING_EVENTS = 2 } sv_option;
 sv_status sv_set_option(sv_handle *h, sv_option opt, int64_t value);

@@ -348,8 +348,7 @@ def test_spot_position_not_masked_is_latched(dbv):
 
 # ------------------------------------------------------------------ any-order Packed-SS
 
-AO_KEYS = ("accept_len", "commit_len", "commit_pos", "commit_tok", "end_pos", "next_draft",
-           "next_order")
+AO_KEYS = ("accept_len", "commit_len", "commit_pos", "commit_tok", "end_pos", "next_draft")
 
 
 def _anyorder_both(dbv, ai, Kv, W, eos=-1, end=None):
@@ -376,22 +375,14 @@ def test_anyorder_parity(dbv, dtype, B, Kv, W, V, ragged, p_draft):
                                  ragged=ragged)
     out, ref = _anyorder_both(dbv, ai, Kv, W)
     _compare_anyorder(out, ref, dtype)
-    # an accepted EOS cuts the end: the first accepted token becomes EOS
+    # an accepted EOS lowers the end: the first accepted token of sequence 0
+    # becomes EOS (window positions lie in 1..4W, so every pair was within
+    # the end before)
     eos = int(ref["commit_tok"][0, 0])
-    end = torch.full((B,), 3 * W, dtype=torch.int32)
-    out, ref = _anyorder_both(dbv, ai, Kv, W, eos=eos, end=end)
+    first = int(ref["commit_pos"][0, 0])
+    out, ref = _anyorder_both(dbv, ai, Kv, W, eos=eos)
     _compare_anyorder(out, ref, dtype)
-    assert ref["end_pos"][0] <= ref["commit_pos"][0, 0]
-
-
-def test_anyorder_ties_in_scores(dbv):
-    """Equal proposal rows give equal scores: the retained positions keep
-    their textual order among themselves."""
-    ai = datagen.anyorder_inputs(3, 4, 4, 1024, dtype="bf16", seed=9, p_draft=0.0)
-    ai.logits[:, 4:] = ai.logits[:, 4:5]
-    out, ref = _anyorder_both(dbv, ai, 4, 4)
-    _compare_anyorder(out, ref, "bf16")
-    assert cpu(out["next_order"])[0, :3].tolist() == [1, 2, 3]
+    assert ref["end_pos"][0] <= first
 
 
 @pytest.mark.parametrize("which", ["not_a_permutation", "too_few_rows"])
