@@ -273,7 +273,7 @@ static __device__ __noinline__ bool cactus_bracket_fast(double plo, double phi, 
     double d1, sc;
     bool ok_lo, ok_hi;
     if (!(plo > 0.0) || !(delta > 0.0) || delta >= -log(plo)) {
-        double a, b;
+        double a;
         ok_lo = cactus_bracket(plo, delta, glo, &a);
     } else {
         *glo = fmax(plo, (double)cactus_newton32((float)plo, (float)delta) * (1.0 - 0x1p-14));

@@ -528,8 +528,9 @@ struct VecTraits<float> {
 // Relative error bounds of exp(L) for a row log-sum-exp L computed in fp32.
 //
 // Streaming kernel.  Terms are t = 2^fl(x c - e), one FFMA and one ex2 each,
-// with an integer reference e; a chunk whose partial sum reaches 2^20 moves
-// the reference up, so every exponent a = x c - e stays below kLseCap + 1.
+// with an integer reference e; a chunk whose max would give a term of 2^20
+// or more first moves the reference up, so every exponent a = x c - e stays
+// below kLseCap + 1.
 // Moves between references are exact powers of two.  With c = fl32(c*),
 // c* = log2(e)/T, the row's value is reported as E c*/c + log2 S (E the
 // reference of S), which leaves per term an exponent error of at most

@@ -498,43 +498,36 @@ __device__ __forceinline__ float2 lse_terms(const Chunk &q, float c, float e)
     return part;
 }
 
-// Adds the chunk to one log-sum-exp accumulator.  The first chunk with an
-// element sets the reference to its max, rounded up to an integer; later, a
-// partial sum of 2^20 or more moves the reference up to the chunk max and
-// rescales the accumulator exactly.
+// Adds the chunk to one log-sum-exp accumulator, given the chunk max cm.
+// The first chunk with an element sets the reference e to ceil(cm c); a later
+// chunk whose max would give a term of 2^20 or more (ceil(cm c) > e + 20)
+// first moves the reference up to ceil(cm c) and rescales the accumulator
+// exactly.  Every term's exponent x c - e thus stays below kLseCap + 1, and
+// the test needs only the chunk max, so the warp does not wait on the sum
+// before going on.
 template <typename In>
-__device__ __forceinline__ void lse_chunk(const Chunk &q, float c, float &e, float2 &acc)
+__device__ __forceinline__ void lse_chunk(const Chunk &q, float c, float cm, float &e,
+                                          float2 &acc)
 {
-    if (e == -INFINITY) {
-        const float cm = chunk_max<In>(q);
-        if (cm == -INFINITY)
-            return;  // no element yet
-        e = ceilf(__fmul_ru(cm, c));
-    }
-    float2 part = lse_terms<In>(q, c, e);
-    if (!(part.x + part.y < 0x1p20f)) {
-        const float cm = chunk_max<In>(q);
-        if (cm == -INFINITY) {
-            part = make_float2(0.f, 0.f);
-        } else {
-            const float en = fmaxf(e, ceilf(__fmul_ru(cm, c)));
-            if (e > -INFINITY) {
-                const float sc = pow2_int(e - en);
-                acc.x *= sc;
-                acc.y *= sc;
-            }
-            e = en;
-            part = lse_terms<In>(q, c, e);
+    if (cm == -INFINITY)
+        return;  // nothing but padding
+    const float ec = ceilf(__fmul_ru(cm, c));
+    if (!(ec <= e + kLseCap)) {  // the first chunk (e = -inf) or a new, larger max
+        if (e > -INFINITY) {
+            const float sc = pow2_int(e - ec);
+            acc.x *= sc;
+            acc.y *= sc;
         }
+        e = ec;
     }
-    acc = add2(acc, part);
+    acc = add2(acc, lse_terms<In>(q, c, e));
 }
 
 // Running max, and with ARG its lowest index: the first vector whose max is
 // the chunk max, then the first element of it that equals it (predicated
 // selects, no search loop).
 template <typename In, bool ARG>
-__device__ __forceinline__ void max_chunk(const Chunk &q, int vbase, TState &s)
+__device__ __forceinline__ float max_chunk(const Chunk &q, int vbase, TState &s)
 {
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
@@ -563,6 +556,7 @@ __device__ __forceinline__ void max_chunk(const Chunk &q, int vbase, TState &s)
         s.amax = (vbase + (int)threadIdx.x + kk * kConsumers) * E + ii;
     }
     s.mx = fmaxf(s.mx, cm);
+    return cm;
 }
 
 // Per-id screen of the queued vectors, 32 at a time, a vector per lane: its
@@ -649,12 +643,15 @@ __device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, i
 {
     Chunk q;
     load_chunk<In>(st, nv, q);
+    float cm = -INFINITY;
     if (MODE & (M_ARGMAX | M_MAX))
-        max_chunk<In, (MODE & M_ARGMAX) != 0>(q, vbase, s);
+        cm = max_chunk<In, (MODE & M_ARGMAX) != 0>(q, vbase, s);
+    else if (MODE & M_LSE)
+        cm = chunk_max<In>(q);
     if (MODE & M_LSE)
-        lse_chunk<In>(q, rm.c1, s.e1, s.acc1);
+        lse_chunk<In>(q, rm.c1, cm, s.e1, s.acc1);
     if (MODE & M_LSE2)
-        lse_chunk<In>(q, rm.c2, s.e2, s.acc2);
+        lse_chunk<In>(q, rm.c2, cm, s.e2, s.acc2);
     if (MODE & M_GUMBEL)
         gumbel_chunk<In>(q, vbase, s, rm, gmax, gt, sm.skip, sm);
 }
