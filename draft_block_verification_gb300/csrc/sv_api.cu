@@ -36,6 +36,7 @@ struct sv_handle {
     int *d_err = nullptr;
     unsigned *d_ctl = nullptr;
     float *d_gtab = nullptr;      // [kGTab] G bounds of ordinary ids
+    float *d_gtop = nullptr;      // [kGTab] G bounds of top ids
     uint64_t *d_skip = nullptr;   // [kSkipN] skip thresholds
     char *ws = nullptr;
     size_t ws_bytes = 0;
@@ -90,6 +91,15 @@ void gumbel_bound_table(float *t)
 {
     for (int c = 0; c < kGTab; ++c)
         t[c] = up_f32(-log(-log((double)(c + 1) * 255.0 / 65536.0)));
+}
+
+// The same for top ids: w < (c + 1)/256 gives 1 - u = (1 - w)/256 >
+// (255 - c)/65536.  The last byte (w up to 1) has no finite bound.
+void gumbel_top_bound_table(float *t)
+{
+    for (int c = 0; c < kGTab - 1; ++c)
+        t[c] = up_f32(-log(-log1p(-(double)(255 - c) / 65536.0)));
+    t[kGTab - 1] = INFINITY;
 }
 
 // Skip thresholds C_g = ceil(2^64 (255/256)^g), g = 1..256 (entry 0 unused):
@@ -235,6 +245,7 @@ void fill_common(Job &j, sv_handle *h, const void *src0, sv_dtype dt, int64_t rs
     j.err = h->d_err;
     j.ctl = h->d_ctl;
     j.gtab = h->d_gtab;
+    j.gtop = h->d_gtop;
     j.skip = h->d_skip;
     j.force_rescue = h->force_rescue;
     j.c1 = 1.4426950408889634f;
@@ -371,6 +382,7 @@ sv_status sv_create(sv_handle **out)
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_ctl, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_gtab, kGTab * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_gtop, kGTab * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_skip, kSkipN * sizeof(uint64_t));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_ctl, 0, C_NCTL * sizeof(unsigned));
@@ -378,6 +390,8 @@ sv_status sv_create(sv_handle **out)
         float t[kGTab];
         gumbel_bound_table(t);
         e = cudaMemcpy(h->d_gtab, t, sizeof t, cudaMemcpyHostToDevice);
+        gumbel_top_bound_table(t);
+        if (e == cudaSuccess) e = cudaMemcpy(h->d_gtop, t, sizeof t, cudaMemcpyHostToDevice);
         uint64_t c[kSkipN];
         skip_table(c);
         if (e == cudaSuccess) e = cudaMemcpy(h->d_skip, c, sizeof c, cudaMemcpyHostToDevice);
@@ -399,6 +413,7 @@ sv_status sv_destroy(sv_handle *h)
     if (h->d_err) cudaFree(h->d_err);
     if (h->d_ctl) cudaFree(h->d_ctl);
     if (h->d_gtab) cudaFree(h->d_gtab);
+    if (h->d_gtop) cudaFree(h->d_gtop);
     if (h->d_skip) cudaFree(h->d_skip);
     delete h;
     return SV_OK;

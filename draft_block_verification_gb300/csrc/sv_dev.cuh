@@ -211,6 +211,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Asynchronous 4-byte copy from global to shared memory (both addresses
+// 4-byte aligned), completed by cp_async_wait_all.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Programmatic dependent launch (sm_90+).  pdl_wait blocks until the kernel
 // that precedes this one in the stream has completed and its writes are
 // visible (a no-op for a kernel launched without the attribute); every

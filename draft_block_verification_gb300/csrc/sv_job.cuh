@@ -130,6 +130,7 @@ struct Job {
     unsigned *svalid;   // SPOT, any-order: rows to stream per sequence [B]
     int *err;
     const float *gtab;     // [kGTab] G bounds of ordinary ids
+    const float *gtop;     // [kGTab] G bounds of top ids (the seed kernel's screen)
     const uint64_t *skip;  // [kSkipN] skip thresholds of the top-id draws
 };
 

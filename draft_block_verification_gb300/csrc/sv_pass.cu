@@ -2022,35 +2022,76 @@ static cudaError_t launch_in(const Job &j, int grid, cudaStream_t s)
 // The warp first lists the chunk's top ids in shared memory: each lane walks
 // one block a draw at a time and, when its block ends, takes the next block
 // of the chunk, so that the lanes stay busy although blocks hold different
-// numbers of top ids; new ids are appended with a ballot.  The list is then
-// scored with every lane converged, two ids a lane with both logit loads in
-// flight.  Warps never wait for one another, so the kernel runs at full
-// occupancy; the streaming pass starts every Gumbel-max unit from its row's
-// threshold and skips top ids, and the decision step merges the seed records
-// into the row's candidates.
+// numbers of top ids; new ids are appended with a ballot, and each listed
+// id's logit is copied to shared memory asynchronously while the draws go
+// on.  The list is then scored with every lane converged, two ids a lane: an
+// id is bounded by its logit and the top byte of its fine bits (a table of G
+// bounds for top ids), and only ids whose bound reaches the warp's threshold
+// get the fp32 interval.  Warps never wait for one another; the streaming
+// pass starts every Gumbel-max unit from its row's threshold and skips top
+// ids, and the decision step merges the seed records into the row's
+// candidates.
 // ---------------------------------------------------------------------------
 constexpr int kSeedThreads = 256;
 constexpr int kSeedList = 64;  // listed top ids a warp scores at once (two a lane)
 
+// Queues the copy of id v's logit into *xw: the 4-byte word that holds it
+// (a bf16 pair, or the fp32 value).  The pair's other element lies in the row
+// unless v is the row's last element with an even index; that one is loaded
+// directly.
 template <typename In>
-__device__ __forceinline__ void seed_score(const uint32_t *ids, int n, const char *row,
-                                           const RowMode &rm, Cand2 &c, float &lomax)
+__device__ __forceinline__ void seed_fetch(const char *row, uint32_t v, uint32_t V, uint32_t *xw)
 {
-    using VT = VecTraits<In>;
-    const int lane = threadIdx.x & 31;
-    const bool a = lane < n, b = lane + 32 < n;
-    const uint32_t va = a ? ids[lane] : 0u, vb = b ? ids[lane + 32] : 0u;
-    const float xa = a ? VT::load1(row, (int)va) : 0.f;
-    const float xb = b ? VT::load1(row, (int)vb) : 0.f;
-    if (a) {
-        const float2 iv = logit_interval_m(xa, rm.invT, fine52(rm.key, va), true);
-        c.add(iv.x, iv.y, (int)va);
-        lomax = fmaxf(lomax, iv.x);
+    if (sizeof(In) == 4) {
+        cp_async4(xw, row + (size_t)v * 4);
+    } else if ((v | 1u) < V) {
+        cp_async4(xw, row + (size_t)(v & ~1u) * 2);
+    } else {
+        *xw = (uint32_t)__ldg((const unsigned short *)row + v) << ((v & 1u) * 16);
     }
-    if (b) {
-        const float2 iv = logit_interval_m(xb, rm.invT, fine52(rm.key, vb), true);
-        c.add(iv.x, iv.y, (int)vb);
-        lomax = fmaxf(lomax, iv.x);
+}
+
+template <typename In>
+__device__ __forceinline__ float seed_logit(uint32_t w, uint32_t v)
+{
+    if (sizeof(In) == 4)
+        return __uint_as_float(w);
+    return __uint_as_float((v & 1u) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// One id of the list: screened against the lane's threshold with the
+// top-id table, else scored.
+__device__ __forceinline__ void seed_one(uint32_t v, float x, const RowMode &rm,
+                                         const float *gtop, Cand2 &c, float &thr, float &thrS)
+{
+    const uint64_t m = fine52(rm.key, v);
+    if (!(fmaf(x, rm.invT, gtop[(int)(m >> 44)]) > thrS))
+        return;  // cannot reach the threshold
+    const float2 iv = logit_interval_m(x, rm.invT, m, true);
+    c.add(iv.x, iv.y, (int)v);
+    const float t = __fsub_rd(iv.x, 1e-9f);
+    if (t > thr) {
+        thr = t;
+        thrS = level1_thr(t);
+    }
+}
+
+template <typename In>
+__device__ __forceinline__ void seed_score(const uint32_t *ids, const uint32_t *xw, int n,
+                                           const RowMode &rm, const float *gtop, Cand2 &c,
+                                           float &thr, float &thrS)
+{
+    const int lane = threadIdx.x & 31;
+    if (lane < n)
+        seed_one(ids[lane], seed_logit<In>(xw[lane], ids[lane]), rm, gtop, c, thr, thrS);
+    if (lane + 32 < n)
+        seed_one(ids[lane + 32], seed_logit<In>(xw[lane + 32], ids[lane + 32]), rm, gtop, c,
+                 thr, thrS);
+    // every lane leaves with the warp's best threshold
+    const float t = warp_max(thr);
+    if (t > thr) {
+        thr = t;
+        thrS = level1_thr(t);
     }
 }
 
@@ -2058,11 +2099,15 @@ template <typename In>
 __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constant__ Job j)
 {
     __shared__ uint64_t skip[kSkipN];
+    __shared__ float gtop[kGTab];
     __shared__ uint32_t idl[kSeedThreads / 32][kSeedList];
+    __shared__ uint32_t xwl[kSeedThreads / 32][kSeedList];
     pdl_wait();
     pdl_trigger();
     for (int i = threadIdx.x; i < kSkipN; i += blockDim.x)
         skip[i] = __ldg(j.skip + i);
+    for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
+        gtop[i] = __ldg(j.gtop + i);
     __syncthreads();
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const unsigned lt = (1u << lane) - 1u;
@@ -2071,6 +2116,7 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
     const uint32_t nblk = ((uint32_t)j.V + 255u) >> 8;
     const long long items = (long long)j.B * H * j.seed_chunks;
     uint32_t *ids = idl[wl];
+    uint32_t *xw = xwl[wl];
     for (long long it = (long long)blockIdx.x * kWarps + wl; it < items;
          it += (long long)gridDim.x * kWarps) {
         const int chunk = (int)(it % j.seed_chunks);
@@ -2093,7 +2139,7 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
             const char *row = slot_row(j, b, slot);
             Cand2 c;
             c.init();
-            float lomax = -INFINITY;
+            float thr = -INFINITY, thrS = -INFINITY;
             const uint32_t b0 = (uint32_t)chunk * (uint32_t)j.seed_bpw;
             const uint32_t bend = min(b0 + (uint32_t)j.seed_bpw, nblk);
             uint32_t nextb = b0 + 32u;  // next block to hand out (warp-uniform)
@@ -2112,8 +2158,11 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
                     done = !got;
                 }
                 const unsigned gm = __ballot_sync(0xFFFFFFFFu, got);
-                if (got)
-                    ids[cnt + __popc(gm & lt)] = v;
+                if (got) {
+                    const int q = cnt + __popc(gm & lt);
+                    ids[q] = v;
+                    seed_fetch<In>(row, v, (uint32_t)j.V, &xw[q]);
+                }
                 cnt += __popc(gm);
                 const unsigned dm = __ballot_sync(0xFFFFFFFFu, done);
                 if (done) {
@@ -2124,19 +2173,20 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
                 }
                 nextb += (uint32_t)__popc(dm);
                 if (cnt > kSeedList - 32) {  // room for one more trip's ids
+                    cp_async_wait_all();
                     __syncwarp();
-                    seed_score<In>(ids, cnt, row, rm, c, lomax);
+                    seed_score<In>(ids, xw, cnt, rm, gtop, c, thr, thrS);
                     __syncwarp();
                     cnt = 0;
                 }
             }
+            cp_async_wait_all();
             __syncwarp();
             if (cnt > 0)
-                seed_score<In>(ids, cnt, row, rm, c, lomax);
+                seed_score<In>(ids, xw, cnt, rm, gtop, c, thr, thrS);
             __syncwarp();
             warp_cand2(c);
-            lomax = warp_max(lomax);
-            r.thr = lomax > -INFINITY ? __fsub_rd(lomax, 1e-9f) : -INFINITY;
+            r.thr = warp_max(thr);
             r.hi1 = c.hi1;
             r.lo1 = c.lo1;
             r.hi2 = c.hi2;
