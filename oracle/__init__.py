@@ -91,6 +91,12 @@ def _L():
         lib.or_packed_anyorder_step.restype = i32
         lib.or_packed_anyorder_step.argtypes = [vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp,
                                                 vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.or_packed_topk_step.restype = i32
+        lib.or_packed_topk_step.argtypes = [vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp,
+                                            vp, vp, vp, dbl, u64, u64, vp, i32, vp, vp, vp, vp,
+                                            vp, vp, vp, vp, vp, vp]
+        lib.or_topk.restype = None
+        lib.or_topk.argtypes = [vp, i32, i32, vp]
         lib.or_num_threads.restype, lib.or_num_threads.argtypes = i32, []
         _lib = lib
     return _lib
@@ -329,6 +335,48 @@ def packed_step(logits, K, W, prev_draft, prev_len, prev_q_at_draft=None,
         _p(out["confidence"]), _p(out["flags"]))
     if rc:
         raise ValueError("oracle: invalid packed-step inputs")
+    return out
+
+
+def topk(x, k):
+    """The k largest entries of the fp64 row x (ties to the lowest id), in
+    that order."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    ids = np.empty(k, np.int32)
+    _L().or_topk(_p(x), x.shape[0], int(k), _p(ids))
+    return ids
+
+
+def packed_topk_step(logits, K, W, kp, kq, prev_draft, prev_len, prev_q_ids, prev_q_probs,
+                     prev_q_offset, T, seed=0, it=0, pos_base=None, eos_id=-1, remaining=None):
+    """Packed-SS step with top-k truncated target (kp) and drafter (kq)
+    distributions; prev_q_ids / prev_q_probs [B, W, kq]; see sv_oracle.c."""
+    logits = np.ascontiguousarray(logits)
+    B, R, V = logits.shape
+    if R != K + W or K < 1:
+        raise ValueError("logits must be [B, K+W, V] with K >= 1")
+    pd = _i32(prev_draft, (B, K - 1))
+    pl = _i32(prev_len)
+    qi = _i32(prev_q_ids, (B, W, kq))
+    qp = np.ascontiguousarray(prev_q_probs, dtype=np.float32).reshape(B, W, kq)
+    off = _i32(prev_q_offset)
+    pb = _i64(pos_base)
+    rem = _i32(remaining)
+    out = {
+        "accept_len": np.empty(B, np.int32), "commit_len": np.empty(B, np.int32),
+        "committed": np.empty((B, K), np.int32), "next_draft": np.empty((B, W), np.int32),
+        "next_len": np.empty(B, np.int32), "next_q_at_draft": np.empty((B, W)),
+        "q_ids": np.empty((B, W, kq), np.int32), "q_probs": np.empty((B, W, kq)),
+        "flags": np.empty(B, np.int32),
+    }
+    rc = _L().or_packed_topk_step(
+        _p(logits), _dtype_code(logits), V, B, K, W, V, int(kp), int(kq), _p(pd), _p(pl),
+        _p(qi), _p(qp), _p(off), f32(T), int(seed) & (2**64 - 1), int(it) & (2**64 - 1),
+        _p(pb), int(eos_id), _p(rem), _p(out["accept_len"]), _p(out["commit_len"]),
+        _p(out["committed"]), _p(out["next_draft"]), _p(out["next_len"]),
+        _p(out["next_q_at_draft"]), _p(out["q_ids"]), _p(out["q_probs"]), _p(out["flags"]))
+    if rc:
+        raise ValueError("oracle: invalid truncated packed-step inputs")
     return out
 
 

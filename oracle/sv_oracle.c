@@ -1059,6 +1059,218 @@ int or_packed_step(const void *logits, int dtype, int64_t row_stride, int B, int
     return err ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Packed-SS with top-k truncated distributions ([PackedSS] §3.2, last       */
+/* paragraph: with top-k truncation only the nonzero entries of the stored   */
+/* drafter distribution Q need to be kept; Alg. 2 otherwise unchanged).      */
+/*   READING: top-k of a row keeps its k largest logits (ties to the lowest  */
+/*   id) and renormalises softmax(x/T) over them.  Both sides are truncated, */
+/*   as in a sampler that applies top-k to the verifier (the AR mode whose   */
+/*   law the step preserves, Thm. 3.3) and to the drafter: the target p of   */
+/*   verify rows keeps kp entries, the drafter Q of proposal rows kq.        */
+/*   The previous call's Q rows arrive as (id, probability) lists:           */
+/*   prev_q_ids / prev_q_probs [B, W, kq] (ids -1 padded); Q_{t-1}^(i) is    */
+/*   list prev_q_offset[b] + i (Alg. 2 line 12).                             */
+/*   Verify position i < prev_len: accept d_i w.p. min{1, p(d_i)/Q(d_i)},    */
+/*   p(d) = 0 off its support; d_i must be in its list.  First rejection h:  */
+/*   the correction is the Gumbel-max over v with [p(v) - Q(v)]_+ > 0 of     */
+/*   log [p(v) - Q(v)]_+ + G(SAMPLE, b, pos + h); all accepted: the bonus is  */
+/*   the Gumbel-max of x/T + G over the support of p.  Proposal j: z_j the   */
+/*   Gumbel-max of y_j/T + G(DRAFT, b, pos + j, iter) over the top-kq ids,   */
+/*   and the list (ids by logit desc, id asc; probabilities) is written to   */
+/*   q_ids / q_probs [B, W, kq] for the next call.                           */
+/*   Stopping, committed tokens and the shift of the next draft are those of */
+/*   or_packed_step.  T > 0.                                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    double x;
+    int32_t v;
+} or_entry;
+
+/* Larger logit first; equal logits: lower id first. */
+static int or_entry_cmp(const void *a, const void *b)
+{
+    const or_entry *p = (const or_entry *)a, *q = (const or_entry *)b;
+    if (p->x != q->x)
+        return p->x > q->x ? -1 : 1;
+    return p->v < q->v ? -1 : (p->v > q->v ? 1 : 0);
+}
+
+/* The k largest entries of x[0..V-1] (ties to the lowest id), in that order
+ * (a full sort of the row, then its first k). */
+void or_topk(const double *x, int V, int k, int32_t *ids)
+{
+    or_entry *e = (or_entry *)malloc(sizeof(or_entry) * (size_t)V);
+    for (int v = 0; v < V; ++v) {
+        e[v].x = x[v];
+        e[v].v = v;
+    }
+    qsort(e, (size_t)V, sizeof(or_entry), or_entry_cmp);
+    for (int m = 0; m < k; ++m)
+        ids[m] = e[m].v;
+    free(e);
+}
+
+/* log of the sum over the k listed ids of exp(x/T): m + log(sum exp(z - m)). */
+static double or_lse_list(const double *x, const int32_t *ids, int k, double T)
+{
+    double m = -INFINITY, s = 0.0;
+    for (int i = 0; i < k; ++i)
+        if (x[ids[i]] / T > m)
+            m = x[ids[i]] / T;
+    for (int i = 0; i < k; ++i)
+        s += exp(x[ids[i]] / T - m);
+    return m + log(s);
+}
+
+/* Probability of v in a stored list (0 when absent). */
+static double or_list_prob(const int32_t *ids, const float *probs, int k, int v)
+{
+    for (int i = 0; i < k; ++i)
+        if (ids[i] == v)
+            return (double)probs[i];
+    return 0.0;
+}
+
+int or_packed_topk_step(const void *logits, int dtype, int64_t row_stride, int B, int K, int W,
+                        int V, int kp, int kq, const int32_t *prev_draft,
+                        const int32_t *prev_len, const int32_t *prev_q_ids,
+                        const float *prev_q_probs, const int32_t *prev_q_offset, double T,
+                        uint64_t seed, uint64_t iter, const int64_t *pos_base, int32_t eos_id,
+                        const int32_t *remaining, int32_t *accept_len, int32_t *commit_len,
+                        int32_t *committed, int32_t *next_draft, int32_t *next_len,
+                        double *next_q_at_draft, int32_t *q_ids, double *q_probs,
+                        int32_t *flags)
+{
+    if (!(T > 0.0) || kp < 1 || kp > V || kq < 1 || kq > V)
+        return -1;
+    int err = 0;
+    int R = K + W;
+#pragma omp parallel for schedule(dynamic) reduction(| : err)
+    for (int b = 0; b < B; ++b) {
+        int64_t pos0 = pos_base ? pos_base[b] : 0;
+        int n = prev_len[b];
+        int off = prev_q_offset ? prev_q_offset[b] : 0;
+        if (n < 0 || n > K - 1 || off < 0 || off + n > W) {
+            err |= 1;
+            continue;
+        }
+        double *x = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t *S = (int32_t *)malloc(sizeof(int32_t) * (size_t)(kp > kq ? kp : kq));
+        int32_t *C = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
+        int32_t *z = (int32_t *)malloc(sizeof(int32_t) * (size_t)W);
+        double *qz = (double *)malloc(sizeof(double) * (size_t)W);
+        int h = 0, nflag = 0, bad = 0;
+        double gap = INFINITY;
+
+        /* ---- verification of D_{t-1} against the truncated target ---- */
+        int rejected = 0;
+        for (int i = 0; i < n && !rejected; ++i) {
+            int d = prev_draft[(int64_t)b * (K - 1) + i];
+            const int32_t *qi = prev_q_ids + ((int64_t)b * W + off + i) * kq;
+            const float *qp = prev_q_probs + ((int64_t)b * W + off + i) * kq;
+            double Qd = (d >= 0 && d < V) ? or_list_prob(qi, qp, kq, d) : 0.0;
+            if (!(Qd > 0.0)) {
+                bad = 1;  /* the draft is not in the list it was drawn from */
+                break;
+            }
+            load_row(logits, dtype, (int64_t)b * R + i, row_stride, V, x);
+            or_topk(x, V, kp, S);
+            double L = or_lse_list(x, S, kp, T);
+            double log_p = -INFINITY;
+            for (int m = 0; m < kp; ++m)
+                if (S[m] == d)
+                    log_p = x[d] / T - L;
+            double alpha = or_accept_prob(log_p, log(Qd), OR_LOSSLESS, 0.0);
+            double u = or_uniform(or_key(seed, ST_ACCEPT, (uint64_t)b, pos0 + i, 0), 0);
+            if (fabs(u - alpha) < OR_FLAG_EPS)
+                ++nflag;
+            if (u < alpha)
+                ++h;
+            else
+                rejected = 1;
+        }
+        if (bad) {
+            err |= 2;
+            free(x), free(w), free(S), free(C), free(z), free(qz);
+            continue;
+        }
+        load_row(logits, dtype, (int64_t)b * R + h, row_stride, V, x);
+        or_topk(x, V, kp, S);
+        double L = or_lse_list(x, S, kp, T);
+        for (int v = 0; v < V; ++v)
+            w[v] = -INFINITY;
+        if (h < n) {
+            /* correction from [p - Q]_+ over the support of p */
+            const int32_t *qi = prev_q_ids + ((int64_t)b * W + off + h) * kq;
+            const float *qp = prev_q_probs + ((int64_t)b * W + off + h) * kq;
+            for (int m = 0; m < kp; ++m) {
+                int v = S[m];
+                double r = exp(x[v] / T - L) - or_list_prob(qi, qp, kq, v);
+                if (r > 0.0)
+                    w[v] = log(r);
+            }
+        } else {
+            for (int m = 0; m < kp; ++m)
+                w[S[m]] = x[S[m]] / T;
+        }
+        int c = or_gumbel_argmax(w, V, or_key(seed, ST_SAMPLE, (uint64_t)b, pos0 + h, 0), &gap);
+        if (gap < OR_FLAG_EPS)
+            ++nflag;
+        for (int i = 0; i < h; ++i)
+            C[i] = prev_draft[(int64_t)b * (K - 1) + i];
+        C[h] = c;
+        int A = h + 1;
+        int a = A;
+        if (remaining && remaining[b] < a)
+            a = remaining[b] < 0 ? 0 : remaining[b];
+        if (eos_id >= 0)
+            for (int i = 0; i < A; ++i)
+                if (C[i] == eos_id) {
+                    if (i + 1 < a)
+                        a = i + 1;
+                    break;
+                }
+
+        /* ---- drafting Z_t from the truncated drafter rows ---- */
+        for (int j = 0; j < W; ++j) {
+            load_row(logits, dtype, (int64_t)b * R + K + j, row_stride, V, x);
+            or_topk(x, V, kq, S);
+            double Lq = or_lse_list(x, S, kq, T);
+            for (int v = 0; v < V; ++v)
+                w[v] = -INFINITY;
+            for (int m = 0; m < kq; ++m) {
+                w[S[m]] = x[S[m]] / T;
+                q_ids[((int64_t)b * W + j) * kq + m] = S[m];
+                q_probs[((int64_t)b * W + j) * kq + m] = exp(x[S[m]] / T - Lq);
+            }
+            double g;
+            z[j] = or_gumbel_argmax(w, V, or_key(seed, ST_DRAFT, (uint64_t)b, pos0 + j, iter), &g);
+            qz[j] = exp(x[z[j]] / T - Lq);
+            if (j >= a && g < OR_FLAG_EPS)
+                ++nflag;
+        }
+
+        accept_len[b] = h;
+        commit_len[b] = a;
+        for (int i = 0; i < K; ++i)
+            committed[(int64_t)b * K + i] = i < a ? C[i] : -1;
+        int nl = W - a > 0 ? W - a : 0;
+        next_len[b] = nl;
+        for (int j = 0; j < W; ++j) {
+            next_draft[(int64_t)b * W + j] = j < nl ? z[a + j] : -1;
+            if (next_q_at_draft)
+                next_q_at_draft[(int64_t)b * W + j] = j < nl ? qz[a + j] : NAN;
+        }
+        if (flags)
+            flags[b] = nflag;
+        free(x), free(w), free(S), free(C), free(z), free(qz);
+    }
+    return err ? -1 : 0;
+}
+
 /* Number of threads the parallel loops above use (for reporting). */
 int or_num_threads(void)
 {
