@@ -43,6 +43,7 @@ WORKLOAD = "packed"
 METRIC = "verified draft rows/sec and logits HBM GB/s (fraction of GB300 peak), 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["sv_pass.cu", "sv_common.cuh", "sv_dev.cuh", "sv_gumbel.cuh", "sv_job.cuh"]
+TOPK_SOURCES = ["sv_topk.cu", "sv_topk.cuh", "sv_common.cuh", "sv_dev.cuh", "sv_gumbel.cuh"]
 
 
 def _peaks():
@@ -54,9 +55,9 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _kernel_hash():
+def _kernel_hash(w=None):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (TOPK_SOURCES if w is not None and w.kind == "packed_topk" else KERNEL_SOURCES):
         with open(os.path.join(ROOT, "draft_block_verification_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -65,7 +66,7 @@ def _kernel_hash():
 def _profile_path(w):
     """The committed ncu summary of the streaming kernel on this workload."""
     t = "" if w.kind == "greedy" else "_t%g" % w.T
-    return os.path.join(ROOT, "profiles", "pass_kernel_%s%s.md" % (w.name, t))
+    return os.path.join(ROOT, "profiles", "%s_%s%s.md" % (w.kernel(), w.name, t))
 
 
 def _profiled_traffic(w):
@@ -81,7 +82,7 @@ def _profiled_traffic(w):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_hash") != _kernel_hash():
+    if vals.get("kernel_source_hash") != _kernel_hash(w):
         return None
     try:
         return int(vals["dram_bytes_per_launch"])
@@ -231,6 +232,8 @@ class Workload:
             self.T = pick(args.T, 1.0)
         elif self.kind == "anyorder":
             self.T = 0.0  # Alg. 3 is greedy
+        elif self.kind == "packed_topk":
+            self.T = pick(args.T, c["T"])
         else:
             self.T = 0.0
         self.esz = 2 if c["dtype"] == "bf16" else 4
@@ -252,6 +255,9 @@ class Workload:
                      max_children=c["max_children"])
         elif self.kind == "anyorder":
             d.update(B=c["B"], Kv=c["K"], W=c["W"], V=c["V"], T=0.0)
+        elif self.kind == "packed_topk":
+            d.update(B=c["B"], K=c["K"], W=c["W"], V=c["V"], T=self.T, top_k_p=c["kp"],
+                     top_k_q=c["kq"])
         else:
             d.update(B=c["B"], K=c["K"], W=c["W"], V=c["V"], T=self.T)
         d["logits"] = c["dtype"]
@@ -285,6 +291,8 @@ class Workload:
                                      device=device)
             return {"state_logits": si.state_logits, "parent": si.parent,
                     "node_pos": si.node_pos, "node_tok": si.node_tok, "root_mask": si.root_mask}
+        if self.kind == "packed_topk":
+            return self.topk_inputs(B, device)
         pi = datagen.packed_inputs(B, c["K"], c["W"], c["V"], dtype=c["dtype"], seed=c["seed"],
                                    T=self.T, device=device)
         d = {"logits": pi.logits, "prev_draft": pi.prev_draft, "prev_len": pi.prev_len}
@@ -293,8 +301,46 @@ class Workload:
                      prev_q_offset=pi.prev_q_offset)
         return d
 
+    def topk_inputs(self, B, device):
+        """This call's rows and the state a previous call leaves: that call
+        (no previous draft) runs on the previous rows -- through the library
+        on a GPU, through the oracle on the CPU -- and is taken to have
+        stopped at a_prev."""
+        c = self.cfg
+        K, W, kp, kq = c["K"], c["W"], c["kp"], c["kq"]
+        ti = datagen.packed_topk_inputs(B, K, W, c["V"], dtype=c["dtype"], seed=c["seed"],
+                                        device=device)
+        if torch.device(device).type == "cuda":
+            import draft_block_verification_gb300 as dbv
+            z = lambda *s, dt=torch.int32: torch.zeros(s, dtype=dt, device=device)
+            prev = dbv.sv_packed_topk_step(ti.prev_logits, K, W, kp, kq, z(B, K - 1), z(B),
+                                           z(B, W, kq), z(B, W, kq, dt=torch.float32), z(B),
+                                           T=self.T, seed=c["seed"], it=1)
+            a_prev = torch.maximum(ti.a_prev, prev["commit_len"])
+        else:
+            import oracle
+            lg = datagen.to_numpy_logits
+            prev = oracle.packed_topk_step(
+                lg(ti.prev_logits), K, W, kp, kq, np.zeros((B, K - 1), np.int32),
+                np.zeros(B, np.int32), np.zeros((B, W, kq), np.int32),
+                np.zeros((B, W, kq), np.float32), np.zeros(B, np.int32), self.T, seed=c["seed"],
+                it=1)
+            prev = {k: torch.from_numpy(np.asarray(v)) for k, v in prev.items()}
+            prev["q_probs"] = prev["q_probs"].float()
+            a_prev = torch.maximum(ti.a_prev, prev["commit_len"])
+        st = datagen.packed_state_from(prev["next_draft"], prev["commit_len"], prev["q_ids"],
+                                       prev["q_probs"], a_prev, K, W)
+        st["logits"] = ti.logits
+        return st
+
     def call(self, dbv, inp, h):
         c = self.cfg
+        if self.kind == "packed_topk":
+            return dbv.sv_packed_topk_step(inp["logits"], c["K"], c["W"], c["kp"], c["kq"],
+                                           inp["prev_draft"], inp["prev_len"],
+                                           inp["prev_q_ids"], inp["prev_q_probs"],
+                                           inp["prev_q_offset"], T=self.T, seed=c["seed"], it=2,
+                                           handle=h)
         if self.kind == "sample":
             return dbv.sv_verify_sample(inp["target"], inp["draft"], inp["draft_ids"], T_p=self.T,
                                         T_q=self.T, mode=self.mode, lam=self.lam, seed=c["seed"],
@@ -345,6 +391,11 @@ class Workload:
             oracle.verify_spot(lg(inp["state_logits"]), n(inp["parent"]), n(inp["node_pos"]),
                                n(inp["node_tok"]), n(inp["root_mask"]).astype(np.uint64),
                                T=self.T, seed=c["seed"])
+        elif self.kind == "packed_topk":
+            oracle.packed_topk_step(lg(inp["logits"]), c["K"], c["W"], c["kp"], c["kq"],
+                                    n(inp["prev_draft"]), n(inp["prev_len"]),
+                                    n(inp["prev_q_ids"]), n(inp["prev_q_probs"]),
+                                    n(inp["prev_q_offset"]), self.T, seed=c["seed"], it=2)
         else:
             pdl = inp.get("prev_draft_logits")
             oracle.packed_step(lg(inp["logits"]), c["K"], c["W"], n(inp["prev_draft"]),
@@ -422,21 +473,35 @@ class Workload:
             d["mean_path_len"] = float(t("path_len").mean())
         else:
             d["mean_accept_len"] = float(t("accept_len").mean())
-        if self.kind == "packed":
+        if self.kind in ("packed", "packed_topk"):
             d["mean_commit_len"] = float(t("commit_len").mean())
         f = t("flags")
         d["flags"] = None if f is None else int(f.sum())
         return d
 
+    def kernel(self):
+        """The streaming kernel the roofline is taken on."""
+        return "topk_select_kernel" if self.kind == "packed_topk" else "pass_kernel"
+
     def launches(self):
-        """Library kernels per call: the streaming pass, plus the residual
-        pass and the fp64 check after a sampling call (and the TV pass when
-        TV is asked for)."""
+        """Library kernels per call: the streaming pass; the seed kernel
+        before it when rows carry a Gumbel-max (a sampling call's bonus rows;
+        trees, SPOT and Packed-SS steps at T > 0); the residual pass and the
+        fp64 check after a sampling call or a Packed-SS step at T > 0 (and
+        the TV pass when TV is asked for); the per-sequence preparation of a
+        SPOT or any-order call.  The truncated Packed-SS step is a selection
+        and a decision kernel."""
+        if self.kind == "packed_topk":
+            return 2
         if self.kind == "sample":
-            return 4 if self.tv else 3
-        if self.kind in ("spot", "anyorder"):
-            return 2  # the per-sequence preparation, then the streaming pass
-        return 3 if (self.kind == "packed" and self.T > 0) else 1
+            return 5 if self.tv else 4
+        if self.kind == "anyorder":
+            return 2
+        if self.kind == "spot":
+            return 3 if self.T > 0 else 2
+        if self.kind == "tree":
+            return 2 if self.T > 0 else 1
+        return 4 if (self.kind == "packed" and self.T > 0) else 1
 
 
 def _cpu_sample(w, seconds, nmax=None):
@@ -608,7 +673,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": _profiled_traffic(w),
-                     "peak_source": peak_kind, "kernel": "pass_kernel", "kernel_ms": kern_ms,
+                     "peak_source": peak_kind, "kernel": w.kernel(), "kernel_ms": kern_ms,
                      "alg_bytes_per_launch": alg_bytes},
         "e2e": {"value": job_rate(ws, units, e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},

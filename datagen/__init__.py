@@ -28,6 +28,11 @@ CONFIGS = {
                  max_depth=8, max_children=4, T=(0.0, 1.0)),
     "packed": dict(kind="packed", B=256, K=32, W=32, V=151936, dtype="bf16", seed=4,
                    T=(0.0, 1.0)),
+    # Packed-SS at T = 1 with top-k truncated target and drafter
+    # distributions, k = 20 of 151,936 (the top-k the truncation passage
+    # quotes for that vocabulary)
+    "packed_topk": dict(kind="packed_topk", B=256, K=32, W=32, V=151936, dtype="bf16", seed=7,
+                        kp=20, kq=20, T=1.0),
     # any-order Packed-SS steps: windows of 32 unresolved positions checked
     # in a random rank order, drafts at 90% of them
     "anyorder": dict(kind="anyorder", B=256, K=32, W=32, V=151936, dtype="bf16", seed=6),
@@ -324,3 +329,58 @@ def anyorder_inputs(B, Kv, W, V, dtype="bf16", seed=6, p_draft=0.9, p_match=0.8,
                     dr[b, od[b, r]] = int(rng.integers(V))
     t = lambda a: torch.as_tensor(a, dtype=torch.int32, device=device)
     return AnyOrderInputs(logits, t(u), t(wp), t(od), t(dr), t(np.full(B, 10 ** 6)))
+
+
+@dataclasses.dataclass
+class PackedTopkInputs:
+    prev_logits: torch.Tensor   # [B, K+W, V] the previous call's rows
+    logits: torch.Tensor        # [B, K+W, V] this call's rows
+    a_prev: torch.Tensor        # [B] int32: the previous call's stopping index, 1..W
+
+
+def packed_topk_inputs(B, K, W, V, dtype="bf16", seed=7, sigma=0.3, device="cpu"):
+    """Two consecutive model calls of a Packed-SS run: rows N(0, 2^2); this
+    call's verify row i repeats the previous call's proposal row a_prev + i
+    plus N(0, sigma^2) noise (a drafter that saw the same context), with
+    a_prev ~ U{1..W}.  The truncated lists and drafts of the previous call
+    are the step's own outputs on prev_logits (see packed_state_from)."""
+    g = _gen(seed, device)
+    dt = _TORCH_DTYPE[dtype]
+    prev = _normal((B, K + W, V), 2.0, g, device)
+    cur = _normal((B, K + W, V), 2.0, g, device)
+    a_prev = torch.randint(1, W + 1, (B,), generator=g, device=device)
+    idx = torch.arange(K, device=device)[None, :] + a_prev[:, None]           # [B, K]
+    use = idx < W
+    src = torch.gather(prev[:, K:], 1, idx.clamp(max=W - 1)[:, :, None].expand(B, K, V))
+    cur[:, :K] = torch.where(use[:, :, None], src + _normal((B, K, V), sigma, g, device),
+                             cur[:, :K])
+    del src
+    return PackedTopkInputs(prev.to(dt), cur.to(dt), a_prev.to(torch.int32))
+
+
+def packed_state_from(next_draft, commit_len, q_ids, q_probs, a_prev, K, W):
+    """The inputs of the next truncated Packed-SS call when the previous call
+    (outputs next_draft, commit_len, q_ids, q_probs; numpy or torch) is taken
+    to have stopped at a_prev instead of its own commit_len: the draft is
+    z_{a_prev + i}, i < min(W - a_prev, K - 1), and Q_{t-1}^(i) is list
+    a_prev + i (offset a_prev).  Pure indexing; a_prev >= commit_len."""
+    lib = torch if isinstance(next_draft, torch.Tensor) else np
+    B = next_draft.shape[0]
+    n = lib.clip(W - a_prev, 0, K - 1) if lib is np else torch.clamp(W - a_prev, 0, K - 1)
+    i = lib.arange(K - 1)[None, :] if lib is np else torch.arange(K - 1,
+                                                                  device=next_draft.device)[None]
+    src = (a_prev - commit_len)[:, None] + i
+    valid = i < n[:, None]
+    if lib is np:
+        d = np.take_along_axis(next_draft, np.clip(src, 0, W - 1), 1)
+        prev_draft = np.where(valid, d, 0).astype(np.int32)
+        return dict(prev_draft=prev_draft, prev_len=n.astype(np.int32),
+                    prev_q_offset=a_prev.astype(np.int32), prev_q_ids=q_ids.astype(np.int32),
+                    prev_q_probs=q_probs.astype(np.float32))
+    d = torch.gather(next_draft, 1, src.clamp(0, W - 1).long())
+    prev_draft = torch.where(valid, d, torch.zeros_like(d)).to(torch.int32).contiguous()
+    return dict(prev_draft=prev_draft, prev_len=n.to(torch.int32).contiguous(),
+                prev_q_offset=a_prev.to(torch.int32).contiguous(),
+                prev_q_ids=q_ids.to(torch.int32).contiguous(),
+                prev_q_probs=q_probs.to(torch.float32).contiguous())
+

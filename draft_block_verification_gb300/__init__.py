@@ -77,6 +77,10 @@ def lib():
         L.sv_packed_step.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                      f32, u64, u64, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                      vp]
+        L.sv_packed_topk_step.restype = i32
+        L.sv_packed_topk_step.argtypes = [vp, vp, i32, i64, i32, i32, i32, i32, i32, i32, vp, vp,
+                                          vp, vp, vp, f32, u64, u64, vp, i32, vp, vp, vp, vp, vp,
+                                          vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -398,3 +402,45 @@ def sv_packed_step(logits, K, W, prev_draft, prev_len, *, prev_q_at_draft=None,
         _p(out["next_len"]), _p(out["next_q_at_draft"]), _p(out["confidence"]),
         _p(out["flags"]), _stream(stream, dev)), "sv_packed_step")
     return out
+
+
+def sv_packed_topk_step(logits, K, W, kp, kq, prev_draft, prev_len, prev_q_ids, prev_q_probs,
+                        prev_q_offset, *, T=1.0, seed=0, it=0, pos_base=None, eos_id=-1,
+                        remaining=None, handle=None, stream=None):
+    """One Packed-SS iteration with top-k truncated target (kp) and drafter
+    (kq) distributions; logits [B, K+W, V]; the previous call's drafter lists
+    prev_q_ids / prev_q_probs [B, W, kq] (int32 / float32)."""
+    B, R, V = logits.shape
+    if R != K + W:
+        raise ValueError("logits must be [B, K+W, V]")
+    dev = logits.device
+    code, rs = _rows(logits, "logits")
+    h = handle or default_handle(dev)
+    pd = _i32(prev_draft, (B, K - 1), "prev_draft", dev) if K > 1 else None
+    pl = _i32(prev_len, (B,), "prev_len", dev)
+    qi = _i32(prev_q_ids, (B, W, kq), "prev_q_ids", dev)
+    off = _i32(prev_q_offset, (B,), "prev_q_offset", dev)
+    rem = _i32(remaining, (B,), "remaining", dev)
+    qp = prev_q_probs
+    if (qp is None or qp.dtype != torch.float32 or not qp.is_contiguous() or
+            tuple(qp.shape) != (B, W, kq) or qp.device != dev):
+        raise ValueError("prev_q_probs must be a contiguous float32 [B, W, kq] tensor on the "
+                         "logits' device")
+    out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "commit_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "committed": torch.empty((B, K), dtype=torch.int32, device=dev),
+           "next_draft": torch.empty((B, W), dtype=torch.int32, device=dev),
+           "next_len": torch.empty(B, dtype=torch.int32, device=dev),
+           "next_q_at_draft": torch.empty((B, W), dtype=torch.float32, device=dev),
+           "q_ids": torch.empty((B, W, kq), dtype=torch.int32, device=dev),
+           "q_probs": torch.empty((B, W, kq), dtype=torch.float32, device=dev),
+           "flags": torch.empty(B, dtype=torch.int32, device=dev)}
+    _check(lib().sv_packed_topk_step(
+        h.ptr, _p(logits), code, rs, B, K, W, V, int(kp), int(kq), _p(pd), _p(pl), _p(qi),
+        _p(qp), _p(off), float(T), int(seed) & (2**64 - 1), int(it) & (2**64 - 1),
+        _p(pos_base), int(eos_id), _p(rem), _p(out["accept_len"]), _p(out["commit_len"]),
+        _p(out["committed"]), _p(out["next_draft"]), _p(out["next_len"]),
+        _p(out["next_q_at_draft"]), _p(out["q_ids"]), _p(out["q_probs"]), _p(out["flags"]),
+        _stream(stream, dev)), "sv_packed_topk_step")
+    return out
+

@@ -13,7 +13,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(HERE, "_lib")
 LIBPATH = os.path.join(LIBDIR, "libsv.so")
-SOURCES = ["sv_pass.cu", "sv_post.cu", "sv_api.cu", "sv_selftest.cu", "sv_static.cu"]
+SOURCES = ["sv_pass.cu", "sv_post.cu", "sv_api.cu", "sv_selftest.cu", "sv_static.cu",
+           "sv_topk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

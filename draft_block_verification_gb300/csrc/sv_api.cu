@@ -1,5 +1,5 @@
 // sv_api.cu -- host side of libsv: handle, argument checks, workspace and
-// launch orchestration for the four verify calls declared in sv.h.
+// launch orchestration for the verify calls declared in sv.h.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdlib.h>
@@ -10,6 +10,7 @@
 
 #include "sv_gumbel.cuh"
 #include "sv_job.cuh"
+#include "sv_topk.cuh"
 
 namespace sv {
 size_t pass_smem_bytes();
@@ -767,6 +768,76 @@ sv_status sv_packed_step(sv_handle *h, const void *logits, sv_dtype dtype, int64
     sv_status st = plan(h, j, K + W, s, 1, &grid);
     if (st != SV_OK) return st;
     return launch(h, j, grid, s, T > 0.f, false);
+}
+
+sv_status sv_packed_topk_step(sv_handle *h, const void *logits, sv_dtype dtype,
+                              int64_t row_stride, int B, int K, int W, int V, int kp, int kq,
+                              const int32_t *prev_draft, const int32_t *prev_len,
+                              const int32_t *prev_q_ids, const float *prev_q_probs,
+                              const int32_t *prev_q_offset, float T, uint64_t seed, uint64_t iter,
+                              const int64_t *pos_base, int32_t eos_id, const int32_t *remaining,
+                              int32_t *accept_len, int32_t *commit_len, int32_t *committed,
+                              int32_t *next_draft, int32_t *next_len, float *next_q_at_draft,
+                              int32_t *q_ids, float *q_probs, int32_t *flags, void *stream)
+{
+    if (!h || B < 0 || K < 1 || K > kMaxK || W < 1 || W > kMaxK) return SV_ERR_INVALID_ARG;
+    if (!(T > 0.f) || !isfinite(T)) return SV_ERR_INVALID_ARG;
+    if (kp < 1 || kq < 1 || kp > kTopkMax || kq > kTopkMax || kp > V || kq > V)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!logits_ok(logits, dtype, row_stride, V) || !prev_len || (K > 1 && !prev_draft) ||
+        !prev_q_ids || !prev_q_probs || !prev_q_offset || !accept_len || !commit_len ||
+        !committed || !next_draft || !next_len || !q_ids || !q_probs)
+        return SV_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(h->mu);
+    cudaStream_t s = (cudaStream_t)stream;
+    TopkJob t;
+    memset(&t, 0, sizeof t);
+    const int esz = dtype == SV_BF16 ? 2 : 4;
+    t.src = (const char *)logits;
+    t.rs = row_stride * esz;
+    t.dtype = dtype;
+    t.V = V;
+    t.nvec = (int)((int64_t)V * esz / 16);
+    t.B = B;
+    t.K = K;
+    t.W = W;
+    t.kp = kp;
+    t.kq = kq;
+    t.T = T;
+    t.seed = seed;
+    t.iter = iter;
+    t.pos_base = pos_base;
+    t.eos = eos_id;
+    t.remaining = remaining;
+    t.prev_draft = prev_draft;
+    t.prev_len = prev_len;
+    t.prev_q_ids = prev_q_ids;
+    t.prev_q_probs = prev_q_probs;
+    t.prev_off = prev_q_offset;
+    t.skip = h->d_skip;
+    t.acc = accept_len;
+    t.commit_len = commit_len;
+    t.committed = committed;
+    t.next_draft = next_draft;
+    t.next_len = next_len;
+    t.next_q = next_q_at_draft;
+    t.q_ids = q_ids;
+    t.q_probs = q_probs;
+    t.flags = flags;
+    t.err = h->d_err;
+    if (sv_status fi = fault_injected("sv_packed_topk_step")) return fi;
+    // workspace: the sorted list of every row, kTopkMax logits and ids
+    const size_t rows = (size_t)B * (K + W);
+    sv_status st = ensure_ws(h, rows * kTopkMax * 8, s);
+    if (st != SV_OK) return st;
+    t.lval = (float *)h->ws;
+    t.lid = (int32_t *)(h->ws + rows * kTopkMax * 4);
+    if (h->timing) cudaEventRecord(h->ev[0], s);
+    cudaError_t e = topk_select_launch(t, s);
+    if (h->timing) cudaEventRecord(h->ev[1], s);
+    if (e == cudaSuccess) e = topk_decide_launch(t, s);
+    return cuda_status(e);
 }
 
 }  // extern "C"

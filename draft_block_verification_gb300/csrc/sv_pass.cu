@@ -80,10 +80,6 @@ struct PassShared {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     StageMeta meta[kStages];
-    // Gumbel threshold of local unit lu, in slot lu % kStages: the ring holds
-    // stages of at most kStages - 1 other units when a unit starts, so no warp
-    // still uses the slot that unit takes over.
-    uint32_t thr[kStages];
     volatile int abort;
     // Gumbel vectors that passed level 1, per consumer warp: raw data and
     // the vector's index in the row
@@ -402,7 +398,6 @@ struct TState {
     float mx;          // running max
     int amax;
     GState g;
-    float pub;         // threshold last published to the CTA
     int gqn;           // groups in this warp's queue (warp-uniform)
     float xd;          // logit at the unit's draft token (its owner thread), else NaN
 };
@@ -413,7 +408,7 @@ __device__ __forceinline__ void tstate_init(TState &s)
     s.acc1 = s.acc2 = make_float2(0.f, 0.f);
     s.mx = -INFINITY;
     s.amax = 0x7FFFFFFF;
-    s.g.thr = s.g.thrS = s.pub = -INFINITY;
+    s.g.thr = s.g.thrS = -INFINITY;
     s.gqn = 0;
     s.xd = __int_as_float(0x7FC00000);
 }
@@ -604,8 +599,12 @@ __device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
 // threshold with that bound.  The comparison is strict: a bound equal to the
 // level-1 threshold stays below thr (the threshold's margin exceeds the
 // bound's rounding slack), and the -inf padding of a short stage never passes,
-// not even a threshold of -inf.  The queue is compacted with a ballot, so a
-// warp does not diverge per vector.
+// not even a threshold of -inf.  The chunk is tested first on its largest
+// logit with one vote per warp (with the seed threshold, nearly every chunk
+// stops there); otherwise each vector is tested and the passing ones are
+// queued, compacted with a ballot, so a warp does not diverge per vector.
+// Each warp keeps its own threshold (the seed records give every warp the
+// row's top-id threshold at the start).
 template <typename In>
 __device__ __forceinline__ void gumbel_chunk(const Chunk &q, int vbase, TState &s,
                                              const RowMode &rm, float gmax,
@@ -616,6 +615,12 @@ __device__ __forceinline__ void gumbel_chunk(const Chunk &q, int vbase, TState &
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     uint4 *qd = sm.gqd[w];
     uint32_t *qv = sm.gqv[w];
+    float cm = VT::hi_of(VT::pmax(q[0]));
+#pragma unroll
+    for (int k = 1; k < kVecsPerThread; ++k)
+        cm = fmaxf(cm, VT::hi_of(VT::pmax(q[k])));
+    if (!__any_sync(0xFFFFFFFFu, fmaf(cm, rm.invT, gmax) > s.g.thrS))
+        return;
 #pragma unroll
     for (int k = 0; k < kVecsPerThread; ++k) {
         const int idx = t + k * kConsumers;
@@ -1632,7 +1637,6 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
     const int lane = threadIdx.x & 31;
     const StageMeta &m0 = sm.meta[stage];
     const UnitHead uh{m0.unit, m0.lu, m0.b, m0.expect, m0.xid};
-    const int tslot = uh.lu % kStages;
     TState s;
     tstate_init(s);
     // a Gumbel-max row starts from the threshold of its top ids, scored
@@ -1647,8 +1651,6 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
         const StageMeta &mt = sm.meta[stage];
         const int nv = mt.nv, vbase = mt.vbase, last = mt.last;
         const uint4 *st = reinterpret_cast<const uint4 *>(stages + (size_t)stage * kStageBytes);
-        if (MODE & M_GUMBEL)
-            raise_thr(s.g, ord2f(*(volatile uint32_t *)&sm.thr[tslot]));
         do_chunk<In, MODE>(st, nv, vbase, s, rm, gmax, gt, sm);
         if (uh.xid >= 0) {
             // the thread that holds the draft token's vector records its logit
@@ -1656,10 +1658,6 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
             const int iv = uh.xid / E - vbase;
             if (iv >= 0 && iv < nv && (int)threadIdx.x == iv % kConsumers)
                 s.xd = VecTraits<In>::elem(st[iv], uh.xid % E);
-        }
-        if ((MODE & M_GUMBEL) && s.g.thr > s.pub) {
-            atomicMax(&sm.thr[tslot], f2ord(s.g.thr));
-            s.pub = s.g.thr;
         }
         __syncwarp();
         if (lane == 0)
@@ -1804,8 +1802,6 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
         }
-        for (int s = 0; s < kStages; ++s)
-            sm.thr[s] = f2ord(-INFINITY);
         for (int q = 0; q < kUnitSlots; ++q) {
             mbar_init(&sm.ubar[q], kConsumerWarps);
             mbar_init(&sm.ufree[q], 1);
@@ -1876,8 +1872,6 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
                     mt.xid = ce.xid;
                     mt.row = ce.row;
                     mt.rm = ce.rm;
-                    if (v == ce.vs)
-                        sm.thr[lu % kStages] = f2ord(-INFINITY);
                     mbar_arrive_tx(&sm.full[stage], (uint32_t)nv * 16u);
                     bulk_g2s(stages + (size_t)stage * kStageBytes, ce.row + (int64_t)v * 16,
                              (uint32_t)nv * 16u, &sm.full[stage]);

@@ -48,7 +48,8 @@
  *   environment variable SV_FAULT_INJECT="call:code[,call:code...]" makes
  *   each listed entry point (sv_create, sv_verify_greedy,
  *   sv_verify_greedy_static, sv_verify_sample, sv_verify_tree,
- *   sv_verify_spot, sv_packed_step, sv_packed_anyorder_step) return the
+ *   sv_verify_spot, sv_packed_step, sv_packed_topk_step,
+ *   sv_packed_anyorder_step) return the
  *   status `code` (1..6) at its launch point,
  *   after its argument checks and before anything is enqueued.  It is read
  *   at every call; unset, nothing is injected.
@@ -297,6 +298,50 @@ sv_status sv_packed_step(sv_handle *h, const void *logits, sv_dtype dtype, int64
                          void *stream);
 
 /* ---------------------------------------------------------------------------
+ * One Packed-SS iteration at T > 0 with top-k truncated distributions
+ * ([PackedSS] §3.2, last paragraph: with top-k truncation only the nonzero
+ * entries of the stored drafter distribution Q need to be kept; Alg. 2).
+ *   Truncation keeps a row's k largest logits (ties to the lowest id) and
+ *   renormalises softmax(x/T) over them: kp entries for the target p of
+ *   verify rows, kq for the drafter Q of proposal rows (1 <= kp, kq <=
+ *   min(64, V)).
+ *   logits [B, K+W, V], prev_draft, prev_len, pos_base, eos_id, remaining,
+ *   seed, iter and the outputs shared with sv_packed_step mean what they
+ *   mean there (K, W <= 32).
+ *   prev_q_ids [B, W, kq] (int32), prev_q_probs [B, W, kq] (float32): the
+ *     previous call's drafter lists (its q_ids / q_probs); Q_{t-1}^(i) is
+ *     list prev_q_offset[b] + i (Alg. 2 line 12).  Each draft token must be
+ *     in its list.
+ *   Verify position i: accept d_i w.p. min{1, p(d_i)/Q(d_i)}, p(d) = 0 off
+ *   the target list.  First rejection h: the correction is the Gumbel-max
+ *   over v with [p(v) - Q(v)]_+ > 0 of log [p(v) - Q(v)]_+ + G(key (seed,
+ *   SAMPLE, b, pos_base + h, 0)); no rejection: the bonus is the Gumbel-max
+ *   of x/T + G over the target list.  Proposal j: z_j is the Gumbel-max of
+ *   y_j/T + G(key (seed, DRAFT, b, pos_base + j, iter)) over its list.
+ * Outputs: accept_len, commit_len, committed, next_draft, next_len,
+ *   next_q_at_draft (optional) as in sv_packed_step; q_ids [B, W, kq] and
+ *   q_probs [B, W, kq]: every proposal row's list (ids by logit desc, id
+ *   asc) and truncated probabilities, to be passed back as prev_q_ids /
+ *   prev_q_probs; flags [B] (optional: acceptance tests within 1e-9 and
+ *   Gumbel-max top-two gaps below 1e-9).
+ *   Every row the step needs is read once (a streaming top-k selection);
+ *   the decisions run in fp64 on the lists.  The caller's buffers are not
+ *   kept; the handle's workspace holds B (K+W) 64 (logit, id) pairs.
+ * Errors: SV_ERR_INVALID_ARG (shapes, T <= 0, kp or kq out of range);
+ *   latched SV_ERR_DEVICE_BOUNDS for prev_len or prev_q_offset out of range,
+ *   or a draft token missing from its stored list.
+ * ------------------------------------------------------------------------- */
+sv_status sv_packed_topk_step(sv_handle *h, const void *logits, sv_dtype dtype,
+                              int64_t row_stride, int B, int K, int W, int V, int kp, int kq,
+                              const int32_t *prev_draft, const int32_t *prev_len,
+                              const int32_t *prev_q_ids, const float *prev_q_probs,
+                              const int32_t *prev_q_offset, float T, uint64_t seed, uint64_t iter,
+                              const int64_t *pos_base, int32_t eos_id, const int32_t *remaining,
+                              int32_t *accept_len, int32_t *commit_len, int32_t *committed,
+                              int32_t *next_draft, int32_t *next_len, float *next_q_at_draft,
+                              int32_t *q_ids, float *q_probs, int32_t *flags, void *stream);
+
+/* ---------------------------------------------------------------------------
  * One iteration of Packed-SS with any-order greedy verification ([PackedSS]
  * App. C "Procedure", Alg. 3 lines 6-15, eq. 8; confidence scores of App.
  * E.6 "Confidence scores").
@@ -340,8 +385,9 @@ sv_status sv_packed_anyorder_step(sv_handle *h, const void *logits, sv_dtype dty
  *   SV_OPT_TIMING_EVENTS: value is a pointer to two cudaEvent_t (start, stop)
  *     recorded around the streaming pass of the next calls, together with
  *     the kernels that prepare it (SPOT state masks, any-order preparation,
- *     the seed records of Gumbel-max rows); 0 = off.  The events stay owned
- *     by the caller.
+ *     the seed records of Gumbel-max rows), or around the top-k selection
+ *     of sv_packed_topk_step; 0 = off.  The events stay owned by the
+ *     caller.
  * ------------------------------------------------------------------------- */
 typedef enum { SV_OPT_FORCE_RESCUE = 1, SV_OPT_TIMING_EVENTS = 2 } sv_option;
 sv_status sv_set_option(sv_handle *h, sv_option opt, int64_t value);
