@@ -827,12 +827,15 @@ sv_status sv_packed_topk_step(sv_handle *h, const void *logits, sv_dtype dtype,
     t.flags = flags;
     t.err = h->d_err;
     if (sv_status fi = fault_injected("sv_packed_topk_step")) return fi;
-    // workspace: the sorted list of every row, kTopkMax logits and ids
+    // workspace: the sorted list of every row (kTopkMax logits, ids and
+    // Gumbel values) and its log-sum-exp
     const size_t rows = (size_t)B * (K + W);
-    sv_status st = ensure_ws(h, rows * kTopkMax * 8, s);
+    sv_status st = ensure_ws(h, rows * (kTopkMax * 16 + 8), s);
     if (st != SV_OK) return st;
-    t.lval = (float *)h->ws;
-    t.lid = (int32_t *)(h->ws + rows * kTopkMax * 4);
+    t.lg = (double *)h->ws;
+    t.lL = (double *)(h->ws + rows * kTopkMax * 8);
+    t.lval = (float *)(h->ws + rows * (kTopkMax * 8 + 8));
+    t.lid = (int32_t *)(h->ws + rows * (kTopkMax * 12 + 8));
     if (h->timing) cudaEventRecord(h->ev[0], s);
     cudaError_t e = topk_select_launch(t, s);
     if (h->timing) cudaEventRecord(h->ev[1], s);

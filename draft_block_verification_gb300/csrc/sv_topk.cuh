@@ -34,6 +34,8 @@ struct TopkJob {
     const uint64_t *skip;         // skip thresholds of the top-id draws
     float *lval;                  // [B * (K+W), kTopkMax] list logits (workspace)
     int32_t *lid;                 // [B * (K+W), kTopkMax] list ids (workspace)
+    double *lg;                   // [B * (K+W), kTopkMax] Gumbel value of each entry
+    double *lL;                   // [B * (K+W)] log-sum-exp of the list at T
     int32_t *acc, *commit_len, *committed, *next_draft, *next_len;
     float *next_q;                // [B, W] (optional)
     int32_t *q_ids;               // [B, W, kq]
