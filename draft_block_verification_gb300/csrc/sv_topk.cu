@@ -321,6 +321,7 @@ __global__ void __launch_bounds__(kTdThreads) topk_decide_kernel(const __grid_co
     __shared__ double Lrow[kTdRows];
     __shared__ int hs, as_, zs[kMaxK];
     __shared__ double qzs[kMaxK], gaps[kMaxK];
+    __shared__ uint64_t rkey[kMaxK];  // the proposal rows' draft keys
     __shared__ int nfl;
     pdl_wait();
     pdl_trigger();
@@ -341,16 +342,15 @@ __global__ void __launch_bounds__(kTdThreads) topk_decide_kernel(const __grid_co
     const int64_t row0 = (int64_t)b * R;
     // local row q: verify rows 0..n are q = 0..n, proposal j is q = K + j
     auto gro = [&](int q) { return row0 + q; };
-    auto kof = [&](int q) { return q < j.K ? j.kp : j.kq; };
 
-    // ---- 1. list terms and log-sum-exps ----
-    const int items = (n + 1) * kTopkMax;
+    // ---- 1. list terms and log-sum-exps (entries spread over all threads) ----
+    if (t < j.W)
+        rkey[t] = rng_key(j.seed, kDraft, (uint64_t)b, p0 + t, j.iter);
+    const int items = (n + 1) * j.kp;
     for (int it = t; it < items; it += kTdThreads) {
-        const int q = it / kTopkMax, e = it - q * kTopkMax;
-        if (e < j.kp) {
-            const float *xv = j.lval + gro(q) * kTopkMax;
-            ex[q][e] = exp((double)xv[e] / T - (double)xv[0] / T);
-        }
+        const int q = it / j.kp, e = it - q * j.kp;
+        const float *xv = j.lval + gro(q) * kTopkMax;
+        ex[q][e] = exp((double)xv[e] / T - (double)xv[0] / T);
     }
     __syncthreads();
     for (int qi = t; qi < n + 1 + j.W; qi += kTdThreads) {
@@ -408,20 +408,24 @@ __global__ void __launch_bounds__(kTdThreads) topk_decide_kernel(const __grid_co
     __syncthreads();
     const int h = hs;
 
-    // ---- 3. scores: row h's correction / bonus terms, proposal terms ----
-    const int items3 = (1 + j.W) * kTopkMax;
+    // ---- 3. scores: row h's correction / bonus terms (every second thread,
+    // so that the fp64 work spreads over the warps), then the proposal terms
+    const uint64_t hkey = rng_key(j.seed, kSample, (uint64_t)b, p0 + h, 0);
+    const int items3 = 2 * j.kp + j.W * j.kq;
     for (int it = t; it < items3; it += kTdThreads) {
-        const int qi = it / kTopkMax, e = it - qi * kTopkMax;
-        const int q = qi == 0 ? h : j.K + qi - 1;
-        if (e >= kof(q))
+        const bool corr = it < 2 * j.kp;
+        if (corr && (it & 1))
             continue;
+        const int qi = corr ? 0 : 1 + (it - 2 * j.kp) / j.kq;
+        const int e = corr ? it >> 1 : (it - 2 * j.kp) - (qi - 1) * j.kq;
+        const int q = qi == 0 ? h : j.K + qi - 1;
         const int64_t gr = gro(q);
         const int v = j.lid[gr * kTopkMax + e];
         const double x = (double)j.lval[gr * kTopkMax + e] / T;
         double w = x;
         uint64_t key;
         if (qi == 0) {
-            key = rng_key(j.seed, kSample, (uint64_t)b, p0 + h, 0);
+            key = hkey;
             if (h < n) {
                 const int32_t *qv = j.prev_q_ids + ((int64_t)b * j.W + off + h) * j.kq;
                 const float *qp = j.prev_q_probs + ((int64_t)b * j.W + off + h) * j.kq;
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(kTdThreads) topk_decide_kernel(const __grid_co
                     ? -INFINITY
                     : w + gumbel64(fine52(key, (uint32_t)v), is_top(key, (uint32_t)v, j.skip));
         } else {
-            key = rng_key(j.seed, kDraft, (uint64_t)b, p0 + (qi - 1), j.iter);
+            key = rkey[qi - 1];
             const int64_t o = ((int64_t)b * j.W + (qi - 1)) * j.kq + e;
             j.q_ids[o] = v;
             j.q_probs[o] = expf((float)(x - Lrow[q]));
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(kTdThreads) topk_decide_kernel(const __grid_co
         double gap = INFINITY;  // certified: above 1e-9
         if (!((double)iv[jj][eb].x - 1e-9 > (double)ho)) {
             // not certified in fp32: the row's scores in fp64
-            const uint64_t key = rng_key(j.seed, kDraft, (uint64_t)b, p0 + jj, j.iter);
+            const uint64_t key = rkey[jj];
             double zb = -INFINITY, z2 = -INFINITY;
             z = -1;
             for (int e = 0; e < j.kq; ++e) {
