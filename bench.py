@@ -485,16 +485,16 @@ class Workload:
 
     def launches(self):
         """Library kernels per call: the streaming pass; the seed kernel
-        before it when rows carry a Gumbel-max (a sampling call's bonus rows;
-        trees, SPOT and Packed-SS steps at T > 0); the residual pass and the
-        fp64 check after a sampling call or a Packed-SS step at T > 0 (and
-        the TV pass when TV is asked for); the per-sequence preparation of a
-        SPOT or any-order call.  The truncated Packed-SS step is a selection
-        and a decision kernel."""
+        before it when rows carry a Gumbel-max (trees, SPOT and Packed-SS
+        steps at T > 0); the residual pass (the correction or the bonus
+        token) and the fp64 check after a sampling call or a Packed-SS step
+        at T > 0 (and the TV pass when TV is asked for); the per-sequence
+        preparation of a SPOT or any-order call.  The truncated Packed-SS step
+        is a selection and a decision kernel."""
         if self.kind == "packed_topk":
             return 2
         if self.kind == "sample":
-            return 5 if self.tv else 4
+            return 4 if self.tv else 3
         if self.kind == "anyorder":
             return 2
         if self.kind == "spot":

@@ -119,7 +119,7 @@ static __device__ RowM merge_row(const Job &j, int b, int slot, double r1, doubl
     // a Gumbel-max row's top ids were scored before the stream (seed
     // records, one per chunk of the row); the stream skipped them
     if (j.seeds) {
-        const int k = gumbel_index(j, slot, clamp_len(j, b));
+        const int k = gumbel_index(j, slot);
         if (k >= 0) {
             const SeedRec *sr =
                 j.seeds + ((int64_t)b * gumbel_rows(j) + k) * j.seed_chunks;

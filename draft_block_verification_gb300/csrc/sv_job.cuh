@@ -11,7 +11,8 @@ struct __align__(16) ResidEntry {
     int b;          // sequence
     int h;          // position of the first rejection (row index)
     int need_lq;    // 1: the q row's log-sum-exp is not known yet (Packed-SS)
-    int pad;
+    int bonus;      // 1: every draft was accepted; the draw is the bonus token,
+                    // the Gumbel-max of x/Tp over the p row (no q row)
     const char *prow;  // target row at position h
     const char *qrow;  // proposal row at position h
     double Lp, Lq;     // natural log-sum-exps of x/Tp and y/Tq
@@ -38,7 +39,8 @@ struct __align__(16) RescueEntry {
     int resid;      // the fp64 path draws a residual at position h
     double Lp, Lq;  // fp64 log-sum-exps of the residual pair
     int flags;      // near-threshold decisions found by the fp64 path so far
-    int pad[3];
+    int bonus;      // the draw at h is the bonus token (every draft accepted)
+    int pad[2];
 };
 
 // Per-draft-row results of a Packed-SS proposal, kept for the fp64 path.
@@ -216,39 +218,34 @@ __device__ __forceinline__ int64_t pos0_of(const Job &j, int b)
     return j.pos_base ? __ldg(j.pos_base + b) : 0;
 }
 
-// Gumbel-max rows: per sequence, the bonus row of a sampling call; the
-// bonus row and the W proposal rows of a Packed-SS step at T > 0; every node
-// row of a tree at T > 0; every (state, position) row of a SPOT call at
-// T > 0.  Row k of sequence b has index b * gumbel_rows(j) + k.
+// Gumbel-max rows of the streaming pass: per sequence, the W proposal rows
+// of a Packed-SS step at T > 0; every node row of a tree at T > 0; every
+// (state, position) row of a SPOT call at T > 0.  Row k of sequence b has
+// index b * gumbel_rows(j) + k.  (The bonus draw of a sampling call or a
+// Packed-SS step is needed only when every draft is accepted; the residual
+// pass takes it then, from the bonus row alone.)
 __host__ __device__ __forceinline__ int gumbel_rows(const Job &j)
 {
     switch (j.kind) {
-    case K_SAMPLE: return 1;
-    case K_PACKED: return j.Tp != 0.f ? 1 + j.W : 0;
+    case K_PACKED: return j.Tp != 0.f ? j.W : 0;
     case K_TREE: return j.Tp != 0.f ? j.N : 0;
     case K_SPOT: return j.Tp != 0.f ? (j.N + 1) * j.L : 0;
     default: return 0;
     }
 }
 
-// Row slot of Gumbel-max row k of sequence b (n: the sequence's clamped
-// draft length, which places the bonus row).
-__device__ __forceinline__ int gumbel_slot(const Job &j, int k, int n)
+// Row slot of Gumbel-max row k of a sequence.
+__device__ __forceinline__ int gumbel_slot(const Job &j, int k)
 {
-    if (j.kind == K_SAMPLE) return n;
-    if (j.kind == K_PACKED) return k == 0 ? n : j.K + k - 1;
-    return k;  // tree, SPOT
+    return j.kind == K_PACKED ? j.K + k : k;  // proposal rows; tree and SPOT rows
 }
 
-// Index k of the Gumbel-max row in `slot` of a sequence with clamped draft
-// length n, or -1 when that row carries no Gumbel-max.
-__device__ __forceinline__ int gumbel_index(const Job &j, int slot, int n)
+// Index k of the Gumbel-max row in `slot`, or -1 when that row carries no
+// Gumbel-max.
+__device__ __forceinline__ int gumbel_index(const Job &j, int slot)
 {
     switch (j.kind) {
-    case K_SAMPLE: return slot == n ? 0 : -1;
-    case K_PACKED:
-        if (j.Tp == 0.f) return -1;
-        return slot == n ? 0 : (slot >= j.K ? 1 + slot - j.K : -1);
+    case K_PACKED: return (j.Tp != 0.f && slot >= j.K) ? slot - j.K : -1;
     case K_TREE:
     case K_SPOT: return j.Tp != 0.f ? slot : -1;
     default: return -1;

@@ -107,7 +107,7 @@ struct UnitPre {
     int len;       // draft length as given (unclamped)
     int64_t p0;    // absolute position of the sequence's first row
     int np;        // tree: position of the node (T > 0)
-    int ida, idb;  // draft tokens of the two slots a light unit can map to
+    int ida;       // the draft token a light unit's row is tested on (or -1)
     uint64_t smask;   // SPOT: masked positions of the unit's state
     unsigned svalid;  // SPOT: rows the tree streams
 };
@@ -118,11 +118,7 @@ struct UnitPre {
 // sequence.  A unit is one part of one row.
 __device__ __forceinline__ int heavy_rows(const Job &j)
 {
-    if (j.kind == K_SAMPLE)
-        return 1;  // the bonus row
-    if (j.kind == K_PACKED && j.Tp != 0.f)
-        return 1 + j.W;  // the bonus row and the proposal rows
-    return 0;
+    return (j.kind == K_PACKED && j.Tp != 0.f) ? j.W : 0;  // the proposal rows
 }
 
 // Sequence of unit u (needs no per-sequence data).
@@ -145,13 +141,20 @@ __device__ __forceinline__ void unit_map(const Job &j, long long u, int b, int n
         const long long rem = u - (long long)b * H * j.parts;
         const int r = (int)(rem / j.parts);
         part = (int)(rem - (long long)r * j.parts);
-        slot = r == 0 ? n : j.K + r - 1;
+        slot = j.K + r;
     } else {
         const long long rem = (u - nh) - (long long)b * (j.rows_per_seq - H) * j.parts;
         const int r = (int)(rem / j.parts);
         part = (int)(rem - (long long)r * j.parts);
-        slot = (H > 0 && r >= n) ? r + 1 : r;
+        slot = r;
     }
+}
+
+// Calls whose rows record the logit at a draft token: the target and drafter
+// rows of a sampling call, the verify rows of a Packed-SS step at T > 0.
+__device__ __forceinline__ bool has_drafts(const Job &j)
+{
+    return j.kind == K_SAMPLE || (j.kind == K_PACKED && j.Tp != 0.f);
 }
 
 // Draft position whose token the row in `slot` is tested on (sample: target
@@ -176,18 +179,16 @@ __device__ __forceinline__ int draft_token(const Job &j, int b, int slot)
 
 __device__ __forceinline__ UnitPre unit_prefetch(const Job &j, long long u)
 {
-    UnitPre p{0, 0, 0, -1, -1, 0ull, 0u};
+    UnitPre p{0, 0, 0, -1, 0ull, 0u};
     if (u >= j.total_units)
         return p;
     const int b = unit_seq(j, u);
     const int H = heavy_rows(j);
     const long long nh = (long long)j.B * H * j.parts;
-    if (H > 0 && u >= nh) {
-        // a light unit's slot is r or r + 1 (the bonus slot is skipped)
+    if (has_drafts(j) && u >= nh) {
+        // a light unit's slot is its rank among the light rows
         const long long rem = (u - nh) - (long long)b * (j.rows_per_seq - H) * j.parts;
-        const int r = (int)(rem / j.parts);
-        p.ida = draft_token(j, b, r);
-        p.idb = draft_token(j, b, r + 1);
+        p.ida = draft_token(j, b, (int)(rem / j.parts));
     }
     p.len = j.kind == K_TREE ? j.N : (j.lens ? __ldg(j.lens + b) : (j.kind == K_PACKED ? 0 : j.K));
     p.p0 = j.pos_base ? __ldg(j.pos_base + b) : 0;
@@ -250,17 +251,7 @@ __device__ __forceinline__ RowMode row_mode(const Job &j, int b, int slot, int n
         break;
     case K_SAMPLE:
         r.mode = M_LSE;
-        if (slot <= j.K) {
-            r.c1 = j.cp;
-            if (slot == n) {  // bonus row: Gumbel-max of x_n / Tp
-                r.mode |= M_GUMBEL;
-                r.invT = j.invTp;
-                r.T = j.Tp;
-                r.key = rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0);
-            }
-        } else {
-            r.c1 = j.cq;
-        }
+        r.c1 = slot <= j.K ? j.cp : j.cq;
         break;
     case K_TREE:
         if (j.Tp == 0.f) {
@@ -303,12 +294,6 @@ __device__ __forceinline__ RowMode row_mode(const Job &j, int b, int slot, int n
             } else {
                 r.mode = M_LSE;
                 r.c1 = j.cp;
-                if (slot == n) {
-                    r.mode |= M_GUMBEL;
-                    r.invT = j.invTp;
-                    r.T = j.Tp;
-                    r.key = rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0);
-                }
             }
         } else {
             const int jj = slot - j.K;
@@ -350,12 +335,10 @@ __device__ __forceinline__ UnitInfo unit_info(const Job &j, long long u, const U
     i.rec = (int)(((long long)i.b * j.rows_per_seq + i.slot) * j.parts + i.part);
     i.xid = -1;
     const int H = heavy_rows(j);
-    if (H > 0 && u >= (long long)j.B * H * j.parts) {
+    if (has_drafts(j) && u >= (long long)j.B * H * j.parts) {
         const int pos = draft_pos(j, i.slot);
         if (pos >= 0 && pos < n) {
-            const long long rem =
-                (u - (long long)j.B * H * j.parts) - (long long)i.b * (j.rows_per_seq - H) * j.parts;
-            const int d = (i.slot == (int)(rem / j.parts)) ? p.ida : p.idb;
+            const int d = p.ida;
             if (d < 0 || d >= j.V)
                 latch(j.err, SV_ERR_DEVICE_BOUNDS);  // tested as probability 0
             else
@@ -375,7 +358,7 @@ __device__ __forceinline__ UnitInfo unit_info(const Job &j, long long u, const U
     }
     i.rm = row_mode(j, i.b, i.slot, n, p.p0, p.np);
     if ((i.rm.mode & M_GUMBEL) && j.seeds) {
-        const int k = gumbel_index(j, i.slot, n);
+        const int k = gumbel_index(j, i.slot);
         const SeedRec *sr = j.seeds + ((int64_t)i.b * gumbel_rows(j) + k) * j.seed_chunks;
         for (int q = 0; q < j.seed_chunks; ++q)
             i.rm.thr0 = fmaxf(i.rm.thr0, __ldcg(&sr[q].thr));
@@ -781,13 +764,9 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
     double eqh = __shfl_sync(0xFFFFFFFFu, eq, f & 31);
     const double lcloh = __shfl_sync(0xFFFFFFFFu, lclo, f & 31);
     const double lchih = __shfl_sync(0xFFFFFFFFu, lchi, f & 31);
-    // bonus row n (always valid): its Gumbel-max with key (SAMPLE, pos + n),
-    // resolved by the lane that holds its record
-    GRes g = resolve_lanes(j, row_ptr(j, b, lane <= j.K ? lane : 0),
-                           rng_key(j.seed, kSample, (uint64_t)b, p0 + lane, 0), (double)j.Tp,
-                           j.invTp, rp.gc, lane == n);
-    const int gbv = __shfl_sync(0xFFFFFFFFu, g.v, n);
-    const int gbf = __shfl_sync(0xFFFFFFFFu, g.flag, n);
+    // bonus row n (always valid): its log-sum-exp; its Gumbel-max with key
+    // (SAMPLE, pos + n) is drawn by the residual pass, and only when every
+    // draft is accepted
     const double Lb = __shfl_sync(0xFFFFFFFFu, rp.L1a, n);
     const float mb = __shfl_sync(0xFFFFFFFFu, rp.m, n);
     if (lane == 0) {
@@ -795,27 +774,24 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
         RowStat *sb = j.rs_stat + (int64_t)b * j.rows_per_seq + n;
         sb->L1 = Lb;
         sb->m = mb;
-        sb->gidx = gbv;
-        sb->gflag = gbf;
         if (rescue) {
             unsigned e = atomicAdd(j.ctl + C_RESCUE_N, 1u);
             j.rescue[e].b = b;
             j.rescue[e].kind = 0;
             j.rescue[e].h = 0;
-        } else if (f == n) {
-            j.acc[b] = n;
-            j.next[b] = gbv;
-            if (j.flags) j.flags[b] = gbf;
+            j.rescue[e].bonus = 0;
         } else {
+            // the correction at the first rejection f < n, or the bonus
+            // token when f == n: both by the residual pass
             j.acc[b] = f;
             unsigned e = atomicAdd(j.ctl + C_RESID_N, 1u);
             ResidEntry re;
             re.b = b;
             re.h = f;
             re.need_lq = 0;
-            re.pad = 0;
+            re.bonus = f == n;
             re.prow = row_ptr(j, b, f);
-            re.qrow = row_ptr(j, b, j.K + 1 + f);
+            re.qrow = f == n ? re.prow : row_ptr(j, b, j.K + 1 + f);
             re.Lp = Lph;
             re.Lq = Lqh;
             re.epsp = eph;
@@ -1034,19 +1010,14 @@ static __device__ __noinline__ void fin_packed(const Job &j, int b)
             j.rescue[e].b = b;
             j.rescue[e].kind = 0;
             j.rescue[e].h = 0;
+            j.rescue[e].bonus = 0;
         }
         return;
     }
-    if (f == n) {
-        RowM rb = merge_row(j, b, n, j.crp, 1.0);
-        GRes g = resolve_lanes(j, row_ptr(j, b, n),
-                               rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0), (double)j.Tp,
-                               j.invTp, rb.gc, lane == 0);
-        int c = __shfl_sync(0xFFFFFFFFu, g.v, 0);
-        int fl = __shfl_sync(0xFFFFFFFFu, g.flag, 0);
-        packed_commit(j, b, n, c, true, fl);
-        return;
-    }
+    // The token at position f -- the correction from [p - Q]_+ after a
+    // rejection, or the bonus (the Gumbel-max of row n) when every draft is
+    // accepted -- is drawn by the residual pass; it is the last committed
+    // token, so the stopping index does not depend on it.
     packed_commit(j, b, f, -1, false, 0);
     if (lane == 0) {
         int off = __ldg(j.prev_off + b);
@@ -1054,10 +1025,10 @@ static __device__ __noinline__ void fin_packed(const Job &j, int b)
         ResidEntry re;
         re.b = b;
         re.h = f;
-        re.need_lq = 1;
-        re.pad = 0;
+        re.need_lq = f < n;
+        re.bonus = f == n;
         re.prow = row_ptr(j, b, f);
-        re.qrow = j.src2 + ((int64_t)b * j.W + off + f) * j.rs;
+        re.qrow = f < n ? j.src2 + ((int64_t)b * j.W + off + f) * j.rs : re.prow;
         re.Lp = Lph;
         re.Lq = 0.0;
         re.epsp = eph;
@@ -1694,8 +1665,6 @@ __device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsi
     if constexpr (KIND == K_GREEDY) {
         return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
     } else if constexpr (KIND == K_SAMPLE) {
-        if (m & M_GUMBEL)
-            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
         return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
     } else if constexpr (KIND == K_TREE) {
         if (m & M_GUMBEL)
@@ -1713,8 +1682,6 @@ __device__ __forceinline__ bool unit_dispatch(const Job &j, PassShared &sm, unsi
         switch (m) {
         case M_ARGMAX: return unit_loop<In, M_ARGMAX>(j, sm, stages, gt, stage, phase, rm);
         case M_LSE: return unit_loop<In, M_LSE>(j, sm, stages, gt, stage, phase, rm);
-        case M_LSE | M_GUMBEL:
-            return unit_loop<In, M_LSE | M_GUMBEL>(j, sm, stages, gt, stage, phase, rm);
         case M_ARGMAX | M_LSE:
             return unit_loop<In, M_ARGMAX | M_LSE>(j, sm, stages, gt, stage, phase, rm);
         case M_GUMBEL | M_LSE | M_MAX:
@@ -2117,7 +2084,7 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
         const long long g = it / j.seed_chunks;
         const int b = (int)(g / H), k = (int)(g % H);
         const int n = clamp_len(j, b);
-        const int slot = gumbel_slot(j, k, n);
+        const int slot = gumbel_slot(j, k);
         bool valid = true;
         int np = 0;
         if (j.kind == K_SPOT)

@@ -790,6 +790,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         int i = (it / (kRescueChunks * 2)) % kMaxPairs;
         int e = it / (kRescueChunks * 2 * kMaxPairs);
         RescueEntry re = j.rescue[e];
+        if (re.kind == 1 && re.bonus) continue;  // a bonus draw needs no log-sum-exp
         int lo = (re.kind == 0) ? 0 : re.h;
         int hi = (re.kind == 0) ? clamp_len(j, re.b) : re.h + 1;
         if (i < lo || i >= hi) continue;
@@ -814,6 +815,13 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         const int b = re.b;
         const int n = clamp_len(j, b);
         const bool cactus = j.kind == K_SAMPLE && j.amode == SV_LENIENT_CACTUS;
+        if (re.kind == 1 && re.bonus) {
+            if (lane == 0) {
+                j.rescue[e].resid = 1;
+                j.rescue[e].flags = 0;
+            }
+            continue;
+        }
         if (re.kind == 1) {
             if (lane == 0) {
                 double Lp = merge64(j, e, re.h, 0);
@@ -869,6 +877,7 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
             if (lane == 0) {
                 j.rescue[e].h = h;
                 j.rescue[e].resid = 1;
+                j.rescue[e].bonus = 0;
                 j.rescue[e].Lp = Lph;
                 j.rescue[e].Lq = Lqh;
                 j.rescue[e].flags = nfl;
@@ -876,25 +885,14 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
             }
             continue;
         }
-        // every draft accepted: the bonus token is the fast path's exact
-        // Gumbel-max of row n
-        if (j.kind == K_SAMPLE) {
-            if (lane == 0) {
-                RowStat sb = j.rs_stat[(int64_t)b * j.rows_per_seq + n];
-                j.acc[b] = n;
-                j.next[b] = sb.gidx;
-                if (j.flags) j.flags[b] = nfl + sb.gflag;
-                j.rescue[e].resid = 0;
-            }
-        } else {
-            RowM rb = merge_row(j, b, n, j.crp, 1.0);
-            GRes g = resolve_lanes(j, slot_row(j, b, n),
-                                   rng_key(j.seed, kSample, (uint64_t)b, p0 + n, 0), (double)j.Tp,
-                                   j.invTp, rb.gc, lane == 0);
-            if (lane == 0) j.rescue[e].resid = 0;
-            int c = __shfl_sync(0xFFFFFFFFu, g.v, 0);
-            int gf = __shfl_sync(0xFFFFFFFFu, g.flag, 0);
-            packed_commit(j, b, n, c, true, nfl + gf);
+        // every draft accepted: the bonus token, the Gumbel-max of row n,
+        // drawn in fp64 by the residual phase below
+        if (lane == 0) {
+            j.rescue[e].h = n;
+            j.rescue[e].resid = 1;
+            j.rescue[e].bonus = 1;
+            j.rescue[e].flags = nfl;
+            if (j.kind == K_SAMPLE) j.acc[b] = n;
         }
     }
     if (!grid_sync(j)) return;
@@ -905,10 +903,16 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
         int e = it / kResidChunks, c = it % kResidChunks;
         RescueEntry re = j.rescue[e];
         if (!re.resid) continue;
-        double D = re.Lq - re.Lp;
-        double eD = 1e-10 * (1.0 + fabs(re.Lp) + fabs(re.Lq));
         RCtx ctx;
-        fill_ctx(j, ctx, pair_row(j, re.b, re.h, 0), pair_row(j, re.b, re.h, 1), D, eD);
+        if (re.bonus) {
+            const char *row = slot_row(j, re.b, re.h);
+            fill_ctx(j, ctx, row, row, 0.0, 0.0);
+            ctx.bonus = true;
+        } else {
+            double D = re.Lq - re.Lp;
+            double eD = 1e-10 * (1.0 + fabs(re.Lp) + fabs(re.Lq));
+            fill_ctx(j, ctx, pair_row(j, re.b, re.h, 0), pair_row(j, re.b, re.h, 1), D, eD);
+        }
         ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
         Track64 tr;
         resid_scan<In>(ctx, chunk_lo(j.nvec, c, kResidChunks),

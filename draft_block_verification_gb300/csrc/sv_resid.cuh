@@ -9,6 +9,8 @@
 // fp64 rounding on the fp64 path).  The scan uses the three-level filter of
 // sv_gumbel.cuh: the table bound ignores log(1 - .) <= 0, survivors get fp32
 // intervals, and the two best candidates are certified or re-scored in fp64.
+// A bonus draw (every draft accepted) is the same scan with the score
+// a_v + G(v) alone (no q row; the common -Lp dropped).
 #pragma once
 
 #include "sv_common.cuh"
@@ -25,6 +27,7 @@ struct RCtx {
     double Tp, Tq, dlo, dhi;
     float invTp, invTq, dlo32, dhi32;  // [dlo32, dhi32] contains [dlo, dhi]
     uint64_t key;
+    bool bonus;  // the bonus draw: score x/Tp + G, the q row unused
 };
 
 // fp64 interval of the residual score of id v (Delta bracket only); false
@@ -33,6 +36,10 @@ __device__ __forceinline__ bool resid_interval64(const RCtx &c, float x, float y
                                                  bool top, double &lo, double &hi)
 {
     double z = (double)x / c.Tp, w = (double)y / c.Tq;
+    if (c.bonus) {
+        lo = hi = z + gumbel64(m, top);
+        return true;
+    }
     double ah = w - z - c.dhi;
     if (!(ah < 0.0))
         return false;
@@ -60,6 +67,12 @@ __device__ __forceinline__ float log1mexp32(float d, float &err)
 __device__ __forceinline__ bool resid_interval32(const RCtx &c, float x, float y, uint64_t m,
                                                  bool top, float &lo, float &hi)
 {
+    if (c.bonus) {
+        const float2 iv = logit_interval_m(x, c.invTp, m, top);
+        lo = iv.x;
+        hi = iv.y;
+        return true;
+    }
     const float z = x * c.invTp, w = y * c.invTq;
     const float dz = w - z;
     const float edz = (fabsf(z) + fabsf(w)) * 0x1p-21f;
@@ -93,6 +106,8 @@ __device__ __forceinline__ bool resid_interval32(const RCtx &c, float x, float y
 // fp32 test that w_v = 0 for every Delta in the bracket.
 __device__ __forceinline__ bool surely_zero(const RCtx &c, float x, float y)
 {
+    if (c.bonus)
+        return false;
     float a = x * c.invTp, b = y * c.invTq;
     float d = (b - a) - c.dhi32;
     return d > (fabsf(a) + fabsf(b) + fabsf(c.dhi32) + 1.f) * 0x1p-20f;
@@ -163,6 +178,7 @@ __device__ __forceinline__ void fill_ctx(const Job &j, RCtx &ctx, const char *pr
     ctx.invTq = (float)(1.0 / ctx.Tq);
     ctx.dlo32 = __double2float_rd(ctx.dlo);
     ctx.dhi32 = __double2float_ru(ctx.dhi);
+    ctx.bonus = false;
 }
 
 // Scores every top id of ids [lo, hi) of the pair into tr.  Thread tid of
@@ -224,6 +240,7 @@ __device__ __forceinline__ void resid_ctx(const Job &j, const ResidEntry &re, RC
     ctx.dlo32 = __double2float_rd(ctx.dlo);
     ctx.dhi32 = __double2float_ru(ctx.dhi);
     ctx.key = rng_key(j.seed, kSample, (uint64_t)re.b, pos0_of(j, re.b) + re.h, 0);
+    ctx.bonus = re.bonus != 0;
 }
 
 // The correction of entry re from the merged candidates of its whole row
@@ -266,7 +283,8 @@ __device__ __forceinline__ void resid_resolve(const Job &j, const ResidEntry &re
         x.Lp = 0;
         x.Lq = 0;
         x.flags = 0;
-        x.pad[0] = x.pad[1] = x.pad[2] = 0;
+        x.bonus = re.bonus;
+        x.pad[0] = x.pad[1] = 0;
         j.rescue[k] = x;
     }
 }

@@ -98,14 +98,14 @@ def test_workload_launch_counts_and_tv_flag():
         d.update(kw)
         return argparse.Namespace(**d)
 
-    # a sampling call: seed kernel, streaming pass, residual pass, fp64 check
-    # (+ the TV pass)
+    # a sampling call: streaming pass, residual pass (correction or bonus),
+    # fp64 check (+ the TV pass)
     w = bench.Workload("lenient_sweep", args())
-    assert w.tv and w.launches() == 5 and w.point()["tv"] is True
+    assert w.tv and w.launches() == 4 and w.point()["tv"] is True
     w = bench.Workload("lenient_sweep", args(no_tv=True))
-    assert not w.tv and w.launches() == 4 and w.point()["tv"] is False
+    assert not w.tv and w.launches() == 3 and w.point()["tv"] is False
     w = bench.Workload("lossless_t1", args())
-    assert not w.tv and w.launches() == 4
+    assert not w.tv and w.launches() == 3
     assert bench.Workload("tree", args(T=1.0)).launches() == 2
     assert bench.Workload("tree", args(T=0.0)).launches() == 1
     assert bench.Workload("packed", args(T=1.0)).launches() == 4
