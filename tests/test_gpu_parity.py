@@ -78,6 +78,11 @@ SAMPLE_CASES = [
     ("f32", 5, 4, 4100, 3, 0.5, 0.7, 0.7, 1.0, True),
     ("bf16", 4, 5, 8200, 3, 3.0, 1.0, 1.0, 0.5, False),
     ("bf16", 4, 5, 8200, 3, 0.0, 1.0, 1.0, 0.5, True),
+    # enough rows for whole-row units (64 x 13 >= 4 x 152): rows of several
+    # stages with a ragged tail, the TV kernel over whole rows
+    ("bf16", 64, 6, 12296, 1, 2.0, 1.0, 1.0, 1.0, True),
+    ("f32", 64, 6, 6148, 0, 1.0, 0.7, 0.7, 0.5, True),
+    ("bf16", 64, 6, 12296, 3, 0.2, 1.0, 1.0, 0.5, False),
 ]
 
 
