@@ -20,6 +20,7 @@ cudaError_t pass_launch(const Job &j, int grid, cudaStream_t s);
 cudaError_t spot_prep_launch(const Job &j, cudaStream_t s);
 cudaError_t anyorder_prep_launch(const Job &j, cudaStream_t s);
 cudaError_t seed_launch(const Job &j, int grid, cudaStream_t s);
+cudaError_t seed_setup(int *blocks_per_sm);
 cudaError_t post_setup(int occ[2]);
 cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
                         cudaStream_t s);
@@ -34,10 +35,11 @@ struct sv_handle {
     int sms = 0;
     int pass_blocks = 1;   // resident streaming CTAs per SM
     int tv_blocks = 1;     // resident total-variation CTAs per SM
+    int seed_blocks = 1;   // resident seed CTAs per SM
     int *d_err = nullptr;
     unsigned *d_ctl = nullptr;
     float *d_gtab = nullptr;      // [kGTab] G bounds of ordinary ids
-    float *d_gtop = nullptr;      // [kGTab] G bounds of top ids
+    float *d_gtop = nullptr;      // [2 * kGTab] upper and lower G bounds of top ids
     uint64_t *d_skip = nullptr;   // [kSkipN] skip thresholds
     char *ws = nullptr;
     size_t ws_bytes = 0;
@@ -94,13 +96,24 @@ void gumbel_bound_table(float *t)
         t[c] = up_f32(-log(-log((double)(c + 1) * 255.0 / 65536.0)));
 }
 
+static float down_f32(double g)
+{
+    float f = (float)g;
+    if ((double)f > g) f = nextafterf(f, -INFINITY);
+    return nextafterf(f, -INFINITY);
+}
+
 // The same for top ids: w < (c + 1)/256 gives 1 - u = (1 - w)/256 >
-// (255 - c)/65536.  The last byte (w up to 1) has no finite bound.
+// (255 - c)/65536.  The last byte (w up to 1) has no finite bound.  Entries
+// kGTab.. hold the lower bounds: w >= c/256 gives 1 - u <= (256 - c)/65536,
+// rounded down with one more ulp of slack.
 void gumbel_top_bound_table(float *t)
 {
     for (int c = 0; c < kGTab - 1; ++c)
         t[c] = up_f32(-log(-log1p(-(double)(255 - c) / 65536.0)));
     t[kGTab - 1] = INFINITY;
+    for (int c = 0; c < kGTab; ++c)
+        t[kGTab + c] = down_f32(-log(-log1p(-(double)(256 - c) / 65536.0)));
 }
 
 // Skip thresholds C_g = ceil(2^64 (255/256)^g), g = 1..256 (entry 0 unused):
@@ -282,20 +295,17 @@ sv_status plan(sv_handle *h, Job &j, int rows_per_seq, cudaStream_t s, int tv_ch
     j.rTp = j.Tp > 0.f ? 1.0 / (double)j.Tp : 0.0;
     j.rTq = j.Tq > 0.f ? 1.0 / (double)j.Tq : 0.0;
     j.tv_chunks = tv_chunks;
-    // seed records: one per chunk of seed_bpw blocks of 256 ids of every
-    // Gumbel-max row.  A warp lists a chunk with its lanes kept busy by
-    // handing out blocks, so larger chunks waste fewer trips; the largest
-    // size that still gives every SM a full wave of seed warps (8 CTAs of 8
-    // warps) is taken, 32 blocks when even that size does not.
+    // seed spans: the blocks of 256 ids of every Gumbel-max row, end to end,
+    // in equal spans, one per seed warp of one resident wave (at least 32
+    // blocks, one per lane).  A row meets at most ceil(nblk / span) span
+    // boundaries, so it has that many records plus one.
     const int nblk = (j.V + 255) / 256;
     const long long grows = (long long)j.B * gumbel_rows(j);
-    j.seed_bpw = 32;
-    for (int bpw = 128; bpw > 32; bpw /= 2)
-        if (grows * ((nblk + bpw - 1) / bpw) >= 64LL * h->sms) {
-            j.seed_bpw = bpw;
-            break;
-        }
-    j.seed_chunks = (nblk + j.seed_bpw - 1) / j.seed_bpw;
+    const long long sblocks = grows * nblk;
+    const long long swarps = 8LL * h->seed_blocks * h->sms;
+    j.seed_span = (int)std::min<long long>(
+        std::max<long long>(32, (sblocks + swarps - 1) / swarps), 1LL << 30);
+    j.seed_chunks = grows ? (nblk + j.seed_span - 1) / j.seed_span + 1 : 0;
     const size_t seed_recs = (size_t)j.B * gumbel_rows(j) * j.seed_chunks;
     Layout L = layout(j.B, rows_per_seq, j.parts, j.K, j.W, tv_chunks,
                       j.kind == K_SPOT ? j.N + 1 : (j.kind == K_ANYORDER ? 1 : 0), seed_recs);
@@ -330,9 +340,10 @@ sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (j.seeds) {
-        // enough warps for every chunk, at most 8 CTAs of 256 threads per SM
-        const long long warps = (long long)j.B * gumbel_rows(j) * j.seed_chunks;
-        const int grid = (int)std::min<long long>((warps + 7) / 8, 8LL * h->sms);
+        // one warp per span (8 warps a CTA): at most one resident wave
+        const long long sblocks = (long long)j.B * gumbel_rows(j) * ((j.V + 255) / 256);
+        const long long warps = (sblocks + j.seed_span - 1) / j.seed_span;
+        const int grid = (int)((warps + 7) / 8);
         cudaError_t e = seed_launch(j, std::max(grid, 1), s);
         if (e != cudaSuccess) return cuda_status(e);
     }
@@ -380,17 +391,20 @@ sv_status sv_create(sv_handle **out)
     h->pass_blocks = std::max(nb, 1);
     if (e == cudaSuccess) e = post_setup(pb);
     h->tv_blocks = std::max(1, pb[0]);
+    int sb = 0;
+    if (e == cudaSuccess) e = seed_setup(&sb);
+    h->seed_blocks = std::max(1, sb);
     if (e == cudaSuccess) e = cudaMalloc(&h->d_err, sizeof(int));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_ctl, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_gtab, kGTab * sizeof(float));
-    if (e == cudaSuccess) e = cudaMalloc(&h->d_gtop, kGTab * sizeof(float));
+    if (e == cudaSuccess) e = cudaMalloc(&h->d_gtop, 2 * kGTab * sizeof(float));
     if (e == cudaSuccess) e = cudaMalloc(&h->d_skip, kSkipN * sizeof(uint64_t));
     if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_ctl, 0, C_NCTL * sizeof(unsigned));
     if (e == cudaSuccess) {
-        float t[kGTab];
+        float t[2 * kGTab];
         gumbel_bound_table(t);
-        e = cudaMemcpy(h->d_gtab, t, sizeof t, cudaMemcpyHostToDevice);
+        e = cudaMemcpy(h->d_gtab, t, kGTab * sizeof(float), cudaMemcpyHostToDevice);
         gumbel_top_bound_table(t);
         if (e == cudaSuccess) e = cudaMemcpy(h->d_gtop, t, sizeof t, cudaMemcpyHostToDevice);
         uint64_t c[kSkipN];

@@ -278,6 +278,16 @@ __device__ __forceinline__ float2 logit_interval_m(float x, float invT, uint64_t
     return make_float2(s - e, s + e);
 }
 
+// A lower bound of x/T + G for an id whose G is at least glo (a table value
+// rounded down, so exact as a bound): the rounding of x/T and of the sum is
+// covered by the same slack as the interval's lower end above.
+__device__ __forceinline__ float logit_lower_bound(float x, float invT, float glo)
+{
+    const float z = x * invT;
+    const float s = z + glo;
+    return s - ((fabsf(z) + fabsf(s)) * 0x1p-21f + kG32Err);
+}
+
 // The same for id v.  Out of line: it runs for a few ids per row.
 static __device__ __noinline__ float2 logit_interval_at(float x, float invT, uint64_t key, uint32_t v,
                                                         bool top)

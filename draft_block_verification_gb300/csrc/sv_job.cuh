@@ -22,14 +22,14 @@ struct __align__(16) ResidEntry {
 };
 
 // One seed record: the top ids (the ids whose uniform lies in the top 1/256)
-// of one chunk of a Gumbel-max row, scored before the stream: the chunk's
-// threshold (best lower end - 1e-9) and its candidates (Cand2 fields).
+// of one piece of a Gumbel-max row, scored before the stream: the piece's
+// threshold (best lower end - 1e-9) and its candidates (Cand2 fields).  An
+// unused record has threshold -inf and no candidate.
 struct __align__(16) SeedRec {
     float thr;
     float hi1, lo1, hi2, lo2, hi3;
     int v1, v2;
 };
-// blocks of 256 ids per seed record: one or two per lane (seed_bpw)
 
 // A sequence that goes to the fp64 path.
 struct __align__(16) RescueEntry {
@@ -126,13 +126,15 @@ struct Job {
     double *rpart;      // residual / fp64 scratch
     SeedRec *seeds;     // [gumbel rows * seed_chunks] (see gumbel_rows)
     int seed_chunks;    // seed records per Gumbel-max row
-    int seed_bpw;       // blocks of 256 ids per seed record (32, 64 or 128)
+    int seed_span;      // blocks of 256 ids a seed warp lists (the Gumbel-max
+                        // rows' blocks laid end to end, split into equal spans)
     uint64_t *smask;    // SPOT: masked positions of every state [B * (N + 1)];
                         // any-order: verify rows needed per sequence [B]
     unsigned *svalid;   // SPOT, any-order: rows to stream per sequence [B]
     int *err;
     const float *gtab;     // [kGTab] G bounds of ordinary ids
-    const float *gtop;     // [kGTab] G bounds of top ids (the seed kernel's screen)
+    const float *gtop;     // [2 * kGTab] upper, then lower G bounds of top ids by
+                           // the top byte of their fine bits (the seed kernel's)
     const uint64_t *skip;  // [kSkipN] skip thresholds of the top-id draws
 };
 

@@ -1976,22 +1976,27 @@ static cudaError_t launch_in(const Job &j, int grid, cudaStream_t s)
 // Seed kernel.  Before the stream, every top id (an id whose uniform lies in
 // the top 1/256, about one per block of 256 ids) of every Gumbel-max row of
 // the call is found by its skip draws, its logit is loaded, and it is scored
-// in an fp32 interval.  One warp takes one chunk of seed_bpw blocks of one
-// row and writes the chunk's seed record: the best lower end - 1e-9 (a
-// threshold no winner can fall below) and the chunk's candidates.
+// in an fp32 interval.  The blocks of all Gumbel-max rows, laid end to end,
+// are split into equal spans, one per warp (one resident wave of warps);
+// a span covers pieces of one or more rows.  A piece's record, the best
+// lower end - 1e-9 (a threshold no winner can fall below) and the piece's
+// candidates, goes to the row's record numbered by the span boundaries that
+// lie inside the row before the piece; the warp that ends a row also writes
+// its unused records as empty.
 //
-// The warp first lists the chunk's top ids in shared memory: each lane walks
+// The warp first lists a piece's top ids in shared memory: each lane walks
 // one block a draw at a time and, when its block ends, takes the next block
-// of the chunk, so that the lanes stay busy although blocks hold different
+// of the piece, so that the lanes stay busy although blocks hold different
 // numbers of top ids; new ids are appended with a ballot, and each listed
 // id's logit is copied to shared memory asynchronously while the draws go
-// on.  The list is then scored with every lane converged, two ids a lane: an
-// id is bounded by its logit and the top byte of its fine bits (a table of G
-// bounds for top ids), and only ids whose bound reaches the warp's threshold
-// get the fp32 interval.  Warps never wait for one another; the streaming
-// pass starts every Gumbel-max unit from its row's threshold and skips top
-// ids, and the decision step merges the seed records into the row's
-// candidates.
+// on.  The list is then scored with every lane converged, two ids a lane:
+// first the best lower bound of the batch (logit and a table of G lower
+// bounds by the top byte of the fine bits) raises the threshold; then an id
+// is bounded by its logit and the matching upper bound, and only ids whose
+// bound reaches the threshold get the fp32 interval.  Warps never wait for
+// one another; the streaming pass starts every Gumbel-max unit from its
+// row's threshold and skips top ids, and the decision step merges the seed
+// records into the row's candidates.
 // ---------------------------------------------------------------------------
 constexpr int kSeedThreads = 256;
 constexpr int kSeedList = 64;  // listed top ids a warp scores at once (two a lane)
@@ -2020,17 +2025,24 @@ __device__ __forceinline__ float seed_logit(uint32_t w, uint32_t v)
     return __uint_as_float((v & 1u) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
-// One id of the list: screened against the lane's threshold with the
-// top-id table, else scored.
-__device__ __forceinline__ void seed_one(uint32_t v, float x, const RowMode &rm,
+// One id of the list (fine bits m): screened against the lane's threshold
+// with the top-id upper bounds, else scored.
+__device__ __forceinline__ void seed_one(uint32_t v, float x, uint64_t m, const RowMode &rm,
                                          const float *gtop, Cand2 &c, float &thr, float &thrS)
 {
-    const uint64_t m = fine52(rm.key, v);
     if (!(fmaf(x, rm.invT, gtop[(int)(m >> 44)]) > thrS))
         return;  // cannot reach the threshold
     const float2 iv = logit_interval_m(x, rm.invT, m, true);
     c.add(iv.x, iv.y, (int)v);
     const float t = __fsub_rd(iv.x, 1e-9f);
+    if (t > thr) {
+        thr = t;
+        thrS = level1_thr(t);
+    }
+}
+
+__device__ __forceinline__ void seed_raise(float t, float &thr, float &thrS)
+{
     if (t > thr) {
         thr = t;
         thrS = level1_thr(t);
@@ -2043,31 +2055,42 @@ __device__ __forceinline__ void seed_score(const uint32_t *ids, const uint32_t *
                                            float &thr, float &thrS)
 {
     const int lane = threadIdx.x & 31;
-    if (lane < n)
-        seed_one(ids[lane], seed_logit<In>(xw[lane], ids[lane]), rm, gtop, c, thr, thrS);
-    if (lane + 32 < n)
-        seed_one(ids[lane + 32], seed_logit<In>(xw[lane + 32], ids[lane + 32]), rm, gtop, c,
-                 thr, thrS);
-    // every lane leaves with the warp's best threshold
-    const float t = warp_max(thr);
-    if (t > thr) {
-        thr = t;
-        thrS = level1_thr(t);
+    const bool h0 = lane < n, h1 = lane + 32 < n;
+    float x0 = 0.f, x1 = 0.f, lo = -INFINITY;
+    uint64_t m0 = 0, m1 = 0;
+    if (h0) {
+        x0 = seed_logit<In>(xw[lane], ids[lane]);
+        m0 = fine52(rm.key, ids[lane]);
+        lo = logit_lower_bound(x0, rm.invT, gtop[kGTab + (int)(m0 >> 44)]);
     }
+    if (h1) {
+        x1 = seed_logit<In>(xw[lane + 32], ids[lane + 32]);
+        m1 = fine52(rm.key, ids[lane + 32]);
+        lo = fmaxf(lo, logit_lower_bound(x1, rm.invT, gtop[kGTab + (int)(m1 >> 44)]));
+    }
+    // the batch's best lower bound: the id it belongs to still passes the
+    // screen below and is scored, so the threshold stays below a candidate
+    seed_raise(__fsub_rd(warp_max(lo), 1e-9f), thr, thrS);
+    if (h0)
+        seed_one(ids[lane], x0, m0, rm, gtop, c, thr, thrS);
+    if (h1)
+        seed_one(ids[lane + 32], x1, m1, rm, gtop, c, thr, thrS);
+    // every lane leaves with the warp's best threshold
+    seed_raise(warp_max(thr), thr, thrS);
 }
 
 template <typename In>
 __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constant__ Job j)
 {
     __shared__ uint64_t skip[kSkipN];
-    __shared__ float gtop[kGTab];
+    __shared__ float gtop[2 * kGTab];
     __shared__ uint32_t idl[kSeedThreads / 32][kSeedList];
     __shared__ uint32_t xwl[kSeedThreads / 32][kSeedList];
     pdl_wait();
     pdl_trigger();
     for (int i = threadIdx.x; i < kSkipN; i += blockDim.x)
         skip[i] = __ldg(j.skip + i);
-    for (int i = threadIdx.x; i < kGTab; i += blockDim.x)
+    for (int i = threadIdx.x; i < 2 * kGTab; i += blockDim.x)
         gtop[i] = __ldg(j.gtop + i);
     __syncthreads();
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
@@ -2075,14 +2098,21 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
     constexpr int kWarps = kSeedThreads / 32;
     const int H = gumbel_rows(j);
     const uint32_t nblk = ((uint32_t)j.V + 255u) >> 8;
-    const long long items = (long long)j.B * H * j.seed_chunks;
+    const long long span = j.seed_span;
+    const long long total = (long long)j.B * H * nblk;
+    const long long w0 = ((long long)blockIdx.x * kWarps + wl) * span;
+    const long long wend = min(w0 + span, total);
     uint32_t *ids = idl[wl];
     uint32_t *xw = xwl[wl];
-    for (long long it = (long long)blockIdx.x * kWarps + wl; it < items;
-         it += (long long)gridDim.x * kWarps) {
-        const int chunk = (int)(it % j.seed_chunks);
-        const long long g = it / j.seed_chunks;
-        const int b = (int)(g / H), k = (int)(g % H);
+    // pieces of the span, one row each (warp-uniform)
+    for (long long s = w0; s < wend;) {
+        const long long grow = s / nblk;
+        const long long rstart = grow * nblk;
+        const uint32_t b0 = (uint32_t)(s - rstart);
+        const uint32_t bend = (uint32_t)min((long long)nblk, wend - rstart);
+        // record number: span boundaries inside the row up to the piece
+        const int rec = b0 == 0u ? 0 : (int)(s / span - rstart / span);
+        const int b = (int)(grow / H), k = (int)(grow % H);
         const int n = clamp_len(j, b);
         const int slot = gumbel_slot(j, k);
         bool valid = true;
@@ -2101,14 +2131,12 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
             Cand2 c;
             c.init();
             float thr = -INFINITY, thrS = -INFINITY;
-            const uint32_t b0 = (uint32_t)chunk * (uint32_t)j.seed_bpw;
-            const uint32_t bend = min(b0 + (uint32_t)j.seed_bpw, nblk);
             uint32_t nextb = b0 + 32u;  // next block to hand out (warp-uniform)
             uint32_t beta = b0 + (uint32_t)lane;
             bool act = beta < bend;
             int pos = -1, i = 0, cnt = 0;
             // Each draw moves its lane's offset up by at least one, so a block
-            // ends within 257 draws and the loop within 257 * seed_bpw trips.
+            // ends within 257 draws and the loop within 257 * span trips.
             while (__any_sync(0xFFFFFFFFu, act)) {
                 bool got = false, done = false;
                 uint32_t v = 0u;
@@ -2156,9 +2184,31 @@ __global__ void __launch_bounds__(kSeedThreads) seed_kernel(const __grid_constan
             r.v1 = c.v1;
             r.v2 = c.v2;
         }
+        SeedRec *rr = j.seeds + grow * j.seed_chunks;
         if (lane == 0)
-            j.seeds[it] = r;
+            rr[rec] = r;
+        if (bend == nblk) {
+            // the row ends in this span: its later records stay empty
+            SeedRec e;
+            e.thr = e.hi1 = e.lo1 = e.hi2 = e.lo2 = e.hi3 = -INFINITY;
+            e.v1 = e.v2 = -1;
+            for (int q = rec + 1 + lane; q < j.seed_chunks; q += 32)
+                rr[q] = e;
+        }
+        s = rstart + bend;
     }
+}
+
+// Resident seed CTAs per SM (the smaller of the two instances).
+cudaError_t seed_setup(int *blocks_per_sm)
+{
+    int a = 0, b = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, seed_kernel<uint16_t>,
+                                                                  kSeedThreads, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, seed_kernel<float>, kSeedThreads, 0);
+    *blocks_per_sm = a < b ? a : b;
+    return e;
 }
 
 cudaError_t seed_launch(const Job &j, int grid, cudaStream_t s)
