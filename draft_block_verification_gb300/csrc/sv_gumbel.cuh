@@ -49,16 +49,29 @@ __device__ __forceinline__ uint64_t fine52(uint64_t key, uint32_t v)
 }
 
 // Gap of a skip draw: the largest g in 0..256 with M < C_g (C decreasing,
-// C_0 taken as 2^64).  Estimated from log2 of u = M / 2^64 (g is about
-// log(u) / log(255/256)) and then corrected against the exact thresholds, so
-// the result is exact; the correction loops usually run zero times.
+// C_0 taken as 2^64), i.e. g = floor(t), t = log(u) / log(255/256), u = M /
+// 2^64, capped at 256.  t is estimated from log2 of u rounded to 24 bits.
+// For u >= 0.36 (t <= 257) the estimate is within 1e-4 of t: the rounding of
+// u moves log2 u by at most 2^-25 / (0.36 ln 2) < 1.2e-7, lg2.approx errs by
+// at most 2^-22.6 < 1.7e-7, and the product and its constant add under
+// 4.2e-5.  So an estimate more than kGapEps = 2^-9 away from every integer
+// (and from 256) has the exact floor; the rest, about 0.4 % of draws, are
+// corrected against the exact thresholds.
+constexpr float kGapEps = 0x1p-9f;
+
 __device__ __forceinline__ int skip_gap(uint64_t M, const uint64_t *__restrict__ C)
 {
     float u = __uint2float_rn((uint32_t)(M >> 40)) * 0x1p-24f + 0x1p-25f;
     float l2;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l2) : "f"(u));
     // 1 / log2(255/256) = -177.0989; u < 1 so the estimate is >= 0
-    int g = (int)fminf(l2 * -177.09888f, 256.f);
+    const float t = l2 * -177.09888f;
+    if (t >= 256.f + kGapEps)
+        return 256;
+    const float fl = floorf(t), fr = t - fl;
+    if (fr >= kGapEps && fr <= 1.f - kGapEps && t < 256.f)
+        return (int)fl;
+    int g = (int)fminf(t, 256.f);
     g = max(0, min(g, 256));
     while (g < 256 && M < C[g + 1])
         ++g;

@@ -408,9 +408,9 @@ __device__ __forceinline__ void raise_thr(GState &s, float t)
 // threshold are kept, and their lower end raises the threshold (anything
 // below it - 1e-9 can neither win nor tie within 1e-9).
 __device__ __forceinline__ void gumbel_level2(float x, uint32_t v, bool top, GState &s,
-                                              Cand2 &c, const RowMode &rm)
+                                              Cand2 &c, float invT, uint64_t key)
 {
-    const float2 iv = logit_interval_at(x, rm.invT, rm.key, v, top);
+    const float2 iv = logit_interval_at(x, invT, key, v, top);
     const float lo = iv.x, hi = iv.y;
     if (hi < s.thr)
         return;
@@ -546,7 +546,7 @@ __device__ __forceinline__ float max_chunk(const Chunk &q, int vbase, TState &s)
 template <typename In>
 __device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
                                             const uint32_t *__restrict__ qv, int n, GState s,
-                                            const RowMode &rm, const float *__restrict__ gt,
+                                            float invT, uint64_t key, const float *__restrict__ gt,
                                             const uint64_t *__restrict__ skip, Cand2 *wc)
 {
     using VT = VecTraits<In>;
@@ -557,16 +557,16 @@ __device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
     for (int i = (int)(threadIdx.x & 31); i < n; i += 32) {
         const uint4 d = qd[i];
         const uint32_t v0 = qv[i] * E;
-        const uint32_t tm = top_mask(rm.key, v0 >> 8, (int)(v0 & 255u), E, skip);
+        const uint32_t tm = top_mask(key, v0 >> 8, (int)(v0 & 255u), E, skip);
 #pragma unroll 1
         for (int e = 0; e < E; ++e) {
             if ((tm >> e) & 1u)
                 continue;
             const uint32_t v = v0 + e;
             const float x = VT::elem(d, e);
-            const uint64_t m = fine52(rm.key, v);
-            if (fmaf(x, rm.invT, gt[(int)(m >> 44)]) >= s.thrS)
-                gumbel_level2(x, v, false, s, c, rm);
+            const uint64_t m = fine52(key, v);
+            if (fmaf(x, invT, gt[(int)(m >> 44)]) >= s.thrS)
+                gumbel_level2(x, v, false, s, c, invT, key);
         }
     }
     warp_cand2(c);
@@ -584,44 +584,59 @@ __device__ __noinline__ GState gumbel_flush(const uint4 *__restrict__ qd,
 // bound's rounding slack), and the -inf padding of a short stage never passes,
 // not even a threshold of -inf.  The chunk is tested first on its largest
 // logit with one vote per warp (with the seed threshold, nearly every chunk
-// stops there); otherwise each vector is tested and the passing ones are
-// queued, compacted with a ballot, so a warp does not diverge per vector.
-// Each warp keeps its own threshold (the seed records give every warp the
-// row's top-id threshold at the start).
+// stops there); otherwise gumbel_queue tests each vector, re-read from the
+// stage, and queues the passing ones, compacted with a ballot, so a warp does
+// not diverge per vector.  Each warp keeps its own threshold (the seed
+// records give every warp the row's top-id threshold at the start).
+struct GQueue {
+    GState g;
+    int n;  // vectors in the warp's queue (warp-uniform)
+};
+
 template <typename In>
-__device__ __forceinline__ void gumbel_chunk(const Chunk &q, int vbase, TState &s,
-                                             const RowMode &rm, float gmax,
-                                             const float *__restrict__ gt,
-                                             const uint64_t *__restrict__ skip, PassShared &sm)
+__device__ __noinline__ GQueue gumbel_queue(const uint4 *__restrict__ st, int nv, int vbase,
+                                            GQueue q, float invT, uint64_t key, float gmax,
+                                            const float *__restrict__ gt,
+                                            const uint64_t *__restrict__ skip, PassShared &sm)
 {
     using VT = VecTraits<In>;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     uint4 *qd = sm.gqd[w];
     uint32_t *qv = sm.gqv[w];
-    float cm = VT::hi_of(VT::pmax(q[0]));
-#pragma unroll
-    for (int k = 1; k < kVecsPerThread; ++k)
-        cm = fmaxf(cm, VT::hi_of(VT::pmax(q[k])));
-    if (!__any_sync(0xFFFFFFFFu, fmaf(cm, rm.invT, gmax) > s.g.thrS))
-        return;
-#pragma unroll
+#pragma unroll 1
     for (int k = 0; k < kVecsPerThread; ++k) {
         const int idx = t + k * kConsumers;
-        const bool pass = fmaf(VT::hi_of(VT::pmax(q[k])), rm.invT, gmax) > s.g.thrS;
+        const uint4 v = idx < nv ? st[idx] : VT::neg_inf_vec();
+        const bool pass = fmaf(VT::hi_of(VT::pmax(v)), invT, gmax) > q.g.thrS;
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, pass);
         if (bal) {
             if (pass) {
-                const int r = s.gqn + __popc(bal & ((1u << lane) - 1u));
-                qd[r] = q[k];
+                const int r = q.n + __popc(bal & ((1u << lane) - 1u));
+                qd[r] = v;
                 qv[r] = (uint32_t)(vbase + idx);
             }
-            s.gqn += __popc(bal);
-            if (s.gqn > kGQ - 32) {
-                s.g = gumbel_flush<In>(qd, qv, s.gqn, s.g, rm, gt, skip, &sm.gcand[w]);
-                s.gqn = 0;
+            q.n += __popc(bal);
+            if (q.n > kGQ - 32) {
+                q.g = gumbel_flush<In>(qd, qv, q.n, q.g, invT, key, gt, skip, &sm.gcand[w]);
+                q.n = 0;
             }
         }
     }
+    return q;
+}
+
+template <typename In>
+__device__ __forceinline__ void gumbel_chunk(const uint4 *__restrict__ st, int nv, float cm,
+                                             int vbase, TState &s, const RowMode &rm, float gmax,
+                                             const float *__restrict__ gt,
+                                             const uint64_t *__restrict__ skip, PassShared &sm)
+{
+    if (!__any_sync(0xFFFFFFFFu, fmaf(cm, rm.invT, gmax) > s.g.thrS))
+        return;
+    GQueue q{s.g, s.gqn};
+    q = gumbel_queue<In>(st, nv, vbase, q, rm.invT, rm.key, gmax, gt, skip, sm);
+    s.g = q.g;
+    s.gqn = q.n;
 }
 
 template <typename In, int MODE>
@@ -634,14 +649,14 @@ __device__ __forceinline__ void do_chunk(const uint4 *__restrict__ st, int nv, i
     float cm = -INFINITY;
     if (MODE & (M_ARGMAX | M_MAX))
         cm = max_chunk<In, (MODE & M_ARGMAX) != 0>(q, vbase, s);
-    else if (MODE & M_LSE)
+    else
         cm = chunk_max<In>(q);
     if (MODE & M_LSE)
         lse_chunk<In>(q, rm.c1, cm, s.e1, s.acc1);
     if (MODE & M_LSE2)
         lse_chunk<In>(q, rm.c2, cm, s.e2, s.acc2);
     if (MODE & M_GUMBEL)
-        gumbel_chunk<In>(q, vbase, s, rm, gmax, gt, sm.skip, sm);
+        gumbel_chunk<In>(st, nv, cm, vbase, s, rm, gmax, gt, sm.skip, sm);
 }
 
 // ---------------------------------------------------------------------------
@@ -1648,7 +1663,8 @@ __device__ __forceinline__ bool unit_loop(const Job &j, PassShared &sm, unsigned
     }
     if ((MODE & M_GUMBEL) && s.gqn > 0) {
         const int w = threadIdx.x >> 5;
-        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqv[w], s.gqn, s.g, rm, gt, sm.skip, &sm.gcand[w]);
+        s.g = gumbel_flush<In>(sm.gqd[w], sm.gqv[w], s.gqn, s.g, rm.invT, rm.key, gt, sm.skip,
+                               &sm.gcand[w]);
         s.gqn = 0;
     }
     finish_unit(j, uh, s, rm, sm);

@@ -3,6 +3,10 @@
 //   [0] max |G32 - G64| / kG32Err                 (Gumbel of sv_gumbel.cuh)
 //   [1] max |ex2(x) / 2^x - 1| / 2^-21            (x in [-126, 64])
 //   [2] max |lg2(x) - log2(x)| / (2^-22 max(1, |log2 x|))   (x in [2^-60, 2^8])
+//   [3] skip gaps whose fast evaluation (skip_gap) differs from a binary
+//       search over the exact thresholds (a count; must be 0), for draws
+//       spread uniformly and draws next to every threshold C_g, within the
+//       window where the fast path decides near its 2^-9 margin
 // Fine bits are drawn, for ordinary and top ids alike, from regions where the
 // formulas are hardest: uniform, w within 2^-28 of 1 (u next to 255/256, or
 // 1 - u near 2^-61 for a top id), w below 2^-29, and u around 3/4 (the
@@ -11,9 +15,24 @@
 
 namespace sv {
 
-__global__ void selftest_kernel(uint64_t seed, long long n, unsigned *out)
+// The largest g in 0..256 with M < C_g (C_0 = 2^64: every M), by bisection.
+__device__ int skip_gap_bisect(uint64_t M, const uint64_t *C)
+{
+    int lo = 0, hi = 256;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (M < C[mid])
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void selftest_kernel(uint64_t seed, long long n, const uint64_t *C, unsigned *out)
 {
     float r0 = 0.f, r1 = 0.f, r2 = 0.f;
+    unsigned bad = 0;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         uint64_t h = splitmix_out(seed ^ (uint64_t)i);
@@ -34,20 +53,35 @@ __global__ void selftest_kernel(uint64_t seed, long long n, unsigned *out)
         float y = exp2f(-60.f + 68.f * (float)(h & 0xFFFFF) * 0x1p-20f);
         double l = log2((double)y);
         r2 = fmaxf(r2, (float)(fabs((double)lg2a(y) - l) / (0x1p-22 * fmax(1.0, fabs(l)))));
+        // a skip draw: uniform, or within 2^48 (about 4 margins of the fast
+        // path) above or below a threshold C_g, g in 1..256
+        const uint64_t h2 = splitmix_out(h);
+        const int g = 1 + (int)(h2 % 256u);
+        const uint64_t off = h2 >> 16;
+        uint64_t M = h2;
+        if ((i & 3) == 1)
+            M = C[g] - 1u - off;
+        else if ((i & 3) == 2)
+            M = C[g] + off;
+        if (skip_gap(M, C) != skip_gap_bisect(M, C))
+            ++bad;
     }
     atomicMax(out + 0, __float_as_uint(r0));
     atomicMax(out + 1, __float_as_uint(r1));
     atomicMax(out + 2, __float_as_uint(r2));
+    if (bad)
+        atomicAdd(out + 3, bad);
 }
 
-cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s)
+cudaError_t selftest_run(uint64_t seed, long long n, const uint64_t *skip, double *res,
+                         cudaStream_t s)
 {
     unsigned *d = nullptr;
-    cudaError_t e = cudaMallocAsync((void **)&d, 3 * sizeof(unsigned), s);
+    cudaError_t e = cudaMallocAsync((void **)&d, 4 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
-    cudaMemsetAsync(d, 0, 3 * sizeof(unsigned), s);
-    selftest_kernel<<<256, 256, 0, s>>>(seed, n, d);
-    unsigned h[3] = {0, 0, 0};
+    cudaMemsetAsync(d, 0, 4 * sizeof(unsigned), s);
+    selftest_kernel<<<256, 256, 0, s>>>(seed, n, skip, d);
+    unsigned h[4] = {0, 0, 0, 0};
     e = cudaMemcpyAsync(h, d, sizeof h, cudaMemcpyDeviceToHost, s);
     cudaFreeAsync(d, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -56,6 +90,7 @@ cudaError_t selftest_run(uint64_t seed, long long n, double *res, cudaStream_t s
         memcpy(&f, &h[i], sizeof f);
         res[i] = f;
     }
+    res[3] = (double)h[3];
     return e;
 }
 
