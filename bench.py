@@ -65,7 +65,7 @@ def _kernel_hash(w=None):
 
 def _profile_path(w):
     """The committed ncu summary of the streaming kernel on this workload."""
-    t = "" if w.kind == "greedy" else "_t%g" % w.T
+    t = "" if w.kind == "greedy" or w.name.endswith("_t%g" % w.T) else "_t%g" % w.T
     return os.path.join(ROOT, "profiles", "%s_%s%s.md" % (w.kernel(), w.name, t))
 
 
