@@ -37,6 +37,7 @@ struct sv_handle {
     int pass_blocks = 1;   // resident streaming CTAs per SM
     int tv_blocks = 1;     // resident total-variation CTAs per SM
     int seed_blocks = 1;   // resident seed CTAs per SM
+    bool resid_pair = false;  // two 512-thread residual CTAs fit on an SM
     int *d_err = nullptr;
     unsigned *d_ctl = nullptr;
     float *d_gtab = nullptr;      // [kGTab] G bounds of ordinary ids
@@ -352,8 +353,11 @@ sv_status launch(sv_handle *h, const Job &j, int grid, cudaStream_t s, bool post
     if (h->timing) cudaEventRecord(h->ev[1], s);
     if (e != cudaSuccess) return cuda_status(e);
     if (!post) return SV_OK;
-    return cuda_status(
-        post_launch(j, h->sms * h->tv_blocks, std::min(j.B, h->sms), h->sms, tv, s));
+    // the residual pass: a CTA per sequence, two per SM when there are more
+    // sequences than SMs
+    const int rgrid = j.B > h->sms && h->resid_pair ? std::min(j.B, 2 * h->sms)
+                                                   : std::min(j.B, h->sms);
+    return cuda_status(post_launch(j, h->sms * h->tv_blocks, rgrid, h->sms, tv, s));
 }
 
 }  // namespace
@@ -392,6 +396,7 @@ sv_status sv_create(sv_handle **out)
     h->pass_blocks = std::max(nb, 1);
     if (e == cudaSuccess) e = post_setup(pb);
     h->tv_blocks = std::max(1, pb[0]);
+    h->resid_pair = pb[1] >= 2;
     int sb = 0;
     if (e == cudaSuccess) e = seed_setup(&sb);
     h->seed_blocks = std::max(1, sb);

@@ -370,26 +370,27 @@ __device__ void resid_scan(const RCtx &c, int vb, int ve, const float *gt, const
 }
 
 // ---------------------------------------------------------------------------
-// The residual pass: one CTA of kResidThreads threads per residual entry
-// scans the entry's whole row pair, so no CTA waits for another: the row's
-// top ids set one threshold for the whole row, and the candidates are merged
-// inside the CTA.
+// The residual pass: one CTA of NT threads per residual entry scans the
+// entry's whole row pair, so no CTA waits for another: the row's top ids set
+// one threshold for the whole row, and the candidates are merged inside the
+// CTA.  NT = 1024 (one CTA per SM) when there are at most as many sequences as
+// SMs, else 512 (two CTAs per SM), so that up to twice as many sequences are
+// drawn in one wave.
 // ---------------------------------------------------------------------------
-constexpr int kResidThreads = 1024;
-constexpr int kResidWarps = kResidThreads / 32;
 constexpr int kRQ = 64;        // vectors per warp queued for the per-id screen
 constexpr int kScanAhead = 8;  // vectors per thread loaded together
 constexpr int kSeedPer = 2;    // listed top ids each thread scores from registers
-constexpr int kSeedList = kSeedPer * kResidThreads;
 
+template <int NT>
 struct ResidShared {
-    int qv[kResidWarps][kRQ];  // queued vectors (row vector index) per warp
-    uint32_t ids[kSeedList];   // top ids of the row
+    static constexpr int W = NT / 32;
+    int qv[W][kRQ];                // queued vectors (row vector index) per warp
+    uint32_t ids[kSeedPer * NT];   // top ids of the row
     int nids;
-    uint32_t thr;              // the CTA's Gumbel threshold (ordered float)
-    float f[kResidWarps][5];   // block reductions
-    int iv[kResidWarps][2];
-    double Lq, epsq;           // Packed-SS: the proposal row's log-sum-exp
+    uint32_t thr;                  // the CTA's Gumbel threshold (ordered float)
+    float f[W][5];                 // block reductions
+    int iv[W][2];
+    double Lq, epsq;               // Packed-SS: the proposal row's log-sum-exp
 };
 
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
@@ -399,19 +400,19 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
 
 // fp32 log-sum-exp of a whole row with the CTA (the arithmetic and error
 // model of lse_chunk32): max, min and sum 2^((x - max) c).
-template <typename In>
-__device__ void resid_lse32(const char *row, int nvec, float c, ResidShared &rs, float &M,
+template <typename In, int NT>
+__device__ void resid_lse32(const char *row, int nvec, float c, ResidShared<NT> &rs, float &M,
                             float &S, float &mn)
 {
     using VT = VecTraits<In>;
     constexpr int E = VT::N;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     float mref = -INFINITY, acc = 0.f, mx = -INFINITY, lo = INFINITY;
-    for (int base = 0; base < nvec; base += kScanAhead * kResidThreads) {
+    for (int base = 0; base < nvec; base += kScanAhead * NT) {
         uint4 qv[kScanAhead];
 #pragma unroll
         for (int u = 0; u < kScanAhead; ++u) {
-            const int k = base + t + u * kResidThreads;
+            const int k = base + t + u * NT;
             qv[u] = k < nvec ? ldv<In>(row, k) : VT::neg_inf_vec();
         }
 #pragma unroll
@@ -451,7 +452,7 @@ __device__ void resid_lse32(const char *row, int nvec, float c, ResidShared &rs,
     }
     __syncthreads();
     float bm = -INFINITY, bl = INFINITY;
-    for (int q = 0; q < kResidWarps; ++q) {
+    for (int q = 0; q < (NT / 32); ++q) {
         bm = fmaxf(bm, rs.f[q][0]);
         bl = fminf(bl, rs.f[q][1]);
     }
@@ -461,7 +462,7 @@ __device__ void resid_lse32(const char *row, int nvec, float c, ResidShared &rs,
     if (lane == 0) rs.f[w][2] = ws;
     __syncthreads();
     float bs = 0.f;
-    for (int q = 0; q < kResidWarps; ++q) bs += rs.f[q][2];
+    for (int q = 0; q < (NT / 32); ++q) bs += rs.f[q][2];
     M = bm;
     S = bs;
     mn = bl;
@@ -473,14 +474,14 @@ __device__ void resid_lse32(const char *row, int nvec, float c, ResidShared &rs,
 // once, into registers, and scores them, so a thread waits for one round of
 // loads.  Ids past the list's capacity (far beyond the expected V/256) are
 // scored where they are found.
-template <typename In>
+template <typename In, int NT>
 __device__ __forceinline__ void seed_row(const RCtx &c, uint32_t V, const uint64_t *skip,
-                                         ResidShared &rs, Track32 &tr)
+                                         ResidShared<NT> &rs, Track32 &tr)
 {
     using VT = VecTraits<In>;
     const int t = threadIdx.x;
     const uint32_t nb = (V + 255u) >> 8;
-    for (uint32_t beta = (uint32_t)t; beta < nb; beta += kResidThreads) {
+    for (uint32_t beta = (uint32_t)t; beta < nb; beta += NT) {
         int pos = -1;
         for (int i = 0; i < kSkipN; ++i) {
             pos = next_top(c.key, beta, i, pos, skip);
@@ -488,7 +489,7 @@ __device__ __forceinline__ void seed_row(const RCtx &c, uint32_t V, const uint64
             if (pos > 255 || v >= V)
                 break;
             const int slot = atomicAdd(&rs.nids, 1);
-            if (slot < kSeedList)
+            if (slot < (kSeedPer * NT))
                 rs.ids[slot] = v;
             else
                 tr.add(c, VT::load1(c.prow, (int)v), VT::load1(c.qrow, (int)v), v,
@@ -496,12 +497,12 @@ __device__ __forceinline__ void seed_row(const RCtx &c, uint32_t V, const uint64
         }
     }
     __syncthreads();
-    const int n = min(rs.nids, kSeedList);
+    const int n = min(rs.nids, (kSeedPer * NT));
     uint32_t id[kSeedPer];
     float x[kSeedPer], y[kSeedPer];
 #pragma unroll
     for (int r = 0; r < kSeedPer; ++r) {
-        const int i = t + r * kResidThreads;
+        const int i = t + r * NT;
         id[r] = i < n ? rs.ids[i] : 0xFFFFFFFFu;
         x[r] = y[r] = 0.f;
         if (i < n) {
@@ -516,8 +517,8 @@ __device__ __forceinline__ void seed_row(const RCtx &c, uint32_t V, const uint64
 }
 
 // Per-id screen of a warp's queued vectors, one vector per lane.
-template <typename In>
-__device__ __forceinline__ void resid_flush(const RCtx &c, const ResidShared &rs, int n,
+template <typename In, int NT>
+__device__ __forceinline__ void resid_flush(const RCtx &c, const ResidShared<NT> &rs, int n,
                                             const float *gt, const uint64_t *skip, Track32 &tr)
 {
     const int w = threadIdx.x >> 5;
@@ -531,7 +532,8 @@ __device__ __forceinline__ void resid_flush(const RCtx &c, const ResidShared &rs
 
 // The warp's best threshold into the CTA's word, when it beats what the
 // warp published before.
-__device__ __forceinline__ void publish_thr(const Track32 &tr, ResidShared &rs, uint32_t &pub)
+template <int NT>
+__device__ __forceinline__ void publish_thr(const Track32 &tr, ResidShared<NT> &rs, uint32_t &pub)
 {
     const uint32_t w = __reduce_max_sync(0xFFFFFFFFu, f2ord(tr.thr));
     if (w > pub) {
@@ -545,30 +547,30 @@ __device__ __forceinline__ void publish_thr(const Track32 &tr, ResidShared &rs, 
 // A vector whose largest logit can reach the threshold with the ordinary-id
 // bound is queued (compacted with a ballot) and the queue is screened per id
 // with a vector per lane, so a warp does not diverge per vector.
-template <typename In>
+template <typename In, int NT>
 __device__ void resid_scan_row(const RCtx &c, int nvec, uint32_t V, const float *gt,
-                               const uint64_t *skip, ResidShared &rs, Track32 &tr)
+                               const uint64_t *skip, ResidShared<NT> &rs, Track32 &tr)
 {
     using VT = VecTraits<In>;
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
     tr.init();
-    seed_row<In>(c, V, skip, rs, tr);
+    seed_row<In, NT>(c, V, skip, rs, tr);
     uint32_t pub = 0u;
     publish_thr(tr, rs, pub);
     __syncthreads();
     const float gmax = gt[kGTab - 1];
     int qn = 0;
-    for (int base = 0; base < nvec; base += kScanAhead * kResidThreads) {
+    for (int base = 0; base < nvec; base += kScanAhead * NT) {
         uint4 px[kScanAhead];
 #pragma unroll
         for (int u = 0; u < kScanAhead; ++u) {
-            const int k = base + t + u * kResidThreads;
+            const int k = base + t + u * NT;
             px[u] = k < nvec ? ldv<In>(c.prow, k) : VT::neg_inf_vec();
         }
         tr.raise(ord2f(*(volatile uint32_t *)&rs.thr));
 #pragma unroll
         for (int u = 0; u < kScanAhead; ++u) {
-            const int k = base + t + u * kResidThreads;
+            const int k = base + t + u * NT;
             // (k < nvec: past the row's end there is no vector, and with no
             // threshold yet a -inf bound would still compare >= -inf)
             const bool pass =
@@ -578,7 +580,7 @@ __device__ void resid_scan_row(const RCtx &c, int nvec, uint32_t V, const float 
                 if (pass) rs.qv[w][qn + __popc(bal & ((1u << lane) - 1u))] = k;
                 qn += __popc(bal);
                 if (qn > kRQ - 32) {
-                    resid_flush<In>(c, rs, qn, gt, skip, tr);
+                    resid_flush<In, NT>(c, rs, qn, gt, skip, tr);
                     qn = 0;
                     tr.raise(ord2f(*(volatile uint32_t *)&rs.thr));
                 }
@@ -586,11 +588,12 @@ __device__ void resid_scan_row(const RCtx &c, int nvec, uint32_t V, const float 
         }
         publish_thr(tr, rs, pub);
     }
-    if (qn) resid_flush<In>(c, rs, qn, gt, skip, tr);
+    if (qn) resid_flush<In, NT>(c, rs, qn, gt, skip, tr);
 }
 
 // The CTA's merged candidates, in thread 0's `out`.
-__device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared &rs, Cand2 &out)
+template <int NT>
+__device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared<NT> &rs, Cand2 &out)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     warp_cand2(c);
@@ -606,7 +609,7 @@ __device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared &rs, Cand2 &ou
     __syncthreads();
     out.init();
     if (w == 0) {
-        if (lane < kResidWarps) {
+        if (lane < (NT / 32)) {
             out.hi1 = rs.f[lane][0];
             out.lo1 = rs.f[lane][1];
             out.hi2 = rs.f[lane][2];
@@ -619,10 +622,10 @@ __device__ __forceinline__ void resid_cand2(Cand2 &c, ResidShared &rs, Cand2 &ou
     }
 }
 
-template <typename In>
-__global__ void __launch_bounds__(kResidThreads, 1) resid_kernel(const __grid_constant__ Job j)
+template <typename In, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) resid_kernel(const __grid_constant__ Job j)
 {
-    __shared__ ResidShared rs;
+    __shared__ ResidShared<NT> rs;
     __shared__ float gt[kGTab];
     __shared__ uint64_t skip[kSkipN];  // skip thresholds of the top-id draws
     const int t = threadIdx.x;
@@ -630,9 +633,9 @@ __global__ void __launch_bounds__(kResidThreads, 1) resid_kernel(const __grid_co
     pdl_trigger();
     const unsigned nE = *(volatile unsigned *)(j.ctl + C_RESID_N);
     if (blockIdx.x < nE) {
-        for (int i = t; i < kGTab; i += kResidThreads)
+        for (int i = t; i < kGTab; i += NT)
             gt[i] = __ldg(j.gtab + i);
-        for (int i = t; i < kSkipN; i += kResidThreads)
+        for (int i = t; i < kSkipN; i += NT)
             skip[i] = __ldg(j.skip + i);
     }
     for (unsigned e = blockIdx.x; e < nE; e += gridDim.x) {
@@ -649,7 +652,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) resid_kernel(const __grid_co
         if (re.need_lq) {
             // Packed-SS: the stored proposal row's log-sum-exp.
             float M, S, mn;
-            resid_lse32<In>(re.qrow, j.nvec, j.cp, rs, M, S, mn);
+            resid_lse32<In, NT>(re.qrow, j.nvec, j.cp, rs, M, S, mn);
             if (t == 0) {
                 rs.Lq = (double)M / (double)j.Tp + log((double)S);
                 rs.epsq = lse_rel_bound(((double)M - (double)mn) * (double)j.cp);
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) resid_kernel(const __grid_co
         RCtx ctx;
         resid_ctx(j, re, ctx);
         Track32 tr;
-        resid_scan_row<In>(ctx, j.nvec, (uint32_t)j.V, gt, skip, rs, tr);
+        resid_scan_row<In, NT>(ctx, j.nvec, (uint32_t)j.V, gt, skip, rs, tr);
         Cand2 all;
         resid_cand2(tr.c, rs, all);
         if (t == 0) resid_resolve(j, re, ctx, all, skip);
@@ -973,7 +976,8 @@ __global__ void __launch_bounds__(kPostThreads) rescue_kernel(const __grid_const
 // Host-side launchers.
 // Resident CTAs per SM of the total-variation kernel (occ[0], which takes
 // work items from a counter, so its grid fills the GPU) and of the residual
-// kernel (occ[1]; its grid is one CTA per sequence, at most one per SM).
+// kernel's 512-thread instance (occ[1]; two per SM let the residual pass
+// draw up to two sequences per SM in one wave).
 cudaError_t post_setup(int occ[2])
 {
     int a = 0, b = 0, c = 0, d = 0;
@@ -982,11 +986,9 @@ cudaError_t post_setup(int occ[2])
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, tv_kernel<float>, kPostThreads, 0);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, resid_kernel<uint16_t>,
-                                                          kResidThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, resid_kernel<uint16_t, 512>, 512, 0);
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, resid_kernel<float>, kResidThreads,
-                                                          0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, resid_kernel<float, 512>, 512, 0);
     occ[0] = a < b ? a : b;
     occ[1] = c < d ? c : d;
     return e;
@@ -1005,9 +1007,15 @@ cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid
                : cudaLaunchKernelEx(&cfg, tv_kernel<float>, j);
         if (e != cudaSuccess) return e;
     }
-    pdl_config(cfg, at, dim3(resid_grid), dim3(kResidThreads), 0, s);
-    e = bf ? cudaLaunchKernelEx(&cfg, resid_kernel<uint16_t>, j)
-           : cudaLaunchKernelEx(&cfg, resid_kernel<float>, j);
+    // more sequences than SMs: two CTAs of 512 threads per SM
+    const bool half = j.B > coop_grid && resid_grid > coop_grid;
+    pdl_config(cfg, at, dim3(resid_grid), dim3(half ? 512 : 1024), 0, s);
+    if (half)
+        e = bf ? cudaLaunchKernelEx(&cfg, resid_kernel<uint16_t, 512>, j)
+               : cudaLaunchKernelEx(&cfg, resid_kernel<float, 512>, j);
+    else
+        e = bf ? cudaLaunchKernelEx(&cfg, resid_kernel<uint16_t, 1024>, j)
+               : cudaLaunchKernelEx(&cfg, resid_kernel<float, 1024>, j);
     if (e != cudaSuccess) return e;
     // The fp64 path's grid barriers need every CTA resident: a cooperative
     // launch guarantees it (or fails).  It returns at once when no sequence
