@@ -504,6 +504,20 @@ def test_packed_full_size(dbv, T):
     _compare_packed(sub, ref, "bf16")
 
 
+@pytest.mark.parametrize("B,W,V", [(152, 32, 8192), (160, 32, 8192), (8, 32, 151936)])
+def test_packed_seed_spans(dbv, B, W, V):
+    """The seed kernel splits the Gumbel-max rows' 256-id blocks, end to end,
+    into one span per resident seed warp (4,864 on 152 SMs with four seed CTAs
+    of eight warps each): 152 x 32 rows of 32 blocks give spans that are whole
+    rows, 160 x 32 rows spans of 34 blocks that cut rows, and 8 x 32 rows of
+    593 blocks spans of 32 blocks (a row in 19 or 20 pieces).  Every sequence
+    is checked against the oracle."""
+    K = 32
+    pi = datagen.packed_inputs(B, K, W, V, dtype="bf16", seed=B + W, T=1.0)
+    out, ref = _packed_both(dbv, pi, K, W, 1.0)
+    _compare_packed(out, ref, "bf16")
+
+
 # ------------------------------------------------------------------ errors
 
 def test_invalid_arguments_raise(dbv):
