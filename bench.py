@@ -506,21 +506,28 @@ class Workload:
 
 def _cpu_sample(w, seconds, nmax=None):
     """Inputs for the oracle on the CPU: as many sequences of the workload as
-    fit in about `seconds` of oracle time (measured on one sequence)."""
+    fit in about `seconds` of oracle time, in whole rounds of one sequence per
+    oracle thread (the oracle runs its sequences in parallel), measured on one
+    sequence."""
     import oracle
     oracle.build()
     B = nmax or w.cfg["B"]
     one = w.inputs("cpu", 1)
     t1 = max(w.oracle_call(one), 1e-4)
-    nseq = int(max(1, min(B, seconds / t1)))
+    P = max(1, oracle.num_threads())
+    nseq = int(max(1, min(B, P * max(1, int(seconds / t1)))))
     return nseq, (one if nseq == 1 else w.inputs("cpu", nseq))
+
+
+def _threads_used(nseq):
+    import oracle
+    return int(min(nseq, max(1, oracle.num_threads())))
 
 
 def cpu_baseline(w, seconds=15.0):
     """Time the fp64 oracle, as it stands, on a bounded sample of the workload
     (the first sequences of a batch drawn on the CPU with the same recipe),
     repeating the call until about `seconds` have passed."""
-    import oracle
     nseq, inp = _cpu_sample(w, seconds / 3)
     times = []
     t_end = time.perf_counter() + seconds
@@ -530,36 +537,47 @@ def cpu_baseline(w, seconds=15.0):
             break
     dt = statistics.median(times)
     units = w.units(inp)
-    return {"value": units / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+    return {"value": units / dt, "unit": "rows/s", "cores": _threads_used(nseq), "kind": "oracle",
             "cpu_model": _cpu_model(),
             "sample": "%d of %d sequences of %s, %d oracle calls, median %.3f s wall"
                       % (nseq, w.cfg["B"], w.name, len(times), dt)}
 
 
+REF_BUDGET_S = 100.0  # oracle time of a whole reference run
+
+
 def run_reference(args):
     """The reference arm is the CPU oracle (the pages ship no code): every step
-    verifies a sample of the workload, sized so that the whole run stays
-    within about two minutes."""
+    verifies a sample of the workload (whole rounds of one sequence per oracle
+    thread).  The run stays within about two minutes: when the requested
+    warm-up and steps would not fit, it times as many steps as fit (at least
+    three, after one warm-up call) and reports that count as `steps`, next to
+    `steps_requested`."""
     dist, rank, ws = _dist()
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
     w = Workload(args.workload, args)
-    import oracle
     n_calls = max(1, args.warmup + args.steps)
-    nseq, inp = _cpu_sample(w, 100.0 / n_calls)
-    vals = []
-    for _ in range(n_calls):
+    nseq, inp = _cpu_sample(w, REF_BUDGET_S / n_calls)
+    t0 = time.perf_counter()
+    vals = [w.units(inp) / w.oracle_call(inp)]  # first call: warm-up, and sizes the run
+    t_call = time.perf_counter() - t0
+    fit = max(4, int(REF_BUDGET_S / max(t_call, 1e-3)))
+    n_run = min(n_calls, fit)
+    warm = min(max(args.warmup, 1), max(1, n_run - 3)) if args.steps else n_run
+    for _ in range(n_run - 1):
         vals.append(w.units(inp) / w.oracle_call(inp))
-    value = statistics.median(vals[args.warmup:]) if args.steps else vals[-1]
-    cb = {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+    timed = vals[warm:]
+    value = statistics.median(timed) if timed else vals[-1]
+    cb = {"value": value, "unit": "rows/s", "cores": _threads_used(nseq), "kind": "oracle",
           "cpu_model": _cpu_model(),
           "sample": "%d of %d sequences of %s per step" % (nseq, w.cfg["B"], w.name)}
     cfg = w.point()
     cfg.update(sample_sequences_per_step=nseq)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
-            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": ws, "steps": len(timed), "steps_requested": args.steps, "warmup": warm,
             "ms_per_step": 1000.0 * w.units(inp) / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": cfg, "cpu_baseline": cb,
