@@ -1816,10 +1816,7 @@ __global__ void __launch_bounds__(kPassThreads, SV_MIN_BLOCKS)
         finalizer_loop<KIND>(j, sm);
     } else if (t >= kConsumers) {
         // ---------------- producer warp ----------------
-        // Lane 0 streams the planned units in order.  The entry after the
-        // current one is read too: if it carries a Gumbel-max, the current
-        // unit's first stage names it, so that the consumers list and copy
-        // its top ids while this unit streams.
+        // Lane 0 streams the planned units in order.
         if (t == kConsumers) {
             int stage = 0;
             uint32_t phase = 0;
