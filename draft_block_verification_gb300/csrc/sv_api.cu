@@ -579,6 +579,7 @@ sv_status sv_verify_sample(sv_handle *h, const void *target, const void *draft, 
     j.invTp = (float)(1.0 / (double)T_p);
     j.amode = mode;
     j.lam = lam;
+    j.cactus_emd = mode == SV_LENIENT_CACTUS ? exp(-(double)lam) * (1.0 - 1e-12) : 0.0;
     j.seed = seed;
     j.ids = draft_ids;
     j.lens = draft_len;

@@ -265,14 +265,15 @@ __device__ __forceinline__ float cactus_newton32(float p, float delta)
 // with p): the fp32 Newton points at plo and phi, widened by 2^-14
 // relative, each checked in fp64 to lie on its side of its root (margin of
 // 64 roundings of Phi's terms).  Two fp64 evaluations of Phi in all; falls
-// back to the fp64 Newton of cactus_bracket when a check fails.  false when
-// no bracket could be certified.
+// back to the fp64 Newton of cactus_bracket when a check fails, or when p
+// reaches emd = exp(-delta) (1 - 1e-12), below which gamma* < 1 (Phi(1) =
+// log(1/p) > delta).  false when no bracket could be certified.
 static __device__ __noinline__ bool cactus_bracket_fast(double plo, double phi, double delta,
-                                                 double *glo, double *ghi)
+                                                 double emd, double *glo, double *ghi)
 {
     double d1, sc;
     bool ok_lo, ok_hi;
-    if (!(plo > 0.0) || !(delta > 0.0) || delta >= -log(plo)) {
+    if (!(plo > 0.0) || !(delta > 0.0) || plo >= emd) {
         double a;
         ok_lo = cactus_bracket(plo, delta, glo, &a);
     } else {
@@ -284,7 +285,7 @@ static __device__ __noinline__ bool cactus_bracket_fast(double plo, double phi, 
             ok_lo = cactus_bracket(plo, delta, glo, &a);
         }
     }
-    if (phi >= 1.0 || !(delta > 0.0) || delta >= -log(phi)) {
+    if (phi >= 1.0 || !(delta > 0.0) || phi >= emd) {
         double a;
         ok_hi = cactus_bracket(phi, delta, &a, ghi);
     } else {

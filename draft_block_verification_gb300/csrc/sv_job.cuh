@@ -87,6 +87,7 @@ struct Job {
     double rTp, rTq;    // 1/Tp, 1/Tq in fp64
     int amode;          // acceptance rule
     float lam;
+    double cactus_emd;  // exp(-lam) (1 - 1e-12): below it, gamma* < 1 (modified Cactus)
     uint64_t seed, iter;
     int eos;
     int force_rescue;

@@ -711,6 +711,7 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
     bool acc = false, und = false;
     double Lp = 0, Lq = 0;
     double lclo = 0.0, lchi = 0.0;  // bracket of log c (modified Cactus residual)
+    double cg0 = 0.0, cg3 = 1.0, cplo = 0.0, cphi = 1.0;  // its inputs, lane by lane
     const double ep = j.eps_lse, eq = j.eps_lse;
     if (lane < n) {
         Lp = rp.L1a;
@@ -731,14 +732,20 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
         // bracket gamma* over p's bracket (it grows with p), then alpha =
         // gamma* / q and the residual scale c = (1 - gamma*)/(1 - p)
         if (j.amode == SV_LENIENT_CACTUS && !(u < alo - kFlagEps)) {
-            const double plo = exp(lp - 1.01 * ep - 1e-13), phi = exp(lp + 1.01 * ep + 1e-13);
-            const double qlo = exp(lq - 1.01 * eq - 1e-13), qhi = exp(lq + 1.01 * eq + 1e-13);
+            // brackets of p and q: exp_fast (within 2^-21 of exp) widened by
+            // 2^-20; fp64 below -80, where fp32 would underflow
+            auto lo = [](double a) { return a > -80.0 ? exp_fast(a) * (1.0 - 0x1p-20) : exp(a); };
+            auto hi = [](double a) { return a > -80.0 ? exp_fast(a) * (1.0 + 0x1p-20) : exp(a); };
+            const double plo = lo(lp - 1.01 * ep - 1e-13), phi = hi(lp + 1.01 * ep + 1e-13);
+            const double qlo = lo(lq - 1.01 * eq - 1e-13), qhi = hi(lq + 1.01 * eq + 1e-13);
             double g0, g3;
-            const bool ok = cactus_bracket_fast(plo, phi, (double)j.lam, &g0, &g3);
+            const bool ok = cactus_bracket_fast(plo, phi, (double)j.lam, j.cactus_emd, &g0, &g3);
             alo = ok ? fmin(1.0, g0 / qhi) : 0.0;
             ahi = ok ? fmin(1.0, g3 / qlo) : 1.0;
-            lclo = (g3 < 1.0) ? log1p(-g3) - log1p(-plo) : -INFINITY;
-            lchi = log1p(-g0) - log1p(-phi);
+            cg0 = g0;
+            cg3 = g3;
+            cplo = plo;
+            cphi = phi;
         }
         acc = u < alo - kFlagEps;
         bool rej = u >= ahi + kFlagEps;
@@ -777,6 +784,11 @@ static __device__ __noinline__ void fin_sample(const Job &j, int b)
     double Lqh = __shfl_sync(0xFFFFFFFFu, Lq, f & 31);
     double eph = __shfl_sync(0xFFFFFFFFu, ep, f & 31);
     double eqh = __shfl_sync(0xFFFFFFFFu, eq, f & 31);
+    // the residual scale's bracket, at the rejected position only
+    if (j.amode == SV_LENIENT_CACTUS && lane == f && f < n) {
+        lclo = (cg3 < 1.0) ? log1p(-cg3) - log1p(-cplo) : -INFINITY;
+        lchi = log1p(-cg0) - log1p(-cphi);
+    }
     const double lcloh = __shfl_sync(0xFFFFFFFFu, lclo, f & 31);
     const double lchih = __shfl_sync(0xFFFFFFFFu, lchi, f & 31);
     // bonus row n (always valid): its log-sum-exp; its Gumbel-max with key
