@@ -662,17 +662,20 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     out_bytes = 0
     _barrier(dist, dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_steps = max(2, min(args.steps, 5))
-    e0.record(stream)
-    for _ in range(e_steps):
+    # one event pair per step; the median step (host-link traffic from other
+    # work on the machine can slow single steps)
+    e_steps = max(3, min(args.steps, 10))
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(e_steps)]
+    for i in range(e_steps):
+        e_ev[i][0].record(stream)
         for k, t in host.items():
             dst[k].copy_(t, non_blocking=True)
         res = [t.to("cpu", non_blocking=True) for t in _tensors(w.call(dbv, dst, h))]
         out_bytes = sum(r.numel() * r.element_size() for r in res)
-    e1.record(stream)
+        e_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    e_ms = _max_over_ranks(dist, e0.elapsed_time(e1) / e_steps, dev)
+    e_ms = _max_over_ranks(dist, statistics.median(a.elapsed_time(b) for a, b in e_ev), dev)
     h.sync_status()
 
     if rank != 0:
@@ -694,7 +697,8 @@ def run_ours(args):
                      "peak_source": peak_kind, "kernel": w.kernel(), "kernel_ms": kern_ms,
                      "alg_bytes_per_launch": alg_bytes},
         "e2e": {"value": job_rate(ws, units, e_ms), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes,
+                "ms_per_step": e_ms, "steps": e_steps},
         "step_ms": _percentiles(step_ms),
         "decisions": dec,
         "gpu_launches": w.launches() * args.steps,
