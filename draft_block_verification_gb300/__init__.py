@@ -132,8 +132,9 @@ class Handle:
 
     def selftest(self, seed: int = 1, n: int = 1 << 22, stream=None):
         """Ratios of the measured fp32 errors to the bounds the kernels assume,
-        and the count of skip gaps whose fast evaluation is not exact."""
-        r = (C.c_double * 4)()
+        the count of skip gaps whose fast evaluation is not exact, and the
+        count of ids outside their Gumbel bound table entries."""
+        r = (C.c_double * 5)()
         _check(lib().sv_selftest(self.ptr, int(seed), int(n), r, _stream(stream, self.device)),
                "sv_selftest")
         return list(r)

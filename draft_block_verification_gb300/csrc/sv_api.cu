@@ -24,8 +24,8 @@ cudaError_t seed_setup(int *blocks_per_sm);
 cudaError_t post_setup(int occ[2]);
 cudaError_t post_launch(const Job &j, int tv_grid, int resid_grid, int coop_grid, bool tv,
                         cudaStream_t s);
-cudaError_t selftest_run(uint64_t seed, long long n, const uint64_t *skip, double *res,
-                         cudaStream_t s);
+cudaError_t selftest_run(uint64_t seed, long long n, const uint64_t *skip, const float *gtab,
+                         const float *gtop, double *res, cudaStream_t s);
 cudaError_t wait_selftest_run(int *err, const unsigned *word, uint32_t limit, cudaStream_t s);
 }  // namespace sv
 
@@ -477,7 +477,8 @@ sv_status sv_rescue_count(sv_handle *h, void *stream, int64_t *count)
 sv_status sv_selftest(sv_handle *h, uint64_t seed, int64_t n, double *ratios, void *stream)
 {
     if (!h || !ratios || n < 1) return SV_ERR_INVALID_ARG;
-    return cuda_status(selftest_run(seed, n, h->d_skip, ratios, (cudaStream_t)stream));
+    return cuda_status(
+        selftest_run(seed, n, h->d_skip, h->d_gtab, h->d_gtop, ratios, (cudaStream_t)stream));
 }
 
 sv_status sv_wait_selftest(sv_handle *h, int64_t limit, void *stream)

@@ -7,6 +7,9 @@
 //       search over the exact thresholds (a count; must be 0), for draws
 //       spread uniformly and draws next to every threshold C_g, within the
 //       window where the fast path decides near its 2^-9 margin
+//   [4] ids whose fp64 G lies outside the table bounds of the top byte of
+//       their fine bits (a count; must be 0): the ordinary ids' upper bound,
+//       the top ids' upper and lower bounds
 // Fine bits are drawn, for ordinary and top ids alike, from regions where the
 // formulas are hardest: uniform, w within 2^-28 of 1 (u next to 255/256, or
 // 1 - u near 2^-61 for a top id), w below 2^-29, and u around 3/4 (the
@@ -29,10 +32,11 @@ __device__ int skip_gap_bisect(uint64_t M, const uint64_t *C)
     return lo;
 }
 
-__global__ void selftest_kernel(uint64_t seed, long long n, const uint64_t *C, unsigned *out)
+__global__ void selftest_kernel(uint64_t seed, long long n, const uint64_t *C, const float *gtab,
+                                const float *gtop, unsigned *out)
 {
     float r0 = 0.f, r1 = 0.f, r2 = 0.f;
-    unsigned bad = 0;
+    unsigned bad = 0, badt = 0;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x) {
         uint64_t h = splitmix_out(seed ^ (uint64_t)i);
@@ -46,6 +50,10 @@ __global__ void selftest_kernel(uint64_t seed, long long n, const uint64_t *C, u
         }
         double g64 = gumbel64(m, top);
         float g32 = gumbel32(m, top);
+        const int cb = (int)(m >> 44);
+        if (top ? !((double)gtop[kGTab + cb] <= g64 && g64 <= (double)gtop[cb])
+                : !(g64 <= (double)gtab[cb]))
+            ++badt;
         r0 = fmaxf(r0, (float)(fabs((double)g32 - g64) / (double)kG32Err));
         float x = -126.f + 190.f * (float)((h >> 11) & 0xFFFFF) * 0x1p-20f;
         double e64 = exp2((double)x);
@@ -71,17 +79,19 @@ __global__ void selftest_kernel(uint64_t seed, long long n, const uint64_t *C, u
     atomicMax(out + 2, __float_as_uint(r2));
     if (bad)
         atomicAdd(out + 3, bad);
+    if (badt)
+        atomicAdd(out + 4, badt);
 }
 
-cudaError_t selftest_run(uint64_t seed, long long n, const uint64_t *skip, double *res,
-                         cudaStream_t s)
+cudaError_t selftest_run(uint64_t seed, long long n, const uint64_t *skip, const float *gtab,
+                         const float *gtop, double *res, cudaStream_t s)
 {
     unsigned *d = nullptr;
-    cudaError_t e = cudaMallocAsync((void **)&d, 4 * sizeof(unsigned), s);
+    cudaError_t e = cudaMallocAsync((void **)&d, 5 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
-    cudaMemsetAsync(d, 0, 4 * sizeof(unsigned), s);
-    selftest_kernel<<<256, 256, 0, s>>>(seed, n, skip, d);
-    unsigned h[4] = {0, 0, 0, 0};
+    cudaMemsetAsync(d, 0, 5 * sizeof(unsigned), s);
+    selftest_kernel<<<256, 256, 0, s>>>(seed, n, skip, gtab, gtop, d);
+    unsigned h[5] = {0, 0, 0, 0, 0};
     e = cudaMemcpyAsync(h, d, sizeof h, cudaMemcpyDeviceToHost, s);
     cudaFreeAsync(d, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -91,6 +101,7 @@ cudaError_t selftest_run(uint64_t seed, long long n, const uint64_t *skip, doubl
         res[i] = f;
     }
     res[3] = (double)h[3];
+    res[4] = (double)h[4];
     return e;
 }
 

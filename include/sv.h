@@ -400,8 +400,10 @@ sv_status sv_set_option(sv_handle *h, sv_option opt, int64_t value);
  *   ratios[2] = max error of lg2.approx / (2^-22 max(1, |log2 x|))
  *   ratios[3] = number of skip draws whose gap (the fast evaluation the
  *               kernels use) differs from the exact threshold search: 0
+ *   ratios[4] = number of ids whose G lies outside the Gumbel bound tables
+ *               for the top byte of their fine bits: 0
  * Every ratio must stay below 1 for the error bounds the kernels use.
- * `ratios` is a caller-owned array of 4 doubles.
+ * `ratios` is a caller-owned array of 5 doubles.
  * ------------------------------------------------------------------------- */
 sv_status sv_selftest(sv_handle *h, uint64_t seed, int64_t n, double *ratios, void *stream);
 

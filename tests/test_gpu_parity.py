@@ -560,3 +560,4 @@ def test_fp32_error_bounds_hold_on_device(dbv):
     r = dbv.default_handle().selftest(seed=7, n=1 << 24)
     assert max(r[:3]) < 1.0, r
     assert r[3] == 0, r  # every fast skip gap equals the exact one
+    assert r[4] == 0, r  # every G within its table bounds (ordinary and top ids)
