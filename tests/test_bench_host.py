@@ -83,6 +83,10 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the steps it timed (all of them here: the run fits its time budget)
+    assert line["steps_requested"] == 2 and line["steps"] == 2 and line["warmup"] == 1
+    # one sequence (greedy tiny has B = 1): one oracle thread had work
+    assert line["cpu_baseline"]["cores"] == 1
 
 
 def test_workload_launch_counts_and_tv_flag():
